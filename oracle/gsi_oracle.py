@@ -1,0 +1,179 @@
+"""Float64 CPU oracle for the gated linear map (TEST INFRASTRUCTURE ONLY).
+
+This module is the parity reference for the CUDA library.  Only the test
+suite, the package's smoke check and the benchmark's CPU-baseline leg may
+import it; the product path never calls it and has no CPU fallback.
+
+It follows "Gated Subspace Inference for Transformer Acceleration"
+(gist.science technical summary), step by step, in the pages' notation:
+
+  §2.1 (core decomposition):   x = V_k V_k^T x + r,   y = (W V_k)(V_k^T x) + W r = M g + W r,
+                               M = W V_k (cached image), g = V_k^T x (projection).
+  §2.2 (gated residual step):  rho_t = ||r|| / ||x||;  rho_t < eps -> fast path y ~= M g;
+                               rho_t >= eps -> slow path, exact y = W x.
+  §2.2 (Theorem 4, bound only): fast-path error per token <= ||W||_2 * eps * ||x||.
+
+Arrays are token-major: X is T x d (row t is token x_t), W is d_out x d,
+V is d x k, M is d_out x k, Y is T x d_out.  Everything is numpy float64,
+computed from the stored (fp32 / bf16) values widened exactly.
+
+Readings where the pages leave a step open (each one is listed with its
+justification in the design notes):
+  * tie rho == eps goes to the slow path (the pages write ">=" for slow);
+  * ||x|| == 0 defines rho := 0 (fast, and M*0 = 0 = W*0);
+  * a non-finite token gives rho = NaN, which is "not < eps", hence slow;
+  * the residual is the explicit x - V_k g of the decomposition, never an
+    identity that assumes V_k exactly orthonormal.
+
+Pins: every function here is checked by tests that do not re-type its
+formula (hand-derived examples, closed forms, invariants, brute force,
+the Theorem 4 bound).  Parity of figures printed on the pages: unpinned
+(the pages print no worked example).
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def image(W: np.ndarray, V: np.ndarray) -> np.ndarray:
+    """Low-rank weight image M = W V_k (§2.1), d_out x k."""
+    return W @ V
+
+
+def gram(V: np.ndarray) -> np.ndarray:
+    """Gram matrix V_k^T V_k (k x k); the identity when V_k is exactly orthonormal.
+
+    Not a step of the method itself: the library caches it next to M so that
+    it can evaluate ||x - V_k g|| without a second pass over V_k; the oracle
+    provides it to check that cached artefact.
+    """
+    return V.T @ V
+
+
+def project(X: np.ndarray, V: np.ndarray) -> np.ndarray:
+    """Subspace projection g_t = V_k^T x_t (§2.1); row t of the result is g_t."""
+    return X @ V
+
+
+def residual(X: np.ndarray, V: np.ndarray, G: np.ndarray) -> np.ndarray:
+    """Residual r_t = x_t - V_k g_t of the exact decomposition (§2.1)."""
+    return X - G @ V.T
+
+
+def residual_ratio(X: np.ndarray, R: np.ndarray) -> np.ndarray:
+    """rho_t = ||r_t|| / ||x_t|| (§2.2); rho := 0 for a zero token."""
+    nx = np.sqrt(np.sum(X * X, axis=1))
+    nr = np.sqrt(np.sum(R * R, axis=1))
+    zero = nx == 0.0
+    with np.errstate(invalid="ignore", divide="ignore"):
+        rho = nr / np.where(zero, 1.0, nx)
+    rho[zero] = 0.0
+    return rho
+
+
+def gate(rho: np.ndarray, eps: float) -> np.ndarray:
+    """Per-token gate (§2.2): True = slow path (rho >= eps, or rho is NaN)."""
+    return ~(rho < eps)
+
+
+def fast_path(M: np.ndarray, G: np.ndarray) -> np.ndarray:
+    """Fast path y_t ~= M g_t for every token (§2.2); rows are tokens."""
+    return G @ M.T
+
+
+def slow_path(W: np.ndarray, X: np.ndarray) -> np.ndarray:
+    """Slow path y_t = W x_t for every token (§2.2): the dense map."""
+    return X @ W.T
+
+
+def compact(flags: np.ndarray):
+    """Stable (ascending token index) lists of fast and slow tokens."""
+    t = np.arange(len(flags), dtype=np.int64)
+    return t[~flags], t[flags]
+
+
+def gsi_linear(W, M, V, X, eps):
+    """One gated linear map over T tokens (§2.1-§2.2).
+
+    Returns (Y, flags, rho, G): Y is T x d_out, flags a bool array
+    (True = slow), rho the residual ratios, G the projections.
+    M is whatever image the caller holds (the oracle does not rebuild it).
+    """
+    G = project(X, V)
+    R = residual(X, V, G)
+    rho = residual_ratio(X, R)
+    flags = gate(rho, eps)
+    fast, slow = compact(flags)
+    Y = np.zeros((X.shape[0], W.shape[0]))
+    if len(fast):
+        Y[fast] = fast_path(M, G[fast])
+    if len(slow):
+        Y[slow] = slow_path(W, X[slow])
+    return Y, flags, rho, G
+
+
+def candidates(W, M, V, X):
+    """Both path results for every token: (M g_t, W x_t) rows.
+
+    Used for tokens whose rho sits in the tolerance band around eps, where
+    either gate decision is acceptable and the output must match the
+    candidate of the decision actually taken.
+    """
+    G = project(X, V)
+    return fast_path(M, G), slow_path(W, X)
+
+
+def gsi_stack(maps, Xs, eps):
+    """The gated map applied to a list of maps, each with its own tokens.
+
+    maps: list of (W, M, V); Xs: list of T x d_i token blocks.  The maps are
+    independent (one output per map), as in a layer's QKV / output / MLP-up /
+    MLP-down projections fed with their own activations.
+    """
+    return [gsi_linear(W, M, V, X, eps) for (W, M, V), X in zip(maps, Xs)]
+
+
+def spectral_norm(W: np.ndarray, iters: int = 200) -> float:
+    """||W||_2 for the Theorem 4 bound: SVD for small W, power iteration on W^T W otherwise."""
+    if W.size <= 4_000_000:
+        return float(np.linalg.norm(W, 2))
+    v = np.random.default_rng(0).standard_normal(W.shape[1])
+    for _ in range(iters):
+        v = W.T @ (W @ v)
+        v /= np.linalg.norm(v)
+    return float(np.linalg.norm(W @ v))
+
+
+def brute_linear(W, M, V, X, eps):
+    """Pure-Python loops for tiny inputs: the same steps, no BLAS.
+
+    Serves as an independent restatement for cross-checking `gsi_linear`
+    on inputs of a few dozen elements.
+    """
+    T, d = len(X), len(X[0])
+    d_out, k = len(W), len(V[0])
+    Y = [[0.0] * d_out for _ in range(T)]
+    flags, rhos = [], []
+    for t in range(T):
+        x = [float(v) for v in X[t]]
+        g = [sum(V[i][j] * x[i] for i in range(d)) for j in range(k)]
+        r = [x[i] - sum(V[i][j] * g[j] for j in range(k)) for i in range(d)]
+        nx = sum(v * v for v in x) ** 0.5
+        nr = sum(v * v for v in r) ** 0.5
+        rho = 0.0 if nx == 0.0 else nr / nx
+        slow = not (rho < eps)
+        for o in range(d_out):
+            if slow:
+                Y[t][o] = sum(W[o][i] * x[i] for i in range(d))
+            else:
+                Y[t][o] = sum(M[o][j] * g[j] for j in range(k))
+        flags.append(slow)
+        rhos.append(rho)
+    return np.array(Y), np.array(flags), np.array(rhos)
+
+
+def brute_image(W, V):
+    """Pure-Python triple loop for M = W V_k on tiny inputs."""
+    d_out, d, k = len(W), len(V), len(V[0])
+    return np.array([[sum(W[o][i] * V[i][j] for i in range(d)) for j in range(k)]
+                     for o in range(d_out)])

@@ -1,0 +1,311 @@
+"""Pins for the float64 oracle: checks against facts that do not come from it.
+
+Each `pin_*` takes an oracle module `o` (the real one, or a copy with a
+planted mistake) and raises if `o` disagrees with what the pages and the
+mathematics fix:
+
+* hand-derived closed-form examples (tests/golden/hand_examples.json);
+* the decomposition's geometry (the residual is orthogonal to span(V_k) and
+  is the closest point; Pythagoras for an orthonormal basis);
+* special cases with closed forms (axis basis, eps = 0, eps = inf,
+  x inside span(V_k), k = d);
+* the Theorem 4 fast-path error bound;
+* invariances (scaling by powers of two, token permutation);
+* pure-Python brute force on tiny inputs.
+
+Definitions: "Gated Subspace Inference for Transformer Acceleration"
+(gist.science technical summary), §2.1 core decomposition and §2.2 gated
+residual step with its Theorem 4 bound.
+"""
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "hand_examples.json")
+
+
+def _rand_basis(rs, d, k):
+    q, r = np.linalg.qr(rs.standard_normal((d, k)))
+    return q * np.sign(np.diag(r))[None, :]
+
+
+def _close(a, b, tol, what):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    assert a.shape == b.shape, f"{what}: shape {a.shape} != {b.shape}"
+    err = np.max(np.abs(a - b)) if a.size else 0.0
+    assert err <= tol, f"{what}: max abs error {err} > {tol}"
+
+
+def pin_hand_examples(o):
+    """Every quantity of the hand-worked examples (§2.1, §2.2)."""
+    ex = json.load(open(GOLDEN))["examples"]
+    for e in ex:
+        V = np.array(e["V"], float)
+        W = np.array(e["W"], float)
+        M = np.array(e["M"], float)
+        tol = max(e["tol"], 1e-12)
+        _close(o.image(W, V), M, tol, e["name"] + " image")
+        X = np.array([t["x"] for t in e["tokens"]], float)
+        G = o.project(X, V)
+        _close(G, [t["g"] for t in e["tokens"]], tol, e["name"] + " g")
+        R = o.residual(X, V, G)
+        _close(R, [t["r"] for t in e["tokens"]], tol, e["name"] + " r")
+        rho = o.residual_ratio(X, R)
+        _close(rho, [t["rho"] for t in e["tokens"]], tol, e["name"] + " rho")
+        flags = o.gate(rho, e["eps"])
+        assert list(flags) == [t["slow"] for t in e["tokens"]], e["name"] + " flags"
+        Y, f2, rho2, _ = o.gsi_linear(W, M, V, X, e["eps"])
+        assert list(f2) == [t["slow"] for t in e["tokens"]], e["name"] + " flags (linear)"
+        _close(Y, [t["y"] for t in e["tokens"]], tol * 100, e["name"] + " y")
+        Yf, Ys = o.candidates(W, M, V, X)
+        for i, t in enumerate(e["tokens"]):
+            cand = Ys[i] if t["slow"] else Yf[i]
+            _close(cand, t["y"], tol * 100, e["name"] + " candidate")
+            if "fast_error_norm" in t:
+                err = np.linalg.norm(Ys[i] - Yf[i])
+                _close(err, t["fast_error_norm"], 1e-9, e["name"] + " fast error")
+        if "W_spectral_norm" in e:
+            _close(o.spectral_norm(W), e["W_spectral_norm"], 1e-9, e["name"] + " ||W||_2")
+        # brute force restatement agrees on the same examples
+        Yb, fb, rb = o.brute_linear(W.tolist(), M.tolist(), V.tolist(), X.tolist(), e["eps"])
+        assert list(fb) == [t["slow"] for t in e["tokens"]], e["name"] + " brute flags"
+        _close(Yb, [t["y"] for t in e["tokens"]], tol * 100, e["name"] + " brute y")
+
+
+def pin_decomposition_geometry(o, seed=11):
+    """r is orthogonal to span(V_k), is the closest point, and ||x||^2 = ||g||^2 + ||r||^2."""
+    rs = np.random.default_rng(seed)
+    d, k, T = 40, 7, 9
+    V = _rand_basis(rs, d, k)
+    X = rs.standard_normal((T, d))
+    G = o.project(X, V)
+    R = o.residual(X, V, G)
+    _close(R @ V, np.zeros((T, k)), 1e-12, "V^T r")
+    _close(np.sum(X * X, 1), np.sum(G * G, 1) + np.sum(R * R, 1), 1e-10, "Pythagoras")
+    for _ in range(5):
+        c = G + 0.1 * rs.standard_normal(G.shape)
+        other = X - c @ V.T
+        assert np.all(np.linalg.norm(other, axis=1) >= np.linalg.norm(R, axis=1) - 1e-12), \
+            "residual is not the closest point"
+    # a non-orthonormal basis: the residual is still x minus the span component V g
+    B = V @ np.diag(np.linspace(0.5, 1.5, k))
+    GB = o.project(X, B)
+    _close(GB, X @ B, 1e-12, "projection with scaled basis")
+    _close(o.residual(X, B, GB) + GB @ B.T, X, 1e-12, "x = V g + r with scaled basis")
+
+
+def pin_axis_basis(o, seed=12):
+    """V_k = I[:, :k]: g = x[:k], M = W[:, :k], rho = ||x[k:]||/||x|| exactly."""
+    rs = np.random.default_rng(seed)
+    d, d_out, k, T = 24, 10, 5, 13
+    V = np.eye(d)[:, :k]
+    W = rs.standard_normal((d_out, d))
+    X = rs.standard_normal((T, d))
+    M = o.image(W, V)
+    _close(M, W[:, :k], 0.0, "axis image")
+    G = o.project(X, V)
+    _close(G, X[:, :k], 0.0, "axis g")
+    rho = o.residual_ratio(X, o.residual(X, V, G))
+    want = np.linalg.norm(X[:, k:], axis=1) / np.linalg.norm(X, axis=1)
+    _close(rho, want, 1e-15, "axis rho")
+    eps = float(np.median(want))
+    Y, flags, _, _ = o.gsi_linear(W, M, V, X, eps)
+    assert np.array_equal(flags, ~(want < eps)), "axis flags"
+    for t in range(T):
+        want_y = W @ X[t] if flags[t] else W[:, :k] @ X[t, :k]
+        _close(Y[t], want_y, 1e-12, f"axis y[{t}]")
+
+
+def _brute_dense(W, X):
+    return np.array([[sum(W[o_, i] * X[t, i] for i in range(W.shape[1]))
+                      for o_ in range(W.shape[0])] for t in range(X.shape[0])])
+
+
+def pin_eps_zero(o, seed=13):
+    """eps = 0: every token is slow and Y equals dense W x (brute force loops)."""
+    rs = np.random.default_rng(seed)
+    d, d_out, k, T = 12, 7, 3, 6
+    V = _rand_basis(rs, d, k)
+    W = rs.standard_normal((d_out, d))
+    X = rs.standard_normal((T, d))
+    X[2] = (V @ rs.standard_normal(k))  # a token inside the span is still slow at eps = 0
+    Y, flags, _, _ = o.gsi_linear(W, o.image(W, V), V, X, 0.0)
+    assert flags.all(), "eps=0 must send every token to the slow path"
+    _close(Y, _brute_dense(W, X), 1e-12, "eps=0 dense")
+
+
+def pin_in_span(o, seed=14):
+    """x in span(V_k): r = 0, every token fast (eps > 0), M g = W x."""
+    rs = np.random.default_rng(seed)
+    d, d_out, k, T = 30, 11, 6, 8
+    V = _rand_basis(rs, d, k)
+    W = rs.standard_normal((d_out, d))
+    A = rs.standard_normal((T, k))
+    X = A @ V.T
+    Y, flags, rho, G = o.gsi_linear(W, o.image(W, V), V, X, 1e-6)
+    assert np.all(rho < 1e-13), "in-span rho"
+    assert not flags.any(), "in-span tokens must be fast"
+    _close(G, A, 1e-12, "in-span coefficients")
+    _close(Y, _brute_dense(W, X), 1e-12, "in-span y")
+
+
+def pin_full_rank(o, seed=15):
+    """k = d (square orthogonal V): everything fast and exact."""
+    rs = np.random.default_rng(seed)
+    d, d_out, T = 9, 5, 7
+    V = _rand_basis(rs, d, d)
+    W = rs.standard_normal((d_out, d))
+    X = rs.standard_normal((T, d))
+    Y, flags, rho, _ = o.gsi_linear(W, o.image(W, V), V, X, 1e-8)
+    assert not flags.any() and np.all(rho < 1e-13), "k=d is all-fast"
+    _close(Y, _brute_dense(W, X), 1e-12, "k=d y")
+
+
+def pin_theorem4(o, seed=16):
+    """Theorem 4 (§2.2): fast-path error <= ||W||_2 * rho * ||x|| < ||W||_2 * eps * ||x||."""
+    rs = np.random.default_rng(seed)
+    d, d_out, k, T = 64, 48, 8, 200
+    V = _rand_basis(rs, d, k)
+    W = rs.standard_normal((d_out, d))
+    s = rs.uniform(0.0, 0.6, T)
+    X = rs.standard_normal((T, k)) @ V.T + s[:, None] * rs.standard_normal((T, d))
+    eps = 0.3
+    M = o.image(W, V)
+    Y, flags, rho, G = o.gsi_linear(W, M, V, X, eps)
+    w2 = float(np.sqrt(np.max(np.linalg.eigvalsh(W.T @ W))))
+    _close(o.spectral_norm(W), w2, 1e-9 * w2, "spectral norm")
+    fast = ~flags
+    assert fast.sum() > 10 and flags.sum() > 10, "theorem-4 case needs both paths"
+    err = np.linalg.norm(Y[fast] - X[fast] @ W.T, axis=1)
+    nx = np.linalg.norm(X[fast], axis=1)
+    assert np.all(err <= w2 * rho[fast] * nx * (1 + 1e-12) + 1e-12), "Theorem 4 (rho) bound"
+    assert np.all(err < w2 * eps * nx), "Theorem 4 (eps) bound"
+    _close(Y[flags], X[flags] @ W.T, 1e-12, "slow tokens exact")
+
+
+def pin_eps_inf(o, seed=17):
+    """eps = +inf is static projection: every token fast; 0 <= rho <= 1 for orthonormal V."""
+    rs = np.random.default_rng(seed)
+    d, d_out, k, T = 20, 6, 4, 15
+    V = _rand_basis(rs, d, k)
+    W = rs.standard_normal((d_out, d))
+    X = rs.standard_normal((T, d)) * rs.uniform(0, 3, (T, 1))
+    Y, flags, rho, G = o.gsi_linear(W, o.image(W, V), V, X, np.inf)
+    assert not flags.any(), "eps=inf is all-fast"
+    assert np.all((rho >= 0) & (rho <= 1 + 1e-15)), "rho in [0, 1]"
+    # fast path output is the image of the projected token: W (V V^T x)
+    _close(Y, (X @ V @ V.T) @ W.T, 1e-12, "static projection output")
+
+
+def pin_scaling(o, seed=18):
+    """x -> 2^j x leaves rho and flags unchanged and scales y by 2^j exactly."""
+    rs = np.random.default_rng(seed)
+    d, d_out, k, T = 16, 9, 4, 12
+    V = _rand_basis(rs, d, k)
+    W = rs.standard_normal((d_out, d))
+    s = rs.uniform(0, 0.5, T)
+    X = rs.standard_normal((T, k)) @ V.T + s[:, None] * rs.standard_normal((T, d))
+    M = o.image(W, V)
+    Y, f, rho, _ = o.gsi_linear(W, M, V, X, 0.2)
+    for j in (-3, 5):
+        Y2, f2, rho2, _ = o.gsi_linear(W, M, V, X * 2.0 ** j, 0.2)
+        assert np.array_equal(f, f2) and np.array_equal(rho, rho2), "scale invariance of the gate"
+        assert np.array_equal(Y2, Y * 2.0 ** j), "scale equivariance of y"
+
+
+def pin_permutation(o, seed=19):
+    """Permuting tokens permutes Y, rho and flags."""
+    rs = np.random.default_rng(seed)
+    d, d_out, k, T = 16, 9, 4, 12
+    V = _rand_basis(rs, d, k)
+    W = rs.standard_normal((d_out, d))
+    s = rs.uniform(0, 0.5, T)
+    X = rs.standard_normal((T, k)) @ V.T + s[:, None] * rs.standard_normal((T, d))
+    M = o.image(W, V)
+    Y, f, rho, _ = o.gsi_linear(W, M, V, X, 0.2)
+    p = rs.permutation(T)
+    Y2, f2, rho2, _ = o.gsi_linear(W, M, V, X[p], 0.2)
+    assert np.array_equal(f2, f[p]), "permutation flags"
+    _close(Y2, Y[p], 1e-13, "permutation y")
+    _close(rho2, rho[p], 1e-15, "permutation rho")
+
+
+def pin_degenerate_tokens(o, seed=20):
+    """Zero token: rho = 0, fast, y = 0.  Non-finite token: slow, NaN propagates."""
+    rs = np.random.default_rng(seed)
+    d, d_out, k = 8, 5, 2
+    V = _rand_basis(rs, d, k)
+    W = rs.standard_normal((d_out, d))
+    X = np.zeros((3, d))
+    X[1, 3] = np.nan
+    X[2] = rs.standard_normal(d)
+    Y, flags, rho, _ = o.gsi_linear(W, o.image(W, V), V, X, 0.5)
+    assert rho[0] == 0.0 and not flags[0] and np.all(Y[0] == 0.0), "zero token"
+    assert flags[1] and np.isnan(rho[1]) and np.all(np.isnan(Y[1])), "NaN token"
+
+
+def pin_compact(o, seed=21):
+    """Stable ascending, disjoint, covering index lists; fast first element of the pair."""
+    rs = np.random.default_rng(seed)
+    for T in (0, 1, 7, 64):
+        flags = rs.random(T) < 0.3
+        fast, slow = o.compact(flags)
+        assert np.all(np.diff(fast) > 0) and np.all(np.diff(slow) > 0), "ascending"
+        assert not flags[fast].any() and flags[slow].all(), "fast/slow membership"
+        assert len(fast) + len(slow) == T and set(fast) | set(slow) == set(range(T)), "cover"
+
+
+def pin_gram(o, seed=22):
+    """Gram of an orthonormal basis is I; of V D (diagonal D) it is D^2."""
+    rs = np.random.default_rng(seed)
+    V = _rand_basis(rs, 30, 6)
+    _close(o.gram(V), np.eye(6), 1e-13, "gram of orthonormal V")
+    D = np.diag([1.0, 2.0, 0.5, 3.0, 1.0, 0.25])
+    _close(o.gram(V @ D), D @ D, 1e-12, "gram of scaled V")
+
+
+def pin_brute(o, seed=23):
+    """The BLAS-based path agrees with the pure-Python loops on tiny random inputs."""
+    rs = np.random.default_rng(seed)
+    d, d_out, k, T = 9, 6, 3, 8
+    V = _rand_basis(rs, d, k)
+    W = rs.standard_normal((d_out, d))
+    s = rs.uniform(0, 0.8, T)
+    X = rs.standard_normal((T, k)) @ V.T + s[:, None] * rs.standard_normal((T, d))
+    M = o.image(W, V)
+    _close(M, o.brute_image(W.tolist(), V.tolist()), 1e-12, "brute image")
+    Y, f, rho, _ = o.gsi_linear(W, M, V, X, 0.3)
+    Yb, fb, rb = o.brute_linear(W.tolist(), M.tolist(), V.tolist(), X.tolist(), 0.3)
+    assert f.any() and (~f).any(), "brute case needs both paths"
+    assert np.array_equal(f, fb), "brute flags"
+    _close(rho, rb, 1e-12, "brute rho")
+    _close(Y, Yb, 1e-12, "brute y")
+
+
+def pin_stack(o):
+    """A list of maps gives each map's own hand-derived result."""
+    ex = json.load(open(GOLDEN))["examples"]
+    a, b = ex[0], ex[2]
+    maps, Xs = [], []
+    for e in (a, b):
+        maps.append((np.array(e["W"], float), np.array(e["M"], float), np.array(e["V"], float)))
+        Xs.append(np.array([t["x"] for t in e["tokens"]], float))
+    out = o.gsi_stack(maps, Xs, 0.55)
+    # eps 0.55: example a: rho (0, 1, 0.6, 0) -> slow only token 1 and 2;
+    # example b: rho (0.6, 0.8, 5/13) -> slow, slow, fast
+    assert list(out[0][1]) == [False, True, True, False], "stack map 0 flags"
+    assert list(out[1][1]) == [True, True, False], "stack map 1 flags"
+    _close(out[0][0], [[11, 32], [34, 73], [44.5, 109], [0, 0]], 1e-12, "stack map 0 y")
+    _close(out[1][0], [[4, 3, 8], [4, 3, 0], [12, 0, 24]], 1e-12, "stack map 1 y")
+
+
+ALL_PINS = [
+    pin_hand_examples, pin_decomposition_geometry, pin_axis_basis, pin_eps_zero,
+    pin_in_span, pin_full_rank, pin_theorem4, pin_eps_inf, pin_scaling,
+    pin_permutation, pin_degenerate_tokens, pin_compact, pin_gram, pin_brute,
+    pin_stack,
+]

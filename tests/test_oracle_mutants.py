@@ -1,0 +1,59 @@
+"""Plant plausible mistakes in a copy of the oracle (on the CPU) and check
+that the pins catch every one of them.
+
+Each mutant edits one line of the oracle's source text -- a flipped sign, a
+dropped term, a transposed operand, a wrong comparison, a wrong index -- and
+re-executes it as a separate module.  The real oracle is never modified.
+"""
+import inspect
+import types
+
+import pytest
+
+from oracle import gsi_oracle
+from tests.oracle_pins import ALL_PINS
+
+SRC = inspect.getsource(gsi_oracle)
+
+MUTANTS = {
+    "image_drops_basis": ("return W @ V\n", "return W[:, :V.shape[1]]\n"),
+    "image_transposed": ("return W @ V\n", "return (V.T @ W.T).T[:, ::-1]\n"),
+    "project_wrong_rows": ("return X @ V\n", "return X[:, :V.shape[1]]\n"),
+    "residual_sign": ("return X - G @ V.T", "return X + G @ V.T"),
+    "residual_dropped": ("return X - G @ V.T", "return X"),
+    "ratio_squared_norm": ("rho = nr / np.where(zero, 1.0, nx)", "rho = nr / np.where(zero, 1.0, nx * nx)"),
+    "ratio_zero_token": ("rho[zero] = 0.0", "rho[zero] = 1.0"),
+    "gate_tie_fast": ("return ~(rho < eps)", "return rho > eps"),
+    "gate_inverted": ("return ~(rho < eps)", "return rho < eps"),
+    "fast_wrong_index": ("return G @ M.T", "return (G @ M.T)[:, ::-1]"),
+    "slow_wrong_index": ("return X @ W.T", "return X[:, ::-1] @ W.T"),
+    "slow_uses_image": ("Y[slow] = slow_path(W, X[slow])", "Y[slow] = fast_path(M, G[slow])"),
+    "fast_uses_dense": ("Y[fast] = fast_path(M, G[fast])", "Y[fast] = slow_path(W, X[fast])"),
+    "compact_swapped": ("return t[~flags], t[flags]", "return t[flags], t[~flags]"),
+    "compact_unstable": ("return t[~flags], t[flags]", "return t[~flags][::-1], t[flags][::-1]"),
+    "gram_outer": ("return V.T @ V", "return V.T @ V + 1e-3 * np.eye(V.shape[1])"),
+    "spectral_frobenius": ("return float(np.linalg.norm(W, 2))", "return float(np.linalg.norm(W))"),
+    "brute_tie": ("slow = not (rho < eps)", "slow = rho > eps"),
+    "brute_slow_uses_image": ("Y[t][o] = sum(W[o][i] * x[i] for i in range(d))",
+                              "Y[t][o] = sum(M[o][j] * g[j] for j in range(k))"),
+    "stack_shares_tokens": ("for (W, M, V), X in zip(maps, Xs)]", "for (W, M, V), X in zip(maps, Xs[:1] * len(Xs))]"),
+}
+
+
+def _mutant(old, new):
+    assert SRC.count(old) >= 1, f"mutation anchor not found: {old!r}"
+    mod = types.ModuleType("oracle_mutant")
+    exec(compile(SRC.replace(old, new, 1), "oracle_mutant", "exec"), mod.__dict__)
+    return mod
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name):
+    mod = _mutant(*MUTANTS[name])
+    caught = []
+    for pin in ALL_PINS:
+        try:
+            pin(mod)
+        except Exception as e:  # AssertionError or a shape error both count
+            caught.append((pin.__name__, type(e).__name__))
+    assert caught, f"no pin caught mutant {name}"
