@@ -1,0 +1,438 @@
+"""Benchmark: gated-subspace linear maps of a 6B-class decoder layer at batch 1.
+
+Workload (one "step"): the four projections of a 6B-class layer (fused QKV
+12288x4096, output 4096x4096, MLP up 16384x4096, MLP down 4096x16384), bf16
+weights, k = 256, eps = 0.05, and 256 sequential single-token decode steps;
+each decode step runs the gated map over the four projections in order
+(gsi_stack with T = 1), so one step is 1024 gated-map calls.  Per map, exactly
+26 of the 256 tokens (10%) have rho >= eps (two-level noise mixture).
+
+Weights rotate over R replicas of the layer (distinct device copies) so the
+working set of consecutive decode steps does not sit in L2: 8 replicas put
+~269 MB of fast-path weights (V, Gram, M) and ~3.2 GB of W behind the 129 MB
+L2, as the 28 distinct layers of a real model would.
+
+Printed: one JSON line with tokens/s (the whole step: 256 tokens through the
+layer's four maps), the achieved HBM bandwidth of the step and of the
+dominant kernel against the measured peak, an end-to-end figure through the
+public API with host buffers, and the float64 oracle timed on the host cores.
+`--impl reference` times the oracle alone on the same metric.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from workloads import synth  # noqa: E402
+
+T_TOKENS = 256
+EPS = synth.EPS
+K_RANK = 256
+N_SLOW = 26
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        j = json.load(open(p))
+        return float(j["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except FileNotFoundError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def make_inputs():
+    """The four 6B maps with their 256 tokens each (CPU, storage dtype)."""
+    return [synth.map_6b(role, T=T_TOKENS, n_slow=N_SLOW, k=K_RANK) for role in synth.ROLES]
+
+
+def map_bytes(m):
+    es = 2
+    return dict(V=m.d * m.k * es, gram=m.k * m.k * 4, M=m.d_out * m.k * es, W=m.d_out * m.d * es,
+                x=m.d * es, y=m.d_out * 4)
+
+
+def algorithmic_bytes(maps_in, flags_np):
+    """Bytes the method must move for the whole step (SURVEY-style model):
+    per call |V| + |Gram| + x + y + flag, plus |M| if fast or |W| if slow."""
+    total = fast_apply = slow_apply = gate = 0
+    n_fast = n_slow = 0
+    for m, f in zip(maps_in, flags_np):
+        b = map_bytes(m)
+        ns = int(f.sum())
+        nf = len(f) - ns
+        g = b["V"] + b["gram"] + b["x"] + m.k * 4 + 4 + 1
+        gate += g * len(f)
+        fast_apply += nf * (b["M"] + m.k * 4 + b["y"])
+        slow_apply += ns * (b["W"] + b["x"] + b["y"])
+        n_fast += nf
+        n_slow += ns
+    total = gate + fast_apply + slow_apply
+    dense = sum((map_bytes(m)["W"] + map_bytes(m)["x"] + map_bytes(m)["y"]) * len(f)
+                for m, f in zip(maps_in, flags_np))
+    return dict(total=total, gate=gate, fast=fast_apply, slow=slow_apply, dense=dense,
+                n_fast=n_fast, n_slow=n_slow)
+
+
+# ---------------------------------------------------------------------------- oracle (CPU)
+def oracle_step(maps64, tokens, eps):
+    """The float64 oracle over `tokens` decode steps through the four maps."""
+    from oracle import gsi_oracle as orc
+
+    for t in tokens:
+        for (W, M, V, X) in maps64:
+            orc.gsi_linear(W, M, V, X[t:t + 1], eps)
+
+
+def oracle_maps(maps_in, M_list=None):
+    from oracle import gsi_oracle as orc
+
+    out = []
+    for i, m in enumerate(maps_in):
+        W, V, X = synth.widen(m.W), synth.widen(m.V), synth.widen(m.X)
+        M = synth.widen(M_list[i]) if M_list is not None else orc.image(W, V)
+        out.append((W, M, V, X))
+    return out
+
+
+def time_oracle(maps64, n_tokens, eps):
+    toks = list(range(n_tokens))
+    t0 = time.perf_counter()
+    oracle_step(maps64, toks, eps)
+    dt = time.perf_counter() - t0
+    return n_tokens / dt, dt
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count()
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    maps_in = make_inputs()
+    maps64 = oracle_maps(maps_in)
+    n_tok = args.ref_tokens
+    for _ in range(args.warmup):
+        oracle_step(maps64, range(min(4, n_tok)), EPS)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(maps64, range(n_tok), EPS)
+    dt = time.perf_counter() - t0
+    value = n_tok * args.steps / dt
+    line = {
+        "impl": "reference", "metric": "gsi_linear_tokens_per_s_batch1", "value": value,
+        "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": dt / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "6B-class layer linears (qkv/out/up/down), bf16 stored, batch-1 decode, "
+                               f"k={K_RANK}, eps={EPS}, 10% slow tokens",
+                   "tokens_per_step": n_tok},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+                         "sample": f"{n_tok} of the 256 decode tokens per step, all four maps, "
+                                   "float64 numpy oracle on host cores"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+# ---------------------------------------------------------------------------- GPU
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--replicas", type=int, default=8)
+    ap.add_argument("--ref-tokens", type=int, default=32)
+    ap.add_argument("--cpu-tokens", type=int, default=64)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist_mod
+
+        dist_mod.init_process_group("nccl")
+        dist = dist_mod
+
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import gated_rank_subspace_gb300 as gsi
+
+    dev = torch.device("cuda", local)
+    maps_in = make_inputs()
+    R = args.replicas
+    # replicas: distinct device copies of every map's W, V, M, Gram
+    base = []
+    for m in maps_in:
+        W, V = m.W.to(dev), m.V.to(dev)
+        base.append(gsi.make_map(W, V))
+    reps = [base]
+    for _ in range(1, R):
+        reps.append([gsi.Map(b.W.clone(), b.V.clone(), b.M.clone(), b.gram.clone()) for b in base])
+    Xs = [m.X.to(dev) for m in maps_in]
+    Ys = [torch.zeros(T_TOKENS, m.d_out, device=dev) for m in maps_in]
+    Fs = [torch.zeros(T_TOKENS, dtype=torch.uint8, device=dev) for _ in maps_in]
+    ws = gsi.new_workspace(gsi.stack_workspace_size(base, 1), dev)
+    args_t = [gsi.stack_args(reps[t % R], [X[t:t + 1] for X in Xs], [Y[t:t + 1] for Y in Ys],
+                             [F[t:t + 1] for F in Fs]) for t in range(T_TOKENS)]
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.synchronize()  # uploads and the workspace zeroing ran on the default stream
+
+    def step():
+        for t in range(T_TOKENS):
+            gsi.stack_raw(args_t[t], 4, 1, EPS, ws, stream=stream)
+
+    # eager run once (validates the step), then capture the whole step
+    with torch.cuda.stream(stream):
+        step()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    for _ in range(max(args.warmup, 3)):
+        graph.replay()
+    stream.synchronize()
+    assert gsi.workspace_status(ws, stream=stream) == 0
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        graph.replay()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    ms = e0.elapsed_time(e1) / args.steps
+    if dist:
+        t = torch.tensor([ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    tokens_per_s = T_TOKENS * world / (ms / 1e3)
+
+    flags_np = [F.cpu().numpy().astype(bool) for F in Fs]
+    ab = algorithmic_bytes(maps_in, flags_np)
+    step_gbs = ab["total"] / (ms * 1e-3) / 1e9
+    hbm_peak, peak_kind = peaks()
+
+    # ---- per-kernel timing: gate and apply launched alone, each between two events
+    G1 = torch.empty(1, K_RANK, device=dev)
+    rho1 = torch.empty(1, device=dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(T_TOKENS * 4)]
+    Yk = [torch.empty_like(Y) for Y in Ys]
+    Fk = [torch.empty_like(F) for F in Fs]
+    with torch.cuda.stream(stream):
+        for t in range(T_TOKENS):
+            for i in range(4):
+                m = reps[t % R][i]
+                e = ev[t * 4 + i]
+                e[0].record(stream)
+                gsi.gate(m, Xs[i][t:t + 1], EPS, workspace=ws, G=G1, rho=rho1,
+                         flags=Fk[i][t:t + 1], stream=stream)
+                e[1].record(stream)
+                gsi.apply(m, Xs[i][t:t + 1], G1, ws, Y=Yk[i][t:t + 1], stream=stream)
+                e[2].record(stream)
+    stream.synchronize()
+    t_gate = t_fast = t_slow = 0.0
+    n_f = n_s = 0
+    for t in range(T_TOKENS):
+        for i in range(4):
+            e = ev[t * 4 + i]
+            t_gate += e[0].elapsed_time(e[1])
+            ta = e[1].elapsed_time(e[2])
+            if flags_np[i][t]:
+                t_slow += ta
+                n_s += 1
+            else:
+                t_fast += ta
+                n_f += 1
+    for i in range(4):
+        assert torch.equal(Yk[i], Ys[i]), "two-launch path disagrees with the fused call"
+    k_gate = ab["gate"] / (t_gate * 1e-3) / 1e9
+    k_fast = ab["fast"] / (t_fast * 1e-3) / 1e9 if t_fast else None
+    k_slow = ab["slow"] / (t_slow * 1e-3) / 1e9 if t_slow else None
+    t_apply = t_fast + t_slow
+    k_apply = (ab["fast"] + ab["slow"]) / (t_apply * 1e-3) / 1e9
+    n_launch = T_TOKENS * 4
+    if t_apply >= t_gate:
+        dom = dict(name="gsi apply (fast y = M g / slow y = W x)", gbs=k_apply,
+                   bytes_per_launch=(ab["fast"] + ab["slow"]) / n_launch, ms=t_apply / n_launch)
+    else:
+        dom = dict(name="gsi gate (g = V^T x, rho, flags)", gbs=k_gate,
+                   bytes_per_launch=ab["gate"] / n_launch, ms=t_gate / n_launch)
+
+    # ---- end to end: pinned host tokens in, outputs and flags out, every step
+    Xh = [X.cpu().pin_memory() for X in Xs]
+    Yh = [torch.empty(Y.shape, dtype=Y.dtype, pin_memory=True) for Y in Ys]
+    Fh = [torch.empty(F.shape, dtype=F.dtype, pin_memory=True) for F in Fs]
+    h2d = sum(x.numel() * x.element_size() for x in Xh)
+    d2h = sum(y.numel() * y.element_size() for y in Yh) + sum(f.numel() for f in Fh)
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            for xd, xh in zip(Xs, Xh):
+                xd.copy_(xh, non_blocking=True)
+            graph.replay()
+            for yd, yh in zip(Ys, Yh):
+                yh.copy_(yd, non_blocking=True)
+            for fd, fh in zip(Fs, Fh):
+                fh.copy_(fd, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    stream.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    e2e_tps = T_TOKENS * world / (e2e_ms / 1e3)
+
+    # ---- oracle on the host cores (bounded sample of the same workload)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        maps64 = oracle_maps(maps_in, [b.M.cpu() for b in base])
+        n_tok = args.cpu_tokens
+        v, dt = time_oracle(maps64, n_tok, EPS)
+        cpu = {"value": v, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
+               "sample": f"first {n_tok} of the 256 decode tokens through all four maps "
+                         f"({dt:.1f} s, float64 numpy, BLAS threads = host cores)"}
+
+    gpu_launches = args.steps * T_TOKENS * 4 * 2
+    line = {
+        "metric": "gsi_linear_tokens_per_s_batch1",
+        "value": tokens_per_s,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": "6B-class decoder layer linears at batch 1: qkv 12288x4096, out 4096x4096, "
+                        "up 16384x4096, down 4096x16384; bf16 W/V/M/x, fp32 accumulate and y; "
+                        f"k={K_RANK}, eps={EPS}; 256 sequential single-token steps x 4 maps "
+                        "(1024 gated-map calls) per step; 26/256 slow tokens per map",
+            "l2": f"inputs larger than L2: weights rotate over {R} device replicas of the layer "
+                  f"({R * sum(map_bytes(m)['V'] + map_bytes(m)['M'] + map_bytes(m)['gram'] for m in maps_in) / 1e6:.0f} MB "
+                  "of fast-path weights, 129 MB L2)",
+            "parallelism": "replicas only" if world > 1 else "single GPU",
+            "graph": "whole step captured in one CUDA graph, programmatic dependent launch between kernels",
+        },
+        "achieved_step_gbs": step_gbs,
+        "step_frac_of_hbm_peak": step_gbs / hbm_peak,
+        "bytes_per_step": ab["total"],
+        "dense_bytes_per_step": ab["dense"],
+        "bytes_saved_vs_dense": ab["dense"] / ab["total"],
+        "slow_fraction": ab["n_slow"] / (ab["n_slow"] + ab["n_fast"]),
+        "kernels_alone_gbs": {"gate": k_gate, "apply_fast": k_fast, "apply_slow": k_slow,
+                              "gate_ms_total": t_gate, "apply_ms_total": t_apply},
+        "roofline": {
+            "kernel": dom["name"], "bound": "hbm", "achieved": dom["gbs"], "peak": hbm_peak,
+            "unit": "GB/s", "frac": dom["gbs"] / hbm_peak, "traffic": None,
+            "peak_kind": peak_kind, "timing": "each launch alone between CUDA events",
+            "bytes_per_launch": dom["bytes_per_launch"], "ms_per_launch": dom["ms"],
+        },
+        "e2e": {"value": e2e_tps, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": gpu_launches,
+        "clocks": clocks,
+        "cpu_baseline": cpu,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

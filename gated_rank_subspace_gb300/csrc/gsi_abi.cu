@@ -1,0 +1,381 @@
+// C ABI of the gated-subspace linear map: argument validation, workspace
+// layout and kernel dispatch.  Declarations and the contract of every entry
+// point are in include/gsi.h.
+
+#include <atomic>
+#include <cstdarg>
+#include <cstdio>
+#include <cmath>
+#include <mutex>
+#include <string>
+
+#include "gsi_common.cuh"
+#include "gsi_kernels.h"
+#include "gsi_plan.h"
+
+namespace gsi {
+
+static thread_local std::string g_err;
+static std::atomic<int> g_fail_after{0};
+
+static gsi_status fail(gsi_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+static gsi_status ok() {
+  g_err.clear();
+  return GSI_OK;
+}
+
+// Host-side fault injection: when armed with n, the n-th launch step fails.
+static bool injected_failure() {
+  int n = g_fail_after.load();
+  if (n <= 0) return false;
+  if (g_fail_after.fetch_sub(1) == 1) return true;
+  return false;
+}
+
+static gsi_status cuda_check(cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return GSI_OK;
+  return fail(GSI_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+static int elem_bytes(gsi_dtype dt) { return dt == GSI_BF16 ? 2 : 4; }
+
+static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+static gsi_status check_dtype(gsi_dtype dt) {
+  if (dt != GSI_F32 && dt != GSI_BF16) return fail(GSI_ERR_INVALID_ARG, "unknown dtype %d", int(dt));
+  return GSI_OK;
+}
+
+static gsi_status check_shape(int64_t d, int64_t d_out, int64_t k, gsi_dtype dt) {
+  gsi_status s = check_dtype(dt);
+  if (s != GSI_OK) return s;
+  if (d <= 0 || d_out <= 0 || k <= 0)
+    return fail(GSI_ERR_INVALID_ARG, "sizes must be positive (d=%lld d_out=%lld k=%lld)",
+                (long long)d, (long long)d_out, (long long)k);
+  if (k > d) return fail(GSI_ERR_INVALID_ARG, "k=%lld exceeds d=%lld", (long long)k, (long long)d);
+  if (k > GSI_MAX_K) return fail(GSI_ERR_UNSUPPORTED, "k=%lld exceeds GSI_MAX_K=%d", (long long)k, GSI_MAX_K);
+  if (d > (int64_t(1) << 30) || d_out > (int64_t(1) << 30))
+    return fail(GSI_ERR_UNSUPPORTED, "dimension above 2^30");
+  const int es = elem_bytes(dt);
+  if ((d * es) % 16 || (k * es) % 16)
+    return fail(GSI_ERR_UNSUPPORTED, "d*%d and k*%d bytes must be multiples of 16 (d=%lld k=%lld)",
+                es, es, (long long)d, (long long)k);
+  return GSI_OK;
+}
+
+static gsi_status check_ptr(const void* p, const char* name) {
+  if (!p) return fail(GSI_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned(p, 16)) return fail(GSI_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  return GSI_OK;
+}
+
+static gsi_status check_map(const gsi_map_desc* m) {
+  if (!m) return fail(GSI_ERR_INVALID_ARG, "map descriptor is NULL");
+  gsi_status s = check_shape(m->d, m->d_out, m->k, m->dtype);
+  if (s != GSI_OK) return s;
+  if ((s = check_ptr(m->W, "map.W")) != GSI_OK) return s;
+  if ((s = check_ptr(m->V, "map.V")) != GSI_OK) return s;
+  if ((s = check_ptr(m->M, "map.M")) != GSI_OK) return s;
+  if (m->dtype == GSI_BF16 && !m->gram)
+    return fail(GSI_ERR_INVALID_ARG, "bf16 maps need the Gram matrix V^T V (map.gram is NULL)");
+  if (m->gram && !aligned(m->gram, 16)) return fail(GSI_ERR_INVALID_ARG, "map.gram is not 16-byte aligned");
+  return GSI_OK;
+}
+
+static gsi_status check_tokens(int64_t T, float eps) {
+  if (T < 0) return fail(GSI_ERR_INVALID_ARG, "T=%lld is negative", (long long)T);
+  if (T > (int64_t(1) << 24)) return fail(GSI_ERR_UNSUPPORTED, "T=%lld above 2^24", (long long)T);
+  if (std::isnan(eps) || eps < 0.f) return fail(GSI_ERR_INVALID_ARG, "eps must be >= 0 and not NaN");
+  return GSI_OK;
+}
+
+static gsi_status check_workspace(const void* ws, size_t have, size_t need) {
+  if (need == 0) return GSI_OK;
+  if (!ws) return fail(GSI_ERR_WORKSPACE, "workspace is NULL (%zu bytes needed)", need);
+  if (!aligned(ws, 256)) return fail(GSI_ERR_WORKSPACE, "workspace is not 256-byte aligned");
+  if (have < need) return fail(GSI_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", have, need);
+  return GSI_OK;
+}
+
+// SM count of the current device, queried once per device (so that nothing
+// but kernel launches happens while a caller captures a CUDA graph).
+static int sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  if (dev < 64 && (n = cache[dev].load()) > 0) return n;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  if (dev < 64) cache[dev].store(n);
+  return n;
+}
+
+// Resolve the path for a call.  Only the streaming (CUDA-core) kernels exist
+// for now; they handle every T.
+static gsi_status resolve_path(const gsi_map_desc* m, int64_t T, gsi_path path, gsi_path* out) {
+  (void)m;
+  (void)T;
+  if (path == GSI_PATH_AUTO || path == GSI_PATH_STREAM) {
+    *out = GSI_PATH_STREAM;
+    return GSI_OK;
+  }
+  if (path == GSI_PATH_TENSOR) return fail(GSI_ERR_UNSUPPORTED, "tensor-core path not built");
+  return fail(GSI_ERR_INVALID_ARG, "unknown path %d", int(path));
+}
+
+static size_t stream_ws(const gsi_map_desc* m, int64_t T) {
+  return layout_stream(m->d, m->k, elem_bytes(m->dtype), T).total;
+}
+
+// Enqueue the apply kernel for one map, reading the counts and index lists
+// the gate kernel left in the workspace.  All arguments validated.
+static gsi_status run_apply(const gsi_map_desc* m, const void* X, const float* G, int64_t T, float* Y,
+                            void* ws, cudaStream_t st) {
+  const int es = elem_bytes(m->dtype);
+  const StreamLayout L = layout_stream(m->d, m->k, es, T);
+  char* base = static_cast<char*>(ws);
+  if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
+  const ApplyPlan ap = plan_apply(m->d, m->d_out, m->k, es);
+  ApplyArgs aa{};
+  aa.W = m->W;
+  aa.M = m->M;
+  aa.X = X;
+  aa.G = G;
+  aa.Y = Y;
+  aa.idx = reinterpret_cast<const int32_t*>(base + L.idx);
+  aa.ctrl = reinterpret_cast<const Ctrl*>(base + L.ctrl);
+  aa.d = m->d;
+  aa.d_out = m->d_out;
+  aa.k = int(m->k);
+  aa.T = int(T);
+  aa.rows_slow = ap.rows_slow;
+  aa.fast_units = ap.fast_units;
+  aa.slow_units = ap.slow_units;
+  aa.x_stage_max = ap.x_stage_tokens_max;
+  aa.g_stage_max = ap.g_stage_tokens_max;
+  const int nsm = sm_count();
+  if (nsm <= 0) return fail(GSI_ERR_CUDA, "cannot query the device's SM count");
+  return cuda_check(launch_apply(aa, ap, m->dtype, nsm, st, true), "apply kernel launch");
+}
+
+// Enqueue gate (+ optional apply) for one map.  All arguments validated.
+static gsi_status run_stream(const gsi_map_desc* m, const void* X, int64_t T, float eps, float* Y,
+                             uint8_t* flags, float* rho, float* G_out, void* ws, cudaStream_t st,
+                             bool apply) {
+  const int es = elem_bytes(m->dtype);
+  const GatePlan gp = plan_gate(m->d, m->k, es, T);
+  const StreamLayout L = layout_stream(m->d, m->k, es, T);
+  char* base = static_cast<char*>(ws);
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(base + L.ctrl);
+
+  if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
+
+  GateArgs ga{};
+  ga.X = X;
+  ga.V = m->V;
+  ga.gram = m->gram;
+  ga.d = m->d;
+  ga.k = int(m->k);
+  ga.T = int(T);
+  ga.eps = eps;
+  ga.rs = gp.rs;
+  ga.nv = gp.nv;
+  ga.nrg = gp.nrg;
+  ga.ks = gp.ks;
+  ga.n_clusters = gp.n_clusters;
+  ga.part_g = reinterpret_cast<float*>(base + L.part_g);
+  ga.part_x = reinterpret_cast<float*>(base + L.part_x);
+  ga.G = G_out ? G_out : reinterpret_cast<float*>(base + L.g);
+  ga.rho = rho;
+  ga.flags = flags;
+  ga.idx = reinterpret_cast<int32_t*>(base + L.idx);
+  ga.ctrl = ctrl;
+  if (apply) {
+    // Speculative L2 prefetch of the image M: most tokens take the fast path.
+    const uint64_t total = uint64_t(m->d_out) * m->k * es;
+    uint64_t share = (total + gp.n_slabs - 1) / gp.n_slabs;
+    share = (share + 15) / 16 * 16;
+    ga.pf_base = static_cast<const char*>(m->M);
+    ga.pf_share = share;
+    ga.pf_total = total;
+  }
+  gsi_status s = cuda_check(launch_gate(ga, gp, m->dtype, st, true), "gate kernel launch");
+  if (s != GSI_OK || !apply) return s;
+  return run_apply(m, X, ga.G, T, Y, ws, st);
+}
+
+}  // namespace gsi
+
+using namespace gsi;
+
+extern "C" {
+
+const char* gsi_last_error(void) { return g_err.c_str(); }
+
+void gsi_debug_fail_after(int n) { g_fail_after.store(n > 0 ? n : 0); }
+
+gsi_status gsi_build_image(const void* W, const void* V, void* M, float* gram, int64_t d,
+                           int64_t d_out, int64_t k, gsi_dtype dtype, void* stream) {
+  gsi_status s = check_shape(d, d_out, k, dtype);
+  if (s != GSI_OK) return s;
+  if ((s = check_ptr(W, "W")) != GSI_OK) return s;
+  if ((s = check_ptr(V, "V")) != GSI_OK) return s;
+  if ((s = check_ptr(M, "M")) != GSI_OK) return s;
+  if (gram && !aligned(gram, 16)) return fail(GSI_ERR_INVALID_ARG, "gram is not 16-byte aligned");
+  if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
+  s = cuda_check(launch_image(W, V, M, gram, d, d_out, k, dtype, static_cast<cudaStream_t>(stream)),
+                 "image kernel launch");
+  return s == GSI_OK ? ok() : s;
+}
+
+gsi_status gsi_linear_workspace_size(const gsi_map_desc* map, int64_t T, gsi_path path,
+                                     size_t* bytes) {
+  if (!bytes) return fail(GSI_ERR_INVALID_ARG, "bytes is NULL");
+  if (!map) return fail(GSI_ERR_INVALID_ARG, "map descriptor is NULL");
+  gsi_status s = check_shape(map->d, map->d_out, map->k, map->dtype);
+  if (s != GSI_OK) return s;
+  if ((s = check_tokens(T, 0.f)) != GSI_OK) return s;
+  gsi_path p;
+  if ((s = resolve_path(map, T, path, &p)) != GSI_OK) return s;
+  *bytes = stream_ws(map, T);
+  return ok();
+}
+
+gsi_status gsi_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
+  if (!workspace) return fail(GSI_ERR_WORKSPACE, "workspace is NULL");
+  if (!aligned(workspace, 256)) return fail(GSI_ERR_WORKSPACE, "workspace is not 256-byte aligned");
+  if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
+  gsi_status s = cuda_check(cudaMemsetAsync(workspace, 0, ws_bytes, static_cast<cudaStream_t>(stream)),
+                            "workspace memset");
+  return s == GSI_OK ? ok() : s;
+}
+
+gsi_status gsi_workspace_status(const void* workspace, uint32_t* code, void* stream) {
+  if (!workspace || !code) return fail(GSI_ERR_INVALID_ARG, "workspace and code must be non-NULL");
+  if (!aligned(workspace, 256)) return fail(GSI_ERR_WORKSPACE, "workspace is not 256-byte aligned");
+  const Ctrl* c = static_cast<const Ctrl*>(workspace);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  gsi_status s = cuda_check(cudaMemcpyAsync(code, &c->err, sizeof(uint32_t), cudaMemcpyDeviceToHost, st),
+                            "error word copy");
+  if (s != GSI_OK) return s;
+  s = cuda_check(cudaStreamSynchronize(st), "stream synchronize");
+  if (s != GSI_OK) return s;
+  if (*code) return fail(GSI_ERR_TIMEOUT, "device error word %u", *code);
+  return ok();
+}
+
+gsi_status gsi_gate(const gsi_map_desc* map, const void* X, int64_t T, float eps, float* G,
+                    float* rho, uint8_t* flags, void* workspace, size_t ws_bytes, void* stream) {
+  gsi_status s = check_map(map);
+  if (s != GSI_OK) return s;
+  if ((s = check_tokens(T, eps)) != GSI_OK) return s;
+  if (T == 0) return ok();
+  if ((s = check_ptr(X, "X")) != GSI_OK) return s;
+  if ((s = check_ptr(G, "G")) != GSI_OK) return s;
+  if (!flags) return fail(GSI_ERR_INVALID_ARG, "flags is NULL");
+  if (rho && !aligned(rho, 4)) return fail(GSI_ERR_INVALID_ARG, "rho is misaligned");
+  if ((s = check_workspace(workspace, ws_bytes, stream_ws(map, T))) != GSI_OK) return s;
+  s = run_stream(map, X, T, eps, nullptr, flags, rho, G, workspace,
+                 static_cast<cudaStream_t>(stream), false);
+  return s == GSI_OK ? ok() : s;
+}
+
+gsi_status gsi_apply(const gsi_map_desc* map, const void* X, const float* G, int64_t T, float* Y,
+                     void* workspace, size_t ws_bytes, void* stream) {
+  gsi_status s = check_map(map);
+  if (s != GSI_OK) return s;
+  if ((s = check_tokens(T, 0.f)) != GSI_OK) return s;
+  if (T == 0) return ok();
+  if ((s = check_ptr(X, "X")) != GSI_OK) return s;
+  if ((s = check_ptr(G, "G")) != GSI_OK) return s;
+  if ((s = check_ptr(Y, "Y")) != GSI_OK) return s;
+  if ((s = check_workspace(workspace, ws_bytes, stream_ws(map, T))) != GSI_OK) return s;
+  s = run_apply(map, X, G, T, Y, workspace, static_cast<cudaStream_t>(stream));
+  return s == GSI_OK ? ok() : s;
+}
+
+gsi_status gsi_compact(const uint8_t* flags, int64_t T, int32_t* idx, int32_t* counts, void* stream) {
+  if (T < 0 || T > (int64_t(1) << 24)) return fail(GSI_ERR_INVALID_ARG, "bad T=%lld", (long long)T);
+  if (!flags || !idx || !counts) return fail(GSI_ERR_INVALID_ARG, "flags, idx and counts must be non-NULL");
+  if (!aligned(idx, 4) || !aligned(counts, 4)) return fail(GSI_ERR_INVALID_ARG, "idx/counts misaligned");
+  if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
+  gsi_status s = cuda_check(launch_compact(flags, int(T), idx, counts, static_cast<cudaStream_t>(stream)),
+                            "compact kernel launch");
+  return s == GSI_OK ? ok() : s;
+}
+
+gsi_status gsi_linear_ex(const gsi_map_desc* map, const void* X, int64_t T, float eps, float* Y,
+                         uint8_t* flags, float* rho, void* workspace, size_t ws_bytes, gsi_path path,
+                         void* stream) {
+  gsi_status s = check_map(map);
+  if (s != GSI_OK) return s;
+  if ((s = check_tokens(T, eps)) != GSI_OK) return s;
+  gsi_path p;
+  if ((s = resolve_path(map, T, path, &p)) != GSI_OK) return s;
+  if (T == 0) return ok();
+  if ((s = check_ptr(X, "X")) != GSI_OK) return s;
+  if ((s = check_ptr(Y, "Y")) != GSI_OK) return s;
+  if (!flags) return fail(GSI_ERR_INVALID_ARG, "flags is NULL");
+  if (rho && !aligned(rho, 4)) return fail(GSI_ERR_INVALID_ARG, "rho is misaligned");
+  if ((s = check_workspace(workspace, ws_bytes, stream_ws(map, T))) != GSI_OK) return s;
+  s = run_stream(map, X, T, eps, Y, flags, rho, nullptr, workspace, static_cast<cudaStream_t>(stream), true);
+  return s == GSI_OK ? ok() : s;
+}
+
+gsi_status gsi_linear(const gsi_map_desc* map, const void* X, int64_t T, float eps, float* Y,
+                      uint8_t* flags, float* rho, void* workspace, size_t ws_bytes, void* stream) {
+  return gsi_linear_ex(map, X, T, eps, Y, flags, rho, workspace, ws_bytes, GSI_PATH_AUTO, stream);
+}
+
+gsi_status gsi_stack_workspace_size(const gsi_map_desc* maps, int64_t n_maps, int64_t T, size_t* bytes) {
+  if (!bytes) return fail(GSI_ERR_INVALID_ARG, "bytes is NULL");
+  if (!maps || n_maps <= 0) return fail(GSI_ERR_INVALID_ARG, "maps is NULL or n_maps <= 0");
+  size_t need = 0;
+  for (int64_t i = 0; i < n_maps; ++i) {
+    size_t b = 0;
+    gsi_status s = gsi_linear_workspace_size(&maps[i], T, GSI_PATH_AUTO, &b);
+    if (s != GSI_OK) return s;
+    if (b > need) need = b;
+  }
+  *bytes = need;
+  return ok();
+}
+
+gsi_status gsi_stack(const gsi_map_desc* maps, int64_t n_maps, const void* const* X, int64_t T,
+                     float eps, float* const* Y, uint8_t* const* flags, void* workspace,
+                     size_t ws_bytes, void* stream) {
+  if (!maps || n_maps <= 0) return fail(GSI_ERR_INVALID_ARG, "maps is NULL or n_maps <= 0");
+  if (!X || !Y || !flags) return fail(GSI_ERR_INVALID_ARG, "X, Y and flags arrays must be non-NULL");
+  gsi_status s = check_tokens(T, eps);
+  if (s != GSI_OK) return s;
+  size_t need = 0;
+  for (int64_t i = 0; i < n_maps; ++i) {
+    if ((s = check_map(&maps[i])) != GSI_OK)
+      return fail(s, "map %lld: %s", (long long)i, g_err.c_str());
+    if (T > 0) {
+      if ((s = check_ptr(X[i], "X[i]")) != GSI_OK) return fail(s, "map %lld: %s", (long long)i, g_err.c_str());
+      if ((s = check_ptr(Y[i], "Y[i]")) != GSI_OK) return fail(s, "map %lld: %s", (long long)i, g_err.c_str());
+      if (!flags[i]) return fail(GSI_ERR_INVALID_ARG, "map %lld: flags is NULL", (long long)i);
+    }
+    size_t b = stream_ws(&maps[i], T);
+    if (b > need) need = b;
+  }
+  if (T == 0) return ok();
+  if ((s = check_workspace(workspace, ws_bytes, need)) != GSI_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  for (int64_t i = 0; i < n_maps; ++i) {
+    s = run_stream(&maps[i], X[i], T, eps, Y[i], flags[i], nullptr, nullptr, workspace, st, true);
+    if (s != GSI_OK) return fail(s, "map %lld: %s", (long long)i, g_err.c_str());
+  }
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,163 @@
+// Shared device helpers for the gated-subspace kernels (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cooperative_groups.h>
+#include <stdint.h>
+
+#include "../../include/gsi.h"
+
+namespace gsi {
+
+namespace cg = cooperative_groups;
+
+// ---------------------------------------------------------------- element types
+// Both storage types are read as 16-byte vectors: 4 float32 or 8 bf16.
+struct F32 {
+  static constexpr int kBytes = 4;
+  static constexpr int kPerVec = 4;
+  __device__ __forceinline__ static void unpack(const uint4& v, float* f) {
+    f[0] = __uint_as_float(v.x);
+    f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z);
+    f[3] = __uint_as_float(v.w);
+  }
+  __device__ __forceinline__ static float load1(const void* base, int64_t i) {
+    return reinterpret_cast<const float*>(base)[i];
+  }
+  __device__ __forceinline__ static void store1(void* base, int64_t i, float v) {
+    reinterpret_cast<float*>(base)[i] = v;
+  }
+  __device__ __forceinline__ static float load1_cg(const void* base, int64_t i) {
+    return __ldcg(reinterpret_cast<const float*>(base) + i);
+  }
+};
+
+struct BF16 {
+  static constexpr int kBytes = 2;
+  static constexpr int kPerVec = 8;
+  // bf16 -> f32 widening is exact: the bf16 bits are the high half of the f32.
+  __device__ __forceinline__ static void unpack2(uint32_t u, float& lo, float& hi) {
+    lo = __uint_as_float(u << 16);
+    hi = __uint_as_float(u & 0xffff0000u);
+  }
+  __device__ __forceinline__ static void unpack(const uint4& v, float* f) {
+    unpack2(v.x, f[0], f[1]);
+    unpack2(v.y, f[2], f[3]);
+    unpack2(v.z, f[4], f[5]);
+    unpack2(v.w, f[6], f[7]);
+  }
+  __device__ __forceinline__ static float load1(const void* base, int64_t i) {
+    uint16_t b = reinterpret_cast<const uint16_t*>(base)[i];
+    return __uint_as_float(uint32_t(b) << 16);
+  }
+  __device__ __forceinline__ static void store1(void* base, int64_t i, float v) {
+    reinterpret_cast<__nv_bfloat16*>(base)[i] = __float2bfloat16_rn(v);
+  }
+  __device__ __forceinline__ static float load1_cg(const void* base, int64_t i) {
+    unsigned short b = __ldcg(reinterpret_cast<const unsigned short*>(base) + i);
+    return __uint_as_float(uint32_t(b) << 16);
+  }
+};
+
+// ---------------------------------------------------------------- memory access
+// Read-only weights (W, V, M, Gram): 16-byte non-coherent loads that do not
+// allocate in L1 (each byte is used once per CTA).
+__device__ __forceinline__ uint4 ld_weight_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+               : "l"(p));
+  return r;
+}
+
+// Data written by an earlier kernel of the stream (tokens, projections,
+// counts, index lists): read at L2 so no stale L1 line can be hit.
+__device__ __forceinline__ uint4 ld_cg_v4(const void* p) {
+  return __ldcg(reinterpret_cast<const uint4*>(p));
+}
+
+__device__ __forceinline__ uint32_t ld_cg_u8(const uint8_t* p) {
+  uint32_t r;
+  asm volatile("ld.global.cg.u8 %0, [%1];" : "=r"(r) : "l"(p));
+  return r;
+}
+
+// Speculative L2 prefetch of a byte range (16-byte aligned, multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// ---------------------------------------------------------------- programmatic dependent launch
+// launch_dependents lets the next kernel of the stream start its prologue
+// (weight prefetch) early; wait blocks until every kernel this one depends on
+// has finished and its writes are visible.  Both are no-ops when the kernel
+// was launched without the programmatic-serialisation attribute.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// ---------------------------------------------------------------- reductions
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Reduce R per-lane partial sums (R = 1, 2, 4, 8, 16 or 32) across the warp
+// with R - 1 + 5 - log2(R) shuffles instead of 5 R: each butterfly stage halves
+// the number of live values while doubling the lanes each one covers.
+// On return, lane l holds the full sum of value index
+//   idx(l) = bits of l above position 5 - log2(R)  (see row_of_lane).
+template <int R>
+__device__ __forceinline__ float warp_reduce_multi(float (&v)[R], int lane) {
+  static_assert(R == 1 || R == 2 || R == 4 || R == 8 || R == 16 || R == 32, "R power of 2");
+#pragma unroll
+  for (int st = 0; st < 5; ++st) {
+    const int off = 16 >> st;
+    const int n = R >> st;  // live values before this stage (compile-time per stage)
+    if (n > 1) {
+      const bool upper = (lane & off) != 0;
+#pragma unroll
+      for (int i = 0; i < n / 2; ++i) {
+        // Upper lanes keep the upper half of the live values, the others the
+        // lower half; each sends the half it does not keep to its partner.
+        const float send = upper ? v[i] : v[i + n / 2];
+        const float keep = upper ? v[i + n / 2] : v[i];
+        v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+      }
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], off);
+    }
+  }
+  return v[0];
+}
+
+// Value index whose total lane `lane` holds after warp_reduce_multi<R>:
+// the stage with offset 16 >> st sets bit (R >> (st + 1)) of the index.
+template <int R>
+__device__ __forceinline__ int row_of_lane(int lane) {
+  int idx = 0;
+#pragma unroll
+  for (int st = 0; st < 5; ++st) {
+    const int n = R >> st;
+    if (n > 1 && (lane & (16 >> st))) idx += n / 2;
+  }
+  return idx;
+}
+
+// ---------------------------------------------------------------- workspace layout
+// Control words at the head of every workspace (256 bytes).
+struct Ctrl {
+  uint32_t ticket;     // cluster arrival counter of the gate kernel (self-resetting)
+  uint32_t err;        // device error word (0 = ok); set by bounded waits
+  int32_t counts[2];   // {n_fast, n_slow} of the last gate
+  uint32_t pad[60];
+};
+static_assert(sizeof(Ctrl) == 256, "Ctrl is 256 bytes");
+
+constexpr uint32_t kErrTimeout = 1;
+
+}  // namespace gsi

@@ -1,0 +1,176 @@
+/*
+ * gsi.h -- C ABI of the gated-subspace linear map on one sm_103a GPU.
+ *
+ * The method ("Gated Subspace Inference for Transformer Acceleration",
+ * gist.science technical summary):
+ *
+ *   §2.1 core decomposition.  For a linear map W (d_out x d) and a token
+ *        x (length d), with an orthonormal rank-k basis V_k (d x k):
+ *        x = V_k V_k^T x + r,  y = W x = (W V_k)(V_k^T x) + W r = M g + W r,
+ *        where M = W V_k is the cached low-rank weight image (d_out x k) and
+ *        g = V_k^T x the projection (length k).
+ *   §2.2 gated residual step.  Per token, rho = ||r|| / ||x||.  If rho < eps
+ *        the token takes the fast path y = M g (reads M, k columns' worth,
+ *        instead of W); if rho >= eps it takes the exact slow path y = W x.
+ *        Theorem 4 bounds the fast-path error by ||W||_2 * eps * ||x||.
+ *   §2.2 (all linear maps) / §3.  The gate applies to every projection of a
+ *        transformer layer (QKV, output, MLP up, MLP down).
+ *
+ * Conventions shared by every entry point:
+ *   - All matrices are dense and row-major.  X is T x d (token t is row t),
+ *     W is d_out x d, V is d x k, M is d_out x k, Y is T x d_out (float32).
+ *     flags is T bytes (1 = slow path, 0 = fast path); rho is T float32.
+ *   - W, V, M and X share one element type (gsi_dtype).  Accumulation is
+ *     always float32.  For GSI_BF16 the caller supplies the k x k float32
+ *     Gram matrix V^T V (built by gsi_build_image): a bf16-rounded basis is
+ *     not exactly orthonormal and the library evaluates ||x - V g||^2 as
+ *     ||x||^2 - 2||g||^2 + g^T (V^T V) g, which is exact for any basis.
+ *     For GSI_F32 the Gram may be NULL, meaning "V is orthonormal"
+ *     (||r||^2 = ||x||^2 - ||g||^2).
+ *   - Readings where the pages are silent: a tie rho == eps is slow; a zero
+ *     token has rho = 0 (fast, y = 0); a token with a NaN/Inf has rho = NaN
+ *     and is slow.  eps = +inf is allowed (static projection: all fast).
+ *   - Pointers to matrices, vectors and the workspace are DEVICE pointers;
+ *     the arrays of pointers passed to gsi_stack and the status outputs
+ *     (bytes, counts) are HOST pointers.  The caller owns every buffer; the
+ *     library allocates nothing in these calls.
+ *   - Every device pointer must be 16-byte aligned, the workspace 256-byte
+ *     aligned.  d * sizeof(elem) and k * sizeof(elem) must be multiples of
+ *     16 bytes (d, k multiples of 8 for bf16, of 4 for f32); otherwise the
+ *     call returns GSI_ERR_UNSUPPORTED.  k <= GSI_MAX_K and k <= d.
+ *   - Execution is asynchronous on `stream` (a cudaStream_t; NULL = the
+ *     legacy default stream).  Argument errors are reported synchronously,
+ *     before anything is enqueued; launch failures return GSI_ERR_CUDA.
+ *     Device-side faults surface on the caller's next synchronisation.
+ *   - The gate's decision never leaves the device: no call synchronises the
+ *     stream, so calls may be captured into a CUDA graph.
+ *   - On any non-OK status, gsi_last_error() returns a message for the
+ *     calling thread.
+ */
+#ifndef GSI_H
+#define GSI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GSI_MAX_K 512
+
+typedef enum gsi_status {
+  GSI_OK = 0,
+  GSI_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad eps, misalignment */
+  GSI_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels handle     */
+  GSI_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed          */
+  GSI_ERR_WORKSPACE = 4,   /* workspace missing, too small or misaligned    */
+  GSI_ERR_TIMEOUT = 5      /* a bounded device wait gave up (see gsi_workspace_status) */
+} gsi_status;
+
+typedef enum gsi_dtype { GSI_F32 = 0, GSI_BF16 = 1 } gsi_dtype;
+
+/* Which kernels run the map.  AUTO picks STREAM for small T (decode) and for
+ * f32, TENSOR (tcgen05 contractions) for bf16 at prefill-sized T. */
+typedef enum gsi_path { GSI_PATH_AUTO = 0, GSI_PATH_STREAM = 1, GSI_PATH_TENSOR = 2 } gsi_path;
+
+/* One linear map with its cached artefacts (all device pointers). */
+typedef struct gsi_map_desc {
+  int64_t d;        /* input dimension (columns of W, rows of V)      */
+  int64_t d_out;    /* output dimension (rows of W and M)             */
+  int64_t k;        /* subspace rank (columns of V and M)             */
+  gsi_dtype dtype;  /* element type of W, V, M and of the tokens X    */
+  const void* W;    /* d_out x d                                      */
+  const void* V;    /* d x k, orthonormal columns (up to rounding)    */
+  const void* M;    /* d_out x k, the image W V (from gsi_build_image)*/
+  const float* gram;/* k x k float32 V^T V; required for GSI_BF16     */
+} gsi_map_desc;
+
+/* §2.1: build the cached low-rank weight image M = W V (float32 accumulate,
+ * rounded to nearest-even into `dtype`) and, if `gram` is non-NULL, the
+ * float32 Gram matrix V^T V.  One-off per map.  W: d_out x d, V: d x k,
+ * M: d_out x k (output), gram: k x k float32 (output, nullable). */
+gsi_status gsi_build_image(const void* W, const void* V, void* M, float* gram,
+                           int64_t d, int64_t d_out, int64_t k, gsi_dtype dtype,
+                           void* stream);
+
+/* Bytes of device workspace gsi_linear needs for `map` and T tokens with the
+ * given path (host-only arithmetic, no device call).  *bytes is a HOST
+ * pointer. */
+gsi_status gsi_linear_workspace_size(const gsi_map_desc* map, int64_t T, gsi_path path,
+                                     size_t* bytes);
+
+/* Zero a workspace before its first use (its control words must start at
+ * zero; every call leaves them at zero again).  Enqueued on `stream`. */
+gsi_status gsi_workspace_init(void* workspace, size_t ws_bytes, void* stream);
+
+/* Read the device error word of a workspace (SYNCHRONISES `stream`).
+ * *code = 0 when no bounded wait has given up since the last init. */
+gsi_status gsi_workspace_status(const void* workspace, uint32_t* code, void* stream);
+
+/* §2.1-§2.2 gate only: projections G (T x k float32), residual ratios rho
+ * (T float32, nullable) and flags (T bytes) for T tokens X. */
+gsi_status gsi_gate(const gsi_map_desc* map, const void* X, int64_t T, float eps,
+                    float* G, float* rho, uint8_t* flags,
+                    void* workspace, size_t ws_bytes, void* stream);
+
+/* §2.2 per-token gate, compaction step: stable (ascending token index) lists
+ * of fast and slow tokens.  idx (device, 2*T int32) receives the fast list in
+ * idx[0 .. n_fast) and the slow list in idx[T .. T + n_slow); counts (device,
+ * 2 int32) receives {n_fast, n_slow}. */
+gsi_status gsi_compact(const uint8_t* flags, int64_t T, int32_t* idx, int32_t* counts,
+                       void* stream);
+
+/* §2.2 fast and slow paths for the tokens gated by the immediately preceding
+ * gsi_gate call on the same workspace, map, X and T (it reads that call's
+ * counts and index lists from the workspace and its projections G):
+ * Y[t] = M g_t for fast tokens, W x_t for slow tokens.  gsi_gate followed by
+ * gsi_apply computes what one gsi_linear call does, in two launches that can
+ * be timed separately. */
+gsi_status gsi_apply(const gsi_map_desc* map, const void* X, const float* G, int64_t T,
+                     float* Y, void* workspace, size_t ws_bytes, void* stream);
+
+/* §2.1-§2.2: the gated linear map.  For each token t of X (T x d):
+ * flags[t] = (rho_t >= eps); Y[t] = M g_t if fast, W x_t if slow.
+ * Y: T x d_out float32 (output); flags: T bytes (output); rho: T float32
+ * (output, nullable).  `workspace` holds at least
+ * gsi_linear_workspace_size(map, T, GSI_PATH_AUTO) bytes, zeroed once. */
+gsi_status gsi_linear(const gsi_map_desc* map, const void* X, int64_t T, float eps,
+                      float* Y, uint8_t* flags, float* rho,
+                      void* workspace, size_t ws_bytes, void* stream);
+
+/* gsi_linear with an explicit choice of kernels (for comparing the decode
+ * kernels with the tensor-core contractions on the same input). */
+gsi_status gsi_linear_ex(const gsi_map_desc* map, const void* X, int64_t T, float eps,
+                         float* Y, uint8_t* flags, float* rho,
+                         void* workspace, size_t ws_bytes, gsi_path path, void* stream);
+
+/* Workspace for gsi_stack: the maximum over its maps (the calls run in
+ * stream order and reuse one workspace). */
+gsi_status gsi_stack_workspace_size(const gsi_map_desc* maps, int64_t n_maps, int64_t T,
+                                    size_t* bytes);
+
+/* §2.2 "all linear maps": the gated map over a list of n_maps maps (e.g. the
+ * QKV / output / MLP-up / MLP-down projections of every layer), in list
+ * order, each with its own T tokens X[i] (T x maps[i].d), output Y[i]
+ * (T x maps[i].d_out) and flags[i] (T bytes).  maps, X, Y, flags are HOST
+ * arrays of n_maps entries; the entries are device pointers.  Outputs are not
+ * chained into inputs.  Map i+1 starts reading its tokens only after map i
+ * has finished, so X[i+1] may be produced by an earlier kernel of the same
+ * stream. */
+gsi_status gsi_stack(const gsi_map_desc* maps, int64_t n_maps, const void* const* X,
+                     int64_t T, float eps, float* const* Y, uint8_t* const* flags,
+                     void* workspace, size_t ws_bytes, void* stream);
+
+/* Message for the calling thread's last non-OK status ("" if none). */
+const char* gsi_last_error(void);
+
+/* Test hook: make the n-th next launch step report GSI_ERR_CUDA without
+ * touching the GPU (n <= 0 disarms).  Host-side fault injection. */
+void gsi_debug_fail_after(int n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GSI_H */

@@ -188,33 +188,39 @@ def layer_slow_fractions(config: int, n_layers: int, lo=0.05, hi=0.15) -> np.nda
     return rng(config, 0, 0, _FRAC).uniform(lo, hi, n_layers)
 
 
+def map_tokens(config: int, layer: int, role: int, V64: np.ndarray, T: int, f_slow: float,
+               eps: float = EPS, bernoulli: bool = False, salt: int = 0) -> torch.Tensor:
+    """T bf16 tokens for one map: slow ones at s(4 eps), fast ones at s(eps/4).
+
+    Slow tokens are either exactly round(f_slow*T) seeded positions, or
+    per-token Bernoulli(f_slow) labels (exact at f=0 and f=1).  `salt`
+    separates token sets drawn for the same map.
+    """
+    d, k = V64.shape
+    gl = rng(config, layer, role, _LBL * 1000 + salt)
+    s_fast, s_slow = noise_scale(eps / 4, d, k), noise_scale(4 * eps, d, k)
+    if bernoulli:
+        s = np.where(gl.random(T) < f_slow, s_slow, s_fast)
+    else:
+        s = two_level_scales(gl, T, int(round(f_slow * T)), s_fast, s_slow)
+    X = mixed_tokens(rng(config, layer, role, _A * 1000 + salt),
+                     rng(config, layer, role, _N * 1000 + salt), V64, s)
+    return storage(X, torch.bfloat16)
+
+
 def stack_layer(config: int, layer: int, basis_by_role: dict, shapes: dict,
                 T: int, f_slow: float, eps: float = EPS, bernoulli: bool = False,
                 roles=ROLES) -> list:
-    """All maps of one layer for a stack workload (bf16).
-
-    basis_by_role[role] is that layer's float64 basis.  Slow tokens are either
-    exactly round(f_slow*T) seeded positions, or per-token Bernoulli(f_slow)
-    labels (exact at f=0 and f=1).
-    """
+    """All maps of one layer for a stack workload (bf16): W, V and T tokens each."""
     maps = []
     for role in roles:
         m = ROLE_ID[role]
         d_out, d = shapes[role]
         V64 = basis_by_role[role]
-        k = V64.shape[1]
         W = gaussian_weight(rng(config, layer, m, _W), d_out, d)
-        gl = rng(config, layer, m, _LBL)
-        s_fast, s_slow = noise_scale(eps / 4, d, k), noise_scale(4 * eps, d, k)
-        if bernoulli:
-            slow = gl.random(T) < f_slow
-            s = np.where(slow, s_slow, s_fast)
-        else:
-            s = two_level_scales(gl, T, int(round(f_slow * T)), s_fast, s_slow)
-        X = mixed_tokens(rng(config, layer, m, _A), rng(config, layer, m, _N), V64, s)
+        X = map_tokens(config, layer, m, V64, T, f_slow, eps, bernoulli)
         maps.append(MapInputs(f"c{config}.l{layer}.{role}", storage(W, torch.bfloat16),
-                              storage(V64, torch.bfloat16), storage(X, torch.bfloat16),
-                              eps, V64))
+                              storage(V64, torch.bfloat16), X, eps, V64))
     return maps
 
 
