@@ -118,17 +118,29 @@ static int sm_count() {
   return n;
 }
 
-// Resolve the path for a call.  Only the streaming (CUDA-core) kernels exist
-// for now; they handle every T.
+// Resolve the path for a call: the tensor cores for bf16 maps at
+// prefill-sized T, the streaming kernels otherwise.
 static gsi_status resolve_path(const gsi_map_desc* m, int64_t T, gsi_path path, gsi_path* out) {
-  (void)m;
-  (void)T;
-  if (path == GSI_PATH_AUTO || path == GSI_PATH_STREAM) {
+  if (path == GSI_PATH_AUTO) {
+    *out = (m->dtype == GSI_BF16 && T >= kTensorMinT) ? GSI_PATH_TENSOR : GSI_PATH_STREAM;
+    return GSI_OK;
+  }
+  if (path == GSI_PATH_STREAM) {
     *out = GSI_PATH_STREAM;
     return GSI_OK;
   }
-  if (path == GSI_PATH_TENSOR) return fail(GSI_ERR_UNSUPPORTED, "tensor-core path not built");
+  if (path == GSI_PATH_TENSOR) {
+    if (m->dtype != GSI_BF16)
+      return fail(GSI_ERR_UNSUPPORTED, "the tensor-core path takes bf16 maps only");
+    *out = GSI_PATH_TENSOR;
+    return GSI_OK;
+  }
   return fail(GSI_ERR_INVALID_ARG, "unknown path %d", int(path));
+}
+
+static size_t path_ws(const gsi_map_desc* m, int64_t T, gsi_path p) {
+  if (p == GSI_PATH_TENSOR) return layout_tensor(m->d, m->k, T).total;
+  return layout_stream(m->d, m->k, m->dtype == GSI_BF16 ? 2 : 4, T).total;
 }
 
 static size_t stream_ws(const gsi_map_desc* m, int64_t T) {
@@ -198,6 +210,10 @@ static gsi_status run_stream(const gsi_map_desc* m, const void* X, int64_t T, fl
   ga.flags = flags;
   ga.idx = reinterpret_cast<int32_t*>(base + L.idx);
   ga.ctrl = ctrl;
+  if (m->gram) {
+    const uint64_t gb = uint64_t(m->k) * m->k * 4;
+    ga.gram_share = ((gb + gp.n_slabs - 1) / gp.n_slabs + 15) / 16 * 16;
+  }
   if (apply) {
     // Speculative L2 prefetch of the image M: most tokens take the fast path.
     const uint64_t total = uint64_t(m->d_out) * m->k * es;
@@ -210,6 +226,38 @@ static gsi_status run_stream(const gsi_map_desc* m, const void* X, int64_t T, fl
   gsi_status s = cuda_check(launch_gate(ga, gp, m->dtype, st, true), "gate kernel launch");
   if (s != GSI_OK || !apply) return s;
   return run_apply(m, X, ga.G, T, Y, ws, st);
+}
+
+// Enqueue the tensor-core path for one bf16 map.  All arguments validated.
+static gsi_status run_tensor(const gsi_map_desc* m, const void* X, int64_t T, float eps, float* Y,
+                             uint8_t* flags, float* rho, void* ws, cudaStream_t st) {
+  const TensorLayout L = layout_tensor(m->d, m->k, T);
+  char* base = static_cast<char*>(ws);
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(base + L.ctrl);
+  if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
+  TensorArgs t{};
+  t.X = X;
+  t.V = m->V;
+  t.W = m->W;
+  t.M = m->M;
+  t.gram = m->gram;
+  t.d = m->d;
+  t.d_out = m->d_out;
+  t.k = m->k;
+  t.T = T;
+  t.eps = eps;
+  t.Vt = reinterpret_cast<uint16_t*>(base + L.vt);
+  t.G = reinterpret_cast<float*>(base + L.g);
+  t.Gbf = reinterpret_cast<uint16_t*>(base + L.gbf);
+  t.Gfast = reinterpret_cast<uint16_t*>(base + L.gfast);
+  t.Xslow = reinterpret_cast<uint16_t*>(base + L.xslow);
+  t.idx = reinterpret_cast<int32_t*>(base + L.idx);
+  t.counts = ctrl->counts;
+  t.rho = rho;
+  t.flags = flags;
+  t.Y = Y;
+  t.err = &ctrl->err;
+  return cuda_check(launch_tensor_path(t, st), "tensor-core path launch");
 }
 
 }  // namespace gsi
@@ -245,7 +293,7 @@ gsi_status gsi_linear_workspace_size(const gsi_map_desc* map, int64_t T, gsi_pat
   if ((s = check_tokens(T, 0.f)) != GSI_OK) return s;
   gsi_path p;
   if ((s = resolve_path(map, T, path, &p)) != GSI_OK) return s;
-  *bytes = stream_ws(map, T);
+  *bytes = path_ws(map, T, p);
   return ok();
 }
 
@@ -304,7 +352,8 @@ gsi_status gsi_apply(const gsi_map_desc* map, const void* X, const float* G, int
 
 gsi_status gsi_compact(const uint8_t* flags, int64_t T, int32_t* idx, int32_t* counts, void* stream) {
   if (T < 0 || T > (int64_t(1) << 24)) return fail(GSI_ERR_INVALID_ARG, "bad T=%lld", (long long)T);
-  if (!flags || !idx || !counts) return fail(GSI_ERR_INVALID_ARG, "flags, idx and counts must be non-NULL");
+  if (!counts) return fail(GSI_ERR_INVALID_ARG, "counts must be non-NULL");
+  if (T > 0 && (!flags || !idx)) return fail(GSI_ERR_INVALID_ARG, "flags and idx must be non-NULL");
   if (!aligned(idx, 4) || !aligned(counts, 4)) return fail(GSI_ERR_INVALID_ARG, "idx/counts misaligned");
   if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
   gsi_status s = cuda_check(launch_compact(flags, int(T), idx, counts, static_cast<cudaStream_t>(stream)),
@@ -325,8 +374,11 @@ gsi_status gsi_linear_ex(const gsi_map_desc* map, const void* X, int64_t T, floa
   if ((s = check_ptr(Y, "Y")) != GSI_OK) return s;
   if (!flags) return fail(GSI_ERR_INVALID_ARG, "flags is NULL");
   if (rho && !aligned(rho, 4)) return fail(GSI_ERR_INVALID_ARG, "rho is misaligned");
-  if ((s = check_workspace(workspace, ws_bytes, stream_ws(map, T))) != GSI_OK) return s;
-  s = run_stream(map, X, T, eps, Y, flags, rho, nullptr, workspace, static_cast<cudaStream_t>(stream), true);
+  if ((s = check_workspace(workspace, ws_bytes, path_ws(map, T, p))) != GSI_OK) return s;
+  if (p == GSI_PATH_TENSOR)
+    s = run_tensor(map, X, T, eps, Y, flags, rho, workspace, static_cast<cudaStream_t>(stream));
+  else
+    s = run_stream(map, X, T, eps, Y, flags, rho, nullptr, workspace, static_cast<cudaStream_t>(stream), true);
   return s == GSI_OK ? ok() : s;
 }
 
@@ -365,14 +417,21 @@ gsi_status gsi_stack(const gsi_map_desc* maps, int64_t n_maps, const void* const
       if ((s = check_ptr(Y[i], "Y[i]")) != GSI_OK) return fail(s, "map %lld: %s", (long long)i, g_err.c_str());
       if (!flags[i]) return fail(GSI_ERR_INVALID_ARG, "map %lld: flags is NULL", (long long)i);
     }
-    size_t b = stream_ws(&maps[i], T);
+    gsi_path p;
+    if ((s = resolve_path(&maps[i], T, GSI_PATH_AUTO, &p)) != GSI_OK) return s;
+    size_t b = path_ws(&maps[i], T, p);
     if (b > need) need = b;
   }
   if (T == 0) return ok();
   if ((s = check_workspace(workspace, ws_bytes, need)) != GSI_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   for (int64_t i = 0; i < n_maps; ++i) {
-    s = run_stream(&maps[i], X[i], T, eps, Y[i], flags[i], nullptr, nullptr, workspace, st, true);
+    gsi_path p;
+    resolve_path(&maps[i], T, GSI_PATH_AUTO, &p);
+    if (p == GSI_PATH_TENSOR)
+      s = run_tensor(&maps[i], X[i], T, eps, Y[i], flags[i], nullptr, workspace, st);
+    else
+      s = run_stream(&maps[i], X[i], T, eps, Y[i], flags[i], nullptr, nullptr, workspace, st, true);
     if (s != GSI_OK) return fail(s, "map %lld: %s", (long long)i, g_err.c_str());
   }
   return ok();

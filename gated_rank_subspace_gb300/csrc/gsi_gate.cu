@@ -77,6 +77,15 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kGateThre
 
   // ---- prologue: read-only weights only (may overlap the previous kernel)
   pdl_launch_dependents();
+  if (a.gram_share && tid == 32) {
+    // The finalising cluster reads the whole Gram: stage it in L2 now.
+    const uint64_t off = uint64_t(blockIdx.x) * a.gram_share;
+    const uint64_t total = uint64_t(k) * k * 4;
+    if (off < total) {
+      const uint64_t rem = total - off;
+      prefetch_l2(reinterpret_cast<const char*>(a.gram) + off, uint32_t(rem < a.gram_share ? rem : a.gram_share));
+    }
+  }
   if (a.pf_share && tid == 0) {
     const uint64_t off = uint64_t(blockIdx.x) * a.pf_share;
     if (off < a.pf_total) {
@@ -188,31 +197,59 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kGateThre
   if (!s_last) return;
   __threadfence();
 
-  float* gsl = red;                     // [TC][ks]   this CTA's slice of g
-  float* gfull = gsl + TC * ks;         // [TC][k]    the whole g
-  float* qw = gfull + TC * k;           // [8][TC]    per-warp g^T Gram g partials
-  float* nw = qw + 8 * TC;              // [8][TC]    per-warp ||g||^2 partials
-  float* qc = nw + 8 * TC;              // [TC]       per-CTA partials
-  float* nc = qc + TC;                  // [TC]
-  float* nx2 = nc + TC;                 // [TC]       ||x||^2 (rank 0)
+  float* gsl = red;                            // [TC][ks]   this CTA's slice of g
+  float* gfull = gsl + ((TC * ks + 3) & ~3);   // [TC][k]    the whole g (16-byte aligned)
+  float* qw = gfull + TC * k;                  // [8][TC]    per-warp g^T Gram g partials
+  float* nw = qw + 8 * TC;                     // [8][TC]    per-warp ||g||^2 partials
+  float* qc = nw + 8 * TC;                     // [TC]       per-CTA partials
+  float* nc = qc + TC;                         // [TC]
+  float* nx2 = nc + TC;                        // [TC]       ||x||^2 (rank 0)
   const int nclu = a.n_clusters;
+  const int64_t cstride = int64_t(T) * k;      // distance between clusters' partials
+
+  // Sums over the clusters' partials are split over groups of `grp` adjacent
+  // lanes (lane g of a group adds clusters g, g + grp, ...), so every thread
+  // has its loads in flight together; the group then combines in a fixed
+  // butterfly order (bitwise reproducible).
+  const int ne = TC * ks;
+  const int grp = kGateThreads / ne >= 8 ? 8 : kGateThreads / ne >= 4 ? 4 : kGateThreads / ne >= 2 ? 2 : 1;
 
   for (int t0 = 0; t0 < T; t0 += TC) {
     const int tc = min(TC, T - t0);
-    for (int e = tid; e < TC * ks; e += kGateThreads) {
+    for (int base = 0; base < ne * grp; base += kGateThreads) {
+      const int id = base + tid;
+      const int e = id / grp, g = id - (id / grp) * grp;
       const int t = e / ks, col = c0 + (e - (e / ks) * ks);
+      const bool valid = e < ne && t < tc && col < c1;
       float s = 0.f;
-      if (t < tc && col < c1) {
-        for (int cl = 0; cl < nclu; ++cl) s += __ldcg(&a.part_g[(int64_t(cl) * T + t0 + t) * k + col]);
-        a.G[int64_t(t0 + t) * k + col] = s;
+      if (valid) {
+        const float* src = a.part_g + int64_t(t0 + t) * k + col;
+        int cl = g;
+        for (; cl + 3 * grp < nclu; cl += 4 * grp) {
+          const float v0 = __ldcg(src + cl * cstride), v1 = __ldcg(src + (cl + grp) * cstride);
+          const float v2 = __ldcg(src + (cl + 2 * grp) * cstride), v3 = __ldcg(src + (cl + 3 * grp) * cstride);
+          s += v0;
+          s += v1;
+          s += v2;
+          s += v3;
+        }
+        for (; cl < nclu; cl += grp) s += __ldcg(src + cl * cstride);
       }
-      gsl[e] = s;
+      for (int o = 1; o < grp; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+      if (g == 0 && e < ne) {
+        if (valid) a.G[int64_t(t0 + t) * k + col] = s;
+        gsl[e] = valid ? s : 0.f;
+      }
     }
-    if (rank == 0 && tid < TC) {
+    if (rank == 0 && warp == 0) {
+      // ||x||^2: token (lane / 4) summed over clusters by 4 lanes
+      const int t = lane >> 2, g = lane & 3;
       float s = 0.f;
-      if (tid < tc)
-        for (int cl = 0; cl < nclu; ++cl) s += __ldcg(&a.part_x[int64_t(cl) * T + t0 + tid]);
-      nx2[tid] = s;
+      if (t < tc)
+        for (int cl = g; cl < nclu; cl += 4) s += __ldcg(&a.part_x[int64_t(cl) * T + t0 + t]);
+      s += __shfl_xor_sync(0xffffffffu, s, 1);
+      s += __shfl_xor_sync(0xffffffffu, s, 2);
+      if (g == 0 && t < TC) nx2[t] = s;
     }
     cluster.sync();
     for (int e = tid; e < TC * k; e += kGateThreads) {
@@ -221,20 +258,41 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kGateThre
       gfull[e] = cluster.map_shared_rank(gsl, q)[t * ks + (col - q * ks)];
     }
     __syncthreads();
-    // g^T Gram g and ||g||^2 over this CTA's Gram rows [c0, c1)
+    // g^T Gram g and ||g||^2 over this CTA's Gram rows [c0, c1): the slice is
+    // read as 16-byte vectors, eight per thread in flight at once.
     float qa[TC], na[TC];
 #pragma unroll
     for (int t = 0; t < TC; ++t) qa[t] = na[t] = 0.f;
-    for (int i = c0 + warp; i < c1; i += kGateThreads / 32) {
-      if (lane == 0) {
+    for (int i = c0 + tid; i < c1; i += kGateThreads) {
 #pragma unroll
-        for (int t = 0; t < TC; ++t) na[t] = fmaf(gfull[t * k + i], gfull[t * k + i], na[t]);
-      }
-      if (a.gram) {
-        for (int j = lane; j < k; j += 32) {
-          const float gij = __ldg(&a.gram[int64_t(i) * k + j]);
+      for (int t = 0; t < TC; ++t) na[t] = fmaf(gfull[t * k + i], gfull[t * k + i], na[t]);
+    }
+    if (a.gram && c1 > c0) {
+      const int k4 = k >> 2;
+      const int nvec = (c1 - c0) * k4;
+      for (int v0 = 0; v0 < nvec; v0 += 8 * kGateThreads) {
+        float4 gv[8];
 #pragma unroll
-          for (int t = 0; t < TC; ++t) qa[t] = fmaf(gfull[t * k + i] * gij, gfull[t * k + j], qa[t]);
+        for (int u = 0; u < 8; ++u) {
+          const int v = v0 + u * kGateThreads + tid;
+          gv[u] = v < nvec ? __ldg(reinterpret_cast<const float4*>(a.gram + int64_t(c0 + v / k4) * k) + (v % k4))
+                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int v = v0 + u * kGateThreads + tid;
+          if (v < nvec) {
+            const int i = c0 + v / k4, j = 4 * (v % k4);
+#pragma unroll
+            for (int t = 0; t < TC; ++t) {
+              const float4 gj = *reinterpret_cast<const float4*>(gfull + t * k + j);
+              float h = gv[u].x * gj.x;
+              h = fmaf(gv[u].y, gj.y, h);
+              h = fmaf(gv[u].z, gj.z, h);
+              h = fmaf(gv[u].w, gj.w, h);
+              qa[t] = fmaf(gfull[t * k + i], h, qa[t]);
+            }
+          }
         }
       }
     }

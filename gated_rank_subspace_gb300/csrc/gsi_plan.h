@@ -50,7 +50,7 @@ inline GatePlan plan_gate(int64_t d, int64_t k, int elem_bytes, int64_t T) {
   // finalizer (aliases red): gsl[tc][ks] + gfull[tc][k] + q/ng partials
   size_t main_b = size_t(p.tc) * p.rs * 4 + size_t(p.nrg) * p.tc * k * 4 +
                   size_t(p.tc) * k * 4 + size_t(p.tc) * 4;
-  size_t fin_b = size_t(p.tc) * p.rs * 4 + size_t(p.tc) * p.ks * 4 + size_t(p.tc) * k * 4 +
+  size_t fin_b = size_t(p.tc) * p.rs * 4 + size_t(p.tc) * p.ks * 4 + 16 + size_t(p.tc) * k * 4 +
                  size_t(p.tc) * k * 4 + size_t(p.tc) * 4 + 2 * 8 * size_t(p.tc) * 4 + 64;
   p.smem = (main_b > fin_b ? main_b : fin_b) + 64;
   return p;
@@ -73,6 +73,28 @@ inline StreamLayout layout_stream(int64_t d, int64_t k, int elem_bytes, int64_t 
   L.total = off;
   return L;
 }
+
+// Workspace layout of one tensor-core-path call.
+struct TensorLayout {
+  size_t ctrl, vt, g, gbf, gfast, xslow, idx, total;
+};
+
+inline TensorLayout layout_tensor(int64_t d, int64_t k, int64_t T) {
+  TensorLayout L{};
+  size_t off = 0;
+  L.ctrl = off;   off += 256;
+  L.vt = off;     off += align256(size_t(k) * d * 2);
+  L.g = off;      off += align256(size_t(T) * k * 4);
+  L.gbf = off;    off += align256(size_t(T) * k * 2);
+  L.gfast = off;  off += align256(size_t(T) * k * 2);
+  L.xslow = off;  off += align256(size_t(T) * d * 2);
+  L.idx = off;    off += align256(size_t(2) * T * 4);
+  L.total = off;
+  return L;
+}
+
+// Token count from which GSI_PATH_AUTO uses the tensor cores for bf16 maps.
+constexpr int64_t kTensorMinT = 128;
 
 // Apply kernel geometry: fast units are `rows_fast` rows of M, slow units
 // `rows_slow` rows of W, each handled by one warp.

@@ -1,0 +1,567 @@
+// Tensor-core path for prefill-sized token counts (sm_103a tcgen05 + TMEM + TMA).
+//
+// "Gated Subspace Inference for Transformer Acceleration", §2.1-§2.2 at large
+// T: the projections G = X V_k, the fast outputs Y_fast = G_fast M^T and the
+// slow outputs Y_slow = X_slow W^T are dense contractions, so they run on the
+// 5th-generation tensor cores:
+//
+//   1. transpose V_k (d x k) into V_k^T (k x d) so both operands of the
+//      projection are K-major;
+//   2. G = X V_k                       (tcgen05, fp32 accumulate in TMEM);
+//   3. per token ||x||^2, g^T Gram g, rho, flag, and g rounded to bf16
+//      (CUDA cores, float32 -- the gate needs more precision than bf16);
+//   4. compaction and gathers: X_slow (slow tokens' rows of X) and G_fast;
+//   5. Y[idx_fast] = G_fast M^T and Y[idx_slow] = X_slow W^T
+//      (tcgen05; the epilogue scatters rows to their token positions).
+//
+// The GEMM kernel: one 128 x BN output tile per CTA, 128 threads.  Thread 0
+// issues TMA tile loads (128-byte swizzle) into a STAGES-deep shared-memory
+// ring guarded by mbarriers; thread 32 issues tcgen05.mma (M = 128, N = BN,
+// K = 16 per instruction) into a TMEM accumulator and commits each stage back
+// to the producer; after the last k-block all four warps read their 32 TMEM
+// lanes with tcgen05.ld and write fp32 rows.  Every wait is bounded (about
+// two seconds of clock): on expiry the CTA records an error in the workspace
+// word, waits (bounded) for its own in-flight copies, frees its TMEM and
+// returns.  The valid row count can come from device memory (the fast / slow
+// counts), so the grid is sized for T and surplus tiles exit at once.
+
+#include <cuda.h>
+
+#include "gsi_common.cuh"
+#include "gsi_kernels.h"
+#include "gsi_plan.h"
+
+namespace gsi {
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
+
+// Bounded wait on an mbarrier phase; false (and the error word set) on expiry.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t* err) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitCycles) {
+      atomicOr(err, kErrTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+      ::"r"(smem_u32(dst)), "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(slot)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16 (bf16 inputs, fp32 accumulate).
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on `bar` once every tcgen05.mma issued so far by this thread is done.
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor: K-major operand tile written by TMA with
+// 128-byte swizzle (rows of 64 bf16, 8-row / 1024-byte swizzle atoms).
+__device__ __forceinline__ uint64_t smem_desc_sw128(const void* tile) {
+  uint64_t d = 0;
+  d |= uint64_t((smem_u32(tile) & 0x3FFFFu) >> 4);  // start address
+  d |= uint64_t(1) << 16;                           // leading byte offset (unused for SW128 K-major)
+  d |= uint64_t(1024 >> 4) << 32;                   // stride byte offset: next 8-row atom
+  d |= uint64_t(1) << 46;                           // descriptor version
+  d |= uint64_t(2) << 61;                           // 128-byte swizzle
+  return d;
+}
+
+// Instruction descriptor: kind::f16, A = B = bf16, D = f32, both K-major.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
+}
+
+// ------------------------------------------------------------------ GEMM kernel
+struct TcArgs {
+  int rows;               // valid rows of A (used when rows_dev is null)
+  const int32_t* rows_dev;  // device count of valid rows, or null
+  int N, K;
+  float* C;
+  int64_t ldc;
+  const int32_t* row_map;  // output row of A-row m is row_map[m] (null: m)
+  uint32_t* err;
+};
+
+constexpr int kBM = 128, kBK = 64;
+
+template <int BN>
+struct TcCfg {
+  static constexpr int STAGES = BN >= 256 ? 4 : 6;
+  static constexpr uint32_t A_BYTES = kBM * kBK * 2;
+  static constexpr uint32_t B_BYTES = BN * kBK * 2;
+  static constexpr size_t SMEM = 1024 + size_t(STAGES) * (A_BYTES + B_BYTES) + 256;
+};
+
+template <int BN>
+__global__ void __launch_bounds__(128, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb, TcArgs a) {
+  using C = TcCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = base;
+  uint8_t* sB = base + C::STAGES * C::A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* done = empty + C::STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m_tile = blockIdx.x, n_tile = blockIdx.y;
+  pdl_wait();
+  const int rows = a.rows_dev ? __ldcg(a.rows_dev) : a.rows;
+  if (m_tile * kBM >= rows) return;  // whole CTA, before any barrier or TMEM
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, BN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int nk = (a.K + kBK - 1) / kBK;
+  __shared__ int s_issued;  // k-blocks whose TMA loads were issued
+
+  if (threadIdx.x == 0) {
+    int kb = 0;
+    for (; kb < nk; ++kb) {
+      const int s = kb % C::STAGES;
+      const uint32_t ph = (kb / C::STAGES) & 1;
+      if (kb >= C::STAGES && !mbar_wait(&empty[s], ph ^ 1, a.err)) break;
+      mbar_expect_tx(&full[s], C::A_BYTES + C::B_BYTES);
+      tma_load_2d(sA + s * C::A_BYTES, &ta, &full[s], kb * kBK, m_tile * kBM);
+      tma_load_2d(sB + s * C::B_BYTES, &tb, &full[s], kb * kBK, n_tile * BN);
+    }
+    s_issued = kb;
+  } else if (threadIdx.x == 32) {
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, BN);
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % C::STAGES;
+      const uint32_t ph = (kb / C::STAGES) & 1;
+      if (!mbar_wait(&full[s], ph, a.err)) break;
+      tc_fence_after();
+      const uint64_t ad = smem_desc_sw128(sA + s * C::A_BYTES);
+      const uint64_t bd = smem_desc_sw128(sB + s * C::B_BYTES);
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk)  // advance 16 bf16 = 32 bytes inside the swizzle row
+        umma_bf16(tmem, ad + uint64_t(kk * 2), bd + uint64_t(kk * 2), idesc, (kb | kk) != 0);
+      umma_commit(&empty[s]);
+    }
+    umma_commit(done);  // fires once every MMA issued above has completed
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(done, 0, a.err);
+  tc_fence_after();
+  // tcgen05.ld is warp-collective: decide per warp, never per thread.
+  const bool go = __all_sync(0xffffffffu, ok && *reinterpret_cast<volatile uint32_t*>(a.err) == 0);
+  if (go) {
+    const int r = m_tile * kBM + warp * 32 + lane;
+    const bool live = r < rows;
+    const int64_t orow = live ? (a.row_map ? int64_t(__ldcg(&a.row_map[r])) : int64_t(r)) : 0;
+    float* crow = a.C + orow * a.ldc;
+    const bool vec = (a.ldc % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.C) & 15) == 0);
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 16) {
+      float v[16];
+      tmem_ld16(tmem + (uint32_t(warp * 32) << 16) + uint32_t(c), v);
+      const int col0 = n_tile * BN + c;
+      if (live) {
+        if (vec && col0 + 16 <= a.N) {
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            *reinterpret_cast<float4*>(crow + col0 + 4 * q) =
+                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        } else {
+          for (int q = 0; q < 16; ++q)
+            if (col0 + q < a.N) crow[col0 + q] = v[q];
+        }
+      }
+    }
+  }
+  // Bounded drain of this CTA's own copies before its shared memory goes away
+  // (only reached with copies in flight after a timeout).
+  if (threadIdx.x == 0 && !ok) {
+    for (int kb = 0; kb < s_issued; ++kb)
+      mbar_wait(&full[kb % C::STAGES], (kb / C::STAGES) & 1, a.err);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, BN);
+}
+
+// ------------------------------------------------------------------ helpers on CUDA cores
+// V_k (d x k) -> V_k^T (k x d), bf16, 32 x 32 tiles through shared memory.
+__global__ void transpose_bf16_kernel(const uint16_t* __restrict__ V, uint16_t* __restrict__ Vt, int d, int k) {
+  __shared__ uint16_t tile[32][33];
+  const int i0 = blockIdx.y * 32, j0 = blockIdx.x * 32;
+  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+    const int i = i0 + r, j = j0 + threadIdx.x;
+    tile[r][threadIdx.x] = (i < d && j < k) ? V[int64_t(i) * k + j] : uint16_t(0);
+  }
+  __syncthreads();
+  for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+    const int j = j0 + r, i = i0 + threadIdx.x;
+    if (j < k && i < d) Vt[int64_t(j) * d + i] = tile[threadIdx.x][r];
+  }
+}
+
+// Per token: ||x||^2, g^T Gram g, rho, flag, and g rounded to bf16.
+// One CTA per 8 tokens; thread j owns column j of g.
+constexpr int kFinTok = 8;
+
+__global__ void __launch_bounds__(256) tc_finalize_kernel(const uint16_t* __restrict__ X, const float* __restrict__ G,
+                                                          const float* __restrict__ gram, int64_t d, int k, int T,
+                                                          float eps, float* __restrict__ rho_out,
+                                                          uint8_t* __restrict__ flags, uint16_t* __restrict__ Gbf) {
+  extern __shared__ float fsm[];
+  float* gs = fsm;                       // [kFinTok][k]
+  float* red = gs + kFinTok * k;         // [8 warps][kFinTok][2]
+  float* x2s = red + 8 * kFinTok * 2;    // [kFinTok]
+  const int t0 = blockIdx.x * kFinTok;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();
+  for (int e = tid; e < kFinTok * k; e += 256) {
+    const int t = e / k, j = e - (e / k) * k;
+    const float g = (t0 + t < T) ? __ldcg(&G[int64_t(t0 + t) * k + j]) : 0.f;
+    gs[e] = g;
+    if (t0 + t < T) {
+      __nv_bfloat16 b = __float2bfloat16_rn(g);
+      Gbf[int64_t(t0 + t) * k + j] = *reinterpret_cast<uint16_t*>(&b);
+    }
+  }
+  __syncthreads();
+  float q[kFinTok], n[kFinTok];
+#pragma unroll
+  for (int t = 0; t < kFinTok; ++t) q[t] = n[t] = 0.f;
+  for (int j = tid; j < k; j += 256) {
+    float h[kFinTok];
+#pragma unroll
+    for (int t = 0; t < kFinTok; ++t) h[t] = 0.f;
+    if (gram) {
+      for (int i = 0; i < k; ++i) {
+        const float gij = __ldg(&gram[int64_t(i) * k + j]);
+#pragma unroll
+        for (int t = 0; t < kFinTok; ++t) h[t] = fmaf(gs[t * k + i], gij, h[t]);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kFinTok; ++t) {
+      const float gj = gs[t * k + j];
+      n[t] = fmaf(gj, gj, n[t]);
+      q[t] = gram ? fmaf(gj, h[t], q[t]) : n[t];
+    }
+  }
+  // ||x||^2: warp w takes token w, lanes stride over 16-byte vectors
+  if (warp < kFinTok) {
+    float s = 0.f;
+    if (t0 + warp < T) {
+      const uint4* xr = reinterpret_cast<const uint4*>(X + int64_t(t0 + warp) * d);
+      for (int64_t v = lane; v < d / 8; v += 32) {
+        float f[8];
+        BF16::unpack(ld_cg_v4(xr + v), f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) s = fmaf(f[e], f[e], s);
+      }
+    }
+    s = warp_sum(s);
+    if (lane == 0) x2s[warp] = s;
+  }
+#pragma unroll
+  for (int t = 0; t < kFinTok; ++t) {
+    const float a = warp_sum(q[t]), b = warp_sum(n[t]);
+    if (lane == 0) {
+      red[(warp * kFinTok + t) * 2 + 0] = a;
+      red[(warp * kFinTok + t) * 2 + 1] = b;
+    }
+  }
+  __syncthreads();
+  if (tid < kFinTok && t0 + tid < T) {
+    float qq = 0.f, nn = 0.f;
+    for (int w = 0; w < 8; ++w) {
+      qq += red[(w * kFinTok + tid) * 2 + 0];
+      nn += red[(w * kFinTok + tid) * 2 + 1];
+    }
+    const float x2 = x2s[tid];
+    float rr = x2 - 2.f * nn + qq;
+    rr = rr < 0.f ? 0.f : rr;
+    const float rho = x2 == 0.f ? 0.f : sqrtf(rr / x2);
+    if (rho_out) rho_out[t0 + tid] = rho;
+    flags[t0 + tid] = (rho < eps) ? uint8_t(0) : uint8_t(1);
+  }
+}
+
+// Gather rows: dst[j] = src[idx[j]] for j < count (16-byte vectors).
+__global__ void gather_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, const int32_t* idx,
+                                   const int32_t* count, int64_t row_vecs, int T) {
+  pdl_wait();
+  const int n = __ldcg(count);
+  const int64_t total = int64_t(n) * row_vecs;
+  for (int64_t e = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; e < total; e += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t j = e / row_vecs, v = e - j * row_vecs;
+    const int32_t t = __ldcg(&idx[j]);
+    dst[e] = ld_cg_v4(src + int64_t(t) * row_vecs + v);
+  }
+  (void)T;
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major (rows x cols) matrix, box of
+// box_rows x 64 columns, 128-byte swizzle, zero fill outside.
+static cudaError_t make_map_2d(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return cudaErrorNotSupported;
+  cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+  cuuint64_t strides[1] = {cuuint64_t(cols) * 2};
+  cuuint32_t box[2] = {cuuint32_t(kBK), cuuint32_t(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int BN>
+static cudaError_t launch_tc_gemm_t(const void* A, int64_t a_rows, const void* B, int64_t b_rows, int K,
+                                    const TcArgs& args, cudaStream_t s) {
+  CUtensorMap ta, tb;
+  cudaError_t e = make_map_2d(&ta, A, a_rows, K, kBM);
+  if (e != cudaSuccess) return e;
+  if ((e = make_map_2d(&tb, B, b_rows, K, BN)) != cudaSuccess) return e;
+  auto kern = tc_gemm_kernel<BN>;
+  static bool attr = false;
+  if (!attr) {
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(TcCfg<BN>::SMEM))) !=
+        cudaSuccess)
+      return e;
+    attr = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(cdiv(a_rows, kBM)), unsigned(cdiv(b_rows, BN)));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = TcCfg<BN>::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, args);
+}
+
+// C[row_map(m)][n] = sum_k A[m][k] B[n][k]; A: a_rows x K, B: b_rows x K, bf16.
+cudaError_t launch_tc_gemm(const void* A, int64_t a_rows, const void* B, int64_t b_rows, int K, int bn,
+                           const TcArgs& args, cudaStream_t s) {
+  switch (bn) {
+    case 64: return launch_tc_gemm_t<64>(A, a_rows, B, b_rows, K, args, s);
+    case 128: return launch_tc_gemm_t<128>(A, a_rows, B, b_rows, K, args, s);
+    default: return launch_tc_gemm_t<256>(A, a_rows, B, b_rows, K, args, s);
+  }
+}
+
+static cudaError_t launch_pdl(const void* kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelExC(&cfg, kern, args);
+}
+
+cudaError_t launch_tensor_path(const TensorArgs& t, cudaStream_t s) {
+  cudaError_t e;
+  const int64_t d = t.d, k = t.k, T = t.T, d_out = t.d_out;
+  // 1. V^T
+  {
+    dim3 grid(unsigned(cdiv(k, 32)), unsigned(cdiv(d, 32)));
+    transpose_bf16_kernel<<<grid, dim3(32, 8), 0, s>>>(static_cast<const uint16_t*>(t.V), t.Vt, int(d), int(k));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  // 2. G = X V
+  TcArgs g{};
+  g.rows = int(T);
+  g.N = int(k);
+  g.K = int(d);
+  g.C = t.G;
+  g.ldc = k;
+  g.err = t.err;
+  if ((e = launch_tc_gemm(t.X, T, t.Vt, k, int(d), 64, g, s)) != cudaSuccess) return e;
+  // 3. rho, flags, bf16 g
+  {
+    const void* X = t.X;
+    const float* G = t.G;
+    const float* gram = t.gram;
+    int64_t dd = d;
+    int kk = int(k), TT = int(T);
+    float eps = t.eps;
+    float* rho = t.rho;
+    uint8_t* flags = t.flags;
+    uint16_t* Gbf = t.Gbf;
+    void* args[] = {&X, &G, &gram, &dd, &kk, &TT, &eps, &rho, &flags, &Gbf};
+    const size_t smem = size_t(kFinTok) * k * 4 + 8 * kFinTok * 2 * 4 + kFinTok * 4;
+    if (smem > 48 * 1024) {
+      if ((e = cudaFuncSetAttribute(tc_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem))) !=
+          cudaSuccess)
+        return e;
+    }
+    if ((e = launch_pdl(reinterpret_cast<const void*>(tc_finalize_kernel), dim3(unsigned(cdiv(T, kFinTok))),
+                        dim3(256), smem, s, args)) != cudaSuccess)
+      return e;
+  }
+  // 4. compaction and gathers
+  if ((e = launch_compact(t.flags, int(T), t.idx, t.counts, s)) != cudaSuccess) return e;
+  {
+    const uint4* src = static_cast<const uint4*>(t.X);
+    uint4* dst = reinterpret_cast<uint4*>(t.Xslow);
+    const int32_t* idx = t.idx + T;
+    const int32_t* cnt = t.counts + 1;
+    int64_t rv = d * 2 / 16;
+    int TT = int(T);
+    void* args[] = {&src, &dst, &idx, &cnt, &rv, &TT};
+    if ((e = launch_pdl(reinterpret_cast<const void*>(gather_rows_kernel), dim3(296), dim3(256), 0, s, args)) !=
+        cudaSuccess)
+      return e;
+  }
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(t.Gbf);
+    uint4* dst = reinterpret_cast<uint4*>(t.Gfast);
+    const int32_t* idx = t.idx;
+    const int32_t* cnt = t.counts;
+    int64_t rv = k * 2 / 16;
+    int TT = int(T);
+    void* args[] = {&src, &dst, &idx, &cnt, &rv, &TT};
+    if ((e = launch_pdl(reinterpret_cast<const void*>(gather_rows_kernel), dim3(148), dim3(256), 0, s, args)) !=
+        cudaSuccess)
+      return e;
+  }
+  // 5. Y_fast = G_fast M^T, Y_slow = X_slow W^T (rows scattered to token positions)
+  TcArgs f{};
+  f.rows_dev = t.counts;
+  f.N = int(d_out);
+  f.K = int(k);
+  f.C = t.Y;
+  f.ldc = d_out;
+  f.row_map = t.idx;
+  f.err = t.err;
+  if ((e = launch_tc_gemm(t.Gfast, T, t.M, d_out, int(k), 128, f, s)) != cudaSuccess) return e;
+  TcArgs sl{};
+  sl.rows_dev = t.counts + 1;
+  sl.N = int(d_out);
+  sl.K = int(d);
+  sl.C = t.Y;
+  sl.ldc = d_out;
+  sl.row_map = t.idx + T;
+  sl.err = t.err;
+  return launch_tc_gemm(t.Xslow, T, t.W, d_out, int(d), 256, sl, s);
+}
+
+}  // namespace gsi

@@ -117,7 +117,8 @@ gsi_status gsi_gate(const gsi_map_desc* map, const void* X, int64_t T, float eps
 /* §2.2 per-token gate, compaction step: stable (ascending token index) lists
  * of fast and slow tokens.  idx (device, 2*T int32) receives the fast list in
  * idx[0 .. n_fast) and the slow list in idx[T .. T + n_slow); counts (device,
- * 2 int32) receives {n_fast, n_slow}. */
+ * 2 int32) receives {n_fast, n_slow}.  With T == 0, flags and idx may be NULL
+ * and counts receives {0, 0}. */
 gsi_status gsi_compact(const uint8_t* flags, int64_t T, int32_t* idx, int32_t* counts,
                        void* stream);
 

@@ -5,8 +5,13 @@ Tolerances (from the arithmetic the kernels do):
   * flags: bit-exact for every token whose oracle rho lies outside
     [eps - 1e-3, eps + 1e-3]; inside that band either decision is correct and
     the output must match the oracle's candidate for the decision taken;
-  * rho: |rho_gpu - rho_oracle| <= 2e-4 (float32 accumulation of the exact
-    Gram form; the band is 5x wider);
+  * rho: |rho_gpu^2 - rho_oracle^2| <= 2e-5.  The library forms
+    rho^2 = (||x||^2 - 2||g||^2 + g^T Gram g) / ||x||^2 from three float32
+    sums of magnitude ~||x||^2 over up to 16384 terms, so the absolute error
+    of rho^2 is a few 1e-6 (observed 7.5e-6 at d = 16384); near eps = 0.05
+    this bounds |rho error| by 2e-5 / (2 * 0.049) ~= 2e-4, five times inside
+    the +-1e-3 band, while at small rho the error in rho itself grows as
+    1/rho (harmlessly: such tokens are far from the gate);
   * Y: relative L2 (||dY||_F / ||Y_ref||_F) <= 1e-5 for float32 maps and
     <= 2e-2 for bf16 maps with float32 accumulation, against the oracle run
     on the same bf16-rounded W, V, X and on the M bytes the library built.
@@ -20,7 +25,7 @@ from oracle import gsi_oracle as orc
 from workloads import synth
 
 BAND = 1e-3
-RHO_TOL = 2e-4
+RHO2_TOL = 2e-5
 TOL = {torch.float32: 1e-5, torch.bfloat16: 2e-2}
 
 
@@ -47,8 +52,8 @@ def compare(m_in, M_dev, Y, flags, rho, X=None, eps=None, tol=None):
     if rho is not None:
         r = rho.cpu().numpy().astype(np.float64)
         fin = np.isfinite(ro)
-        err = np.max(np.abs(r[fin] - ro[fin])) if fin.any() else 0.0
-        assert err <= RHO_TOL, f"rho error {err} > {RHO_TOL}"
+        err = np.max(np.abs(r[fin] ** 2 - ro[fin] ** 2)) if fin.any() else 0.0
+        assert err <= RHO2_TOL, f"rho^2 error {err} > {RHO2_TOL}"
         assert np.array_equal(np.isnan(r), np.isnan(ro)), "NaN rho mismatch"
     ref = np.empty((len(f), Wn.shape[0]))
     if (~f).any():
@@ -63,5 +68,11 @@ def compare(m_in, M_dev, Y, flags, rho, X=None, eps=None, tol=None):
     tol = TOL[m_in.W.dtype] if tol is None else tol
     assert rel <= tol, f"relative L2 error {rel} > {tol}"
     if (~fin).any():
-        assert np.all(np.isnan(y[~fin])), "non-finite tokens must give NaN outputs"
+        # non-finite tokens: the library must reproduce the oracle's pattern
+        # (NaN where the exact path gives NaN, the same infinity where it
+        # gives +-inf)
+        yr, rr = y[~fin], ref[~fin]
+        assert np.array_equal(np.isnan(yr), np.isnan(rr)), "NaN pattern of non-finite tokens"
+        inf = np.isinf(rr)
+        assert np.array_equal(yr[inf], rr[inf]), "infinities of non-finite tokens"
     return dict(rel=rel, n_slow=int(f.sum()), n_band=int(band.sum()), T=len(f))
