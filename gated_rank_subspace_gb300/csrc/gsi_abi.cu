@@ -28,6 +28,12 @@ static gsi_status fail(gsi_status s, const char* fmt, ...) {
   return s;
 }
 
+// Records a message for gsi_last_error() from another translation unit.
+gsi_status record_error(gsi_status s, const char* msg) {
+  g_err = msg;
+  return s;
+}
+
 static gsi_status ok() {
   g_err.clear();
   return GSI_OK;

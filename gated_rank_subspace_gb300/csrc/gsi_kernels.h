@@ -72,6 +72,9 @@ struct TensorArgs {
 
 cudaError_t launch_tensor_path(const TensorArgs& t, cudaStream_t s);
 
+// Sets the calling thread's gsi_last_error() message and returns s.
+gsi_status record_error(gsi_status s, const char* msg);
+
 cudaError_t launch_gate(const GateArgs& a, const GatePlan& p, gsi_dtype dt, cudaStream_t s,
                         bool pdl);
 cudaError_t launch_compact(const uint8_t* flags, int T, int32_t* idx, int32_t* counts,

@@ -163,6 +163,25 @@ gsi_status gsi_stack(const gsi_map_desc* maps, int64_t n_maps, const void* const
                      int64_t T, float eps, float* const* Y, uint8_t* const* flags,
                      void* workspace, size_t ws_bytes, void* stream);
 
+/* No counterpart in the paper: a library convenience.  gsi_linear for
+ * callers that cannot allocate device memory (code where cudaMalloc is
+ * forbidden or unavailable, such as an allocator hook, a plug-in inside a
+ * host program that owns all device memory, or a loop that must never
+ * allocate).  Same arguments and results as gsi_linear on the streaming
+ * kernels, minus the workspace: the scratch is a built-in device array of
+ * gsi_linear_noalloc_max_bytes() bytes (4 MiB) that every GPU loading the
+ * library holds until the process exits.  Calls needing more scratch than
+ * that (large T) return GSI_ERR_WORKSPACE.  The first call on each device
+ * looks up the array's device address (cudaGetSymbolAddress), so make that
+ * first call before any stream capture.  Every call shares the one array:
+ * calls whose executions overlap on the GPU (different streams, or host
+ * threads) race and must be serialised by the caller.  Allocates nothing. */
+gsi_status gsi_linear_noalloc(const gsi_map_desc* map, const void* X, int64_t T, float eps,
+                              float* Y, uint8_t* flags, float* rho, void* stream);
+
+/* Size in bytes of the built-in scratch array used by gsi_linear_noalloc. */
+size_t gsi_linear_noalloc_max_bytes(void);
+
 /* Message for the calling thread's last non-OK status ("" if none). */
 const char* gsi_last_error(void);
 
