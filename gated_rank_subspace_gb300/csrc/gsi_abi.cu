@@ -112,18 +112,6 @@ static gsi_status check_workspace(const void* ws, size_t have, size_t need) {
   return GSI_OK;
 }
 
-// SM count of the current device, queried once per device (so that nothing
-// but kernel launches happens while a caller captures a CUDA graph).
-static int sm_count() {
-  static std::atomic<int> cache[64];
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
-  if (dev < 64 && (n = cache[dev].load()) > 0) return n;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  if (dev < 64) cache[dev].store(n);
-  return n;
-}
-
 // Resolve the path for a call: the tensor cores for bf16 maps at
 // prefill-sized T, the streaming kernels otherwise.
 static gsi_status resolve_path(const gsi_map_desc* m, int64_t T, gsi_path path, gsi_path* out) {
@@ -153,57 +141,116 @@ static size_t stream_ws(const gsi_map_desc* m, int64_t T) {
   return layout_stream(m->d, m->k, elem_bytes(m->dtype), T).total;
 }
 
-// Enqueue the apply kernel for one map, reading the counts and index lists
-// the gate kernel left in the workspace.  All arguments validated.
-static gsi_status run_apply(const gsi_map_desc* m, const void* X, const float* G, int64_t T, float* Y,
-                            void* ws, cudaStream_t st) {
-  const int es = elem_bytes(m->dtype);
-  const StreamLayout L = layout_stream(m->d, m->k, es, T);
-  char* base = static_cast<char*>(ws);
-  if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
-  const ApplyPlan ap = plan_apply(m->d, m->d_out, m->k, es);
-  ApplyArgs aa{};
-  aa.W = m->W;
-  aa.M = m->M;
-  aa.X = X;
-  aa.G = G;
-  aa.Y = Y;
-  aa.idx = reinterpret_cast<const int32_t*>(base + L.idx);
-  aa.ctrl = reinterpret_cast<const Ctrl*>(base + L.ctrl);
-  aa.d = m->d;
-  aa.d_out = m->d_out;
-  aa.k = int(m->k);
-  aa.T = int(T);
-  aa.rows_slow = ap.rows_slow;
-  aa.fast_units = ap.fast_units;
-  aa.slow_units = ap.slow_units;
-  aa.x_stage_max = ap.x_stage_tokens_max;
-  aa.g_stage_max = ap.g_stage_tokens_max;
-  const int nsm = sm_count();
-  if (nsm <= 0) return fail(GSI_ERR_CUDA, "cannot query the device's SM count");
-  return cuda_check(launch_apply(aa, ap, m->dtype, nsm, st, true), "apply kernel launch");
+// Device facts the decide-and-apply plan needs, queried once per device.
+struct DeviceFacts {
+  int nsm = 0;
+  int smem_optin = 0;
+  int clusters[2] = {0, 0};  // co-resident decide-and-apply clusters per dtype
+};
+
+static gsi_status device_facts(gsi_dtype dt, size_t smem_budget, DeviceFacts** out) {
+  static DeviceFacts facts[64];
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) return cuda_check(e, "cudaGetDevice");
+  std::lock_guard<std::mutex> lock(mu);
+  DeviceFacts& f = facts[dev];
+  if (f.nsm == 0) {
+    if ((e = cudaDeviceGetAttribute(&f.nsm, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_check(e, "SM count");
+    if ((e = cudaDeviceGetAttribute(&f.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+      return cuda_check(e, "shared memory limit");
+  }
+  const int di = dt == GSI_BF16 ? 1 : 0;
+  if (smem_budget > 0 && f.clusters[di] == 0) {
+    DecidePlan q{};
+    q.smem = smem_budget;
+    const int n = decide_apply_max_clusters(q, dt);
+    if (n <= 0) return fail(GSI_ERR_CUDA, "cannot size the decide-and-apply grid (cluster occupancy query failed)");
+    f.clusters[di] = n;
+  }
+  *out = &f;
+  return GSI_OK;
 }
 
-// Enqueue gate (+ optional apply) for one map.  All arguments validated.
-static gsi_status run_stream(const gsi_map_desc* m, const void* X, int64_t T, float eps, float* Y,
-                             uint8_t* flags, float* rho, float* G_out, void* ws, cudaStream_t st,
-                             bool apply) {
+// Shared memory the decide-and-apply kernel may use: the device limit less
+// room for one CTA of the next projection kernel, which starts early.
+static size_t decide_smem_budget(int smem_optin) { return size_t(smem_optin) - 16 * 1024; }
+
+// Enqueue the decide-and-apply kernel for one map (all arguments validated).
+// mode 0: decide and apply (gsi_linear); 1: decide only (gsi_gate, writes
+// G, rho, flags and the compaction); 2: apply the decision stored by a
+// preceding gsi_gate on the same workspace (gsi_apply).
+static gsi_status run_decide(const gsi_map_desc* m, const void* X, int64_t T, float eps, int mode, float* Y,
+                             uint8_t* flags, float* rho, float* G, const float* Gin, void* ws, cudaStream_t st) {
   const int es = elem_bytes(m->dtype);
   const GatePlan gp = plan_gate(m->d, m->k, es, T);
   const StreamLayout L = layout_stream(m->d, m->k, es, T);
   char* base = static_cast<char*>(ws);
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(base + L.ctrl);
-
+  DeviceFacts* f = nullptr;
+  gsi_status s = device_facts(GSI_F32, 0, &f);
+  if (s != GSI_OK) return s;
+  const size_t budget = decide_smem_budget(f->smem_optin);
+  if ((s = device_facts(m->dtype, budget, &f)) != GSI_OK) return s;
+  const DecidePlan dp = plan_decide(m->d, m->d_out, m->k, es, T, f->clusters[m->dtype == GSI_BF16 ? 1 : 0] * kClusterSize,
+                                    budget);
+  if (!dp.ok) return fail(GSI_ERR_UNSUPPORTED, "the streaming kernels' shared memory does not fit this map");
   if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
+  DecideArgs a{};
+  a.X = X;
+  a.W = m->W;
+  a.M = m->M;
+  a.gram = m->gram;
+  a.part_g = reinterpret_cast<const float*>(base + L.part_g);
+  a.part_x = reinterpret_cast<const float*>(base + L.part_x);
+  a.nclu = gp.n_clusters;
+  a.d = m->d;
+  a.d_out = m->d_out;
+  a.k = int(m->k);
+  a.T = int(T);
+  a.ks = gp.ks;
+  a.eps = eps;
+  a.mode = mode;
+  a.Y = Y;
+  a.G = G;
+  a.rho = rho;
+  a.flags = mode == 1 ? reinterpret_cast<uint8_t*>(base + L.flags) : flags;
+  a.idx = reinterpret_cast<int32_t*>(base + L.idx);
+  a.counts = ctrl->counts;
+  a.Gin = Gin;
+  a.flags_in = reinterpret_cast<const uint8_t*>(base + L.flags);
+  a.rows_per_cta = dp.rows_per_cta;
+  a.seg_bytes = dp.seg_bytes;
+  a.wstages = dp.wstages;
+  a.x_stage_max = dp.x_stage_max;
+  a.stage_m = dp.stage_m;
+  a.off_m = dp.off_m;
+  a.off_x = dp.off_x;
+  a.off_g = dp.off_g;
+  a.err = &ctrl->err;
+  s = cuda_check(launch_decide_apply(a, dp, m->dtype, st), "decide-and-apply kernel launch");
+  if (s != GSI_OK || mode != 1 || !flags) return s;
+  // gsi_gate: the caller's flags are a copy of the stored decision
+  return cuda_check(cudaMemcpyAsync(flags, base + L.flags, size_t(T), cudaMemcpyDeviceToDevice, st),
+                    "flags copy");
+}
 
+// Enqueue the projection kernel, then (mode) the decide-and-apply kernel.
+static gsi_status run_stream(const gsi_map_desc* m, const void* X, int64_t T, float eps, float* Y,
+                             uint8_t* flags, float* rho, float* G_out, void* ws, cudaStream_t st, bool apply) {
+  const int es = elem_bytes(m->dtype);
+  const GatePlan gp = plan_gate(m->d, m->k, es, T);
+  const StreamLayout L = layout_stream(m->d, m->k, es, T);
+  char* base = static_cast<char*>(ws);
+  if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
   GateArgs ga{};
   ga.X = X;
   ga.V = m->V;
-  ga.gram = m->gram;
   ga.d = m->d;
   ga.k = int(m->k);
   ga.T = int(T);
-  ga.eps = eps;
   ga.rs = gp.rs;
   ga.nv = gp.nv;
   ga.nrg = gp.nrg;
@@ -211,27 +258,9 @@ static gsi_status run_stream(const gsi_map_desc* m, const void* X, int64_t T, fl
   ga.n_clusters = gp.n_clusters;
   ga.part_g = reinterpret_cast<float*>(base + L.part_g);
   ga.part_x = reinterpret_cast<float*>(base + L.part_x);
-  ga.G = G_out ? G_out : reinterpret_cast<float*>(base + L.g);
-  ga.rho = rho;
-  ga.flags = flags;
-  ga.idx = reinterpret_cast<int32_t*>(base + L.idx);
-  ga.ctrl = ctrl;
-  if (m->gram) {
-    const uint64_t gb = uint64_t(m->k) * m->k * 4;
-    ga.gram_share = ((gb + gp.n_slabs - 1) / gp.n_slabs + 15) / 16 * 16;
-  }
-  if (apply) {
-    // Speculative L2 prefetch of the image M: most tokens take the fast path.
-    const uint64_t total = uint64_t(m->d_out) * m->k * es;
-    uint64_t share = (total + gp.n_slabs - 1) / gp.n_slabs;
-    share = (share + 15) / 16 * 16;
-    ga.pf_base = static_cast<const char*>(m->M);
-    ga.pf_share = share;
-    ga.pf_total = total;
-  }
-  gsi_status s = cuda_check(launch_gate(ga, gp, m->dtype, st, true), "gate kernel launch");
-  if (s != GSI_OK || !apply) return s;
-  return run_apply(m, X, ga.G, T, Y, ws, st);
+  gsi_status s = cuda_check(launch_gate(ga, gp, m->dtype, st, true), "projection kernel launch");
+  if (s != GSI_OK) return s;
+  return run_decide(m, X, T, eps, apply ? 0 : 1, Y, flags, rho, G_out, nullptr, ws, st);
 }
 
 // Enqueue the tensor-core path for one bf16 map.  All arguments validated.
@@ -352,7 +381,7 @@ gsi_status gsi_apply(const gsi_map_desc* map, const void* X, const float* G, int
   if ((s = check_ptr(G, "G")) != GSI_OK) return s;
   if ((s = check_ptr(Y, "Y")) != GSI_OK) return s;
   if ((s = check_workspace(workspace, ws_bytes, stream_ws(map, T))) != GSI_OK) return s;
-  s = run_apply(map, X, G, T, Y, workspace, static_cast<cudaStream_t>(stream));
+  s = run_decide(map, X, T, 0.f, 2, Y, nullptr, nullptr, nullptr, G, workspace, static_cast<cudaStream_t>(stream));
   return s == GSI_OK ? ok() : s;
 }
 

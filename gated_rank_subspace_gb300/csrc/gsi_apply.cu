@@ -1,203 +1,501 @@
-// Apply kernel: the fast path y = M g and the slow path y = W x in one launch.
+// Decide-and-apply kernel: residual ratio, gate, and the fast / slow paths.
 //
-// "Gated Subspace Inference for Transformer Acceleration", §2.2: fast tokens
-// (rho < eps) read only the cached image M (d_out x k); slow tokens read the
-// full W (d_out x d).  The gate's decision stays on the device: this kernel
-// reads the fast / slow counts and the stable index lists the gate kernel
-// wrote, so the host never waits for the flags.
+// "Gated Subspace Inference for Transformer Acceleration", §2.2: per token,
+// rho = ||x - V_k g|| / ||x||; fast tokens (rho < eps) take y = M g (the
+// cached image, d_out x k), slow tokens the exact y = W x (d_out x d).
 //
-// Work is split into units of about 8 KB of weights, each handled by one
-// warp: a fast unit is 16 / vplm rows of M, a slow unit one or more rows of W.
-// Fast units come first, then slow units; the persistent grid's warps stride
-// over them, so a call with both kinds of tokens streams M and W at once and
-// a call with one kind streams only that matrix.  Weights are read with
-// 16-byte non-allocating loads, each row once per block of tokens; the
-// projections g of fast tokens and the slow tokens' x are staged in shared
-// memory when they fit.  Row sums use warp shuffles (a butterfly that reduces
-// 16 rows in 16 shuffles for the fast path).  Fixed summation order:
-// results are bitwise reproducible.
+// Input: the cluster partials of g = V_k^T x and ||x||^2 written by the
+// projection kernel.  Every 8-CTA cluster of this grid finishes the gate on
+// its own: CTA r adds the partials of its slice of g's columns, the slices are
+// exchanged through distributed shared memory, CTA r forms its share of
+// g^T (V_k^T V_k) g from a Gram slice it loaded into registers before the
+// dependency wait, and the shares are added in rank order.  All clusters do
+// the same arithmetic on the same data in the same order, so they reach the
+// same bits, and every CTA knows every token's flag without a grid-wide sync
+// or a host round trip.
+//
+// Each CTA owns a contiguous block of output rows.  Before the dependency
+// wait it copies its rows of M into shared memory (TMA bulk copy), so a fast
+// call only computes from shared memory once the gate is known.  Slow tokens
+// stream the CTA's rows of W through a ring of bulk copies (a producer warp,
+// eight consumer warps, mbarriers); each chunk of Rc rows is split into
+// 8 / Rc column segments, one per warp, and the segments' sums are added in
+// warp order.  Every wait on an mbarrier is bounded: on expiry the kernel
+// sets the workspace error word, drains its own copies (bounded) and returns.
+//
+// Modes: decide and apply (gsi_linear), decide only (gsi_gate: writes G,
+// rho, flags and the compaction), apply a stored decision (gsi_apply).
 
 #include "gsi_common.cuh"
-#include "gsi_plan.h"
 #include "gsi_kernels.h"
+#include "gsi_plan.h"
 
 namespace gsi {
 
-template <class E, int VPLM>
-__device__ __forceinline__ void fast_unit(const ApplyArgs& a, int64_t u, int n_fast, int ngs,
-                                          const float* gst, int lane) {
-  constexpr int RM = 16 / VPLM;
-  constexpr int PV = E::kPerVec;
-  const int k = a.k;
-  const int nvm = k * E::kBytes / 16;
-  const int64_t row0 = u * RM;
-  const char* mbase = reinterpret_cast<const char*>(a.M);
-  uint4 mv[RM][VPLM];
-#pragma unroll
-  for (int r = 0; r < RM; ++r)
-#pragma unroll
-    for (int j = 0; j < VPLM; ++j) {
-      const int vv = lane + 32 * j;
-      const int64_t row = row0 + r;
-      mv[r][j] = (row < a.d_out && vv < nvm)
-                     ? ld_weight_v4(mbase + row * k * E::kBytes + int64_t(vv) * 16)
-                     : make_uint4(0u, 0u, 0u, 0u);
+// ------------------------------------------------------------------ async-copy wrappers
+__device__ __forceinline__ uint32_t sa(const void* p) { return static_cast<uint32_t>(__cvta_generic_to_shared(p)); }
+
+__device__ __forceinline__ void bar_init(uint64_t* b, uint32_t n) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(b)), "r"(n) : "memory");
+}
+__device__ __forceinline__ void bar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa(b)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(sa(b)) : "memory");
+}
+__device__ __forceinline__ bool bar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(sa(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+constexpr long long kSpinCycles = 4000000000LL;  // ~2 s at 2 GHz
+__device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t parity, uint32_t* err) {
+  const long long t0 = clock64();
+  while (!bar_try(b, parity)) {
+    if (clock64() - t0 > kSpinCycles) {
+      atomicOr(err, kErrTimeout);
+      return false;
     }
-  for (int f = 0; f < n_fast; ++f) {
-    const int tok = __ldcg(&a.idx[f]);
-    float gv[VPLM][PV];
-#pragma unroll
-    for (int j = 0; j < VPLM; ++j) {
-      const int vv = lane + 32 * j;
-      if (vv < nvm) {
-        const float* src = f < ngs ? gst + int64_t(f) * k + vv * PV : nullptr;
-#pragma unroll
-        for (int e4 = 0; e4 < PV / 4; ++e4) {
-          float4 g4 = src ? reinterpret_cast<const float4*>(src)[e4]
-                          : __ldcg(reinterpret_cast<const float4*>(a.G + int64_t(tok) * k + vv * PV) + e4);
-          gv[j][e4 * 4 + 0] = g4.x;
-          gv[j][e4 * 4 + 1] = g4.y;
-          gv[j][e4 * 4 + 2] = g4.z;
-          gv[j][e4 * 4 + 3] = g4.w;
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < PV; ++e) gv[j][e] = 0.f;
-      }
-    }
-    float part[RM];
-#pragma unroll
-    for (int r = 0; r < RM; ++r) {
-      float s = 0.f;
-#pragma unroll
-      for (int j = 0; j < VPLM; ++j) {
-        float w[PV];
-        E::unpack(mv[r][j], w);
-#pragma unroll
-        for (int e = 0; e < PV; ++e) s = fmaf(w[e], gv[j][e], s);
-      }
-      part[r] = s;
-    }
-    const float s = warp_reduce_multi<RM>(part, lane);
-    const int r = row_of_lane<RM>(lane);
-    if ((lane & (32 / RM - 1)) == 0 && row0 + r < a.d_out)
-      a.Y[int64_t(tok) * a.d_out + row0 + r] = s;
   }
+  return true;
+}
+// 1-D bulk copy global -> shared (16-byte aligned, multiple of 16 bytes).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* b) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   sa(dst)),
+               "l"(src), "r"(bytes), "r"(sa(b))
+               : "memory");
 }
 
-template <class E>
-__device__ __forceinline__ void slow_unit(const ApplyArgs& a, int64_t u, int n_slow, int nxs,
-                                          const unsigned char* xst, int lane) {
+// ------------------------------------------------------------------ kernel
+template <class E, int TC, int GRV>
+__global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kApplyThreads, 1)
+    decide_apply_kernel(DecideArgs a) {
   constexpr int PV = E::kPerVec;
-  constexpr int CH = 8;   // 16-byte vectors per lane in flight per chunk
-  constexpr int TB = 4;   // tokens per pass over a row
-  const int64_t nvw = a.d * E::kBytes / 16;
-  const int64_t xrow_b = a.d * E::kBytes;
-  for (int rr = 0; rr < a.rows_slow; ++rr) {
-    const int64_t row = u * a.rows_slow + rr;
-    if (row >= a.d_out) return;
-    const char* wrow = reinterpret_cast<const char*>(a.W) + row * xrow_b;
-    for (int s0 = 0; s0 < n_slow; s0 += TB) {
-      const int tb = min(TB, n_slow - s0);
-      int tok[TB];
+  constexpr int NCW = 8;  // consumer warps
+  extern __shared__ __align__(128) unsigned char smem[];
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = int(cluster.block_rank());
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int k = a.k, T = a.T, ks = a.ks;
+  const int64_t d = a.d, d_out = a.d_out;
+  const int64_t r0 = int64_t(blockIdx.x) * a.rows_per_cta;
+  const int nrows = int(r0 >= d_out ? 0 : (d_out - r0 < a.rows_per_cta ? d_out - r0 : a.rows_per_cta));
+  const int64_t row_b = d * E::kBytes;      // bytes of a W row
+  const int mrow_b = k * E::kBytes;         // bytes of an M row
+  const int c0 = rank * ks, c1 = min(k, c0 + ks);
+
+  // shared-memory carve-up (offsets computed on the host, see plan_decide)
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);          // [9 warps][wstages]
+  uint64_t* mfull = full + (kApplyThreads / 32) * a.wstages;   // [1]
+  unsigned char* Ms = smem + a.off_m;                          // staged M rows / W rings
+  unsigned char* xst = smem + a.off_x;                         // staged x of slow tokens
+  float* gfull = reinterpret_cast<float*>(smem + a.off_g);     // [TC][k]
+  float* gsl = gfull + TC * k;                                 // [TC][ks]
+  float* qw = gsl + TC * ks;                                   // [8][TC]
+  float* nw = qw + 8 * TC;                                     // [8][TC]
+  float* qin = nw + 8 * TC;                                    // [8 ranks][TC] pushed shares
+  float* nin = qin + kClusterSize * TC;                        // [8 ranks][TC]
+  float* nx2 = nin + kClusterSize * TC;                        // [TC]
+  float* rowpart = nx2 + TC;                                   // [8 warps][4]
+  int* sflag = reinterpret_cast<int*>(rowpart + 8 * 4);        // [TC]
+  int* slist = sflag + TC;                                     // [TC] slow tokens of the chunk
+  int* flist = slist + TC;                                     // [TC] fast tokens of the chunk
+  int* scount = flist + TC;                                    // [2]
+
+  // ---- prologue: only weights (may overlap the projection kernel)
+  pdl_launch_dependents();
+  if (tid == 0) {
+    for (int s = 0; s < (kApplyThreads / 32) * a.wstages; ++s) bar_init(&full[s], 1);
+    bar_init(mfull, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  const bool stage_m = a.stage_m && a.mode != 1 && nrows > 0;
+  if (tid == kApplyThreads - 32 && stage_m) {
+    const uint32_t bytes = uint32_t(nrows) * mrow_b;
+    bar_expect_tx(mfull, bytes);
+    bulk_g2s(Ms, static_cast<const char*>(a.M) + r0 * mrow_b, bytes, mfull);
+  }
+  // Gram slice rows [c0, c1) into registers (GRV float4 per thread)
+  float4 gr[GRV > 0 ? GRV : 1];
+  const int k4 = k >> 2;
+  const int gvec = (c1 > c0) ? (c1 - c0) * k4 : 0;
+  if (GRV > 0 && a.gram && a.mode != 2 && tid < 256) {
 #pragma unroll
-      for (int i = 0; i < TB; ++i) tok[i] = i < tb ? __ldcg(&a.idx[a.T + s0 + i]) : 0;
-      float acc[TB];
-#pragma unroll
-      for (int i = 0; i < TB; ++i) acc[i] = 0.f;
-      for (int64_t c0 = 0; c0 < nvw; c0 += 32 * CH) {
-        uint4 wv[CH];
-#pragma unroll
-        for (int j = 0; j < CH; ++j) {
-          const int64_t vv = c0 + lane + 32 * j;
-          wv[j] = vv < nvw ? ld_weight_v4(wrow + vv * 16) : make_uint4(0u, 0u, 0u, 0u);
+    for (int u = 0; u < (GRV > 0 ? GRV : 1); ++u) {
+      const int v = u * 256 + tid;
+      gr[u] = v < gvec ? __ldg(reinterpret_cast<const float4*>(a.gram + int64_t(c0 + v / k4) * k) + (v % k4))
+                       : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  if (GRV == 0 && a.gram && a.mode != 2 && tid == 0 && gvec > 0)
+    prefetch_l2(a.gram + int64_t(c0) * k, uint32_t(gvec) * 16u);  // read after the wait
+  cluster_arrive_relaxed();
+  pdl_wait();
+  bool started = false;
+
+  bool ok = true;
+  bool m_live = stage_m;  // staged M rows still in shared memory (the W ring reuses it)
+  bool m_waited = false;  // the M copy has been waited for
+  int wuse = 0;           // this warp's ring items used so far (running count over token chunks)
+  const int E_ = TC * ks;
+  const int grp = 256 / E_ >= 8 ? 8 : 256 / E_ >= 4 ? 4 : 256 / E_ >= 2 ? 2 : 1;
+  const int64_t cstride = int64_t(T) * k;
+
+  for (int t0 = 0; t0 < T; t0 += TC) {
+    const int tc = min(TC, T - t0);
+    if (a.mode != 2) {
+      // -- g: this CTA's column slice summed over the projection clusters
+      if (tid < 256) {
+        for (int base = 0; base < E_ * grp; base += 256) {
+          const int id = base + tid;
+          const int e = id / grp, g = id - (id / grp) * grp;
+          const int t = e / ks, col = c0 + (e - (e / ks) * ks);
+          const bool valid = e < E_ && t < tc && col < c1;
+          float s = 0.f;
+          if (valid) {
+            const float* src = a.part_g + int64_t(t0 + t) * k + col;
+            int cl = g;
+            for (; cl + 3 * grp < a.nclu; cl += 4 * grp) {
+              const float v0 = __ldcg(src + cl * cstride), v1 = __ldcg(src + (cl + grp) * cstride);
+              const float v2 = __ldcg(src + (cl + 2 * grp) * cstride), v3 = __ldcg(src + (cl + 3 * grp) * cstride);
+              s += v0;
+              s += v1;
+              s += v2;
+              s += v3;
+            }
+            for (; cl < a.nclu; cl += grp) s += __ldcg(src + cl * cstride);
+          }
+          for (int o = 1; o < grp; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+          if (g == 0 && e < E_) gsl[e] = valid ? s : 0.f;
         }
+        if (warp == 0) {
+          // ||x||^2: every CTA sums the projection clusters' partials itself;
+          // lane l adds clusters l, l + 32, ... of every token (loads issued
+          // together), then the warp adds the lanes in a fixed order.
 #pragma unroll
-        for (int j = 0; j < CH; ++j) {
-          const int64_t vv = c0 + lane + 32 * j;
-          if (vv < nvw) {
-            float w[PV];
-            E::unpack(wv[j], w);
+          for (int t = 0; t < TC; ++t) {
+            float s = 0.f;
+            if (t < tc)
+              for (int cl = lane; cl < a.nclu; cl += 32) s += __ldcg(&a.part_x[int64_t(cl) * T + t0 + t]);
+            s = warp_sum(s);
+            if (lane == 0) nx2[t] = s;
+          }
+        }
+      }
+      if (!started) {
+        cluster_wait();  // every CTA of the cluster is running
+        started = true;
+      }
+      __syncthreads();
+      // push this CTA's slice of g into every CTA's full copy
+      for (int e = tid; e < E_ * kClusterSize; e += blockDim.x) {
+        const int q = e / E_, f = e - (e / E_) * E_;
+        const int t = f / ks, col = c0 + (f - (f / ks) * ks);
+        if (col < c1) cluster.map_shared_rank(gfull, q)[t * k + col] = gsl[f];
+      }
+      cluster.sync();
+      // -- ||g||^2 and g^T Gram g over this CTA's Gram rows
+      float qa[TC], na[TC];
 #pragma unroll
-            for (int i = 0; i < TB; ++i) {
-              if (i < tb) {
-                const int si = s0 + i;
-                const uint4 xv =
-                    si < nxs ? reinterpret_cast<const uint4*>(xst + int64_t(si) * xrow_b)[vv]
-                             : ld_cg_v4(reinterpret_cast<const char*>(a.X) + int64_t(tok[i]) * xrow_b + vv * 16);
-                float xf[PV];
-                E::unpack(xv, xf);
+      for (int t = 0; t < TC; ++t) qa[t] = na[t] = 0.f;
+      if (tid < 256) {
+        for (int i = c0 + tid; i < c1; i += 256) {
 #pragma unroll
-                for (int e = 0; e < PV; ++e) acc[i] = fmaf(w[e], xf[e], acc[i]);
+          for (int t = 0; t < TC; ++t) na[t] = fmaf(gfull[t * k + i], gfull[t * k + i], na[t]);
+        }
+        if (a.gram) {
+          if (GRV > 0) {
+#pragma unroll
+            for (int u = 0; u < (GRV > 0 ? GRV : 1); ++u) {
+              const int v = u * 256 + tid;
+              if (v < gvec) {
+                const int i = c0 + v / k4, j = 4 * (v % k4);
+#pragma unroll
+                for (int t = 0; t < TC; ++t) {
+                  const float4 gj = *reinterpret_cast<const float4*>(gfull + t * k + j);
+                  float h = gr[u].x * gj.x;
+                  h = fmaf(gr[u].y, gj.y, h);
+                  h = fmaf(gr[u].z, gj.z, h);
+                  h = fmaf(gr[u].w, gj.w, h);
+                  qa[t] = fmaf(gfull[t * k + i], h, qa[t]);
+                }
+              }
+            }
+          } else {
+            for (int v = tid; v < gvec; v += 256) {
+              const float4 gv = __ldg(reinterpret_cast<const float4*>(a.gram + int64_t(c0 + v / k4) * k) + (v % k4));
+              const int i = c0 + v / k4, j = 4 * (v % k4);
+#pragma unroll
+              for (int t = 0; t < TC; ++t) {
+                const float4 gj = *reinterpret_cast<const float4*>(gfull + t * k + j);
+                float h = gv.x * gj.x;
+                h = fmaf(gv.y, gj.y, h);
+                h = fmaf(gv.z, gj.z, h);
+                h = fmaf(gv.w, gj.w, h);
+                qa[t] = fmaf(gfull[t * k + i], h, qa[t]);
               }
             }
           }
         }
-      }
 #pragma unroll
-      for (int i = 0; i < TB; ++i) {
-        const float s = warp_sum(acc[i]);
-        if (i < tb && lane == 0) a.Y[int64_t(tok[i]) * a.d_out + row] = s;
+        for (int t = 0; t < TC; ++t) {
+          const float q = warp_sum(qa[t]);
+          const float n = warp_sum(na[t]);
+          if (lane == 0) {
+            qw[warp * TC + t] = q;
+            nw[warp * TC + t] = n;
+          }
+        }
+      }
+      __syncthreads();
+      if (tid < TC * kClusterSize) {
+        // this CTA's share of g^T Gram g and ||g||^2, pushed to every CTA
+        const int t = tid % TC, dst = tid / TC;
+        float q = 0.f, n = 0.f;
+        for (int w = 0; w < 8; ++w) {
+          q += qw[w * TC + t];
+          n += nw[w * TC + t];
+        }
+        cluster.map_shared_rank(qin, dst)[rank * TC + t] = q;
+        cluster.map_shared_rank(nin, dst)[rank * TC + t] = n;
+      }
+      cluster.sync();
+      if (tid < TC) {
+        int slow = 0;
+        if (tid < tc) {
+          float q = 0.f, n = 0.f;
+#pragma unroll
+          for (int r = 0; r < kClusterSize; ++r) {
+            q += qin[r * TC + tid];
+            n += nin[r * TC + tid];
+          }
+          if (!a.gram) q = n;  // orthonormal basis: ||V g||^2 = ||g||^2
+          const float xx = nx2[tid];
+          float rr = xx - 2.f * n + q;
+          rr = rr < 0.f ? 0.f : rr;  // keeps NaN
+          const float rho = xx == 0.f ? 0.f : sqrtf(rr / xx);
+          slow = rho < a.eps ? 0 : 1;
+          if (blockIdx.x == 0) {
+            if (a.rho) a.rho[t0 + tid] = rho;
+            a.flags[t0 + tid] = uint8_t(slow);
+          }
+        }
+        sflag[tid] = slow;
+      }
+      if (blockIdx.x == 0 && a.G) {
+        for (int e = tid; e < tc * k; e += blockDim.x) a.G[int64_t(t0) * k + e] = gfull[e];
+      }
+
+    } else {
+      // stored decision (gsi_apply): flags and g from the preceding gate
+      for (int e = tid; e < TC * k; e += blockDim.x) {
+        const int t = e / k;
+        gfull[e] = t < tc ? __ldcg(&a.Gin[int64_t(t0) * k + e]) : 0.f;
+      }
+      if (tid < TC) sflag[tid] = tid < tc ? int(ld_cg_u8(a.flags_in + t0 + tid) != 0) : 0;
+      __syncthreads();
+    }
+    // -- per-chunk token lists (every thread reads the same smem flags);
+    //    decide-only calls apply nothing
+    if (tid == 0) {
+      int nf = 0, ns = 0;
+      for (int t = 0; t < tc; ++t) {
+        if (a.mode == 1) break;
+        if (sflag[t])
+          slist[ns++] = t;
+        else
+          flist[nf++] = t;
+      }
+      scount[0] = ok ? nf : 0;
+      scount[1] = ok ? ns : 0;
+    }
+    __syncthreads();
+    const int nf = scount[0], ns = scount[1];
+
+    // -- fast tokens: y = M g from the staged (or global) rows of M
+    if (nf > 0 && nrows > 0 && tid < 256) {
+      const unsigned char* mrows =
+          m_live ? Ms : static_cast<const unsigned char*>(a.M) + r0 * mrow_b;
+      if (m_live && !m_waited && !bar_wait(mfull, 0, a.err)) ok = false;
+      if (ok) {
+        const int nvm = mrow_b / 16;
+        constexpr int RB = 16;
+        for (int rb = warp * RB; rb < nrows; rb += NCW * RB) {
+          for (int f = 0; f < nf; ++f) {
+            const int t = flist[f];
+            float part[RB];
+#pragma unroll
+            for (int r = 0; r < RB; ++r) part[r] = 0.f;
+            for (int vv = lane; vv < nvm; vv += 32) {
+              float gv[PV];
+#pragma unroll
+              for (int e4 = 0; e4 < PV / 4; ++e4) {
+                const float4 g4 = *reinterpret_cast<const float4*>(gfull + t * k + vv * PV + 4 * e4);
+                gv[4 * e4] = g4.x;
+                gv[4 * e4 + 1] = g4.y;
+                gv[4 * e4 + 2] = g4.z;
+                gv[4 * e4 + 3] = g4.w;
+              }
+#pragma unroll
+              for (int r = 0; r < RB; ++r) {
+                if (rb + r < nrows) {
+                  float w[PV];
+                  E::unpack(*reinterpret_cast<const uint4*>(mrows + int64_t(rb + r) * mrow_b + vv * 16), w);
+#pragma unroll
+                  for (int e = 0; e < PV; ++e) part[r] = fmaf(w[e], gv[e], part[r]);
+                }
+              }
+            }
+            const float s = warp_reduce_multi<RB>(part, lane);
+            const int r = row_of_lane<RB>(lane);
+            if ((lane & (32 / RB - 1)) == 0 && rb + r < nrows) a.Y[int64_t(t0 + t) * d_out + r0 + rb + r] = s;
+          }
+        }
       }
     }
+
+    ok = __syncthreads_and(ok) != 0;
+    if (nf > 0 && nrows > 0) m_waited = m_waited || m_live;
+    // -- slow tokens: every warp streams its own rows of W (rows warp,
+    //    warp + 9, ...) in segments through a private ring of bulk copies.
+    //    The ring shares shared memory with the staged M rows: wait for that
+    //    copy and retire the staged rows before the first segment lands.
+    if (ns > 0 && nrows > 0 && ok) {
+      const int nxs = min(ns, a.x_stage_max);
+      const int64_t xv = row_b / 16;
+      for (int64_t e = tid; e < int64_t(nxs) * xv; e += blockDim.x) {
+        const int j = int(e / xv);
+        const int64_t v = e - int64_t(j) * xv;
+        reinterpret_cast<uint4*>(xst)[e] =
+            ld_cg_v4(static_cast<const char*>(a.X) + int64_t(t0 + slist[j]) * row_b + v * 16);
+      }
+      if (m_live) {
+        if (tid == 0 && !m_waited && !bar_wait(mfull, 0, a.err)) ok = false;
+        m_live = false;
+        m_waited = true;
+      }
+      __syncthreads();
+      const int nwarp = kApplyThreads / 32;
+      const int seg_b = a.seg_bytes;
+      const int SW = a.wstages;
+      const int nseg = int((row_b + seg_b - 1) / seg_b);
+      const int my_rows = warp < nrows ? (nrows - warp + nwarp - 1) / nwarp : 0;
+      const int items = my_rows * nseg;
+      unsigned char* wring = Ms + int64_t(warp) * SW * seg_b;
+      uint64_t* wfull = full + warp * SW;
+      const char* wbase = static_cast<const char*>(a.W) + r0 * row_b;
+      int issued = 0;
+      if (lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        for (; issued < items && issued < SW; ++issued) {
+          const int j = issued / nseg, sg = issued - (issued / nseg) * nseg;
+          const int64_t off = int64_t(sg) * seg_b;
+          const uint32_t bytes = uint32_t(min(int64_t(seg_b), row_b - off));
+          const int slot = (wuse + issued) % SW;
+          bar_expect_tx(&wfull[slot], bytes);
+          bulk_g2s(wring + slot * seg_b, wbase + (int64_t(warp) + int64_t(j) * nwarp) * row_b + off, bytes,
+                   &wfull[slot]);
+        }
+      }
+      issued = __shfl_sync(0xffffffffu, issued, 0);
+      float acc[TC];
+#pragma unroll
+      for (int t = 0; t < TC; ++t) acc[t] = 0.f;
+      int i = 0;
+      for (; i < items; ++i) {
+        const int slot = (wuse + i) % SW;
+        const uint32_t ph = ((wuse + i) / SW) & 1;
+        if (!__all_sync(0xffffffffu, bar_wait(&wfull[slot], ph, a.err))) {
+          ok = false;
+          break;
+        }
+        const int j = i / nseg, sg = i - (i / nseg) * nseg;
+        const int64_t off = int64_t(sg) * seg_b;
+        const int nvec = int(min(int64_t(seg_b), row_b - off) / 16);
+        const unsigned char* segp = wring + slot * seg_b;
+        for (int vv = lane; vv < nvec; vv += 32) {
+          float w[PV];
+          E::unpack(*reinterpret_cast<const uint4*>(segp + vv * 16), w);
+          const int64_t xo = off + int64_t(vv) * 16;
+#pragma unroll
+          for (int t = 0; t < TC; ++t) {
+            if (t < ns) {
+              const uint4 xq = t < nxs ? *reinterpret_cast<const uint4*>(xst + int64_t(t) * row_b + xo)
+                                       : ld_cg_v4(static_cast<const char*>(a.X) + int64_t(t0 + slist[t]) * row_b + xo);
+              float xf[PV];
+              E::unpack(xq, xf);
+#pragma unroll
+              for (int e = 0; e < PV; ++e) acc[t] = fmaf(w[e], xf[e], acc[t]);
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0 && issued < items) {
+          // the slot just read is refilled with the segment SW items ahead
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          const int q = issued;
+          const int jq = q / nseg, sq = q - (q / nseg) * nseg;
+          const int64_t offq = int64_t(sq) * seg_b;
+          const uint32_t bytes = uint32_t(min(int64_t(seg_b), row_b - offq));
+          const int sl = (wuse + q) % SW;
+          bar_expect_tx(&wfull[sl], bytes);
+          bulk_g2s(wring + sl * seg_b, wbase + (int64_t(warp) + int64_t(jq) * nwarp) * row_b + offq, bytes,
+                   &wfull[sl]);
+        }
+        issued = __shfl_sync(0xffffffffu, issued + ((issued < items) ? 1 : 0), 0);
+        if (sg == nseg - 1) {
+#pragma unroll
+          for (int t = 0; t < TC; ++t) {
+            if (t < ns) {
+              const float sum = warp_sum(acc[t]);
+              if (lane == 0) a.Y[int64_t(t0 + slist[t]) * d_out + r0 + warp + int64_t(j) * nwarp] = sum;
+            }
+            acc[t] = 0.f;
+          }
+        }
+      }
+      // after an error: wait (bounded) for this warp's copies still in flight
+      if (lane == 0)
+        for (int q = i; q < issued; ++q) bar_wait(&wfull[(wuse + q) % SW], ((wuse + q) / SW) & 1, a.err);
+      wuse += issued;
+    }
+    ok = __syncthreads_and(ok && *reinterpret_cast<volatile uint32_t*>(a.err) == 0) != 0;
+    // every CTA of the cluster is done with this chunk's g copy and shares
+    // before the next chunk's pushes; after an error the remaining chunks
+    // only pass through their barriers (a CTA leaving early would strand the
+    // cluster's other CTAs at a barrier)
+    if (t0 + TC < T) cluster.sync();
   }
+
+  if (a.mode == 1 && blockIdx.x == 0) {
+    __threadfence();
+    __syncthreads();
+    if (warp == 0) compact_warp(a.flags, T, a.idx, a.counts, lane);
+  }
+  if (!started) cluster_wait();
+  // bounded drain of the M copy if it was never waited for
+  if (stage_m && !m_waited && tid == 0) bar_wait(mfull, 0, a.err);
 }
 
-template <class E, int VPLM>
-__global__ void __launch_bounds__(kApplyThreads) apply_kernel(ApplyArgs a) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  unsigned char* xst = smem_raw;                                  // [nxs][d] raw elements
-  float* gst = reinterpret_cast<float*>(smem_raw + kApplyXStage);  // [ngs][k]
-  pdl_launch_dependents();
-  pdl_wait();
-  const int n_fast = __ldcg(&a.ctrl->counts[0]);
-  const int n_slow = __ldcg(&a.ctrl->counts[1]);
-  const int nxs = min(n_slow, a.x_stage_max);
-  const int ngs = min(n_fast, a.g_stage_max);
-  const int64_t xrow_v = a.d * E::kBytes / 16;
-  for (int64_t e = threadIdx.x; e < int64_t(nxs) * xrow_v; e += blockDim.x) {
-    const int j = int(e / xrow_v);
-    const int64_t vv = e - int64_t(j) * xrow_v;
-    const int tok = __ldcg(&a.idx[a.T + j]);
-    reinterpret_cast<uint4*>(xst)[e] =
-        ld_cg_v4(reinterpret_cast<const char*>(a.X) + int64_t(tok) * a.d * E::kBytes + vv * 16);
-  }
-  const int kv4 = a.k / 4;
-  for (int e = threadIdx.x; e < ngs * kv4; e += blockDim.x) {
-    const int j = e / kv4, vv = e - (e / kv4) * kv4;
-    const int tok = __ldcg(&a.idx[j]);
-    reinterpret_cast<float4*>(gst)[e] = __ldcg(reinterpret_cast<const float4*>(a.G + int64_t(tok) * a.k) + vv);
-  }
-  __syncthreads();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int64_t uf = n_fast > 0 ? a.fast_units : 0;
-  const int64_t us = n_slow > 0 ? a.slow_units : 0;
-  const int64_t wpb = blockDim.x >> 5;
-  const int64_t nwarps = int64_t(gridDim.x) * wpb;
-  for (int64_t u = int64_t(blockIdx.x) * wpb + warp; u < uf + us; u += nwarps) {
-    if (u < uf)
-      fast_unit<E, VPLM>(a, u, n_fast, ngs, gst, lane);
-    else
-      slow_unit<E>(a, u - uf, n_slow, nxs, xst, lane);
-  }
-}
-
-template <class E, int VPLM>
-static cudaError_t launch_apply_t(const ApplyArgs& a, const ApplyPlan& p, int nsm, cudaStream_t s,
-                                  bool pdl) {
-  auto kern = apply_kernel<E, VPLM>;
-  // One persistent wave: as many CTAs as fit on the device at once.
-  static int per_sm = 0;
-  if (per_sm == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(p.smem));
+template <class E, int TC, int GRV>
+static cudaError_t launch_da_t(const DecideArgs& a, const DecidePlan& p, cudaStream_t s) {
+  auto kern = decide_apply_kernel<E, TC, GRV>;
+  static size_t smem_set = 0;
+  if (p.smem > smem_set) {
+    cudaError_t e = set_kernel_smem(kern, p.smem);
     if (e != cudaSuccess) return e;
-    int n = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kApplyThreads, p.smem);
-    if (e != cudaSuccess) return e;
-    per_sm = n > 0 ? n : 1;
+    smem_set = p.smem;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(nsm * per_sm));
+  cfg.gridDim = dim3(unsigned(p.ncta));
   cfg.blockDim = dim3(kApplyThreads);
   cfg.dynamicSmemBytes = p.smem;
   cfg.stream = s;
@@ -205,24 +503,48 @@ static cudaError_t launch_apply_t(const ApplyArgs& a, const ApplyPlan& p, int ns
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = pdl ? 1 : 0;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <class E>
-static cudaError_t launch_apply_e(const ApplyArgs& a, const ApplyPlan& p, int nsm, cudaStream_t s,
-                                  bool pdl) {
-  switch (p.vplm) {
-    case 1: return launch_apply_t<E, 1>(a, p, nsm, s, pdl);
-    case 2: return launch_apply_t<E, 2>(a, p, nsm, s, pdl);
-    default: return launch_apply_t<E, 4>(a, p, nsm, s, pdl);
+template <class E, int TC>
+static cudaError_t launch_da_tc(const DecideArgs& a, const DecidePlan& p, cudaStream_t s) {
+  switch (p.grv) {
+    case 8: return launch_da_t<E, TC, 8>(a, p, s);
+    default: return launch_da_t<E, TC, 0>(a, p, s);
   }
 }
 
-cudaError_t launch_apply(const ApplyArgs& a, const ApplyPlan& p, gsi_dtype dt, int nsm,
-                         cudaStream_t s, bool pdl) {
-  return dt == GSI_BF16 ? launch_apply_e<BF16>(a, p, nsm, s, pdl)
-                        : launch_apply_e<F32>(a, p, nsm, s, pdl);
+template <class E>
+static cudaError_t launch_da_e(const DecideArgs& a, const DecidePlan& p, cudaStream_t s) {
+  switch (p.tc) {
+    case 1: return launch_da_tc<E, 1>(a, p, s);
+    case 2: return launch_da_tc<E, 2>(a, p, s);
+    case 4: return launch_da_tc<E, 4>(a, p, s);
+    default: return launch_da_tc<E, 8>(a, p, s);
+  }
+}
+
+cudaError_t launch_decide_apply(const DecideArgs& a, const DecidePlan& p, gsi_dtype dt, cudaStream_t s) {
+  return dt == GSI_BF16 ? launch_da_e<BF16>(a, p, s) : launch_da_e<F32>(a, p, s);
+}
+
+// Co-resident clusters of the decide-and-apply kernel for a plan (grid size).
+template <class E>
+static int max_clusters_e(const DecidePlan& p) {
+  auto kern = decide_apply_kernel<E, 1, 8>;
+  if (set_kernel_smem(kern, p.smem) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kClusterSize * 64);
+  cfg.blockDim = dim3(kApplyThreads);
+  cfg.dynamicSmemBytes = p.smem;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
+  return n;
+}
+
+int decide_apply_max_clusters(const DecidePlan& p, gsi_dtype dt) {
+  return dt == GSI_BF16 ? max_clusters_e<BF16>(p) : max_clusters_e<F32>(p);
 }
 
 }  // namespace gsi

@@ -99,6 +99,15 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// ---------------------------------------------------------------- cluster barrier halves
+// A relaxed arrive early in the kernel and the matching wait just before the
+// first access to a peer's shared memory: the "every CTA of the cluster has
+// started" barrier then overlaps the kernel's weight loads.
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.aligned;" ::: "memory"); }
+
 // ---------------------------------------------------------------- reductions
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
@@ -148,10 +157,49 @@ __device__ __forceinline__ int row_of_lane(int lane) {
   return idx;
 }
 
+// One warp: stable compaction of T flags into fast / slow index lists
+// (fast list at idx[0..), slow list at idx[T..)) and their counts.
+__device__ __forceinline__ void compact_warp(const uint8_t* flags, int T, int32_t* idx, int32_t* counts,
+                                             int lane) {
+  int nf = 0, ns = 0;
+  for (int base = 0; base < T; base += 32) {
+    const int t = base + lane;
+    const bool valid = t < T;
+    const bool slow = valid && ld_cg_u8(flags + t) != 0;
+    const unsigned ms = __ballot_sync(0xffffffffu, slow);
+    const unsigned mf = __ballot_sync(0xffffffffu, valid && !slow);
+    const unsigned lt = (1u << lane) - 1u;
+    if (valid && idx) {
+      if (slow)
+        idx[T + ns + __popc(ms & lt)] = t;
+      else
+        idx[nf + __popc(mf & lt)] = t;
+    }
+    nf += __popc(mf);
+    ns += __popc(ms);
+  }
+  if (lane == 0 && counts) {
+    counts[0] = nf;
+    counts[1] = ns;
+  }
+}
+
+// Every kernel of the decode path asks for the largest shared-memory
+// carve-out: consecutive kernels then run in one L1 / shared-memory
+// configuration, so an SM never has to drain and reconfigure between the
+// projection kernel and the decide-and-apply kernel that overlaps it.
+template <class K>
+inline cudaError_t set_kernel_smem(K kern, size_t dyn_bytes) {
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                       int(cudaSharedmemCarveoutMaxShared));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(dyn_bytes));
+}
+
 // ---------------------------------------------------------------- workspace layout
 // Control words at the head of every workspace (256 bytes).
 struct Ctrl {
-  uint32_t ticket;     // cluster arrival counter of the gate kernel (self-resetting)
+  uint32_t reserved;
   uint32_t err;        // device error word (0 = ok); set by bounded waits
   int32_t counts[2];   // {n_fast, n_slow} of the last gate
   uint32_t pad[60];

@@ -14,38 +14,39 @@ struct Ctrl;
 struct GateArgs {
   const void* X;        // T x d tokens
   const void* V;        // d x k basis
-  const float* gram;    // k x k V^T V, or null (orthonormal)
   int64_t d;
   int k, T;
-  float eps;
   int rs, nv, nrg, ks, n_clusters;
   float* part_g;        // [n_clusters][T][k]
   float* part_x;        // [n_clusters][T]
-  float* G;             // [T][k] projections (output)
-  float* rho;           // [T] or null
-  uint8_t* flags;       // [T]
-  int32_t* idx;         // [2T] compaction lists, or null
-  Ctrl* ctrl;
-  const char* pf_base;  // L2 prefetch of the image M (speculative fast path)
-  uint64_t pf_share;    // bytes per CTA (multiple of 16), 0 = off
-  uint64_t pf_total;
-  uint64_t gram_share;  // L2 prefetch of the Gram: bytes per CTA (multiple of 16), 0 = off
 };
 
-struct ApplyArgs {
+// Decide-and-apply kernel arguments (see gsi_apply.cu).
+struct DecideArgs {
+  const void* X;        // T x d
   const void* W;        // d_out x d
   const void* M;        // d_out x k
-  const void* X;        // T x d
-  const float* G;       // T x k
-  float* Y;             // T x d_out
-  const int32_t* idx;   // [2T]
-  const Ctrl* ctrl;
+  const float* gram;    // k x k, or null (orthonormal)
+  const float* part_g;  // [nclu][T][k] projection partials
+  const float* part_x;  // [nclu][T]
+  int nclu;
   int64_t d, d_out;
-  int k, T;
-  int rows_slow;
-  int64_t fast_units, slow_units;
-  int x_stage_max, g_stage_max;
+  int k, T, ks;
+  float eps;
+  int mode;             // 0 decide + apply, 1 decide only, 2 apply a stored decision
+  float* Y;             // T x d_out (modes 0, 2)
+  float* G;             // T x k projections out (mode 1), or null
+  float* rho;           // T, or null
+  uint8_t* flags;       // T flags out (modes 0, 1)
+  int32_t* idx;         // 2T compaction (mode 1)
+  int32_t* counts;      // 2 (mode 1)
+  const float* Gin;     // T x k stored projections (mode 2)
+  const uint8_t* flags_in;  // T stored flags (mode 2)
+  int rows_per_cta, seg_bytes, wstages, x_stage_max, stage_m;
+  int off_m, off_x, off_g;
+  uint32_t* err;
 };
+
 
 // Tensor-core path (bf16, prefill-sized T).  All pointers are device pointers;
 // Vt, G, Gbf, Gfast, Xslow and idx live in the call's workspace.
@@ -79,8 +80,8 @@ cudaError_t launch_gate(const GateArgs& a, const GatePlan& p, gsi_dtype dt, cuda
                         bool pdl);
 cudaError_t launch_compact(const uint8_t* flags, int T, int32_t* idx, int32_t* counts,
                            cudaStream_t s);
-cudaError_t launch_apply(const ApplyArgs& a, const ApplyPlan& p, gsi_dtype dt, int nsm,
-                         cudaStream_t s, bool pdl);
+cudaError_t launch_decide_apply(const DecideArgs& a, const DecidePlan& p, gsi_dtype dt, cudaStream_t s);
+int decide_apply_max_clusters(const DecidePlan& p, gsi_dtype dt);
 cudaError_t launch_image(const void* W, const void* V, void* M, float* gram, int64_t d,
                          int64_t d_out, int64_t k, gsi_dtype dt, cudaStream_t s);
 

@@ -9,8 +9,8 @@
 namespace gsi {
 
 constexpr int kClusterSize = 8;     // CTAs per cluster in the gate kernel
-constexpr int kGateThreads = 256;
-constexpr int kApplyThreads = 256;
+constexpr int kGateThreads = 128;  // small enough to share an SM with a decide-and-apply CTA
+constexpr int kApplyThreads = 288;  // 8 consumer warps + 1 copy-producer warp
 constexpr int kGateMaxRowsPerThread = 8;
 constexpr int kGateTargetSlabs = 256;
 
@@ -49,7 +49,8 @@ inline GatePlan plan_gate(int64_t d, int64_t k, int elem_bytes, int64_t T) {
   // main loop:  xs[tc][rs] + red[nrg][tc][k] + pg[tc][k] + px[tc]
   // finalizer (aliases red): gsl[tc][ks] + gfull[tc][k] + q/ng partials
   size_t main_b = size_t(p.tc) * p.rs * 4 + size_t(p.nrg) * p.tc * k * 4 +
-                  size_t(p.tc) * k * 4 + size_t(p.tc) * 4;
+                  size_t(p.tc) * k * 4 + size_t(p.tc) * 4 +
+                  size_t(kClusterSize) * p.tc * (p.ks + 1) * 4;
   size_t fin_b = size_t(p.tc) * p.rs * 4 + size_t(p.tc) * p.ks * 4 + 16 + size_t(p.tc) * k * 4 +
                  size_t(p.tc) * k * 4 + size_t(p.tc) * 4 + 2 * 8 * size_t(p.tc) * 4 + 64;
   p.smem = (main_b > fin_b ? main_b : fin_b) + 64;
@@ -58,7 +59,7 @@ inline GatePlan plan_gate(int64_t d, int64_t k, int elem_bytes, int64_t T) {
 
 // Workspace layout of one stream-path call (offsets in bytes, 256-aligned).
 struct StreamLayout {
-  size_t ctrl, part_g, part_x, g, idx, total;
+  size_t ctrl, part_g, part_x, g, idx, flags, total;
 };
 
 inline StreamLayout layout_stream(int64_t d, int64_t k, int elem_bytes, int64_t T) {
@@ -70,6 +71,7 @@ inline StreamLayout layout_stream(int64_t d, int64_t k, int elem_bytes, int64_t 
   L.part_x = off;  off += align256(size_t(p.n_clusters) * T * 4);
   L.g = off;       off += align256(size_t(T) * k * 4);
   L.idx = off;     off += align256(size_t(2) * T * 4);
+  L.flags = off;   off += align256(size_t(T));
   L.total = off;
   return L;
 }
@@ -96,33 +98,54 @@ inline TensorLayout layout_tensor(int64_t d, int64_t k, int64_t T) {
 // Token count from which GSI_PATH_AUTO uses the tensor cores for bf16 maps.
 constexpr int64_t kTensorMinT = 128;
 
-// Apply kernel geometry: fast units are `rows_fast` rows of M, slow units
-// `rows_slow` rows of W, each handled by one warp.
-struct ApplyPlan {
-  int vplm;        // 16-byte vectors of an M row per lane (1, 2 or 4)
-  int rows_fast;   // M rows per fast unit (16 / vplm)
-  int rows_slow;   // W rows per slow unit
-  int64_t fast_units, slow_units;
-  int x_stage_tokens_max;  // slow tokens whose x fits the staging budget
-  int g_stage_tokens_max;  // fast tokens whose g fits the staging budget
+// Decide-and-apply kernel geometry (see gsi_apply.cu).  The device part
+// (how many CTAs are co-resident) comes in as ncta; everything else is
+// arithmetic on the shapes.  Each CTA owns rows_per_cta contiguous output
+// rows.  Its nine warps stream their own W rows in seg_bytes segments through
+// private rings of wstages slots; the rings share one shared-memory region
+// with the staged M rows (a call's fast rows are computed before its slow
+// rows stream).
+struct DecidePlan {
+  int tc, grv, ncta, rows_per_cta, seg_bytes, wstages, x_stage_max, stage_m;
+  int off_m, off_x, off_g;
   size_t smem;
+  bool ok;
 };
 
-constexpr size_t kApplyXStage = 64 * 1024;
-constexpr size_t kApplyGStage = 32 * 1024;
+constexpr int kSegBytes = 4096;
+constexpr int kWarpStages = 4;
+constexpr int kXStage = 32 * 1024;
 
-inline ApplyPlan plan_apply(int64_t d, int64_t d_out, int64_t k, int elem_bytes) {
-  ApplyPlan p{};
-  int64_t nvm = k * elem_bytes / 16;
-  p.vplm = nvm <= 32 ? 1 : nvm <= 64 ? 2 : 4;
-  p.rows_fast = 16 / p.vplm;
-  int64_t row_b = d * elem_bytes;
-  p.rows_slow = row_b >= 8192 ? 1 : int(8192 / row_b);
-  p.fast_units = cdiv(d_out, p.rows_fast);
-  p.slow_units = cdiv(d_out, p.rows_slow);
-  p.x_stage_tokens_max = int(kApplyXStage / size_t(row_b));
-  p.g_stage_tokens_max = int(kApplyGStage / size_t(k * 4));
-  p.smem = kApplyXStage + kApplyGStage;
+inline DecidePlan plan_decide(int64_t d, int64_t d_out, int64_t k, int es, int64_t T, int ncta,
+                              size_t smem_budget) {
+  DecidePlan p{};
+  p.ok = true;
+  p.tc = T >= 8 ? 8 : T >= 4 ? 4 : T >= 2 ? 2 : 1;
+  const int64_t ks = cdiv(k, kClusterSize);
+  const int64_t gvec = ks * k / 4;
+  p.grv = gvec <= 8 * 256 ? 8 : 0;
+  const int64_t row_b = d * es;
+  p.seg_bytes = int(row_b < kSegBytes ? row_b : kSegBytes);
+  p.wstages = kWarpStages;
+  const size_t ring = size_t(kApplyThreads / 32) * p.wstages * p.seg_bytes;
+  const int64_t xs = kXStage / row_b;
+  p.x_stage_max = int(xs < p.tc ? xs : p.tc);
+  const size_t g_area = (size_t(p.tc) * k + size_t(p.tc) * ks + 40 * size_t(p.tc) + 40) * 4;
+  const size_t bars = size_t(kApplyThreads / 32) * p.wstages * 8 + 8;
+  size_t off = (bars + 127) & ~size_t(127);
+  p.off_x = int(off);
+  off += size_t(p.x_stage_max) * row_b;
+  off = (off + 127) & ~size_t(127);
+  p.off_g = int(off);
+  off += g_area;
+  off = (off + 127) & ~size_t(127);
+  p.off_m = int(off);
+  p.ncta = ncta;
+  p.rows_per_cta = int(cdiv(d_out, ncta));
+  const size_t m_bytes = size_t(p.rows_per_cta) * k * es;
+  p.stage_m = off + (m_bytes > ring ? m_bytes : ring) <= smem_budget ? 1 : 0;
+  p.smem = off + (p.stage_m && m_bytes > ring ? m_bytes : ring);
+  p.ok = p.smem <= smem_budget;
   return p;
 }
 
