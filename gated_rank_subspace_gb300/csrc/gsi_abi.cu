@@ -229,6 +229,7 @@ static gsi_status run_decide(const gsi_map_desc* m, const void* X, int64_t T, fl
   a.off_m = dp.off_m;
   a.off_x = dp.off_x;
   a.off_g = dp.off_g;
+  a.off_gram = dp.off_gram;
   a.err = &ctrl->err;
   s = cuda_check(launch_decide_apply(a, dp, m->dtype, st), "decide-and-apply kernel launch");
   if (s != GSI_OK || mode != 1 || !flags) return s;
@@ -258,6 +259,14 @@ static gsi_status run_stream(const gsi_map_desc* m, const void* X, int64_t T, fl
   ga.n_clusters = gp.n_clusters;
   ga.part_g = reinterpret_cast<float*>(base + L.part_g);
   ga.part_x = reinterpret_cast<float*>(base + L.part_x);
+  if (apply) {
+    ga.pf_m = static_cast<const char*>(m->M);
+    ga.pf_m_bytes = uint64_t(m->d_out) * m->k * es;
+  }
+  if (m->gram) {
+    ga.pf_g = reinterpret_cast<const char*>(m->gram);
+    ga.pf_g_bytes = uint64_t(m->k) * m->k * 4;
+  }
   gsi_status s = cuda_check(launch_gate(ga, gp, m->dtype, st, true), "projection kernel launch");
   if (s != GSI_OK) return s;
   return run_decide(m, X, T, eps, apply ? 0 : 1, Y, flags, rho, G_out, nullptr, ws, st);

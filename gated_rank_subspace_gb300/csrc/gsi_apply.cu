@@ -94,6 +94,8 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kApplyThr
   // shared-memory carve-up (offsets computed on the host, see plan_decide)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);          // [9 warps][wstages]
   uint64_t* mfull = full + (kApplyThreads / 32) * a.wstages;   // [1]
+  uint64_t* gfull_bar = mfull + 1;                             // [1] Gram slice copy
+  const float* gram_s = reinterpret_cast<const float*>(smem + a.off_gram);
   unsigned char* Ms = smem + a.off_m;                          // staged M rows / W rings
   unsigned char* xst = smem + a.off_x;                         // staged x of slow tokens
   float* gfull = reinterpret_cast<float*>(smem + a.off_g);     // [TC][k]
@@ -114,6 +116,7 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kApplyThr
   if (tid == 0) {
     for (int s = 0; s < (kApplyThreads / 32) * a.wstages; ++s) bar_init(&full[s], 1);
     bar_init(mfull, 1);
+    bar_init(gfull_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -123,7 +126,17 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kApplyThr
     bar_expect_tx(mfull, bytes);
     bulk_g2s(Ms, static_cast<const char*>(a.M) + r0 * mrow_b, bytes, mfull);
   }
-  // Gram slice rows [c0, c1) into registers (GRV float4 per thread)
+  // Gram slice rows [c0, c1) into shared memory (bulk copy, overlaps the wait)
+  const int k4_ = k >> 2;
+  const int gvec_ = (c1 > c0) ? (c1 - c0) * k4_ : 0;
+  const bool gram_smem = a.off_gram != 0 && a.gram && a.mode != 2 && gvec_ > 0;
+  if (gram_smem && tid == kApplyThreads - 32) {
+    const uint32_t bytes = uint32_t(gvec_) * 16u;
+    bar_expect_tx(gfull_bar, bytes);
+    bulk_g2s(smem + a.off_gram, a.gram + int64_t(c0) * k, bytes, gfull_bar);
+  }
+  bool gram_waited = false;
+  // (alternative when the slice does not fit: GRV float4 registers per thread)
   float4 gr[GRV > 0 ? GRV : 1];
   const int k4 = k >> 2;
   const int gvec = (c1 > c0) ? (c1 - c0) * k4 : 0;
@@ -131,11 +144,14 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kApplyThr
 #pragma unroll
     for (int u = 0; u < (GRV > 0 ? GRV : 1); ++u) {
       const int v = u * 256 + tid;
-      gr[u] = v < gvec ? __ldg(reinterpret_cast<const float4*>(a.gram + int64_t(c0 + v / k4) * k) + (v % k4))
-                       : make_float4(0.f, 0.f, 0.f, 0.f);
+      // volatile loads: issued here, before the dependency wait, not sunk to their use
+      uint4 raw = v < gvec ? ld_weight_v4(a.gram + (int64_t(c0 + v / k4) * k + 4 * (v % k4)))
+                           : make_uint4(0u, 0u, 0u, 0u);
+      gr[u] = make_float4(__uint_as_float(raw.x), __uint_as_float(raw.y), __uint_as_float(raw.z),
+                          __uint_as_float(raw.w));
     }
   }
-  if (GRV == 0 && a.gram && a.mode != 2 && tid == 0 && gvec > 0)
+  if (GRV == 0 && !gram_smem && a.gram && a.mode != 2 && tid == 0 && gvec > 0)
     prefetch_l2(a.gram + int64_t(c0) * k, uint32_t(gvec) * 16u);  // read after the wait
   cluster_arrive_relaxed();
   pdl_wait();
@@ -211,7 +227,23 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kApplyThr
 #pragma unroll
           for (int t = 0; t < TC; ++t) na[t] = fmaf(gfull[t * k + i], gfull[t * k + i], na[t]);
         }
-        if (a.gram) {
+        if (a.gram && gram_smem) {
+          if (!gram_waited && !bar_wait(gfull_bar, 0, a.err)) ok = false;
+          gram_waited = true;
+          for (int v = tid; v < gvec; v += 256) {
+            const float4 gv = reinterpret_cast<const float4*>(gram_s)[v];
+            const int i = c0 + v / k4, j = 4 * (v % k4);
+#pragma unroll
+            for (int t = 0; t < TC; ++t) {
+              const float4 gj = *reinterpret_cast<const float4*>(gfull + t * k + j);
+              float h = gv.x * gj.x;
+              h = fmaf(gv.y, gj.y, h);
+              h = fmaf(gv.z, gj.z, h);
+              h = fmaf(gv.w, gj.w, h);
+              qa[t] = fmaf(gfull[t * k + i], h, qa[t]);
+            }
+          }
+        } else if (a.gram) {
           if (GRV > 0) {
 #pragma unroll
             for (int u = 0; u < (GRV > 0 ? GRV : 1); ++u) {
@@ -481,6 +513,7 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kApplyThr
     if (warp == 0) compact_warp(a.flags, T, a.idx, a.counts, lane);
   }
   if (!started) cluster_wait();
+  if (gram_smem && tid < 256 && !gram_waited) bar_wait(gfull_bar, 0, a.err);
   // bounded drain of the M copy if it was never waited for
   if (stage_m && !m_waited && tid == 0) bar_wait(mfull, 0, a.err);
 }
@@ -509,10 +542,7 @@ static cudaError_t launch_da_t(const DecideArgs& a, const DecidePlan& p, cudaStr
 
 template <class E, int TC>
 static cudaError_t launch_da_tc(const DecideArgs& a, const DecidePlan& p, cudaStream_t s) {
-  switch (p.grv) {
-    case 8: return launch_da_t<E, TC, 8>(a, p, s);
-    default: return launch_da_t<E, TC, 0>(a, p, s);
-  }
+  return launch_da_t<E, TC, 0>(a, p, s);
 }
 
 template <class E>
@@ -532,7 +562,7 @@ cudaError_t launch_decide_apply(const DecideArgs& a, const DecidePlan& p, gsi_dt
 // Co-resident clusters of the decide-and-apply kernel for a plan (grid size).
 template <class E>
 static int max_clusters_e(const DecidePlan& p) {
-  auto kern = decide_apply_kernel<E, 1, 8>;
+  auto kern = decide_apply_kernel<E, 1, 0>;
   if (set_kernel_smem(kern, p.smem) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(kClusterSize * 64);

@@ -40,6 +40,19 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kGateThre
 
   // ---- prologue: read-only weights only (may overlap the previous kernel)
   pdl_launch_dependents();
+  if (tid == 0 || tid == 32) {
+    // this CTA's share of M (thread 0) or of the Gram (thread 32), into L2
+    const char* base = tid == 0 ? a.pf_m : a.pf_g;
+    const uint64_t total = tid == 0 ? a.pf_m_bytes : a.pf_g_bytes;
+    if (base && total) {
+      const uint64_t share = ((total + gridDim.x - 1) / gridDim.x + 15) / 16 * 16;
+      const uint64_t off = uint64_t(blockIdx.x) * share;
+      if (off < total) {
+        const uint64_t rem = total - off;
+        prefetch_l2(base + off, uint32_t(rem < share ? rem : share));
+      }
+    }
+  }
   const int rg = tid / nv, v = tid - (tid / nv) * nv;
   const bool active = rg < nrg;
   uint4 vreg[kGateMaxRowsPerThread];

@@ -19,6 +19,12 @@ struct GateArgs {
   int rs, nv, nrg, ks, n_clusters;
   float* part_g;        // [n_clusters][T][k]
   float* part_x;        // [n_clusters][T]
+  // Speculative L2 prefetch, for the decide-and-apply kernel that follows:
+  // the image M (most tokens take the fast path) and the Gram matrix.
+  const char* pf_m;
+  uint64_t pf_m_bytes;
+  const char* pf_g;
+  uint64_t pf_g_bytes;
 };
 
 // Decide-and-apply kernel arguments (see gsi_apply.cu).
@@ -43,7 +49,7 @@ struct DecideArgs {
   const float* Gin;     // T x k stored projections (mode 2)
   const uint8_t* flags_in;  // T stored flags (mode 2)
   int rows_per_cta, seg_bytes, wstages, x_stage_max, stage_m;
-  int off_m, off_x, off_g;
+  int off_m, off_x, off_g, off_gram;
   uint32_t* err;
 };
 

@@ -107,14 +107,14 @@ constexpr int64_t kTensorMinT = 128;
 // rows stream).
 struct DecidePlan {
   int tc, grv, ncta, rows_per_cta, seg_bytes, wstages, x_stage_max, stage_m;
-  int off_m, off_x, off_g;
+  int off_m, off_x, off_g, off_gram;  // off_gram = 0: Gram slice read from global
   size_t smem;
   bool ok;
 };
 
 constexpr int kSegBytes = 4096;
 constexpr int kWarpStages = 4;
-constexpr int kXStage = 32 * 1024;
+constexpr int kXStage = 16 * 1024;
 
 inline DecidePlan plan_decide(int64_t d, int64_t d_out, int64_t k, int es, int64_t T, int ncta,
                               size_t smem_budget) {
@@ -122,8 +122,7 @@ inline DecidePlan plan_decide(int64_t d, int64_t d_out, int64_t k, int es, int64
   p.ok = true;
   p.tc = T >= 8 ? 8 : T >= 4 ? 4 : T >= 2 ? 2 : 1;
   const int64_t ks = cdiv(k, kClusterSize);
-  const int64_t gvec = ks * k / 4;
-  p.grv = gvec <= 8 * 256 ? 8 : 0;
+  p.grv = 0;  // Gram slice comes from shared memory (or global when it does not fit)
   const int64_t row_b = d * es;
   p.seg_bytes = int(row_b < kSegBytes ? row_b : kSegBytes);
   p.wstages = kWarpStages;
@@ -131,8 +130,15 @@ inline DecidePlan plan_decide(int64_t d, int64_t d_out, int64_t k, int es, int64
   const int64_t xs = kXStage / row_b;
   p.x_stage_max = int(xs < p.tc ? xs : p.tc);
   const size_t g_area = (size_t(p.tc) * k + size_t(p.tc) * ks + 40 * size_t(p.tc) + 40) * 4;
-  const size_t bars = size_t(kApplyThreads / 32) * p.wstages * 8 + 8;
+  const size_t bars = size_t(kApplyThreads / 32) * p.wstages * 8 + 16;
   size_t off = (bars + 127) & ~size_t(127);
+  // Gram slice of one cluster rank (ks rows of k floats), staged by a bulk copy
+  const size_t gram_b = size_t(ks) * k * 4;
+  p.off_gram = 0;
+  if (gram_b <= 40 * 1024) {
+    p.off_gram = int(off);
+    off += (gram_b + 127) & ~size_t(127);
+  }
   p.off_x = int(off);
   off += size_t(p.x_stage_max) * row_b;
   off = (off + 127) & ~size_t(127);

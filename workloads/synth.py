@@ -227,3 +227,36 @@ def stack_layer(config: int, layer: int, basis_by_role: dict, shapes: dict,
 def config5(T: int = 2048, n_slow: int = 410) -> MapInputs:
     """Prefill-sized map: T=2048, d=4096, d_out=16384, k=256, 410 slow tokens."""
     return map_6b("up", T=T, n_slow=n_slow, k=256, config=5)
+
+
+def layer_weight_rows(config: int, layer: int, role: int, d_out: int):
+    """Seeded row permutation and signs that derive layer `layer`'s W from its
+    role's base Gaussian draw (W_l = S_l P_l W_base): still N(0, 1/fan_in),
+    distinct per layer, and cheap to form for deep stacks."""
+    g = rng(config, layer, role, _W * 1000 + 7)
+    perm = g.permutation(d_out)
+    signs = np.where(g.random(d_out) < 0.5, -1.0, 1.0).astype(np.float32)
+    return perm, signs
+
+
+def stack_config3(n_layers: int = 28, steps: int = 512, k: int = 256, eps: float = EPS):
+    """28-layer linear-only stack of the 6B shapes with depth-coherent bases.
+
+    Returns (bases, fractions, base_W, tokens): bases[role][l] float64 d x k,
+    fractions[l] the layer's slow-token fraction, base_W[role] the role's
+    base weight draw (bf16 tensor), tokens[(l, role)] a steps x d bf16 tensor
+    of per-step activations in span(V^(l)) plus noise.
+    """
+    c = 3
+    fr = layer_slow_fractions(c, n_layers)
+    bases, base_W = {}, {}
+    for role in ROLES:
+        d_out, d = SHAPES_6B[role]
+        r = ROLE_ID[role]
+        bases[role] = depth_chain(c, r, d, k, n_layers)
+        base_W[role] = storage(gaussian_weight(rng(c, 0, r, _W), d_out, d), torch.bfloat16)
+    tokens = {}
+    for l in range(n_layers):
+        for role in ROLES:
+            tokens[(l, role)] = map_tokens(c, l, ROLE_ID[role], bases[role][l], steps, float(fr[l]), eps)
+    return bases, fr, base_W, tokens
