@@ -231,11 +231,8 @@ static gsi_status run_decide(const gsi_map_desc* m, const void* X, int64_t T, fl
   a.off_g = dp.off_g;
   a.off_gram = dp.off_gram;
   a.err = &ctrl->err;
-  s = cuda_check(launch_decide_apply(a, dp, m->dtype, st), "decide-and-apply kernel launch");
-  if (s != GSI_OK || mode != 1 || !flags) return s;
-  // gsi_gate: the caller's flags are a copy of the stored decision
-  return cuda_check(cudaMemcpyAsync(flags, base + L.flags, size_t(T), cudaMemcpyDeviceToDevice, st),
-                    "flags copy");
+  a.flags_user = mode == 1 ? flags : nullptr;  // gsi_gate: also the caller's copy
+  return cuda_check(launch_decide_apply(a, dp, m->dtype, st), "decide-and-apply kernel launch");
 }
 
 // Enqueue the projection kernel, then (mode) the decide-and-apply kernel.

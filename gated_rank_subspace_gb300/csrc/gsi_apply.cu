@@ -318,6 +318,7 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kApplyThr
           if (blockIdx.x == 0) {
             if (a.rho) a.rho[t0 + tid] = rho;
             a.flags[t0 + tid] = uint8_t(slow);
+            if (a.flags_user) a.flags_user[t0 + tid] = uint8_t(slow);
           }
         }
         sflag[tid] = slow;

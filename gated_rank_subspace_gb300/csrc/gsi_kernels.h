@@ -44,6 +44,7 @@ struct DecideArgs {
   float* G;             // T x k projections out (mode 1), or null
   float* rho;           // T, or null
   uint8_t* flags;       // T flags out (modes 0, 1)
+  uint8_t* flags_user;  // mode 1: the caller's flags (a copy of the stored ones), or null
   int32_t* idx;         // 2T compaction (mode 1)
   int32_t* counts;      // 2 (mode 1)
   const float* Gin;     // T x k stored projections (mode 2)
