@@ -112,15 +112,38 @@ static gsi_status check_workspace(const void* ws, size_t have, size_t need) {
   return GSI_OK;
 }
 
-// Resolve the path for a call: the tensor cores for bf16 maps at
-// prefill-sized T, the streaming kernels otherwise.
+// Per-block shared memory a kernel may opt into on sm_100-class GPUs (bytes).
+constexpr size_t kSmemOptinSm100 = 232448;
+
+// The fused decode kernel handles T <= 2 when one cluster rank's slice of V
+// (with 16 ranks) fits in shared memory beside its working buffers.
+// Host-only arithmetic, so workspace sizing needs no device.
+static bool fused_fits(const gsi_map_desc* m, int64_t T) {
+  if (T < 1 || T > 2) return false;
+  const int es = elem_bytes(m->dtype);
+  if (m->k * es / 4 > kApplyThreads) return false;  // one thread per 4-byte word of a V row
+  const DecidePlan p = plan_decide(m->d, m->d_out, m->k, es, T, 1 << 20, kSmemOptinSm100, true, 16);
+  return p.ok;
+}
+
+// Resolve the path for a call: the single-launch decode for T <= 2 where it
+// fits, the tensor cores for bf16 maps at prefill-sized T, the two-launch
+// streaming kernels otherwise.
 static gsi_status resolve_path(const gsi_map_desc* m, int64_t T, gsi_path path, gsi_path* out) {
   if (path == GSI_PATH_AUTO) {
+    // (the fused decode is not chosen automatically: measured, its V-slice
+    // projection costs as much as the second launch it saves)
     *out = (m->dtype == GSI_BF16 && T >= kTensorMinT) ? GSI_PATH_TENSOR : GSI_PATH_STREAM;
     return GSI_OK;
   }
   if (path == GSI_PATH_STREAM) {
     *out = GSI_PATH_STREAM;
+    return GSI_OK;
+  }
+  if (path == GSI_PATH_FUSED) {
+    if (!fused_fits(m, T))
+      return fail(GSI_ERR_UNSUPPORTED, "the fused decode takes T <= 2 and a slice of V that fits shared memory");
+    *out = GSI_PATH_FUSED;
     return GSI_OK;
   }
   if (path == GSI_PATH_TENSOR) {
@@ -132,6 +155,9 @@ static gsi_status resolve_path(const gsi_map_desc* m, int64_t T, gsi_path path, 
   return fail(GSI_ERR_INVALID_ARG, "unknown path %d", int(path));
 }
 
+// Workspace of a path.  The fused decode uses only the control block, but it
+// is sized like the streaming path so a device that cannot run it can fall
+// back to the two-launch kernels on the same workspace.
 static size_t path_ws(const gsi_map_desc* m, int64_t T, gsi_path p) {
   if (p == GSI_PATH_TENSOR) return layout_tensor(m->d, m->k, T).total;
   return layout_stream(m->d, m->k, m->dtype == GSI_BF16 ? 2 : 4, T).total;
@@ -141,14 +167,18 @@ static size_t stream_ws(const gsi_map_desc* m, int64_t T) {
   return layout_stream(m->d, m->k, elem_bytes(m->dtype), T).total;
 }
 
-// Device facts the decide-and-apply plan needs, queried once per device.
+// Device facts the decide-and-apply plans need, queried once per device.
 struct DeviceFacts {
   int nsm = 0;
   int smem_optin = 0;
-  int clusters[2] = {0, 0};  // co-resident decide-and-apply clusters per dtype
+  int clusters[2][2][2] = {};  // co-resident clusters per [dtype][fused][cs == 16]; -1: not possible
 };
 
-static gsi_status device_facts(gsi_dtype dt, size_t smem_budget, DeviceFacts** out) {
+// Shared memory of the two-launch decide-and-apply kernel: the device limit
+// less room for one CTA of the next projection kernel, which starts early.
+static size_t decide_smem_budget(int smem_optin) { return size_t(smem_optin) - 16 * 1024; }
+
+static gsi_status device_facts(DeviceFacts** out) {
   static DeviceFacts facts[64];
   static std::mutex mu;
   int dev = 0;
@@ -162,42 +192,60 @@ static gsi_status device_facts(gsi_dtype dt, size_t smem_budget, DeviceFacts** o
     if ((e = cudaDeviceGetAttribute(&f.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
       return cuda_check(e, "shared memory limit");
   }
-  const int di = dt == GSI_BF16 ? 1 : 0;
-  if (smem_budget > 0 && f.clusters[di] == 0) {
-    DecidePlan q{};
-    q.smem = smem_budget;
-    const int n = decide_apply_max_clusters(q, dt);
-    if (n <= 0) return fail(GSI_ERR_CUDA, "cannot size the decide-and-apply grid (cluster occupancy query failed)");
-    f.clusters[di] = n;
-  }
   *out = &f;
   return GSI_OK;
 }
 
-// Shared memory the decide-and-apply kernel may use: the device limit less
-// room for one CTA of the next projection kernel, which starts early.
-static size_t decide_smem_budget(int smem_optin) { return size_t(smem_optin) - 16 * 1024; }
+// Co-resident clusters for a decide-and-apply variant (cached); 0 if none.
+static int decide_clusters(DeviceFacts* f, gsi_dtype dt, bool fused, int cs) {
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  int& c = f->clusters[dt == GSI_BF16][fused][cs == 16];
+  if (c == 0) {
+    const size_t smem = fused ? size_t(f->smem_optin) : decide_smem_budget(f->smem_optin);
+    const int n = decide_apply_max_clusters(smem, dt, fused, cs);
+    c = n > 0 ? n : -1;
+  }
+  return c > 0 ? c : 0;
+}
 
 // Enqueue the decide-and-apply kernel for one map (all arguments validated).
 // mode 0: decide and apply (gsi_linear); 1: decide only (gsi_gate, writes
 // G, rho, flags and the compaction); 2: apply the decision stored by a
 // preceding gsi_gate on the same workspace (gsi_apply).
+// fused: the single-launch decode (mode 0 only; the cluster projects x on
+// its own slices of V).  next: the map that follows in a stack, whose
+// weights are staged in L2 while this one runs (nullable).  Returns
+// GSI_ERR_UNSUPPORTED before launching anything when the fused decode cannot
+// run on this device, so that callers may fall back to the two launches.
 static gsi_status run_decide(const gsi_map_desc* m, const void* X, int64_t T, float eps, int mode, float* Y,
-                             uint8_t* flags, float* rho, float* G, const float* Gin, void* ws, cudaStream_t st) {
+                             uint8_t* flags, float* rho, float* G, const float* Gin, void* ws, cudaStream_t st,
+                             bool fused = false, const gsi_map_desc* next = nullptr) {
   const int es = elem_bytes(m->dtype);
   const GatePlan gp = plan_gate(m->d, m->k, es, T);
   const StreamLayout L = layout_stream(m->d, m->k, es, T);
   char* base = static_cast<char*>(ws);
   Ctrl* ctrl = reinterpret_cast<Ctrl*>(base + L.ctrl);
-  DeviceFacts* f = nullptr;
-  gsi_status s = device_facts(GSI_F32, 0, &f);
-  if (s != GSI_OK) return s;
-  const size_t budget = decide_smem_budget(f->smem_optin);
-  if ((s = device_facts(m->dtype, budget, &f)) != GSI_OK) return s;
-  const DecidePlan dp = plan_decide(m->d, m->d_out, m->k, es, T, f->clusters[m->dtype == GSI_BF16 ? 1 : 0] * kClusterSize,
-                                    budget);
-  if (!dp.ok) return fail(GSI_ERR_UNSUPPORTED, "the streaming kernels' shared memory does not fit this map");
   if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
+  DeviceFacts* f = nullptr;
+  gsi_status s = device_facts(&f);
+  if (s != GSI_OK) return s;
+  DecidePlan dp{};
+  if (fused) {
+    int cs = 16;
+    int nc = decide_clusters(f, m->dtype, true, 16);
+    if (nc == 0) {
+      cs = 8;
+      nc = decide_clusters(f, m->dtype, true, 8);
+    }
+    if (nc > 0) dp = plan_decide(m->d, m->d_out, m->k, es, T, nc * cs, size_t(f->smem_optin), true, cs);
+    if (nc == 0 || !dp.ok) return fail(GSI_ERR_UNSUPPORTED, "the fused decode does not fit this device");
+  } else {
+    const int nc = decide_clusters(f, m->dtype, false, kClusterSize);
+    if (nc == 0) return fail(GSI_ERR_CUDA, "cannot size the decide-and-apply grid (cluster occupancy query failed)");
+    dp = plan_decide(m->d, m->d_out, m->k, es, T, nc * kClusterSize, decide_smem_budget(f->smem_optin));
+    if (!dp.ok) return fail(GSI_ERR_UNSUPPORTED, "the streaming kernels' shared memory does not fit this map");
+  }
   DecideArgs a{};
   a.X = X;
   a.W = m->W;
@@ -210,7 +258,7 @@ static gsi_status run_decide(const gsi_map_desc* m, const void* X, int64_t T, fl
   a.d_out = m->d_out;
   a.k = int(m->k);
   a.T = int(T);
-  a.ks = gp.ks;
+  a.ks = dp.ks;
   a.eps = eps;
   a.mode = mode;
   a.Y = Y;
@@ -230,6 +278,20 @@ static gsi_status run_decide(const gsi_map_desc* m, const void* X, int64_t T, fl
   a.off_x = dp.off_x;
   a.off_g = dp.off_g;
   a.off_gram = dp.off_gram;
+  a.V = m->V;
+  a.v_rows = dp.v_rows;
+  a.ngrp = dp.ngrp;
+  a.off_v = dp.off_v;
+  a.off_xs = dp.off_xs;
+  if (next) {
+    const int nes = elem_bytes(next->dtype);
+    a.next_v = static_cast<const char*>(next->V);
+    a.next_v_bytes = uint64_t(next->d) * next->k * nes;
+    a.next_m = static_cast<const char*>(next->M);
+    a.next_m_bytes = uint64_t(next->d_out) * next->k * nes;
+    a.next_gram = reinterpret_cast<const char*>(next->gram);
+    a.next_gram_bytes = next->gram ? uint64_t(next->k) * next->k * 4 : 0;
+  }
   a.err = &ctrl->err;
   a.flags_user = mode == 1 ? flags : nullptr;  // gsi_gate: also the caller's copy
   return cuda_check(launch_decide_apply(a, dp, m->dtype, st), "decide-and-apply kernel launch");
@@ -237,7 +299,8 @@ static gsi_status run_decide(const gsi_map_desc* m, const void* X, int64_t T, fl
 
 // Enqueue the projection kernel, then (mode) the decide-and-apply kernel.
 static gsi_status run_stream(const gsi_map_desc* m, const void* X, int64_t T, float eps, float* Y,
-                             uint8_t* flags, float* rho, float* G_out, void* ws, cudaStream_t st, bool apply) {
+                             uint8_t* flags, float* rho, float* G_out, void* ws, cudaStream_t st, bool apply,
+                             const gsi_map_desc* next = nullptr) {
   const int es = elem_bytes(m->dtype);
   const GatePlan gp = plan_gate(m->d, m->k, es, T);
   const StreamLayout L = layout_stream(m->d, m->k, es, T);
@@ -266,8 +329,9 @@ static gsi_status run_stream(const gsi_map_desc* m, const void* X, int64_t T, fl
   }
   gsi_status s = cuda_check(launch_gate(ga, gp, m->dtype, st, true), "projection kernel launch");
   if (s != GSI_OK) return s;
-  return run_decide(m, X, T, eps, apply ? 0 : 1, Y, flags, rho, G_out, nullptr, ws, st);
+  return run_decide(m, X, T, eps, apply ? 0 : 1, Y, flags, rho, G_out, nullptr, ws, st, false, next);
 }
+
 
 // Enqueue the tensor-core path for one bf16 map.  All arguments validated.
 static gsi_status run_tensor(const gsi_map_desc* m, const void* X, int64_t T, float eps, float* Y,
@@ -299,6 +363,19 @@ static gsi_status run_tensor(const gsi_map_desc* m, const void* X, int64_t T, fl
   t.Y = Y;
   t.err = &ctrl->err;
   return cuda_check(launch_tensor_path(t, st), "tensor-core path launch");
+}
+
+// One gated map along a resolved path (fused falls back to the two-launch
+// streaming kernels when the device cannot run it and `strict` is false).
+static gsi_status run_path(const gsi_map_desc* m, gsi_path p, bool strict, const void* X, int64_t T, float eps,
+                           float* Y, uint8_t* flags, float* rho, void* ws, cudaStream_t st,
+                           const gsi_map_desc* next = nullptr) {
+  if (p == GSI_PATH_TENSOR) return run_tensor(m, X, T, eps, Y, flags, rho, ws, st);
+  if (p == GSI_PATH_FUSED) {
+    const gsi_status s = run_decide(m, X, T, eps, 0, Y, flags, rho, nullptr, nullptr, ws, st, true, next);
+    if (s != GSI_ERR_UNSUPPORTED || strict) return s;
+  }
+  return run_stream(m, X, T, eps, Y, flags, rho, nullptr, ws, st, true, next);
 }
 
 }  // namespace gsi
@@ -416,10 +493,8 @@ gsi_status gsi_linear_ex(const gsi_map_desc* map, const void* X, int64_t T, floa
   if (!flags) return fail(GSI_ERR_INVALID_ARG, "flags is NULL");
   if (rho && !aligned(rho, 4)) return fail(GSI_ERR_INVALID_ARG, "rho is misaligned");
   if ((s = check_workspace(workspace, ws_bytes, path_ws(map, T, p))) != GSI_OK) return s;
-  if (p == GSI_PATH_TENSOR)
-    s = run_tensor(map, X, T, eps, Y, flags, rho, workspace, static_cast<cudaStream_t>(stream));
-  else
-    s = run_stream(map, X, T, eps, Y, flags, rho, nullptr, workspace, static_cast<cudaStream_t>(stream), true);
+  s = run_path(map, p, path == GSI_PATH_FUSED, X, T, eps, Y, flags, rho, workspace,
+               static_cast<cudaStream_t>(stream));
   return s == GSI_OK ? ok() : s;
 }
 
@@ -469,10 +544,8 @@ gsi_status gsi_stack(const gsi_map_desc* maps, int64_t n_maps, const void* const
   for (int64_t i = 0; i < n_maps; ++i) {
     gsi_path p;
     resolve_path(&maps[i], T, GSI_PATH_AUTO, &p);
-    if (p == GSI_PATH_TENSOR)
-      s = run_tensor(&maps[i], X[i], T, eps, Y[i], flags[i], nullptr, workspace, st);
-    else
-      s = run_stream(&maps[i], X[i], T, eps, Y[i], flags[i], nullptr, nullptr, workspace, st, true);
+    s = run_path(&maps[i], p, false, X[i], T, eps, Y[i], flags[i], nullptr, workspace, st,
+                 i + 1 < n_maps ? &maps[i + 1] : nullptr);
     if (s != GSI_OK) return fail(s, "map %lld: %s", (long long)i, g_err.c_str());
   }
   return ok();

@@ -17,11 +17,11 @@
 // Each CTA owns a contiguous block of output rows.  Before the dependency
 // wait it copies its rows of M into shared memory (TMA bulk copy), so a fast
 // call only computes from shared memory once the gate is known.  Slow tokens
-// stream the CTA's rows of W through a ring of bulk copies (a producer warp,
-// eight consumer warps, mbarriers); each chunk of Rc rows is split into
-// 8 / Rc column segments, one per warp, and the segments' sums are added in
-// warp order.  Every wait on an mbarrier is bounded: on expiry the kernel
-// sets the workspace error word, drains its own copies (bounded) and returns.
+// stream the CTA's rows of W: each of the eight warps owns rows warp,
+// warp + 8, ... and pulls them in 4 KB segments through a private ring of bulk
+// copies completed on mbarriers; a row's sum is one warp's, in lane order.
+// Every wait on an mbarrier is bounded: on expiry the kernel sets the
+// workspace error word, drains its own copies (bounded) and returns.
 //
 // Modes: decide and apply (gsi_linear), decide only (gsi_gate: writes G,
 // rho, flags and the compaction), apply a stored decision (gsi_apply).
@@ -56,6 +56,7 @@ __device__ __forceinline__ bool bar_try(uint64_t* b, uint32_t parity) {
 }
 constexpr long long kSpinCycles = 4000000000LL;  // ~2 s at 2 GHz
 __device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t parity, uint32_t* err) {
+  if (bar_try(b, parity)) return true;
   const long long t0 = clock64();
   while (!bar_try(b, parity)) {
     if (clock64() - t0 > kSpinCycles) {
@@ -73,10 +74,17 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                : "memory");
 }
 
+template <bool B>
+struct BoolC {
+  static constexpr bool value = B;
+};
+
 // ------------------------------------------------------------------ kernel
-template <class E, int TC, int GRV>
-__global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kApplyThreads, 1)
-    decide_apply_kernel(DecideArgs a) {
+// FUSED: the cluster computes g = V_k^T x itself (one launch per call, T <= 2);
+// otherwise g comes from the projection kernel's cluster partials.
+// CS: CTAs per cluster (8, or 16 where the device allows it), set at launch.
+template <class E, int TC, int GRV, bool FUSED, int CS>
+__global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
   constexpr int PV = E::kPerVec;
   constexpr int NCW = 8;  // consumer warps
   extern __shared__ __align__(128) unsigned char smem[];
@@ -92,7 +100,7 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kApplyThr
   const int c0 = rank * ks, c1 = min(k, c0 + ks);
 
   // shared-memory carve-up (offsets computed on the host, see plan_decide)
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem);          // [9 warps][wstages]
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);          // [8 warps][wstages]
   uint64_t* mfull = full + (kApplyThreads / 32) * a.wstages;   // [1]
   uint64_t* gfull_bar = mfull + 1;                             // [1] Gram slice copy
   const float* gram_s = reinterpret_cast<const float*>(smem + a.off_gram);
@@ -102,14 +110,22 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kApplyThr
   float* gsl = gfull + TC * k;                                 // [TC][ks]
   float* qw = gsl + TC * ks;                                   // [8][TC]
   float* nw = qw + 8 * TC;                                     // [8][TC]
-  float* qin = nw + 8 * TC;                                    // [8 ranks][TC] pushed shares
-  float* nin = qin + kClusterSize * TC;                        // [8 ranks][TC]
-  float* nx2 = nin + kClusterSize * TC;                        // [TC]
+  float* qin = nw + 8 * TC;                                    // [CS ranks][TC] pushed shares
+  float* nin = qin + CS * TC;                                  // [CS ranks][TC]
+  float* nx2 = nin + CS * TC;                                  // [TC]
   float* rowpart = nx2 + TC;                                   // [8 warps][4]
   int* sflag = reinterpret_cast<int*>(rowpart + 8 * 4);        // [TC]
   int* slist = sflag + TC;                                     // [TC] slow tokens of the chunk
   int* flist = slist + TC;                                     // [TC] fast tokens of the chunk
   int* scount = flist + TC;                                    // [2]
+  // fused decode only: V slice, token slice, partial sums and inboxes
+  uint64_t* vbar = gfull_bar + 1;                              // [1] V slice copy
+  const unsigned char* Vs = smem + a.off_v;                    // [v_rows][k] elements
+  float* xsl = reinterpret_cast<float*>(smem + a.off_xs);      // [TC][v_rows]
+  float* red2 = xsl + TC * a.v_rows;                           // [ngrp][TC][k]
+  float* inbox = red2 + a.ngrp * TC * k;                       // [CS][TC][ks]
+  float* inbox_x = inbox + CS * TC * ks;                       // [CS][TC]
+  float* xsq = inbox_x + CS * TC;                              // [TC]
 
   // ---- prologue: only weights (may overlap the projection kernel)
   pdl_launch_dependents();
@@ -117,6 +133,7 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kApplyThr
     for (int s = 0; s < (kApplyThreads / 32) * a.wstages; ++s) bar_init(&full[s], 1);
     bar_init(mfull, 1);
     bar_init(gfull_bar, 1);
+    bar_init(gfull_bar + 1, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -136,6 +153,28 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kApplyThr
     bulk_g2s(smem + a.off_gram, a.gram + int64_t(c0) * k, bytes, gfull_bar);
   }
   bool gram_waited = false;
+  // fused decode: this rank's slice of V (rows [v0, v0 + vn)), one bulk copy
+  const int64_t v0 = int64_t(rank) * a.v_rows;
+  const int vn = FUSED ? int(v0 >= d ? 0 : (d - v0 < a.v_rows ? d - v0 : a.v_rows)) : 0;
+  if (FUSED && a.mode != 2 && vn > 0 && tid == kApplyThreads - 32) {
+    const uint32_t bytes = uint32_t(vn) * uint32_t(mrow_b);
+    bar_expect_tx(vbar, bytes);
+    bulk_g2s(smem + a.off_v, static_cast<const char*>(a.V) + v0 * mrow_b, bytes, vbar);
+  }
+  bool v_waited = !(FUSED && a.mode != 2 && vn > 0);
+  // weights of the next map of a stack, into L2 (this CTA's share)
+  if (tid == 64 || tid == 96 || tid == 128) {
+    const char* base = tid == 64 ? a.next_v : tid == 96 ? a.next_m : a.next_gram;
+    const uint64_t total = tid == 64 ? a.next_v_bytes : tid == 96 ? a.next_m_bytes : a.next_gram_bytes;
+    if (base && total) {
+      const uint64_t share = ((total + gridDim.x - 1) / gridDim.x + 15) / 16 * 16;
+      const uint64_t off = uint64_t(blockIdx.x) * share;
+      if (off < total) {
+        const uint64_t rem = total - off;
+        prefetch_l2(base + off, uint32_t(rem < share ? rem : share));
+      }
+    }
+  }
   // (alternative when the slice does not fit: GRV float4 registers per thread)
   float4 gr[GRV > 0 ? GRV : 1];
   const int k4 = k >> 2;
@@ -167,7 +206,88 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kApplyThr
 
   for (int t0 = 0; t0 < T; t0 += TC) {
     const int tc = min(TC, T - t0);
-    if (a.mode != 2) {
+    if (a.mode != 2 && FUSED) {
+      // -- g from this cluster's own slices of V: rank r projects rows
+      //    [v0, v0 + vn) of V; the k columns' partials go to their owning ranks
+      for (int e = tid; e < TC * a.v_rows; e += blockDim.x) {
+        const int t = e / a.v_rows, i = e - (e / a.v_rows) * a.v_rows;
+        xsl[e] = (t < tc && i < vn) ? E::load1_cg(a.X, int64_t(t0 + t) * d + v0 + i) : 0.f;
+      }
+      if (!v_waited) {
+        if (!__all_sync(0xffffffffu, bar_wait(vbar, 0, a.err))) ok = false;
+        v_waited = true;
+      }
+      __syncthreads();
+      if (warp < TC) {
+        float sq = 0.f;
+        for (int i = lane; i < vn; i += 32) sq = fmaf(xsl[warp * a.v_rows + i], xsl[warp * a.v_rows + i], sq);
+        sq = warp_sum(sq);
+        if (lane == 0) xsq[warp] = sq;
+      }
+      {
+        // thread (group g, word w): 4-byte word w of every row g, g + ngrp, ...
+        constexpr int PW = 4 / E::kBytes;  // elements per 4-byte word
+        const int words = mrow_b / 4;
+        const int grp_id = tid / words, w = tid - (tid / words) * words;
+        if (ok && grp_id < a.ngrp) {
+          float acc[TC][PW];
+#pragma unroll
+          for (int t = 0; t < TC; ++t)
+#pragma unroll
+            for (int e = 0; e < PW; ++e) acc[t][e] = 0.f;
+          for (int i = grp_id; i < vn; i += a.ngrp) {
+            const uint32_t u = *reinterpret_cast<const uint32_t*>(Vs + int64_t(i) * mrow_b + 4 * w);
+            float wv[PW];
+            if (PW == 2) {
+              BF16::unpack2(u, wv[0], wv[PW - 1]);
+            } else {
+              wv[0] = __uint_as_float(u);
+            }
+#pragma unroll
+            for (int t = 0; t < TC; ++t) {
+              const float xv = xsl[t * a.v_rows + i];
+#pragma unroll
+              for (int e = 0; e < PW; ++e) acc[t][e] = fmaf(xv, wv[e], acc[t][e]);
+            }
+          }
+#pragma unroll
+          for (int t = 0; t < TC; ++t)
+#pragma unroll
+            for (int e = 0; e < PW; ++e) red2[(grp_id * TC + t) * k + w * PW + e] = acc[t][e];
+        }
+      }
+      if (!started) {
+        cluster_wait();  // every CTA of the cluster is running: peers' shared memory is live
+        started = true;
+      }
+      __syncthreads();
+      for (int e = tid; e < TC * k; e += blockDim.x) {
+        float s2 = 0.f;
+        for (int g = 0; g < a.ngrp; ++g) s2 += red2[g * TC * k + e];
+        const int t = e / k, col = e - (e / k) * k;
+        const int q = col / ks;
+        cluster.map_shared_rank(inbox, q)[(rank * TC + t) * ks + (col - q * ks)] = s2;
+      }
+      if (tid < TC * CS) {
+        const int t = tid % TC, q = tid / TC;
+        cluster.map_shared_rank(inbox_x, q)[rank * TC + t] = xsq[t];
+      }
+      cluster.sync();
+      for (int e = tid; e < TC * ks; e += blockDim.x) {
+        const int t = e / ks, j = e - (e / ks) * ks;
+        float s2 = 0.f;
+#pragma unroll
+        for (int r = 0; r < CS; ++r) s2 += inbox[(r * TC + t) * ks + j];
+        gsl[e] = (t < tc && c0 + j < c1) ? s2 : 0.f;
+      }
+      if (tid < TC) {
+        float s2 = 0.f;
+#pragma unroll
+        for (int r = 0; r < CS; ++r) s2 += inbox_x[r * TC + tid];
+        nx2[tid] = s2;
+      }
+    }
+    if (a.mode != 2 && !FUSED) {
       // -- g: this CTA's column slice summed over the projection clusters
       if (tid < 256) {
         for (int base = 0; base < E_ * grp; base += 256) {
@@ -206,13 +326,15 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kApplyThr
           }
         }
       }
+    }
+    if (a.mode != 2) {
       if (!started) {
         cluster_wait();  // every CTA of the cluster is running
         started = true;
       }
       __syncthreads();
       // push this CTA's slice of g into every CTA's full copy
-      for (int e = tid; e < E_ * kClusterSize; e += blockDim.x) {
+      for (int e = tid; e < E_ * CS; e += blockDim.x) {
         const int q = e / E_, f = e - (e / E_) * E_;
         const int t = f / ks, col = c0 + (f - (f / ks) * ks);
         if (col < c1) cluster.map_shared_rank(gfull, q)[t * k + col] = gsl[f];
@@ -288,7 +410,7 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kApplyThr
         }
       }
       __syncthreads();
-      if (tid < TC * kClusterSize) {
+      if (tid < TC * CS) {
         // this CTA's share of g^T Gram g and ||g||^2, pushed to every CTA
         const int t = tid % TC, dst = tid / TC;
         float q = 0.f, n = 0.f;
@@ -305,7 +427,7 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kApplyThr
         if (tid < tc) {
           float q = 0.f, n = 0.f;
 #pragma unroll
-          for (int r = 0; r < kClusterSize; ++r) {
+          for (int r = 0; r < CS; ++r) {
             q += qin[r * TC + tid];
             n += nin[r * TC + tid];
           }
@@ -398,11 +520,50 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kApplyThr
     ok = __syncthreads_and(ok) != 0;
     if (nf > 0 && nrows > 0) m_waited = m_waited || m_live;
     // -- slow tokens: every warp streams its own rows of W (rows warp,
-    //    warp + 9, ...) in segments through a private ring of bulk copies.
+    //    warp + 8, ...) in segments through a private ring of bulk copies.
     //    The ring shares shared memory with the staged M rows: wait for that
     //    copy and retire the staged rows before the first segment lands.
     if (ns > 0 && nrows > 0 && ok) {
       const int nxs = min(ns, a.x_stage_max);
+      if (m_live) {
+        if (tid == 0 && !m_waited && !bar_wait(mfull, 0, a.err)) ok = false;
+        m_live = false;
+        m_waited = true;
+      }
+      // the staged M rows are retired: the rings may overwrite them
+      const bool ring_ok = __syncthreads_and(ok) != 0;
+      const int nwarp = kApplyThreads / 32;
+      const int seg_b = a.seg_bytes;
+      const int SW = a.wstages;
+      const int nseg = int((row_b + seg_b - 1) / seg_b);
+      const int my_rows = warp < nrows ? (nrows - warp + nwarp - 1) / nwarp : 0;
+      const int items = ring_ok ? my_rows * nseg : 0;
+      unsigned char* wring = Ms + int64_t(warp) * SW * seg_b;
+      uint64_t* wfull = full + warp * SW;
+      const char* wbase = static_cast<const char*>(a.W) + r0 * row_b;
+      // Item q of this warp is segment q % nseg of its row q / nseg (CTA row
+      // warp + (q / nseg) * nwarp), in ring slot (wuse + q) % SW.  The copy
+      // issuer (lane 0) and the consumer step through the items with
+      // counters, so the loop does no integer division.
+      int q_row = 0, q_seg = 0, q_slot = wuse % SW;  // next item to issue (lane 0)
+      auto issue_next = [&]() {
+        const int64_t offq = int64_t(q_seg) * seg_b;
+        const uint32_t bytes = uint32_t(min(int64_t(seg_b), row_b - offq));
+        bar_expect_tx(&wfull[q_slot], bytes);
+        bulk_g2s(wring + q_slot * seg_b, wbase + (int64_t(warp) + int64_t(q_row) * nwarp) * row_b + offq, bytes,
+                 &wfull[q_slot]);
+        if (++q_seg == nseg) {
+          q_seg = 0;
+          ++q_row;
+        }
+        if (++q_slot == SW) q_slot = 0;
+      };
+      int issued = min(items, SW);  // warp-uniform
+      if (lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        for (int q = 0; q < issued; ++q) issue_next();
+      }
+      // the slow tokens' x is staged while the first segments of W are in flight
       const int64_t xv = row_b / 16;
       for (int64_t e = tid; e < int64_t(nxs) * xv; e += blockDim.x) {
         const int j = int(e / xv);
@@ -410,94 +571,107 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kApplyThr
         reinterpret_cast<uint4*>(xst)[e] =
             ld_cg_v4(static_cast<const char*>(a.X) + int64_t(t0 + slist[j]) * row_b + v * 16);
       }
-      if (m_live) {
-        if (tid == 0 && !m_waited && !bar_wait(mfull, 0, a.err)) ok = false;
-        m_live = false;
-        m_waited = true;
-      }
       __syncthreads();
-      const int nwarp = kApplyThreads / 32;
-      const int seg_b = a.seg_bytes;
-      const int SW = a.wstages;
-      const int nseg = int((row_b + seg_b - 1) / seg_b);
-      const int my_rows = warp < nrows ? (nrows - warp + nwarp - 1) / nwarp : 0;
-      const int items = my_rows * nseg;
-      unsigned char* wring = Ms + int64_t(warp) * SW * seg_b;
-      uint64_t* wfull = full + warp * SW;
-      const char* wbase = static_cast<const char*>(a.W) + r0 * row_b;
-      int issued = 0;
-      if (lane == 0) {
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-        for (; issued < items && issued < SW; ++issued) {
-          const int j = issued / nseg, sg = issued - (issued / nseg) * nseg;
-          const int64_t off = int64_t(sg) * seg_b;
-          const uint32_t bytes = uint32_t(min(int64_t(seg_b), row_b - off));
-          const int slot = (wuse + issued) % SW;
-          bar_expect_tx(&wfull[slot], bytes);
-          bulk_g2s(wring + slot * seg_b, wbase + (int64_t(warp) + int64_t(j) * nwarp) * row_b + off, bytes,
-                   &wfull[slot]);
-        }
-      }
-      issued = __shfl_sync(0xffffffffu, issued, 0);
-      float acc[TC];
+      // two partial sums per token, added at the row's end
+      float acc[TC][2];
 #pragma unroll
-      for (int t = 0; t < TC; ++t) acc[t] = 0.f;
+      for (int t = 0; t < TC; ++t) acc[t][0] = acc[t][1] = 0.f;
+      int c_slot = wuse % SW, c_row = 0, c_seg = 0;
+      uint32_t c_ph = uint32_t(wuse / SW) & 1u;
       int i = 0;
       for (; i < items; ++i) {
-        const int slot = (wuse + i) % SW;
-        const uint32_t ph = ((wuse + i) / SW) & 1;
-        if (!__all_sync(0xffffffffu, bar_wait(&wfull[slot], ph, a.err))) {
+        if (!__all_sync(0xffffffffu, bar_wait(&wfull[c_slot], c_ph, a.err))) {
           ok = false;
           break;
         }
-        const int j = i / nseg, sg = i - (i / nseg) * nseg;
-        const int64_t off = int64_t(sg) * seg_b;
+        const int64_t off = int64_t(c_seg) * seg_b;
         const int nvec = int(min(int64_t(seg_b), row_b - off) / 16);
-        const unsigned char* segp = wring + slot * seg_b;
-        for (int vv = lane; vv < nvec; vv += 32) {
-          float w[PV];
-          E::unpack(*reinterpret_cast<const uint4*>(segp + vv * 16), w);
-          const int64_t xo = off + int64_t(vv) * 16;
+        const unsigned char* segp = wring + c_slot * seg_b;
+        // lane l takes 16-byte vectors l, l + 32, ... of the segment.  They
+        // are copied to registers and the slot is refilled at once, so the
+        // ring keeps SW segments in flight while the warp multiplies.
+        const bool full_seg = nvec == kSegVecs * 32;
+        uint4 wq[kSegVecs];
+        if (full_seg) {
 #pragma unroll
-          for (int t = 0; t < TC; ++t) {
-            if (t < ns) {
-              const uint4 xq = t < nxs ? *reinterpret_cast<const uint4*>(xst + int64_t(t) * row_b + xo)
-                                       : ld_cg_v4(static_cast<const char*>(a.X) + int64_t(t0 + slist[t]) * row_b + xo);
-              float xf[PV];
-              E::unpack(xq, xf);
+          for (int u = 0; u < kSegVecs; ++u) wq[u] = *reinterpret_cast<const uint4*>(segp + (u * 32 + lane) * 16);
+        } else {
 #pragma unroll
-              for (int e = 0; e < PV; ++e) acc[t] = fmaf(w[e], xf[e], acc[t]);
-            }
+          for (int u = 0; u < kSegVecs; ++u) {
+            const int v = u * 32 + lane;
+            wq[u] = v < nvec ? *reinterpret_cast<const uint4*>(segp + v * 16) : make_uint4(0u, 0u, 0u, 0u);
           }
         }
+        // the loaded values are in registers before the slot is handed back
+        uint32_t dep = 0;
+#pragma unroll
+        for (int u = 0; u < kSegVecs; ++u) dep ^= wq[u].x;
+        asm volatile("" ::"r"(dep) : "memory");
         __syncwarp();
-        if (lane == 0 && issued < items) {
-          // the slot just read is refilled with the segment SW items ahead
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          const int q = issued;
-          const int jq = q / nseg, sq = q - (q / nseg) * nseg;
-          const int64_t offq = int64_t(sq) * seg_b;
-          const uint32_t bytes = uint32_t(min(int64_t(seg_b), row_b - offq));
-          const int sl = (wuse + q) % SW;
-          bar_expect_tx(&wfull[sl], bytes);
-          bulk_g2s(wring + sl * seg_b, wbase + (int64_t(warp) + int64_t(jq) * nwarp) * row_b + offq, bytes,
-                   &wfull[sl]);
+        if (issued < items) {
+          if (lane == 0) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue_next();
+          }
+          ++issued;
         }
-        issued = __shfl_sync(0xffffffffu, issued + ((issued < items) ? 1 : 0), 0);
-        if (sg == nseg - 1) {
+        // x of each slow token: a batch of loads, then the multiplies
+        auto dot = [&](auto full_c) {
+          constexpr bool FULL = decltype(full_c)::value;
 #pragma unroll
           for (int t = 0; t < TC; ++t) {
             if (t < ns) {
-              const float sum = warp_sum(acc[t]);
-              if (lane == 0) a.Y[int64_t(t0 + slist[t]) * d_out + r0 + warp + int64_t(j) * nwarp] = sum;
+              uint4 xq[kSegVecs];
+              if (t < nxs) {
+                const unsigned char* xs = xst + int64_t(t) * row_b + off;
+#pragma unroll
+                for (int u = 0; u < kSegVecs; ++u) {
+                  const int v = u * 32 + lane;
+                  xq[u] = (FULL || v < nvec) ? *reinterpret_cast<const uint4*>(xs + v * 16) : make_uint4(0u, 0u, 0u, 0u);
+                }
+              } else {
+                const char* xg = static_cast<const char*>(a.X) + int64_t(t0 + slist[t]) * row_b + off;
+#pragma unroll
+                for (int u = 0; u < kSegVecs; ++u) {
+                  const int v = u * 32 + lane;
+                  xq[u] = (FULL || v < nvec) ? ld_cg_v4(xg + v * 16) : make_uint4(0u, 0u, 0u, 0u);
+                }
+              }
+#pragma unroll
+              for (int u = 0; u < kSegVecs; ++u) E::dot_acc(wq[u], xq[u], acc[t][0], acc[t][1]);
             }
-            acc[t] = 0.f;
           }
+        };
+        if (full_seg)
+          dot(BoolC<true>{});
+        else
+          dot(BoolC<false>{});
+        if (++c_slot == SW) {
+          c_slot = 0;
+          c_ph ^= 1u;
+        }
+        if (++c_seg == nseg) {
+#pragma unroll
+          for (int t = 0; t < TC; ++t) {
+            if (t < ns) {
+              const float sum = warp_sum(acc[t][0] + acc[t][1]);
+              if (lane == 0) a.Y[int64_t(t0 + slist[t]) * d_out + r0 + warp + int64_t(c_row) * nwarp] = sum;
+            }
+            acc[t][0] = acc[t][1] = 0.f;
+          }
+          c_seg = 0;
+          ++c_row;
         }
       }
       // after an error: wait (bounded) for this warp's copies still in flight
       if (lane == 0)
-        for (int q = i; q < issued; ++q) bar_wait(&wfull[(wuse + q) % SW], ((wuse + q) / SW) & 1, a.err);
+        for (int q = i; q < issued; ++q) {
+          bar_wait(&wfull[c_slot], c_ph, a.err);
+          if (++c_slot == SW) {
+            c_slot = 0;
+            c_ph ^= 1u;
+          }
+        }
       wuse += issued;
     }
     ok = __syncthreads_and(ok && *reinterpret_cast<volatile uint32_t*>(a.err) == 0) != 0;
@@ -515,17 +689,20 @@ __global__ void __cluster_dims__(kClusterSize, 1, 1) __launch_bounds__(kApplyThr
   }
   if (!started) cluster_wait();
   if (gram_smem && tid < 256 && !gram_waited) bar_wait(gfull_bar, 0, a.err);
+  if (!v_waited && tid == 0) bar_wait(vbar, 0, a.err);
   // bounded drain of the M copy if it was never waited for
   if (stage_m && !m_waited && tid == 0) bar_wait(mfull, 0, a.err);
 }
 
-template <class E, int TC, int GRV>
+template <class E, int TC, bool FUSED, int CS>
 static cudaError_t launch_da_t(const DecideArgs& a, const DecidePlan& p, cudaStream_t s) {
-  auto kern = decide_apply_kernel<E, TC, GRV>;
+  auto kern = decide_apply_kernel<E, TC, 0, FUSED, CS>;
   static size_t smem_set = 0;
   if (p.smem > smem_set) {
     cudaError_t e = set_kernel_smem(kern, p.smem);
     if (e != cudaSuccess) return e;
+    if (CS > 8 && (e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
+      return e;
     smem_set = p.smem;
   }
   cudaLaunchConfig_t cfg = {};
@@ -533,49 +710,76 @@ static cudaError_t launch_da_t(const DecideArgs& a, const DecidePlan& p, cudaStr
   cfg.blockDim = dim3(kApplyThreads);
   cfg.dynamicSmemBytes = p.smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CS;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, a);
 }
 
-template <class E, int TC>
-static cudaError_t launch_da_tc(const DecideArgs& a, const DecidePlan& p, cudaStream_t s) {
-  return launch_da_t<E, TC, 0>(a, p, s);
+template <class E, bool FUSED, int CS>
+static cudaError_t launch_da_f(const DecideArgs& a, const DecidePlan& p, cudaStream_t s) {
+  switch (p.tc) {
+    case 1: return launch_da_t<E, 1, FUSED, CS>(a, p, s);
+    case 2: return launch_da_t<E, 2, FUSED, CS>(a, p, s);
+    case 4: return launch_da_t<E, 4, FUSED, CS>(a, p, s);
+    default: return launch_da_t<E, 8, FUSED, CS>(a, p, s);
+  }
 }
 
 template <class E>
 static cudaError_t launch_da_e(const DecideArgs& a, const DecidePlan& p, cudaStream_t s) {
-  switch (p.tc) {
-    case 1: return launch_da_tc<E, 1>(a, p, s);
-    case 2: return launch_da_tc<E, 2>(a, p, s);
-    case 4: return launch_da_tc<E, 4>(a, p, s);
-    default: return launch_da_tc<E, 8>(a, p, s);
-  }
+  if (!p.fused) return launch_da_f<E, false, 8>(a, p, s);
+  if (p.tc > 2) return cudaErrorInvalidValue;  // the fused decode handles one chunk of at most 2 tokens
+  if (p.cs == 16) return p.tc == 1 ? launch_da_t<E, 1, true, 16>(a, p, s) : launch_da_t<E, 2, true, 16>(a, p, s);
+  return p.tc == 1 ? launch_da_t<E, 1, true, 8>(a, p, s) : launch_da_t<E, 2, true, 8>(a, p, s);
 }
 
 cudaError_t launch_decide_apply(const DecideArgs& a, const DecidePlan& p, gsi_dtype dt, cudaStream_t s) {
   return dt == GSI_BF16 ? launch_da_e<BF16>(a, p, s) : launch_da_e<F32>(a, p, s);
 }
 
-// Co-resident clusters of the decide-and-apply kernel for a plan (grid size).
-template <class E>
-static int max_clusters_e(const DecidePlan& p) {
-  auto kern = decide_apply_kernel<E, 1, 0>;
-  if (set_kernel_smem(kern, p.smem) != cudaSuccess) return 0;
+// Co-resident clusters of cs CTAs of the decide-and-apply kernel with `smem`
+// bytes of shared memory each (the grid size of a plan); 0 if not possible.
+template <class E, bool FUSED, int CS>
+static int max_clusters_t(size_t smem) {
+  auto kern = decide_apply_kernel<E, 1, 0, FUSED, CS>;
+  if (set_kernel_smem(kern, smem) != cudaSuccess) return 0;
+  if (CS > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(kClusterSize * 64);
+  cfg.gridDim = dim3(CS * 64);
   cfg.blockDim = dim3(kApplyThreads);
-  cfg.dynamicSmemBytes = p.smem;
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) return 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
   return n;
 }
 
-int decide_apply_max_clusters(const DecidePlan& p, gsi_dtype dt) {
-  return dt == GSI_BF16 ? max_clusters_e<BF16>(p) : max_clusters_e<F32>(p);
+int decide_apply_max_clusters(size_t smem, gsi_dtype dt, bool fused, int cs) {
+  if (dt == GSI_BF16) {
+    if (!fused) return max_clusters_t<BF16, false, 8>(smem);
+    return cs == 16 ? max_clusters_t<BF16, true, 16>(smem) : max_clusters_t<BF16, true, 8>(smem);
+  }
+  if (!fused) return max_clusters_t<F32, false, 8>(smem);
+  return cs == 16 ? max_clusters_t<F32, true, 16>(smem) : max_clusters_t<F32, true, 8>(smem);
 }
 
 }  // namespace gsi

@@ -32,6 +32,13 @@ struct F32 {
   __device__ __forceinline__ static float load1_cg(const void* base, int64_t i) {
     return __ldcg(reinterpret_cast<const float*>(base) + i);
   }
+  // a0 += w.x*x.x + w.z*x.z, a1 += w.y*x.y + w.w*x.w (in that order)
+  __device__ __forceinline__ static void dot_acc(const uint4& w, const uint4& x, float& a0, float& a1) {
+    a0 = fmaf(__uint_as_float(w.x), __uint_as_float(x.x), a0);
+    a1 = fmaf(__uint_as_float(w.y), __uint_as_float(x.y), a1);
+    a0 = fmaf(__uint_as_float(w.z), __uint_as_float(x.z), a0);
+    a1 = fmaf(__uint_as_float(w.w), __uint_as_float(x.w), a1);
+  }
 };
 
 struct BF16 {
@@ -58,6 +65,23 @@ struct BF16 {
   __device__ __forceinline__ static float load1_cg(const void* base, int64_t i) {
     unsigned short b = __ldcg(reinterpret_cast<const unsigned short*>(base) + i);
     return __uint_as_float(uint32_t(b) << 16);
+  }
+  // lo += lo(w) * lo(x); hi += hi(w) * hi(x) for one word of two bf16 each:
+  // the mixed-precision FMA takes the bf16 halves as they are (the product
+  // of two bf16 is exact in f32) and rounds once into the f32 sum, which is
+  // what widening both and calling fmaf computes.
+  __device__ __forceinline__ static void fma2(uint32_t w, uint32_t x, float& lo, float& hi) {
+    asm("{\n\t.reg .b16 wl, wh, xl, xh;\n\tmov.b32 {wl, wh}, %2;\n\tmov.b32 {xl, xh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, wl, xl, %0;\n\tfma.rn.f32.bf16 %1, wh, xh, %1;\n\t}"
+        : "+f"(lo), "+f"(hi)
+        : "r"(w), "r"(x));
+  }
+  // a0 += the products of the even elements, a1 of the odd ones, in order
+  __device__ __forceinline__ static void dot_acc(const uint4& w, const uint4& x, float& a0, float& a1) {
+    fma2(w.x, x.x, a0, a1);
+    fma2(w.y, x.y, a0, a1);
+    fma2(w.z, x.z, a0, a1);
+    fma2(w.w, x.w, a0, a1);
   }
 };
 

@@ -51,6 +51,16 @@ struct DecideArgs {
   const uint8_t* flags_in;  // T stored flags (mode 2)
   int rows_per_cta, seg_bytes, wstages, x_stage_max, stage_m;
   int off_m, off_x, off_g, off_gram;
+  // fused decode (the cluster projects x itself)
+  const void* V;        // d x k
+  int v_rows, ngrp, off_v, off_xs;
+  // weights of the next map of a stack, staged in L2 while this one runs
+  const char* next_v;
+  uint64_t next_v_bytes;
+  const char* next_m;
+  uint64_t next_m_bytes;
+  const char* next_gram;
+  uint64_t next_gram_bytes;
   uint32_t* err;
 };
 
@@ -88,7 +98,7 @@ cudaError_t launch_gate(const GateArgs& a, const GatePlan& p, gsi_dtype dt, cuda
 cudaError_t launch_compact(const uint8_t* flags, int T, int32_t* idx, int32_t* counts,
                            cudaStream_t s);
 cudaError_t launch_decide_apply(const DecideArgs& a, const DecidePlan& p, gsi_dtype dt, cudaStream_t s);
-int decide_apply_max_clusters(const DecidePlan& p, gsi_dtype dt);
+int decide_apply_max_clusters(size_t smem, gsi_dtype dt, bool fused, int cs);
 cudaError_t launch_image(const void* W, const void* V, void* M, float* gram, int64_t d,
                          int64_t d_out, int64_t k, gsi_dtype dt, cudaStream_t s);
 

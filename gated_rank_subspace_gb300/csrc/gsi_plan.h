@@ -10,7 +10,10 @@ namespace gsi {
 
 constexpr int kClusterSize = 8;     // CTAs per cluster in the gate kernel
 constexpr int kGateThreads = 128;  // small enough to share an SM with a decide-and-apply CTA
-constexpr int kApplyThreads = 288;  // 8 consumer warps + 1 copy-producer warp
+// 8 warps: with at most 168 registers a thread, two warps of a decide CTA on
+// each SM sub-partition leave room for one warp of a projection CTA, so the
+// two kernels of consecutive calls can share an SM and overlap.
+constexpr int kApplyThreads = 256;
 constexpr int kGateMaxRowsPerThread = 8;
 constexpr int kGateTargetSlabs = 256;
 
@@ -101,38 +104,47 @@ constexpr int64_t kTensorMinT = 128;
 // Decide-and-apply kernel geometry (see gsi_apply.cu).  The device part
 // (how many CTAs are co-resident) comes in as ncta; everything else is
 // arithmetic on the shapes.  Each CTA owns rows_per_cta contiguous output
-// rows.  Its nine warps stream their own W rows in seg_bytes segments through
+// rows.  Its eight warps stream their own W rows in seg_bytes segments through
 // private rings of wstages slots; the rings share one shared-memory region
 // with the staged M rows (a call's fast rows are computed before its slow
 // rows stream).
 struct DecidePlan {
   int tc, grv, ncta, rows_per_cta, seg_bytes, wstages, x_stage_max, stage_m;
   int off_m, off_x, off_g, off_gram;  // off_gram = 0: Gram slice read from global
+  bool fused;  // single-launch decode: the cluster projects x itself
+  int cs;      // CTAs per cluster
+  int ks;      // columns of g owned by each rank
+  int v_rows, ngrp, off_v, off_xs;
   size_t smem;
   bool ok;
 };
 
 constexpr int kSegBytes = 4096;
+constexpr int kSegVecs = kSegBytes / (32 * 16);  // 16-byte vectors per lane in one segment
 constexpr int kWarpStages = 4;
 constexpr int kXStage = 16 * 1024;
 
 inline DecidePlan plan_decide(int64_t d, int64_t d_out, int64_t k, int es, int64_t T, int ncta,
-                              size_t smem_budget) {
+                              size_t smem_budget, bool fused = false, int cs = kClusterSize) {
   DecidePlan p{};
   p.ok = true;
+  p.fused = fused;
+  p.cs = cs;
   p.tc = T >= 8 ? 8 : T >= 4 ? 4 : T >= 2 ? 2 : 1;
-  const int64_t ks = cdiv(k, kClusterSize);
-  p.grv = 0;  // Gram slice comes from shared memory (or global when it does not fit)
+  const int64_t ks = cdiv(k, cs);
+  p.ks = int(ks);
+  p.grv = 0;
   const int64_t row_b = d * es;
+  const int64_t mrow_b = k * es;
   p.seg_bytes = int(row_b < kSegBytes ? row_b : kSegBytes);
   p.wstages = kWarpStages;
   const size_t ring = size_t(kApplyThreads / 32) * p.wstages * p.seg_bytes;
-  const int64_t xs = kXStage / row_b;
+  const int64_t xs = fused ? 0 : kXStage / row_b;
   p.x_stage_max = int(xs < p.tc ? xs : p.tc);
-  const size_t g_area = (size_t(p.tc) * k + size_t(p.tc) * ks + 40 * size_t(p.tc) + 40) * 4;
-  const size_t bars = size_t(kApplyThreads / 32) * p.wstages * 8 + 16;
+  size_t g_area = (size_t(p.tc) * k + size_t(p.tc) * ks + 8 * 2 * size_t(p.tc) + 2 * size_t(cs) * p.tc +
+                   6 * size_t(p.tc) + 40) * 4;
+  const size_t bars = size_t(kApplyThreads / 32) * p.wstages * 8 + 24;
   size_t off = (bars + 127) & ~size_t(127);
-  // Gram slice of one cluster rank (ks rows of k floats), staged by a bulk copy
   const size_t gram_b = size_t(ks) * k * 4;
   p.off_gram = 0;
   if (gram_b <= 40 * 1024) {
@@ -145,13 +157,48 @@ inline DecidePlan plan_decide(int64_t d, int64_t d_out, int64_t k, int es, int64
   p.off_g = int(off);
   off += g_area;
   off = (off + 127) & ~size_t(127);
+  p.v_rows = 0;
+  p.ngrp = 0;
+  p.off_xs = 0;
+  if (fused) {
+    // token slice, group partials, inboxes
+    p.v_rows = int(cdiv(d, cs));
+    const int words = int(mrow_b / 4);
+    p.ngrp = kApplyThreads / words >= 1 ? kApplyThreads / words : 1;
+    p.off_xs = int(off);
+    off += (size_t(p.tc) * p.v_rows + size_t(p.ngrp) * p.tc * k + size_t(cs) * p.tc * ks + size_t(cs) * p.tc +
+            size_t(p.tc) + 8) * 4;
+    off = (off + 127) & ~size_t(127);
+  }
   p.off_m = int(off);
   p.ncta = ncta;
   p.rows_per_cta = int(cdiv(d_out, ncta));
-  const size_t m_bytes = size_t(p.rows_per_cta) * k * es;
-  p.stage_m = off + (m_bytes > ring ? m_bytes : ring) <= smem_budget ? 1 : 0;
-  p.smem = off + (p.stage_m && m_bytes > ring ? m_bytes : ring);
+  const size_t m_bytes = (size_t(p.rows_per_cta) * mrow_b + 127) & ~size_t(127);
+  const size_t v_bytes = fused ? size_t(p.v_rows) * mrow_b : 0;
+  // region after off_m: [M rows | V slice] before the decision, W rings after it
+  size_t need_mv = m_bytes + v_bytes;
+  p.stage_m = off + (need_mv > ring ? need_mv : ring) <= smem_budget ? 1 : 0;
+  if (fused && !p.stage_m) {
+    need_mv = v_bytes;  // M then comes from global (L2) after the decision
+  }
+  p.off_v = int(off + (p.stage_m ? m_bytes : 0));
+  const size_t region = (p.stage_m || fused) ? (need_mv > ring ? need_mv : ring) : ring;
+  p.smem = off + region;
   p.ok = p.smem <= smem_budget;
+  // shared memory left over stages more slow tokens' x (up to the chunk)
+  if (p.ok && p.x_stage_max < p.tc) {
+    const int64_t more = int64_t(smem_budget - p.smem) / row_b;
+    const int64_t grow = more < p.tc - p.x_stage_max ? more : p.tc - p.x_stage_max;
+    const size_t shift = (size_t(grow) * row_b + 127) & ~size_t(127);
+    if (grow > 0 && p.smem + shift <= smem_budget) {
+      p.x_stage_max += int(grow);
+      p.off_g += int(shift);
+      if (fused) p.off_xs += int(shift);
+      p.off_m += int(shift);
+      p.off_v += int(shift);
+      p.smem += shift;
+    }
+  }
   return p;
 }
 

@@ -70,9 +70,19 @@ typedef enum gsi_status {
 
 typedef enum gsi_dtype { GSI_F32 = 0, GSI_BF16 = 1 } gsi_dtype;
 
-/* Which kernels run the map.  AUTO picks STREAM for small T (decode) and for
- * f32, TENSOR (tcgen05 contractions) for bf16 at prefill-sized T. */
-typedef enum gsi_path { GSI_PATH_AUTO = 0, GSI_PATH_STREAM = 1, GSI_PATH_TENSOR = 2 } gsi_path;
+/* Which kernels run the map.
+ *   FUSED  -- one launch per call for T <= 2: clusters of CTAs project the
+ *             tokens on their own slices of V, decide, and apply;
+ *   STREAM -- two launches (projection kernel, then decide-and-apply), any T;
+ *   TENSOR -- tcgen05 contractions, bf16 only, for prefill-sized T.
+ * AUTO picks TENSOR for bf16 with T >= 128 and STREAM otherwise; FUSED is
+ * available on request (T <= 2 and a slice of V that fits shared memory). */
+typedef enum gsi_path {
+  GSI_PATH_AUTO = 0,
+  GSI_PATH_STREAM = 1,
+  GSI_PATH_TENSOR = 2,
+  GSI_PATH_FUSED = 3
+} gsi_path;
 
 /* One linear map with its cached artefacts (all device pointers). */
 typedef struct gsi_map_desc {

@@ -264,3 +264,45 @@ def test_config5_prefill_tensor_path(gsi):
     Y2, f2, r2 = gsi.linear(gm, X, m_in.eps, workspace=ws)
     torch.cuda.synchronize()
     assert torch.equal(Y, Y2) and torch.equal(flags, f2)
+
+
+# ------------------------------------------------------------------ fused single-launch decode
+@pytest.mark.parametrize("role", ["qkv", "out", "up"])
+@pytest.mark.parametrize("T", [1, 2])
+def test_fused_decode_against_oracle(gsi, role, T):
+    """The single-launch decode (clusters project x on their own V slices)."""
+    m_in = synth.map_6b(role, T=24, n_slow=6)
+    gm, X = upload(m_in)
+    n = X.shape[0]
+    ws = gsi.new_workspace(gsi.workspace_size(gm, T, "fused"))
+    Y = torch.empty(n, gm.d_out, device="cuda")
+    F = torch.empty(n, dtype=torch.uint8, device="cuda")
+    R = torch.empty(n, device="cuda")
+    Ys = torch.empty_like(Y)
+    Fs = torch.empty_like(F)
+    for t0 in range(0, n, T):
+        sl = slice(t0, t0 + T)
+        gsi.linear(gm, X[sl], m_in.eps, Y=Y[sl], flags=F[sl], rho=R[sl], workspace=ws, path="fused")
+        gsi.linear(gm, X[sl], m_in.eps, Y=Ys[sl], flags=Fs[sl], want_rho=False, path="stream")
+    st = compare(m_in, gm.M, Y, F, R)
+    assert st["n_slow"] == 6
+    compare(m_in, gm.M, Ys, Fs, None)
+    assert gsi.workspace_status(ws) == 0
+    # bitwise determinism of the fused kernel
+    Y2 = torch.empty_like(Y)
+    for t0 in range(0, n, T):
+        sl = slice(t0, t0 + T)
+        gsi.linear(gm, X[sl], m_in.eps, Y=Y2[sl], flags=F[sl], want_rho=False, workspace=ws, path="fused")
+    torch.cuda.synchronize()
+    assert torch.equal(Y, Y2)
+
+
+def test_fused_rejects_what_it_cannot_run(gsi):
+    m_in = synth.map_6b("down", T=1, n_slow=0)  # d = 16384: the V slice does not fit
+    gm, X = upload(m_in)
+    with pytest.raises(gsi.GsiError):
+        gsi.workspace_size(gm, 1, "fused")
+    small = synth.map_6b("out", T=4, n_slow=1)
+    gm2, X2 = upload(small)
+    with pytest.raises(gsi.GsiError):
+        gsi.workspace_size(gm2, 4, "fused")
