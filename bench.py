@@ -21,6 +21,7 @@ public API with host buffers, and the float64 oracle timed on the host cores.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -209,6 +210,38 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------- GPU
+# DRAM bytes per decide_apply_kernel launch over the step's 1024 stored-decision
+# launches, from one ncu capture of `bench.py --kernel-traffic`
+# (dram__bytes_read.sum + dram__bytes_write.sum, launches 2049-3072): valid only for the kernel source it was taken on (first 16 hex digits of the
+# SHA-256 of csrc/gsi_apply.cu); otherwise the roofline reports traffic null.
+KERNEL_TRAFFIC = {"gsi_apply_sha256": "dce71edd205b6b9e", "bytes_per_launch": 15.01558825e6 + 0.01082125e6}
+
+
+def kernel_traffic():
+    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "gated_rank_subspace_gb300", "csrc", "gsi_apply.cu")
+    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    return KERNEL_TRAFFIC["bytes_per_launch"] if h == KERNEL_TRAFFIC["gsi_apply_sha256"] else None
+
+
+def probe_map(role, eps):
+    """Eight one-token gsi_linear calls of one 6B map (default stream)."""
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import gated_rank_subspace_gb300 as gsi
+
+    m_in = synth.map_6b(role, T=1, n_slow=0)
+    m = gsi.make_map(m_in.W.cuda(), m_in.V.cuda())
+    X = m_in.X.cuda()
+    ws = gsi.new_workspace(gsi.workspace_size(m, 1))
+    Y = torch.empty(1, m.d_out, device="cuda")
+    F = torch.empty(1, dtype=torch.uint8, device="cuda")
+    for _ in range(8):
+        gsi.linear(m, X, eps, Y=Y, flags=F, workspace=ws, want_rho=False)
+    torch.cuda.synchronize()
+    print(json.dumps({"probe_map": role, "eps": eps, "flag": int(F[0])}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -219,7 +252,17 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel-traffic", action="store_true",
+                    help="only run the step's 1024 gate launches, then its 1024 apply launches, once "
+                         "(the command an ncu DRAM-byte capture of the apply launches profiles)")
+    ap.add_argument("--probe-map", choices=["qkv", "out", "up", "down"], default=None,
+                    help="only run 8 one-token gsi_linear calls of this 6B map (a small case for ncu)")
+    ap.add_argument("--probe-eps", type=float, default=0.0,
+                    help="threshold of the --probe-map calls (0: every token slow)")
     args = ap.parse_args()
+    if args.probe_map:
+        probe_map(args.probe_map, args.probe_eps)
+        return
     if args.impl == "reference":
         run_reference(args)
         return
@@ -268,43 +311,44 @@ def main():
     with torch.cuda.stream(stream):
         step()
     stream.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph, stream=stream):
-        step()
-    with torch.cuda.stream(stream):
-        for _ in range(max(args.warmup, 3)):
-            graph.replay()
-    stream.synchronize()
-    assert gsi.workspace_status(ws, stream=stream) == 0
+    if not args.kernel_traffic:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+        with torch.cuda.stream(stream):
+            for _ in range(max(args.warmup, 3)):
+                graph.replay()
+        stream.synchronize()
+        assert gsi.workspace_status(ws, stream=stream) == 0
 
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(args.steps):
-            graph.replay()
-        e1.record(stream)
-    torch.cuda.synchronize()
-    if dist:
-        dist.barrier()
-    clocks = sampler.stop()
-    ms = e0.elapsed_time(e1) / args.steps
-    if dist:
-        t = torch.tensor([ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    tokens_per_s = T_TOKENS * world / (ms / 1e3)
+        sampler = ClockSampler(local)
+        sampler.start()
+        time.sleep(0.3)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(args.steps):
+                graph.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        clocks = sampler.stop()
+        ms = e0.elapsed_time(e1) / args.steps
+        if dist:
+            t = torch.tensor([ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            ms = float(t.item())
+        tokens_per_s = T_TOKENS * world / (ms / 1e3)
 
-    flags_np = [F.cpu().numpy().astype(bool) for F in Fs]
-    ab = algorithmic_bytes(maps_in, flags_np)
-    step_gbs = ab["total"] / (ms * 1e-3) / 1e9
-    hbm_peak, peak_kind = peaks()
+        flags_np = [F.cpu().numpy().astype(bool) for F in Fs]
+        ab = algorithmic_bytes(maps_in, flags_np)
+        step_gbs = ab["total"] / (ms * 1e-3) / 1e9
+        hbm_peak, peak_kind = peaks()
 
     # ---- per-kernel timing: the same 1024 calls split into their two launches
     # (gsi_gate then gsi_apply, each call with its own workspace), and each
@@ -357,6 +401,12 @@ def main():
         stream.synchronize()
         return a0.elapsed_time(a1) / reps_n
 
+    if args.kernel_traffic:
+        with torch.cuda.stream(stream):
+            run_gates()
+            run_applies(None)
+        stream.synchronize()
+        return
     t_gate = timed_graph(run_gates, args.steps)
     t_fast = timed_graph(lambda: run_applies(False), args.steps)
     t_slow = timed_graph(lambda: run_applies(True), args.steps)
@@ -451,7 +501,7 @@ def main():
         },
         "roofline": {
             "kernel": dom["name"], "bound": "hbm", "achieved": dom["gbs"], "peak": hbm_peak,
-            "unit": "GB/s", "frac": dom["gbs"] / hbm_peak, "traffic": None,
+            "unit": "GB/s", "frac": dom["gbs"] / hbm_peak, "traffic": kernel_traffic(),
             "peak_kind": peak_kind,
             "timing": "CUDA events around a graph of this kernel's 1024 launches of one step",
             "bytes_per_launch": dom["bytes_per_launch"], "ms_per_launch": dom["ms"],
