@@ -115,14 +115,15 @@ static gsi_status check_workspace(const void* ws, size_t have, size_t need) {
 // Per-block shared memory a kernel may opt into on sm_100-class GPUs (bytes).
 constexpr size_t kSmemOptinSm100 = 232448;
 
-// The fused decode kernel handles T <= 2 when one cluster rank's slice of V
-// (with 16 ranks) fits in shared memory beside its working buffers.
-// Host-only arithmetic, so workspace sizing needs no device.
+// The fused decode kernel handles T <= 2 when one CTA's slab of V (with a
+// grid of at least kFusedMinCtas CTAs) fits in shared memory beside its
+// working buffers.  Host-only arithmetic, so workspace sizing needs no device.
+constexpr int kFusedMinCtas = 64;
 static bool fused_fits(const gsi_map_desc* m, int64_t T) {
   if (T < 1 || T > 2) return false;
   const int es = elem_bytes(m->dtype);
-  if (m->k * es / 4 > kApplyThreads) return false;  // one thread per 4-byte word of a V row
-  const DecidePlan p = plan_decide(m->d, m->d_out, m->k, es, T, 1 << 20, kSmemOptinSm100, true, 16);
+  if (m->k * es / 16 > kApplyThreads) return false;  // one thread per 16-byte vector of a V row
+  const DecidePlan p = plan_decide(m->d, m->d_out, m->k, es, T, kFusedMinCtas, kSmemOptinSm100, true, 16);
   return p.ok;
 }
 
@@ -131,9 +132,10 @@ static bool fused_fits(const gsi_map_desc* m, int64_t T) {
 // streaming kernels otherwise.
 static gsi_status resolve_path(const gsi_map_desc* m, int64_t T, gsi_path path, gsi_path* out) {
   if (path == GSI_PATH_AUTO) {
-    // (the fused decode is not chosen automatically: measured, its V-slice
-    // projection costs as much as the second launch it saves)
-    *out = (m->dtype == GSI_BF16 && T >= kTensorMinT) ? GSI_PATH_TENSOR : GSI_PATH_STREAM;
+    if (fused_fits(m, T))
+      *out = GSI_PATH_FUSED;  // falls back to STREAM at run time where the device cannot run it
+    else
+      *out = (m->dtype == GSI_BF16 && T >= kTensorMinT) ? GSI_PATH_TENSOR : GSI_PATH_STREAM;
     return GSI_OK;
   }
   if (path == GSI_PATH_STREAM) {
@@ -155,12 +157,15 @@ static gsi_status resolve_path(const gsi_map_desc* m, int64_t T, gsi_path path, 
   return fail(GSI_ERR_INVALID_ARG, "unknown path %d", int(path));
 }
 
-// Workspace of a path.  The fused decode uses only the control block, but it
-// is sized like the streaming path so a device that cannot run it can fall
-// back to the two-launch kernels on the same workspace.
+// Workspace of a path.  The fused decode's is also large enough for the
+// streaming path, so a device that cannot run it can fall back to the
+// two-launch kernels on the same workspace.
 static size_t path_ws(const gsi_map_desc* m, int64_t T, gsi_path p) {
   if (p == GSI_PATH_TENSOR) return layout_tensor(m->d, m->k, T).total;
-  return layout_stream(m->d, m->k, m->dtype == GSI_BF16 ? 2 : 4, T).total;
+  const size_t st = layout_stream(m->d, m->k, m->dtype == GSI_BF16 ? 2 : 4, T).total;
+  if (p != GSI_PATH_FUSED) return st;
+  const size_t fu = layout_fused(m->k, T).total;
+  return st > fu ? st : fu;
 }
 
 static size_t stream_ws(const gsi_map_desc* m, int64_t T) {
@@ -238,6 +243,7 @@ static gsi_status run_decide(const gsi_map_desc* m, const void* X, int64_t T, fl
       cs = 8;
       nc = decide_clusters(f, m->dtype, true, 8);
     }
+    if (nc * cs > kFusedMaxCtas) nc = kFusedMaxCtas / cs;
     if (nc > 0) dp = plan_decide(m->d, m->d_out, m->k, es, T, nc * cs, size_t(f->smem_optin), true, cs);
     if (nc == 0 || !dp.ok) return fail(GSI_ERR_UNSUPPORTED, "the fused decode does not fit this device");
   } else {
@@ -278,6 +284,15 @@ static gsi_status run_decide(const gsi_map_desc* m, const void* X, int64_t T, fl
   a.off_x = dp.off_x;
   a.off_g = dp.off_g;
   a.off_gram = dp.off_gram;
+  if (fused) {
+    const FusedLayout FL = layout_fused(m->k, T);
+    a.fpart_g = reinterpret_cast<float*>(base + FL.part_g);
+    a.fpart_x = reinterpret_cast<float*>(base + FL.part_x);
+    a.part_g = a.fpart_g;
+    a.part_x = a.fpart_x;
+    a.nclu = dp.ncta;
+    a.ticket = &ctrl->ticket[m->dtype == GSI_BF16 ? 1 : 0];
+  }
   a.V = m->V;
   a.v_rows = dp.v_rows;
   a.ngrp = dp.ngrp;

@@ -66,6 +66,34 @@ __device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t parity, uint32_t*
   }
   return true;
 }
+// Grid barrier of the fused decode on a ticket counter in the workspace.
+// One thread per CTA, after a __syncthreads that follows the CTA's stores:
+// publish them (fence), take a ticket, and wait, bounded, until the n CTAs of
+// this barrier episode have all taken theirs.  Episodes never overlap: a
+// call's CTAs reach the barrier only after the dependency wait on the previous
+// kernel, and every call's grid has the same n for an element type, so the
+// episode of ticket t ends at (t / n + 1) * n.  The grid is sized so that all
+// its CTAs are co-resident.
+__device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ bool grid_barrier(unsigned long long* ticket, unsigned long long n, uint32_t* err) {
+  __threadfence();
+  const unsigned long long mine = atomicAdd(ticket, 1ull);
+  const unsigned long long target = (mine / n + 1) * n;
+  if (ld_acquire_gpu(ticket) >= target) return true;
+  const long long t0 = clock64();
+  while (ld_acquire_gpu(ticket) < target) {
+    if (clock64() - t0 > kSpinCycles) {
+      atomicOr(err, kErrTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
 // 1-D bulk copy global -> shared (16-byte aligned, multiple of 16 bytes).
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* b) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -80,8 +108,9 @@ struct BoolC {
 };
 
 // ------------------------------------------------------------------ kernel
-// FUSED: the cluster computes g = V_k^T x itself (one launch per call, T <= 2);
-// otherwise g comes from the projection kernel's cluster partials.
+// FUSED: the grid computes g = V_k^T x itself (one launch per call, T <= 2):
+// every CTA projects its own slab of V_k and the partials meet at a grid
+// barrier; otherwise g comes from the projection kernel's cluster partials.
 // CS: CTAs per cluster (8, or 16 where the device allows it), set at launch.
 template <class E, int TC, int GRV, bool FUSED, int CS>
 __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
@@ -118,14 +147,13 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
   int* slist = sflag + TC;                                     // [TC] slow tokens of the chunk
   int* flist = slist + TC;                                     // [TC] fast tokens of the chunk
   int* scount = flist + TC;                                    // [2]
-  // fused decode only: V slice, token slice, partial sums and inboxes
+  float* red3 = reinterpret_cast<float*>(scount + 4);          // [kApplyThreads] partial-sum scratch
+  // fused decode only: V slab, token slice, partial sums
   uint64_t* vbar = gfull_bar + 1;                              // [1] V slice copy
   const unsigned char* Vs = smem + a.off_v;                    // [v_rows][k] elements
   float* xsl = reinterpret_cast<float*>(smem + a.off_xs);      // [TC][v_rows]
-  float* red2 = xsl + TC * a.v_rows;                           // [ngrp][TC][k]
-  float* inbox = red2 + a.ngrp * TC * k;                       // [CS][TC][ks]
-  float* inbox_x = inbox + CS * TC * ks;                       // [CS][TC]
-  float* xsq = inbox_x + CS * TC;                              // [TC]
+  float* red2 = xsl + TC * ((a.v_rows + 3) & ~3);              // [ngrp][TC][k], 16-byte aligned
+  float* xsq = red2 + a.ngrp * TC * k;                         // [TC]
 
   // ---- prologue: only weights (may overlap the projection kernel)
   pdl_launch_dependents();
@@ -153,8 +181,8 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
     bulk_g2s(smem + a.off_gram, a.gram + int64_t(c0) * k, bytes, gfull_bar);
   }
   bool gram_waited = false;
-  // fused decode: this rank's slice of V (rows [v0, v0 + vn)), one bulk copy
-  const int64_t v0 = int64_t(rank) * a.v_rows;
+  // fused decode: this CTA's slab of V (rows [v0, v0 + vn)), one bulk copy
+  const int64_t v0 = int64_t(blockIdx.x) * a.v_rows;
   const int vn = FUSED ? int(v0 >= d ? 0 : (d - v0 < a.v_rows ? d - v0 : a.v_rows)) : 0;
   if (FUSED && a.mode != 2 && vn > 0 && tid == kApplyThreads - 32) {
     const uint32_t bytes = uint32_t(vn) * uint32_t(mrow_b);
@@ -201,14 +229,15 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
   bool m_waited = false;  // the M copy has been waited for
   int wuse = 0;           // this warp's ring items used so far (running count over token chunks)
   const int E_ = TC * ks;
-  const int grp = 256 / E_ >= 8 ? 8 : 256 / E_ >= 4 ? 4 : 256 / E_ >= 2 ? 2 : 1;
+  int grp = 1;  // threads that share one column of g when its partials are added
+  while (grp < 32 && E_ * grp * 2 <= kApplyThreads) grp *= 2;
   const int64_t cstride = int64_t(T) * k;
 
   for (int t0 = 0; t0 < T; t0 += TC) {
     const int tc = min(TC, T - t0);
     if (a.mode != 2 && FUSED) {
-      // -- g from this cluster's own slices of V: rank r projects rows
-      //    [v0, v0 + vn) of V; the k columns' partials go to their owning ranks
+      // -- g from the grid's own slabs of V: CTA b projects rows
+      //    [v0, v0 + vn) of V and publishes its partials for all clusters
       for (int e = tid; e < TC * a.v_rows; e += blockDim.x) {
         const int t = e / a.v_rows, i = e - (e / a.v_rows) * a.v_rows;
         xsl[e] = (t < tc && i < vn) ? E::load1_cg(a.X, int64_t(t0 + t) * d + v0 + i) : 0.f;
@@ -225,105 +254,151 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
         if (lane == 0) xsq[warp] = sq;
       }
       {
-        // thread (group g, word w): 4-byte word w of every row g, g + ngrp, ...
-        constexpr int PW = 4 / E::kBytes;  // elements per 4-byte word
-        const int words = mrow_b / 4;
-        const int grp_id = tid / words, w = tid - (tid / words) * words;
+        // thread (group g, vector w): 16-byte vector w of rows g, g + ngrp, ...
+        const int vecs = mrow_b / 16;
+        const int grp_id = tid / vecs, w = tid - (tid / vecs) * vecs;
         if (ok && grp_id < a.ngrp) {
-          float acc[TC][PW];
+          float acc[TC][PV];
 #pragma unroll
           for (int t = 0; t < TC; ++t)
 #pragma unroll
-            for (int e = 0; e < PW; ++e) acc[t][e] = 0.f;
-          for (int i = grp_id; i < vn; i += a.ngrp) {
-            const uint32_t u = *reinterpret_cast<const uint32_t*>(Vs + int64_t(i) * mrow_b + 4 * w);
-            float wv[PW];
-            if (PW == 2) {
-              BF16::unpack2(u, wv[0], wv[PW - 1]);
-            } else {
-              wv[0] = __uint_as_float(u);
-            }
+            for (int e = 0; e < PV; ++e) acc[t][e] = 0.f;
+          int i = grp_id;
+          for (; i + a.ngrp < vn; i += 2 * a.ngrp) {
+            const uint4 u0 = *reinterpret_cast<const uint4*>(Vs + int64_t(i) * mrow_b + 16 * w);
+            const uint4 u1 = *reinterpret_cast<const uint4*>(Vs + int64_t(i + a.ngrp) * mrow_b + 16 * w);
+            float w0[PV], w1[PV];
+            E::unpack(u0, w0);
+            E::unpack(u1, w1);
 #pragma unroll
             for (int t = 0; t < TC; ++t) {
-              const float xv = xsl[t * a.v_rows + i];
+              const float x0 = xsl[t * a.v_rows + i], x1 = xsl[t * a.v_rows + i + a.ngrp];
 #pragma unroll
-              for (int e = 0; e < PW; ++e) acc[t][e] = fmaf(xv, wv[e], acc[t][e]);
+              for (int e = 0; e < PV; ++e) acc[t][e] = fmaf(x1, w1[e], fmaf(x0, w0[e], acc[t][e]));
+            }
+          }
+          if (i < vn) {
+            const uint4 u0 = *reinterpret_cast<const uint4*>(Vs + int64_t(i) * mrow_b + 16 * w);
+            float w0[PV];
+            E::unpack(u0, w0);
+#pragma unroll
+            for (int t = 0; t < TC; ++t) {
+              const float x0 = xsl[t * a.v_rows + i];
+#pragma unroll
+              for (int e = 0; e < PV; ++e) acc[t][e] = fmaf(x0, w0[e], acc[t][e]);
             }
           }
 #pragma unroll
           for (int t = 0; t < TC; ++t)
 #pragma unroll
-            for (int e = 0; e < PW; ++e) red2[(grp_id * TC + t) * k + w * PW + e] = acc[t][e];
+            for (int e = 0; e < PV; e += 4)
+              *reinterpret_cast<float4*>(&red2[(grp_id * TC + t) * k + w * PV + e]) =
+                  make_float4(acc[t][e], acc[t][e + 1], acc[t][e + 2], acc[t][e + 3]);
         }
-      }
-      if (!started) {
-        cluster_wait();  // every CTA of the cluster is running: peers' shared memory is live
-        started = true;
       }
       __syncthreads();
+      // this CTA's partials to the workspace, laid out like the projection
+      // kernel's cluster partials (one "cluster" per CTA)
       for (int e = tid; e < TC * k; e += blockDim.x) {
-        float s2 = 0.f;
-        for (int g = 0; g < a.ngrp; ++g) s2 += red2[g * TC * k + e];
-        const int t = e / k, col = e - (e / k) * k;
-        const int q = col / ks;
-        cluster.map_shared_rank(inbox, q)[(rank * TC + t) * ks + (col - q * ks)] = s2;
-      }
-      if (tid < TC * CS) {
-        const int t = tid % TC, q = tid / TC;
-        cluster.map_shared_rank(inbox_x, q)[rank * TC + t] = xsq[t];
-      }
-      cluster.sync();
-      for (int e = tid; e < TC * ks; e += blockDim.x) {
-        const int t = e / ks, j = e - (e / ks) * ks;
-        float s2 = 0.f;
-#pragma unroll
-        for (int r = 0; r < CS; ++r) s2 += inbox[(r * TC + t) * ks + j];
-        gsl[e] = (t < tc && c0 + j < c1) ? s2 : 0.f;
-      }
-      if (tid < TC) {
-        float s2 = 0.f;
-#pragma unroll
-        for (int r = 0; r < CS; ++r) s2 += inbox_x[r * TC + tid];
-        nx2[tid] = s2;
-      }
-    }
-    if (a.mode != 2 && !FUSED) {
-      // -- g: this CTA's column slice summed over the projection clusters
-      if (tid < 256) {
-        for (int base = 0; base < E_ * grp; base += 256) {
-          const int id = base + tid;
-          const int e = id / grp, g = id - (id / grp) * grp;
-          const int t = e / ks, col = c0 + (e - (e / ks) * ks);
-          const bool valid = e < E_ && t < tc && col < c1;
-          float s = 0.f;
-          if (valid) {
-            const float* src = a.part_g + int64_t(t0 + t) * k + col;
-            int cl = g;
-            for (; cl + 3 * grp < a.nclu; cl += 4 * grp) {
-              const float v0 = __ldcg(src + cl * cstride), v1 = __ldcg(src + (cl + grp) * cstride);
-              const float v2 = __ldcg(src + (cl + 2 * grp) * cstride), v3 = __ldcg(src + (cl + 3 * grp) * cstride);
-              s += v0;
-              s += v1;
-              s += v2;
-              s += v3;
-            }
-            for (; cl < a.nclu; cl += grp) s += __ldcg(src + cl * cstride);
-          }
-          for (int o = 1; o < grp; o <<= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-          if (g == 0 && e < E_) gsl[e] = valid ? s : 0.f;
+        if (e / k < tc) {
+          float s2 = 0.f;
+          for (int g = 0; g < a.ngrp; ++g) s2 += red2[g * TC * k + e];
+          a.fpart_g[(int64_t(blockIdx.x) * T + t0) * k + e] = s2;
         }
-        if (warp == 0) {
-          // ||x||^2: every CTA sums the projection clusters' partials itself;
-          // lane l adds clusters l, l + 32, ... of every token (loads issued
-          // together), then the warp adds the lanes in a fixed order.
+      }
+      if (tid < tc) a.fpart_x[int64_t(blockIdx.x) * T + t0 + tid] = xsq[tid];
+      __syncthreads();
+      // every CTA's partials of this chunk are published
+      if (tid == 0 && !grid_barrier(a.ticket, gridDim.x, a.err)) ok = false;
+      ok = __syncthreads_and(ok) != 0;
+    }
+    if (a.mode != 2) {
+      // -- g: this CTA's column slice summed over the published partials
+      //    (the projection clusters', or every CTA's of a fused grid) in one
+      //    fixed order.  Thread (g, e) takes column e (consecutive threads:
+      //    consecutive columns, so a warp's loads are contiguous) and adds
+      //    partials g, g + grp, ... (16 loads in flight); the grp sums of a
+      //    column are then added in g order.  Every cluster gets the same bits.
+      // decode chunks: warp 0 issues its loads of the ||x||^2 partials first,
+      // so they are in flight together with the loads of g's partials
+      constexpr bool kXEarly = TC <= 2;
+      float xpart[kXEarly ? TC : 1][8];
+      const bool x_early = kXEarly && a.nclu <= 256;
+      if (kXEarly && x_early && warp == 0) {
 #pragma unroll
-          for (int t = 0; t < TC; ++t) {
-            float s = 0.f;
-            if (t < tc)
-              for (int cl = lane; cl < a.nclu; cl += 32) s += __ldcg(&a.part_x[int64_t(cl) * T + t0 + t]);
-            s = warp_sum(s);
-            if (lane == 0) nx2[t] = s;
+        for (int t = 0; t < (kXEarly ? TC : 1); ++t)
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const int cl = lane + 32 * u;
+            xpart[t][u] = (t < tc && cl < a.nclu) ? __ldcg(&a.part_x[int64_t(cl) * T + t0 + t]) : 0.f;
           }
+      }
+      if (grp > 1) {
+        if (tid < E_ * grp) {
+          const int g = tid / E_, e = tid - (tid / E_) * E_;
+          const int t = e / ks, col = c0 + (e - (e / ks) * ks);
+          float s = 0.f;
+          if (t < tc && col < c1) {
+            const float* src = a.part_g + int64_t(t0 + t) * k + col;
+            for (int cb = g; cb < a.nclu; cb += 16 * grp) {
+              float v[16];
+#pragma unroll
+              for (int u = 0; u < 16; ++u) {
+                const int cl = cb + u * grp;
+                v[u] = cl < a.nclu ? __ldcg(src + int64_t(cl) * cstride) : 0.f;
+              }
+#pragma unroll
+              for (int u = 0; u < 16; ++u) s += v[u];
+            }
+          }
+          red3[tid] = s;
+        }
+        __syncthreads();
+        if (tid < E_) {
+          float s = 0.f;
+          for (int g = 0; g < grp; ++g) s += red3[g * E_ + tid];
+          const int t = tid / ks, col = c0 + (tid - (tid / ks) * ks);
+          gsl[tid] = (t < tc && col < c1) ? s : 0.f;
+        }
+      } else {
+        for (int e = tid; e < E_; e += kApplyThreads) {
+          const int t = e / ks, col = c0 + (e - (e / ks) * ks);
+          float s = 0.f;
+          if (t < tc && col < c1) {
+            const float* src = a.part_g + int64_t(t0 + t) * k + col;
+            for (int cb = 0; cb < a.nclu; cb += 16) {
+              float v[16];
+#pragma unroll
+              for (int u = 0; u < 16; ++u) v[u] = cb + u < a.nclu ? __ldcg(src + int64_t(cb + u) * cstride) : 0.f;
+#pragma unroll
+              for (int u = 0; u < 16; ++u) s += v[u];
+            }
+          }
+          gsl[e] = (t < tc && col < c1) ? s : 0.f;
+        }
+      }
+      if (warp == 0) {
+        // ||x||^2: lane l adds partials l, l + 32, ... (8 in flight), then
+        // the warp adds the lanes in a fixed order
+#pragma unroll
+        for (int t = 0; t < TC; ++t) {
+          float s = 0.f;
+          if (kXEarly && x_early) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) s += xpart[kXEarly ? t : 0][u];
+          } else if (t < tc)
+            for (int cb = lane; cb < a.nclu; cb += 32 * 8) {
+              float v[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) {
+                const int cl = cb + 32 * u;
+                v[u] = cl < a.nclu ? __ldcg(&a.part_x[int64_t(cl) * T + t0 + t]) : 0.f;
+              }
+#pragma unroll
+              for (int u = 0; u < 8; ++u) s += v[u];
+            }
+          s = warp_sum(s);
+          if (lane == 0) nx2[t] = s;
         }
       }
     }
@@ -674,7 +749,9 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
         }
       wuse += issued;
     }
-    ok = __syncthreads_and(ok && *reinterpret_cast<volatile uint32_t*>(a.err) == 0) != 0;
+    // another chunk follows: stop applying if any CTA has met an error
+    // (the last chunk skips this read of the error word, an L2 round trip)
+    if (t0 + TC < T) ok = __syncthreads_and(ok && *reinterpret_cast<volatile uint32_t*>(a.err) == 0) != 0;
     // every CTA of the cluster is done with this chunk's g copy and shares
     // before the next chunk's pushes; after an error the remaining chunks
     // only pass through their barriers (a CTA leaving early would strand the

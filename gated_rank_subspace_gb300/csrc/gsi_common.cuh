@@ -226,7 +226,10 @@ struct Ctrl {
   uint32_t reserved;
   uint32_t err;        // device error word (0 = ok); set by bounded waits
   int32_t counts[2];   // {n_fast, n_slow} of the last gate
-  uint32_t pad[60];
+  // fused decode's grid barrier, one ticket counter per element type: the
+  // arrivals of all calls so far (zeroed by gsi_workspace_init, never reset)
+  unsigned long long ticket[2];
+  uint32_t pad[56];
 };
 static_assert(sizeof(Ctrl) == 256, "Ctrl is 256 bytes");
 

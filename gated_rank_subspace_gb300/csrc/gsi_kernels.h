@@ -51,9 +51,15 @@ struct DecideArgs {
   const uint8_t* flags_in;  // T stored flags (mode 2)
   int rows_per_cta, seg_bytes, wstages, x_stage_max, stage_m;
   int off_m, off_x, off_g, off_gram;
-  // fused decode (the cluster projects x itself)
+  // fused decode (the grid projects x itself): CTA b projects V rows
+  // [b * v_rows, ...), publishes its partials in fpart_g / fpart_x (laid out
+  // like the projection kernel's cluster partials, one per CTA) and meets the
+  // other CTAs at a grid barrier on the workspace's ticket counter
   const void* V;        // d x k
   int v_rows, ngrp, off_v, off_xs;
+  float* fpart_g;       // [grid][T][k]
+  float* fpart_x;       // [grid][T]
+  unsigned long long* ticket;
   // weights of the next map of a stack, staged in L2 while this one runs
   const char* next_v;
   uint64_t next_v_bytes;

@@ -79,6 +79,24 @@ inline StreamLayout layout_stream(int64_t d, int64_t k, int elem_bytes, int64_t 
   return L;
 }
 
+// Workspace layout of one fused-decode call: every CTA of the grid (at most
+// kFusedMaxCtas) publishes its partial g and ||x||^2 for the grid's barrier.
+constexpr int kFusedMaxCtas = 256;
+
+struct FusedLayout {
+  size_t ctrl, part_g, part_x, total;
+};
+
+inline FusedLayout layout_fused(int64_t k, int64_t T) {
+  FusedLayout L{};
+  size_t off = 0;
+  L.ctrl = off;    off += 256;
+  L.part_g = off;  off += align256(size_t(kFusedMaxCtas) * T * k * 4);
+  L.part_x = off;  off += align256(size_t(kFusedMaxCtas) * T * 4);
+  L.total = off;
+  return L;
+}
+
 // Workspace layout of one tensor-core-path call.
 struct TensorLayout {
   size_t ctrl, vt, g, gbf, gfast, xslow, idx, total;
@@ -142,7 +160,7 @@ inline DecidePlan plan_decide(int64_t d, int64_t d_out, int64_t k, int es, int64
   const int64_t xs = fused ? 0 : kXStage / row_b;
   p.x_stage_max = int(xs < p.tc ? xs : p.tc);
   size_t g_area = (size_t(p.tc) * k + size_t(p.tc) * ks + 8 * 2 * size_t(p.tc) + 2 * size_t(cs) * p.tc +
-                   6 * size_t(p.tc) + 40) * 4;
+                   6 * size_t(p.tc) + 40 + kApplyThreads + 4) * 4;
   const size_t bars = size_t(kApplyThreads / 32) * p.wstages * 8 + 24;
   size_t off = (bars + 127) & ~size_t(127);
   const size_t gram_b = size_t(ks) * k * 4;
@@ -161,13 +179,13 @@ inline DecidePlan plan_decide(int64_t d, int64_t d_out, int64_t k, int es, int64
   p.ngrp = 0;
   p.off_xs = 0;
   if (fused) {
-    // token slice, group partials, inboxes
-    p.v_rows = int(cdiv(d, cs));
-    const int words = int(mrow_b / 4);
-    p.ngrp = kApplyThreads / words >= 1 ? kApplyThreads / words : 1;
+    // CTA b projects rows [b * v_rows, (b + 1) * v_rows) of V: its token
+    // slice, the row groups' partial sums and its slice of ||x||^2
+    p.v_rows = int(cdiv(d, ncta));
+    const int vecs = int(mrow_b / 16);  // 16-byte vectors per V row
+    p.ngrp = kApplyThreads / vecs >= 1 ? kApplyThreads / vecs : 1;
     p.off_xs = int(off);
-    off += (size_t(p.tc) * p.v_rows + size_t(p.ngrp) * p.tc * k + size_t(cs) * p.tc * ks + size_t(cs) * p.tc +
-            size_t(p.tc) + 8) * 4;
+    off += (size_t(p.tc) * rup(p.v_rows, 4) + size_t(p.ngrp) * p.tc * k + size_t(p.tc) + 8) * 4;
     off = (off + 127) & ~size_t(127);
   }
   p.off_m = int(off);

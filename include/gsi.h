@@ -71,12 +71,16 @@ typedef enum gsi_status {
 typedef enum gsi_dtype { GSI_F32 = 0, GSI_BF16 = 1 } gsi_dtype;
 
 /* Which kernels run the map.
- *   FUSED  -- one launch per call for T <= 2: clusters of CTAs project the
- *             tokens on their own slices of V, decide, and apply;
+ *   FUSED  -- one launch per call for T <= 2: every CTA projects the tokens
+ *             on its own slab of V, the partials meet at a grid barrier on
+ *             the workspace, then clusters decide and apply;
  *   STREAM -- two launches (projection kernel, then decide-and-apply), any T;
  *   TENSOR -- tcgen05 contractions, bf16 only, for prefill-sized T.
- * AUTO picks TENSOR for bf16 with T >= 128 and STREAM otherwise; FUSED is
- * available on request (T <= 2 and a slice of V that fits shared memory). */
+ * AUTO picks FUSED for T <= 2 where a slab of V fits shared memory (and
+ * STREAM at run time on a device that cannot hold the fused grid), TENSOR
+ * for bf16 with T >= 128, STREAM otherwise.  The fused grid must be
+ * co-resident: its barrier gives up after ~2 s (GSI_ERR_TIMEOUT, and the
+ * workspace must then be re-initialised) if other work keeps SMs busy. */
 typedef enum gsi_path {
   GSI_PATH_AUTO = 0,
   GSI_PATH_STREAM = 1,
@@ -111,7 +115,9 @@ gsi_status gsi_linear_workspace_size(const gsi_map_desc* map, int64_t T, gsi_pat
                                      size_t* bytes);
 
 /* Zero a workspace before its first use (its control words must start at
- * zero; every call leaves them at zero again).  Enqueued on `stream`. */
+ * zero; calls keep them consistent from then on, so it is zeroed once).
+ * Zero it again after a call has reported GSI_ERR_TIMEOUT.  A workspace
+ * serves one stream at a time.  Enqueued on `stream`. */
 gsi_status gsi_workspace_init(void* workspace, size_t ws_bytes, void* stream);
 
 /* Read the device error word of a workspace (SYNCHRONISES `stream`).

@@ -267,10 +267,11 @@ def test_config5_prefill_tensor_path(gsi):
 
 
 # ------------------------------------------------------------------ fused single-launch decode
-@pytest.mark.parametrize("role", ["qkv", "out", "up"])
+@pytest.mark.parametrize("role", ["qkv", "out", "up", "down"])
 @pytest.mark.parametrize("T", [1, 2])
 def test_fused_decode_against_oracle(gsi, role, T):
-    """The single-launch decode (clusters project x on their own V slices)."""
+    """The single-launch decode (every CTA projects x on its own slab of V;
+    the partials meet at a grid barrier)."""
     m_in = synth.map_6b(role, T=24, n_slow=6)
     gm, X = upload(m_in)
     n = X.shape[0]
@@ -298,11 +299,13 @@ def test_fused_decode_against_oracle(gsi, role, T):
 
 
 def test_fused_rejects_what_it_cannot_run(gsi):
-    m_in = synth.map_6b("down", T=1, n_slow=0)  # d = 16384: the V slice does not fit
-    gm, X = upload(m_in)
-    with pytest.raises(gsi.GsiError):
-        gsi.workspace_size(gm, 1, "fused")
     small = synth.map_6b("out", T=4, n_slow=1)
     gm2, X2 = upload(small)
     with pytest.raises(gsi.GsiError):
-        gsi.workspace_size(gm2, 4, "fused")
+        gsi.workspace_size(gm2, 4, "fused")  # more than 2 tokens
+    d, k = 65536, 512  # one CTA's slab of V (d / 64 rows of 1 KB) does not fit shared memory
+    f = lambda *s: torch.zeros(*s, device="cuda", dtype=torch.bfloat16)
+    wide = gsi.Map(f(256, d), f(d, k), f(256, k), torch.zeros(k, k, device="cuda"))
+    with pytest.raises(gsi.GsiError):
+        gsi.workspace_size(wide, 1, "fused")
+    assert gsi.workspace_size(wide, 1, "stream") > 0
