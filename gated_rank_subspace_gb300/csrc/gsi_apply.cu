@@ -94,6 +94,41 @@ __device__ __forceinline__ bool grid_barrier(unsigned long long* ticket, unsigne
   return true;
 }
 
+// Exchanges inside a cluster: st.async stores into a peer's shared memory
+// that complete on the peer's mbarrier, so each CTA waits (acquire at
+// cluster scope, bounded) only for the bytes it receives.
+__device__ __forceinline__ uint32_t map_rank(uint32_t saddr, int r) {
+  uint32_t out;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(out) : "r"(saddr), "r"(r));
+  return out;
+}
+__device__ __forceinline__ void st_async_f32(uint32_t raddr, float v, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(raddr),
+               "r"(__float_as_uint(v)), "r"(rbar)
+               : "memory");
+}
+__device__ __forceinline__ bool bar_try_cluster(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(sa(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool bar_wait_cluster(uint64_t* b, uint32_t parity, uint32_t* err) {
+  if (bar_try_cluster(b, parity)) return true;
+  const long long t0 = clock64();
+  while (!bar_try_cluster(b, parity)) {
+    if (clock64() - t0 > kSpinCycles) {
+      atomicOr(err, kErrTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
 // 1-D bulk copy global -> shared (16-byte aligned, multiple of 16 bytes).
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* b) {
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -149,7 +184,9 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
   int* scount = flist + TC;                                    // [2]
   float* red3 = reinterpret_cast<float*>(scount + 4);          // [kApplyThreads] partial-sum scratch
   // fused decode only: V slab, token slice, partial sums
-  uint64_t* vbar = gfull_bar + 1;                              // [1] V slice copy
+  uint64_t* vbar = gfull_bar + 1;                              // [1] V slab copy
+  uint64_t* gx_bar = gfull_bar + 2;                            // [1] peers' slices of g received
+  uint64_t* qn_bar = gfull_bar + 3;                            // [1] peers' Gram / norm shares received
   const unsigned char* Vs = smem + a.off_v;                    // [v_rows][k] elements
   float* xsl = reinterpret_cast<float*>(smem + a.off_xs);      // [TC][v_rows]
   float* red2 = xsl + TC * ((a.v_rows + 3) & ~3);              // [ngrp][TC][k], 16-byte aligned
@@ -162,6 +199,8 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
     bar_init(mfull, 1);
     bar_init(gfull_bar, 1);
     bar_init(gfull_bar + 1, 1);
+    bar_init(gfull_bar + 2, 1);
+    bar_init(gfull_bar + 3, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -408,13 +447,16 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
         started = true;
       }
       __syncthreads();
-      // push this CTA's slice of g into every CTA's full copy
+      // push this CTA's slice of g into every CTA's full copy; each CTA
+      // receives TC x k floats per chunk (the slices partition [0, k))
+      const uint32_t xph = uint32_t(t0 / TC) & 1u;
+      if (tid == 0) bar_expect_tx(gx_bar, uint32_t(TC * k * 4));
       for (int e = tid; e < E_ * CS; e += blockDim.x) {
         const int q = e / E_, f = e - (e / E_) * E_;
         const int t = f / ks, col = c0 + (f - (f / ks) * ks);
-        if (col < c1) cluster.map_shared_rank(gfull, q)[t * k + col] = gsl[f];
+        if (col < c1) st_async_f32(map_rank(sa(gfull + t * k + col), q), gsl[f], map_rank(sa(gx_bar), q));
       }
-      cluster.sync();
+      if (!__all_sync(0xffffffffu, bar_wait_cluster(gx_bar, xph, a.err))) ok = false;
       // -- ||g||^2 and g^T Gram g over this CTA's Gram rows
       float qa[TC], na[TC];
 #pragma unroll
@@ -485,6 +527,7 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
         }
       }
       __syncthreads();
+      if (tid == 0) bar_expect_tx(qn_bar, uint32_t(CS * TC * 8));
       if (tid < TC * CS) {
         // this CTA's share of g^T Gram g and ||g||^2, pushed to every CTA
         const int t = tid % TC, dst = tid / TC;
@@ -493,10 +536,12 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
           q += qw[w * TC + t];
           n += nw[w * TC + t];
         }
-        cluster.map_shared_rank(qin, dst)[rank * TC + t] = q;
-        cluster.map_shared_rank(nin, dst)[rank * TC + t] = n;
+        const uint32_t rb = map_rank(sa(qn_bar), dst);
+        st_async_f32(map_rank(sa(qin + rank * TC + t), dst), q, rb);
+        st_async_f32(map_rank(sa(nin + rank * TC + t), dst), n, rb);
       }
-      cluster.sync();
+      // warp 0 decides (the shares of all CS ranks have landed)
+      if (warp == 0 && !__all_sync(0xffffffffu, bar_wait_cluster(qn_bar, xph, a.err))) ok = false;
       if (tid < TC) {
         int slow = 0;
         if (tid < tc) {
@@ -535,6 +580,7 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
     }
     // -- per-chunk token lists (every thread reads the same smem flags);
     //    decide-only calls apply nothing
+    __syncwarp();  // warp 0's lanes wrote the chunk's flags
     if (tid == 0) {
       int nf = 0, ns = 0;
       for (int t = 0; t < tc; ++t) {

@@ -161,7 +161,7 @@ inline DecidePlan plan_decide(int64_t d, int64_t d_out, int64_t k, int es, int64
   p.x_stage_max = int(xs < p.tc ? xs : p.tc);
   size_t g_area = (size_t(p.tc) * k + size_t(p.tc) * ks + 8 * 2 * size_t(p.tc) + 2 * size_t(cs) * p.tc +
                    6 * size_t(p.tc) + 40 + kApplyThreads + 4) * 4;
-  const size_t bars = size_t(kApplyThreads / 32) * p.wstages * 8 + 24;
+  const size_t bars = size_t(kApplyThreads / 32) * p.wstages * 8 + 40;  // + M, Gram, V, two exchanges
   size_t off = (bars + 127) & ~size_t(127);
   const size_t gram_b = size_t(ks) * k * 4;
   p.off_gram = 0;
