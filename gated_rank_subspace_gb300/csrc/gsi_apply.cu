@@ -73,7 +73,8 @@ __device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t parity, uint32_t*
 // call's CTAs reach the barrier only after the dependency wait on the previous
 // kernel, and every call's grid has the same n for an element type, so the
 // episode of ticket t ends at (t / n + 1) * n.  The grid is sized so that all
-// its CTAs are co-resident.
+// its CTAs are co-resident.  (Measured: taking the ticket with a returning
+// atomic beats a fire-and-forget add against a count read in advance.)
 __device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long* p) {
   unsigned long long v;
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
@@ -140,6 +141,10 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 template <bool B>
 struct BoolC {
   static constexpr bool value = B;
+};
+template <int N>
+struct IntC {
+  static constexpr int value = N;
 };
 
 // ------------------------------------------------------------------ kernel
@@ -603,38 +608,48 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
       if (m_live && !m_waited && !bar_wait(mfull, 0, a.err)) ok = false;
       if (ok) {
         const int nvm = mrow_b / 16;
-        constexpr int RB = 16;
-        for (int rb = warp * RB; rb < nrows; rb += NCW * RB) {
-          for (int f = 0; f < nf; ++f) {
-            const int t = flist[f];
-            float part[RB];
+        // RB rows per warp pass: the smallest block that gives all NCW
+        // warps rows, so few rows (small d_out, many CTAs) still use every warp
+        auto fast_rows = [&](auto rb_c) {
+          constexpr int RB = decltype(rb_c)::value;
+          for (int rb = warp * RB; rb < nrows; rb += NCW * RB) {
+            for (int f = 0; f < nf; ++f) {
+              const int t = flist[f];
+              float part[RB];
 #pragma unroll
-            for (int r = 0; r < RB; ++r) part[r] = 0.f;
-            for (int vv = lane; vv < nvm; vv += 32) {
-              float gv[PV];
+              for (int r = 0; r < RB; ++r) part[r] = 0.f;
+              for (int vv = lane; vv < nvm; vv += 32) {
+                float gv[PV];
 #pragma unroll
-              for (int e4 = 0; e4 < PV / 4; ++e4) {
-                const float4 g4 = *reinterpret_cast<const float4*>(gfull + t * k + vv * PV + 4 * e4);
-                gv[4 * e4] = g4.x;
-                gv[4 * e4 + 1] = g4.y;
-                gv[4 * e4 + 2] = g4.z;
-                gv[4 * e4 + 3] = g4.w;
-              }
+                for (int e4 = 0; e4 < PV / 4; ++e4) {
+                  const float4 g4 = *reinterpret_cast<const float4*>(gfull + t * k + vv * PV + 4 * e4);
+                  gv[4 * e4] = g4.x;
+                  gv[4 * e4 + 1] = g4.y;
+                  gv[4 * e4 + 2] = g4.z;
+                  gv[4 * e4 + 3] = g4.w;
+                }
 #pragma unroll
-              for (int r = 0; r < RB; ++r) {
-                if (rb + r < nrows) {
-                  float w[PV];
-                  E::unpack(*reinterpret_cast<const uint4*>(mrows + int64_t(rb + r) * mrow_b + vv * 16), w);
+                for (int r = 0; r < RB; ++r) {
+                  if (rb + r < nrows) {
+                    float w[PV];
+                    E::unpack(*reinterpret_cast<const uint4*>(mrows + int64_t(rb + r) * mrow_b + vv * 16), w);
 #pragma unroll
-                  for (int e = 0; e < PV; ++e) part[r] = fmaf(w[e], gv[e], part[r]);
+                    for (int e = 0; e < PV; ++e) part[r] = fmaf(w[e], gv[e], part[r]);
+                  }
                 }
               }
+              const float s = warp_reduce_multi<RB>(part, lane);
+              const int r = row_of_lane<RB>(lane);
+              if ((lane & (32 / RB - 1)) == 0 && rb + r < nrows) a.Y[int64_t(t0 + t) * d_out + r0 + rb + r] = s;
             }
-            const float s = warp_reduce_multi<RB>(part, lane);
-            const int r = row_of_lane<RB>(lane);
-            if ((lane & (32 / RB - 1)) == 0 && rb + r < nrows) a.Y[int64_t(t0 + t) * d_out + r0 + rb + r] = s;
           }
-        }
+        };
+        if (nrows <= NCW * 4)
+          fast_rows(IntC<4>{});
+        else if (nrows <= NCW * 8)
+          fast_rows(IntC<8>{});
+        else
+          fast_rows(IntC<16>{});
       }
     }
 
