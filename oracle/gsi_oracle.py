@@ -133,6 +133,55 @@ def gsi_stack(maps, Xs, eps):
     return [gsi_linear(W, M, V, X, eps) for (W, M, V), X in zip(maps, Xs)]
 
 
+def path_errors(W, M, V, X):
+    """Per-token accounting of what the fast path would cost (§2.2 and the
+    Theorem 4 bound; §4's static-projection control).
+
+    Returns (rho, err, ynorm): rho_t the residual ratio, err_t = ||M g_t - W x_t||
+    (the output error token t takes on the fast path) and ynorm_t = ||W x_t||
+    (the dense output's norm).
+    """
+    G = project(X, V)
+    rho = residual_ratio(X, residual(X, V, G))
+    Yf = fast_path(M, G)
+    Ys = slow_path(W, X)
+    return rho, np.linalg.norm(Yf - Ys, axis=1), np.linalg.norm(Ys, axis=1)
+
+
+def eps_sweep(rho, err, ynorm, eps_list, tokens_per_call=1):
+    """The gate at each threshold of `eps_list` (§2.2), given `path_errors`.
+
+    For each eps: (n_slow, n_slow_calls, rel_err) with n_slow the tokens the
+    gate sends to the slow path, n_slow_calls the calls (consecutive blocks
+    of `tokens_per_call` tokens) that hold at least one slow token and so read
+    W, and rel_err = sqrt(sum of err_t^2 over fast tokens) / sqrt(sum of
+    ynorm_t^2), the gated map's relative output error against dense W x
+    (slow tokens are exact).  eps = inf is the static projection: every token
+    with a finite ratio takes the fast path.
+    """
+    rho = np.asarray(rho, dtype=np.float64)
+    err = np.asarray(err, dtype=np.float64)
+    y2 = float(np.sum(np.asarray(ynorm, dtype=np.float64) ** 2))
+    T = len(rho)
+    out = []
+    for eps in eps_list:
+        slow = gate(rho, eps)
+        calls = [bool(slow[c:c + tokens_per_call].any()) for c in range(0, T, tokens_per_call)]
+        e2 = float(np.sum(err[~slow] ** 2))
+        out.append((int(slow.sum()), int(sum(calls)), float(np.sqrt(e2 / y2)) if y2 > 0 else 0.0))
+    return out
+
+
+def effective_params(shapes, slow_fraction):
+    """Parameters a token reads on average through maps of the given
+    (d, d_out, k) shapes when a fraction `slow_fraction` of its calls take
+    the slow path (§4 "effective parameter count": the parameters of the
+    directions the token visits): (1 - f) d_out k on the fast path (the
+    image M) plus f d_out d on the slow path (W)."""
+    f = float(slow_fraction)
+    return float(sum((1.0 - f) * d_out * k + f * d_out * d for d, d_out, k in shapes))
+
+
 def spectral_norm(W: np.ndarray, iters: int = 200) -> float:
     """||W||_2 for the Theorem 4 bound: SVD for small W, power iteration on W^T W otherwise."""
     if W.size <= 4_000_000:

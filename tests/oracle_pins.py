@@ -303,9 +303,72 @@ def pin_stack(o):
     _close(out[1][0], [[4, 3, 8], [4, 3, 0], [12, 0, 24]], 1e-12, "stack map 1 y")
 
 
+def pin_path_errors_axis(o, seed=24):
+    """Axis basis V = I[:, :k]: the fast path drops exactly W[:, k:] x[k:]
+    (closed form), and the dense output is W x."""
+    rs = np.random.default_rng(seed)
+    d, k, d_out, T = 12, 5, 7, 6
+    V = np.eye(d)[:, :k]
+    W = rs.standard_normal((d_out, d))
+    X = rs.standard_normal((T, d))
+    rho, err, ynorm = o.path_errors(W, W[:, :k], V, X)
+    want_err = [np.sqrt(sum(sum(W[i, j] * x[j] for j in range(k, d)) ** 2 for i in range(d_out))) for x in X]
+    want_y = [np.sqrt(sum(sum(W[i, j] * x[j] for j in range(d)) ** 2 for i in range(d_out))) for x in X]
+    want_rho = [np.sqrt(sum(v * v for v in x[k:]) / sum(v * v for v in x)) for x in X]
+    _close(err, want_err, 1e-12, "path_errors err (axis basis)")
+    _close(ynorm, want_y, 1e-12, "path_errors ynorm (axis basis)")
+    _close(rho, want_rho, 1e-12, "path_errors rho (axis basis)")
+
+
+def pin_sweep_by_hand(o):
+    """A sweep worked out by hand: ties go slow, NaN is slow at every eps,
+    a call reads W when any of its tokens is slow."""
+    rho = [0.0, 0.3, 0.5, float("nan"), 0.5]
+    err = [1.0, 2.0, 3.0, 4.0, 5.0]
+    ynorm = [1.0] * 5
+    got = o.eps_sweep(rho, err, ynorm, [0.0, 0.3, 0.5, 0.6, float("inf")], tokens_per_call=2)
+    want = [(5, 3, 0.0), (4, 3, np.sqrt(1 / 5)), (3, 2, 1.0), (1, 1, np.sqrt(39 / 5)), (1, 1, np.sqrt(39 / 5))]
+    for g, w in zip(got, want):
+        assert g[0] == w[0] and g[1] == w[1], f"sweep counts {g[:2]} != {w[:2]}"
+        assert abs(g[2] - w[2]) <= 1e-12, f"sweep error {g[2]} != {w[2]}"
+
+
+def pin_sweep_theorem4(o, seed=25):
+    """On an orthonormal basis every token's fast-path error obeys the
+    Theorem 4 bound ||W||_2 rho ||x||; the sweep is monotone in eps
+    (fewer slow tokens, larger error), exact at eps = 0, and at eps = inf
+    equals the static projection's error ||G M^T - X W^T|| / ||X W^T||."""
+    rs = np.random.default_rng(seed)
+    d, k, d_out, T = 40, 6, 9, 30
+    V = _rand_basis(rs, d, k)
+    W = rs.standard_normal((d_out, d))
+    X = (V @ rs.standard_normal((k, T))).T + 0.3 * rs.standard_normal((T, d))
+    M = W @ V
+    rho, err, ynorm = o.path_errors(W, M, V, X)
+    w2 = np.linalg.svd(W, compute_uv=False)[0]
+    bound = w2 * rho * np.linalg.norm(X, axis=1)
+    assert np.all(err <= bound * (1 + 1e-9) + 1e-12), "Theorem 4 bound violated"
+    eps = [0.0, 0.05, 0.1, 0.2, 0.4, 0.8, float("inf")]
+    sw = o.eps_sweep(rho, err, ynorm, eps)
+    assert sw[0][0] == T and sw[0][2] == 0.0, "eps = 0: every token slow, exact"
+    assert all(a[0] >= b[0] for a, b in zip(sw, sw[1:])), "slow count not monotone"
+    assert all(a[2] <= b[2] + 1e-15 for a, b in zip(sw, sw[1:])), "error not monotone"
+    static = np.linalg.norm((X @ V) @ M.T - X @ W.T) / np.linalg.norm(X @ W.T)
+    assert sw[-1][0] == 0 and abs(sw[-1][2] - static) <= 1e-12, "eps = inf is the static projection"
+
+
+def pin_effective_params(o):
+    """Effective parameters: d_out k per map on the fast path, d_out d on the slow path."""
+    assert o.effective_params([(4, 2, 1)], 0.0) == 2.0
+    assert o.effective_params([(4, 2, 1)], 1.0) == 8.0
+    assert o.effective_params([(4, 2, 1), (3, 5, 2)], 0.5) == 0.5 * (2 + 10) + 0.5 * (8 + 15)
+    six_b = [(4096, 12288, 256), (4096, 4096, 256), (4096, 16384, 256), (16384, 4096, 256)]
+    assert o.effective_params(six_b, 0.0) == (12288 + 4096 + 16384 + 4096) * 256
+
+
 ALL_PINS = [
     pin_hand_examples, pin_decomposition_geometry, pin_axis_basis, pin_eps_zero,
     pin_in_span, pin_full_rank, pin_theorem4, pin_eps_inf, pin_scaling,
     pin_permutation, pin_degenerate_tokens, pin_compact, pin_gram, pin_brute,
-    pin_stack,
+    pin_stack, pin_path_errors_axis, pin_sweep_by_hand, pin_sweep_theorem4, pin_effective_params,
 ]

@@ -36,6 +36,14 @@ MUTANTS = {
     "brute_tie": ("slow = not (rho < eps)", "slow = rho > eps"),
     "brute_slow_uses_image": ("Y[t][o] = sum(W[o][i] * x[i] for i in range(d))",
                               "Y[t][o] = sum(M[o][j] * g[j] for j in range(k))"),
+    "path_err_sign": ("np.linalg.norm(Yf - Ys, axis=1), np.linalg.norm(Ys, axis=1)",
+                      "np.linalg.norm(Yf + Ys, axis=1), np.linalg.norm(Ys, axis=1)"),
+    "path_ynorm_of_fast": ("np.linalg.norm(Yf - Ys, axis=1), np.linalg.norm(Ys, axis=1)",
+                           "np.linalg.norm(Yf - Ys, axis=1), np.linalg.norm(Yf, axis=1)"),
+    "sweep_error_all_tokens": ("e2 = float(np.sum(err[~slow] ** 2))", "e2 = float(np.sum(err ** 2))"),
+    "sweep_calls_all_slow": ("calls = [bool(slow[c:c + tokens_per_call].any())",
+                             "calls = [bool(slow[c:c + tokens_per_call].all())"),
+    "effective_swapped": ("(1.0 - f) * d_out * k + f * d_out * d", "f * d_out * k + (1.0 - f) * d_out * d"),
     "stack_shares_tokens": ("for (W, M, V), X in zip(maps, Xs)]", "for (W, M, V), X in zip(maps, Xs[:1] * len(Xs))]"),
 }
 
