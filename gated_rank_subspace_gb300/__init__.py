@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
         "gsi_linear_ex": [P(MapDesc), vp, i64, f32, vp, vp, vp, vp, sz, ctypes.c_int, vp],
         "gsi_stack_workspace_size": [P(MapDesc), i64, i64, P(sz)],
         "gsi_stack": [P(MapDesc), i64, P(vp), i64, f32, P(vp), P(vp), vp, sz, vp],
+        "gsi_path_errors": [P(MapDesc), vp, i64, vp, vp, vp, vp, vp, vp, vp, sz, vp],
+        "gsi_eps_sweep": [vp, vp, vp, i64, vp, i64, i64, vp, vp, vp, vp],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
@@ -214,6 +216,41 @@ def linear(m: Map, X: torch.Tensor, eps: float, Y=None, flags=None, rho=None, wo
                                _ptr(rho), _ptr(workspace), workspace.numel(), PATHS[path],
                                _stream(stream)))
     return Y, flags, rho
+
+
+def path_errors(m: Map, X: torch.Tensor, workspace=None, stream=None):
+    """Both candidate outputs of every token and their distance.
+
+    Returns (Y_fast, Y_slow, rho, err, ynorm): M g_t and W x_t rows, the
+    residual ratios, ||Y_fast[t] - Y_slow[t]|| and ||Y_slow[t]||.
+    """
+    _require_cuda(X)
+    T, dev = X.shape[0], X.device
+    f32 = dict(dtype=torch.float32, device=dev)
+    Yf, Ys = torch.empty(T, m.d_out, **f32), torch.empty(T, m.d_out, **f32)
+    rho, err, ynorm = torch.empty(T, **f32), torch.empty(T, **f32), torch.empty(T, **f32)
+    flags = torch.empty(T, dtype=torch.uint8, device=dev)
+    if workspace is None:
+        workspace = new_workspace(workspace_size(m, T), dev, stream)
+    desc = m.desc()
+    _check(lib().gsi_path_errors(ctypes.byref(desc), _ptr(X), T, _ptr(Yf), _ptr(Ys), _ptr(flags), _ptr(rho),
+                                 _ptr(err), _ptr(ynorm), _ptr(workspace), workspace.numel(), _stream(stream)))
+    return Yf, Ys, rho, err, ynorm
+
+
+def eps_sweep(rho: torch.Tensor, err: torch.Tensor, ynorm: torch.Tensor, eps, tokens_per_call: int = 1,
+              stream=None):
+    """The gate at each threshold of `eps`; returns (n_slow, n_slow_calls, rel_err) device tensors."""
+    _require_cuda(rho, err, ynorm)
+    dev = rho.device
+    e = torch.as_tensor(list(eps), dtype=torch.float32).to(dev)
+    n = e.numel()
+    n_slow = torch.empty(n, dtype=torch.int32, device=dev)
+    n_calls = torch.empty(n, dtype=torch.int32, device=dev)
+    rel = torch.empty(n, dtype=torch.float32, device=dev)
+    _check(lib().gsi_eps_sweep(_ptr(rho), _ptr(err), _ptr(ynorm), rho.numel(), _ptr(e), n, int(tokens_per_call),
+                               _ptr(n_slow), _ptr(n_calls), _ptr(rel), _stream(stream)))
+    return n_slow, n_calls, rel
 
 
 def gate(m: Map, X: torch.Tensor, eps: float, workspace=None, G=None, rho=None, flags=None,

@@ -515,6 +515,47 @@ gsi_status gsi_linear(const gsi_map_desc* map, const void* X, int64_t T, float e
   return gsi_linear_ex(map, X, T, eps, Y, flags, rho, workspace, ws_bytes, GSI_PATH_AUTO, stream);
 }
 
+gsi_status gsi_path_errors(const gsi_map_desc* map, const void* X, int64_t T, float* Y_fast, float* Y_slow,
+                           uint8_t* flags, float* rho, float* err, float* ynorm, void* workspace, size_t ws_bytes,
+                           void* stream) {
+  gsi_status s = check_map(map);
+  if (s != GSI_OK) return s;
+  if ((s = check_tokens(T, 0.f)) != GSI_OK) return s;
+  gsi_path p;
+  if ((s = resolve_path(map, T, GSI_PATH_AUTO, &p)) != GSI_OK) return s;
+  if (T == 0) return ok();
+  if ((s = check_ptr(X, "X")) != GSI_OK) return s;
+  if ((s = check_ptr(Y_fast, "Y_fast")) != GSI_OK) return s;
+  if ((s = check_ptr(Y_slow, "Y_slow")) != GSI_OK) return s;
+  if (!flags) return fail(GSI_ERR_INVALID_ARG, "flags is NULL");
+  if (!rho || !err || !ynorm || !aligned(rho, 4) || !aligned(err, 4) || !aligned(ynorm, 4))
+    return fail(GSI_ERR_INVALID_ARG, "rho, err and ynorm must be 4-byte aligned device arrays");
+  if ((s = check_workspace(workspace, ws_bytes, path_ws(map, T, p))) != GSI_OK) return s;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const float inf = __builtin_huge_valf();
+  if ((s = run_path(map, p, false, X, T, inf, Y_fast, flags, rho, workspace, st)) != GSI_OK) return s;
+  if ((s = run_path(map, p, false, X, T, 0.f, Y_slow, flags, nullptr, workspace, st)) != GSI_OK) return s;
+  if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
+  s = cuda_check(launch_path_norms(Y_fast, Y_slow, T, map->d_out, err, ynorm, st), "path-norm kernel launch");
+  return s == GSI_OK ? ok() : s;
+}
+
+gsi_status gsi_eps_sweep(const float* rho, const float* err, const float* ynorm, int64_t T, const float* eps,
+                         int64_t n_eps, int64_t tokens_per_call, int32_t* n_slow, int32_t* n_slow_calls,
+                         float* rel_err, void* stream) {
+  if (T < 0 || n_eps < 0) return fail(GSI_ERR_INVALID_ARG, "T and n_eps must be >= 0");
+  if (tokens_per_call < 1) return fail(GSI_ERR_INVALID_ARG, "tokens_per_call must be >= 1");
+  if (T > (int64_t(1) << 31) - 1 || n_eps > 65535) return fail(GSI_ERR_UNSUPPORTED, "T or n_eps too large");
+  if (n_eps == 0) return ok();
+  if (!eps || !n_slow || !n_slow_calls || !rel_err) return fail(GSI_ERR_INVALID_ARG, "a sweep output or eps is NULL");
+  if (T > 0 && (!rho || !err || !ynorm)) return fail(GSI_ERR_INVALID_ARG, "rho, err or ynorm is NULL");
+  if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
+  const gsi_status s = cuda_check(launch_sweep(rho, err, ynorm, T, eps, n_eps, tokens_per_call, n_slow, n_slow_calls,
+                                               rel_err, static_cast<cudaStream_t>(stream)),
+                                  "sweep kernel launch");
+  return s == GSI_OK ? ok() : s;
+}
+
 gsi_status gsi_stack_workspace_size(const gsi_map_desc* maps, int64_t n_maps, int64_t T, size_t* bytes) {
   if (!bytes) return fail(GSI_ERR_INVALID_ARG, "bytes is NULL");
   if (!maps || n_maps <= 0) return fail(GSI_ERR_INVALID_ARG, "maps is NULL or n_maps <= 0");

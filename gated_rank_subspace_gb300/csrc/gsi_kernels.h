@@ -105,6 +105,11 @@ cudaError_t launch_compact(const uint8_t* flags, int T, int32_t* idx, int32_t* c
                            cudaStream_t s);
 cudaError_t launch_decide_apply(const DecideArgs& a, const DecidePlan& p, gsi_dtype dt, cudaStream_t s);
 int decide_apply_max_clusters(size_t smem, gsi_dtype dt, bool fused, int cs);
+cudaError_t launch_path_norms(const float* Yf, const float* Ys, int64_t T, int64_t d_out, float* err, float* ynorm,
+                              cudaStream_t s);
+cudaError_t launch_sweep(const float* rho, const float* err, const float* ynorm, int64_t T, const float* eps,
+                         int64_t n_eps, int64_t tokens_per_call, int32_t* n_slow, int32_t* n_slow_calls,
+                         float* rel_err, cudaStream_t s);
 cudaError_t launch_image(const void* W, const void* V, void* M, float* gram, int64_t d,
                          int64_t d_out, int64_t k, gsi_dtype dt, cudaStream_t s);
 

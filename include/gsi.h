@@ -179,6 +179,31 @@ gsi_status gsi_stack(const gsi_map_desc* maps, int64_t n_maps, const void* const
                      int64_t T, float eps, float* const* Y, uint8_t* const* flags,
                      void* workspace, size_t ws_bytes, void* stream);
 
+/* §2.2 (Theorem 4) and §4 (static-projection control): both candidate
+ * outputs of every token, for error accounting and threshold sweeps.
+ * Y_fast (T x d_out float32) receives M g_t for every token (the map at
+ * eps = +inf; a token with a non-finite value still takes W x_t), Y_slow
+ * (T x d_out float32) receives W x_t (the map at eps = 0), rho (T float32)
+ * the residual ratios, err (T float32) ||Y_fast[t] - Y_slow[t]|| and ynorm
+ * (T float32) ||Y_slow[t]||.  flags (T bytes) is scratch.  All device
+ * pointers; the workspace is gsi_linear's.  Enqueued on `stream`. */
+gsi_status gsi_path_errors(const gsi_map_desc* map, const void* X, int64_t T, float* Y_fast, float* Y_slow,
+                           uint8_t* flags, float* rho, float* err, float* ynorm, void* workspace, size_t ws_bytes,
+                           void* stream);
+
+/* §2.2: the gate at each of n_eps thresholds eps[i] (device array), from
+ * gsi_path_errors' rho, err and ynorm.  n_slow[i] (int32) receives the
+ * tokens with !(rho < eps[i]) (ties and NaN are slow), n_slow_calls[i] the
+ * calls -- consecutive blocks of tokens_per_call tokens -- holding at least
+ * one slow token (the calls that read W), and rel_err[i] (float32) the
+ * gated map's relative output error against W x:
+ * sqrt(sum of err^2 over fast tokens) / sqrt(sum of ynorm^2).  eps = +inf is
+ * the static projection.  All device pointers; sums in double, fixed order.
+ * n_eps <= 65535.  Enqueued on `stream`. */
+gsi_status gsi_eps_sweep(const float* rho, const float* err, const float* ynorm, int64_t T, const float* eps,
+                         int64_t n_eps, int64_t tokens_per_call, int32_t* n_slow, int32_t* n_slow_calls,
+                         float* rel_err, void* stream);
+
 /* No counterpart in the paper: a library convenience.  gsi_linear for
  * callers that cannot allocate device memory (code where cudaMalloc is
  * forbidden or unavailable, such as an allocator hook, a plug-in inside a

@@ -132,3 +132,35 @@ def test_build_image_validation():
 def test_compact_validation():
     assert L.gsi_compact(0, 4, P, P, None) == 1
     assert L.gsi_compact(P, -1, P, P, None) == 1
+
+
+def test_path_errors_validation():
+    m = desc()
+    _, need = ws_size(m, 4)
+
+    def call(T=4, rho=P, err=P, ynorm=P, flags=P, ws_bytes=need):
+        return L.gsi_path_errors(ctypes.byref(m), P, T, P, P, flags, rho, err, ynorm, P, ws_bytes, None)
+
+    assert call(T=0) == 0
+    assert call(rho=None) == 1 and "aligned" in L.gsi_last_error().decode()
+    assert call(ynorm=P + 2) == 1
+    assert call(flags=None) == 1
+    assert call(ws_bytes=need - 1) == 4
+    L.gsi_debug_fail_after(1)
+    try:
+        assert call() == 3 and "injected" in L.gsi_last_error().decode()
+    finally:
+        L.gsi_debug_fail_after(0)
+
+
+def test_eps_sweep_validation():
+    def call(T=8, n_eps=3, tpc=1, eps=P, out=P, rho=P):
+        return L.gsi_eps_sweep(rho, P, P, T, eps, n_eps, tpc, out, P, P, None)
+
+    assert call(n_eps=0) == 0
+    assert call(tpc=0) == 1 and "tokens_per_call" in L.gsi_last_error().decode()
+    assert call(T=-1) == 1
+    assert call(n_eps=70000) == 2
+    assert call(eps=None) == 1
+    assert call(out=None) == 1
+    assert call(rho=None) == 1
