@@ -23,6 +23,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -223,6 +224,86 @@ def kernel_traffic():
     return KERNEL_TRAFFIC["bytes_per_launch"] if h == KERNEL_TRAFFIC["gsi_apply_sha256"] else None
 
 
+SWEEP_EPS = [0.0, 0.0125, 0.025, 0.05, 0.1, 0.2, 0.4, float("inf")]
+
+
+def run_sweep():
+    """The gate's trade-off across thresholds (eps = inf: static projection)
+    on configs 2-4, from the library's gsi_path_errors and gsi_eps_sweep:
+    slow fraction, relative output error against dense W x, modelled bytes
+    per token (W read by a call when any of its tokens is slow) and effective
+    parameters per token.  Prints one JSON line."""
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import gated_rank_subspace_gb300 as gsi
+
+    dev = torch.device("cuda")
+    n_eps = len(SWEEP_EPS)
+
+    def one_map(W, V, X, tpc):
+        gm = gsi.make_map(W.to(dev), V.to(dev))
+        Xd = X.to(dev)
+        _, _, rho, err, ynorm = gsi.path_errors(gm, Xd)
+        ns, nc, _ = gsi.eps_sweep(rho, err, ynorm, SWEEP_EPS, tpc)
+        T, (d_out, d), k = X.shape[0], W.shape, V.shape[1]
+        es = W.element_size()
+        r = rho.cpu().numpy()
+        n_calls = (T + tpc - 1) // tpc
+        fast_calls = [sum(bool((r[c:c + tpc] < e).any()) for c in range(0, T, tpc)) for e in SWEEP_EPS]
+        fixed = n_calls * (d * k * es + k * k * 4) + T * (d * es + d_out * 4)
+        nbytes = [fixed + fc * d_out * k * es + sc * d_out * d * es for fc, sc in zip(fast_calls, nc.cpu().tolist())]
+        dense = n_calls * d_out * d * es + T * (d * es + d_out * 4)
+        e2 = (err.double() ** 2).cpu().numpy()
+        e2_fast = [float(e2[r < e].sum()) for e in SWEEP_EPS]  # fast tokens (NaN: slow)
+        out = dict(T=T, ns=ns.cpu().tolist(), e2=e2_fast, y2=float((ynorm.double() ** 2).sum()), bytes=nbytes,
+                   dense=dense, params=(d_out * k, d_out * d))
+        del gm, Xd, rho, err, ynorm
+        return out
+
+    def summarize(parts, tokens):
+        y2 = sum(p["y2"] for p in parts)
+        rows = []
+        for i in range(n_eps):
+            slow = sum(p["ns"][i] for p in parts) / sum(p["T"] for p in parts)
+            eff = sum(((p["T"] - p["ns"][i]) * p["params"][0] + p["ns"][i] * p["params"][1]) / p["T"] for p in parts)
+            b = sum(p["bytes"][i] for p in parts) / tokens
+            rows.append({"eps": SWEEP_EPS[i] if math.isfinite(SWEEP_EPS[i]) else "inf",
+                         "slow_fraction": slow,
+                         "rel_err": math.sqrt(sum(p["e2"][i] for p in parts) / y2),
+                         "max_map_rel_err": max(math.sqrt(p["e2"][i] / p["y2"]) for p in parts),
+                         "MB_per_token": b / 1e6,
+                         "saved_vs_dense": sum(p["dense"] for p in parts) / tokens / b,
+                         "effective_params_per_token": eff})
+        return rows
+
+    report = {"metric": "gsi_eps_sweep", "data": "synthetic", "rows_per_config": {}}
+    # config 2: the bench's 6B layer maps, 256 single-token calls each
+    parts = [one_map(m.W, m.V, m.X, 1) for m in make_inputs()]
+    report["rows_per_config"]["cfg2 6B layer, 256 tokens, T=1 calls"] = summarize(parts, T_TOKENS)
+    # config 3: the first 4 layers of the depth-coherent 28-layer stack, 64 steps
+    bases, fr, base_W, tokens = synth.stack_config3(n_layers=4, steps=64)
+    parts = []
+    for l in range(4):
+        for role in synth.ROLES:
+            perm, signs = synth.layer_weight_rows(3, l, synth.ROLE_ID[role], base_W[role].shape[0])
+            W = (base_W[role][torch.from_numpy(perm)] * torch.from_numpy(signs).to(torch.bfloat16)[:, None]).contiguous()
+            parts.append(one_map(W, synth.storage(bases[role][l], torch.bfloat16), tokens[(l, role)], 1))
+    report["rows_per_config"]["cfg3 stack layers 0-3, 64 steps, T=1 calls"] = summarize(parts, 64)
+    # config 4: 13B maps (k = 320), calls of 16 tokens, Bernoulli slow labels
+    for f in (0.0, 0.05, 0.25, 1.0):
+        parts = []
+        for role in synth.ROLES:
+            d_out, d = synth.SHAPES_13B[role]
+            r = synth.ROLE_ID[role]
+            V64 = synth.orthonormal_basis(synth.rng(4, 0, r, 1), d, 320)
+            W = synth.storage(synth.gaussian_weight(synth.rng(4, 0, r, 2), d_out, d), torch.bfloat16)
+            X = synth.map_tokens(4, 0, r, V64, 64, f, bernoulli=True)
+            parts.append(one_map(W, synth.storage(V64, torch.bfloat16), X, 16))
+        report["rows_per_config"][f"cfg4 13B layer, f={f}, 64 tokens, T=16 calls"] = summarize(parts, 64)
+    print(json.dumps(report))
+
+
 def probe_map(role, eps):
     """Eight one-token gsi_linear calls of one 6B map (default stream)."""
     import __graft_entry__
@@ -259,7 +340,12 @@ def main():
                     help="only run 8 one-token gsi_linear calls of this 6B map (a small case for ncu)")
     ap.add_argument("--probe-eps", type=float, default=0.0,
                     help="threshold of the --probe-map calls (0: every token slow)")
+    ap.add_argument("--eps-sweep", action="store_true",
+                    help="only report the threshold sweep on configs 2-4 (one JSON line)")
     args = ap.parse_args()
+    if args.eps_sweep:
+        run_sweep()
+        return
     if args.probe_map:
         probe_map(args.probe_map, args.probe_eps)
         return
