@@ -182,6 +182,72 @@ def effective_params(shapes, slow_fraction):
     return float(sum((1.0 - f) * d_out * k + f * d_out * d for d, d_out, k in shapes))
 
 
+# ---------------------------------------------------------------- basis construction
+# "Gated Subspace Inference for Transformer Acceleration", §2.3 depth cascade
+# and calibration: the basis of a layer is computed once from a calibration
+# pass (the principal subspace of its activations); the next layer's basis
+# starts from this one and is corrected by rank-1 updates kept orthogonal by
+# DGKS re-orthogonalisation instead of a full SVD.  Readings: the principal
+# subspace is the top-k eigenvectors of X^T X for a calibration block X
+# (T x d); the correction is subspace iteration warm-started from the previous
+# layer's basis, each step orthonormalised column by column (one rank-1 update
+# of the projector per column) by classical Gram-Schmidt with the
+# Daniel-Gragg-Kaufman-Stewart test: project again when the norm after a
+# projection falls below eta = 1/sqrt(2) of the norm before it.
+
+
+def calibration_basis(X: np.ndarray, k: int) -> np.ndarray:
+    """Top-k principal directions of the activation block X (T x d): the
+    eigenvectors of X^T X with the k largest eigenvalues, as the columns of a
+    d x k matrix (largest first; each column's largest-magnitude entry
+    positive)."""
+    w, U = np.linalg.eigh(X.T @ X)
+    V = U[:, np.argsort(w)[::-1][:k]]
+    piv = np.argmax(np.abs(V), axis=0)
+    return V * np.sign(V[piv, np.arange(V.shape[1])])[None, :]
+
+
+def dgks_orthonormalize(A: np.ndarray, eta: float = 1.0 / np.sqrt(2.0)):
+    """Orthonormalise the columns of A (d x k) in order by classical
+    Gram-Schmidt with DGKS re-orthogonalisation.
+
+    Column j: v = a_j; h = Q_{<j}^T v; v <- v - Q_{<j} h; if ||v|| < eta * ||a_j||
+    the projection is repeated once on the result; q_j = v / ||v||.  Returns
+    (Q, n_reorth), n_reorth the number of columns projected twice.
+    """
+    d, k = A.shape
+    Q = np.zeros((d, k))
+    n_reorth = 0
+    for j in range(k):
+        v = A[:, j].astype(np.float64).copy()
+        before = np.linalg.norm(v)
+        v = v - Q[:, :j] @ (Q[:, :j].T @ v)
+        if np.linalg.norm(v) < eta * before:
+            v = v - Q[:, :j] @ (Q[:, :j].T @ v)
+            n_reorth += 1
+        Q[:, j] = v / np.linalg.norm(v)
+    return Q, n_reorth
+
+
+def subspace_step(X: np.ndarray, V: np.ndarray):
+    """One correction step: V <- DGKS-orthonormalise((X^T X) V), formed as
+    X^T (X V).  Returns (V_next, n_reorth)."""
+    return dgks_orthonormalize(X.T @ (X @ V))
+
+
+def coherence(Va: np.ndarray, Vb: np.ndarray) -> float:
+    """Mean squared cosine of the principal angles between span(Va) and
+    span(Vb) (orthonormal d x k bases): ||Va^T Vb||_F^2 / k.  It is a lower
+    bound on the mean cosine (each cosine lies in [0, 1])."""
+    return float(np.sum((Va.T @ Vb) ** 2) / Va.shape[1])
+
+
+def principal_cosines(Va: np.ndarray, Vb: np.ndarray) -> np.ndarray:
+    """Cosines of the principal angles between span(Va) and span(Vb):
+    the singular values of Va^T Vb, largest first."""
+    return np.linalg.svd(Va.T @ Vb, compute_uv=False)
+
+
 def spectral_norm(W: np.ndarray, iters: int = 200) -> float:
     """||W||_2 for the Theorem 4 bound: SVD for small W, power iteration on W^T W otherwise."""
     if W.size <= 4_000_000:

@@ -366,9 +366,80 @@ def pin_effective_params(o):
     assert o.effective_params(six_b, 0.0) == (12288 + 4096 + 16384 + 4096) * 256
 
 
+def pin_dgks_qr(o, seed=26):
+    """DGKS Gram-Schmidt on a well-conditioned A is the thin QR of A with a
+    positive R diagonal (the textbook factorisation, here through numpy's
+    Householder QR): Q^T Q = I, and no column needs a second projection."""
+    rs = np.random.default_rng(seed)
+    A = rs.standard_normal((30, 6))
+    Q, n = o.dgks_orthonormalize(A)
+    q, r = np.linalg.qr(A)
+    _close(Q, q * np.sign(np.diag(r))[None, :], 1e-12, "DGKS Q vs QR")
+    assert n == 0, "a well-conditioned A needs no re-orthogonalisation"
+
+
+def pin_dgks_reorth(o):
+    """Hand example: the second column is almost the first; after one
+    projection only 1e-9 of it is left (< ||a|| / sqrt 2), so it is projected
+    again; Q is the identity."""
+    A = np.array([[1.0, 1.0, 0.0], [0.0, 1e-9, 0.0], [0.0, 0.0, 5.0]])
+    Q, n = o.dgks_orthonormalize(A)
+    _close(Q, np.eye(3), 1e-15, "DGKS hand example Q")
+    assert n == 1, f"re-orthogonalised {n} columns, want 1"
+
+
+def _spectral_block(rs, T=60, d=24, r=10):
+    """X = A diag(sigma) U^T with known principal directions U (distinct,
+    decreasing sigma)."""
+    A = _rand_basis(rs, T, r)
+    U = _rand_basis(rs, d, r)
+    sig = np.linspace(3.0, 0.5, r)
+    return (A * sig[None, :]) @ U.T, U
+
+
+def pin_calibration_basis(o, seed=27):
+    """The calibration basis of X = A diag(sigma) U^T is U[:, :k] up to the
+    column signs, which put each column's largest-magnitude entry positive."""
+    rs = np.random.default_rng(seed)
+    X, U = _spectral_block(rs)
+    k = 4
+    V = o.calibration_basis(X, k)
+    _close(np.abs(V.T @ U[:, :k]), np.eye(k), 1e-10, "calibration basis vs U_k")
+    piv = np.argmax(np.abs(V), axis=0)
+    assert np.all(V[piv, np.arange(k)] > 0), "sign convention"
+
+
+def pin_subspace_iteration(o, seed=28):
+    """Subspace iteration reaches the principal subspace from a random start
+    (gap sigma_4 / sigma_5 > 1), and the principal subspace is a fixed point."""
+    rs = np.random.default_rng(seed)
+    X, U = _spectral_block(rs)
+    k = 4
+    V = _rand_basis(rs, X.shape[1], k)
+    for _ in range(80):
+        V, _ = o.subspace_step(X, V)
+    Uk = U[:, :k]
+    assert np.sum((Uk.T @ V) ** 2) / k >= 1 - 1e-10, "did not converge to span(U_k)"
+    W, _ = o.subspace_step(X, Uk)
+    assert np.sum((Uk.T @ W) ** 2) / k >= 1 - 1e-13, "principal subspace not fixed"
+
+
+def pin_coherence(o):
+    """Hand example: lines at angle theta in the plane have cos^2 theta;
+    a basis with itself 1, with its orthogonal complement 0."""
+    th = 0.3
+    a = np.array([[1.0], [0.0]])
+    b = np.array([[np.cos(th)], [np.sin(th)]])
+    assert abs(o.coherence(a, b) - np.cos(th) ** 2) <= 1e-15
+    _close(o.principal_cosines(a, b), [np.cos(th)], 1e-15, "principal cosine")
+    I = np.eye(4)
+    assert o.coherence(I[:, :2], I[:, :2]) == 1.0 and o.coherence(I[:, :2], I[:, 2:]) == 0.0
+
+
 ALL_PINS = [
     pin_hand_examples, pin_decomposition_geometry, pin_axis_basis, pin_eps_zero,
     pin_in_span, pin_full_rank, pin_theorem4, pin_eps_inf, pin_scaling,
     pin_permutation, pin_degenerate_tokens, pin_compact, pin_gram, pin_brute,
     pin_stack, pin_path_errors_axis, pin_sweep_by_hand, pin_sweep_theorem4, pin_effective_params,
+    pin_dgks_qr, pin_dgks_reorth, pin_calibration_basis, pin_subspace_iteration, pin_coherence,
 ]

@@ -44,6 +44,14 @@ MUTANTS = {
     "sweep_calls_all_slow": ("calls = [bool(slow[c:c + tokens_per_call].any())",
                              "calls = [bool(slow[c:c + tokens_per_call].all())"),
     "effective_swapped": ("(1.0 - f) * d_out * k + f * d_out * d", "f * d_out * k + (1.0 - f) * d_out * d"),
+    "dgks_never_again": ("if np.linalg.norm(v) < eta * before:", "if False:"),
+    "dgks_always_again": ("if np.linalg.norm(v) < eta * before:", "if np.linalg.norm(v) <= before:"),
+    "dgks_no_normalise": ("Q[:, j] = v / np.linalg.norm(v)", "Q[:, j] = v"),
+    "calibration_smallest": ("V = U[:, np.argsort(w)[::-1][:k]]", "V = U[:, np.argsort(w)[:k]]"),
+    "calibration_no_sign": ("return V * np.sign(V[piv, np.arange(V.shape[1])])[None, :]", "return V"),
+    "subspace_skips_cov": ("return dgks_orthonormalize(X.T @ (X @ V))", "return dgks_orthonormalize(V + 0 * X[:1, :1])"),
+    "coherence_not_squared": ("return float(np.sum((Va.T @ Vb) ** 2) / Va.shape[1])",
+                              "return float(np.sum(np.abs(Va.T @ Vb)) / Va.shape[1])"),
     "stack_shares_tokens": ("for (W, M, V), X in zip(maps, Xs)]", "for (W, M, V), X in zip(maps, Xs[:1] * len(Xs))]"),
 }
 
