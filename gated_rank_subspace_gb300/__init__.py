@@ -71,11 +71,17 @@ def lib() -> ctypes.CDLL:
         "gsi_stack": [P(MapDesc), i64, P(vp), i64, f32, P(vp), P(vp), vp, sz, vp],
         "gsi_path_errors": [P(MapDesc), vp, i64, vp, vp, vp, vp, vp, vp, vp, sz, vp],
         "gsi_eps_sweep": [vp, vp, vp, i64, vp, i64, i64, vp, vp, vp, vp],
+        "gsi_basis_orthonormalize": [vp, i64, i64, vp, vp],
+        "gsi_basis_step": [vp, ctypes.c_int, i64, i64, i64, vp, vp, sz, vp, vp],
+        "gsi_basis_coherence": [vp, vp, i64, i64, vp, vp, vp],
+        "gsi_basis_export": [vp, i64, i64, vp, ctypes.c_int, vp],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
         fn.argtypes = args
         fn.restype = ctypes.c_int
+    L.gsi_basis_step_work_bytes.argtypes = [i64, i64, i64]
+    L.gsi_basis_step_work_bytes.restype = sz
     L.gsi_last_error.argtypes = []
     L.gsi_last_error.restype = ctypes.c_char_p
     L.gsi_debug_fail_after.argtypes = [ctypes.c_int]
@@ -251,6 +257,48 @@ def eps_sweep(rho: torch.Tensor, err: torch.Tensor, ynorm: torch.Tensor, eps, to
     _check(lib().gsi_eps_sweep(_ptr(rho), _ptr(err), _ptr(ynorm), rho.numel(), _ptr(e), n, int(tokens_per_call),
                                _ptr(n_slow), _ptr(n_calls), _ptr(rel), _stream(stream)))
     return n_slow, n_calls, rel
+
+
+def basis_orthonormalize(Vt: torch.Tensor, stream=None):
+    """DGKS Gram-Schmidt of the rows of Vt (k x d float32) in place; returns
+    (Vt, n_reorth) with n_reorth a device int32 tensor."""
+    _require_cuda(Vt)
+    n = torch.zeros(1, dtype=torch.int32, device=Vt.device)
+    _check(lib().gsi_basis_orthonormalize(_ptr(Vt), Vt.shape[0], Vt.shape[1], _ptr(n), _stream(stream)))
+    return Vt, n
+
+
+def basis_step(X: torch.Tensor, Vt: torch.Tensor, work=None, stream=None):
+    """One correction step Vt <- DGKS((X^T X V)^T) on the calibration block X
+    (T x d, float32 or bfloat16); returns (Vt, n_reorth)."""
+    _require_cuda(X, Vt)
+    T, d = X.shape
+    k = Vt.shape[0]
+    if work is None:
+        work = new_workspace(int(lib().gsi_basis_step_work_bytes(T, d, k)), X.device, stream)
+    n = torch.zeros(1, dtype=torch.int32, device=X.device)
+    _check(lib().gsi_basis_step(_ptr(X), _dtype_code(X.dtype), T, d, k, _ptr(Vt), _ptr(work), work.numel(),
+                                _ptr(n), _stream(stream)))
+    return Vt, n
+
+
+def basis_coherence(Vt_a: torch.Tensor, Vt_b: torch.Tensor, stream=None) -> torch.Tensor:
+    """||Va^T Vb||_F^2 / k for two orthonormal bases held as k x d rows."""
+    _require_cuda(Vt_a, Vt_b)
+    k, d = Vt_a.shape
+    out = torch.empty(1, dtype=torch.float32, device=Vt_a.device)
+    work = torch.empty(k * k, dtype=torch.float32, device=Vt_a.device)
+    _check(lib().gsi_basis_coherence(_ptr(Vt_a), _ptr(Vt_b), k, d, _ptr(out), _ptr(work), _stream(stream)))
+    return out
+
+
+def basis_export(Vt: torch.Tensor, dtype=torch.bfloat16, stream=None) -> torch.Tensor:
+    """The basis in a map's layout: V = Vt^T (d x k, row-major) in `dtype`."""
+    _require_cuda(Vt)
+    k, d = Vt.shape
+    V = torch.empty(d, k, dtype=dtype, device=Vt.device)
+    _check(lib().gsi_basis_export(_ptr(Vt), k, d, _ptr(V), _dtype_code(dtype), _stream(stream)))
+    return V
 
 
 def gate(m: Map, X: torch.Tensor, eps: float, workspace=None, G=None, rho=None, flags=None,

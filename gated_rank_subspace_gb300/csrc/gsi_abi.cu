@@ -556,6 +556,81 @@ gsi_status gsi_eps_sweep(const float* rho, const float* err, const float* ynorm,
   return s == GSI_OK ? ok() : s;
 }
 
+static gsi_status check_basis(int64_t k, int64_t d) {
+  if (k < 1 || d < 1) return fail(GSI_ERR_INVALID_ARG, "k and d must be positive");
+  if (k > GSI_MAX_K) return fail(GSI_ERR_UNSUPPORTED, "k=%lld above GSI_MAX_K", (long long)k);
+  if (k > d) return fail(GSI_ERR_INVALID_ARG, "k=%lld above d=%lld", (long long)k, (long long)d);
+  if (d > (int64_t(1) << 31)) return fail(GSI_ERR_UNSUPPORTED, "d above 2^31");
+  return GSI_OK;
+}
+
+size_t gsi_basis_step_work_bytes(int64_t T, int64_t d, int64_t k) {
+  if (T < 1 || d < 1 || k < 1) return 0;
+  return align256(size_t(T) * k * 4) + size_t(k) * d * 4;
+}
+
+gsi_status gsi_basis_orthonormalize(float* Vt, int64_t k, int64_t d, int32_t* n_reorth, void* stream) {
+  gsi_status s = check_basis(k, d);
+  if (s != GSI_OK) return s;
+  if (!Vt || !aligned(Vt, 4)) return fail(GSI_ERR_INVALID_ARG, "Vt is NULL or misaligned");
+  if (n_reorth && !aligned(n_reorth, 4)) return fail(GSI_ERR_INVALID_ARG, "n_reorth is misaligned");
+  if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
+  s = cuda_check(launch_dgks(Vt, d, int(k), n_reorth, static_cast<cudaStream_t>(stream)), "DGKS kernel launch");
+  return s == GSI_OK ? ok() : s;
+}
+
+gsi_status gsi_basis_step(const void* X, gsi_dtype xdt, int64_t T, int64_t d, int64_t k, float* Vt, void* work,
+                          size_t work_bytes, int32_t* n_reorth, void* stream) {
+  gsi_status s = check_basis(k, d);
+  if (s != GSI_OK) return s;
+  if (T < 1) return fail(GSI_ERR_INVALID_ARG, "T must be positive");
+  if (xdt != GSI_F32 && xdt != GSI_BF16) return fail(GSI_ERR_INVALID_ARG, "unknown dtype %d", int(xdt));
+  if (!X || !aligned(X, xdt == GSI_BF16 ? 2 : 4)) return fail(GSI_ERR_INVALID_ARG, "X is NULL or misaligned");
+  if (!Vt || !aligned(Vt, 4)) return fail(GSI_ERR_INVALID_ARG, "Vt is NULL or misaligned");
+  const size_t need = gsi_basis_step_work_bytes(T, d, k);
+  if (!work || !aligned(work, 256) || work_bytes < need)
+    return fail(GSI_ERR_WORKSPACE, "work must be 256-byte aligned and hold %zu bytes", need);
+  if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  float* P = static_cast<float*>(work);                                              // T x k: X V
+  float* Zt = reinterpret_cast<float*>(static_cast<char*>(work) + align256(size_t(T) * k * 4));  // k x d
+  // P[t][i] = sum_r X[t][r] Vt[i][r];  Zt[i][r] = sum_t P[t][i] X[t][r]
+  if ((s = cuda_check(launch_contract(X, xdt, d, 1, Vt, GSI_F32, 1, d, P, k, T, k, d, st), "X V")) != GSI_OK) return s;
+  if ((s = cuda_check(launch_contract(P, GSI_F32, 1, k, X, xdt, d, 1, Zt, d, k, d, T, st), "X^T (X V)")) != GSI_OK)
+    return s;
+  if ((s = cuda_check(launch_dgks(Zt, d, int(k), n_reorth, st), "DGKS kernel launch")) != GSI_OK) return s;
+  s = cuda_check(cudaMemcpyAsync(Vt, Zt, size_t(k) * d * 4, cudaMemcpyDeviceToDevice, st), "basis copy");
+  return s == GSI_OK ? ok() : s;
+}
+
+gsi_status gsi_basis_coherence(const float* Vt_a, const float* Vt_b, int64_t k, int64_t d, float* out, float* work,
+                               void* stream) {
+  gsi_status s = check_basis(k, d);
+  if (s != GSI_OK) return s;
+  if (!Vt_a || !Vt_b || !out || !work || !aligned(Vt_a, 4) || !aligned(Vt_b, 4) || !aligned(out, 4) ||
+      !aligned(work, 4))
+    return fail(GSI_ERR_INVALID_ARG, "Vt_a, Vt_b, out and work must be 4-byte aligned device pointers");
+  if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // S[i][j] = sum_r Vt_a[i][r] Vt_b[j][r]
+  if ((s = cuda_check(launch_contract(Vt_a, GSI_F32, d, 1, Vt_b, GSI_F32, 1, d, work, k, k, k, d, st), "Va^T Vb")) !=
+      GSI_OK)
+    return s;
+  s = cuda_check(launch_sumsq(work, k * k, 1.f / float(k), out, st), "coherence reduction");
+  return s == GSI_OK ? ok() : s;
+}
+
+gsi_status gsi_basis_export(const float* Vt, int64_t k, int64_t d, void* V, gsi_dtype dt, void* stream) {
+  gsi_status s = check_basis(k, d);
+  if (s != GSI_OK) return s;
+  if (dt != GSI_F32 && dt != GSI_BF16) return fail(GSI_ERR_INVALID_ARG, "unknown dtype %d", int(dt));
+  if (!Vt || !V || !aligned(Vt, 4) || !aligned(V, dt == GSI_BF16 ? 2 : 4))
+    return fail(GSI_ERR_INVALID_ARG, "Vt or V is NULL or misaligned");
+  if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
+  s = cuda_check(launch_transpose_cast(Vt, k, d, V, dt, static_cast<cudaStream_t>(stream)), "basis export");
+  return s == GSI_OK ? ok() : s;
+}
+
 gsi_status gsi_stack_workspace_size(const gsi_map_desc* maps, int64_t n_maps, int64_t T, size_t* bytes) {
   if (!bytes) return fail(GSI_ERR_INVALID_ARG, "bytes is NULL");
   if (!maps || n_maps <= 0) return fail(GSI_ERR_INVALID_ARG, "maps is NULL or n_maps <= 0");

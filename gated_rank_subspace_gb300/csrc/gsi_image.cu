@@ -19,7 +19,7 @@ namespace gsi {
 
 constexpr int kTM = 64, kTN = 64, kTK = 16;
 
-template <class E>
+template <class EA, class EB>
 __global__ void __launch_bounds__(256) contract_kernel(const void* A, int64_t sam, int64_t sak,
                                                        const void* B, int64_t sbk, int64_t sbn,
                                                        void* C, int c_bf16, int64_t ldc,
@@ -43,13 +43,13 @@ __global__ void __launch_bounds__(256) contract_kernel(const void* A, int64_t sa
       const int mm = a_k_fast ? e / kTK : e % kTM;
       const int kk = a_k_fast ? e % kTK : e / kTM;
       const int64_t m = m0 + mm, kx = k0 + kk;
-      As[kk][mm] = (m < Md && kx < Kd) ? E::load1(A, m * sam + kx * sak) : 0.f;
+      As[kk][mm] = (m < Md && kx < Kd) ? EA::load1(A, m * sam + kx * sak) : 0.f;
     }
     for (int e = tid; e < kTN * kTK; e += 256) {
       const int nn = b_n_fast ? e % kTN : e / kTK;
       const int kk = b_n_fast ? e / kTN : e % kTK;
       const int64_t n = n0 + nn, kx = k0 + kk;
-      Bs[kk][nn] = (n < Nd && kx < Kd) ? E::load1(B, kx * sbk + n * sbn) : 0.f;
+      Bs[kk][nn] = (n < Nd && kx < Kd) ? EB::load1(B, kx * sbk + n * sbn) : 0.f;
     }
     __syncthreads();
 #pragma unroll
@@ -80,13 +80,26 @@ __global__ void __launch_bounds__(256) contract_kernel(const void* A, int64_t sa
     }
 }
 
-template <class E>
+template <class EA, class EB = EA>
 static cudaError_t contract(const void* A, int64_t sam, int64_t sak, const void* B, int64_t sbk,
                             int64_t sbn, void* C, int c_bf16, int64_t ldc, int64_t Md, int64_t Nd,
                             int64_t Kd, cudaStream_t s) {
   dim3 grid(unsigned(cdiv(Nd, kTN)), unsigned(cdiv(Md, kTM)));
-  contract_kernel<E><<<grid, 256, 0, s>>>(A, sam, sak, B, sbk, sbn, C, c_bf16, ldc, Md, Nd, Kd);
+  contract_kernel<EA, EB><<<grid, 256, 0, s>>>(A, sam, sak, B, sbk, sbn, C, c_bf16, ldc, Md, Nd, Kd);
   return cudaGetLastError();
+}
+
+// C (float32, Md x Nd, row stride ldc) = A (Md x Kd) B (Kd x Nd) through
+// element strides; A of element type adt, B of bdt.
+cudaError_t launch_contract(const void* A, gsi_dtype adt, int64_t sam, int64_t sak, const void* B, gsi_dtype bdt,
+                            int64_t sbk, int64_t sbn, float* C, int64_t ldc, int64_t Md, int64_t Nd, int64_t Kd,
+                            cudaStream_t s) {
+  if (adt == GSI_BF16 && bdt == GSI_F32)
+    return contract<BF16, F32>(A, sam, sak, B, sbk, sbn, C, 0, ldc, Md, Nd, Kd, s);
+  if (adt == GSI_F32 && bdt == GSI_BF16)
+    return contract<F32, BF16>(A, sam, sak, B, sbk, sbn, C, 0, ldc, Md, Nd, Kd, s);
+  if (adt == GSI_BF16) return contract<BF16>(A, sam, sak, B, sbk, sbn, C, 0, ldc, Md, Nd, Kd, s);
+  return contract<F32>(A, sam, sak, B, sbk, sbn, C, 0, ldc, Md, Nd, Kd, s);
 }
 
 cudaError_t launch_image(const void* W, const void* V, void* M, float* gram, int64_t d,

@@ -110,6 +110,13 @@ cudaError_t launch_path_norms(const float* Yf, const float* Ys, int64_t T, int64
 cudaError_t launch_sweep(const float* rho, const float* err, const float* ynorm, int64_t T, const float* eps,
                          int64_t n_eps, int64_t tokens_per_call, int32_t* n_slow, int32_t* n_slow_calls,
                          float* rel_err, cudaStream_t s);
+cudaError_t launch_contract(const void* A, gsi_dtype adt, int64_t sam, int64_t sak, const void* B, gsi_dtype bdt,
+                            int64_t sbk, int64_t sbn, float* C, int64_t ldc, int64_t Md, int64_t Nd, int64_t Kd,
+                            cudaStream_t s);
+// Basis construction (see gsi_basis.cu).
+cudaError_t launch_dgks(float* Qt, int64_t d, int k, int32_t* n_reorth, cudaStream_t s);
+cudaError_t launch_sumsq(const float* S, int64_t n, float scale, float* out, cudaStream_t s);
+cudaError_t launch_transpose_cast(const float* Qt, int64_t k, int64_t d, void* V, gsi_dtype dt, cudaStream_t s);
 cudaError_t launch_image(const void* W, const void* V, void* M, float* gram, int64_t d,
                          int64_t d_out, int64_t k, gsi_dtype dt, cudaStream_t s);
 

@@ -204,6 +204,39 @@ gsi_status gsi_eps_sweep(const float* rho, const float* err, const float* ynorm,
                          int64_t n_eps, int64_t tokens_per_call, int32_t* n_slow, int32_t* n_slow_calls,
                          float* rel_err, void* stream);
 
+/* §2.3 depth cascade and calibration.  A basis under construction is held
+ * transposed and in float32: Vt is k x d, row i is basis vector i (device).
+ * Readings: a layer's basis is the principal subspace of X^T X for a
+ * calibration block X (T x d tokens); the next layer's basis starts from the
+ * previous one and is corrected by steps V <- orthonormalise((X^T X) V),
+ * the orthonormalisation being classical Gram-Schmidt in column order with
+ * the DGKS test: a vector is projected a second time when its norm after a
+ * projection is below 1/sqrt(2) of its norm before.  k <= GSI_MAX_K, k <= d. */
+
+/* Orthonormalise the k rows of Vt in place (DGKS Gram-Schmidt).  n_reorth
+ * (device int32, nullable) receives the number of vectors projected twice.
+ * Rows that are linearly dependent on earlier ones give non-finite values. */
+gsi_status gsi_basis_orthonormalize(float* Vt, int64_t k, int64_t d, int32_t* n_reorth, void* stream);
+
+/* Bytes of `work` gsi_basis_step needs (host arithmetic; 0 for bad sizes). */
+size_t gsi_basis_step_work_bytes(int64_t T, int64_t d, int64_t k);
+
+/* One correction step on the calibration block X (T x d, element type xdt,
+ * row-major, device): Vt <- DGKS((X^T (X V))^T), in place.  work: device,
+ * 256-byte aligned, gsi_basis_step_work_bytes(T, d, k) bytes. */
+gsi_status gsi_basis_step(const void* X, gsi_dtype xdt, int64_t T, int64_t d, int64_t k, float* Vt, void* work,
+                          size_t work_bytes, int32_t* n_reorth, void* stream);
+
+/* Subspace coherence of two orthonormal bases (Vt_a, Vt_b: k x d float32):
+ * *out (device float32) = ||Va^T Vb||_F^2 / k, the mean squared cosine of the
+ * principal angles (a lower bound on the mean cosine).  work: k*k floats. */
+gsi_status gsi_basis_coherence(const float* Vt_a, const float* Vt_b, int64_t k, int64_t d, float* out, float* work,
+                               void* stream);
+
+/* Export a basis to a map's layout: V (d x k, row-major, dtype dt; bf16
+ * rounded to nearest even) = Vt^T. */
+gsi_status gsi_basis_export(const float* Vt, int64_t k, int64_t d, void* V, gsi_dtype dt, void* stream);
+
 /* No counterpart in the paper: a library convenience.  gsi_linear for
  * callers that cannot allocate device memory (code where cudaMalloc is
  * forbidden or unavailable, such as an allocator hook, a plug-in inside a

@@ -43,7 +43,7 @@ ROLE_ID = {r: i for i, r in enumerate(ROLES)}
 
 # Purpose codes mixed into the seed so that W, V, the token draws and the
 # slow-token labels of one map come from independent streams.
-_W, _V, _A, _N, _LBL, _CHAIN, _FRAC = 1, 2, 3, 4, 5, 6, 7
+_W, _V, _A, _N, _LBL, _CHAIN, _FRAC, _CAL = 1, 2, 3, 4, 5, 6, 7, 8
 
 
 def rng(config: int, layer: int, role: int, purpose: int) -> np.random.Generator:
@@ -260,3 +260,30 @@ def stack_config3(n_layers: int = 28, steps: int = 512, k: int = 256, eps: float
         for role in ROLES:
             tokens[(l, role)] = map_tokens(c, l, ROLE_ID[role], bases[role][l], steps, float(fr[l]), eps)
     return bases, fr, base_W, tokens
+
+
+def calibration_stream(config: int, n_layers: int, d: int, m: int, T: int, decay: float = 0.97,
+                       noise: float = 0.01, role: int = 0):
+    """Depth-coherent calibration blocks for basis construction.
+
+    Layer l's activations are x = U^(l) diag(sigma) a + noise * n with
+    U^(l) (d x m) the depth chain U^(l+1) = orth(U^(l) + 0.1 N(0,1)/sqrt(d)),
+    sigma_i = decay^i (a gradual spectrum, so the principal subspace is not
+    found in one step), a ~ N(0, I_m), n ~ N(0, I_d).  Returns
+    (U_list float64, blocks) with blocks[l] a T x d float64 array; round it
+    to the storage dtype with `storage`.
+    """
+    U = depth_chain(config, role, d, m, n_layers)
+    sig = decay ** np.arange(m)
+    blocks = []
+    for l in range(n_layers):
+        g = rng(config, l, role, _CAL)
+        a = g.standard_normal((T, m)) * sig[None, :]
+        blocks.append(a @ U[l].T + noise * g.standard_normal((T, d)))
+    return U, blocks
+
+
+def random_basis_t(config: int, k: int, d: int, salt: int = 0) -> np.ndarray:
+    """A seeded random start for basis construction: k x d Gaussian rows
+    (orthonormalised by the code under test)."""
+    return rng(config, 0, 0, _CAL * 1000 + salt).standard_normal((k, d))
