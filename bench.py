@@ -304,6 +304,75 @@ def run_sweep():
     print(json.dumps(report))
 
 
+def run_cascade(n_layers=4, d=4096, m=512, k=256, T=2048, target=0.999, ref_steps=100, cap=100):
+    """Basis construction on depth-coherent calibration blocks (bf16, 6B
+    width, spectrum 0.995^i with a gap of 0.5 at k): for each layer, the
+    steps until the basis is within `target` coherence of that layer's
+    converged basis (`ref_steps` steps from a random start), from a random
+    start and from the previous layer's basis (the cascade); the depth
+    coherence of consecutive layers' bases.  Prints one JSON line."""
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import gated_rank_subspace_gb300 as gsi
+
+    dev = torch.device("cuda")
+    U, blocks = synth.calibration_stream(6, n_layers, d=d, m=m, T=T, decay=0.995, gap_at=k, gap=0.5)
+    Xs = [synth.storage(b, torch.bfloat16).to(dev) for b in blocks]
+    work = gsi.new_workspace(int(gsi.lib().gsi_basis_step_work_bytes(T, d, k)), dev)
+
+    def start(l, salt):
+        Vt = torch.tensor(synth.random_basis_t(6, k, d, salt=100 * l + salt), dtype=torch.float32, device=dev)
+        gsi.basis_orthonormalize(Vt)
+        return Vt
+
+    def steps_to(X, Vt, ref):
+        c = gsi.basis_coherence(Vt, ref).item()
+        n = 0
+        while c < target and n < cap:
+            gsi.basis_step(X, Vt, work)
+            n += 1
+            c = gsi.basis_coherence(Vt, ref).item()
+        return n, c
+
+    # time of one step (two contractions of 2 T d k flop each, then DGKS)
+    Vt = start(0, 9)
+    for _ in range(2):
+        gsi.basis_step(Xs[0], Vt, work)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(5):
+        gsi.basis_step(Xs[0], Vt, work)
+    e1.record()
+    torch.cuda.synchronize()
+    step_ms = e0.elapsed_time(e1) / 5
+    layers, prev = [], None
+    for l in range(n_layers):
+        ref = start(l, 1)
+        for _ in range(ref_steps):
+            gsi.basis_step(Xs[l], ref, work)
+        n_cold, c_cold = steps_to(Xs[l], start(l, 2), ref)
+        row = {"layer": l, "cold_steps": n_cold, "cold_coherence": c_cold}
+        if prev is not None:
+            warm = prev.clone()
+            row["start_coherence"] = gsi.basis_coherence(warm, ref).item()
+            n_warm, c_warm = steps_to(Xs[l], warm, ref)
+            row.update(warm_steps=n_warm, warm_coherence=c_warm,
+                       saving=1 - n_warm / n_cold if n_cold else 0.0,
+                       depth_coherence=gsi.basis_coherence(prev, ref).item())
+        layers.append(row)
+        prev = ref
+    report = {"metric": "gsi_basis_cascade", "data": "synthetic",
+              "config": {"d": d, "k": k, "calibration_tokens": T, "dtype": "bf16 tokens, f32 basis",
+                         "spectrum": f"0.995^i over {m} directions, x0.5 from direction {k} on",
+                         "chain": "U(l+1) = orth(U(l) + 0.1 N/sqrt(d))",
+                         "target": f"coherence >= {target} with the layer's basis after {ref_steps} steps"},
+              "step_ms": step_ms, "step_gflop": 4 * T * d * k / 1e9,
+              "step_tflops": 4 * T * d * k / (step_ms * 1e-3) / 1e12, "layers": layers}
+    print(json.dumps(report))
+
+
 def probe_map(role, eps):
     """Eight one-token gsi_linear calls of one 6B map (default stream)."""
     import __graft_entry__
@@ -342,7 +411,12 @@ def main():
                     help="threshold of the --probe-map calls (0: every token slow)")
     ap.add_argument("--eps-sweep", action="store_true",
                     help="only report the threshold sweep on configs 2-4 (one JSON line)")
+    ap.add_argument("--cascade", action="store_true",
+                    help="only report basis construction on depth-coherent calibration blocks (one JSON line)")
     args = ap.parse_args()
+    if args.cascade:
+        run_cascade()
+        return
     if args.eps_sweep:
         run_sweep()
         return

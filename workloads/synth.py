@@ -263,18 +263,22 @@ def stack_config3(n_layers: int = 28, steps: int = 512, k: int = 256, eps: float
 
 
 def calibration_stream(config: int, n_layers: int, d: int, m: int, T: int, decay: float = 0.97,
-                       noise: float = 0.01, role: int = 0):
+                       noise: float = 0.01, role: int = 0, gap_at: int = 0, gap: float = 1.0):
     """Depth-coherent calibration blocks for basis construction.
 
     Layer l's activations are x = U^(l) diag(sigma) a + noise * n with
     U^(l) (d x m) the depth chain U^(l+1) = orth(U^(l) + 0.1 N(0,1)/sqrt(d)),
     sigma_i = decay^i (a gradual spectrum, so the principal subspace is not
-    found in one step), a ~ N(0, I_m), n ~ N(0, I_d).  Returns
+    found in one step), multiplied by `gap` for i >= gap_at when gap_at > 0
+    (a spectral gap that makes the top-gap_at subspace well defined),
+    a ~ N(0, I_m), n ~ N(0, I_d).  Returns
     (U_list float64, blocks) with blocks[l] a T x d float64 array; round it
     to the storage dtype with `storage`.
     """
     U = depth_chain(config, role, d, m, n_layers)
     sig = decay ** np.arange(m)
+    if gap_at > 0:
+        sig[gap_at:] *= gap
     blocks = []
     for l in range(n_layers):
         g = rng(config, l, role, _CAL)
