@@ -211,11 +211,15 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------- GPU
-# DRAM bytes per decide_apply_kernel launch over the step's 1024 stored-decision
-# launches, from one ncu capture of `bench.py --kernel-traffic`
-# (dram__bytes_read.sum + dram__bytes_write.sum, launches 2049-3072): valid only for the kernel source it was taken on (first 16 hex digits of the
-# SHA-256 of csrc/gsi_apply.cu); otherwise the roofline reports traffic null.
-KERNEL_TRAFFIC = {"gsi_apply_sha256": "dce71edd205b6b9e", "bytes_per_launch": 15.01558825e6 + 0.01082125e6}
+# DRAM bytes per launch of the step's kernel (decide_apply_kernel, one launch
+# per gated-map call) averaged over the step's 1024 launches, from one ncu
+# capture of `bench.py --kernel-traffic` (dram__bytes_read.sum +
+# dram__bytes_write.sum, decide_apply launches 1-1024, with --cache-control
+# none so that the L2 prefetch of the next map serves the next launch as in
+# the live step): valid only for the
+# kernel source it was taken on (first 16 hex digits of the SHA-256 of
+# csrc/gsi_apply.cu); otherwise the roofline reports traffic null.
+KERNEL_TRAFFIC = {"gsi_apply_sha256": "0b3164c7a7ec751d", "bytes_per_launch": 19459175.75}
 
 
 def kernel_traffic():
@@ -510,6 +514,15 @@ def main():
         step_gbs = ab["total"] / (ms * 1e-3) / 1e9
         hbm_peak, peak_kind = peaks()
 
+    # launches per gated-map call: one on the single-launch decode (AUTO's
+    # choice for one token where a slab of V fits), two on the streaming path
+    per_call = []
+    for b in base:
+        try:
+            gsi.workspace_size(b, 1, "fused")
+            per_call.append(1)
+        except gsi.GsiError:
+            per_call.append(2)
     # ---- per-kernel timing: the same 1024 calls split into their two launches
     # (gsi_gate then gsi_apply, each call with its own workspace), and each
     # kernel's launches captured in a CUDA graph of their own so that they run
@@ -581,11 +594,21 @@ def main():
     k_fast = ab["fast"] / (t_fast * 1e-3) / 1e9 if t_fast else None
     k_slow = ab["slow"] / (t_slow * 1e-3) / 1e9 if t_slow else None
     k_apply = (ab["fast"] + ab["slow"]) / (t_apply * 1e-3) / 1e9
-    # The dominant kernel is decide_apply_kernel: it moves M (fast tokens) or
-    # W (slow tokens), most of the step's bytes.  Its stored-decision launches
-    # (gsi_apply) time exactly that streaming, without the decision phase.
-    dom = dict(name="decide_apply_kernel (stored decision: y = M g fast, y = W x slow)", gbs=k_apply,
-               bytes_per_launch=(ab["fast"] + ab["slow"]) / n_launch, ms=t_apply / n_launch)
+    # The dominant kernel is decide_apply_kernel.  On the single-launch decode
+    # it is the step's only kernel: each launch moves one call's algorithmic
+    # bytes, and its mean launch interval over the timed replays (launch gaps
+    # included, so the achieved figure is a lower bound) is ms / 1024.  On the
+    # two-launch path its stored-decision launches (gsi_apply) are timed in a
+    # graph of their own.
+    if sum(per_call) == 4:
+        dom = dict(name="decide_apply_kernel (single-launch decode: projection, gate, M g / W x)",
+                   gbs=step_gbs, bytes_per_launch=ab["total"] / n_launch, ms=ms / n_launch,
+                   timing="CUDA events over the timed region (graph replays of the step); "
+                          "per-launch time = mean launch interval, gaps included")
+    else:
+        dom = dict(name="decide_apply_kernel (stored decision: y = M g fast, y = W x slow)", gbs=k_apply,
+                   bytes_per_launch=(ab["fast"] + ab["slow"]) / n_launch, ms=t_apply / n_launch,
+                   timing="CUDA events around a graph of this kernel's 1024 launches of one step")
 
     # ---- end to end: pinned host tokens in, outputs and flags out, every step
     Xh = [X.cpu().pin_memory() for X in Xs]
@@ -624,15 +647,6 @@ def main():
                "sample": f"{passes} passes of the 256 decode tokens through all four maps "
                          f"({dt:.1f} s of float64 numpy; BLAS threads = host cores)"}
 
-    # launches per gated-map call: one on the single-launch decode (AUTO's
-    # choice for one token where a slab of V fits), two on the streaming path
-    per_call = []
-    for b in base:
-        try:
-            gsi.workspace_size(b, 1, "fused")
-            per_call.append(1)
-        except gsi.GsiError:
-            per_call.append(2)
     gpu_launches = args.steps * T_TOKENS * sum(per_call)
     line = {
         "metric": "gsi_linear_tokens_per_s_batch1",
@@ -678,7 +692,7 @@ def main():
             "kernel": dom["name"], "bound": "hbm", "achieved": dom["gbs"], "peak": hbm_peak,
             "unit": "GB/s", "frac": dom["gbs"] / hbm_peak, "traffic": kernel_traffic(),
             "peak_kind": peak_kind,
-            "timing": "CUDA events around a graph of this kernel's 1024 launches of one step",
+            "timing": dom["timing"],
             "bytes_per_launch": dom["bytes_per_launch"], "ms_per_launch": dom["ms"],
         },
         "e2e": {"value": e2e_tps, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
