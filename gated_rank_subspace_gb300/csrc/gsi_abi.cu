@@ -280,6 +280,7 @@ static gsi_status run_decide(const gsi_map_desc* m, const void* X, int64_t T, fl
   a.off_m = dp.off_m;
   a.off_x = dp.off_x;
   a.off_g = dp.off_g;
+  a.off_y = dp.off_y;
   a.off_gram = dp.off_gram;
   if (fused) {
     const FusedLayout FL = layout_fused(m->k, T);

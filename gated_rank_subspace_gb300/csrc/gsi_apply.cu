@@ -277,6 +277,58 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
   while (grp < 32 && E_ * grp * 2 <= kApplyThreads) grp *= 2;
   const int64_t cstride = int64_t(T) * k;
 
+  float* ybuf = reinterpret_cast<float*>(smem + a.off_y);  // [TC][rows_per_cta]
+  // y[t][r] = M[r0 + r] . g_t for the tokens tok_of(0 .. ntok), each result
+  // handed to emit(t, r, value); warp w takes row blocks of RB rows, RB the
+  // smallest block that gives all NCW warps rows (few rows per CTA still use
+  // every warp)
+  auto fast_apply = [&](int ntok, auto tok_of, auto emit) {
+    const unsigned char* mrows = m_live ? Ms : static_cast<const unsigned char*>(a.M) + r0 * mrow_b;
+    const int nvm = mrow_b / 16;
+    auto fast_rows = [&](auto rb_c) {
+      constexpr int RB = decltype(rb_c)::value;
+      for (int rb = warp * RB; rb < nrows; rb += NCW * RB) {
+        for (int f = 0; f < ntok; ++f) {
+          const int t = tok_of(f);
+          float part[RB];
+#pragma unroll
+          for (int r = 0; r < RB; ++r) part[r] = 0.f;
+          for (int vv = lane; vv < nvm; vv += 32) {
+            float gv[PV];
+#pragma unroll
+            for (int e4 = 0; e4 < PV / 4; ++e4) {
+              const float4 g4 = *reinterpret_cast<const float4*>(gfull + t * k + vv * PV + 4 * e4);
+              gv[4 * e4] = g4.x;
+              gv[4 * e4 + 1] = g4.y;
+              gv[4 * e4 + 2] = g4.z;
+              gv[4 * e4 + 3] = g4.w;
+            }
+#pragma unroll
+            for (int r = 0; r < RB; ++r) {
+              if (rb + r < nrows) {
+                float w[PV];
+                E::unpack(*reinterpret_cast<const uint4*>(mrows + int64_t(rb + r) * mrow_b + vv * 16), w);
+#pragma unroll
+                for (int e = 0; e < PV; ++e) part[r] = fmaf(w[e], gv[e], part[r]);
+              }
+            }
+          }
+          const float sum = warp_reduce_multi<RB>(part, lane);
+          const int r = row_of_lane<RB>(lane);
+          if ((lane & (32 / RB - 1)) == 0 && rb + r < nrows) emit(t, rb + r, sum);
+        }
+      }
+    };
+    if (nrows <= NCW * 4)
+      fast_rows(IntC<4>{});
+    else if (nrows <= NCW * 8)
+      fast_rows(IntC<8>{});
+    else
+      fast_rows(IntC<16>{});
+  };
+  // decide-and-apply calls compute the fast outputs before the decision ends
+  const bool yspec = a.mode == 0 && nrows > 0;
+
   for (int t0 = 0; t0 < T; t0 += TC) {
     const int tc = min(TC, T - t0);
     if (a.mode != 2 && FUSED) {
@@ -545,6 +597,14 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
         st_async_f32(map_rank(sa(qin + rank * TC + t), dst), q, rb);
         st_async_f32(map_rank(sa(nin + rank * TC + t), dst), n, rb);
       }
+      // decide-and-apply: y = M g for every token of the chunk while the
+      // shares travel (the decision only picks which rows are kept)
+      if (yspec) {
+        if (m_live && !m_waited && !bar_wait(mfull, 0, a.err)) ok = false;
+        m_waited = m_waited || m_live;
+        if (ok)
+          fast_apply(tc, [](int f) { return f; }, [&](int t, int r, float v) { ybuf[t * a.rows_per_cta + r] = v; });
+      }
       // warp 0 decides (the shares of all CS ranks have landed)
       if (warp == 0 && !__all_sync(0xffffffffu, bar_wait_cluster(qn_bar, xph, a.err))) ok = false;
       if (tid < TC) {
@@ -601,55 +661,20 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
     __syncthreads();
     const int nf = scount[0], ns = scount[1];
 
-    // -- fast tokens: y = M g from the staged (or global) rows of M
-    if (nf > 0 && nrows > 0 && tid < 256) {
-      const unsigned char* mrows =
-          m_live ? Ms : static_cast<const unsigned char*>(a.M) + r0 * mrow_b;
-      if (m_live && !m_waited && !bar_wait(mfull, 0, a.err)) ok = false;
-      if (ok) {
-        const int nvm = mrow_b / 16;
-        // RB rows per warp pass: the smallest block that gives all NCW
-        // warps rows, so few rows (small d_out, many CTAs) still use every warp
-        auto fast_rows = [&](auto rb_c) {
-          constexpr int RB = decltype(rb_c)::value;
-          for (int rb = warp * RB; rb < nrows; rb += NCW * RB) {
-            for (int f = 0; f < nf; ++f) {
-              const int t = flist[f];
-              float part[RB];
-#pragma unroll
-              for (int r = 0; r < RB; ++r) part[r] = 0.f;
-              for (int vv = lane; vv < nvm; vv += 32) {
-                float gv[PV];
-#pragma unroll
-                for (int e4 = 0; e4 < PV / 4; ++e4) {
-                  const float4 g4 = *reinterpret_cast<const float4*>(gfull + t * k + vv * PV + 4 * e4);
-                  gv[4 * e4] = g4.x;
-                  gv[4 * e4 + 1] = g4.y;
-                  gv[4 * e4 + 2] = g4.z;
-                  gv[4 * e4 + 3] = g4.w;
-                }
-#pragma unroll
-                for (int r = 0; r < RB; ++r) {
-                  if (rb + r < nrows) {
-                    float w[PV];
-                    E::unpack(*reinterpret_cast<const uint4*>(mrows + int64_t(rb + r) * mrow_b + vv * 16), w);
-#pragma unroll
-                    for (int e = 0; e < PV; ++e) part[r] = fmaf(w[e], gv[e], part[r]);
-                  }
-                }
-              }
-              const float s = warp_reduce_multi<RB>(part, lane);
-              const int r = row_of_lane<RB>(lane);
-              if ((lane & (32 / RB - 1)) == 0 && rb + r < nrows) a.Y[int64_t(t0 + t) * d_out + r0 + rb + r] = s;
-            }
-          }
-        };
-        if (nrows <= NCW * 4)
-          fast_rows(IntC<4>{});
-        else if (nrows <= NCW * 8)
-          fast_rows(IntC<8>{});
-        else
-          fast_rows(IntC<16>{});
+    // -- fast tokens: y = M g.  Decide-and-apply calls computed it for every
+    //    token of the chunk while the decision's last exchange was in flight
+    //    (yspec): copy the fast tokens' rows out; otherwise compute it now.
+    if (nf > 0 && nrows > 0) {
+      if (yspec) {
+        for (int f = 0; f < nf; ++f) {
+          const int t = flist[f];
+          for (int r = tid; r < nrows; r += blockDim.x) a.Y[int64_t(t0 + t) * d_out + r0 + r] = ybuf[t * a.rows_per_cta + r];
+        }
+      } else {
+        if (m_live && !m_waited && !bar_wait(mfull, 0, a.err)) ok = false;
+        if (ok)
+          fast_apply(nf, [&](int f) { return flist[f]; },
+                     [&](int t, int r, float v) { a.Y[int64_t(t0 + t) * d_out + r0 + r] = v; });
       }
     }
 

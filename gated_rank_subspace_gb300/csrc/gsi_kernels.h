@@ -51,6 +51,7 @@ struct DecideArgs {
   const uint8_t* flags_in;  // T stored flags (mode 2)
   int rows_per_cta, seg_bytes, wstages, x_stage_max, stage_m;
   int off_m, off_x, off_g, off_gram;
+  int off_y;            // [TC][rows_per_cta] fast outputs computed before the decision (mode 0)
   // fused decode (the grid projects x itself): CTA b projects V rows
   // [b * v_rows, ...), publishes its partials in fpart_g / fpart_x (laid out
   // like the projection kernel's cluster partials, one per CTA) and meets the

@@ -129,6 +129,7 @@ constexpr int64_t kTensorMinT = 128;
 struct DecidePlan {
   int tc, grv, ncta, rows_per_cta, seg_bytes, wstages, x_stage_max, stage_m;
   int off_m, off_x, off_g, off_gram;  // off_gram = 0: Gram slice read from global
+  int off_y;                          // [tc][rows_per_cta] fast outputs computed before the decision
   bool fused;  // single-launch decode: the cluster projects x itself
   int cs;      // CTAs per cluster
   int ks;      // columns of g owned by each rank
@@ -175,6 +176,9 @@ inline DecidePlan plan_decide(int64_t d, int64_t d_out, int64_t k, int es, int64
   p.off_g = int(off);
   off += g_area;
   off = (off + 127) & ~size_t(127);
+  p.off_y = int(off);
+  off += size_t(p.tc) * size_t(cdiv(d_out, ncta)) * 4;
+  off = (off + 127) & ~size_t(127);
   p.v_rows = 0;
   p.ngrp = 0;
   p.off_xs = 0;
@@ -211,6 +215,7 @@ inline DecidePlan plan_decide(int64_t d, int64_t d_out, int64_t k, int es, int64
     if (grow > 0 && p.smem + shift <= smem_budget) {
       p.x_stage_max += int(grow);
       p.off_g += int(shift);
+      p.off_y += int(shift);
       if (fused) p.off_xs += int(shift);
       p.off_m += int(shift);
       p.off_v += int(shift);
