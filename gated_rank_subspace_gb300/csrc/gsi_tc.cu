@@ -164,18 +164,21 @@ struct TcArgs {
 
 constexpr int kBM = 128, kBK = 64;
 
-template <int BN>
+// SG: pipeline stages (0: the default for BN -- 4 for BN = 256, else 6).
+// Short contractions (K = 256) take 3 stages, so two CTAs share an SM and
+// one's epilogue overlaps the other's loads and MMAs.
+template <int BN, int SG = 0>
 struct TcCfg {
-  static constexpr int STAGES = BN >= 256 ? 4 : 6;
+  static constexpr int STAGES = SG > 0 ? SG : (BN >= 256 ? 4 : 6);
   static constexpr uint32_t A_BYTES = kBM * kBK * 2;
   static constexpr uint32_t B_BYTES = BN * kBK * 2;
   static constexpr size_t SMEM = 1024 + size_t(STAGES) * (A_BYTES + B_BYTES) + 256;
 };
 
-template <int BN>
+template <int BN, int SG>
 __global__ void __launch_bounds__(128, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb, TcArgs a) {
-  using C = TcCfg<BN>;
+  using C = TcCfg<BN, SG>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = base;
@@ -243,25 +246,37 @@ __global__ void __launch_bounds__(128, 1)
   // tcgen05.ld is warp-collective: decide per warp, never per thread.
   const bool go = __all_sync(0xffffffffu, ok && *reinterpret_cast<volatile uint32_t*>(a.err) == 0);
   if (go) {
-    const int r = m_tile * kBM + warp * 32 + lane;
-    const bool live = r < rows;
-    const int64_t orow = live ? (a.row_map ? int64_t(__ldcg(&a.row_map[r])) : int64_t(r)) : 0;
-    float* crow = a.C + orow * a.ldc;
-    const bool vec = (a.ldc % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.C) & 15) == 0);
+    // The pipeline buffers are idle (every MMA, and so every operand load,
+    // has completed): each warp stages its 32 rows x BN columns there, then
+    // writes whole row segments -- consecutive lanes on consecutive columns,
+    // 16-byte stores -- instead of one 16-byte piece of 32 rows per store.
+    constexpr int LD = BN + 4;  // staged row stride in floats (conflict-free 16-byte accesses)
+    static_assert(size_t(kBM) * LD * 4 <= size_t(C::STAGES) * (C::A_BYTES + C::B_BYTES), "staging fits");
+    float* st = reinterpret_cast<float*>(sA) + size_t(warp) * 32 * LD;
 #pragma unroll 1
     for (int c = 0; c < BN; c += 16) {
       float v[16];
       tmem_ld16(tmem + (uint32_t(warp * 32) << 16) + uint32_t(c), v);
-      const int col0 = n_tile * BN + c;
-      if (live) {
-        if (vec && col0 + 16 <= a.N) {
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            *reinterpret_cast<float4*>(crow + col0 + 4 * q) =
-                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<float4*>(st + lane * LD + c + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    }
+    __syncwarp();
+    const int r_base = m_tile * kBM + warp * 32;
+    const int my_r = r_base + lane;
+    const int64_t my_orow = my_r < rows ? (a.row_map ? int64_t(__ldcg(&a.row_map[my_r])) : int64_t(my_r)) : 0;
+    const bool vec = (a.ldc % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.C) & 15) == 0);
+    for (int i = 0; i < 32 && r_base + i < rows; ++i) {
+      const int64_t orow = __shfl_sync(0xffffffffu, my_orow, i);
+      float* crow = a.C + orow * a.ldc + int64_t(n_tile) * BN;
+      const float* srow = st + i * LD;
+      for (int q = lane; q < BN / 4; q += 32) {
+        const int col = n_tile * BN + 4 * q;
+        if (vec && col + 4 <= a.N) {
+          *reinterpret_cast<float4*>(crow + 4 * q) = *reinterpret_cast<const float4*>(srow + 4 * q);
         } else {
-          for (int q = 0; q < 16; ++q)
-            if (col0 + q < a.N) crow[col0 + q] = v[q];
+          for (int e2 = 0; e2 < 4; ++e2)
+            if (col + e2 < a.N) crow[4 * q + e2] = srow[4 * q + e2];
         }
       }
     }
@@ -425,25 +440,23 @@ static cudaError_t make_map_2d(CUtensorMap* m, const void* ptr, int64_t rows, in
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int BN>
+template <int BN, int SG = 0>
 static cudaError_t launch_tc_gemm_t(const void* A, int64_t a_rows, const void* B, int64_t b_rows, int K,
                                     const TcArgs& args, cudaStream_t s) {
   CUtensorMap ta, tb;
   cudaError_t e = make_map_2d(&ta, A, a_rows, K, kBM);
   if (e != cudaSuccess) return e;
   if ((e = make_map_2d(&tb, B, b_rows, K, BN)) != cudaSuccess) return e;
-  auto kern = tc_gemm_kernel<BN>;
+  auto kern = tc_gemm_kernel<BN, SG>;
   static bool attr = false;
   if (!attr) {
-    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(TcCfg<BN>::SMEM))) !=
-        cudaSuccess)
-      return e;
+    if ((e = set_kernel_smem(kern, TcCfg<BN, SG>::SMEM)) != cudaSuccess) return e;
     attr = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(cdiv(a_rows, kBM)), unsigned(cdiv(b_rows, BN)));
   cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = TcCfg<BN>::SMEM;
+  cfg.dynamicSmemBytes = TcCfg<BN, SG>::SMEM;
   cfg.stream = s;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -458,7 +471,9 @@ cudaError_t launch_tc_gemm(const void* A, int64_t a_rows, const void* B, int64_t
                            const TcArgs& args, cudaStream_t s) {
   switch (bn) {
     case 64: return launch_tc_gemm_t<64>(A, a_rows, B, b_rows, K, args, s);
-    case 128: return launch_tc_gemm_t<128>(A, a_rows, B, b_rows, K, args, s);
+    case 128:
+      return K <= 256 ? launch_tc_gemm_t<128, 3>(A, a_rows, B, b_rows, K, args, s)
+                      : launch_tc_gemm_t<128>(A, a_rows, B, b_rows, K, args, s);
     default: return launch_tc_gemm_t<256>(A, a_rows, B, b_rows, K, args, s);
   }
 }
