@@ -102,12 +102,15 @@ struct TensorLayout {
   size_t ctrl, vt, g, gbf, gfast, xslow, idx, total;
 };
 
+// Split-K slices of the tensor path's projection contraction G = X V_k.
+constexpr int kGSplit = 8;
+
 inline TensorLayout layout_tensor(int64_t d, int64_t k, int64_t T) {
   TensorLayout L{};
   size_t off = 0;
   L.ctrl = off;   off += 256;
   L.vt = off;     off += align256(size_t(k) * d * 2);
-  L.g = off;      off += align256(size_t(T) * k * 4);
+  L.g = off;      off += align256(size_t(kGSplit) * T * k * 4);  // kGSplit partial projections
   L.gbf = off;    off += align256(size_t(T) * k * 2);
   L.gfast = off;  off += align256(size_t(T) * k * 2);
   L.xslow = off;  off += align256(size_t(T) * d * 2);

@@ -160,6 +160,8 @@ struct TcArgs {
   int64_t ldc;
   const int32_t* row_map;  // output row of A-row m is row_map[m] (null: m)
   uint32_t* err;
+  int ksplit;              // K is cut into ksplit slices (grid z); 0 or 1: none
+  int64_t c_split;         // elements between the slices' outputs
 };
 
 constexpr int kBM = 128, kBK = 64;
@@ -210,7 +212,11 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int nk = (a.K + kBK - 1) / kBK;
+  // this CTA's slice of K (grid z): k-blocks [kb0, kb0 + nk)
+  const int nk_all = (a.K + kBK - 1) / kBK;
+  const int ns = a.ksplit > 1 ? a.ksplit : 1;
+  const int kb0 = int(int64_t(nk_all) * blockIdx.z / ns);
+  const int nk = int(int64_t(nk_all) * (blockIdx.z + 1) / ns) - kb0;
   __shared__ int s_issued;  // k-blocks whose TMA loads were issued
 
   if (threadIdx.x == 0) {
@@ -220,8 +226,8 @@ __global__ void __launch_bounds__(128, 1)
       const uint32_t ph = (kb / C::STAGES) & 1;
       if (kb >= C::STAGES && !mbar_wait(&empty[s], ph ^ 1, a.err)) break;
       mbar_expect_tx(&full[s], C::A_BYTES + C::B_BYTES);
-      tma_load_2d(sA + s * C::A_BYTES, &ta, &full[s], kb * kBK, m_tile * kBM);
-      tma_load_2d(sB + s * C::B_BYTES, &tb, &full[s], kb * kBK, n_tile * BN);
+      tma_load_2d(sA + s * C::A_BYTES, &ta, &full[s], (kb0 + kb) * kBK, m_tile * kBM);
+      tma_load_2d(sB + s * C::B_BYTES, &tb, &full[s], (kb0 + kb) * kBK, n_tile * BN);
     }
     s_issued = kb;
   } else if (threadIdx.x == 32) {
@@ -268,7 +274,7 @@ __global__ void __launch_bounds__(128, 1)
     const bool vec = (a.ldc % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.C) & 15) == 0);
     for (int i = 0; i < 32 && r_base + i < rows; ++i) {
       const int64_t orow = __shfl_sync(0xffffffffu, my_orow, i);
-      float* crow = a.C + orow * a.ldc + int64_t(n_tile) * BN;
+      float* crow = a.C + int64_t(blockIdx.z) * a.c_split + orow * a.ldc + int64_t(n_tile) * BN;
       const float* srow = st + i * LD;
       for (int q = lane; q < BN / 4; q += 32) {
         const int col = n_tile * BN + 4 * q;
@@ -315,7 +321,8 @@ constexpr int kFinTok = 8;
 __global__ void __launch_bounds__(256) tc_finalize_kernel(const uint16_t* __restrict__ X, const float* __restrict__ G,
                                                           const float* __restrict__ gram, int64_t d, int k, int T,
                                                           float eps, float* __restrict__ rho_out,
-                                                          uint8_t* __restrict__ flags, uint16_t* __restrict__ Gbf) {
+                                                          uint8_t* __restrict__ flags, uint16_t* __restrict__ Gbf,
+                                                          int gsplit) {
   extern __shared__ float fsm[];
   float* gs = fsm;                       // [kFinTok][k]
   float* red = gs + kFinTok * k;         // [8 warps][kFinTok][2]
@@ -325,7 +332,10 @@ __global__ void __launch_bounds__(256) tc_finalize_kernel(const uint16_t* __rest
   pdl_wait();
   for (int e = tid; e < kFinTok * k; e += 256) {
     const int t = e / k, j = e - (e / k) * k;
-    const float g = (t0 + t < T) ? __ldcg(&G[int64_t(t0 + t) * k + j]) : 0.f;
+    // g = the split-K slices' partial projections, added in slice order
+    float g = 0.f;
+    if (t0 + t < T)
+      for (int sl = 0; sl < gsplit; ++sl) g += __ldcg(&G[(int64_t(sl) * T + t0 + t) * k + j]);
     gs[e] = g;
     if (t0 + t < T) {
       __nv_bfloat16 b = __float2bfloat16_rn(g);
@@ -454,7 +464,7 @@ static cudaError_t launch_tc_gemm_t(const void* A, int64_t a_rows, const void* B
     attr = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(cdiv(a_rows, kBM)), unsigned(cdiv(b_rows, BN)));
+  cfg.gridDim = dim3(unsigned(cdiv(a_rows, kBM)), unsigned(cdiv(b_rows, BN)), unsigned(args.ksplit > 1 ? args.ksplit : 1));
   cfg.blockDim = dim3(128);
   cfg.dynamicSmemBytes = TcCfg<BN, SG>::SMEM;
   cfg.stream = s;
@@ -509,7 +519,12 @@ cudaError_t launch_tensor_path(const TensorArgs& t, cudaStream_t s) {
   g.C = t.G;
   g.ldc = k;
   g.err = t.err;
-  if ((e = launch_tc_gemm(t.X, T, t.Vt, k, int(d), 64, g, s)) != cudaSuccess) return e;
+  // 128 x 256 tiles where k >= 256 (at k = 256, X is read once) and K cut
+  // into kGSplit slices for parallelism; the finalize kernel adds the slices
+  const int gsplit = int(cdiv(d, kBK)) < kGSplit ? int(cdiv(d, kBK)) : kGSplit;  // each slice >= 1 k-block
+  g.ksplit = gsplit;
+  g.c_split = T * k;
+  if ((e = launch_tc_gemm(t.X, T, t.Vt, k, int(d), k >= 256 ? 256 : 64, g, s)) != cudaSuccess) return e;
   // 3. rho, flags, bf16 g
   {
     const void* X = t.X;
@@ -521,7 +536,8 @@ cudaError_t launch_tensor_path(const TensorArgs& t, cudaStream_t s) {
     float* rho = t.rho;
     uint8_t* flags = t.flags;
     uint16_t* Gbf = t.Gbf;
-    void* args[] = {&X, &G, &gram, &dd, &kk, &TT, &eps, &rho, &flags, &Gbf};
+    int gs = gsplit;
+    void* args[] = {&X, &G, &gram, &dd, &kk, &TT, &eps, &rho, &flags, &Gbf, &gs};
     const size_t smem = size_t(kFinTok) * k * 4 + 8 * kFinTok * 2 * 4 + kFinTok * 4;
     if (smem > 48 * 1024) {
       if ((e = cudaFuncSetAttribute(tc_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem))) !=
