@@ -18,9 +18,79 @@
 
 namespace gsi {
 
-__global__ void __launch_bounds__(32) compact_kernel(const uint8_t* flags, int T, int32_t* idx,
-                                                     int32_t* counts) {
-  compact_warp(flags, T, idx, counts, threadIdx.x);
+// Stable compaction by one 1024-thread CTA: per chunk of 4096 flags, thread
+// i takes flags 4i .. 4i + 3 (loaded together), a block scan of the per-thread
+// fast / slow counts gives each thread its output positions, and chunks
+// follow one another with running totals.  Token order is kept in both lists.
+constexpr int kCompactThreads = 1024;
+constexpr int kCompactPer = 4;
+
+__global__ void __launch_bounds__(kCompactThreads) compact_kernel(const uint8_t* flags, int T, int32_t* idx,
+                                                                  int32_t* counts) {
+  __shared__ int wf[kCompactThreads / 32], wsl[kCompactThreads / 32];
+  __shared__ int tot[2];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int base_f = 0, base_s = 0;
+  for (int c0 = 0; c0 < T; c0 += kCompactThreads * kCompactPer) {
+    int kind[kCompactPer];  // 0: none, 1: fast, 2: slow
+    int nf = 0, ns = 0;
+#pragma unroll
+    for (int u = 0; u < kCompactPer; ++u) {
+      const int t = c0 + tid * kCompactPer + u;
+      kind[u] = t < T ? (ld_cg_u8(flags + t) != 0 ? 2 : 1) : 0;
+      nf += kind[u] == 1;
+      ns += kind[u] == 2;
+    }
+    // inclusive scans inside the warp, then over the warps' totals
+    int xf = nf, xs = ns;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int yf = __shfl_up_sync(0xffffffffu, xf, o), ys = __shfl_up_sync(0xffffffffu, xs, o);
+      if (lane >= o) {
+        xf += yf;
+        xs += ys;
+      }
+    }
+    if (lane == 31) {
+      wf[warp] = xf;
+      wsl[warp] = xs;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      int a = wf[lane], b = wsl[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int ya = __shfl_up_sync(0xffffffffu, a, o), yb = __shfl_up_sync(0xffffffffu, b, o);
+        if (lane >= o) {
+          a += ya;
+          b += yb;
+        }
+      }
+      wf[lane] = a - wf[lane];  // exclusive
+      wsl[lane] = b - wsl[lane];
+      if (lane == 31) {
+        tot[0] = a;
+        tot[1] = b;
+      }
+    }
+    __syncthreads();
+    int of = base_f + wf[warp] + xf - nf, os = base_s + wsl[warp] + xs - ns;
+    if (idx) {
+#pragma unroll
+      for (int u = 0; u < kCompactPer; ++u) {
+        const int t = c0 + tid * kCompactPer + u;
+        if (kind[u] == 1) idx[of++] = t;
+        if (kind[u] == 2) idx[T + os++] = t;
+      }
+    }
+    base_f += tot[0];
+    base_s += tot[1];
+    __syncthreads();  // wf / wsl / tot are rewritten by the next chunk
+  }
+  if (tid == 0 && counts) {
+    counts[0] = base_f;
+    counts[1] = base_s;
+  }
 }
 
 template <class E, int TC>
@@ -195,7 +265,7 @@ cudaError_t launch_gate(const GateArgs& a, const GatePlan& p, gsi_dtype dt, cuda
 
 cudaError_t launch_compact(const uint8_t* flags, int T, int32_t* idx, int32_t* counts,
                            cudaStream_t s) {
-  compact_kernel<<<1, 32, 0, s>>>(flags, T, idx, counts);
+  compact_kernel<<<1, kCompactThreads, 0, s>>>(flags, T, idx, counts);
   return cudaGetLastError();
 }
 

@@ -330,16 +330,32 @@ __global__ void __launch_bounds__(256) tc_finalize_kernel(const uint16_t* __rest
   const int t0 = blockIdx.x * kFinTok;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   pdl_wait();
-  for (int e = tid; e < kFinTok * k; e += 256) {
-    const int t = e / k, j = e - (e / k) * k;
-    // g = the split-K slices' partial projections, added in slice order
-    float g = 0.f;
-    if (t0 + t < T)
-      for (int sl = 0; sl < gsplit; ++sl) g += __ldcg(&G[(int64_t(sl) * T + t0 + t) * k + j]);
-    gs[e] = g;
-    if (t0 + t < T) {
-      __nv_bfloat16 b = __float2bfloat16_rn(g);
-      Gbf[int64_t(t0 + t) * k + j] = *reinterpret_cast<uint16_t*>(&b);
+  // g = the split-K slices' partial projections, added in slice order; a
+  // thread loads the slices of 4 elements (32 loads in flight) before adding
+  for (int e0 = tid; e0 < kFinTok * k; e0 += 256 * 4) {
+    float v[4][kGSplit];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int e = e0 + q * 256;
+      const int t = e / k, j = e - (e / k) * k;
+      const bool live = e < kFinTok * k && t0 + t < T;
+#pragma unroll
+      for (int sl = 0; sl < kGSplit; ++sl)
+        v[q][sl] = (live && sl < gsplit) ? __ldcg(&G[(int64_t(sl) * T + t0 + t) * k + j]) : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int e = e0 + q * 256;
+      if (e >= kFinTok * k) break;
+      const int t = e / k, j = e - (e / k) * k;
+      float g = 0.f;
+#pragma unroll
+      for (int sl = 0; sl < kGSplit; ++sl) g += v[q][sl];
+      gs[e] = g;
+      if (t0 + t < T) {
+        __nv_bfloat16 b = __float2bfloat16_rn(g);
+        Gbf[int64_t(t0 + t) * k + j] = *reinterpret_cast<uint16_t*>(&b);
+      }
     }
   }
   __syncthreads();
@@ -351,7 +367,19 @@ __global__ void __launch_bounds__(256) tc_finalize_kernel(const uint16_t* __rest
 #pragma unroll
     for (int t = 0; t < kFinTok; ++t) h[t] = 0.f;
     if (gram) {
-      for (int i = 0; i < k; ++i) {
+      // Gram rows in batches of 32 loads in flight (a row at a time would
+      // wait one L2 round trip per row), added in row order
+      int i = 0;
+      for (; i + 32 <= k; i += 32) {
+        float gv[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) gv[u] = __ldg(&gram[int64_t(i + u) * k + j]);
+#pragma unroll
+        for (int u = 0; u < 32; ++u)
+#pragma unroll
+          for (int t = 0; t < kFinTok; ++t) h[t] = fmaf(gs[t * k + i + u], gv[u], h[t]);
+      }
+      for (; i < k; ++i) {
         const float gij = __ldg(&gram[int64_t(i) * k + j]);
 #pragma unroll
         for (int t = 0; t < kFinTok; ++t) h[t] = fmaf(gs[t * k + i], gij, h[t]);

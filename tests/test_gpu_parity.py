@@ -71,7 +71,7 @@ def test_gate_only_config1(gsi):
     assert np.array_equal(f[~band], orc.gate(ro, m_in.eps)[~band])
 
 
-@pytest.mark.parametrize("T", [0, 1, 31, 32, 33, 100, 2048])
+@pytest.mark.parametrize("T", [0, 1, 31, 32, 33, 100, 2048, 4095, 4096, 4097, 12289])
 def test_compact_bit_exact(gsi, T):
     rs = np.random.default_rng(T)
     f = (rs.random(T) < 0.3).astype(np.uint8)
