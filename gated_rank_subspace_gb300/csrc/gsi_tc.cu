@@ -396,12 +396,20 @@ __global__ void __launch_bounds__(256) tc_finalize_kernel(const uint16_t* __rest
   if (warp < kFinTok) {
     float s = 0.f;
     if (t0 + warp < T) {
+      // eight 16-byte loads in flight per lane, then their squares in order
       const uint4* xr = reinterpret_cast<const uint4*>(X + int64_t(t0 + warp) * d);
-      for (int64_t v = lane; v < d / 8; v += 32) {
-        float f[8];
-        BF16::unpack(ld_cg_v4(xr + v), f);
+      const int64_t nv = d / 8;
+      for (int64_t v0 = lane; v0 < nv; v0 += 32 * 8) {
+        uint4 xq[8];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) s = fmaf(f[e], f[e], s);
+        for (int u = 0; u < 8; ++u) xq[u] = v0 + 32 * u < nv ? ld_cg_v4(xr + v0 + 32 * u) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          float f[8];
+          BF16::unpack(xq[u], f);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) s = fmaf(f[e], f[e], s);
+        }
       }
     }
     s = warp_sum(s);
