@@ -166,21 +166,26 @@ struct TcArgs {
 
 constexpr int kBM = 128, kBK = 64;
 
-// SG: pipeline stages (0: the default for BN -- 4 for BN = 256, else 6).
-// Short contractions (K = 256) take 3 stages, so two CTAs share an SM and
-// one's epilogue overlaps the other's loads and MMAs.
-template <int BN, int SG = 0>
+// SG: pipeline stages (0: the default -- 4 for BN = 256, else 6; 3 when the
+// CTA takes two row tiles).  Short contractions (K = 256) take 3 stages, so
+// two CTAs share an SM and one's epilogue overlaps the other's loads and MMAs.
+// MT: 128-row tiles of A per CTA; with MT = 2 every B tile feeds two MMAs
+// into two TMEM accumulators (B is read from L2 half as often).
+template <int BN, int SG = 0, int MT = 1>
 struct TcCfg {
-  static constexpr int STAGES = SG > 0 ? SG : (BN >= 256 ? 4 : 6);
-  static constexpr uint32_t A_BYTES = kBM * kBK * 2;
+  static constexpr int STAGES = SG > 0 ? SG : (MT > 1 ? 3 : (BN >= 256 ? 4 : 6));
+  static constexpr uint32_t A_TILE = kBM * kBK * 2;  // one 128-row tile of a stage
+  static constexpr uint32_t A_BYTES = MT * A_TILE;
+  static constexpr int TMEM_COLS = BN * MT;
+  static_assert(TMEM_COLS <= 512, "TMEM holds 512 columns");
   static constexpr uint32_t B_BYTES = BN * kBK * 2;
   static constexpr size_t SMEM = 1024 + size_t(STAGES) * (A_BYTES + B_BYTES) + 256;
 };
 
-template <int BN, int SG>
+template <int BN, int SG, int MT>
 __global__ void __launch_bounds__(128, 1)
     tc_gemm_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb, TcArgs a) {
-  using C = TcCfg<BN, SG>;
+  using C = TcCfg<BN, SG, MT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = base;
@@ -194,7 +199,7 @@ __global__ void __launch_bounds__(128, 1)
   const int m_tile = blockIdx.x, n_tile = blockIdx.y;
   pdl_wait();
   const int rows = a.rows_dev ? __ldcg(a.rows_dev) : a.rows;
-  if (m_tile * kBM >= rows) return;  // whole CTA, before any barrier or TMEM
+  if (m_tile * kBM * MT >= rows) return;  // whole CTA, before any barrier or TMEM
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -205,7 +210,7 @@ __global__ void __launch_bounds__(128, 1)
     fence_barrier_init();
   }
   if (warp == 0) {
-    tmem_alloc(tmem_slot, BN);
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -226,7 +231,7 @@ __global__ void __launch_bounds__(128, 1)
       const uint32_t ph = (kb / C::STAGES) & 1;
       if (kb >= C::STAGES && !mbar_wait(&empty[s], ph ^ 1, a.err)) break;
       mbar_expect_tx(&full[s], C::A_BYTES + C::B_BYTES);
-      tma_load_2d(sA + s * C::A_BYTES, &ta, &full[s], (kb0 + kb) * kBK, m_tile * kBM);
+      tma_load_2d(sA + s * C::A_BYTES, &ta, &full[s], (kb0 + kb) * kBK, m_tile * kBM * MT);
       tma_load_2d(sB + s * C::B_BYTES, &tb, &full[s], (kb0 + kb) * kBK, n_tile * BN);
     }
     s_issued = kb;
@@ -237,11 +242,14 @@ __global__ void __launch_bounds__(128, 1)
       const uint32_t ph = (kb / C::STAGES) & 1;
       if (!mbar_wait(&full[s], ph, a.err)) break;
       tc_fence_after();
-      const uint64_t ad = smem_desc_sw128(sA + s * C::A_BYTES);
       const uint64_t bd = smem_desc_sw128(sB + s * C::B_BYTES);
 #pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk)  // advance 16 bf16 = 32 bytes inside the swizzle row
-        umma_bf16(tmem, ad + uint64_t(kk * 2), bd + uint64_t(kk * 2), idesc, (kb | kk) != 0);
+      for (int u = 0; u < MT; ++u) {  // row tile u accumulates in TMEM columns [u * BN, (u + 1) * BN)
+        const uint64_t ad = smem_desc_sw128(sA + s * C::A_BYTES + u * C::A_TILE);
+#pragma unroll
+        for (int kk = 0; kk < kBK / 16; ++kk)  // advance 16 bf16 = 32 bytes inside the swizzle row
+          umma_bf16(tmem + uint32_t(u * BN), ad + uint64_t(kk * 2), bd + uint64_t(kk * 2), idesc, (kb | kk) != 0);
+      }
       umma_commit(&empty[s]);
     }
     umma_commit(done);  // fires once every MMA issued above has completed
@@ -259,19 +267,21 @@ __global__ void __launch_bounds__(128, 1)
     constexpr int LD = BN + 4;  // staged row stride in floats (conflict-free 16-byte accesses)
     static_assert(size_t(kBM) * LD * 4 <= size_t(C::STAGES) * (C::A_BYTES + C::B_BYTES), "staging fits");
     float* st = reinterpret_cast<float*>(sA) + size_t(warp) * 32 * LD;
+    const bool vec = (a.ldc % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.C) & 15) == 0);
+#pragma unroll 1
+    for (int u = 0; u < MT; ++u) {
 #pragma unroll 1
     for (int c = 0; c < BN; c += 16) {
       float v[16];
-      tmem_ld16(tmem + (uint32_t(warp * 32) << 16) + uint32_t(c), v);
+      tmem_ld16(tmem + (uint32_t(warp * 32) << 16) + uint32_t(u * BN + c), v);
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         *reinterpret_cast<float4*>(st + lane * LD + c + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
     }
     __syncwarp();
-    const int r_base = m_tile * kBM + warp * 32;
+    const int r_base = (m_tile * MT + u) * kBM + warp * 32;
     const int my_r = r_base + lane;
     const int64_t my_orow = my_r < rows ? (a.row_map ? int64_t(__ldcg(&a.row_map[my_r])) : int64_t(my_r)) : 0;
-    const bool vec = (a.ldc % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.C) & 15) == 0);
     for (int i = 0; i < 32 && r_base + i < rows; ++i) {
       const int64_t orow = __shfl_sync(0xffffffffu, my_orow, i);
       float* crow = a.C + int64_t(blockIdx.z) * a.c_split + orow * a.ldc + int64_t(n_tile) * BN;
@@ -286,6 +296,8 @@ __global__ void __launch_bounds__(128, 1)
         }
       }
     }
+    __syncwarp();  // the staging rows are read before the next row tile overwrites them
+    }
   }
   // Bounded drain of this CTA's own copies before its shared memory goes away
   // (only reached with copies in flight after a timeout).
@@ -295,7 +307,7 @@ __global__ void __launch_bounds__(128, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, BN);
+  if (warp == 0) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
 // ------------------------------------------------------------------ helpers on CUDA cores
@@ -486,23 +498,23 @@ static cudaError_t make_map_2d(CUtensorMap* m, const void* ptr, int64_t rows, in
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int BN, int SG = 0>
+template <int BN, int SG = 0, int MT = 1>
 static cudaError_t launch_tc_gemm_t(const void* A, int64_t a_rows, const void* B, int64_t b_rows, int K,
                                     const TcArgs& args, cudaStream_t s) {
   CUtensorMap ta, tb;
-  cudaError_t e = make_map_2d(&ta, A, a_rows, K, kBM);
+  cudaError_t e = make_map_2d(&ta, A, a_rows, K, kBM * MT);
   if (e != cudaSuccess) return e;
   if ((e = make_map_2d(&tb, B, b_rows, K, BN)) != cudaSuccess) return e;
-  auto kern = tc_gemm_kernel<BN, SG>;
+  auto kern = tc_gemm_kernel<BN, SG, MT>;
   static bool attr = false;
   if (!attr) {
-    if ((e = set_kernel_smem(kern, TcCfg<BN, SG>::SMEM)) != cudaSuccess) return e;
+    if ((e = set_kernel_smem(kern, TcCfg<BN, SG, MT>::SMEM)) != cudaSuccess) return e;
     attr = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(unsigned(cdiv(a_rows, kBM)), unsigned(cdiv(b_rows, BN)), unsigned(args.ksplit > 1 ? args.ksplit : 1));
+  cfg.gridDim = dim3(unsigned(cdiv(a_rows, kBM * MT)), unsigned(cdiv(b_rows, BN)), unsigned(args.ksplit > 1 ? args.ksplit : 1));
   cfg.blockDim = dim3(128);
-  cfg.dynamicSmemBytes = TcCfg<BN, SG>::SMEM;
+  cfg.dynamicSmemBytes = TcCfg<BN, SG, MT>::SMEM;
   cfg.stream = s;
   cudaLaunchAttribute at[1];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -513,8 +525,10 @@ static cudaError_t launch_tc_gemm_t(const void* A, int64_t a_rows, const void* B
 }
 
 // C[row_map(m)][n] = sum_k A[m][k] B[n][k]; A: a_rows x K, B: b_rows x K, bf16.
+// mt = 2 (bn = 256 only): each CTA takes 256 rows of A as two 128-row tiles.
 cudaError_t launch_tc_gemm(const void* A, int64_t a_rows, const void* B, int64_t b_rows, int K, int bn,
-                           const TcArgs& args, cudaStream_t s) {
+                           const TcArgs& args, cudaStream_t s, int mt = 1) {
+  if (mt == 2 && bn == 256) return launch_tc_gemm_t<256, 0, 2>(A, a_rows, B, b_rows, K, args, s);
   switch (bn) {
     case 64: return launch_tc_gemm_t<64>(A, a_rows, B, b_rows, K, args, s);
     case 128:
@@ -628,7 +642,8 @@ cudaError_t launch_tensor_path(const TensorArgs& t, cudaStream_t s) {
   sl.ldc = d_out;
   sl.row_map = t.idx + T;
   sl.err = t.err;
-  return launch_tc_gemm(t.Xslow, T, t.W, d_out, int(d), 256, sl, s);
+  // 256 rows per CTA: W is read from L2 once per 256 slow tokens
+  return launch_tc_gemm(t.Xslow, T, t.W, d_out, int(d), 256, sl, s, 2);
 }
 
 }  // namespace gsi
