@@ -176,7 +176,7 @@ static size_t stream_ws(const gsi_map_desc* m, int64_t T) {
 struct DeviceFacts {
   int nsm = 0;
   int smem_optin = 0;
-  int clusters[2][2][2] = {};  // co-resident clusters per [dtype][fused][cs == 16]; -1: not possible
+  int clusters[2][2] = {};  // co-resident 8-CTA clusters per [dtype][fused]; -1: not possible
 };
 
 // Shared memory of the two-launch decide-and-apply kernel: the device limit
@@ -205,7 +205,7 @@ static gsi_status device_facts(DeviceFacts** out) {
 static int decide_clusters(DeviceFacts* f, gsi_dtype dt, bool fused, int cs) {
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
-  int& c = f->clusters[dt == GSI_BF16][fused][cs == 16];
+  int& c = f->clusters[dt == GSI_BF16][fused];
   if (c == 0) {
     const size_t smem = fused ? size_t(f->smem_optin) : decide_smem_budget(f->smem_optin);
     const int n = decide_apply_max_clusters(smem, dt, fused, cs);

@@ -4,19 +4,24 @@
 // rho = ||x - V_k g|| / ||x||; fast tokens (rho < eps) take y = M g (the
 // cached image, d_out x k), slow tokens the exact y = W x (d_out x d).
 //
-// Input: the cluster partials of g = V_k^T x and ||x||^2 written by the
-// projection kernel.  Every 8-CTA cluster of this grid finishes the gate on
-// its own: CTA r adds the partials of its slice of g's columns, the slices are
-// exchanged through distributed shared memory, CTA r forms its share of
-// g^T (V_k^T V_k) g from a Gram slice it loaded into registers before the
-// dependency wait, and the shares are added in rank order.  All clusters do
-// the same arithmetic on the same data in the same order, so they reach the
-// same bits, and every CTA knows every token's flag without a grid-wide sync
-// or a host round trip.
+// Input: partial sums of g = V_k^T x and ||x||^2 -- either the projection
+// kernel's cluster partials (two-launch path) or, in the single-launch form
+// (FUSED), the partials every CTA of this grid publishes after projecting x
+// on its own slab of V_k, behind a grid barrier on the workspace's ticket
+// counter.  Every 8-CTA cluster then finishes the gate on its own: CTA r adds
+// the partials of its slice of g's columns (coalesced loads, one fixed
+// order), the slices are pushed into every CTA's shared memory by st.async
+// (completion on the receiver's mbarrier), CTA r forms its share of
+// g^T (V_k^T V_k) g from the Gram slice it copied into shared memory before
+// the dependency wait, and the shares are pushed the same way and added in
+// rank order.  All clusters do the same arithmetic on the same data in the
+// same order, so they reach the same bits, and every CTA knows every token's
+// flag without a host round trip.
 //
 // Each CTA owns a contiguous block of output rows.  Before the dependency
-// wait it copies its rows of M into shared memory (TMA bulk copy), so a fast
-// call only computes from shared memory once the gate is known.  Slow tokens
+// wait it copies its rows of M into shared memory (TMA bulk copy); a
+// decide-and-apply call computes y = M g for its tokens while the decision's
+// last exchange is in flight and keeps the rows of the fast ones.  Slow tokens
 // stream the CTA's rows of W: each of the eight warps owns rows warp,
 // warp + 8, ... and pulls them in 4 KB segments through a private ring of bulk
 // copies completed on mbarriers; a row's sum is one warp's, in lane order.
@@ -151,7 +156,7 @@ struct IntC {
 // FUSED: the grid computes g = V_k^T x itself (one launch per call, T <= 2):
 // every CTA projects its own slab of V_k and the partials meet at a grid
 // barrier; otherwise g comes from the projection kernel's cluster partials.
-// CS: CTAs per cluster (8, or 16 where the device allows it), set at launch.
+// CS: CTAs per cluster (8), set at launch.
 template <class E, int TC, int GRV, bool FUSED, int CS>
 __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
   constexpr int PV = E::kPerVec;
@@ -864,8 +869,6 @@ static cudaError_t launch_da_t(const DecideArgs& a, const DecidePlan& p, cudaStr
   if (p.smem > smem_set) {
     cudaError_t e = set_kernel_smem(kern, p.smem);
     if (e != cudaSuccess) return e;
-    if (CS > 8 && (e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
-      return e;
     smem_set = p.smem;
   }
   cudaLaunchConfig_t cfg = {};
@@ -899,7 +902,6 @@ template <class E>
 static cudaError_t launch_da_e(const DecideArgs& a, const DecidePlan& p, cudaStream_t s) {
   if (!p.fused) return launch_da_f<E, false, 8>(a, p, s);
   if (p.tc > 2) return cudaErrorInvalidValue;  // the fused decode handles one chunk of at most 2 tokens
-  if (p.cs == 16) return p.tc == 1 ? launch_da_t<E, 1, true, 16>(a, p, s) : launch_da_t<E, 2, true, 16>(a, p, s);
   return p.tc == 1 ? launch_da_t<E, 1, true, 8>(a, p, s) : launch_da_t<E, 2, true, 8>(a, p, s);
 }
 
@@ -913,10 +915,6 @@ template <class E, bool FUSED, int CS>
 static int max_clusters_t(size_t smem) {
   auto kern = decide_apply_kernel<E, 1, 0, FUSED, CS>;
   if (set_kernel_smem(kern, smem) != cudaSuccess) return 0;
-  if (CS > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(CS * 64);
   cfg.blockDim = dim3(kApplyThreads);
@@ -939,10 +937,10 @@ static int max_clusters_t(size_t smem) {
 int decide_apply_max_clusters(size_t smem, gsi_dtype dt, bool fused, int cs) {
   if (dt == GSI_BF16) {
     if (!fused) return max_clusters_t<BF16, false, 8>(smem);
-    return cs == 16 ? max_clusters_t<BF16, true, 16>(smem) : max_clusters_t<BF16, true, 8>(smem);
+    return max_clusters_t<BF16, true, 8>(smem);
   }
   if (!fused) return max_clusters_t<F32, false, 8>(smem);
-  return cs == 16 ? max_clusters_t<F32, true, 16>(smem) : max_clusters_t<F32, true, 8>(smem);
+  return max_clusters_t<F32, true, 8>(smem);
 }
 
 }  // namespace gsi
