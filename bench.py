@@ -180,6 +180,18 @@ def cores():
         return os.cpu_count()
 
 
+def combine_ranks(ms, world, dist=None, device=None):
+    """The whole job's step time and throughput: every rank runs its own
+    replica of the workload (no data-path collective), so the job's step
+    takes the slowest rank's time (all-reduce MAX) and the job processes
+    T_TOKENS tokens per rank per step.  Returns (ms, tokens per second)."""
+    if dist is not None and world > 1:
+        t = torch.tensor([float(ms)], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    return ms, T_TOKENS * world / (ms / 1e3)
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -502,12 +514,7 @@ def main():
         if dist:
             dist.barrier()
         clocks = sampler.stop()
-        ms = e0.elapsed_time(e1) / args.steps
-        if dist:
-            t = torch.tensor([ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            ms = float(t.item())
-        tokens_per_s = T_TOKENS * world / (ms / 1e3)
+        ms, tokens_per_s = combine_ranks(e0.elapsed_time(e1) / args.steps, world, dist, dev)
 
         flags_np = [F.cpu().numpy().astype(bool) for F in Fs]
         ab = algorithmic_bytes(maps_in, flags_np)
