@@ -309,3 +309,71 @@ def test_fused_rejects_what_it_cannot_run(gsi):
     with pytest.raises(gsi.GsiError):
         gsi.workspace_size(wide, 1, "fused")
     assert gsi.workspace_size(wide, 1, "stream") > 0
+
+
+# ------------------------------------------------------------------ the single-launch decode on edge cases
+def _per_call(gsi, gm, X, eps, T_call, path="auto"):
+    """Run the map in calls of T_call tokens (one workspace), as a decoder would."""
+    n = X.shape[0]
+    Y = torch.empty(n, gm.d_out, device="cuda")
+    F = torch.empty(n, dtype=torch.uint8, device="cuda")
+    R = torch.empty(n, device="cuda")
+    ws = gsi.new_workspace(gsi.workspace_size(gm, T_call, path))
+    for t0 in range(0, n, T_call):
+        sl = slice(t0, min(n, t0 + T_call))
+        # each call writes its own buffer: output rows must start 16-byte aligned
+        Yc = torch.empty(sl.stop - sl.start, gm.d_out, device="cuda")
+        gsi.linear(gm, X[sl], eps, Y=Yc, flags=F[sl], rho=R[sl], workspace=ws, path=path)
+        Y[sl] = Yc
+    torch.cuda.synchronize()
+    assert gsi.workspace_status(ws) == 0
+    return Y, F, R
+
+
+@pytest.mark.parametrize("T_call", [1, 2])
+def test_decode_calls_eps_zero_and_inf(gsi, T_call):
+    m_in = _small_bf16()
+    gm, X = upload(m_in)
+    Y, F, R = _per_call(gsi, gm, X, 0.0, T_call)
+    assert bool(F.all())
+    dense = orc.slow_path(synth.widen(m_in.W), synth.widen(m_in.X))
+    assert np.linalg.norm(Y.cpu().numpy() - dense) / np.linalg.norm(dense) <= 1e-5
+    Y, F, R = _per_call(gsi, gm, X, float("inf"), T_call)
+    assert not bool(F.any())
+    Mn = synth.widen(gm.M)
+    static = orc.fast_path(Mn, orc.project(synth.widen(m_in.X), synth.widen(m_in.V)))
+    assert np.linalg.norm(Y.cpu().numpy() - static) / np.linalg.norm(static) <= 2e-2
+
+
+@pytest.mark.parametrize("T_call", [1, 2])
+def test_decode_calls_zero_and_nonfinite_tokens(gsi, T_call):
+    m_in = _small_bf16(T=6)
+    X = m_in.X.clone()
+    X[1] = 0
+    X[3, 5] = float("nan")
+    X[4, 0] = float("inf")
+    gm, _ = upload(m_in)
+    Y, F, R = _per_call(gsi, gm, X.cuda(), m_in.eps, T_call)
+    f = F.cpu().numpy()
+    assert f[1] == 0 and float(R[1]) == 0.0 and bool((Y[1] == 0).all())
+    assert f[3] == 1 and f[4] == 1
+    assert bool(torch.isnan(R[3])) and bool(torch.isnan(Y[3]).all())
+    compare(m_in, gm.M, Y, F, R, X=X)
+
+
+@pytest.mark.parametrize("shape", [(520, 333, 24), (1032, 2056, 40), (16, 8, 8)])
+def test_decode_calls_ragged_shapes(gsi, shape):
+    d, d_out, k = shape
+    V64 = synth.orthonormal_basis(synth.rng(8, d, k, 3), d, k)
+    m_in = synth.stack_layer(8, 1, {"qkv": V64}, {"qkv": (d_out, d)}, T=10, f_slow=0.4, roles=("qkv",))[0]
+    gm, X = upload(m_in)
+    for T_call in (1, 2):
+        Y, F, R = _per_call(gsi, gm, X, m_in.eps, T_call)
+        compare(m_in, gm.M, Y, F, R)
+
+
+def test_decode_calls_fp32(gsi):
+    m_in = synth.config1()
+    gm, X = upload(m_in)
+    Y, F, R = _per_call(gsi, gm, X[:16], m_in.eps, 1)
+    compare(m_in, gm.M, Y, F, R, X=m_in.X[:16])
