@@ -176,7 +176,7 @@ static size_t stream_ws(const gsi_map_desc* m, int64_t T) {
 struct DeviceFacts {
   int nsm = 0;
   int smem_optin = 0;
-  int clusters[2][2] = {};  // co-resident 8-CTA clusters per [dtype][fused]; -1: not possible
+  int clusters[2][2][2] = {};  // co-resident clusters per [dtype][fused][cs == 16]; -1: not possible
 };
 
 // Shared memory of the two-launch decide-and-apply kernel: the device limit
@@ -205,7 +205,7 @@ static gsi_status device_facts(DeviceFacts** out) {
 static int decide_clusters(DeviceFacts* f, gsi_dtype dt, bool fused, int cs) {
   static std::mutex mu;
   std::lock_guard<std::mutex> lock(mu);
-  int& c = f->clusters[dt == GSI_BF16][fused];
+  int& c = f->clusters[dt == GSI_BF16][fused][cs == 16];
   if (c == 0) {
     const size_t smem = fused ? size_t(f->smem_optin) : decide_smem_budget(f->smem_optin);
     const int n = decide_apply_max_clusters(smem, dt, fused, cs);
@@ -237,12 +237,20 @@ static gsi_status run_decide(const gsi_map_desc* m, const void* X, int64_t T, fl
   if (s != GSI_OK) return s;
   DecidePlan dp{};
   if (fused) {
-    // 8-CTA clusters: measured faster than 16 (cheaper cluster exchanges)
-    const int cs = kClusterSize;
-    int nc = decide_clusters(f, m->dtype, true, cs);
-    if (nc * cs > kFusedMaxCtas) nc = kFusedMaxCtas / cs;
-    if (nc > 0) dp = plan_decide(m->d, m->d_out, m->k, es, T, nc * cs, size_t(f->smem_optin), true, cs);
-    if (nc == 0 || !dp.ok) return fail(GSI_ERR_UNSUPPORTED, "the fused decode does not fit this device");
+    // Cluster projection (each cluster projects x on all of V; no grid
+    // barrier) where a sixteenth of V fits beside the other buffers, else
+    // grid projection.  Both use 16-CTA clusters where the device allows
+    // them: consecutive launches with different cluster shapes were measured
+    // to cost ~1.4 us each in a sequence of maps (6B layer, batch-1 decode).
+    const int nc16 = decide_clusters(f, m->dtype, true, 16);
+    if (nc16 > 0) dp = plan_decide(m->d, m->d_out, m->k, es, T, nc16 * 16, size_t(f->smem_optin), true, 16, true);
+    if (nc16 == 0 || !dp.ok) {
+      const int cs = nc16 > 0 ? 16 : kClusterSize;
+      int nc = nc16 > 0 ? nc16 : decide_clusters(f, m->dtype, true, cs);
+      if (nc * cs > kFusedMaxCtas) nc = kFusedMaxCtas / cs;
+      if (nc > 0) dp = plan_decide(m->d, m->d_out, m->k, es, T, nc * cs, size_t(f->smem_optin), true, cs);
+      if (nc == 0 || !dp.ok) return fail(GSI_ERR_UNSUPPORTED, "the fused decode does not fit this device");
+    }
   } else {
     const int nc = decide_clusters(f, m->dtype, false, kClusterSize);
     if (nc == 0) return fail(GSI_ERR_CUDA, "cannot size the decide-and-apply grid (cluster occupancy query failed)");
@@ -283,6 +291,7 @@ static gsi_status run_decide(const gsi_map_desc* m, const void* X, int64_t T, fl
   a.off_y = dp.off_y;
   a.off_gram = dp.off_gram;
   if (fused) {
+    a.cproj = dp.cproj ? 1 : 0;
     const FusedLayout FL = layout_fused(m->k, T);
     a.fpart_g = reinterpret_cast<float*>(base + FL.part_g);
     a.fpart_x = reinterpret_cast<float*>(base + FL.part_x);

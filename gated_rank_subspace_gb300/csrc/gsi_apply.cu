@@ -113,6 +113,12 @@ __device__ __forceinline__ void st_async_f32(uint32_t raddr, float v, uint32_t r
                "r"(__float_as_uint(v)), "r"(rbar)
                : "memory");
 }
+__device__ __forceinline__ void st_async_v4(uint32_t raddr, float4 v, uint32_t rbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(raddr),
+               "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)),
+               "r"(__float_as_uint(v.w)), "r"(rbar)
+               : "memory");
+}
 __device__ __forceinline__ bool bar_try_cluster(uint64_t* b, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -156,7 +162,7 @@ struct IntC {
 // FUSED: the grid computes g = V_k^T x itself (one launch per call, T <= 2):
 // every CTA projects its own slab of V_k and the partials meet at a grid
 // barrier; otherwise g comes from the projection kernel's cluster partials.
-// CS: CTAs per cluster (8), set at launch.
+// CS: CTAs per cluster (8; 16 for the cluster projection), set at launch.
 template <class E, int TC, int GRV, bool FUSED, int CS>
 __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
   constexpr int PV = E::kPerVec;
@@ -201,6 +207,10 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
   float* xsl = reinterpret_cast<float*>(smem + a.off_xs);      // [TC][v_rows]
   float* red2 = xsl + TC * ((a.v_rows + 3) & ~3);              // [ngrp][TC][k], 16-byte aligned
   float* xsq = red2 + a.ngrp * TC * k;                         // [TC]
+  // cluster projection only: this CTA's partial g and the all-to-all inboxes
+  float* pg = xsq + 8;                                         // [TC][k]; xsq is 16-byte aligned, TC <= 8
+  float* inbox = pg + TC * k;                                  // [CS][TC][k]
+  float* inbox_x = inbox + CS * TC * k;                        // [CS][TC]
 
   // ---- prologue: only weights (may overlap the projection kernel)
   pdl_launch_dependents();
@@ -215,7 +225,9 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
   }
   __syncthreads();
   const bool stage_m = a.stage_m && a.mode != 1 && nrows > 0;
-  if (tid == kApplyThreads - 32 && stage_m) {
+  // (with the cluster projection the M rows take the V slice's place once it
+  // has been read, so their copy is issued after the projection)
+  if (tid == kApplyThreads - 32 && stage_m && !(FUSED && a.cproj)) {
     const uint32_t bytes = uint32_t(nrows) * mrow_b;
     bar_expect_tx(mfull, bytes);
     bulk_g2s(Ms, static_cast<const char*>(a.M) + r0 * mrow_b, bytes, mfull);
@@ -231,7 +243,7 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
   }
   bool gram_waited = false;
   // fused decode: this CTA's slab of V (rows [v0, v0 + vn)), one bulk copy
-  const int64_t v0 = int64_t(blockIdx.x) * a.v_rows;
+  const int64_t v0 = int64_t(FUSED && a.cproj ? rank : int(blockIdx.x)) * a.v_rows;
   const int vn = FUSED ? int(v0 >= d ? 0 : (d - v0 < a.v_rows ? d - v0 : a.v_rows)) : 0;
   if (FUSED && a.mode != 2 && vn > 0 && tid == kApplyThreads - 32) {
     const uint32_t bytes = uint32_t(vn) * uint32_t(mrow_b);
@@ -398,6 +410,57 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
         }
       }
       __syncthreads();
+      if (a.cproj) {
+        // The V slice has been read: the M rows take its place (bulk copy,
+        // from L2 when the previous call staged them there).
+        if (stage_m && tid == kApplyThreads - 32) {
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          const uint32_t bytes = uint32_t(nrows) * mrow_b;
+          bar_expect_tx(mfull, bytes);
+          bulk_g2s(Ms, static_cast<const char*>(a.M) + r0 * mrow_b, bytes, mfull);
+        }
+        // this CTA's partial g (rows [v0, v0 + vn) of V), then an all-to-all
+        // inside the cluster: every CTA receives every rank's partial g and
+        // ||x||^2 slice (st.async, completion on its own mbarrier) and adds
+        // them in rank order -- the full g, the same bits in every CTA and,
+        // as every cluster does the same arithmetic, in every cluster
+        for (int e = tid; e < TC * k; e += blockDim.x) {
+          float s2 = 0.f;
+          for (int g = 0; g < a.ngrp; ++g) s2 += red2[g * TC * k + e];
+          pg[e] = s2;
+        }
+        if (!started) {
+          cluster_wait();  // every CTA of the cluster is running: peers' shared memory is live
+          started = true;
+        }
+        __syncthreads();
+        const uint32_t aph = uint32_t(t0 / TC) & 1u;
+        if (tid == 0) bar_expect_tx(gx_bar, uint32_t(CS * TC * (k + 1) * 4));
+        const int n4 = TC * k / 4;
+        for (int e = tid; e < CS * n4; e += blockDim.x) {
+          const int q = e / n4, f4 = e - (e / n4) * n4;
+          st_async_v4(map_rank(sa(inbox + rank * TC * k + 4 * f4), q),
+                      *reinterpret_cast<const float4*>(pg + 4 * f4), map_rank(sa(gx_bar), q));
+        }
+        if (tid < TC * CS) {
+          const int t = tid % TC, q = tid / TC;
+          st_async_f32(map_rank(sa(inbox_x + rank * TC + t), q), xsq[t], map_rank(sa(gx_bar), q));
+        }
+        if (!__all_sync(0xffffffffu, bar_wait_cluster(gx_bar, aph, a.err))) ok = false;
+        for (int e = tid; e < TC * k; e += blockDim.x) {
+          float s2 = 0.f;
+#pragma unroll
+          for (int r = 0; r < CS; ++r) s2 += inbox[r * TC * k + e];
+          gfull[e] = e / k < tc ? s2 : 0.f;
+        }
+        if (tid < TC) {
+          float s2 = 0.f;
+#pragma unroll
+          for (int r = 0; r < CS; ++r) s2 += inbox_x[r * TC + tid];
+          nx2[tid] = s2;
+        }
+        ok = __syncthreads_and(ok) != 0;
+      } else {
       // this CTA's partials to the workspace, laid out like the projection
       // kernel's cluster partials (one "cluster" per CTA)
       for (int e = tid; e < TC * k; e += blockDim.x) {
@@ -412,8 +475,11 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
       // every CTA's partials of this chunk are published
       if (tid == 0 && !grid_barrier(a.ticket, gridDim.x, a.err)) ok = false;
       ok = __syncthreads_and(ok) != 0;
+      }
     }
-    if (a.mode != 2) {
+    // the cluster projection already holds the full g
+    const bool have_g = FUSED && a.cproj;
+    if (a.mode != 2 && !have_g) {
       // -- g: this CTA's column slice summed over the published partials
       //    (the projection clusters', or every CTA's of a fused grid) in one
       //    fixed order.  Thread (g, e) takes column e (consecutive threads:
@@ -510,15 +576,18 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
       }
       __syncthreads();
       // push this CTA's slice of g into every CTA's full copy; each CTA
-      // receives TC x k floats per chunk (the slices partition [0, k))
+      // receives TC x k floats per chunk (the slices partition [0, k)).
+      // (The cluster projection already has the full g in every CTA.)
       const uint32_t xph = uint32_t(t0 / TC) & 1u;
-      if (tid == 0) bar_expect_tx(gx_bar, uint32_t(TC * k * 4));
-      for (int e = tid; e < E_ * CS; e += blockDim.x) {
-        const int q = e / E_, f = e - (e / E_) * E_;
-        const int t = f / ks, col = c0 + (f - (f / ks) * ks);
-        if (col < c1) st_async_f32(map_rank(sa(gfull + t * k + col), q), gsl[f], map_rank(sa(gx_bar), q));
+      if (!have_g) {
+        if (tid == 0) bar_expect_tx(gx_bar, uint32_t(TC * k * 4));
+        for (int e = tid; e < E_ * CS; e += blockDim.x) {
+          const int q = e / E_, f = e - (e / E_) * E_;
+          const int t = f / ks, col = c0 + (f - (f / ks) * ks);
+          if (col < c1) st_async_f32(map_rank(sa(gfull + t * k + col), q), gsl[f], map_rank(sa(gx_bar), q));
+        }
+        if (!__all_sync(0xffffffffu, bar_wait_cluster(gx_bar, xph, a.err))) ok = false;
       }
-      if (!__all_sync(0xffffffffu, bar_wait_cluster(gx_bar, xph, a.err))) ok = false;
       // -- ||g||^2 and g^T Gram g over this CTA's Gram rows
       float qa[TC], na[TC];
 #pragma unroll
@@ -869,6 +938,8 @@ static cudaError_t launch_da_t(const DecideArgs& a, const DecidePlan& p, cudaStr
   if (p.smem > smem_set) {
     cudaError_t e = set_kernel_smem(kern, p.smem);
     if (e != cudaSuccess) return e;
+    if (CS > 8 && (e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess)
+      return e;
     smem_set = p.smem;
   }
   cudaLaunchConfig_t cfg = {};
@@ -902,6 +973,7 @@ template <class E>
 static cudaError_t launch_da_e(const DecideArgs& a, const DecidePlan& p, cudaStream_t s) {
   if (!p.fused) return launch_da_f<E, false, 8>(a, p, s);
   if (p.tc > 2) return cudaErrorInvalidValue;  // the fused decode handles one chunk of at most 2 tokens
+  if (p.cs == 16) return p.tc == 1 ? launch_da_t<E, 1, true, 16>(a, p, s) : launch_da_t<E, 2, true, 16>(a, p, s);
   return p.tc == 1 ? launch_da_t<E, 1, true, 8>(a, p, s) : launch_da_t<E, 2, true, 8>(a, p, s);
 }
 
@@ -915,6 +987,10 @@ template <class E, bool FUSED, int CS>
 static int max_clusters_t(size_t smem) {
   auto kern = decide_apply_kernel<E, 1, 0, FUSED, CS>;
   if (set_kernel_smem(kern, smem) != cudaSuccess) return 0;
+  if (CS > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(CS * 64);
   cfg.blockDim = dim3(kApplyThreads);
@@ -937,10 +1013,10 @@ static int max_clusters_t(size_t smem) {
 int decide_apply_max_clusters(size_t smem, gsi_dtype dt, bool fused, int cs) {
   if (dt == GSI_BF16) {
     if (!fused) return max_clusters_t<BF16, false, 8>(smem);
-    return max_clusters_t<BF16, true, 8>(smem);
+    return cs == 16 ? max_clusters_t<BF16, true, 16>(smem) : max_clusters_t<BF16, true, 8>(smem);
   }
   if (!fused) return max_clusters_t<F32, false, 8>(smem);
-  return max_clusters_t<F32, true, 8>(smem);
+  return cs == 16 ? max_clusters_t<F32, true, 16>(smem) : max_clusters_t<F32, true, 8>(smem);
 }
 
 }  // namespace gsi

@@ -58,6 +58,7 @@ struct DecideArgs {
   // other CTAs at a grid barrier on the workspace's ticket counter
   const void* V;        // d x k
   int v_rows, ngrp, off_v, off_xs;
+  int cproj;            // each cluster projects x on all of V (16-CTA clusters; no grid barrier)
   float* fpart_g;       // [grid][T][k]
   float* fpart_x;       // [grid][T]
   unsigned long long* ticket;

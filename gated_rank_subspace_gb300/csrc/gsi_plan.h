@@ -133,7 +133,8 @@ struct DecidePlan {
   int tc, grv, ncta, rows_per_cta, seg_bytes, wstages, x_stage_max, stage_m;
   int off_m, off_x, off_g, off_gram;  // off_gram = 0: Gram slice read from global
   int off_y;                          // [tc][rows_per_cta] fast outputs computed before the decision
-  bool fused;  // single-launch decode: the cluster projects x itself
+  bool fused;  // single-launch decode: the grid projects x itself
+  bool cproj;  // fused, and each cluster projects x on all of V (no grid barrier)
   int cs;      // CTAs per cluster
   int ks;      // columns of g owned by each rank
   int v_rows, ngrp, off_v, off_xs;
@@ -147,10 +148,11 @@ constexpr int kWarpStages = 4;
 constexpr int kXStage = 16 * 1024;
 
 inline DecidePlan plan_decide(int64_t d, int64_t d_out, int64_t k, int es, int64_t T, int ncta,
-                              size_t smem_budget, bool fused = false, int cs = kClusterSize) {
+                              size_t smem_budget, bool fused = false, int cs = kClusterSize, bool cproj = false) {
   DecidePlan p{};
   p.ok = true;
   p.fused = fused;
+  p.cproj = fused && cproj;
   p.cs = cs;
   p.tc = T >= 8 ? 8 : T >= 4 ? 4 : T >= 2 ? 2 : 1;
   const int64_t ks = cdiv(k, cs);
@@ -186,13 +188,18 @@ inline DecidePlan plan_decide(int64_t d, int64_t d_out, int64_t k, int es, int64
   p.ngrp = 0;
   p.off_xs = 0;
   if (fused) {
-    // CTA b projects rows [b * v_rows, (b + 1) * v_rows) of V: its token
-    // slice, the row groups' partial sums and its slice of ||x||^2
-    p.v_rows = int(cdiv(d, ncta));
+    // CTA b (grid projection) or cluster rank r (cluster projection)
+    // projects rows [b * v_rows, ...) or [r * v_rows, ...) of V: its token
+    // slice, the row groups' partial sums and its slice of ||x||^2; the
+    // cluster projection adds this CTA's partial g [tc][k] and the inboxes
+    // of the all-to-all, [cs][tc][k] and [cs][tc]
+    p.v_rows = int(cdiv(d, p.cproj ? cs : ncta));
     const int vecs = int(mrow_b / 16);  // 16-byte vectors per V row
     p.ngrp = kApplyThreads / vecs >= 1 ? kApplyThreads / vecs : 1;
     p.off_xs = int(off);
+    // (xsq takes 8 floats when the cluster projection's 16-byte aligned pg follows it)
     off += (size_t(p.tc) * rup(p.v_rows, 4) + size_t(p.ngrp) * p.tc * k + size_t(p.tc) + 8) * 4;
+    if (p.cproj) off += (size_t(p.tc) * k + size_t(cs) * p.tc * k + size_t(cs) * p.tc + 8) * 4;
     off = (off + 127) & ~size_t(127);
   }
   p.off_m = int(off);
@@ -200,13 +207,15 @@ inline DecidePlan plan_decide(int64_t d, int64_t d_out, int64_t k, int es, int64
   p.rows_per_cta = int(cdiv(d_out, ncta));
   const size_t m_bytes = (size_t(p.rows_per_cta) * mrow_b + 127) & ~size_t(127);
   const size_t v_bytes = fused ? size_t(p.v_rows) * mrow_b : 0;
-  // region after off_m: [M rows | V slice] before the decision, W rings after it
-  size_t need_mv = m_bytes + v_bytes;
+  // region after off_m: [M rows | V slice] before the decision, W rings after
+  // it; with the cluster projection the M rows replace the V slice once it
+  // is consumed (copied after the projection)
+  size_t need_mv = p.cproj ? (m_bytes > v_bytes ? m_bytes : v_bytes) : m_bytes + v_bytes;
   p.stage_m = off + (need_mv > ring ? need_mv : ring) <= smem_budget ? 1 : 0;
   if (fused && !p.stage_m) {
     need_mv = v_bytes;  // M then comes from global (L2) after the decision
   }
-  p.off_v = int(off + (p.stage_m ? m_bytes : 0));
+  p.off_v = int(off + (p.stage_m && !p.cproj ? m_bytes : 0));
   const size_t region = (p.stage_m || fused) ? (need_mv > ring ? need_mv : ring) : ring;
   p.smem = off + region;
   p.ok = p.smem <= smem_budget;
