@@ -380,26 +380,16 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
           for (; i + a.ngrp < vn; i += 2 * a.ngrp) {
             const uint4 u0 = *reinterpret_cast<const uint4*>(Vs + int64_t(i) * mrow_b + 16 * w);
             const uint4 u1 = *reinterpret_cast<const uint4*>(Vs + int64_t(i + a.ngrp) * mrow_b + 16 * w);
-            float w0[PV], w1[PV];
-            E::unpack(u0, w0);
-            E::unpack(u1, w1);
 #pragma unroll
             for (int t = 0; t < TC; ++t) {
-              const float x0 = xsl[t * a.v_rows + i], x1 = xsl[t * a.v_rows + i + a.ngrp];
-#pragma unroll
-              for (int e = 0; e < PV; ++e) acc[t][e] = fmaf(x1, w1[e], fmaf(x0, w0[e], acc[t][e]));
+              E::axpy(u0, xsl[t * a.v_rows + i], acc[t]);  // rows i, then i + ngrp
+              E::axpy(u1, xsl[t * a.v_rows + i + a.ngrp], acc[t]);
             }
           }
           if (i < vn) {
             const uint4 u0 = *reinterpret_cast<const uint4*>(Vs + int64_t(i) * mrow_b + 16 * w);
-            float w0[PV];
-            E::unpack(u0, w0);
 #pragma unroll
-            for (int t = 0; t < TC; ++t) {
-              const float x0 = xsl[t * a.v_rows + i];
-#pragma unroll
-              for (int e = 0; e < PV; ++e) acc[t][e] = fmaf(x0, w0[e], acc[t][e]);
-            }
+            for (int t = 0; t < TC; ++t) E::axpy(u0, xsl[t * a.v_rows + i], acc[t]);
           }
 #pragma unroll
           for (int t = 0; t < TC; ++t)

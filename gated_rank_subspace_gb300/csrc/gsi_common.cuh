@@ -32,6 +32,13 @@ struct F32 {
   __device__ __forceinline__ static float load1_cg(const void* base, int64_t i) {
     return __ldcg(reinterpret_cast<const float*>(base) + i);
   }
+  // acc[e] += x * w[e] for the 4 elements of w
+  __device__ __forceinline__ static void axpy(const uint4& w, float x, float* acc) {
+    acc[0] = fmaf(x, __uint_as_float(w.x), acc[0]);
+    acc[1] = fmaf(x, __uint_as_float(w.y), acc[1]);
+    acc[2] = fmaf(x, __uint_as_float(w.z), acc[2]);
+    acc[3] = fmaf(x, __uint_as_float(w.w), acc[3]);
+  }
   // a0 += w.x*x.x + w.z*x.z, a1 += w.y*x.y + w.w*x.w (in that order)
   __device__ __forceinline__ static void dot_acc(const uint4& w, const uint4& x, float& a0, float& a1) {
     a0 = fmaf(__uint_as_float(w.x), __uint_as_float(x.x), a0);
@@ -75,6 +82,19 @@ struct BF16 {
         "fma.rn.f32.bf16 %0, wl, xl, %0;\n\tfma.rn.f32.bf16 %1, wh, xh, %1;\n\t}"
         : "+f"(lo), "+f"(hi)
         : "r"(w), "r"(x));
+  }
+  // acc[e] += x * w[e] for the 8 elements of w, x a widened bf16 value: the
+  // mixed-precision FMA on x's bf16 bits (its f32 image's upper half) and
+  // the halves of w, one rounding each -- what fmaf on the widened values gives
+  __device__ __forceinline__ static void axpy(const uint4& w, float x, float* acc) {
+    const unsigned short xb = static_cast<unsigned short>(__float_as_uint(x) >> 16);
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      asm("{\n\t.reg .b16 wl, wh;\n\tmov.b32 {wl, wh}, %2;\n\t"
+          "fma.rn.f32.bf16 %0, wl, %3, %0;\n\tfma.rn.f32.bf16 %1, wh, %3, %1;\n\t}"
+          : "+f"(acc[2 * c]), "+f"(acc[2 * c + 1])
+          : "r"(wv[c]), "h"(xb));
   }
   // a0 += the products of the even elements, a1 of the odd ones, in order
   __device__ __forceinline__ static void dot_acc(const uint4& w, const uint4& x, float& a0, float& a1) {
