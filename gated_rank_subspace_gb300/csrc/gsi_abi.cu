@@ -177,6 +177,7 @@ struct DeviceFacts {
   int nsm = 0;
   int smem_optin = 0;
   int clusters[2][2][2] = {};  // co-resident clusters per [dtype][fused][cs == 16]; -1: not possible
+  int decode_clusters[2] = {};  // co-resident clusters of the single-token decode kernel per dtype
 };
 
 // Shared memory of the two-launch decide-and-apply kernel: the device limit
@@ -214,6 +215,70 @@ static int decide_clusters(DeviceFacts* f, gsi_dtype dt, bool fused, int cs) {
   return c > 0 ? c : 0;
 }
 
+// Co-resident clusters of the single-token decode kernel (cached); 0 if none.
+static int decode_clusters(DeviceFacts* f, gsi_dtype dt) {
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  int& c = f->decode_clusters[dt == GSI_BF16];
+  if (c == 0) {
+    const int n = decode_max_clusters(size_t(f->smem_optin), dt);
+    c = n > 0 ? n : -1;
+  }
+  return c > 0 ? c : 0;
+}
+
+// Enqueue the single-token decode kernel when the map's basis fits a
+// cluster (all arguments validated); GSI_ERR_UNSUPPORTED, with nothing
+// launched, when it does not.
+static gsi_status run_decode(const gsi_map_desc* m, const void* X, float eps, float* Y, uint8_t* flags, float* rho,
+                             void* ws, cudaStream_t st, DeviceFacts* f, const gsi_map_desc* next) {
+  const int ncl = decode_clusters(f, m->dtype);
+  if (ncl == 0) return GSI_ERR_UNSUPPORTED;
+  const DecodePlan p = plan_decode(m->d, m->d_out, m->k, elem_bytes(m->dtype), ncl * kDecodeCluster,
+                                   size_t(f->smem_optin));
+  if (!p.ok) return GSI_ERR_UNSUPPORTED;
+  Ctrl* ctrl = static_cast<Ctrl*>(ws);
+  DecodeArgs a{};
+  a.X = X;
+  a.W = m->W;
+  a.V = m->V;
+  a.M = m->M;
+  a.gram = m->gram;
+  a.d = m->d;
+  a.d_out = m->d_out;
+  a.k = int(m->k);
+  a.eps = eps;
+  a.Y = Y;
+  a.flags = flags;
+  a.rho = rho;
+  a.vr = p.vr;
+  a.rw = p.rw;
+  a.rpc = p.rpc;
+  a.ks = p.ks;
+  a.seg_bytes = p.seg_bytes;
+  a.sw = p.sw;
+  a.red_stride = p.red_stride;
+  a.m_late = p.m_late;
+  a.off_g = p.off_g;
+  a.off_y = p.off_y;
+  a.off_in = p.off_in;
+  a.off_gram = p.off_gram;
+  a.off_red = p.off_red;
+  a.off_v = p.off_v;
+  a.off_m = p.off_m;
+  if (next) {
+    const int nes = elem_bytes(next->dtype);
+    a.next_v = static_cast<const char*>(next->V);
+    a.next_v_bytes = uint64_t(next->d) * next->k * nes;
+    a.next_m = static_cast<const char*>(next->M);
+    a.next_m_bytes = uint64_t(next->d_out) * next->k * nes;
+    a.next_gram = reinterpret_cast<const char*>(next->gram);
+    a.next_gram_bytes = next->gram ? uint64_t(next->k) * next->k * 4 : 0;
+  }
+  a.err = &ctrl->err;
+  return cuda_check(launch_decode(a, p, m->dtype, st), "single-token decode kernel launch");
+}
+
 // Enqueue the decide-and-apply kernel for one map (all arguments validated).
 // mode 0: decide and apply (gsi_linear); 1: decide only (gsi_gate, writes
 // G, rho, flags and the compaction); 2: apply the decision stored by a
@@ -236,6 +301,11 @@ static gsi_status run_decide(const gsi_map_desc* m, const void* X, int64_t T, fl
   gsi_status s = device_facts(&f);
   if (s != GSI_OK) return s;
   DecidePlan dp{};
+  if (fused && mode == 0 && T == 1) {
+    // one token: the single-token decode kernel where the basis fits a cluster
+    s = run_decode(m, X, eps, Y, flags, rho, ws, st, f, next);
+    if (s != GSI_ERR_UNSUPPORTED) return s;
+  }
   if (fused) {
     // Cluster projection (each cluster projects x on all of V; no grid
     // barrier) where a sixteenth of V fits beside the other buffers, else

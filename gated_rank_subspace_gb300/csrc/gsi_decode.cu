@@ -1,0 +1,491 @@
+// Single-token decode kernel: the whole gated map for one token in one launch.
+//
+// "Gated Subspace Inference for Transformer Acceleration", §2.1-§2.2: for a
+// token x, g = V_k^T x, rho = ||x - V_k g|| / ||x||; rho < eps takes the fast
+// path y = M g (M = W V_k, the cached image), rho >= eps the exact y = W x.
+//
+// This is the batch-1 decode form for maps whose basis fits a cluster: each
+// cluster of 16 CTAs holds all of V_k in shared memory, so every cluster
+// finds g on its own and no CTA waits on another cluster.
+//
+//   prologue   each warp bulk-copies its own rows of the rank's V slab (one
+//              mbarrier per warp); the Gram slice and the CTA's M rows follow.
+//              All of this is weight traffic, issued before the dependency
+//              wait on the previous kernel of the stream.
+//   project    lane l of warp w loads token element v0 + w*rw + l and
+//              leaves it in the warp's slot of shared memory; the warp walks
+//              its V rows in batches of eight (vectors and elements loaded
+//              first) and keeps one 16-byte column group of g per lane;
+//              ||x||^2 is a warp sum.  Each warp leaves its partial in the
+//              space of its own, consumed, V rows.
+//   exchange   every thread adds the eight warps' partials of one column
+//              group and pushes the sum into the matching inbox slot of
+//              every rank of the cluster (st.async, completion on the
+//              receiver's mbarrier); each rank then adds the 16 inboxes in
+//              rank order -- the same bits in every CTA of every cluster.
+//   decide     warp w takes Gram rows c0 + w, c0 + w + 8, ... of the rank's
+//              slice: its share of g^T (V_k^T V_k) g and of ||g||^2 goes to
+//              every rank at once, and the warp goes on to y = M g for its
+//              own groups of four output rows.  Every warp then adds all
+//              ranks' shares in one fixed order, so all warps of all CTAs
+//              reach the same rho = sqrt(||x||^2 - 2||g||^2 + g^T G g) / ||x||
+//              and flag with no block-wide barrier.
+//   apply      fast: each warp writes its own y rows.  Slow: the eight
+//              warps stream the CTA's W rows (warp w: rows w, w + 8, ...)
+//              through per-warp rings of bulk copies that reuse the V and M
+//              space, with the token staged in shared memory.
+//
+// Every wait is bounded (~2 s of clock): on expiry the workspace error word
+// is set and the kernel carries on to its end without further waits on that
+// barrier.  There are no float atomics; every sum has one fixed order.
+
+#include "gsi_async.cuh"
+#include "gsi_common.cuh"
+#include "gsi_kernels.h"
+#include "gsi_plan.h"
+
+namespace gsi {
+
+template <class E>
+__global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) {
+  constexpr int PV = E::kPerVec;
+  constexpr int CS = kDecodeCluster;
+  constexpr int NW = kApplyThreads / 32;
+  constexpr unsigned FULL = 0xffffffffu;
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rank = int(cg::this_cluster().block_rank());
+  const int k = a.k;
+  const int64_t d = a.d, d_out = a.d_out;
+  const int mrow_b = k * E::kBytes;  // bytes of a V / M row
+  const int nvec = mrow_b / 16;      // 16-byte vectors of such a row (<= 32)
+  const int nf4 = k >> 2;            // float4 groups of g
+  const int64_t row_b = d * E::kBytes;
+
+  const int64_t r0 = int64_t(blockIdx.x) * a.rpc;  // this CTA's output rows
+  const int nrows = r0 >= d_out ? 0 : int(d_out - r0 < a.rpc ? d_out - r0 : a.rpc);
+  const int64_t v0 = int64_t(rank) * a.vr;         // this rank's V rows
+  const int vn = v0 >= d ? 0 : int(d - v0 < a.vr ? d - v0 : a.vr);
+  const int wr0 = warp * a.rw;                     // this warp's rows of the slab
+  const int wrn = vn - wr0 < 0 ? 0 : (vn - wr0 < a.rw ? vn - wr0 : a.rw);
+  const int c0 = rank * a.ks, c1 = min(k, c0 + a.ks);  // this rank's Gram rows
+
+  uint64_t* vbar = reinterpret_cast<uint64_t*>(smem);  // [NW] V rows of warp w
+  uint64_t* gbar = vbar + NW;                          // Gram slice
+  uint64_t* mbar = vbar + NW + 1;                      // M rows
+  uint64_t* xbar = vbar + NW + 2;                      // every rank's partial g and ||x||^2
+  uint64_t* qbar = vbar + NW + 3;                      // every rank's Gram and norm shares
+  uint64_t* ring = vbar + NW + 4;                      // [NW][sw] W segments
+  float* gfull = reinterpret_cast<float*>(smem + a.off_g);  // [k]
+  float* inx = gfull + k;                                   // [CS] ||x||^2 partials
+  float* qin = inx + CS;                                    // [CS][NW] g^T G g shares
+  float* nin = qin + CS * NW;                               // [CS][NW] ||g||^2 shares
+  float* nx2 = nin + CS * NW;                               // [1]
+  float* xw = nx2 + 4;                                      // [NW][32] token elements of each warp
+  float* ybuf = reinterpret_cast<float*>(smem + a.off_y);   // [rpc] y = M g
+  float* inbox = reinterpret_cast<float*>(smem + a.off_in); // [CS][k]; later the slow token
+  const float* gram_s = reinterpret_cast<const float*>(smem + a.off_gram);  // [ks][k]
+  unsigned char* Vs = smem + a.off_v;                       // V slab, then the W rings
+  unsigned char* Ms = smem + a.off_m;                       // M rows
+  float* red = reinterpret_cast<float*>(smem + a.off_red);  // warp w's partial at w * red_stride
+
+  // ---- prologue: weights only (may overlap the previous kernel's tail)
+  pdl_launch_dependents();
+  // one barrier per thread; the exchanges' byte counts are known now: every
+  // rank pushes k + 1 floats of projection partials and two shares per warp
+  if (tid < NW + 4 + NW * a.sw) {
+    bar_init(&vbar[tid], 1);
+    if (tid == NW + 2) bar_expect_tx(xbar, uint32_t(CS * (k + 1) * 4));
+    if (tid == NW + 3) bar_expect_tx(qbar, uint32_t(CS * NW * 2 * 4));
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (lane == 0 && wrn > 0) {
+    const uint32_t bytes = uint32_t(wrn) * uint32_t(mrow_b);
+    bar_expect_tx(&vbar[warp], bytes);
+    bulk_g2s(Vs + int64_t(wr0) * mrow_b, static_cast<const char*>(a.V) + (v0 + wr0) * mrow_b, bytes, &vbar[warp]);
+  }
+  const bool have_gram = a.gram != nullptr && c1 > c0;
+  if (tid == kApplyThreads - 32) {
+    if (have_gram) {
+      const uint32_t bytes = uint32_t(c1 - c0) * uint32_t(k) * 4u;
+      bar_expect_tx(gbar, bytes);
+      bulk_g2s(smem + a.off_gram, a.gram + int64_t(c0) * k, bytes, gbar);
+    }
+    if (nrows > 0 && !a.m_late) {
+      const uint32_t bytes = uint32_t(nrows) * uint32_t(mrow_b);
+      bar_expect_tx(mbar, bytes);
+      bulk_g2s(Ms, static_cast<const char*>(a.M) + r0 * mrow_b, bytes, mbar);
+    }
+  }
+  // weights of the next map of a stack, into L2 (this CTA's share)
+  if (tid == 64 || tid == 96 || tid == 128) {
+    const char* base = tid == 64 ? a.next_v : tid == 96 ? a.next_m : a.next_gram;
+    const uint64_t total = tid == 64 ? a.next_v_bytes : tid == 96 ? a.next_m_bytes : a.next_gram_bytes;
+    if (base && total) {
+      const uint64_t share = ((total + gridDim.x - 1) / gridDim.x + 15) / 16 * 16;
+      const uint64_t off = uint64_t(blockIdx.x) * share;
+      if (off < total) {
+        const uint64_t rem = total - off;
+        prefetch_l2(base + off, uint32_t(rem < share ? rem : share));
+      }
+    }
+  }
+  cluster_arrive_relaxed();
+  pdl_wait();
+
+  // ---- projection of this warp's rows
+  const float xv = lane < wrn ? E::load1_cg(a.X, v0 + wr0 + lane) : 0.f;
+  float* xme = xw + warp * 32;
+  xme[lane] = xv;
+  __syncwarp();
+  const float xsq = warp_sum(xv * xv);
+  float acc[PV];
+#pragma unroll
+  for (int e = 0; e < PV; ++e) acc[e] = 0.f;
+  if (wrn > 0) {
+    __all_sync(FULL, bar_wait(&vbar[warp], 0, a.err));
+    // rows in batches of 8: the vectors and token elements are loaded first,
+    // then multiplied in row order
+    const unsigned char* vrow = Vs + int64_t(wr0) * mrow_b + lane * 16;
+    const bool on = lane < nvec;
+    int i = 0;
+    for (; i + 8 <= wrn; i += 8) {
+      uint4 u[8];
+      float xi[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        u[j] = on ? *reinterpret_cast<const uint4*>(vrow + int64_t(i + j) * mrow_b) : make_uint4(0u, 0u, 0u, 0u);
+        xi[j] = xme[i + j];
+      }
+#pragma unroll
+      for (int j = 0; j < 8; ++j) E::axpy(u[j], xi[j], acc);
+    }
+    for (; i < wrn; ++i) {
+      const uint4 u = on ? *reinterpret_cast<const uint4*>(vrow + int64_t(i) * mrow_b) : make_uint4(0u, 0u, 0u, 0u);
+      E::axpy(u, xme[i], acc);
+    }
+  }
+  __syncwarp();
+  {
+    float* mine = red + warp * a.red_stride;  // this warp's own (consumed) V rows, or a separate slot
+    if (lane < nvec) {
+#pragma unroll
+      for (int e = 0; e < PV; e += 4)
+        *reinterpret_cast<float4*>(mine + lane * PV + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
+    }
+    if (lane == 0) mine[k] = xsq;
+  }
+  __syncthreads();
+  if (a.m_late && nrows > 0 && tid == kApplyThreads - 32) {
+    // the V slab is consumed: the M rows take its place
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    const uint32_t bytes = uint32_t(nrows) * uint32_t(mrow_b);
+    bar_expect_tx(mbar, bytes);
+    bulk_g2s(Ms, static_cast<const char*>(a.M) + r0 * mrow_b, bytes, mbar);
+  }
+
+  // ---- all-to-all inside the cluster: every rank gets every rank's partial
+  cluster_wait();  // every CTA of the cluster runs and has initialised its barriers
+  {
+    const int qstep = kApplyThreads / nf4;  // ranks served by the threads of one column group
+    if (tid < qstep * nf4) {
+      const int f4 = tid % nf4, q0 = tid / nf4;
+      float4 s = *reinterpret_cast<const float4*>(red + 4 * f4);
+#pragma unroll
+      for (int w = 1; w < NW; ++w) {
+        const float4 t = *reinterpret_cast<const float4*>(red + w * a.red_stride + 4 * f4);
+        s.x += t.x;
+        s.y += t.y;
+        s.z += t.z;
+        s.w += t.w;
+      }
+      const uint32_t dst = sa(inbox + rank * k + 4 * f4), bar = sa(xbar);
+      for (int q = q0; q < CS; q += qstep) st_async_v4(map_rank(dst, q), s, map_rank(bar, q));
+    }
+    if (tid < CS) {
+      float s = red[k];
+#pragma unroll
+      for (int w = 1; w < NW; ++w) s += red[w * a.red_stride + k];
+      st_async_f32(map_rank(sa(inx + rank), tid), s, map_rank(sa(xbar), tid));
+    }
+  }
+  __all_sync(FULL, bar_wait_cluster(xbar, 0, a.err));
+  if (tid < k) {
+    float s = 0.f;
+#pragma unroll
+    for (int r = 0; r < CS; ++r) s += inbox[r * k + tid];
+    gfull[tid] = s;
+  }
+  if (tid == kApplyThreads - 1) {
+    float s = 0.f;
+#pragma unroll
+    for (int r = 0; r < CS; ++r) s += inx[r];
+    *nx2 = s;
+  }
+  __syncthreads();
+
+  // ---- every warp: its share of the Gram form (Gram rows c0 + warp,
+  //      c0 + warp + NW, ...) and of ||g||^2, pushed to every rank, then
+  //      y = M g for its rows (groups of RB rows: RB warp, RB warp + RB NW, ...)
+  {
+    float q = 0.f, n = 0.f;
+    if (have_gram) {
+      __all_sync(FULL, bar_wait(gbar, 0, a.err));
+      // lane l takes column groups l and l + 32 (clamped loads, masked)
+      const float4* g4 = reinterpret_cast<const float4*>(gfull);
+      const bool oa = lane < nf4, ob = lane + 32 < nf4;
+      const int ja = oa ? lane : 0, jb = ob ? lane + 32 : 0;
+      const float4 ga = g4[ja], gb = g4[jb];
+      for (int i = c0 + warp; i < c1; i += NW) {
+        const float4* grow = reinterpret_cast<const float4*>(gram_s) + (i - c0) * nf4;
+        const float4 va = grow[ja], vb = grow[jb];
+        const float gi = gfull[i];
+        float ha = va.x * ga.x;
+        ha = fmaf(va.y, ga.y, ha);
+        ha = fmaf(va.z, ga.z, ha);
+        ha = fmaf(va.w, ga.w, ha);
+        float hb = vb.x * gb.x;
+        hb = fmaf(vb.y, gb.y, hb);
+        hb = fmaf(vb.z, gb.z, hb);
+        hb = fmaf(vb.w, gb.w, hb);
+        const float h = (oa ? ha : 0.f) + (ob ? hb : 0.f);
+        q = fmaf(gi, h, q);
+      }
+    }
+    for (int i = c0 + warp; i < c1; i += NW) n = fmaf(gfull[i], gfull[i], n);
+    q = warp_sum(q);
+    if (lane < CS) {
+      const uint32_t rb = map_rank(sa(qbar), lane);
+      st_async_f32(map_rank(sa(qin + rank * NW + warp), lane), q, rb);
+      st_async_f32(map_rank(sa(nin + rank * NW + warp), lane), n, rb);
+    }
+  }
+  if (nrows > 0) {
+    __all_sync(FULL, bar_wait(mbar, 0, a.err));
+    // lane l multiplies column group l of RB rows at a time; the row loads
+    // are unconditional (rows past the CTA's last repeat it, lanes past the
+    // row's vectors repeat vector 0) and masked afterwards, so all RB are in
+    // flight together
+    const bool on = lane < nvec;
+    const int vl = on ? lane : 0;
+    float gv[PV];
+#pragma unroll
+    for (int e = 0; e < PV; ++e) gv[e] = gfull[vl * PV + e];
+    auto apply_rows = [&](auto rb_c) {
+      constexpr int RB = decltype(rb_c)::value;
+      for (int rb = warp * RB; rb < nrows; rb += NW * RB) {
+        uint4 u[RB];
+#pragma unroll
+        for (int r = 0; r < RB; ++r)
+          u[r] = *reinterpret_cast<const uint4*>(Ms + int64_t(min(rb + r, nrows - 1)) * mrow_b + vl * 16);
+        float part[RB];
+#pragma unroll
+        for (int r = 0; r < RB; ++r) {
+          float w[PV];
+          E::unpack(u[r], w);
+          float p = 0.f;
+#pragma unroll
+          for (int e = 0; e < PV; ++e) p = fmaf(w[e], gv[e], p);
+          part[r] = on ? p : 0.f;
+        }
+        const float sum = warp_reduce_multi<RB>(part, lane);
+        const int r = row_of_lane<RB>(lane);
+        if ((lane & (32 / RB - 1)) == 0 && rb + r < nrows) ybuf[rb + r] = sum;
+      }
+    };
+    if (nrows <= NW * 4)
+      apply_rows(IntC<4>{});
+    else
+      apply_rows(IntC<8>{});
+  }
+  // ---- the decision, taken by every warp from the same shares in the same
+  //      order (rank r's shares by lane r in warp order, then a butterfly)
+  __all_sync(FULL, bar_wait_cluster(qbar, 0, a.err));
+  float Qr = 0.f, Nr = 0.f;
+  if (lane < CS) {
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+      Qr += qin[lane * NW + w];
+      Nr += nin[lane * NW + w];
+    }
+  }
+  float Q = warp_sum(Qr);
+  const float N = warp_sum(Nr);
+  if (!a.gram) Q = N;  // orthonormal basis: ||V g||^2 = ||g||^2
+  const float xx = *nx2;
+  float rr = xx - 2.f * N + Q;
+  rr = rr < 0.f ? 0.f : rr;  // keeps NaN
+  const float rho = xx == 0.f ? 0.f : sqrtf(rr / xx);
+  const bool slow = !(rho < a.eps);
+  if (blockIdx.x == 0 && tid == 0) {
+    if (a.rho) a.rho[0] = rho;
+    a.flags[0] = uint8_t(slow ? 1 : 0);
+  }
+
+  // ---- apply
+  if (!slow) {
+    // this warp's rows of y (the row groups it computed), from its own lanes
+    __syncwarp();
+    const int rbw = nrows <= NW * 4 ? 4 : 8;
+    for (int rb = warp * rbw; rb < nrows; rb += NW * rbw)
+      if (lane < rbw && rb + lane < nrows) a.Y[r0 + rb + lane] = ybuf[rb + lane];
+    return;
+  }
+  if (nrows == 0) return;
+  // Slow token: the V slab, the partials and the M rows are consumed, so the
+  // W rings take their space; the token goes where the inboxes were.
+  const int seg_b = a.seg_bytes, SW = a.sw;
+  const int nseg = int((row_b + seg_b - 1) / seg_b);
+  const int my_rows = warp < nrows ? (nrows - warp + NW - 1) / NW : 0;
+  const int items = my_rows * nseg;
+  unsigned char* wring = Vs + int64_t(warp) * SW * seg_b;
+  uint64_t* wfull = ring + warp * SW;
+  const char* wbase = static_cast<const char*>(a.W) + r0 * row_b;
+  // item q of this warp: segment q % nseg of its row q / nseg (CTA row
+  // warp + (q / nseg) * NW), in ring slot q % SW; issuer and consumer step
+  // through the items with counters
+  int q_row = 0, q_seg = 0, q_slot = 0;
+  auto issue_next = [&]() {
+    const int64_t offq = int64_t(q_seg) * seg_b;
+    const uint32_t bytes = uint32_t(min(int64_t(seg_b), row_b - offq));
+    bar_expect_tx(&wfull[q_slot], bytes);
+    bulk_g2s(wring + q_slot * seg_b, wbase + (int64_t(warp) + int64_t(q_row) * NW) * row_b + offq, bytes,
+             &wfull[q_slot]);
+    if (++q_seg == nseg) {
+      q_seg = 0;
+      ++q_row;
+    }
+    if (++q_slot == SW) q_slot = 0;
+  };
+  int issued = min(items, SW);
+  __syncthreads();  // every warp is done with the V slab and the M rows
+  if (lane == 0) {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    for (int q = 0; q < issued; ++q) issue_next();
+  }
+  unsigned char* xst = reinterpret_cast<unsigned char*>(inbox);
+  for (int64_t e = tid; e < row_b / 16; e += kApplyThreads)
+    reinterpret_cast<uint4*>(xst)[e] = ld_cg_v4(static_cast<const char*>(a.X) + e * 16);
+  __syncthreads();
+  float acc0 = 0.f, acc1 = 0.f;
+  int c_slot = 0, c_seg = 0, c_row = 0;
+  uint32_t c_ph = 0;
+  int i = 0;
+  for (; i < items; ++i) {
+    if (!__all_sync(FULL, bar_wait(&wfull[c_slot], c_ph, a.err))) break;
+    const int64_t off = int64_t(c_seg) * seg_b;
+    const int nv = int(min(int64_t(seg_b), row_b - off) / 16);
+    const unsigned char* segp = wring + c_slot * seg_b;
+    uint4 wq[kSegVecs];
+#pragma unroll
+    for (int u = 0; u < kSegVecs; ++u) {
+      const int v = u * 32 + lane;
+      wq[u] = v < nv ? *reinterpret_cast<const uint4*>(segp + v * 16) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    // the segment is in registers before its slot is refilled
+    uint32_t dep = 0;
+#pragma unroll
+    for (int u = 0; u < kSegVecs; ++u) dep ^= wq[u].x;
+    asm volatile("" ::"r"(dep) : "memory");
+    __syncwarp();
+    if (issued < items) {
+      if (lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        issue_next();
+      }
+      ++issued;
+    }
+    const unsigned char* xs = xst + off;
+#pragma unroll
+    for (int u = 0; u < kSegVecs; ++u) {
+      const int v = u * 32 + lane;
+      const uint4 xq = v < nv ? *reinterpret_cast<const uint4*>(xs + v * 16) : make_uint4(0u, 0u, 0u, 0u);
+      E::dot_acc(wq[u], xq, acc0, acc1);
+    }
+    if (++c_slot == SW) {
+      c_slot = 0;
+      c_ph ^= 1u;
+    }
+    if (++c_seg == nseg) {
+      const float sum = warp_sum(acc0 + acc1);
+      if (lane == 0) a.Y[r0 + warp + int64_t(c_row) * NW] = sum;
+      acc0 = acc1 = 0.f;
+      c_seg = 0;
+      ++c_row;
+    }
+  }
+  // after an expired wait: wait (bounded) for this warp's copies still in flight
+  if (lane == 0)
+    for (int q = i; q < issued; ++q) {
+      bar_wait(&wfull[c_slot], c_ph, a.err);
+      if (++c_slot == SW) {
+        c_slot = 0;
+        c_ph ^= 1u;
+      }
+    }
+}
+
+template <class E>
+static cudaError_t launch_decode_t(const DecodeArgs& a, const DecodePlan& p, cudaStream_t s) {
+  auto kern = decode_kernel<E>;
+  static size_t smem_set = 0;
+  if (p.smem > smem_set) {
+    cudaError_t e = set_kernel_smem(kern, p.smem);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess) return e;
+    smem_set = p.smem;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(p.ncta));
+  cfg.blockDim = dim3(kApplyThreads);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kDecodeCluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, gsi_dtype dt, cudaStream_t s) {
+  return dt == GSI_BF16 ? launch_decode_t<BF16>(a, p, s) : launch_decode_t<F32>(a, p, s);
+}
+
+template <class E>
+static int decode_max_clusters_t(size_t smem) {
+  auto kern = decode_kernel<E>;
+  if (set_kernel_smem(kern, smem) != cudaSuccess ||
+      cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(kDecodeCluster * 64);
+  cfg.blockDim = dim3(kApplyThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = kDecodeCluster;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+int decode_max_clusters(size_t smem, gsi_dtype dt) {
+  return dt == GSI_BF16 ? decode_max_clusters_t<BF16>(smem) : decode_max_clusters_t<F32>(smem);
+}
+
+}  // namespace gsi

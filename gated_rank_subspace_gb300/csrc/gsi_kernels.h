@@ -73,6 +73,38 @@ struct DecideArgs {
 };
 
 
+// Single-token decode kernel arguments (see gsi_decode.cu): one call of the
+// gated map for one token, decide and apply, in one launch.
+struct DecodeArgs {
+  const void* X;        // 1 x d token
+  const void* W;        // d_out x d
+  const void* V;        // d x k
+  const void* M;        // d_out x k
+  const float* gram;    // k x k, or null (orthonormal basis)
+  int64_t d, d_out;
+  int k;
+  float eps;
+  float* Y;             // 1 x d_out
+  uint8_t* flags;       // 1
+  float* rho;           // 1, or null
+  // geometry and shared-memory offsets (DecodePlan)
+  int vr, rw, rpc, ks, seg_bytes, sw, red_stride, m_late;
+  int off_g, off_y, off_in, off_gram, off_red, off_v, off_m;
+  // weights of the next map of a stack, staged in L2 while this one runs
+  const char* next_v;
+  uint64_t next_v_bytes;
+  const char* next_m;
+  uint64_t next_m_bytes;
+  const char* next_gram;
+  uint64_t next_gram_bytes;
+  uint32_t* err;        // device error word (bounded waits)
+};
+
+cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, gsi_dtype dt, cudaStream_t s);
+// Co-resident kDecodeCluster-CTA clusters of the single-token decode kernel
+// with `smem` bytes of shared memory per CTA; 0 if none.
+int decode_max_clusters(size_t smem, gsi_dtype dt);
+
 // Tensor-core path (bf16, prefill-sized T).  All pointers are device pointers;
 // Vt, G, Gbf, Gfast, Xslow and idx live in the call's workspace.
 struct TensorArgs {

@@ -237,4 +237,78 @@ inline DecidePlan plan_decide(int64_t d, int64_t d_out, int64_t k, int es, int64
   return p;
 }
 
+// Single-token decode kernel geometry (see gsi_decode.cu).  Clusters of
+// kDecodeCluster CTAs; cluster rank r projects V rows [r * vr, (r + 1) * vr)
+// (warp w of it rows [w * rw, (w + 1) * rw) of that slab, at most 32, one per
+// lane), CTA b applies output rows [b * rpc, (b + 1) * rpc).  Shared memory:
+// mbarriers | g, exchange inboxes, token elements | fast outputs | partial-g inbox
+// (then the slow token's x) | Gram slice | V slab | M rows.  The W rings of a
+// slow token reuse the V slab and M rows once the decision is taken.  When V
+// and M do not fit side by side, the M rows are copied over the V slab after
+// the projection (m_late) and the warps' partial sums get their own region.
+constexpr int kDecodeCluster = 16;
+constexpr int kDecodeMaxStages = 6;
+
+struct DecodePlan {
+  int vr, rw, rpc, ks, seg_bytes, sw, red_stride, m_late;
+  int off_g, off_y, off_in, off_gram, off_red, off_v, off_m;
+  int ncta;
+  size_t smem;
+  bool ok;
+};
+
+inline DecodePlan plan_decode(int64_t d, int64_t d_out, int64_t k, int es, int ncta, size_t smem_budget) {
+  DecodePlan p{};
+  p.ok = false;
+  const int64_t mrow_b = k * es, row_b = d * es;
+  const int nw = kApplyThreads / 32;
+  if (ncta < kDecodeCluster || ncta % kDecodeCluster || k % 4 || mrow_b % 16 || row_b % 16) return p;
+  if (mrow_b / 16 > 32) return p;  // one 16-byte vector of a V / M row per lane
+  p.ncta = ncta;
+  p.vr = int(cdiv(d, kDecodeCluster));
+  p.rw = int(cdiv(p.vr, nw));
+  if (p.rw > 32) return p;  // one token element per lane
+  p.rpc = int(cdiv(d_out, ncta));
+  p.ks = int(cdiv(k, kDecodeCluster));
+  p.seg_bytes = int(row_b < kSegBytes ? row_b : kSegBytes);
+  const size_t bars = size_t(nw + 4 + nw * kDecodeMaxStages) * 8;
+  size_t off = (bars + 127) & ~size_t(127);
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = (off + bytes + 127) & ~size_t(127);
+    return int(at);
+  };
+  p.off_g = take(size_t(k + kDecodeCluster + 2 * kDecodeCluster * nw + 4 + nw * 32) * 4);
+  p.off_y = take(size_t(p.rpc) * 4);
+  const size_t inbox = size_t(kDecodeCluster) * k * 4;
+  p.off_in = take(inbox > size_t(row_b) ? inbox : size_t(row_b));
+  p.off_gram = take(size_t(p.ks) * k * 4);
+  const size_t v_bytes = size_t(nw) * p.rw * mrow_b;
+  const size_t m_bytes = size_t(p.rpc) * mrow_b;
+  const size_t red_b = size_t(k + 4) * 4;  // a warp's partial g and its ||x||^2
+  const size_t rest = off;
+  for (int late = 0; late < 2; ++late) {
+    off = rest;
+    const bool alias = !late && size_t(p.rw) * mrow_b >= red_b;
+    p.off_red = alias ? 0 : take(size_t(nw) * red_b);
+    p.red_stride = int(alias ? size_t(p.rw) * mrow_b / 4 : red_b / 4);
+    p.off_v = int(off);
+    if (alias) p.off_red = p.off_v;
+    p.off_m = late ? p.off_v : int(off + v_bytes);
+    size_t region = late ? (v_bytes > m_bytes ? v_bytes : m_bytes) : v_bytes + m_bytes;
+    int sw = int(region / (size_t(nw) * p.seg_bytes));
+    sw = sw > kDecodeMaxStages ? kDecodeMaxStages : sw < 2 ? 2 : sw;
+    const size_t ring = size_t(nw) * sw * p.seg_bytes;
+    if (ring > region) region = ring;
+    p.sw = sw;
+    p.m_late = late;
+    p.smem = size_t(p.off_v) + region;
+    if (p.smem <= smem_budget) {
+      p.ok = true;
+      return p;
+    }
+  }
+  return p;
+}
+
 }  // namespace gsi
