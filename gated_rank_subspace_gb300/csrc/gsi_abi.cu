@@ -227,15 +227,16 @@ static int decode_clusters(DeviceFacts* f, gsi_dtype dt) {
   return c > 0 ? c : 0;
 }
 
-// Enqueue the single-token decode kernel when the map's basis fits a
-// cluster (all arguments validated); GSI_ERR_UNSUPPORTED, with nothing
-// launched, when it does not.
+// Enqueue the single-token decode kernel (all arguments validated): the
+// cluster projection where the basis fits a cluster, else the grid
+// projection; GSI_ERR_UNSUPPORTED, with nothing launched, when neither fits.
 static gsi_status run_decode(const gsi_map_desc* m, const void* X, float eps, float* Y, uint8_t* flags, float* rho,
                              void* ws, cudaStream_t st, DeviceFacts* f, const gsi_map_desc* next) {
+  const int es = elem_bytes(m->dtype);
+  DecodePlan p{};
   const int ncl = decode_clusters(f, m->dtype);
-  if (ncl == 0) return GSI_ERR_UNSUPPORTED;
-  const DecodePlan p = plan_decode(m->d, m->d_out, m->k, elem_bytes(m->dtype), ncl * kDecodeCluster,
-                                   size_t(f->smem_optin));
+  for (int grid = 0; grid < 2 && ncl > 0 && !p.ok; ++grid)
+    p = plan_decode(m->d, m->d_out, m->k, es, ncl * kDecodeCluster, size_t(f->smem_optin), grid != 0);
   if (!p.ok) return GSI_ERR_UNSUPPORTED;
   Ctrl* ctrl = static_cast<Ctrl*>(ws);
   DecodeArgs a{};
@@ -266,6 +267,13 @@ static gsi_status run_decode(const gsi_map_desc* m, const void* X, float eps, fl
   a.off_red = p.off_red;
   a.off_v = p.off_v;
   a.off_m = p.off_m;
+  a.grid = p.grid;
+  if (p.grid) {
+    const FusedLayout FL = layout_fused(m->k, 1);
+    a.part_g = reinterpret_cast<float*>(static_cast<char*>(ws) + FL.part_g);
+    a.part_x = reinterpret_cast<float*>(static_cast<char*>(ws) + FL.part_x);
+    a.ticket = &ctrl->ticket1[m->dtype == GSI_BF16 ? 1 : 0];
+  }
   if (next) {
     const int nes = elem_bytes(next->dtype);
     a.next_v = static_cast<const char*>(next->V);

@@ -69,6 +69,18 @@ __device__ __forceinline__ bool grid_barrier(unsigned long long* ticket, unsigne
   return true;
 }
 
+// Epoch-tagged words across the grid: a 64-bit word (epoch << 32 | value
+// bits) is stored and loaded whole, so a reader that sees the current epoch
+// also sees that value, with no fence or flag between them.
+__device__ __forceinline__ void st_relaxed_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // Exchanges inside a cluster: st.async stores into a peer's shared memory
 // that complete on the peer's mbarrier, so each CTA waits (acquire at
 // cluster scope, bounded) only for the bytes it receives.

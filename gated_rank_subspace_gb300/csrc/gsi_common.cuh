@@ -249,7 +249,9 @@ struct Ctrl {
   // fused decode's grid barrier, one ticket counter per element type: the
   // arrivals of all calls so far (zeroed by gsi_workspace_init, never reset)
   unsigned long long ticket[2];
-  uint32_t pad[56];
+  // the single-token decode's grid barrier (grid projection), per element type
+  unsigned long long ticket1[2];
+  uint32_t pad[52];
 };
 static_assert(sizeof(Ctrl) == 256, "Ctrl is 256 bytes");
 

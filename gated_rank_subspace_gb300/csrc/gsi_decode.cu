@@ -4,9 +4,16 @@
 // token x, g = V_k^T x, rho = ||x - V_k g|| / ||x||; rho < eps takes the fast
 // path y = M g (M = W V_k, the cached image), rho >= eps the exact y = W x.
 //
-// This is the batch-1 decode form for maps whose basis fits a cluster: each
-// cluster of 16 CTAs holds all of V_k in shared memory, so every cluster
-// finds g on its own and no CTA waits on another cluster.
+// This is the batch-1 decode form.  Where the basis fits a cluster, each
+// cluster of 16 CTAs holds all of V_k in shared memory and finds g on its
+// own (cluster projection: no CTA waits on another cluster).  Larger bases
+// are split over the whole grid (grid projection): each cluster reduces its
+// CTAs' partials by a reduce-scatter in distributed shared memory and every
+// rank publishes its slice of columns as epoch-tagged 64-bit words; rank q
+// of every cluster polls the clusters' words of its slice until they carry
+// the call's epoch, adds them in cluster order and gathers g inside its
+// cluster.  No grid-wide barrier: the epoch comes from a ticket each CTA
+// takes in its prologue.  Both forms give every CTA the same bits of g.
 //
 //   prologue   each warp bulk-copies its own rows of the rank's V slab (one
 //              mbarrier per warp); the Gram slice and the CTA's M rows follow.
@@ -55,6 +62,9 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int rank = int(cg::this_cluster().block_rank());
+  // one instantiation for both projection forms: the four maps of a layer
+  // then run the same code, which stays in the instruction cache
+  const bool grid_proj = a.grid != 0;
   const int k = a.k;
   const int64_t d = a.d, d_out = a.d_out;
   const int mrow_b = k * E::kBytes;  // bytes of a V / M row
@@ -64,7 +74,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
 
   const int64_t r0 = int64_t(blockIdx.x) * a.rpc;  // this CTA's output rows
   const int nrows = r0 >= d_out ? 0 : int(d_out - r0 < a.rpc ? d_out - r0 : a.rpc);
-  const int64_t v0 = int64_t(rank) * a.vr;         // this rank's V rows
+  const int64_t v0 = int64_t(grid_proj ? int(blockIdx.x) : rank) * a.vr;  // this CTA's V rows
   const int vn = v0 >= d ? 0 : int(d - v0 < a.vr ? d - v0 : a.vr);
   const int wr0 = warp * a.rw;                     // this warp's rows of the slab
   const int wrn = vn - wr0 < 0 ? 0 : (vn - wr0 < a.rw ? vn - wr0 : a.rw);
@@ -75,31 +85,40 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
   uint64_t* mbar = vbar + NW + 1;                      // M rows
   uint64_t* xbar = vbar + NW + 2;                      // every rank's partial g and ||x||^2
   uint64_t* qbar = vbar + NW + 3;                      // every rank's Gram and norm shares
-  uint64_t* ring = vbar + NW + 4;                      // [NW][sw] W segments
+  uint64_t* gxbar = vbar + NW + 4;                     // grid projection: g gathered from the ranks
+  uint64_t* ring = vbar + NW + kDecodeBars;            // [NW][sw] W segments
   float* gfull = reinterpret_cast<float*>(smem + a.off_g);  // [k]
   float* inx = gfull + k;                                   // [CS] ||x||^2 partials
   float* qin = inx + CS;                                    // [CS][NW] g^T G g shares
   float* nin = qin + CS * NW;                               // [CS][NW] ||g||^2 shares
   float* nx2 = nin + CS * NW;                               // [1]
+  uint32_t* sepoch = reinterpret_cast<uint32_t*>(nx2 + 1);  // [1] grid projection: this call's epoch
   float* xw = nx2 + 4;                                      // [NW][32] token elements of each warp
   float* ybuf = reinterpret_cast<float*>(smem + a.off_y);   // [rpc] y = M g
-  float* inbox = reinterpret_cast<float*>(smem + a.off_in); // [CS][k]; later the slow token
+  float* inbox = reinterpret_cast<float*>(smem + a.off_in); // [CS][k] (grid: [CS][ks]); later the slow token
   const float* gram_s = reinterpret_cast<const float*>(smem + a.off_gram);  // [ks][k]
   unsigned char* Vs = smem + a.off_v;                       // V slab, then the W rings
   unsigned char* Ms = smem + a.off_m;                       // M rows
   float* red = reinterpret_cast<float*>(smem + a.off_red);  // warp w's partial at w * red_stride
 
   // ---- prologue: weights only (may overlap the previous kernel's tail)
-  pdl_launch_dependents();
+  // Grid projection: this CTA's ticket, taken before the next kernel of the
+  // stream may start, numbers the call: every CTA of call e takes one of the
+  // tickets [(e - 1) n, e n), n = the grid size, so epoch e = ticket / n + 1
+  // is known to all of them without a barrier.
+  if (grid_proj && tid == 0) *sepoch = uint32_t(atomicAdd(a.ticket, 1ull) / gridDim.x) + 1u;
   // one barrier per thread; the exchanges' byte counts are known now: every
-  // rank pushes k + 1 floats of projection partials and two shares per warp
-  if (tid < NW + 4 + NW * a.sw) {
+  // rank pushes its partial g (all k columns; grid projection: the receiver's
+  // ks) and ||x||^2, and two shares per warp; the gathered g is k + 1 floats
+  if (tid < NW + kDecodeBars + NW * a.sw) {
     bar_init(&vbar[tid], 1);
-    if (tid == NW + 2) bar_expect_tx(xbar, uint32_t(CS * (k + 1) * 4));
+    if (tid == NW + 2) bar_expect_tx(xbar, uint32_t(CS * ((grid_proj ? a.ks : k) + 1) * 4));
     if (tid == NW + 3) bar_expect_tx(qbar, uint32_t(CS * NW * 2 * 4));
+    if (grid_proj && tid == NW + 4) bar_expect_tx(gxbar, uint32_t((k + 1) * 4));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  pdl_launch_dependents();
   if (lane == 0 && wrn > 0) {
     const uint32_t bytes = uint32_t(wrn) * uint32_t(mrow_b);
     bar_expect_tx(&vbar[warp], bytes);
@@ -185,9 +204,9 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
     bulk_g2s(Ms, static_cast<const char*>(a.M) + r0 * mrow_b, bytes, mbar);
   }
 
-  // ---- all-to-all inside the cluster: every rank gets every rank's partial
   cluster_wait();  // every CTA of the cluster runs and has initialised its barriers
-  {
+  if (!grid_proj) {
+    // ---- all-to-all inside the cluster: every rank gets every rank's partial
     const int qstep = kApplyThreads / nf4;  // ranks served by the threads of one column group
     if (tid < qstep * nf4) {
       const int f4 = tid % nf4, q0 = tid / nf4;
@@ -209,21 +228,90 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
       for (int w = 1; w < NW; ++w) s += red[w * a.red_stride + k];
       st_async_f32(map_rank(sa(inx + rank), tid), s, map_rank(sa(xbar), tid));
     }
-  }
-  __all_sync(FULL, bar_wait_cluster(xbar, 0, a.err));
-  if (tid < k) {
-    float s = 0.f;
+    __all_sync(FULL, bar_wait_cluster(xbar, 0, a.err));
+    if (tid < k) {
+      float s = 0.f;
 #pragma unroll
-    for (int r = 0; r < CS; ++r) s += inbox[r * k + tid];
-    gfull[tid] = s;
-  }
-  if (tid == kApplyThreads - 1) {
-    float s = 0.f;
+      for (int r = 0; r < CS; ++r) s += inbox[r * k + tid];
+      gfull[tid] = s;
+    }
+    if (tid == kApplyThreads - 1) {
+      float s = 0.f;
 #pragma unroll
-    for (int r = 0; r < CS; ++r) s += inx[r];
-    *nx2 = s;
+      for (int r = 0; r < CS; ++r) s += inx[r];
+      *nx2 = s;
+    }
+    __syncthreads();
+  } else {
+    // ---- grid projection: reduce-scatter inside the cluster (rank q gets
+    //      every rank's columns [q ks, (q + 1) ks)), one published slice per
+    //      rank, the grid barrier, then rank q adds the clusters' slices in
+    //      cluster order and pushes them to every rank of its cluster
+    const int ks = a.ks;
+    if (tid < k) {
+      float s = red[tid];
+#pragma unroll
+      for (int w = 1; w < NW; ++w) s += red[w * a.red_stride + tid];
+      const int q = tid / ks;
+      st_async_f32(map_rank(sa(inbox + rank * ks + (tid - q * ks)), q), s, map_rank(sa(xbar), q));
+    }
+    if (tid < CS) {
+      float s = red[k];
+#pragma unroll
+      for (int w = 1; w < NW; ++w) s += red[w * a.red_stride + k];
+      st_async_f32(map_rank(sa(inx + rank), tid), s, map_rank(sa(xbar), tid));
+    }
+    __all_sync(FULL, bar_wait_cluster(xbar, 0, a.err));
+    const int cl = int(blockIdx.x) / CS, ncl = int(gridDim.x) / CS;
+    const uint32_t epoch = *sepoch;
+    unsigned long long* pw = reinterpret_cast<unsigned long long*>(a.part_g);  // [ncl][k] tagged
+    unsigned long long* px = reinterpret_cast<unsigned long long*>(a.part_x);  // [ncl] tagged
+    const bool xlane = tid == ks && rank == 0;
+    if (tid < ks) {
+      float s = 0.f;
+#pragma unroll
+      for (int r = 0; r < CS; ++r) s += inbox[r * ks + tid];
+      st_relaxed_u64(pw + int64_t(cl) * k + c0 + tid, (uint64_t(epoch) << 32) | __float_as_uint(s));
+    }
+    if (xlane) {
+      float s = 0.f;
+#pragma unroll
+      for (int r = 0; r < CS; ++r) s += inx[r];
+      st_relaxed_u64(px + cl, (uint64_t(epoch) << 32) | __float_as_uint(s));
+    }
+    if (tid < ks || xlane) {
+      // every cluster's word of this column (or of ||x||^2), polled until
+      // it carries this call's epoch (bounded), added in cluster order
+      const unsigned long long* src = tid < ks ? pw + c0 + tid : px;
+      const int64_t stride = tid < ks ? k : 1;
+      float v[kDecodeMaxClusters];
+      uint32_t pending = (1u << ncl) - 1u;
+      const long long t0 = clock64();
+      while (pending) {
+        unsigned long long w[kDecodeMaxClusters];  // all loads in flight, then the checks
+#pragma unroll
+        for (int c = 0; c < kDecodeMaxClusters; ++c)
+          w[c] = ((pending >> c) & 1u) ? ld_relaxed_u64(src + c * stride) : 0ull;
+#pragma unroll
+        for (int c = 0; c < kDecodeMaxClusters; ++c)
+          if (((pending >> c) & 1u) && uint32_t(w[c] >> 32) == epoch) {
+            v[c] = __uint_as_float(uint32_t(w[c]));
+            pending &= ~(1u << c);
+          }
+        if (pending && clock64() - t0 > kSpinCycles) {
+          atomicOr(a.err, kErrTimeout);
+          break;
+        }
+      }
+      float s = 0.f;
+#pragma unroll
+      for (int c = 0; c < kDecodeMaxClusters; ++c)
+        if (c < ncl) s += ((pending >> c) & 1u) ? 0.f : v[c];
+      const uint32_t dst = sa(tid < ks ? gfull + c0 + tid : nx2), bar = sa(gxbar);
+      for (int q = 0; q < CS; ++q) st_async_f32(map_rank(dst, q), s, map_rank(bar, q));
+    }
+    __all_sync(FULL, bar_wait_cluster(gxbar, 0, a.err));
   }
-  __syncthreads();
 
   // ---- every warp: its share of the Gram form (Gram rows c0 + warp,
   //      c0 + warp + NW, ...) and of ||g||^2, pushed to every rank, then

@@ -90,6 +90,12 @@ struct DecodeArgs {
   // geometry and shared-memory offsets (DecodePlan)
   int vr, rw, rpc, ks, seg_bytes, sw, red_stride, m_late;
   int off_g, off_y, off_in, off_gram, off_red, off_v, off_m;
+  // grid projection: each cluster's partial g [clusters][k] and ||x||^2
+  // [clusters], published before the grid barrier on the ticket counter
+  int grid;
+  float* part_g;
+  float* part_x;
+  unsigned long long* ticket;
   // weights of the next map of a stack, staged in L2 while this one runs
   const char* next_v;
   uint64_t next_v_bytes;

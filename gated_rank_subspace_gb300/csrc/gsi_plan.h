@@ -238,40 +238,49 @@ inline DecidePlan plan_decide(int64_t d, int64_t d_out, int64_t k, int es, int64
 }
 
 // Single-token decode kernel geometry (see gsi_decode.cu).  Clusters of
-// kDecodeCluster CTAs; cluster rank r projects V rows [r * vr, (r + 1) * vr)
-// (warp w of it rows [w * rw, (w + 1) * rw) of that slab, at most 32, one per
-// lane), CTA b applies output rows [b * rpc, (b + 1) * rpc).  Shared memory:
-// mbarriers | g, exchange inboxes, token elements | fast outputs | partial-g inbox
-// (then the slow token's x) | Gram slice | V slab | M rows.  The W rings of a
-// slow token reuse the V slab and M rows once the decision is taken.  When V
-// and M do not fit side by side, the M rows are copied over the V slab after
-// the projection (m_late) and the warps' partial sums get their own region.
+// kDecodeCluster CTAs.  Cluster projection: cluster rank r projects V rows
+// [r * vr, (r + 1) * vr), so every cluster holds all of V.  Grid projection
+// (bases too large for that): CTA b projects rows [b * vr, (b + 1) * vr).
+// Warp w takes rows [w * rw, (w + 1) * rw) of the CTA's slab, at most 32, one
+// per lane.  CTA b applies output rows [b * rpc, (b + 1) * rpc).  Shared
+// memory: mbarriers | g, exchange inboxes, token elements | fast outputs |
+// partial-g inbox (then the slow token's x) | Gram slice | V slab | M rows.
+// The W rings of a slow token reuse the V slab and M rows (and the space
+// after them) once the decision is taken.  When V and M do not fit side by
+// side, the M rows are copied over the V slab after the projection (m_late)
+// and the warps' partial sums get their own region.
 constexpr int kDecodeCluster = 16;
 constexpr int kDecodeMaxStages = 6;
+constexpr int kDecodeBars = 5;  // Gram, M, partials, shares, gathered g
+constexpr int kDecodeMaxClusters = 16;  // grid projection: clusters whose slices are polled
 
 struct DecodePlan {
-  int vr, rw, rpc, ks, seg_bytes, sw, red_stride, m_late;
+  int vr, rw, rpc, ks, seg_bytes, sw, red_stride, m_late, grid;
   int off_g, off_y, off_in, off_gram, off_red, off_v, off_m;
   int ncta;
   size_t smem;
   bool ok;
 };
 
-inline DecodePlan plan_decode(int64_t d, int64_t d_out, int64_t k, int es, int ncta, size_t smem_budget) {
+inline DecodePlan plan_decode(int64_t d, int64_t d_out, int64_t k, int es, int ncta, size_t smem_budget,
+                              bool grid) {
   DecodePlan p{};
   p.ok = false;
   const int64_t mrow_b = k * es, row_b = d * es;
   const int nw = kApplyThreads / 32;
   if (ncta < kDecodeCluster || ncta % kDecodeCluster || k % 4 || mrow_b % 16 || row_b % 16) return p;
-  if (mrow_b / 16 > 32) return p;  // one 16-byte vector of a V / M row per lane
+  if (mrow_b / 16 > 32) return p;             // one 16-byte vector of a V / M row per lane
+  if (grid && k % kDecodeCluster) return p;  // equal column slices for the reduce-scatter
+  if (grid && ncta > kDecodeCluster * kDecodeMaxClusters) return p;
   p.ncta = ncta;
-  p.vr = int(cdiv(d, kDecodeCluster));
+  p.grid = grid ? 1 : 0;
+  p.vr = int(cdiv(d, grid ? ncta : kDecodeCluster));
   p.rw = int(cdiv(p.vr, nw));
   if (p.rw > 32) return p;  // one token element per lane
   p.rpc = int(cdiv(d_out, ncta));
   p.ks = int(cdiv(k, kDecodeCluster));
   p.seg_bytes = int(row_b < kSegBytes ? row_b : kSegBytes);
-  const size_t bars = size_t(nw + 4 + nw * kDecodeMaxStages) * 8;
+  const size_t bars = size_t(nw + kDecodeBars + nw * kDecodeMaxStages) * 8;
   size_t off = (bars + 127) & ~size_t(127);
   auto take = [&](size_t bytes) {
     const size_t at = off;
@@ -295,17 +304,18 @@ inline DecodePlan plan_decode(int64_t d, int64_t d_out, int64_t k, int es, int n
     p.off_v = int(off);
     if (alias) p.off_red = p.off_v;
     p.off_m = late ? p.off_v : int(off + v_bytes);
-    size_t region = late ? (v_bytes > m_bytes ? v_bytes : m_bytes) : v_bytes + m_bytes;
-    int sw = int(region / (size_t(nw) * p.seg_bytes));
-    sw = sw > kDecodeMaxStages ? kDecodeMaxStages : sw < 2 ? 2 : sw;
-    const size_t ring = size_t(nw) * sw * p.seg_bytes;
-    if (ring > region) region = ring;
-    p.sw = sw;
-    p.m_late = late;
-    p.smem = size_t(p.off_v) + region;
-    if (p.smem <= smem_budget) {
-      p.ok = true;
-      return p;
+    const size_t need = late ? (v_bytes > m_bytes ? v_bytes : m_bytes) : v_bytes + m_bytes;
+    // the deepest W ring (at least 2 slots a warp) that fits
+    for (int sw = kDecodeMaxStages; sw >= 2; --sw) {
+      const size_t ring = size_t(nw) * sw * p.seg_bytes;
+      const size_t region = ring > need ? ring : need;
+      if (size_t(p.off_v) + region <= smem_budget) {
+        p.sw = sw;
+        p.m_late = late;
+        p.smem = size_t(p.off_v) + region;
+        p.ok = true;
+        return p;
+      }
     }
   }
   return p;
