@@ -25,11 +25,12 @@
 //              first) and keeps one 16-byte column group of g per lane;
 //              ||x||^2 is a warp sum.  Each warp leaves its partial in the
 //              space of its own, consumed, V rows.
-//   exchange   every thread adds the eight warps' partials of one column
-//              group and pushes the sum into the matching inbox slot of
-//              every rank of the cluster (st.async, completion on the
-//              receiver's mbarrier); each rank then adds the 16 inboxes in
-//              rank order -- the same bits in every CTA of every cluster.
+//   exchange   thread c adds the eight warps' partials of column c and
+//              pushes the sum to the rank that owns the column (a
+//              reduce-scatter by st.async, completion on the receiver's
+//              mbarrier); each rank adds its 16 inboxes in rank order and
+//              pushes its slice of g to every rank (an all-gather) -- the
+//              same bits in every CTA of every cluster.
 //   decide     warp w takes Gram rows c0 + w, c0 + w + 8, ... of the rank's
 //              slice: its share of g^T (V_k^T V_k) g and of ||g||^2 goes to
 //              every rank at once, and the warp goes on to y = M g for its
@@ -40,7 +41,10 @@
 //   apply      fast: each warp writes its own y rows.  Slow: the eight
 //              warps stream the CTA's W rows (warp w: rows w, w + 8, ...)
 //              through per-warp rings of bulk copies that reuse the V and M
-//              space, with the token staged in shared memory.
+//              space (as deep as shared memory allows, up to six 4 KB
+//              slots a warp), with the token staged in shared memory.  (An
+//              L2 prefetch of the segments ahead of the rings was measured
+//              slower at every distance tried.)
 //
 // Every wait is bounded (~2 s of clock): on expiry the workspace error word
 // is set and the kernel carries on to its end without further waits on that
@@ -85,7 +89,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
   uint64_t* mbar = vbar + NW + 1;                      // M rows
   uint64_t* xbar = vbar + NW + 2;                      // every rank's partial g and ||x||^2
   uint64_t* qbar = vbar + NW + 3;                      // every rank's Gram and norm shares
-  uint64_t* gxbar = vbar + NW + 4;                     // grid projection: g gathered from the ranks
+  uint64_t* gxbar = vbar + NW + 4;                     // g and ||x||^2 gathered from the ranks
   uint64_t* ring = vbar + NW + kDecodeBars;            // [NW][sw] W segments
   float* gfull = reinterpret_cast<float*>(smem + a.off_g);  // [k]
   float* inx = gfull + k;                                   // [CS] ||x||^2 partials
@@ -95,7 +99,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
   uint32_t* sepoch = reinterpret_cast<uint32_t*>(nx2 + 1);  // [1] grid projection: this call's epoch
   float* xw = nx2 + 4;                                      // [NW][32] token elements of each warp
   float* ybuf = reinterpret_cast<float*>(smem + a.off_y);   // [rpc] y = M g
-  float* inbox = reinterpret_cast<float*>(smem + a.off_in); // [CS][k] (grid: [CS][ks]); later the slow token
+  float* inbox = reinterpret_cast<float*>(smem + a.off_in); // [CS][ks] partial-g slices; later the slow token
   const float* gram_s = reinterpret_cast<const float*>(smem + a.off_gram);  // [ks][k]
   unsigned char* Vs = smem + a.off_v;                       // V slab, then the W rings
   unsigned char* Ms = smem + a.off_m;                       // M rows
@@ -108,13 +112,13 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
   // is known to all of them without a barrier.
   if (grid_proj && tid == 0) *sepoch = uint32_t(atomicAdd(a.ticket, 1ull) / gridDim.x) + 1u;
   // one barrier per thread; the exchanges' byte counts are known now: every
-  // rank pushes its partial g (all k columns; grid projection: the receiver's
-  // ks) and ||x||^2, and two shares per warp; the gathered g is k + 1 floats
+  // rank pushes the receiver's columns of its partial g and its ||x||^2, and
+  // two shares per warp; the gathered g and ||x||^2 are k + 1 floats
   if (tid < NW + kDecodeBars + NW * a.sw) {
     bar_init(&vbar[tid], 1);
-    if (tid == NW + 2) bar_expect_tx(xbar, uint32_t(CS * ((grid_proj ? a.ks : k) + 1) * 4));
+    if (tid == NW + 2) bar_expect_tx(xbar, uint32_t(CS * ((c1 > c0 ? c1 - c0 : 0) + 1) * 4));
     if (tid == NW + 3) bar_expect_tx(qbar, uint32_t(CS * NW * 2 * 4));
-    if (grid_proj && tid == NW + 4) bar_expect_tx(gxbar, uint32_t((k + 1) * 4));
+    if (tid == NW + 4) bar_expect_tx(gxbar, uint32_t((k + 1) * 4));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -205,85 +209,40 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
   }
 
   cluster_wait();  // every CTA of the cluster runs and has initialised its barriers
-  if (!grid_proj) {
-    // ---- all-to-all inside the cluster: every rank gets every rank's partial
-    const int qstep = kApplyThreads / nf4;  // ranks served by the threads of one column group
-    if (tid < qstep * nf4) {
-      const int f4 = tid % nf4, q0 = tid / nf4;
-      float4 s = *reinterpret_cast<const float4*>(red + 4 * f4);
+  // ---- reduce-scatter inside the cluster: rank q gets every rank's columns
+  //      [q ks, (q + 1) ks) of the partial g, and every rank's ||x||^2
+  const int ks = a.ks;
+  if (tid < k) {
+    float s = red[tid];
 #pragma unroll
-      for (int w = 1; w < NW; ++w) {
-        const float4 t = *reinterpret_cast<const float4*>(red + w * a.red_stride + 4 * f4);
-        s.x += t.x;
-        s.y += t.y;
-        s.z += t.z;
-        s.w += t.w;
-      }
-      const uint32_t dst = sa(inbox + rank * k + 4 * f4), bar = sa(xbar);
-      for (int q = q0; q < CS; q += qstep) st_async_v4(map_rank(dst, q), s, map_rank(bar, q));
-    }
-    if (tid < CS) {
-      float s = red[k];
+    for (int w = 1; w < NW; ++w) s += red[w * a.red_stride + tid];
+    const int q = tid / ks;
+    st_async_f32(map_rank(sa(inbox + rank * ks + (tid - q * ks)), q), s, map_rank(sa(xbar), q));
+  }
+  if (tid < CS) {
+    float s = red[k];
 #pragma unroll
-      for (int w = 1; w < NW; ++w) s += red[w * a.red_stride + k];
-      st_async_f32(map_rank(sa(inx + rank), tid), s, map_rank(sa(xbar), tid));
-    }
-    __all_sync(FULL, bar_wait_cluster(xbar, 0, a.err));
-    if (tid < k) {
-      float s = 0.f;
+    for (int w = 1; w < NW; ++w) s += red[w * a.red_stride + k];
+    st_async_f32(map_rank(sa(inx + rank), tid), s, map_rank(sa(xbar), tid));
+  }
+  __all_sync(FULL, bar_wait_cluster(xbar, 0, a.err));
+  // ---- this rank's slice of g (rank 0: also ||x||^2), summed over the ranks
+  //      in rank order -- grid projection: then over the clusters, through
+  //      epoch-tagged words -- and pushed to every rank of the cluster
+  const bool xlane = tid == ks && rank == 0;
+  if (tid < c1 - c0 || xlane) {
+    float s = 0.f;
 #pragma unroll
-      for (int r = 0; r < CS; ++r) s += inbox[r * k + tid];
-      gfull[tid] = s;
-    }
-    if (tid == kApplyThreads - 1) {
-      float s = 0.f;
-#pragma unroll
-      for (int r = 0; r < CS; ++r) s += inx[r];
-      *nx2 = s;
-    }
-    __syncthreads();
-  } else {
-    // ---- grid projection: reduce-scatter inside the cluster (rank q gets
-    //      every rank's columns [q ks, (q + 1) ks)), one published slice per
-    //      rank, the grid barrier, then rank q adds the clusters' slices in
-    //      cluster order and pushes them to every rank of its cluster
-    const int ks = a.ks;
-    if (tid < k) {
-      float s = red[tid];
-#pragma unroll
-      for (int w = 1; w < NW; ++w) s += red[w * a.red_stride + tid];
-      const int q = tid / ks;
-      st_async_f32(map_rank(sa(inbox + rank * ks + (tid - q * ks)), q), s, map_rank(sa(xbar), q));
-    }
-    if (tid < CS) {
-      float s = red[k];
-#pragma unroll
-      for (int w = 1; w < NW; ++w) s += red[w * a.red_stride + k];
-      st_async_f32(map_rank(sa(inx + rank), tid), s, map_rank(sa(xbar), tid));
-    }
-    __all_sync(FULL, bar_wait_cluster(xbar, 0, a.err));
-    const int cl = int(blockIdx.x) / CS, ncl = int(gridDim.x) / CS;
-    const uint32_t epoch = *sepoch;
-    unsigned long long* pw = reinterpret_cast<unsigned long long*>(a.part_g);  // [ncl][k] tagged
-    unsigned long long* px = reinterpret_cast<unsigned long long*>(a.part_x);  // [ncl] tagged
-    const bool xlane = tid == ks && rank == 0;
-    if (tid < ks) {
-      float s = 0.f;
-#pragma unroll
-      for (int r = 0; r < CS; ++r) s += inbox[r * ks + tid];
-      st_relaxed_u64(pw + int64_t(cl) * k + c0 + tid, (uint64_t(epoch) << 32) | __float_as_uint(s));
-    }
-    if (xlane) {
-      float s = 0.f;
-#pragma unroll
-      for (int r = 0; r < CS; ++r) s += inx[r];
-      st_relaxed_u64(px + cl, (uint64_t(epoch) << 32) | __float_as_uint(s));
-    }
-    if (tid < ks || xlane) {
-      // every cluster's word of this column (or of ||x||^2), polled until
-      // it carries this call's epoch (bounded), added in cluster order
-      const unsigned long long* src = tid < ks ? pw + c0 + tid : px;
-      const int64_t stride = tid < ks ? k : 1;
+    for (int r = 0; r < CS; ++r) s += xlane ? inx[r] : inbox[r * ks + tid];
+    if (grid_proj) {
+      const int cl = int(blockIdx.x) / CS, ncl = int(gridDim.x) / CS;
+      const uint32_t epoch = *sepoch;
+      unsigned long long* src = xlane ? reinterpret_cast<unsigned long long*>(a.part_x)
+                                      : reinterpret_cast<unsigned long long*>(a.part_g) + c0 + tid;
+      const int64_t stride = xlane ? 1 : k;  // [ncl][k] slices, [ncl] norms
+      st_relaxed_u64(src + cl * stride, (uint64_t(epoch) << 32) | __float_as_uint(s));
+      // every cluster's word, polled until it carries this call's epoch
+      // (bounded), added in cluster order
       float v[kDecodeMaxClusters];
       uint32_t pending = (1u << ncl) - 1u;
       const long long t0 = clock64();
@@ -303,15 +262,15 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
           break;
         }
       }
-      float s = 0.f;
+      s = 0.f;
 #pragma unroll
       for (int c = 0; c < kDecodeMaxClusters; ++c)
         if (c < ncl) s += ((pending >> c) & 1u) ? 0.f : v[c];
-      const uint32_t dst = sa(tid < ks ? gfull + c0 + tid : nx2), bar = sa(gxbar);
-      for (int q = 0; q < CS; ++q) st_async_f32(map_rank(dst, q), s, map_rank(bar, q));
     }
-    __all_sync(FULL, bar_wait_cluster(gxbar, 0, a.err));
+    const uint32_t dst = sa(xlane ? nx2 : gfull + c0 + tid), bar = sa(gxbar);
+    for (int q = 0; q < CS; ++q) st_async_f32(map_rank(dst, q), s, map_rank(bar, q));
   }
+  __all_sync(FULL, bar_wait_cluster(gxbar, 0, a.err));
 
   // ---- every warp: its share of the Gram form (Gram rows c0 + warp,
   //      c0 + warp + NW, ...) and of ||g||^2, pushed to every rank, then

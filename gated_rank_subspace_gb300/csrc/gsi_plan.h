@@ -289,7 +289,7 @@ inline DecodePlan plan_decode(int64_t d, int64_t d_out, int64_t k, int es, int n
   };
   p.off_g = take(size_t(k + kDecodeCluster + 2 * kDecodeCluster * nw + 4 + nw * 32) * 4);
   p.off_y = take(size_t(p.rpc) * 4);
-  const size_t inbox = size_t(kDecodeCluster) * k * 4;
+  const size_t inbox = size_t(kDecodeCluster) * p.ks * 4;  // partial-g slices of every rank
   p.off_in = take(inbox > size_t(row_b) ? inbox : size_t(row_b));
   p.off_gram = take(size_t(p.ks) * k * 4);
   const size_t v_bytes = size_t(nw) * p.rw * mrow_b;
