@@ -223,21 +223,28 @@ def run_reference(args):
 
 
 # ---------------------------------------------------------------------------- GPU
-# DRAM bytes per launch of the step's kernel (decide_apply_kernel, one launch
-# per gated-map call) averaged over the step's 1024 launches, from one ncu
-# capture of `bench.py --kernel-traffic` (dram__bytes_read.sum +
-# dram__bytes_write.sum, decide_apply launches 1-1024, with --cache-control
-# none so that the L2 prefetch of the next map serves the next launch as in
-# the live step): valid only for the
-# kernel source it was taken on (first 16 hex digits of the SHA-256 of
-# csrc/gsi_apply.cu); otherwise the roofline reports traffic null.
-KERNEL_TRAFFIC = {"gsi_apply_sha256": "8e113407b18ce6dd", "bytes_per_launch": 19459247.5}
+# DRAM bytes per launch of the step's kernel (decode_kernel, one launch per
+# gated-map call), from one ncu capture of `bench.py --kernel-traffic`
+# (dram__bytes_read.sum + dram__bytes_write.sum over decode_kernel launches
+# 1-1024, i.e. exactly the step's calls, with --cache-control none so that
+# the L2 prefetch of the next map serves the next launch as in the live
+# step): valid only for the kernel source it was taken on (first 16 hex
+# digits of the SHA-256 of csrc/gsi_decode.cu followed by csrc/gsi_plan.h);
+# otherwise the roofline reports traffic null.
+KERNEL_TRAFFIC = {"src_sha256": "fca1d9d14c715ea4", "bytes_per_launch": 19428662.0}
+TRAFFIC_SOURCES = ("gsi_decode.cu", "gsi_plan.h")
+
+
+def kernel_source_hash():
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "gated_rank_subspace_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in TRAFFIC_SOURCES:
+        h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
 
 
 def kernel_traffic():
-    src = os.path.join(os.path.dirname(os.path.abspath(__file__)), "gated_rank_subspace_gb300", "csrc", "gsi_apply.cu")
-    h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    return KERNEL_TRAFFIC["bytes_per_launch"] if h == KERNEL_TRAFFIC["gsi_apply_sha256"] else None
+    return KERNEL_TRAFFIC["bytes_per_launch"] if kernel_source_hash() == KERNEL_TRAFFIC["src_sha256"] else None
 
 
 SWEEP_EPS = [0.0, 0.0125, 0.025, 0.05, 0.1, 0.2, 0.4, float("inf")]
@@ -389,6 +396,61 @@ def run_cascade(n_layers=4, d=4096, m=512, k=256, T=2048, target=0.999, ref_step
     print(json.dumps(report))
 
 
+def run_per_call(R=4, n=32, reps_n=10):
+    """Latency of one gated-map call per 6B map: a CUDA graph of n
+    single-token calls (weights rotating over R device replicas, so W of a
+    slow call comes from HBM), timed with CUDA events over reps_n replays,
+    once with every token slow (eps = 0) and once with every token fast
+    (eps = inf).  One JSON line per map."""
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import gated_rank_subspace_gb300 as gsi
+
+    dev = torch.device("cuda", 0)
+    for role in synth.ROLES:
+        m_in = synth.map_6b(role, T=n, n_slow=0, k=K_RANK)
+        base = gsi.make_map(m_in.W.to(dev), m_in.V.to(dev))
+        reps = [base] + [gsi.Map(base.W.clone(), base.V.clone(), base.M.clone(), base.gram.clone())
+                         for _ in range(R - 1)]
+        X = m_in.X.to(dev)
+        Y = torch.zeros(n, base.d_out, device=dev)
+        F = torch.zeros(n, dtype=torch.uint8, device=dev)
+        ws = gsi.new_workspace(gsi.stack_workspace_size([base], 1), dev)
+        stream = torch.cuda.Stream(dev)
+        args = [gsi.stack_args([reps[t % R]], [X[t:t + 1]], [Y[t:t + 1]], [F[t:t + 1]]) for t in range(n)]
+        torch.cuda.synchronize()
+        out = {"per_call": role, "calls": n, "replicas": R}
+        for key, eps in (("slow", 0.0), ("fast", float("inf"))):
+            def run():
+                for a in args:
+                    gsi.stack_raw(a, 1, 1, eps, ws, stream=stream)
+
+            with torch.cuda.stream(stream):
+                run()
+            stream.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                run()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(stream):
+                for _ in range(3):
+                    g.replay()
+                e0.record(stream)
+                for _ in range(reps_n):
+                    g.replay()
+                e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / (reps_n * n)
+            out[key + "_us"] = round(us, 2)
+            mb = map_bytes(m_in)
+            moved = mb["V"] + mb["gram"] + (mb["W"] if key == "slow" else mb["M"]) + mb["x"] + mb["y"]
+            out[key + "_gbs"] = round(moved / (us * 1e-6) / 1e9, 1)
+        assert int(F.sum()) == 0 and gsi.workspace_status(ws, stream=stream) == 0
+        print(json.dumps(out))
+
+
 def probe_map(role, eps):
     """Eight one-token gsi_linear calls of one 6B map (default stream)."""
     import __graft_entry__
@@ -427,11 +489,16 @@ def main():
                     help="threshold of the --probe-map calls (0: every token slow)")
     ap.add_argument("--eps-sweep", action="store_true",
                     help="only report the threshold sweep on configs 2-4 (one JSON line)")
+    ap.add_argument("--per-call", action="store_true",
+                    help="only report one call's latency per 6B map, all tokens slow and all fast (JSON lines)")
     ap.add_argument("--cascade", action="store_true",
                     help="only report basis construction on depth-coherent calibration blocks (one JSON line)")
     args = ap.parse_args()
     if args.cascade:
         run_cascade()
+        return
+    if args.per_call:
+        run_per_call()
         return
     if args.eps_sweep:
         run_sweep()
@@ -601,14 +668,14 @@ def main():
     k_fast = ab["fast"] / (t_fast * 1e-3) / 1e9 if t_fast else None
     k_slow = ab["slow"] / (t_slow * 1e-3) / 1e9 if t_slow else None
     k_apply = (ab["fast"] + ab["slow"]) / (t_apply * 1e-3) / 1e9
-    # The dominant kernel is decide_apply_kernel.  On the single-launch decode
-    # it is the step's only kernel: each launch moves one call's algorithmic
-    # bytes, and its mean launch interval over the timed replays (launch gaps
-    # included, so the achieved figure is a lower bound) is ms / 1024.  On the
-    # two-launch path its stored-decision launches (gsi_apply) are timed in a
-    # graph of their own.
+    # The dominant kernel is decode_kernel, the step's only kernel: each
+    # launch moves one call's algorithmic bytes, and its mean launch interval
+    # over the timed replays (launch gaps included, so the achieved figure is
+    # a lower bound) is ms / 1024.  On the two-launch path the dominant kernel
+    # is decide_apply_kernel, whose stored-decision launches (gsi_apply) are
+    # timed in a graph of their own.
     if sum(per_call) == 4:
-        dom = dict(name="decide_apply_kernel (single-launch decode: projection, gate, M g / W x)",
+        dom = dict(name="decode_kernel (single-token decode: projection, gate, M g / W x in one launch)",
                    gbs=step_gbs, bytes_per_launch=ab["total"] / n_launch, ms=ms / n_launch,
                    timing="CUDA events over the timed region (graph replays of the step); "
                           "per-launch time = mean launch interval, gaps included")
@@ -678,7 +745,8 @@ def main():
                   "of fast-path weights, 129 MB L2)",
             "parallelism": "replicas only" if world > 1 else "single GPU",
             "graph": "whole step captured in one CUDA graph, programmatic dependent launch between kernels",
-            "path": "single-launch decode (grid-projected gate, decide and apply in one kernel per call)"
+            "path": "single-token decode kernel, one launch per call (cluster projection for qkv, out and "
+                    "up, grid projection for down)"
                     if sum(per_call) == 4 else "two-launch streaming kernels",
         },
         "achieved_step_gbs": step_gbs,

@@ -343,20 +343,20 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
     };
     if (nrows <= NW * 4)
       apply_rows(IntC<4>{});
-    else
+    else if (nrows <= NW * 8)
       apply_rows(IntC<8>{});
+    else
+      apply_rows(IntC<16>{});
   }
   // ---- the decision, taken by every warp from the same shares in the same
-  //      order (rank r's shares by lane r in warp order, then a butterfly)
+  //      order (lane l adds shares 4l .. 4l + 3 of the rank-major list, then
+  //      a butterfly over the lanes)
   __all_sync(FULL, bar_wait_cluster(qbar, 0, a.err));
-  float Qr = 0.f, Nr = 0.f;
-  if (lane < CS) {
-#pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      Qr += qin[lane * NW + w];
-      Nr += nin[lane * NW + w];
-    }
-  }
+  static_assert(CS * NW == 4 * 32, "four shares per lane");
+  const float4 q4 = reinterpret_cast<const float4*>(qin)[lane];
+  const float4 n4 = reinterpret_cast<const float4*>(nin)[lane];
+  const float Qr = (q4.x + q4.y) + (q4.z + q4.w);
+  const float Nr = (n4.x + n4.y) + (n4.z + n4.w);
   float Q = warp_sum(Qr);
   const float N = warp_sum(Nr);
   if (!a.gram) Q = N;  // orthonormal basis: ||V g||^2 = ||g||^2
@@ -374,7 +374,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
   if (!slow) {
     // this warp's rows of y (the row groups it computed), from its own lanes
     __syncwarp();
-    const int rbw = nrows <= NW * 4 ? 4 : 8;
+    const int rbw = nrows <= NW * 4 ? 4 : nrows <= NW * 8 ? 8 : 16;
     for (int rb = warp * rbw; rb < nrows; rb += NW * rbw)
       if (lane < rbw && rb + lane < nrows) a.Y[r0 + rb + lane] = ybuf[rb + lane];
     return;
