@@ -266,12 +266,13 @@ def test_config5_prefill_tensor_path(gsi):
     assert torch.equal(Y, Y2) and torch.equal(flags, f2)
 
 
-# ------------------------------------------------------------------ fused single-launch decode
+# ------------------------------------------------------------------ single-launch decode (one or two tokens)
 @pytest.mark.parametrize("role", ["qkv", "out", "up", "down"])
 @pytest.mark.parametrize("T", [1, 2])
 def test_fused_decode_against_oracle(gsi, role, T):
-    """The single-launch decode (every CTA projects x on its own slab of V;
-    the partials meet at a grid barrier)."""
+    """The single-launch decode: one token per call runs the single-token
+    decode kernel (cluster projection for qkv, out and up; grid projection for
+    the 16384-wide down map), two tokens the fused decide-and-apply kernel."""
     m_in = synth.map_6b(role, T=24, n_slow=6)
     gm, X = upload(m_in)
     n = X.shape[0]
@@ -361,7 +362,10 @@ def test_decode_calls_zero_and_nonfinite_tokens(gsi, T_call):
     compare(m_in, gm.M, Y, F, R, X=X)
 
 
-@pytest.mark.parametrize("shape", [(520, 333, 24), (1032, 2056, 40), (16, 8, 8)])
+# (8200, 520, 64): the single-token kernel's grid projection (the basis is too
+# wide for one cluster) with a last CTA that holds no V rows and 5 output rows
+# per CTA; (16, 8, 8): one V row per rank, partial sums in their own slots
+@pytest.mark.parametrize("shape", [(520, 333, 24), (1032, 2056, 40), (16, 8, 8), (8200, 520, 64)])
 def test_decode_calls_ragged_shapes(gsi, shape):
     d, d_out, k = shape
     V64 = synth.orthonormal_basis(synth.rng(8, d, k, 3), d, k)
