@@ -71,16 +71,21 @@ typedef enum gsi_status {
 typedef enum gsi_dtype { GSI_F32 = 0, GSI_BF16 = 1 } gsi_dtype;
 
 /* Which kernels run the map.
- *   FUSED  -- one launch per call for T <= 2: every CTA projects the tokens
- *             on its own slab of V, the partials meet at a grid barrier on
- *             the workspace, then clusters decide and apply;
+ *   FUSED  -- one launch per call for T <= 2.  One token: the single-token
+ *             decode kernel, in which each 16-CTA cluster holds all of V in
+ *             shared memory (or, for wider bases, the clusters exchange
+ *             slices of g through epoch-tagged words in the workspace) and
+ *             every CTA decides and applies; two tokens: every cluster
+ *             projects on its share of V, with a grid barrier on the
+ *             workspace where V does not fit a cluster;
  *   STREAM -- two launches (projection kernel, then decide-and-apply), any T;
  *   TENSOR -- tcgen05 contractions, bf16 only, for prefill-sized T.
  * AUTO picks FUSED for T <= 2 where a slab of V fits shared memory (and
  * STREAM at run time on a device that cannot hold the fused grid), TENSOR
  * for bf16 with T >= 128, STREAM otherwise.  The fused grid must be
- * co-resident: its barrier gives up after ~2 s (GSI_ERR_TIMEOUT, and the
- * workspace must then be re-initialised) if other work keeps SMs busy. */
+ * co-resident: its waits on other CTAs give up after ~2 s (GSI_ERR_TIMEOUT,
+ * and the workspace must then be re-initialised) if other work keeps SMs
+ * busy. */
 typedef enum gsi_path {
   GSI_PATH_AUTO = 0,
   GSI_PATH_STREAM = 1,
