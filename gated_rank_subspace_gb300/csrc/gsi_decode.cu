@@ -57,7 +57,9 @@
 
 namespace gsi {
 
-template <class E>
+// NV: 16-byte vectors of a V / M row per lane (1: a row of at most 512 bytes,
+// 2: up to 1 KB, e.g. k = 320 or 512 in bf16).
+template <class E, int NV>
 __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) {
   constexpr int PV = E::kPerVec;
   constexpr int CS = kDecodeCluster;
@@ -72,7 +74,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
   const int k = a.k;
   const int64_t d = a.d, d_out = a.d_out;
   const int mrow_b = k * E::kBytes;  // bytes of a V / M row
-  const int nvec = mrow_b / 16;      // 16-byte vectors of such a row (<= 32)
+  const int nvec = mrow_b / 16;      // 16-byte vectors of such a row (<= 32 NV)
   const int nf4 = k >> 2;            // float4 groups of g
   const int64_t row_b = d * E::kBytes;
 
@@ -163,40 +165,62 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
   xme[lane] = xv;
   __syncwarp();
   const float xsq = warp_sum(xv * xv);
-  float acc[PV];
+  // lane l owns column groups l and (NV = 2) l + 32 of g
+  bool on[NV];
+  int vl[NV];  // the lane's vectors, clamped to vector 0 where a row has fewer
 #pragma unroll
-  for (int e = 0; e < PV; ++e) acc[e] = 0.f;
+  for (int v = 0; v < NV; ++v) {
+    on[v] = lane + 32 * v < nvec;
+    vl[v] = on[v] ? lane + 32 * v : 0;
+  }
+  float acc[NV][PV];
+#pragma unroll
+  for (int v = 0; v < NV; ++v)
+#pragma unroll
+    for (int e = 0; e < PV; ++e) acc[v][e] = 0.f;
   if (wrn > 0) {
     __all_sync(FULL, bar_wait(&vbar[warp], 0, a.err));
-    // rows in batches of 8: the vectors and token elements are loaded first,
-    // then multiplied in row order
-    const unsigned char* vrow = Vs + int64_t(wr0) * mrow_b + lane * 16;
-    const bool on = lane < nvec;
+    // rows in batches of 8 / NV: the vectors and token elements are loaded
+    // first, then multiplied in row order
+    constexpr int RBT = 8 / NV;
+    const unsigned char* vrows = Vs + int64_t(wr0) * mrow_b;
     int i = 0;
-    for (; i + 8 <= wrn; i += 8) {
-      uint4 u[8];
-      float xi[8];
+    for (; i + RBT <= wrn; i += RBT) {
+      uint4 u[RBT][NV];
+      float xi[RBT];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        u[j] = on ? *reinterpret_cast<const uint4*>(vrow + int64_t(i + j) * mrow_b) : make_uint4(0u, 0u, 0u, 0u);
+      for (int j = 0; j < RBT; ++j) {
+#pragma unroll
+        for (int v = 0; v < NV; ++v)
+          u[j][v] = on[v] ? *reinterpret_cast<const uint4*>(vrows + int64_t(i + j) * mrow_b + vl[v] * 16)
+                          : make_uint4(0u, 0u, 0u, 0u);
         xi[j] = xme[i + j];
       }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) E::axpy(u[j], xi[j], acc);
+      for (int j = 0; j < RBT; ++j)
+#pragma unroll
+        for (int v = 0; v < NV; ++v) E::axpy(u[j][v], xi[j], acc[v]);
     }
     for (; i < wrn; ++i) {
-      const uint4 u = on ? *reinterpret_cast<const uint4*>(vrow + int64_t(i) * mrow_b) : make_uint4(0u, 0u, 0u, 0u);
-      E::axpy(u, xme[i], acc);
+#pragma unroll
+      for (int v = 0; v < NV; ++v) {
+        const uint4 u = on[v] ? *reinterpret_cast<const uint4*>(vrows + int64_t(i) * mrow_b + vl[v] * 16)
+                              : make_uint4(0u, 0u, 0u, 0u);
+        E::axpy(u, xme[i], acc[v]);
+      }
     }
   }
   __syncwarp();
   {
     float* mine = red + warp * a.red_stride;  // this warp's own (consumed) V rows, or a separate slot
-    if (lane < nvec) {
 #pragma unroll
-      for (int e = 0; e < PV; e += 4)
-        *reinterpret_cast<float4*>(mine + lane * PV + e) = make_float4(acc[e], acc[e + 1], acc[e + 2], acc[e + 3]);
-    }
+    for (int v = 0; v < NV; ++v)
+      if (on[v]) {
+#pragma unroll
+        for (int e = 0; e < PV; e += 4)
+          *reinterpret_cast<float4*>(mine + vl[v] * PV + e) =
+              make_float4(acc[v][e], acc[v][e + 1], acc[v][e + 2], acc[v][e + 3]);
+      }
     if (lane == 0) mine[k] = xsq;
   }
   __syncthreads();
@@ -212,12 +236,12 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
   // ---- reduce-scatter inside the cluster: rank q gets every rank's columns
   //      [q ks, (q + 1) ks) of the partial g, and every rank's ||x||^2
   const int ks = a.ks;
-  if (tid < k) {
-    float s = red[tid];
+  for (int c = tid; c < k; c += kApplyThreads) {
+    float s = red[c];
 #pragma unroll
-    for (int w = 1; w < NW; ++w) s += red[w * a.red_stride + tid];
-    const int q = tid / ks;
-    st_async_f32(map_rank(sa(inbox + rank * ks + (tid - q * ks)), q), s, map_rank(sa(xbar), q));
+    for (int w = 1; w < NW; ++w) s += red[w * a.red_stride + c];
+    const int q = c / ks;
+    st_async_f32(map_rank(sa(inbox + rank * ks + (c - q * ks)), q), s, map_rank(sa(xbar), q));
   }
   if (tid < CS) {
     float s = red[k];
@@ -279,24 +303,33 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
     float q = 0.f, n = 0.f;
     if (have_gram) {
       __all_sync(FULL, bar_wait(gbar, 0, a.err));
-      // lane l takes column groups l and l + 32 (clamped loads, masked)
+      // lane l takes column groups l, l + 32, ... (clamped loads, masked)
+      constexpr int NG = 2 * NV;  // float4 groups of a Gram row per lane (k <= 256 NV)
       const float4* g4 = reinterpret_cast<const float4*>(gfull);
-      const bool oa = lane < nf4, ob = lane + 32 < nf4;
-      const int ja = oa ? lane : 0, jb = ob ? lane + 32 : 0;
-      const float4 ga = g4[ja], gb = g4[jb];
+      bool og[NG];
+      int jg[NG];
+      float4 gq[NG];
+#pragma unroll
+      for (int u = 0; u < NG; ++u) {
+        og[u] = lane + 32 * u < nf4;
+        jg[u] = og[u] ? lane + 32 * u : 0;
+        gq[u] = g4[jg[u]];
+      }
       for (int i = c0 + warp; i < c1; i += NW) {
         const float4* grow = reinterpret_cast<const float4*>(gram_s) + (i - c0) * nf4;
-        const float4 va = grow[ja], vb = grow[jb];
+        float4 vg[NG];
+#pragma unroll
+        for (int u = 0; u < NG; ++u) vg[u] = grow[jg[u]];
         const float gi = gfull[i];
-        float ha = va.x * ga.x;
-        ha = fmaf(va.y, ga.y, ha);
-        ha = fmaf(va.z, ga.z, ha);
-        ha = fmaf(va.w, ga.w, ha);
-        float hb = vb.x * gb.x;
-        hb = fmaf(vb.y, gb.y, hb);
-        hb = fmaf(vb.z, gb.z, hb);
-        hb = fmaf(vb.w, gb.w, hb);
-        const float h = (oa ? ha : 0.f) + (ob ? hb : 0.f);
+        float h = 0.f;
+#pragma unroll
+        for (int u = 0; u < NG; ++u) {
+          float hu = vg[u].x * gq[u].x;
+          hu = fmaf(vg[u].y, gq[u].y, hu);
+          hu = fmaf(vg[u].z, gq[u].z, hu);
+          hu = fmaf(vg[u].w, gq[u].w, hu);
+          h += og[u] ? hu : 0.f;
+        }
         q = fmaf(gi, h, q);
       }
     }
@@ -314,27 +347,33 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
     // are unconditional (rows past the CTA's last repeat it, lanes past the
     // row's vectors repeat vector 0) and masked afterwards, so all RB are in
     // flight together
-    const bool on = lane < nvec;
-    const int vl = on ? lane : 0;
-    float gv[PV];
+    float gv[NV][PV];
 #pragma unroll
-    for (int e = 0; e < PV; ++e) gv[e] = gfull[vl * PV + e];
+    for (int v = 0; v < NV; ++v)
+#pragma unroll
+      for (int e = 0; e < PV; ++e) gv[v][e] = gfull[vl[v] * PV + e];
     auto apply_rows = [&](auto rb_c) {
       constexpr int RB = decltype(rb_c)::value;
       for (int rb = warp * RB; rb < nrows; rb += NW * RB) {
-        uint4 u[RB];
+        uint4 u[RB][NV];
 #pragma unroll
         for (int r = 0; r < RB; ++r)
-          u[r] = *reinterpret_cast<const uint4*>(Ms + int64_t(min(rb + r, nrows - 1)) * mrow_b + vl * 16);
+#pragma unroll
+          for (int v = 0; v < NV; ++v)
+            u[r][v] = *reinterpret_cast<const uint4*>(Ms + int64_t(min(rb + r, nrows - 1)) * mrow_b + vl[v] * 16);
         float part[RB];
 #pragma unroll
         for (int r = 0; r < RB; ++r) {
-          float w[PV];
-          E::unpack(u[r], w);
-          float p = 0.f;
+          part[r] = 0.f;
 #pragma unroll
-          for (int e = 0; e < PV; ++e) p = fmaf(w[e], gv[e], p);
-          part[r] = on ? p : 0.f;
+          for (int v = 0; v < NV; ++v) {
+            float w[PV];
+            E::unpack(u[r][v], w);
+            float p = 0.f;
+#pragma unroll
+            for (int e = 0; e < PV; ++e) p = fmaf(w[e], gv[v][e], p);
+            part[r] += on[v] ? p : 0.f;
+          }
         }
         const float sum = warp_reduce_multi<RB>(part, lane);
         const int r = row_of_lane<RB>(lane);
@@ -343,10 +382,10 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
     };
     if (nrows <= NW * 4)
       apply_rows(IntC<4>{});
-    else if (nrows <= NW * 8)
+    else if (nrows <= NW * 8 || NV > 1)  // (16 rows of two vectors: too many registers)
       apply_rows(IntC<8>{});
     else
-      apply_rows(IntC<16>{});
+      apply_rows(IntC<16 / NV>{});
   }
   // ---- the decision, taken by every warp from the same shares in the same
   //      order (lane l adds shares 4l .. 4l + 3 of the rank-major list, then
@@ -374,7 +413,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
   if (!slow) {
     // this warp's rows of y (the row groups it computed), from its own lanes
     __syncwarp();
-    const int rbw = nrows <= NW * 4 ? 4 : nrows <= NW * 8 ? 8 : 16;
+    const int rbw = nrows <= NW * 4 ? 4 : (nrows <= NW * 8 || NV > 1) ? 8 : 16;
     for (int rb = warp * rbw; rb < nrows; rb += NW * rbw)
       if (lane < rbw && rb + lane < nrows) a.Y[r0 + rb + lane] = ybuf[rb + lane];
     return;
@@ -473,9 +512,9 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
     }
 }
 
-template <class E>
+template <class E, int NV>
 static cudaError_t launch_decode_t(const DecodeArgs& a, const DecodePlan& p, cudaStream_t s) {
-  auto kern = decode_kernel<E>;
+  auto kern = decode_kernel<E, NV>;
   static size_t smem_set = 0;
   if (p.smem > smem_set) {
     cudaError_t e = set_kernel_smem(kern, p.smem);
@@ -501,12 +540,14 @@ static cudaError_t launch_decode_t(const DecodeArgs& a, const DecodePlan& p, cud
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, gsi_dtype dt, cudaStream_t s) {
-  return dt == GSI_BF16 ? launch_decode_t<BF16>(a, p, s) : launch_decode_t<F32>(a, p, s);
+  const bool two = a.k * (dt == GSI_BF16 ? 2 : 4) > 512;  // two 16-byte vectors of a row per lane
+  if (dt == GSI_BF16) return two ? launch_decode_t<BF16, 2>(a, p, s) : launch_decode_t<BF16, 1>(a, p, s);
+  return two ? launch_decode_t<F32, 2>(a, p, s) : launch_decode_t<F32, 1>(a, p, s);
 }
 
 template <class E>
 static int decode_max_clusters_t(size_t smem) {
-  auto kern = decode_kernel<E>;
+  auto kern = decode_kernel<E, 1>;
   if (set_kernel_smem(kern, smem) != cudaSuccess ||
       cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
     cudaGetLastError();

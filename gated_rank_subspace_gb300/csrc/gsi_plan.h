@@ -269,7 +269,7 @@ inline DecodePlan plan_decode(int64_t d, int64_t d_out, int64_t k, int es, int n
   const int64_t mrow_b = k * es, row_b = d * es;
   const int nw = kApplyThreads / 32;
   if (ncta < kDecodeCluster || ncta % kDecodeCluster || k % 4 || mrow_b % 16 || row_b % 16) return p;
-  if (mrow_b / 16 > 32) return p;             // one 16-byte vector of a V / M row per lane
+  if (mrow_b / 16 > 64) return p;             // at most two 16-byte vectors of a V / M row per lane
   if (grid && k % kDecodeCluster) return p;  // equal column slices for the reduce-scatter
   if (grid && ncta > kDecodeCluster * kDecodeMaxClusters) return p;
   p.ncta = ncta;
