@@ -134,4 +134,8 @@ def test_plan_invariants(plans):
         assert p["off_v"] + nw * p["sw"] * p["seg_bytes"] <= p["smem"], ctx
         # the mbarriers initialised by the kernel (one per thread) fit the bars region
         assert nw + p["bars"] + nw * p["sw"] <= 256, ctx
+        # grid projection: the clusters' epoch-tagged words fit the workspace's
+        # partial areas ([clusters][k] and [clusters] 64-bit words)
+        if p["grid"]:
+            assert p["ws_part_g"] >= (ncta // cs) * k * 8 and p["ws_part_x"] >= (ncta // cs) * 8, ctx
     assert n_ok > 100
