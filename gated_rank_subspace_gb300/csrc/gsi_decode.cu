@@ -21,10 +21,11 @@
 //              wait on the previous kernel of the stream.
 //   project    lane l of warp w loads token element v0 + w*rw + l and
 //              leaves it in the warp's slot of shared memory; the warp walks
-//              its V rows in batches of eight (vectors and elements loaded
-//              first) and keeps one 16-byte column group of g per lane;
-//              ||x||^2 is a warp sum.  Each warp leaves its partial in the
-//              space of its own, consumed, V rows.
+//              its V rows in batches of eight (four when a lane holds two
+//              vectors; vectors and elements loaded first) and keeps one
+//              16-byte column group of g per lane (two for rows longer than
+//              512 bytes); ||x||^2 is a warp sum.  Each warp leaves its
+//              partial in the space of its own, consumed, V rows.
 //   exchange   thread c adds the eight warps' partials of column c and
 //              pushes the sum to the rank that owns the column (a
 //              reduce-scatter by st.async, completion on the receiver's
@@ -34,7 +35,7 @@
 //   decide     warp w takes Gram rows c0 + w, c0 + w + 8, ... of the rank's
 //              slice: its share of g^T (V_k^T V_k) g and of ||g||^2 goes to
 //              every rank at once, and the warp goes on to y = M g for its
-//              own groups of four output rows.  Every warp then adds all
+//              own groups of 4, 8 or 16 output rows.  Every warp then adds all
 //              ranks' shares in one fixed order, so all warps of all CTAs
 //              reach the same rho = sqrt(||x||^2 - 2||g||^2 + g^T G g) / ||x||
 //              and flag with no block-wide barrier.
