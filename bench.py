@@ -118,7 +118,7 @@ def map_bytes(m):
 
 
 def algorithmic_bytes(maps_in, flags_np):
-    """Bytes the method must move for the whole step (SURVEY-style model):
+    """Bytes the method must move for the whole step (the algorithmic model):
     per call |V| + |Gram| + x + y + flag, plus |M| if fast or |W| if slow."""
     total = fast_apply = slow_apply = gate = 0
     n_fast = n_slow = 0

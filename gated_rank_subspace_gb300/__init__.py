@@ -86,6 +86,14 @@ def lib() -> ctypes.CDLL:
     L.gsi_last_error.restype = ctypes.c_char_p
     L.gsi_debug_fail_after.argtypes = [ctypes.c_int]
     L.gsi_debug_fail_after.restype = None
+    L.gsi_debug_withhold_slice.argtypes = [ctypes.c_int]
+    L.gsi_debug_withhold_slice.restype = None
+    L.gsi_linear_noalloc.argtypes = [P(MapDesc), vp, i64, f32, vp, vp, vp, vp]
+    L.gsi_linear_noalloc.restype = ctypes.c_int
+    L.gsi_linear_noalloc_max_bytes.argtypes = []
+    L.gsi_linear_noalloc_max_bytes.restype = sz
+    L.gsi_linear_noalloc_status.argtypes = [P(ctypes.c_uint32), vp]
+    L.gsi_linear_noalloc_status.restype = ctypes.c_int
     _lib = L
     return L
 

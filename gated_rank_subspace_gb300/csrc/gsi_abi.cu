@@ -17,6 +17,7 @@ namespace gsi {
 
 static thread_local std::string g_err;
 static std::atomic<int> g_fail_after{0};
+static std::atomic<int> g_withhold{0};  // test hook: grid-projection launches left to withhold a slice
 
 static gsi_status fail(gsi_status s, const char* fmt, ...) {
   char buf[512];
@@ -284,6 +285,10 @@ static gsi_status run_decode(const gsi_map_desc* m, const void* X, float eps, fl
     a.next_gram_bytes = next->gram ? uint64_t(next->k) * next->k * 4 : 0;
   }
   a.err = &ctrl->err;
+  if (p.grid && g_withhold.load() > 0 && g_withhold.fetch_sub(1) > 0) {
+    a.dbg_withhold = 1;
+    a.poll_cycles = 20000000;  // ~10 ms
+  }
   return cuda_check(launch_decode(a, p, m->dtype, st), "single-token decode kernel launch");
 }
 
@@ -487,6 +492,8 @@ extern "C" {
 const char* gsi_last_error(void) { return g_err.c_str(); }
 
 void gsi_debug_fail_after(int n) { g_fail_after.store(n > 0 ? n : 0); }
+
+void gsi_debug_withhold_slice(int n) { g_withhold.store(n > 0 ? n : 0); }
 
 gsi_status gsi_build_image(const void* W, const void* V, void* M, float* gram, int64_t d,
                            int64_t d_out, int64_t k, gsi_dtype dtype, void* stream) {

@@ -265,11 +265,12 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
       unsigned long long* src = xlane ? reinterpret_cast<unsigned long long*>(a.part_x)
                                       : reinterpret_cast<unsigned long long*>(a.part_g) + c0 + tid;
       const int64_t stride = xlane ? 1 : k;  // [ncl][k] slices, [ncl] norms
-      st_relaxed_u64(src + cl * stride, (uint64_t(epoch) << 32) | __float_as_uint(s));
+      if (!(a.dbg_withhold && cl == 0)) st_relaxed_u64(src + cl * stride, (uint64_t(epoch) << 32) | __float_as_uint(s));
       // every cluster's word, polled until it carries this call's epoch
       // (bounded), added in cluster order
       float v[kDecodeMaxClusters];
       uint32_t pending = (1u << ncl) - 1u;
+      const long long lim = a.poll_cycles > 0 ? a.poll_cycles : kSpinCycles;
       const long long t0 = clock64();
       while (pending) {
         unsigned long long w[kDecodeMaxClusters];  // all loads in flight, then the checks
@@ -282,7 +283,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
             v[c] = __uint_as_float(uint32_t(w[c]));
             pending &= ~(1u << c);
           }
-        if (pending && clock64() - t0 > kSpinCycles) {
+        if (pending && clock64() - t0 > lim) {
           atomicOr(a.err, kErrTimeout);
           break;
         }

@@ -104,6 +104,10 @@ struct DecodeArgs {
   const char* next_gram;
   uint64_t next_gram_bytes;
   uint32_t* err;        // device error word (bounded waits)
+  // test hook (grid projection): cluster 0 withholds its slice words, so the
+  // other ranks' polls give up after poll_cycles (0: the default ~2 s)
+  int dbg_withhold;
+  long long poll_cycles;
 };
 
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, gsi_dtype dt, cudaStream_t s);

@@ -60,6 +60,29 @@ gsi_status scratch_address(void** out) {
 
 extern "C" size_t gsi_linear_noalloc_max_bytes(void) { return kScratchBytes; }
 
+extern "C" gsi_status gsi_linear_noalloc_status(uint32_t* code, void* stream) {
+  if (!code) return gsi::record_error(GSI_ERR_INVALID_ARG, "gsi_linear_noalloc_status: code is NULL");
+  void* ws = nullptr;
+  gsi_status s = scratch_address(&ws);
+  if (s != GSI_OK) return s;
+  // the error word sits in the control block at the head of the scratch
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const uint32_t* err = &static_cast<const gsi::Ctrl*>(ws)->err;
+  cudaError_t e = cudaMemcpyAsync(code, err, sizeof(uint32_t), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) {
+    char msg[256];
+    snprintf(msg, sizeof msg, "gsi_linear_noalloc_status: reading the error word failed (%s)", cudaGetErrorString(e));
+    return gsi::record_error(GSI_ERR_CUDA, msg);
+  }
+  if (*code) {
+    char msg[128];
+    snprintf(msg, sizeof msg, "gsi_linear_noalloc: a bounded device wait gave up (error word %u)", *code);
+    return gsi::record_error(GSI_ERR_TIMEOUT, msg);
+  }
+  return gsi::record_error(GSI_OK, "");
+}
+
 extern "C" gsi_status gsi_linear_noalloc(const gsi_map_desc* map, const void* X, int64_t T, float eps,
                                          float* Y, uint8_t* flags, float* rho, void* stream) {
   size_t need = 0;

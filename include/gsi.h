@@ -261,12 +261,29 @@ gsi_status gsi_linear_noalloc(const gsi_map_desc* map, const void* X, int64_t T,
 /* Size in bytes of the built-in scratch array used by gsi_linear_noalloc. */
 size_t gsi_linear_noalloc_max_bytes(void);
 
+/* Error word of the built-in scratch (SYNCHRONISES `stream`): *code (a HOST
+ * pointer) = 0 when the last gsi_linear_noalloc call on the current device
+ * had no bounded device wait give up; otherwise *code is nonzero, the call's
+ * outputs may be wrong and GSI_ERR_TIMEOUT is returned.  Each
+ * gsi_linear_noalloc call clears the word when it starts, so query it before
+ * the next call.  Allocates nothing. */
+gsi_status gsi_linear_noalloc_status(uint32_t* code, void* stream);
+
 /* Message for the calling thread's last non-OK status ("" if none). */
 const char* gsi_last_error(void);
 
 /* Test hook: make the n-th next launch step report GSI_ERR_CUDA without
  * touching the GPU (n <= 0 disarms).  Host-side fault injection. */
 void gsi_debug_fail_after(int n);
+
+/* Test hook for the bounded waits (n <= 0 disarms): in the next n one-token
+ * calls that run the single-token decode kernel's grid projection (bases
+ * wider than a 16-CTA cluster holds), cluster 0 withholds its slice of g, so
+ * every rank's poll for it gives up after ~10 ms instead of ~2 s.  The call
+ * then completes with wrong outputs and the workspace error word set:
+ * gsi_workspace_status returns GSI_ERR_TIMEOUT, and the workspace must be
+ * re-initialised before its next use.  Nothing faults or hangs. */
+void gsi_debug_withhold_slice(int n);
 
 #ifdef __cplusplus
 }

@@ -436,10 +436,34 @@ def pin_coherence(o):
     assert o.coherence(I[:, :2], I[:, :2]) == 1.0 and o.coherence(I[:, :2], I[:, 2:]) == 0.0
 
 
+def pin_spectral_norm_large(o, seed=29):
+    """The power-iteration branch of ||W||_2 (maps above 4 M elements) against a
+    closed form: W block-diagonal with 2 x 2 blocks B, whose spectral norm is
+    max over blocks of sqrt((t + sqrt(t^2 - 4 det(B)^2)) / 2), t = ||B||_F^2.
+    One block is scaled so its norm leads the rest by 10% (power iteration on
+    W^T W then converges as 0.81 per step)."""
+    rs = np.random.default_rng(seed)
+    nb = 1025  # 2050 x 2050 = 4.2 M elements: the large-map branch
+    B = rs.standard_normal((nb, 2, 2))
+    t = np.sum(B * B, axis=(1, 2))
+    det = B[:, 0, 0] * B[:, 1, 1] - B[:, 0, 1] * B[:, 1, 0]
+    norms = np.sqrt((t + np.sqrt(t * t - 4.0 * det * det)) / 2.0)
+    top = int(rs.integers(nb))
+    rest = np.max(np.delete(norms, top))
+    B[top] *= 1.1 * rest / norms[top]
+    want = 1.1 * rest
+    W = np.zeros((2 * nb, 2 * nb))
+    for b in range(nb):
+        W[2 * b:2 * b + 2, 2 * b:2 * b + 2] = B[b]
+    assert W.size > 4_000_000
+    _close(o.spectral_norm(W), want, 1e-9 * want, "spectral norm, power-iteration branch")
+
+
 ALL_PINS = [
     pin_hand_examples, pin_decomposition_geometry, pin_axis_basis, pin_eps_zero,
     pin_in_span, pin_full_rank, pin_theorem4, pin_eps_inf, pin_scaling,
     pin_permutation, pin_degenerate_tokens, pin_compact, pin_gram, pin_brute,
     pin_stack, pin_path_errors_axis, pin_sweep_by_hand, pin_sweep_theorem4, pin_effective_params,
     pin_dgks_qr, pin_dgks_reorth, pin_calibration_basis, pin_subspace_iteration, pin_coherence,
+    pin_spectral_norm_large,
 ]

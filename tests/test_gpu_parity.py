@@ -12,7 +12,7 @@ import pytest
 import torch
 
 from oracle import gsi_oracle as orc
-from tests.gpu_util import RHO2_TOL, compare, upload
+from tests.gpu_util import RHO2_TOL, compare, per_token_rel, upload
 from workloads import synth
 
 pytestmark = pytest.mark.gpu
@@ -169,6 +169,7 @@ def test_eps_zero_is_dense(gsi):
     dense = orc.slow_path(synth.widen(m_in.W), synth.widen(m_in.X))
     y = Y.cpu().numpy()
     assert np.linalg.norm(y - dense) / np.linalg.norm(dense) <= 1e-5
+    per_token_rel(y, dense, 1e-5)
 
 
 def test_eps_inf_is_static_projection(gsi):
@@ -339,11 +340,13 @@ def test_decode_calls_eps_zero_and_inf(gsi, T_call):
     assert bool(F.all())
     dense = orc.slow_path(synth.widen(m_in.W), synth.widen(m_in.X))
     assert np.linalg.norm(Y.cpu().numpy() - dense) / np.linalg.norm(dense) <= 1e-5
+    per_token_rel(Y.cpu().numpy(), dense, 1e-5)
     Y, F, R = _per_call(gsi, gm, X, float("inf"), T_call)
     assert not bool(F.any())
     Mn = synth.widen(gm.M)
     static = orc.fast_path(Mn, orc.project(synth.widen(m_in.X), synth.widen(m_in.V)))
     assert np.linalg.norm(Y.cpu().numpy() - static) / np.linalg.norm(static) <= 2e-2
+    per_token_rel(Y.cpu().numpy(), static, 2e-2)
 
 
 @pytest.mark.parametrize("T_call", [1, 2])

@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 import torch
 
-from tests.gpu_util import compare
+from tests.gpu_util import compare, per_token_rel
 from workloads import synth
 
 pytestmark = pytest.mark.gpu
@@ -81,3 +81,4 @@ def test_config3_28_layer_stack(gsi):
             ref = orc.fast_path(Mn, G[fast])
             rel = np.linalg.norm(Y[fast] - ref) / np.linalg.norm(ref)
             assert rel <= 2e-2, (l, role, rel)
+            per_token_rel(Y[fast], ref, 2e-2, f"layer {l} {role}")

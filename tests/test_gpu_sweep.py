@@ -14,7 +14,7 @@ import pytest
 import torch
 
 from oracle import gsi_oracle as orc
-from tests.gpu_util import BAND, RHO2_TOL, TOL, upload
+from tests.gpu_util import BAND, RHO2_TOL, TOL, per_token_rel, upload
 from workloads import synth
 
 pytestmark = pytest.mark.gpu
@@ -52,6 +52,8 @@ def _check_map(gsi, m_in, tokens_per_call=1):
     finite = np.isfinite(ro)
     assert _rel(Yf.cpu().numpy()[finite], orc.fast_path(Mn, G)[finite]) <= tol
     assert _rel(Ys.cpu().numpy(), orc.slow_path(Wn, Xn)) <= tol
+    per_token_rel(Yf.cpu().numpy()[finite], orc.fast_path(Mn, G)[finite], tol, "Y_fast")
+    per_token_rel(Ys.cpu().numpy(), orc.slow_path(Wn, Xn), tol, "Y_slow")
     r = rho.cpu().numpy().astype(np.float64)
     assert np.max(np.abs(r[finite] ** 2 - ro[finite] ** 2)) <= RHO2_TOL
     # per-token distances, relative to the dense output's norm

@@ -33,6 +33,8 @@ MUTANTS = {
     "compact_unstable": ("return t[~flags], t[flags]", "return t[~flags][::-1], t[flags][::-1]"),
     "gram_outer": ("return V.T @ V", "return V.T @ V + 1e-3 * np.eye(V.shape[1])"),
     "spectral_frobenius": ("return float(np.linalg.norm(W, 2))", "return float(np.linalg.norm(W))"),
+    "spectral_power_wrong_side": ("v = W.T @ (W @ v)", "v = W @ (W.T @ v)"),
+    "spectral_power_few_steps": ("for _ in range(iters):", "for _ in range(3):"),
     "brute_tie": ("slow = not (rho < eps)", "slow = rho > eps"),
     "brute_slow_uses_image": ("Y[t][o] = sum(W[o][i] * x[i] for i in range(d))",
                               "Y[t][o] = sum(M[o][j] * g[j] for j in range(k))"),

@@ -13,7 +13,7 @@ import ctypes
 import pytest
 import torch
 
-from tests.gpu_util import compare, upload
+from tests.gpu_util import compare, per_token_rel, upload
 from workloads import synth
 
 pytestmark = pytest.mark.gpu
@@ -62,8 +62,13 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(gsi):
         assert torch.equal(fn, fw)
         rel = (torch.linalg.norm(Yn - Yw) / torch.linalg.norm(Yw)).item()
         assert rel <= 2e-2, rel
+        per_token_rel(Yn.cpu().numpy(), Yw.cpu().numpy(), 2e-2, "noalloc vs workspace")
         assert torch.allclose(rn, rw, rtol=0, atol=1e-6)
         compare(m_in, gm.M, Yn, fn, rn)
+        # the built-in scratch's error word: no bounded wait gave up
+        code = ctypes.c_uint32(7)
+        st = gsi.lib().gsi_linear_noalloc_status(ctypes.byref(code), torch.cuda.current_stream().cuda_stream)
+        assert st == 0 and code.value == 0, gsi.lib().gsi_last_error().decode()
 
 
 def test_noalloc_rejects_calls_beyond_its_scratch(gsi):
