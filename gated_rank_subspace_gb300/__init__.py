@@ -75,11 +75,14 @@ def lib() -> ctypes.CDLL:
         "gsi_basis_step": [vp, ctypes.c_int, i64, i64, i64, vp, vp, sz, vp, vp],
         "gsi_basis_coherence": [vp, vp, i64, i64, vp, vp, vp],
         "gsi_basis_export": [vp, i64, i64, vp, ctypes.c_int, vp],
+        "gsi_residual_check": [P(MapDesc), vp, i64, vp, vp, vp, vp, vp, sz, vp],
     }
     for name, args in sig.items():
         fn = getattr(L, name)
         fn.argtypes = args
         fn.restype = ctypes.c_int
+    L.gsi_residual_check_work_bytes.argtypes = [i64, i64]
+    L.gsi_residual_check_work_bytes.restype = sz
     L.gsi_basis_step_work_bytes.argtypes = [i64, i64, i64]
     L.gsi_basis_step_work_bytes.restype = sz
     L.gsi_last_error.argtypes = []
@@ -88,6 +91,8 @@ def lib() -> ctypes.CDLL:
     L.gsi_debug_fail_after.restype = None
     L.gsi_debug_withhold_slice.argtypes = [ctypes.c_int]
     L.gsi_debug_withhold_slice.restype = None
+    L.gsi_debug_refuse_coresident.argtypes = [ctypes.c_int]
+    L.gsi_debug_refuse_coresident.restype = None
     L.gsi_linear_noalloc.argtypes = [P(MapDesc), vp, i64, f32, vp, vp, vp, vp]
     L.gsi_linear_noalloc.restype = ctypes.c_int
     L.gsi_linear_noalloc_max_bytes.argtypes = []
@@ -326,6 +331,23 @@ def gate(m: Map, X: torch.Tensor, eps: float, workspace=None, G=None, rho=None, 
     _check(lib().gsi_gate(ctypes.byref(desc), _ptr(X), T, float(eps), _ptr(G), _ptr(rho),
                           _ptr(flags), _ptr(workspace), workspace.numel(), _stream(stream)))
     return G, rho, flags
+
+
+def residual_check(m: Map, X: torch.Tensor, G: torch.Tensor, rho: torch.Tensor, work=None, stream=None):
+    """The gate's residual ratios checked against the explicit residual
+    x - V g (a second pass over V); returns (rho_explicit, max_dev) with
+    max_dev = max_t |rho_t^2 - rho_explicit_t^2| (device tensors)."""
+    _require_cuda(X, G, rho)
+    T = X.shape[0]
+    rho_x = torch.empty(T, dtype=torch.float32, device=X.device)
+    dev = torch.empty(1, dtype=torch.float32, device=X.device)
+    if work is None:
+        work = torch.empty(max(int(lib().gsi_residual_check_work_bytes(m.d, T)), 256), dtype=torch.uint8,
+                           device=X.device)
+    desc = m.desc()
+    _check(lib().gsi_residual_check(ctypes.byref(desc), _ptr(X), T, _ptr(G), _ptr(rho), _ptr(rho_x), _ptr(dev),
+                                    _ptr(work), work.numel(), _stream(stream)))
+    return rho_x, dev
 
 
 def apply(m: Map, X: torch.Tensor, G: torch.Tensor, workspace: torch.Tensor, Y=None, stream=None):

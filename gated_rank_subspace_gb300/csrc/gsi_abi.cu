@@ -53,6 +53,21 @@ static gsi_status cuda_check(cudaError_t e, const char* what) {
   return fail(GSI_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// Test hook: the next n launches that need a co-resident grid are refused
+// on the host, as the driver refuses a grid that cannot be co-resident.
+static std::atomic<int> g_refuse_coresident{0};
+static bool refused_coresident() { return g_refuse_coresident.load() > 0 && g_refuse_coresident.fetch_sub(1) > 0; }
+
+// Status of a launch that needs a co-resident grid: a refusal for size is
+// GSI_ERR_UNSUPPORTED, on which callers take the two-launch streaming path.
+static gsi_status coresident_status(cudaError_t e, const char* what) {
+  if (e == cudaErrorCooperativeLaunchTooLarge) {
+    cudaGetLastError();
+    return fail(GSI_ERR_UNSUPPORTED, "%s: the grid cannot be co-resident on this device now", what);
+  }
+  return cuda_check(e, what);
+}
+
 static int elem_bytes(gsi_dtype dt) { return dt == GSI_BF16 ? 2 : 4; }
 
 static bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
@@ -289,7 +304,9 @@ static gsi_status run_decode(const gsi_map_desc* m, const void* X, float eps, fl
     a.dbg_withhold = 1;
     a.poll_cycles = 20000000;  // ~10 ms
   }
-  return cuda_check(launch_decode(a, p, m->dtype, st), "single-token decode kernel launch");
+  if (p.grid && refused_coresident())
+    return fail(GSI_ERR_UNSUPPORTED, "single-token decode kernel launch: co-resident grid refused (test hook)");
+  return coresident_status(launch_decode(a, p, m->dtype, st), "single-token decode kernel launch");
 }
 
 // Enqueue the decide-and-apply kernel for one map (all arguments validated).
@@ -399,7 +416,9 @@ static gsi_status run_decide(const gsi_map_desc* m, const void* X, int64_t T, fl
   }
   a.err = &ctrl->err;
   a.flags_user = mode == 1 ? flags : nullptr;  // gsi_gate: also the caller's copy
-  return cuda_check(launch_decide_apply(a, dp, m->dtype, st), "decide-and-apply kernel launch");
+  if (fused && !dp.cproj && refused_coresident())
+    return fail(GSI_ERR_UNSUPPORTED, "decide-and-apply kernel launch: co-resident grid refused (test hook)");
+  return coresident_status(launch_decide_apply(a, dp, m->dtype, st), "decide-and-apply kernel launch");
 }
 
 // Enqueue the projection kernel, then (mode) the decide-and-apply kernel.
@@ -494,6 +513,8 @@ const char* gsi_last_error(void) { return g_err.c_str(); }
 void gsi_debug_fail_after(int n) { g_fail_after.store(n > 0 ? n : 0); }
 
 void gsi_debug_withhold_slice(int n) { g_withhold.store(n > 0 ? n : 0); }
+
+void gsi_debug_refuse_coresident(int n) { g_refuse_coresident.store(n > 0 ? n : 0); }
 
 gsi_status gsi_build_image(const void* W, const void* V, void* M, float* gram, int64_t d,
                            int64_t d_out, int64_t k, gsi_dtype dtype, void* stream) {
@@ -648,6 +669,37 @@ gsi_status gsi_eps_sweep(const float* rho, const float* err, const float* ynorm,
   const gsi_status s = cuda_check(launch_sweep(rho, err, ynorm, T, eps, n_eps, tokens_per_call, n_slow, n_slow_calls,
                                                rel_err, static_cast<cudaStream_t>(stream)),
                                   "sweep kernel launch");
+  return s == GSI_OK ? ok() : s;
+}
+
+size_t gsi_residual_check_work_bytes(int64_t d, int64_t T) {
+  if (d < 1 || T < 1) return 0;
+  return residual_check_work_bytes(d, T);
+}
+
+gsi_status gsi_residual_check(const gsi_map_desc* map, const void* X, int64_t T, const float* G, const float* rho,
+                              float* rho_explicit, float* max_dev, void* work, size_t work_bytes, void* stream) {
+  gsi_status s = check_map(map);
+  if (s != GSI_OK) return s;
+  if ((s = check_tokens(T, 0.f)) != GSI_OK) return s;
+  if (T > (int64_t(65535) * 8)) return fail(GSI_ERR_UNSUPPORTED, "the residual check takes T <= 524280");
+  if (!max_dev || !aligned(max_dev, 4)) return fail(GSI_ERR_INVALID_ARG, "max_dev is NULL or misaligned");
+  if (T == 0) {
+    if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
+    s = cuda_check(cudaMemsetAsync(max_dev, 0, sizeof(float), static_cast<cudaStream_t>(stream)), "max_dev clear");
+    return s == GSI_OK ? ok() : s;
+  }
+  if ((s = check_ptr(X, "X")) != GSI_OK) return s;
+  if ((s = check_ptr(G, "G")) != GSI_OK) return s;
+  if (!rho || !rho_explicit || !aligned(rho, 4) || !aligned(rho_explicit, 4))
+    return fail(GSI_ERR_INVALID_ARG, "rho and rho_explicit must be 4-byte aligned device arrays");
+  const size_t need = residual_check_work_bytes(map->d, T);
+  if (!work || !aligned(work, 256) || work_bytes < need)
+    return fail(GSI_ERR_WORKSPACE, "work must be 256-byte aligned and hold %zu bytes", need);
+  if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
+  s = cuda_check(launch_residual_check(X, map->V, G, rho, map->d, int(map->k), T, map->dtype, rho_explicit, max_dev,
+                                       work, static_cast<cudaStream_t>(stream)),
+                 "residual check launch");
   return s == GSI_OK ? ok() : s;
 }
 

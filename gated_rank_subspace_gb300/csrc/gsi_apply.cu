@@ -817,16 +817,16 @@ static cudaError_t launch_da_t(const DecideArgs& a, const DecidePlan& p, cudaStr
   cfg.blockDim = dim3(kApplyThreads);
   cfg.dynamicSmemBytes = p.smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
   attr[1].val.clusterDim.x = CS;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, a);
+  // the fused form without the cluster projection meets at a grid barrier
+  static int no_coop = 0;
+  return launch_maybe_coop(cfg, attr, 2, FUSED && !a.cproj, &no_coop, kern, a);
 }
 
 template <class E, bool FUSED, int CS>

@@ -240,6 +240,34 @@ inline cudaError_t set_kernel_smem(K kern, size_t dyn_bytes) {
   return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(dyn_bytes));
 }
 
+// ---------------------------------------------------------------- co-resident launches
+// Kernels whose CTAs wait on CTAs of other clusters (a grid barrier, polled
+// epoch words) are launched with the cooperative attribute: a grid that
+// cannot be co-resident (other work holding SMs, or a smaller device share)
+// is then refused at launch instead of running into its bounded waits.
+// Where the driver refuses the attribute together with a cluster shape, the
+// refusal is remembered in *no_coop and the launch is repeated without it
+// (the waits stay bounded).  A refusal for size comes back as
+// cudaErrorCooperativeLaunchTooLarge, for the caller to take another path.
+template <class K, class A>
+inline cudaError_t launch_maybe_coop(cudaLaunchConfig_t cfg, cudaLaunchAttribute* attrs, int n_attrs, bool coop,
+                                     int* no_coop, K kern, const A& args) {
+  if (coop && !*no_coop) {
+    attrs[n_attrs].id = cudaLaunchAttributeCooperative;
+    attrs[n_attrs].val.cooperative = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = unsigned(n_attrs + 1);
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, args);
+    if (e == cudaSuccess || e == cudaErrorCooperativeLaunchTooLarge) return e;
+    if (e != cudaErrorInvalidValue && e != cudaErrorNotSupported && e != cudaErrorInvalidConfiguration) return e;
+    cudaGetLastError();
+    *no_coop = 1;
+  }
+  cfg.attrs = attrs;
+  cfg.numAttrs = unsigned(n_attrs);
+  return cudaLaunchKernelEx(&cfg, kern, args);
+}
+
 // ---------------------------------------------------------------- workspace layout
 // Control words at the head of every workspace (256 bytes).
 struct Ctrl {

@@ -529,16 +529,16 @@ static cudaError_t launch_decode_t(const DecodeArgs& a, const DecodePlan& p, cud
   cfg.blockDim = dim3(kApplyThreads);
   cfg.dynamicSmemBytes = p.smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
+  cudaLaunchAttribute attr[3];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
   attr[1].val.clusterDim.x = kDecodeCluster;
   attr[1].val.clusterDim.y = 1;
   attr[1].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, a);
+  // the grid projection's CTAs poll other clusters' words: co-resident launch
+  static int no_coop = 0;
+  return launch_maybe_coop(cfg, attr, 2, p.grid != 0, &no_coop, kern, a);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, gsi_dtype dt, cudaStream_t s) {

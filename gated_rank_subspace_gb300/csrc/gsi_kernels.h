@@ -161,6 +161,11 @@ cudaError_t launch_contract(const void* A, gsi_dtype adt, int64_t sam, int64_t s
 cudaError_t launch_dgks(float* Qt, int64_t d, int k, int32_t* n_reorth, cudaStream_t s);
 cudaError_t launch_sumsq(const float* S, int64_t n, float scale, float* out, cudaStream_t s);
 cudaError_t launch_transpose_cast(const float* Qt, int64_t k, int64_t d, void* V, gsi_dtype dt, cudaStream_t s);
+// Explicit-residual check of the gate (see gsi_check.cu).
+size_t residual_check_work_bytes(int64_t d, int64_t T);
+cudaError_t launch_residual_check(const void* X, const void* V, const float* G, const float* rho, int64_t d, int k,
+                                  int64_t T, gsi_dtype dt, float* rho_x, float* max_dev, void* work,
+                                  cudaStream_t s);
 cudaError_t launch_image(const void* W, const void* V, void* M, float* gram, int64_t d,
                          int64_t d_out, int64_t k, gsi_dtype dt, cudaStream_t s);
 

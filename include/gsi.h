@@ -82,10 +82,12 @@ typedef enum gsi_dtype { GSI_F32 = 0, GSI_BF16 = 1 } gsi_dtype;
  *   TENSOR -- tcgen05 contractions, bf16 only, for prefill-sized T.
  * AUTO picks FUSED for T <= 2 where a slab of V fits shared memory (and
  * STREAM at run time on a device that cannot hold the fused grid), TENSOR
- * for bf16 with T >= 128, STREAM otherwise.  The fused grid must be
- * co-resident: its waits on other CTAs give up after ~2 s (GSI_ERR_TIMEOUT,
- * and the workspace must then be re-initialised) if other work keeps SMs
- * busy. */
+ * for bf16 with T >= 128, STREAM otherwise.  Where the fused kernels' CTAs
+ * wait on other clusters, they are launched as a co-resident (cooperative)
+ * grid: a grid that cannot be co-resident is refused at launch, and AUTO
+ * then runs the call on the STREAM kernels.  Every device wait stays bounded
+ * (~2 s, then GSI_ERR_TIMEOUT from gsi_workspace_status, after which the
+ * workspace must be re-initialised). */
 typedef enum gsi_path {
   GSI_PATH_AUTO = 0,
   GSI_PATH_STREAM = 1,
@@ -134,6 +136,22 @@ gsi_status gsi_workspace_status(const void* workspace, uint32_t* code, void* str
 gsi_status gsi_gate(const gsi_map_desc* map, const void* X, int64_t T, float eps,
                     float* G, float* rho, uint8_t* flags,
                     void* workspace, size_t ws_bytes, void* stream);
+
+/* §2.1 core decomposition, checked (a validation mode, off the hot path).
+ * The gate kernels evaluate ||x - V g||^2 from the Gram form without a
+ * second pass over V.  This call forms the residual itself, r_t = x_t - V g_t,
+ * for the projections G (T x k float32, as written by gsi_gate) with a second
+ * pass over V, and writes rho_explicit[t] = ||r_t|| / ||x_t|| (T float32; 0
+ * for a zero token) and *max_dev = max over tokens of
+ * |rho[t]^2 - rho_explicit[t]^2| (one float32), rho (T float32) being the
+ * gate's ratios; tokens where either value is not finite are skipped.
+ * Partial sums in float32 per 64-row slab of V, added in slab order in
+ * double: bitwise reproducible.  work: device, 256-byte aligned,
+ * gsi_residual_check_work_bytes(d, T) bytes.  All array arguments are device
+ * pointers; T <= 524280.  Enqueued on `stream`. */
+size_t gsi_residual_check_work_bytes(int64_t d, int64_t T);
+gsi_status gsi_residual_check(const gsi_map_desc* map, const void* X, int64_t T, const float* G, const float* rho,
+                              float* rho_explicit, float* max_dev, void* work, size_t work_bytes, void* stream);
 
 /* §2.2 per-token gate, compaction step: stable (ascending token index) lists
  * of fast and slow tokens.  idx (device, 2*T int32) receives the fast list in
@@ -284,6 +302,14 @@ void gsi_debug_fail_after(int n);
  * gsi_workspace_status returns GSI_ERR_TIMEOUT, and the workspace must be
  * re-initialised before its next use.  Nothing faults or hangs. */
 void gsi_debug_withhold_slice(int n);
+
+/* Test hook (n <= 0 disarms): the next n launches that need a co-resident
+ * grid (the single-token decode kernel's grid projection, the two-token
+ * fused kernel's grid barrier) are refused on the host, as the driver
+ * refuses a grid that cannot be co-resident.  gsi_linear and gsi_stack then
+ * run those calls on the two-launch streaming kernels; gsi_linear_ex with
+ * GSI_PATH_FUSED returns GSI_ERR_UNSUPPORTED. */
+void gsi_debug_refuse_coresident(int n);
 
 #ifdef __cplusplus
 }

@@ -67,3 +67,35 @@ def test_withheld_slice_times_out_and_recovers(gsi):
     torch.cuda.synchronize()
     assert gsi.workspace_status(ws) == 0
     compare(m_in, gm.M, Y2, F2, R2)
+
+
+@pytest.mark.parametrize("shape", [(8200, 520, 64), (32768, 64, 64)])
+def test_refused_coresident_grid_falls_back(gsi, shape):
+    """Launches refused for co-residency: AUTO still runs every call (on a
+    kernel that needs no co-resident grid, at the end the two-launch
+    streaming kernels) with the same results.  (8200, 520, 64): the
+    single-token kernel's grid projection is refused; (32768, 64, 64): a
+    sixteenth of V does not fit one CTA, so both single-launch forms need a
+    co-resident grid and an explicit fused call reports the refusal."""
+    d, d_out, k = shape
+    V64 = synth.orthonormal_basis(synth.rng(8, d, k, 3), d, k)
+    m_in = synth.stack_layer(8, 1, {"qkv": V64}, {"qkv": (d_out, d)}, T=4, f_slow=0.5, roles=("qkv",))[0]
+    gm, X = upload(m_in)
+    ws = gsi.new_workspace(gsi.workspace_size(gm, 1))
+    Y = torch.empty(4, d_out, device="cuda")
+    F = torch.empty(4, dtype=torch.uint8, device="cuda")
+    R = torch.empty(4, device="cuda")
+    gsi.lib().gsi_debug_refuse_coresident(1 << 20)
+    try:
+        for t in range(4):
+            Yc = torch.empty(1, d_out, device="cuda")
+            gsi.linear(gm, X[t:t + 1], m_in.eps, Y=Yc, flags=F[t:t + 1], rho=R[t:t + 1], workspace=ws)
+            Y[t:t + 1] = Yc
+        if d == 32768:
+            with pytest.raises(gsi.GsiError, match="co-resident"):
+                gsi.linear(gm, X[:1], m_in.eps, workspace=ws, path="fused")
+    finally:
+        gsi.lib().gsi_debug_refuse_coresident(0)
+    torch.cuda.synchronize()
+    assert gsi.workspace_status(ws) == 0
+    compare(m_in, gm.M, Y, F, R)
