@@ -53,6 +53,14 @@ def peaks():
     return 6800.0, "fallback"
 
 
+def bf16_peak():
+    """Dense bf16 tensor peak (TFLOP/s, burst): measured, else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        return float(json.load(open(p))["bf16_tflops"]), "measured"
+    return 1900.0, "fallback"
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons while the timed region runs."""
 
@@ -245,6 +253,199 @@ def kernel_source_hash():
 
 def kernel_traffic():
     return KERNEL_TRAFFIC["bytes_per_launch"] if kernel_source_hash() == KERNEL_TRAFFIC["src_sha256"] else None
+
+
+def call_bytes(d, d_out, k, T, n_fast, n_slow, es=2):
+    """Algorithmic bytes of one gated-map call of T tokens: V_k and its Gram,
+    M if any token is fast, W if any is slow, and per token x in, y out,
+    g and rho and the flag: |V| + |Gram| + [n_f > 0] |M| + [n_s > 0] |W|
+    + T (d s_x + d_out 4 + k 4 + 5)."""
+    return (d * k * es + k * k * 4 + (d_out * k * es if n_fast else 0) + (d_out * d * es if n_slow else 0)
+            + T * (d * es + d_out * 4 + k * 4 + 5))
+
+
+def dense_bytes(d, d_out, T, es=2):
+    """The dense map's bytes for the same call: W once, x in, y out."""
+    return d_out * d * es + T * (d * es + d_out * 4)
+
+
+def graph_time_ms(fn, stream, reps, warm=2):
+    """Mean time of one call of fn, captured in a CUDA graph, over reps replays."""
+    with torch.cuda.stream(stream):
+        fn()
+    stream.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        fn()
+    with torch.cuda.stream(stream):
+        for _ in range(warm):
+            g.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            g.replay()
+        e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) / reps
+
+
+def run_config3(gsi, dev, stream, hbm_peak, steps=64, reps=2):
+    """The 28-layer linear-only stack of the 6B shapes (depth-coherent bases,
+    per-layer slow fraction 5-15%): `steps` single-token decode steps, each one
+    gsi_stack call over the 112 maps (one persistent launch), all steps in one
+    CUDA graph.  Tokens/s counts one token per 28-layer step."""
+    L = 28
+    bases, fr, base_W, tokens = synth.stack_config3(L, steps)
+    maps, Xs = [], []
+    for role in synth.ROLES:
+        base_W[role] = base_W[role].to(dev)
+    for l in range(L):
+        for role in synth.ROLES:
+            d_out, d = synth.SHAPES_6B[role]
+            perm, signs = synth.layer_weight_rows(3, l, synth.ROLE_ID[role], d_out)
+            W = (base_W[role][torch.from_numpy(perm).to(dev)] *
+                 torch.from_numpy(signs).to(dev, torch.bfloat16)[:, None]).contiguous()
+            maps.append(gsi.make_map(W, synth.storage(bases[role][l], torch.bfloat16).to(dev)))
+            Xs.append(tokens[(l, role)].to(dev))
+    del base_W
+    Ys = [torch.zeros(steps, m.d_out, device=dev) for m in maps]
+    Fs = [torch.zeros(steps, dtype=torch.uint8, device=dev) for _ in maps]
+    ws = gsi.new_workspace(gsi.stack_workspace_size(maps, 1), dev)
+    args = [gsi.stack_args(maps, [X[t:t + 1] for X in Xs], [Y[t:t + 1] for Y in Ys], [F[t:t + 1] for F in Fs])
+            for t in range(steps)]
+    torch.cuda.synchronize()
+
+    def run():
+        for a in args:
+            gsi.stack_raw(a, len(maps), 1, EPS, ws, stream=stream)
+
+    ms = graph_time_ms(run, stream, reps)
+    assert gsi.workspace_status(ws, stream=stream) == 0
+    flags = [F.cpu().numpy().astype(bool) for F in Fs]
+    nbytes = dense = 0
+    for m, f in zip(maps, flags):
+        for t in range(steps):
+            nbytes += call_bytes(m.d, m.d_out, m.k, 1, int(not f[t]), int(f[t]))
+            dense += dense_bytes(m.d, m.d_out, 1)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    out = {"workload": "28-layer linear-only stack, 6B shapes, depth-coherent bases, k=256, eps=0.05, "
+                       f"{steps} single-token decode steps (one gsi_stack call of 112 maps per step)",
+           "tokens_per_s": steps / (ms * 1e-3), "ms_per_token": ms / steps, "achieved_gbs": gbs,
+           "frac_of_hbm_peak": gbs / hbm_peak, "bytes_saved_vs_dense": dense / nbytes,
+           "slow_fraction": float(np.mean([f.mean() for f in flags])),
+           "kernel": "stack_decode_kernel (one persistent launch per 112-map step)"}
+    del maps, Xs, Ys, Fs, args, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def config4_maps(gsi, dev, L=40):
+    """The 40-layer 13B stack on the device (layer weights and bases derived
+    from per-role base draws, see synth.stack_config4); returns (maps, pools)."""
+    base_W, V64, rows, cols, pools = synth.stack_config4(L)
+    maps = []
+    for role in synth.ROLES:
+        base_W[role] = base_W[role].to(dev)
+    Vb = {r: synth.storage(V64[r], torch.bfloat16).to(dev) for r in synth.ROLES}
+    for l in range(L):
+        for role in synth.ROLES:
+            perm, signs = rows[(l, role)]
+            W = (base_W[role][torch.from_numpy(perm).to(dev)] *
+                 torch.from_numpy(signs).to(dev, torch.bfloat16)[:, None]).contiguous()
+            V = Vb[role][:, torch.from_numpy(cols[(l, role)]).to(dev)].contiguous()
+            maps.append(gsi.make_map(W, V))
+    return maps, pools
+
+
+def run_config4(gsi, dev, stream, hbm_peak, reps=2):
+    """13B linears, 40 layers, k=320, small-batch decode: T in {1, 4, 16}
+    tokens per call, slow fraction f in {0, 5, 25, 100}% (per-token Bernoulli
+    labels); every decode step is one gsi_stack call over the 160 maps.  Per
+    point: tokens/s of the 40-layer model, GB/s of the algorithmic bytes, and
+    the bytes saved against dense W x (a call reads W when any of its T
+    tokens is slow)."""
+    L = 40
+    maps, pools = config4_maps(gsi, dev, L)
+    ws = gsi.new_workspace(max(gsi.stack_workspace_size(maps, T) for T in (1, 4, 16)), dev)
+    points = []
+    for T, steps in ((1, 16), (4, 8), (16, 4)):
+        for f in (0.0, 0.05, 0.25, 1.0):
+            n = T * steps
+            Xs, Ys, Fs = [], [], []
+            for l in range(L):
+                for role in synth.ROLES:
+                    Xs.append(synth.pool_tokens(pools, role, l, n, f, salt=int(T * 100 + f * 100)).to(dev))
+            for m in maps:
+                Ys.append(torch.zeros(n, m.d_out, device=dev))
+                Fs.append(torch.zeros(n, dtype=torch.uint8, device=dev))
+            args = [gsi.stack_args(maps, [X[s * T:(s + 1) * T] for X in Xs], [Y[s * T:(s + 1) * T] for Y in Ys],
+                                   [F[s * T:(s + 1) * T] for F in Fs]) for s in range(steps)]
+
+            def run():
+                for a in args:
+                    gsi.stack_raw(a, len(maps), T, EPS, ws, stream=stream)
+
+            ms = graph_time_ms(run, stream, reps)
+            assert gsi.workspace_status(ws, stream=stream) == 0
+            nbytes = dense = 0
+            n_slow = 0
+            for m, F in zip(maps, Fs):
+                fl = F.cpu().numpy().astype(bool).reshape(steps, T)
+                n_slow += int(fl.sum())
+                for s in range(steps):
+                    ns = int(fl[s].sum())
+                    nbytes += call_bytes(m.d, m.d_out, m.k, T, T - ns, ns)
+                    dense += dense_bytes(m.d, m.d_out, T)
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            points.append({"T": T, "f": f, "tokens_per_s": n / (ms * 1e-3), "ms_per_step": ms / steps,
+                           "achieved_gbs": gbs, "frac_of_hbm_peak": gbs / hbm_peak,
+                           "bytes_saved_vs_dense": dense / nbytes,
+                           "slow_fraction": n_slow / (n * len(maps))})
+            del Xs, Ys, Fs, args
+    out = {"workload": "13B-class linears (qkv 15360x5120, out 5120^2, up 13824x5120, down 5120x13824), "
+                       "40 layers, bf16, k=320, eps=0.05; each decode step one gsi_stack call over the 160 maps",
+           "points": points,
+           "kernels": "T=1: stack_decode_kernel (persistent); T=4, 16: project_kernel + decide_apply_kernel per map"}
+    del maps, ws
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_config5(gsi, dev, stream, hbm_peak, tflops_peak, reps=20, R=2):
+    """The prefill-sized map (T=2048, d=4096, d_out=16384, k=256, 410 slow
+    tokens) on the tensor-core path, calls alternating over R weight
+    replicas."""
+    m_in = synth.config5()
+    base = gsi.make_map(m_in.W.to(dev), m_in.V.to(dev))
+    reps_m = [base] + [gsi.Map(base.W.clone(), base.V.clone(), base.M.clone(), base.gram.clone())
+                       for _ in range(R - 1)]
+    X = m_in.X.to(dev)
+    T = X.shape[0]
+    Y = torch.zeros(T, base.d_out, device=dev)
+    F = torch.zeros(T, dtype=torch.uint8, device=dev)
+    ws = gsi.new_workspace(gsi.workspace_size(base, T, "auto"), dev)
+
+    def run():
+        for m in reps_m:
+            gsi.linear(m, X, EPS, Y=Y, flags=F, workspace=ws, want_rho=False, stream=stream)
+
+    ms = graph_time_ms(run, stream, reps) / R
+    assert gsi.workspace_status(ws, stream=stream) == 0
+    ns = int(F.sum())
+    nf = T - ns
+    d, d_out, k = base.d, base.d_out, base.k
+    flop = 2 * (T * d * k + nf * d_out * k + ns * d_out * d)
+    nbytes = call_bytes(d, d_out, k, T, nf, ns)
+    out = {"workload": "prefill-sized map: T=2048, d=4096, d_out=16384, k=256, 410 slow tokens, bf16, "
+                       "tensor-core path (gsi_linear AUTO)",
+           "tokens_per_s": T / (ms * 1e-3), "us_per_call": ms * 1e3,
+           "tflops": flop / (ms * 1e-3) / 1e12, "frac_of_bf16_peak": flop / (ms * 1e-3) / 1e12 / tflops_peak,
+           "achieved_gbs": nbytes / (ms * 1e-3) / 1e9, "frac_of_hbm_peak": nbytes / (ms * 1e-3) / 1e9 / hbm_peak,
+           "gflop_per_call": flop / 1e9, "dense_gflop_per_call": 2 * T * d_out * d / 1e9, "n_slow": ns}
+    del reps_m, base, X, Y, F, ws
+    torch.cuda.empty_cache()
+    return out
 
 
 SWEEP_EPS = [0.0, 0.0125, 0.025, 0.05, 0.1, 0.2, 0.4, float("inf")]
@@ -493,7 +694,17 @@ def main():
                     help="only report one call's latency per 6B map, all tokens slow and all fast (JSON lines)")
     ap.add_argument("--cascade", action="store_true",
                     help="only report basis construction on depth-coherent calibration blocks (one JSON line)")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the secondary workloads (28-layer stack, 13B small-batch stack, prefill map)")
+    ap.add_argument("--oracle-probe", action="store_true",
+                    help="only time the oracle on the bench workload's tokens (JSON line; thread count from the "
+                         "environment), as the single-thread leg of the CPU baseline")
     args = ap.parse_args()
+    if args.oracle_probe:
+        maps_in = make_inputs()
+        v, dt, passes = time_oracle(oracle_maps(maps_in), EPS, args.cpu_seconds)
+        print(json.dumps({"value": v, "seconds": dt, "passes": passes}))
+        return
     if args.cascade:
         run_cascade()
         return
@@ -721,6 +932,44 @@ def main():
                "sample": f"{passes} passes of the 256 decode tokens through all four maps "
                          f"({dt:.1f} s of float64 numpy; BLAS threads = host cores)"}
 
+    if cpu is not None:
+        # the same sample on one host thread (a fresh process whose BLAS
+        # threads are set to one before numpy loads)
+        env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-probe", "--cpu-seconds",
+                            str(args.cpu_seconds)], capture_output=True, text=True, env=env)
+        try:
+            one = json.loads(r.stdout.strip().splitlines()[-1])
+            cpu["value_1_thread"] = one["value"]
+            cpu["sample_1_thread"] = f"{one['passes']} passes ({one['seconds']:.1f} s) on one thread"
+        except (ValueError, IndexError, KeyError):
+            cpu["value_1_thread"] = None
+
+    # ---- the gate's Gram form checked on the device against the explicit
+    # residual x - V g (second pass over V) for the step's 1024 calls
+    rho_dev = []
+    for i, b in enumerate(base):
+        G_i = G_all[i::4].contiguous()
+        r_i = rho_all[i::4].contiguous()
+        _, dv = gsi.residual_check(b, Xs[i], G_i, r_i, stream=stream)
+        rho_dev.append(dv)
+    stream.synchronize()
+    gate_check = {"max_abs_rho2_gram_minus_explicit": max(float(v.item()) for v in rho_dev),
+                  "what": "largest |rho^2 (Gram form, gate kernels) - rho^2 (explicit x - V g, second pass)| "
+                          "over the 1024 single-token calls of the step (gsi_residual_check)"}
+
+    secondary = None
+    if not args.no_secondary and world == 1:
+        tf_peak, _ = bf16_peak()
+        secondary = {"note": "further synthetic workloads, each timed on its own after the headline step"}
+        for key, fn in (("cfg3_28_layer_stack", lambda: run_config3(gsi, dev, stream, hbm_peak)),
+                        ("cfg4_13b_small_batch", lambda: run_config4(gsi, dev, stream, hbm_peak)),
+                        ("cfg5_prefill", lambda: run_config5(gsi, dev, stream, hbm_peak, tf_peak))):
+            try:
+                secondary[key] = fn()
+            except Exception as e:  # report and go on: the headline line still prints
+                secondary[key] = {"error": f"{type(e).__name__}: {e}"}
+
     gpu_launches = args.steps * T_TOKENS * sum(per_call)
     line = {
         "metric": "gsi_linear_tokens_per_s_batch1",
@@ -775,6 +1024,8 @@ def main():
         "gpu_launches": gpu_launches,
         "clocks": clocks,
         "cpu_baseline": cpu,
+        "gate_check": gate_check,
+        "secondary": secondary,
     }
     if rank == 0:
         print(json.dumps(line))

@@ -59,6 +59,7 @@ def lib() -> ctypes.CDLL:
     P = ctypes.POINTER
     sig = {
         "gsi_build_image": [vp, vp, vp, vp, i64, i64, i64, ctypes.c_int, vp],
+        "gsi_build_image_ex": [vp, vp, vp, vp, i64, i64, i64, ctypes.c_int, vp, sz, vp],
         "gsi_linear_workspace_size": [P(MapDesc), i64, ctypes.c_int, P(sz)],
         "gsi_workspace_init": [vp, sz, vp],
         "gsi_workspace_status": [vp, P(ctypes.c_uint32), vp],
@@ -81,6 +82,8 @@ def lib() -> ctypes.CDLL:
         fn = getattr(L, name)
         fn.argtypes = args
         fn.restype = ctypes.c_int
+    L.gsi_build_image_work_bytes.argtypes = [i64, i64, ctypes.c_int]
+    L.gsi_build_image_work_bytes.restype = sz
     L.gsi_residual_check_work_bytes.argtypes = [i64, i64]
     L.gsi_residual_check_work_bytes.restype = sz
     L.gsi_basis_step_work_bytes.argtypes = [i64, i64, i64]
@@ -167,8 +170,11 @@ class Map:
                        self.gram.data_ptr() if self.gram is not None else None)
 
 
-def build_image(W: torch.Tensor, V: torch.Tensor, M=None, gram=None, with_gram=True, stream=None):
-    """M = W V (and the Gram V^T V) on the GPU; returns (M, gram)."""
+def build_image(W: torch.Tensor, V: torch.Tensor, M=None, gram=None, with_gram=True, stream=None,
+                tensor_cores=True):
+    """M = W V (and the Gram V^T V) on the GPU; returns (M, gram).  bf16 maps
+    use the tensor cores (a scratch area is allocated here, by PyTorch)
+    unless tensor_cores is False, which keeps the CUDA-core kernel."""
     _require_cuda(W, V)
     d_out, d = W.shape
     k = V.shape[1]
@@ -176,8 +182,16 @@ def build_image(W: torch.Tensor, V: torch.Tensor, M=None, gram=None, with_gram=T
         M = torch.empty(d_out, k, dtype=W.dtype, device=W.device)
     if gram is None and with_gram:
         gram = torch.empty(k, k, dtype=torch.float32, device=W.device)
-    _check(lib().gsi_build_image(_ptr(W), _ptr(V), _ptr(M), _ptr(gram), d, d_out, k,
-                                 _dtype_code(W.dtype), _stream(stream)))
+    dt = _dtype_code(W.dtype)
+    nwork = int(lib().gsi_build_image_work_bytes(d, k, dt)) if tensor_cores else 0
+    if nwork:
+        work = torch.empty(nwork, dtype=torch.uint8, device=W.device)
+        _check(lib().gsi_build_image_ex(_ptr(W), _ptr(V), _ptr(M), _ptr(gram), d, d_out, k, dt, _ptr(work),
+                                        nwork, _stream(stream)))
+        if workspace_status(work, stream) != 0:
+            raise GsiError(5, "image build: a bounded device wait gave up")
+    else:
+        _check(lib().gsi_build_image(_ptr(W), _ptr(V), _ptr(M), _ptr(gram), d, d_out, k, dt, _stream(stream)))
     return M, gram
 
 

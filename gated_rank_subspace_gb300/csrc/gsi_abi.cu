@@ -194,6 +194,7 @@ struct DeviceFacts {
   int smem_optin = 0;
   int clusters[2][2][2] = {};  // co-resident clusters per [dtype][fused][cs == 16]; -1: not possible
   int decode_clusters[2] = {};  // co-resident clusters of the single-token decode kernel per dtype
+  int stack_clusters[2][2] = {};  // ... of the persistent stack kernel per [dtype][two vectors a lane]
 };
 
 // Shared memory of the two-launch decide-and-apply kernel: the device limit
@@ -231,6 +232,18 @@ static int decide_clusters(DeviceFacts* f, gsi_dtype dt, bool fused, int cs) {
   return c > 0 ? c : 0;
 }
 
+// Co-resident clusters of the persistent stack kernel (cached); 0 if none.
+static int stack_clusters(DeviceFacts* f, gsi_dtype dt, int nv) {
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  int& c = f->stack_clusters[dt == GSI_BF16][nv == 2];
+  if (c == 0) {
+    const int n = stack_max_clusters(size_t(f->smem_optin), dt, nv);
+    c = n > 0 ? n : -1;
+  }
+  return c > 0 ? c : 0;
+}
+
 // Co-resident clusters of the single-token decode kernel (cached); 0 if none.
 static int decode_clusters(DeviceFacts* f, gsi_dtype dt) {
   static std::mutex mu;
@@ -243,31 +256,31 @@ static int decode_clusters(DeviceFacts* f, gsi_dtype dt) {
   return c > 0 ? c : 0;
 }
 
-// Enqueue the single-token decode kernel (all arguments validated): the
-// cluster projection where the basis fits a cluster, else the grid
-// projection; GSI_ERR_UNSUPPORTED, with nothing launched, when neither fits.
-static gsi_status run_decode(const gsi_map_desc* m, const void* X, float eps, float* Y, uint8_t* flags, float* rho,
-                             void* ws, cudaStream_t st, DeviceFacts* f, const gsi_map_desc* next) {
-  const int es = elem_bytes(m->dtype);
+// The single-token decode kernel's plan for a map: the cluster projection
+// where the basis fits a cluster, else the grid projection (ok = false when
+// neither fits this device).
+static DecodePlan decode_plan(const gsi_map_desc* m, DeviceFacts* f) {
   DecodePlan p{};
   const int ncl = decode_clusters(f, m->dtype);
   for (int grid = 0; grid < 2 && ncl > 0 && !p.ok; ++grid)
-    p = plan_decode(m->d, m->d_out, m->k, es, ncl * kDecodeCluster, size_t(f->smem_optin), grid != 0);
-  if (!p.ok) return GSI_ERR_UNSUPPORTED;
-  Ctrl* ctrl = static_cast<Ctrl*>(ws);
-  DecodeArgs a{};
+    p = plan_decode(m->d, m->d_out, m->k, elem_bytes(m->dtype), ncl * kDecodeCluster, size_t(f->smem_optin),
+                    grid != 0);
+  return p;
+}
+
+static void fill_decode_map(DecodeMap& a, const gsi_map_desc* m, const DecodePlan& p, const void* X, float* Y,
+                            uint8_t* flags, float* rho) {
   a.X = X;
   a.W = m->W;
   a.V = m->V;
   a.M = m->M;
   a.gram = m->gram;
-  a.d = m->d;
-  a.d_out = m->d_out;
-  a.k = int(m->k);
-  a.eps = eps;
   a.Y = Y;
   a.flags = flags;
   a.rho = rho;
+  a.d = m->d;
+  a.d_out = m->d_out;
+  a.k = int(m->k);
   a.vr = p.vr;
   a.rw = p.rw;
   a.rpc = p.rpc;
@@ -284,6 +297,21 @@ static gsi_status run_decode(const gsi_map_desc* m, const void* X, float eps, fl
   a.off_v = p.off_v;
   a.off_m = p.off_m;
   a.grid = p.grid;
+}
+
+// 16-byte vectors of a V / M row per lane in the single-token kernels.
+static int decode_nv(const gsi_map_desc* m) { return m->k * elem_bytes(m->dtype) > 512 ? 2 : 1; }
+
+// Enqueue the single-token decode kernel (all arguments validated);
+// GSI_ERR_UNSUPPORTED, with nothing launched, when its plan does not fit.
+static gsi_status run_decode(const gsi_map_desc* m, const void* X, float eps, float* Y, uint8_t* flags, float* rho,
+                             void* ws, cudaStream_t st, DeviceFacts* f, const gsi_map_desc* next) {
+  const DecodePlan p = decode_plan(m, f);
+  if (!p.ok) return GSI_ERR_UNSUPPORTED;
+  Ctrl* ctrl = static_cast<Ctrl*>(ws);
+  DecodeArgs a{};
+  fill_decode_map(a.m, m, p, X, Y, flags, rho);
+  a.eps = eps;
   if (p.grid) {
     const FusedLayout FL = layout_fused(m->k, 1);
     a.part_g = reinterpret_cast<float*>(static_cast<char*>(ws) + FL.part_g);
@@ -307,6 +335,42 @@ static gsi_status run_decode(const gsi_map_desc* m, const void* X, float eps, fl
   if (p.grid && refused_coresident())
     return fail(GSI_ERR_UNSUPPORTED, "single-token decode kernel launch: co-resident grid refused (test hook)");
   return coresident_status(launch_decode(a, p, m->dtype, st), "single-token decode kernel launch");
+}
+
+// Persistent stack decode over maps[0 .. n) (n >= 2, T = 1, every map with a
+// single-token plan, one element type, row width and k): one launch, the
+// calls in list order with a grid barrier between them.  GSI_ERR_UNSUPPORTED,
+// with nothing launched, when the kernel cannot run here (the caller then
+// runs the maps one launch each).
+static gsi_status run_stack_decode(const gsi_map_desc* maps, int n, const void* const* X, float eps,
+                                   float* const* Y, uint8_t* const* flags, void* ws, cudaStream_t st,
+                                   DeviceFacts* f) {
+  const gsi_dtype dt = maps[0].dtype;
+  const int ncl = decode_clusters(f, dt);
+  if (ncl == 0 || stack_clusters(f, dt, decode_nv(&maps[0])) != ncl) return GSI_ERR_UNSUPPORTED;
+  static thread_local StackDecodeArgs a;  // 17 KB: kept off the stack
+  a = StackDecodeArgs{};
+  size_t smem = 0;
+  for (int i = 0; i < n; ++i) {
+    const DecodePlan p = decode_plan(&maps[i], f);
+    if (!p.ok) return GSI_ERR_UNSUPPORTED;
+    fill_decode_map(a.maps[i], &maps[i], p, X[i], Y[i], flags[i], nullptr);
+    if (p.smem > smem) smem = p.smem;
+  }
+  Ctrl* ctrl = static_cast<Ctrl*>(ws);
+  const FusedLayout FL = layout_fused(maps[0].k, 1);
+  a.n_maps = n;
+  a.eps = eps;
+  a.part_g = reinterpret_cast<float*>(static_cast<char*>(ws) + FL.part_g);
+  a.part_x = reinterpret_cast<float*>(static_cast<char*>(ws) + FL.part_x);
+  a.ticket = &ctrl->ticket1[dt == GSI_BF16 ? 1 : 0];
+  a.arrive = &ctrl->arrive[dt == GSI_BF16 ? 1 : 0];
+  a.err = &ctrl->err;
+  if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
+  if (refused_coresident())
+    return fail(GSI_ERR_UNSUPPORTED, "stack decode kernel launch: co-resident grid refused (test hook)");
+  return coresident_status(launch_stack_decode(a, smem, ncl * kDecodeCluster, decode_nv(&maps[0]), dt, st),
+                           "stack decode kernel launch");
 }
 
 // Enqueue the decide-and-apply kernel for one map (all arguments validated).
@@ -527,6 +591,31 @@ gsi_status gsi_build_image(const void* W, const void* V, void* M, float* gram, i
   if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
   s = cuda_check(launch_image(W, V, M, gram, d, d_out, k, dtype, static_cast<cudaStream_t>(stream)),
                  "image kernel launch");
+  return s == GSI_OK ? ok() : s;
+}
+
+size_t gsi_build_image_work_bytes(int64_t d, int64_t k, gsi_dtype dtype) {
+  if (dtype != GSI_BF16 || d < 1 || k < 1) return 0;
+  return 256 + align256(size_t(k) * size_t(d) * 2);
+}
+
+gsi_status gsi_build_image_ex(const void* W, const void* V, void* M, float* gram, int64_t d, int64_t d_out, int64_t k,
+                              gsi_dtype dtype, void* work, size_t work_bytes, void* stream) {
+  if (!work || dtype != GSI_BF16) return gsi_build_image(W, V, M, gram, d, d_out, k, dtype, stream);
+  gsi_status s = check_shape(d, d_out, k, dtype);
+  if (s != GSI_OK) return s;
+  if ((s = check_ptr(W, "W")) != GSI_OK) return s;
+  if ((s = check_ptr(V, "V")) != GSI_OK) return s;
+  if ((s = check_ptr(M, "M")) != GSI_OK) return s;
+  if (gram && !aligned(gram, 16)) return fail(GSI_ERR_INVALID_ARG, "gram is not 16-byte aligned");
+  if (d > (int64_t(1) << 30) || d_out > (int64_t(1) << 30)) return fail(GSI_ERR_UNSUPPORTED, "dimension above 2^30");
+  if ((s = check_workspace(work, work_bytes, gsi_build_image_work_bytes(d, k, dtype))) != GSI_OK) return s;
+  if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  Ctrl* ctrl = static_cast<Ctrl*>(work);
+  if ((s = cuda_check(cudaMemsetAsync(ctrl, 0, sizeof(Ctrl), st), "image scratch clear")) != GSI_OK) return s;
+  uint16_t* Vt = reinterpret_cast<uint16_t*>(static_cast<char*>(work) + 256);
+  s = cuda_check(launch_image_tc(W, V, M, gram, d, d_out, k, Vt, &ctrl->err, st), "image kernel launch");
   return s == GSI_OK ? ok() : s;
 }
 
@@ -816,12 +905,38 @@ gsi_status gsi_stack(const gsi_map_desc* maps, int64_t n_maps, const void* const
   if (T == 0) return ok();
   if ((s = check_workspace(workspace, ws_bytes, need)) != GSI_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  for (int64_t i = 0; i < n_maps; ++i) {
+  // One token per map: runs of consecutive maps that the single-token kernel
+  // takes (one element type, row width and k) go to the persistent stack
+  // kernel, up to kStackMaxMaps per launch; every other map (and a run the
+  // device refuses) is one call each.
+  DeviceFacts* f = nullptr;
+  if (T == 1 && (s = device_facts(&f)) != GSI_OK) return s;
+  auto stackable = [&](int64_t j) {
+    gsi_path p;
+    return resolve_path(&maps[j], 1, GSI_PATH_AUTO, &p) == GSI_OK && p == GSI_PATH_FUSED &&
+           decode_plan(&maps[j], f).ok;
+  };
+  for (int64_t i = 0; i < n_maps;) {
+    if (f && stackable(i)) {
+      int64_t j = i + 1;
+      while (j < n_maps && j - i < kStackMaxMaps && maps[j].dtype == maps[i].dtype && maps[j].k == maps[i].k &&
+             stackable(j))
+        ++j;
+      if (j - i >= 2) {
+        s = run_stack_decode(&maps[i], int(j - i), X + i, eps, Y + i, flags + i, workspace, st, f);
+        if (s == GSI_OK) {
+          i = j;
+          continue;
+        }
+        if (s != GSI_ERR_UNSUPPORTED) return fail(s, "maps %lld-%lld: %s", (long long)i, (long long)(j - 1), g_err.c_str());
+      }
+    }
     gsi_path p;
     resolve_path(&maps[i], T, GSI_PATH_AUTO, &p);
     s = run_path(&maps[i], p, false, X[i], T, eps, Y[i], flags[i], nullptr, workspace, st,
                  i + 1 < n_maps ? &maps[i + 1] : nullptr);
     if (s != GSI_OK) return fail(s, "map %lld: %s", (long long)i, g_err.c_str());
+    ++i;
   }
   return ok();
 }

@@ -12,6 +12,11 @@ __device__ __forceinline__ uint32_t sa(const void* p) { return static_cast<uint3
 __device__ __forceinline__ void bar_init(uint64_t* b, uint32_t n) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(sa(b)), "r"(n) : "memory");
 }
+// A barrier's memory is reused for a new barrier only after the old one is
+// invalidated (init on a valid mbarrier object is undefined).
+__device__ __forceinline__ void bar_inval(uint64_t* b) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(sa(b)) : "memory");
+}
 __device__ __forceinline__ void bar_expect_tx(uint64_t* b, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(sa(b)), "r"(bytes) : "memory");
 }
@@ -29,12 +34,18 @@ __device__ __forceinline__ bool bar_try(uint64_t* b, uint32_t parity) {
   return ok != 0;
 }
 constexpr long long kSpinCycles = 4000000000LL;  // ~2 s at 2 GHz
-__device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t parity, uint32_t* err) {
+// After an earlier wait of the same launch gave up, the remaining waits use
+// this short limit (~1 ms): every wait still runs, so no CTA leaves while a
+// peer may write into its shared memory, but the launch ends promptly.
+constexpr long long kSpinCyclesAfterError = 2000000LL;
+// `site` (a bit above kErrTimeout) records which wait gave up.
+__device__ __forceinline__ bool bar_wait(uint64_t* b, uint32_t parity, uint32_t* err, long long lim = kSpinCycles,
+                                         uint32_t site = 0) {
   if (bar_try(b, parity)) return true;
   const long long t0 = clock64();
   while (!bar_try(b, parity)) {
-    if (clock64() - t0 > kSpinCycles) {
-      atomicOr(err, kErrTimeout);
+    if (clock64() - t0 > lim) {
+      atomicOr(err, kErrTimeout | site);
       return false;
     }
   }
@@ -110,12 +121,13 @@ __device__ __forceinline__ bool bar_try_cluster(uint64_t* b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-__device__ __forceinline__ bool bar_wait_cluster(uint64_t* b, uint32_t parity, uint32_t* err) {
+__device__ __forceinline__ bool bar_wait_cluster(uint64_t* b, uint32_t parity, uint32_t* err,
+                                                 long long lim = kSpinCycles, uint32_t site = 0) {
   if (bar_try_cluster(b, parity)) return true;
   const long long t0 = clock64();
   while (!bar_try_cluster(b, parity)) {
-    if (clock64() - t0 > kSpinCycles) {
-      atomicOr(err, kErrTimeout);
+    if (clock64() - t0 > lim) {
+      atomicOr(err, kErrTimeout | site);
       return false;
     }
   }

@@ -277,12 +277,20 @@ struct Ctrl {
   // fused decode's grid barrier, one ticket counter per element type: the
   // arrivals of all calls so far (zeroed by gsi_workspace_init, never reset)
   unsigned long long ticket[2];
-  // the single-token decode's grid barrier (grid projection), per element type
+  // the single-token decode's call numbers (the grid projection's epochs),
+  // per element type; also numbers the persistent stack kernel's launches
   unsigned long long ticket1[2];
-  uint32_t pad[52];
+  // the persistent stack kernel's arrivals at its barriers between maps
+  unsigned long long arrive[2];
+  uint32_t pad[48];
 };
 static_assert(sizeof(Ctrl) == 256, "Ctrl is 256 bytes");
 
 constexpr uint32_t kErrTimeout = 1;
+// Which bounded wait gave up (bits above kErrTimeout, or-ed into the error
+// word of the single-token and stack decode kernels).
+constexpr uint32_t kWaitV = 1u << 4, kWaitGram = 1u << 5, kWaitM = 1u << 6, kWaitPartials = 1u << 7,
+                   kWaitGathered = 1u << 8, kWaitShares = 1u << 9, kWaitRing = 1u << 10, kWaitSlices = 1u << 11,
+                   kWaitGrid = 1u << 12;
 
 }  // namespace gsi

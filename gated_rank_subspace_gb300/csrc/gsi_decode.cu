@@ -47,6 +47,11 @@
 //              L2 prefetch of the segments ahead of the rings was measured
 //              slower at every distance tried.)
 //
+// The persistent stack kernel runs this call for each map of a list in one
+// launch (the maps of a layer, or of several layers), with a grid barrier
+// between consecutive maps; a CTA sets up the next map's barriers and weight
+// copies while the rest of the grid finishes the current map.
+//
 // Every wait is bounded (~2 s of clock): on expiry the workspace error word
 // is set and the kernel carries on to its end without further waits on that
 // barrier.  There are no float atomics; every sum has one fixed order.
@@ -58,96 +63,100 @@
 
 namespace gsi {
 
+// One map's call, split so that a kernel can run one call (decode_kernel) or
+// a list of calls (stack_decode_kernel):
+//   decode_init_bars    mbarriers and the exchanges' byte counts;
+//   decode_issue_copies the weight copies (V slab rows, Gram slice, M rows);
+//   decode_prefetch_l2  this CTA's share of another map's weights into L2;
+//   decode_run          everything after the dependency wait.
 // NV: 16-byte vectors of a V / M row per lane (1: a row of at most 512 bytes,
 // 2: up to 1 KB, e.g. k = 320 or 512 in bf16).
-template <class E, int NV>
-__global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) {
-  constexpr int PV = E::kPerVec;
-  constexpr int CS = kDecodeCluster;
+
+struct DecodeBars {
+  uint64_t* vbar;   // [NW] V rows of warp w
+  uint64_t* gbar;   // Gram slice
+  uint64_t* mbar;   // M rows
+  uint64_t* xbar;   // every rank's partial g and ||x||^2
+  uint64_t* qbar;   // every rank's Gram and norm shares
+  uint64_t* gxbar;  // g and ||x||^2 gathered from the ranks
+  uint64_t* ring;   // [NW][sw] W segments
+  uint32_t* words;  // [kDecodeCtaWords] CTA words
+  __device__ __forceinline__ explicit DecodeBars(unsigned char* smem) {
+    constexpr int NW = kApplyThreads / 32;
+    vbar = reinterpret_cast<uint64_t*>(smem);
+    gbar = vbar + NW;
+    mbar = vbar + NW + 1;
+    xbar = vbar + NW + 2;
+    qbar = vbar + NW + 3;
+    gxbar = vbar + NW + 4;
+    ring = vbar + NW + kDecodeBars;
+    words = reinterpret_cast<uint32_t*>(smem + kDecodeWordsOff);
+  }
+};
+
+// One barrier per thread; the exchanges' byte counts are known now: every
+// rank pushes the receiver's columns of its partial g and its ||x||^2, and
+// two shares per warp; the gathered g and ||x||^2 are k + 1 floats.  The
+// caller synchronises the block before any barrier is used.  `reinit`: the
+// barriers of the previous call (quiescent: every copy and push into them
+// has completed) are invalidated first.
+__device__ __forceinline__ void decode_init_bars(const DecodeMap& m, unsigned char* smem, int tid, int rank,
+                                                 bool reinit = false) {
   constexpr int NW = kApplyThreads / 32;
-  constexpr unsigned FULL = 0xffffffffu;
-  extern __shared__ __align__(128) unsigned char smem[];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int rank = int(cg::this_cluster().block_rank());
-  // one instantiation for both projection forms: the four maps of a layer
-  // then run the same code, which stays in the instruction cache
-  const bool grid_proj = a.grid != 0;
-  const int k = a.k;
-  const int64_t d = a.d, d_out = a.d_out;
-  const int mrow_b = k * E::kBytes;  // bytes of a V / M row
-  const int nvec = mrow_b / 16;      // 16-byte vectors of such a row (<= 32 NV)
-  const int nf4 = k >> 2;            // float4 groups of g
-  const int64_t row_b = d * E::kBytes;
-
-  const int64_t r0 = int64_t(blockIdx.x) * a.rpc;  // this CTA's output rows
-  const int nrows = r0 >= d_out ? 0 : int(d_out - r0 < a.rpc ? d_out - r0 : a.rpc);
-  const int64_t v0 = int64_t(grid_proj ? int(blockIdx.x) : rank) * a.vr;  // this CTA's V rows
-  const int vn = v0 >= d ? 0 : int(d - v0 < a.vr ? d - v0 : a.vr);
-  const int wr0 = warp * a.rw;                     // this warp's rows of the slab
-  const int wrn = vn - wr0 < 0 ? 0 : (vn - wr0 < a.rw ? vn - wr0 : a.rw);
-  const int c0 = rank * a.ks, c1 = min(k, c0 + a.ks);  // this rank's Gram rows
-
-  uint64_t* vbar = reinterpret_cast<uint64_t*>(smem);  // [NW] V rows of warp w
-  uint64_t* gbar = vbar + NW;                          // Gram slice
-  uint64_t* mbar = vbar + NW + 1;                      // M rows
-  uint64_t* xbar = vbar + NW + 2;                      // every rank's partial g and ||x||^2
-  uint64_t* qbar = vbar + NW + 3;                      // every rank's Gram and norm shares
-  uint64_t* gxbar = vbar + NW + 4;                     // g and ||x||^2 gathered from the ranks
-  uint64_t* ring = vbar + NW + kDecodeBars;            // [NW][sw] W segments
-  float* gfull = reinterpret_cast<float*>(smem + a.off_g);  // [k]
-  float* inx = gfull + k;                                   // [CS] ||x||^2 partials
-  float* qin = inx + CS;                                    // [CS][NW] g^T G g shares
-  float* nin = qin + CS * NW;                               // [CS][NW] ||g||^2 shares
-  float* nx2 = nin + CS * NW;                               // [1]
-  uint32_t* sepoch = reinterpret_cast<uint32_t*>(nx2 + 1);  // [1] grid projection: this call's epoch
-  float* xw = nx2 + 4;                                      // [NW][32] token elements of each warp
-  float* ybuf = reinterpret_cast<float*>(smem + a.off_y);   // [rpc] y = M g
-  float* inbox = reinterpret_cast<float*>(smem + a.off_in); // [CS][ks] partial-g slices; later the slow token
-  const float* gram_s = reinterpret_cast<const float*>(smem + a.off_gram);  // [ks][k]
-  unsigned char* Vs = smem + a.off_v;                       // V slab, then the W rings
-  unsigned char* Ms = smem + a.off_m;                       // M rows
-  float* red = reinterpret_cast<float*>(smem + a.off_red);  // warp w's partial at w * red_stride
-
-  // ---- prologue: weights only (may overlap the previous kernel's tail)
-  // Grid projection: this CTA's ticket, taken before the next kernel of the
-  // stream may start, numbers the call: every CTA of call e takes one of the
-  // tickets [(e - 1) n, e n), n = the grid size, so epoch e = ticket / n + 1
-  // is known to all of them without a barrier.
-  if (grid_proj && tid == 0) *sepoch = uint32_t(atomicAdd(a.ticket, 1ull) / gridDim.x) + 1u;
-  // one barrier per thread; the exchanges' byte counts are known now: every
-  // rank pushes the receiver's columns of its partial g and its ||x||^2, and
-  // two shares per warp; the gathered g and ||x||^2 are k + 1 floats
-  if (tid < NW + kDecodeBars + NW * a.sw) {
-    bar_init(&vbar[tid], 1);
-    if (tid == NW + 2) bar_expect_tx(xbar, uint32_t(CS * ((c1 > c0 ? c1 - c0 : 0) + 1) * 4));
-    if (tid == NW + 3) bar_expect_tx(qbar, uint32_t(CS * NW * 2 * 4));
-    if (tid == NW + 4) bar_expect_tx(gxbar, uint32_t((k + 1) * 4));
+  constexpr int CS = kDecodeCluster;
+  const DecodeBars b(smem);
+  const int c0 = rank * m.ks, c1 = min(m.k, c0 + m.ks);
+  if (tid < NW + kDecodeBars + NW * kDecodeMaxStages) {
+    if (reinit) bar_inval(&b.vbar[tid]);
+    bar_init(&b.vbar[tid], 1);
+    if (tid == NW + 2) bar_expect_tx(b.xbar, uint32_t(CS * ((c1 > c0 ? c1 - c0 : 0) + 1) * 4));
+    if (tid == NW + 3) bar_expect_tx(b.qbar, uint32_t(CS * NW * 2 * 4));
+    if (tid == NW + 4) bar_expect_tx(b.gxbar, uint32_t((m.k + 1) * 4));
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  __syncthreads();
-  pdl_launch_dependents();
+}
+
+// Weight copies of one call (after decode_init_bars and a block barrier):
+// each warp its own rows of the rank's V slab, then the Gram slice and the
+// CTA's M rows (unless they wait for the consumed V slab: m_late).
+template <class E>
+__device__ __forceinline__ void decode_issue_copies(const DecodeMap& m, unsigned char* smem, int tid, int lane,
+                                                    int warp, int rank) {
+  const DecodeBars b(smem);
+  const int mrow_b = m.k * E::kBytes;
+  const int64_t r0 = int64_t(blockIdx.x) * m.rpc;
+  const int nrows = r0 >= m.d_out ? 0 : int(m.d_out - r0 < m.rpc ? m.d_out - r0 : m.rpc);
+  const int64_t v0 = int64_t(m.grid ? int(blockIdx.x) : rank) * m.vr;
+  const int vn = v0 >= m.d ? 0 : int(m.d - v0 < m.vr ? m.d - v0 : m.vr);
+  const int wr0 = warp * m.rw;
+  const int wrn = vn - wr0 < 0 ? 0 : (vn - wr0 < m.rw ? vn - wr0 : m.rw);
+  const int c0 = rank * m.ks, c1 = min(m.k, c0 + m.ks);
   if (lane == 0 && wrn > 0) {
     const uint32_t bytes = uint32_t(wrn) * uint32_t(mrow_b);
-    bar_expect_tx(&vbar[warp], bytes);
-    bulk_g2s(Vs + int64_t(wr0) * mrow_b, static_cast<const char*>(a.V) + (v0 + wr0) * mrow_b, bytes, &vbar[warp]);
+    bar_expect_tx(&b.vbar[warp], bytes);
+    bulk_g2s(smem + m.off_v + int64_t(wr0) * mrow_b, static_cast<const char*>(m.V) + (v0 + wr0) * mrow_b, bytes,
+             &b.vbar[warp]);
   }
-  const bool have_gram = a.gram != nullptr && c1 > c0;
   if (tid == kApplyThreads - 32) {
-    if (have_gram) {
-      const uint32_t bytes = uint32_t(c1 - c0) * uint32_t(k) * 4u;
-      bar_expect_tx(gbar, bytes);
-      bulk_g2s(smem + a.off_gram, a.gram + int64_t(c0) * k, bytes, gbar);
+    if (m.gram != nullptr && c1 > c0) {
+      const uint32_t bytes = uint32_t(c1 - c0) * uint32_t(m.k) * 4u;
+      bar_expect_tx(b.gbar, bytes);
+      bulk_g2s(smem + m.off_gram, m.gram + int64_t(c0) * m.k, bytes, b.gbar);
     }
-    if (nrows > 0 && !a.m_late) {
+    if (nrows > 0 && !m.m_late) {
       const uint32_t bytes = uint32_t(nrows) * uint32_t(mrow_b);
-      bar_expect_tx(mbar, bytes);
-      bulk_g2s(Ms, static_cast<const char*>(a.M) + r0 * mrow_b, bytes, mbar);
+      bar_expect_tx(b.mbar, bytes);
+      bulk_g2s(smem + m.off_m, static_cast<const char*>(m.M) + r0 * mrow_b, bytes, b.mbar);
     }
   }
-  // weights of the next map of a stack, into L2 (this CTA's share)
+}
+
+// This CTA's share of another map's V, M and Gram, into L2.
+__device__ __forceinline__ void decode_prefetch_l2(const char* v, uint64_t vb, const char* mm, uint64_t mb,
+                                                   const char* g, uint64_t gb, int tid) {
   if (tid == 64 || tid == 96 || tid == 128) {
-    const char* base = tid == 64 ? a.next_v : tid == 96 ? a.next_m : a.next_gram;
-    const uint64_t total = tid == 64 ? a.next_v_bytes : tid == 96 ? a.next_m_bytes : a.next_gram_bytes;
+    const char* base = tid == 64 ? v : tid == 96 ? mm : g;
+    const uint64_t total = tid == 64 ? vb : tid == 96 ? mb : gb;
     if (base && total) {
       const uint64_t share = ((total + gridDim.x - 1) / gridDim.x + 15) / 16 * 16;
       const uint64_t off = uint64_t(blockIdx.x) * share;
@@ -157,11 +166,63 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
       }
     }
   }
-  cluster_arrive_relaxed();
-  pdl_wait();
+}
+
+// Everything of one call after the dependency wait: projection, exchanges,
+// decision, apply.  `epoch` tags the grid projection's published words;
+// `lim` bounds every wait (kSpinCycles, or the short limit after an error).
+// Returns with every warp done with its shared memory and its copies.
+template <class E, int NV>
+__device__ __forceinline__ void decode_run(const DecodeMap& m, float eps, float* part_g_ws, float* part_x_ws,
+                                           uint32_t epoch, uint32_t* err, long long lim, int withhold,
+                                           long long poll_cycles, unsigned char* smem) {
+  constexpr int PV = E::kPerVec;
+  constexpr int CS = kDecodeCluster;
+  constexpr int NW = kApplyThreads / 32;
+  constexpr unsigned FULL = 0xffffffffu;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rank = int(cg::this_cluster().block_rank());
+  // one instantiation for both projection forms: the four maps of a layer
+  // then run the same code, which stays in the instruction cache
+  const bool grid_proj = m.grid != 0;
+  const int k = m.k;
+  const int64_t d = m.d, d_out = m.d_out;
+  const int mrow_b = k * E::kBytes;  // bytes of a V / M row
+  const int nvec = mrow_b / 16;      // 16-byte vectors of such a row (<= 32 NV)
+  const int nf4 = k >> 2;            // float4 groups of g
+  const int64_t row_b = d * E::kBytes;
+
+  const int64_t r0 = int64_t(blockIdx.x) * m.rpc;  // this CTA's output rows
+  const int nrows = r0 >= d_out ? 0 : int(d_out - r0 < m.rpc ? d_out - r0 : m.rpc);
+  const int64_t v0 = int64_t(grid_proj ? int(blockIdx.x) : rank) * m.vr;  // this CTA's V rows
+  const int vn = v0 >= d ? 0 : int(d - v0 < m.vr ? d - v0 : m.vr);
+  const int wr0 = warp * m.rw;                     // this warp's rows of the slab
+  const int wrn = vn - wr0 < 0 ? 0 : (vn - wr0 < m.rw ? vn - wr0 : m.rw);
+  const int c0 = rank * m.ks, c1 = min(k, c0 + m.ks);  // this rank's Gram rows
+
+  const DecodeBars b(smem);
+  uint64_t* vbar = b.vbar;
+  uint64_t* gbar = b.gbar;
+  uint64_t* mbar = b.mbar;
+  uint64_t* xbar = b.xbar;
+  uint64_t* qbar = b.qbar;
+  uint64_t* gxbar = b.gxbar;
+  uint64_t* ring = b.ring;
+  float* gfull = reinterpret_cast<float*>(smem + m.off_g);  // [k]
+  float* inx = gfull + k;                                   // [CS] ||x||^2 partials
+  float* qin = inx + CS;                                    // [CS][NW] g^T G g shares
+  float* nin = qin + CS * NW;                               // [CS][NW] ||g||^2 shares
+  float* nx2 = nin + CS * NW;                               // [1]
+  float* xw = nx2 + 4;                                      // [NW][32] token elements of each warp
+  float* ybuf = reinterpret_cast<float*>(smem + m.off_y);   // [rpc] y = M g
+  float* inbox = reinterpret_cast<float*>(smem + m.off_in); // [CS][ks] partial-g slices; later the slow token
+  const float* gram_s = reinterpret_cast<const float*>(smem + m.off_gram);  // [ks][k]
+  unsigned char* Vs = smem + m.off_v;                       // V slab, then the W rings
+  unsigned char* Ms = smem + m.off_m;                       // M rows
+  float* red = reinterpret_cast<float*>(smem + m.off_red);  // warp w's partial at w * red_stride
 
   // ---- projection of this warp's rows
-  const float xv = lane < wrn ? E::load1_cg(a.X, v0 + wr0 + lane) : 0.f;
+  const float xv = lane < wrn ? E::load1_cg(m.X, v0 + wr0 + lane) : 0.f;
   float* xme = xw + warp * 32;
   xme[lane] = xv;
   __syncwarp();
@@ -180,7 +241,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
 #pragma unroll
     for (int e = 0; e < PV; ++e) acc[v][e] = 0.f;
   if (wrn > 0) {
-    __all_sync(FULL, bar_wait(&vbar[warp], 0, a.err));
+    __all_sync(FULL, bar_wait(&vbar[warp], 0, err, lim, kWaitV));
     // rows in batches of 8 / NV: the vectors and token elements are loaded
     // first, then multiplied in row order
     constexpr int RBT = 8 / NV;
@@ -213,7 +274,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
   }
   __syncwarp();
   {
-    float* mine = red + warp * a.red_stride;  // this warp's own (consumed) V rows, or a separate slot
+    float* mine = red + warp * m.red_stride;  // this warp's own (consumed) V rows, or a separate slot
 #pragma unroll
     for (int v = 0; v < NV; ++v)
       if (on[v]) {
@@ -225,32 +286,32 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
     if (lane == 0) mine[k] = xsq;
   }
   __syncthreads();
-  if (a.m_late && nrows > 0 && tid == kApplyThreads - 32) {
+  if (m.m_late && nrows > 0 && tid == kApplyThreads - 32) {
     // the V slab is consumed: the M rows take its place
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     const uint32_t bytes = uint32_t(nrows) * uint32_t(mrow_b);
     bar_expect_tx(mbar, bytes);
-    bulk_g2s(Ms, static_cast<const char*>(a.M) + r0 * mrow_b, bytes, mbar);
+    bulk_g2s(Ms, static_cast<const char*>(m.M) + r0 * mrow_b, bytes, mbar);
   }
 
   cluster_wait();  // every CTA of the cluster runs and has initialised its barriers
   // ---- reduce-scatter inside the cluster: rank q gets every rank's columns
   //      [q ks, (q + 1) ks) of the partial g, and every rank's ||x||^2
-  const int ks = a.ks;
+  const int ks = m.ks;
   for (int c = tid; c < k; c += kApplyThreads) {
     float s = red[c];
 #pragma unroll
-    for (int w = 1; w < NW; ++w) s += red[w * a.red_stride + c];
+    for (int w = 1; w < NW; ++w) s += red[w * m.red_stride + c];
     const int q = c / ks;
     st_async_f32(map_rank(sa(inbox + rank * ks + (c - q * ks)), q), s, map_rank(sa(xbar), q));
   }
   if (tid < CS) {
     float s = red[k];
 #pragma unroll
-    for (int w = 1; w < NW; ++w) s += red[w * a.red_stride + k];
+    for (int w = 1; w < NW; ++w) s += red[w * m.red_stride + k];
     st_async_f32(map_rank(sa(inx + rank), tid), s, map_rank(sa(xbar), tid));
   }
-  __all_sync(FULL, bar_wait_cluster(xbar, 0, a.err));
+  __all_sync(FULL, bar_wait_cluster(xbar, 0, err, lim, kWaitPartials));
   // ---- this rank's slice of g (rank 0: also ||x||^2), summed over the ranks
   //      in rank order -- grid projection: then over the clusters, through
   //      epoch-tagged words -- and pushed to every rank of the cluster
@@ -261,16 +322,15 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
     for (int r = 0; r < CS; ++r) s += xlane ? inx[r] : inbox[r * ks + tid];
     if (grid_proj) {
       const int cl = int(blockIdx.x) / CS, ncl = int(gridDim.x) / CS;
-      const uint32_t epoch = *sepoch;
-      unsigned long long* src = xlane ? reinterpret_cast<unsigned long long*>(a.part_x)
-                                      : reinterpret_cast<unsigned long long*>(a.part_g) + c0 + tid;
+      unsigned long long* src = xlane ? reinterpret_cast<unsigned long long*>(part_x_ws)
+                                      : reinterpret_cast<unsigned long long*>(part_g_ws) + c0 + tid;
       const int64_t stride = xlane ? 1 : k;  // [ncl][k] slices, [ncl] norms
-      if (!(a.dbg_withhold && cl == 0)) st_relaxed_u64(src + cl * stride, (uint64_t(epoch) << 32) | __float_as_uint(s));
+      if (!(withhold && cl == 0)) st_relaxed_u64(src + cl * stride, (uint64_t(epoch) << 32) | __float_as_uint(s));
       // every cluster's word, polled until it carries this call's epoch
       // (bounded), added in cluster order
       float v[kDecodeMaxClusters];
       uint32_t pending = (1u << ncl) - 1u;
-      const long long lim = a.poll_cycles > 0 ? a.poll_cycles : kSpinCycles;
+      const long long plim = poll_cycles > 0 ? poll_cycles : lim;
       const long long t0 = clock64();
       while (pending) {
         unsigned long long w[kDecodeMaxClusters];  // all loads in flight, then the checks
@@ -283,8 +343,8 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
             v[c] = __uint_as_float(uint32_t(w[c]));
             pending &= ~(1u << c);
           }
-        if (pending && clock64() - t0 > lim) {
-          atomicOr(a.err, kErrTimeout);
+        if (pending && clock64() - t0 > plim) {
+          atomicOr(err, kErrTimeout | kWaitSlices);
           break;
         }
       }
@@ -296,15 +356,16 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
     const uint32_t dst = sa(xlane ? nx2 : gfull + c0 + tid), bar = sa(gxbar);
     for (int q = 0; q < CS; ++q) st_async_f32(map_rank(dst, q), s, map_rank(bar, q));
   }
-  __all_sync(FULL, bar_wait_cluster(gxbar, 0, a.err));
+  __all_sync(FULL, bar_wait_cluster(gxbar, 0, err, lim, kWaitGathered));
 
   // ---- every warp: its share of the Gram form (Gram rows c0 + warp,
   //      c0 + warp + NW, ...) and of ||g||^2, pushed to every rank, then
   //      y = M g for its rows (groups of RB rows: RB warp, RB warp + RB NW, ...)
+  const bool have_gram = m.gram != nullptr && c1 > c0;
   {
     float q = 0.f, n = 0.f;
     if (have_gram) {
-      __all_sync(FULL, bar_wait(gbar, 0, a.err));
+      __all_sync(FULL, bar_wait(gbar, 0, err, lim, kWaitGram));
       // lane l takes column groups l, l + 32, ... (clamped loads, masked)
       constexpr int NG = 2 * NV;  // float4 groups of a Gram row per lane (k <= 256 NV)
       const float4* g4 = reinterpret_cast<const float4*>(gfull);
@@ -344,7 +405,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
     }
   }
   if (nrows > 0) {
-    __all_sync(FULL, bar_wait(mbar, 0, a.err));
+    __all_sync(FULL, bar_wait(mbar, 0, err, lim, kWaitM));
     // lane l multiplies column group l of RB rows at a time; the row loads
     // are unconditional (rows past the CTA's last repeat it, lanes past the
     // row's vectors repeat vector 0) and masked afterwards, so all RB are in
@@ -392,7 +453,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
   // ---- the decision, taken by every warp from the same shares in the same
   //      order (lane l adds shares 4l .. 4l + 3 of the rank-major list, then
   //      a butterfly over the lanes)
-  __all_sync(FULL, bar_wait_cluster(qbar, 0, a.err));
+  __all_sync(FULL, bar_wait_cluster(qbar, 0, err, lim, kWaitShares));
   static_assert(CS * NW == 4 * 32, "four shares per lane");
   const float4 q4 = reinterpret_cast<const float4*>(qin)[lane];
   const float4 n4 = reinterpret_cast<const float4*>(nin)[lane];
@@ -400,15 +461,15 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
   const float Nr = (n4.x + n4.y) + (n4.z + n4.w);
   float Q = warp_sum(Qr);
   const float N = warp_sum(Nr);
-  if (!a.gram) Q = N;  // orthonormal basis: ||V g||^2 = ||g||^2
+  if (!m.gram) Q = N;  // orthonormal basis: ||V g||^2 = ||g||^2
   const float xx = *nx2;
   float rr = xx - 2.f * N + Q;
   rr = rr < 0.f ? 0.f : rr;  // keeps NaN
   const float rho = xx == 0.f ? 0.f : sqrtf(rr / xx);
-  const bool slow = !(rho < a.eps);
+  const bool slow = !(rho < eps);
   if (blockIdx.x == 0 && tid == 0) {
-    if (a.rho) a.rho[0] = rho;
-    a.flags[0] = uint8_t(slow ? 1 : 0);
+    if (m.rho) m.rho[0] = rho;
+    m.flags[0] = uint8_t(slow ? 1 : 0);
   }
 
   // ---- apply
@@ -417,19 +478,19 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
     __syncwarp();
     const int rbw = nrows <= NW * 4 ? 4 : (nrows <= NW * 8 || NV > 1) ? 8 : 16;
     for (int rb = warp * rbw; rb < nrows; rb += NW * rbw)
-      if (lane < rbw && rb + lane < nrows) a.Y[r0 + rb + lane] = ybuf[rb + lane];
+      if (lane < rbw && rb + lane < nrows) m.Y[r0 + rb + lane] = ybuf[rb + lane];
     return;
   }
   if (nrows == 0) return;
   // Slow token: the V slab, the partials and the M rows are consumed, so the
   // W rings take their space; the token goes where the inboxes were.
-  const int seg_b = a.seg_bytes, SW = a.sw;
+  const int seg_b = m.seg_bytes, SW = m.sw;
   const int nseg = int((row_b + seg_b - 1) / seg_b);
   const int my_rows = warp < nrows ? (nrows - warp + NW - 1) / NW : 0;
   const int items = my_rows * nseg;
   unsigned char* wring = Vs + int64_t(warp) * SW * seg_b;
   uint64_t* wfull = ring + warp * SW;
-  const char* wbase = static_cast<const char*>(a.W) + r0 * row_b;
+  const char* wbase = static_cast<const char*>(m.W) + r0 * row_b;
   // item q of this warp: segment q % nseg of its row q / nseg (CTA row
   // warp + (q / nseg) * NW), in ring slot q % SW; issuer and consumer step
   // through the items with counters
@@ -454,14 +515,14 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
   }
   unsigned char* xst = reinterpret_cast<unsigned char*>(inbox);
   for (int64_t e = tid; e < row_b / 16; e += kApplyThreads)
-    reinterpret_cast<uint4*>(xst)[e] = ld_cg_v4(static_cast<const char*>(a.X) + e * 16);
+    reinterpret_cast<uint4*>(xst)[e] = ld_cg_v4(static_cast<const char*>(m.X) + e * 16);
   __syncthreads();
   float acc0 = 0.f, acc1 = 0.f;
   int c_slot = 0, c_seg = 0, c_row = 0;
   uint32_t c_ph = 0;
   int i = 0;
   for (; i < items; ++i) {
-    if (!__all_sync(FULL, bar_wait(&wfull[c_slot], c_ph, a.err))) break;
+    if (!__all_sync(FULL, bar_wait(&wfull[c_slot], c_ph, err, lim, kWaitRing))) break;
     const int64_t off = int64_t(c_seg) * seg_b;
     const int nv = int(min(int64_t(seg_b), row_b - off) / 16);
     const unsigned char* segp = wring + c_slot * seg_b;
@@ -497,7 +558,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
     }
     if (++c_seg == nseg) {
       const float sum = warp_sum(acc0 + acc1);
-      if (lane == 0) a.Y[r0 + warp + int64_t(c_row) * NW] = sum;
+      if (lane == 0) m.Y[r0 + warp + int64_t(c_row) * NW] = sum;
       acc0 = acc1 = 0.f;
       c_seg = 0;
       ++c_row;
@@ -506,12 +567,127 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
   // after an expired wait: wait (bounded) for this warp's copies still in flight
   if (lane == 0)
     for (int q = i; q < issued; ++q) {
-      bar_wait(&wfull[c_slot], c_ph, a.err);
+      bar_wait(&wfull[c_slot], c_ph, err, lim, kWaitRing);
       if (++c_slot == SW) {
         c_slot = 0;
         c_ph ^= 1u;
       }
     }
+}
+
+template <class E, int NV>
+__global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rank = int(cg::this_cluster().block_rank());
+  const DecodeBars b(smem);
+  // ---- prologue: weights only (may overlap the previous kernel's tail)
+  // Grid projection: this CTA's ticket, taken before the next kernel of the
+  // stream may start, numbers the call: every CTA of call e takes one of the
+  // tickets [(e - 1) n, e n), n = the grid size, so epoch e = ticket / n + 1
+  // is known to all of them without a barrier.  (The word carries the call
+  // number in its upper 24 bits and the map's place in a launch, here 1, in
+  // the lower 8, as the persistent stack kernel's do.)
+  if (a.m.grid && tid == 0) b.words[0] = ((uint32_t(atomicAdd(a.ticket, 1ull) / gridDim.x) + 1u) << 8) | 1u;
+  decode_init_bars(a.m, smem, tid, rank);
+  __syncthreads();
+  pdl_launch_dependents();
+  decode_issue_copies<E>(a.m, smem, tid, lane, warp, rank);
+  // weights of the next map of a stack, into L2 (this CTA's share)
+  decode_prefetch_l2(a.next_v, a.next_v_bytes, a.next_m, a.next_m_bytes, a.next_gram, a.next_gram_bytes, tid);
+  cluster_arrive_relaxed();
+  pdl_wait();
+  decode_run<E, NV>(a.m, a.eps, a.part_g, a.part_x, b.words[0], a.err, kSpinCycles, a.dbg_withhold, a.poll_cycles,
+                    smem);
+}
+
+// The persistent stack kernel: the calls of a list of maps in order, in one
+// launch.  Map i + 1's barriers and weight copies are set up as soon as the
+// CTA has finished map i (while the other CTAs finish theirs), and the CTAs
+// then meet at a grid barrier on the workspace's arrival counter before
+// map i + 1 reads its token.  The counter only grows: an episode is the n
+// arrivals after a multiple of n (n the grid size), and a CTA's returning
+// add tells it the episode's target.  Episodes cannot overlap: a CTA
+// arrives for map i + 1 only after the episode of map i is complete, and a
+// launch's first arrival comes after its dependency wait on the previous
+// kernel of the stream.  The launch number (from the ticket the single-token
+// kernel also draws, so that grid-projection epochs never repeat) and the
+// map's place give each grid-projection call its epoch.  After a wait has
+// given up anywhere in the grid (the error word, read after each barrier),
+// the remaining waits use a short limit.
+template <class E, int NV>
+__global__ void __launch_bounds__(kApplyThreads, 1) stack_decode_kernel(const __grid_constant__ StackDecodeArgs a) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int rank = int(cg::this_cluster().block_rank());
+  const DecodeBars b(smem);
+  const int n = a.n_maps;
+  if (tid == 0) {
+    b.words[0] = uint32_t(atomicAdd(a.ticket, 1ull) / gridDim.x) + 1u;  // launch number
+    b.words[1] = 0u;                                                     // error seen
+  }
+  decode_init_bars(a.maps[0], smem, tid, rank);
+  __syncthreads();
+  const uint32_t launch = b.words[0];
+  decode_issue_copies<E>(a.maps[0], smem, tid, lane, warp, rank);
+  if (n > 1) {
+    const DecodeMap& nx = a.maps[1];
+    decode_prefetch_l2(static_cast<const char*>(nx.V), uint64_t(nx.d) * nx.k * E::kBytes,
+                       static_cast<const char*>(nx.M), uint64_t(nx.d_out) * nx.k * E::kBytes,
+                       reinterpret_cast<const char*>(nx.gram), nx.gram ? uint64_t(nx.k) * nx.k * 4 : 0, tid);
+  }
+  cluster_arrive_relaxed();
+  if (n == 1) pdl_launch_dependents();
+  pdl_wait();
+  long long lim = kSpinCycles;
+  for (int i = 0; i < n; ++i) {
+    const DecodeMap& m = a.maps[i];
+    decode_run<E, NV>(m, a.eps, a.part_g, a.part_x, (launch << 8) | uint32_t(i + 1), a.err, lim, 0, 0, smem);
+    if (i + 1 == n) break;
+    // every warp has written its rows of map i and is done with shared
+    // memory; its generic writes are ordered before the next map's copies
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    unsigned long long target = 0;
+    if (tid == 0) {
+      __threadfence();
+      const unsigned long long mine = atomicAdd(a.arrive, 1ull);
+      target = (mine / gridDim.x + 1) * gridDim.x;
+    }
+    // map i + 1: barriers and weight copies, then the L2 prefetch of map i + 2
+    const DecodeMap& m1 = a.maps[i + 1];
+    decode_init_bars(m1, smem, tid, rank, true);
+    __syncthreads();
+    decode_issue_copies<E>(m1, smem, tid, lane, warp, rank);
+    if (i + 2 < n) {
+      const DecodeMap& nx = a.maps[i + 2];
+      decode_prefetch_l2(static_cast<const char*>(nx.V), uint64_t(nx.d) * nx.k * E::kBytes,
+                         static_cast<const char*>(nx.M), uint64_t(nx.d_out) * nx.k * E::kBytes,
+                         reinterpret_cast<const char*>(nx.gram), nx.gram ? uint64_t(nx.k) * nx.k * 4 : 0, tid);
+    }
+    cluster_arrive_relaxed();
+    if (tid == 0) {
+      // every CTA has finished map i (bounded); then the grid's error word
+      if (ld_acquire_gpu(a.arrive) < target) {
+        const long long t0 = clock64();
+        while (ld_acquire_gpu(a.arrive) < target) {
+          if (clock64() - t0 > lim) {
+            atomicOr(a.err, kErrTimeout | kWaitGrid);
+            break;
+          }
+        }
+      }
+      b.words[1] = *reinterpret_cast<volatile uint32_t*>(a.err);
+    }
+    if (i + 2 == n) pdl_launch_dependents();
+    __syncthreads();
+    if (b.words[1] != 0u) lim = kSpinCyclesAfterError;
+  }
+  // No CTA leaves while a peer of its cluster may still push into its shared
+  // memory: after a wait has given up, the CTAs of a cluster can be at
+  // different steps of the last call.
+  cluster_arrive_relaxed();
+  cluster_wait();
 }
 
 template <class E, int NV>
@@ -538,18 +714,50 @@ static cudaError_t launch_decode_t(const DecodeArgs& a, const DecodePlan& p, cud
   attr[1].val.clusterDim.z = 1;
   // the grid projection's CTAs poll other clusters' words: co-resident launch
   static int no_coop = 0;
-  return launch_maybe_coop(cfg, attr, 2, p.grid != 0, &no_coop, kern, a);
+  return launch_maybe_coop(cfg, attr, 2, a.m.grid != 0, &no_coop, kern, a);
 }
 
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, gsi_dtype dt, cudaStream_t s) {
-  const bool two = a.k * (dt == GSI_BF16 ? 2 : 4) > 512;  // two 16-byte vectors of a row per lane
+  const bool two = a.m.k * (dt == GSI_BF16 ? 2 : 4) > 512;  // two 16-byte vectors of a row per lane
   if (dt == GSI_BF16) return two ? launch_decode_t<BF16, 2>(a, p, s) : launch_decode_t<BF16, 1>(a, p, s);
   return two ? launch_decode_t<F32, 2>(a, p, s) : launch_decode_t<F32, 1>(a, p, s);
 }
 
-template <class E>
-static int decode_max_clusters_t(size_t smem) {
-  auto kern = decode_kernel<E, 1>;
+template <class E, int NV>
+static cudaError_t launch_stack_t(const StackDecodeArgs& a, size_t smem, int ncta, cudaStream_t s) {
+  auto kern = stack_decode_kernel<E, NV>;
+  static size_t smem_set = 0;
+  if (smem > smem_set) {
+    cudaError_t e = set_kernel_smem(kern, smem);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1)) != cudaSuccess) return e;
+    smem_set = smem;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(ncta));
+  cfg.blockDim = dim3(kApplyThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[3];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kDecodeCluster;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  // the CTAs meet at grid barriers between maps: co-resident launch
+  static int no_coop = 0;
+  return launch_maybe_coop(cfg, attr, 2, true, &no_coop, kern, a);
+}
+
+cudaError_t launch_stack_decode(const StackDecodeArgs& a, size_t smem, int ncta, int nv, gsi_dtype dt,
+                                cudaStream_t s) {
+  if (dt == GSI_BF16) return nv == 2 ? launch_stack_t<BF16, 2>(a, smem, ncta, s) : launch_stack_t<BF16, 1>(a, smem, ncta, s);
+  return nv == 2 ? launch_stack_t<F32, 2>(a, smem, ncta, s) : launch_stack_t<F32, 1>(a, smem, ncta, s);
+}
+
+template <class K>
+static int max_clusters_of(K kern, size_t smem) {
   if (set_kernel_smem(kern, smem) != cudaSuccess ||
       cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) {
     cudaGetLastError();
@@ -575,7 +783,13 @@ static int decode_max_clusters_t(size_t smem) {
 }
 
 int decode_max_clusters(size_t smem, gsi_dtype dt) {
-  return dt == GSI_BF16 ? decode_max_clusters_t<BF16>(smem) : decode_max_clusters_t<F32>(smem);
+  return dt == GSI_BF16 ? max_clusters_of(decode_kernel<BF16, 1>, smem) : max_clusters_of(decode_kernel<F32, 1>, smem);
+}
+
+int stack_max_clusters(size_t smem, gsi_dtype dt, int nv) {
+  if (dt == GSI_BF16)
+    return nv == 2 ? max_clusters_of(stack_decode_kernel<BF16, 2>, smem) : max_clusters_of(stack_decode_kernel<BF16, 1>, smem);
+  return nv == 2 ? max_clusters_of(stack_decode_kernel<F32, 2>, smem) : max_clusters_of(stack_decode_kernel<F32, 1>, smem);
 }
 
 }  // namespace gsi

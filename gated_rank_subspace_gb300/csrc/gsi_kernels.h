@@ -73,26 +73,33 @@ struct DecideArgs {
 };
 
 
-// Single-token decode kernel arguments (see gsi_decode.cu): one call of the
-// gated map for one token, decide and apply, in one launch.
-struct DecodeArgs {
+// One map's single-token call (see gsi_decode.cu): the operands and the
+// DecodePlan geometry and shared-memory offsets.
+struct DecodeMap {
   const void* X;        // 1 x d token
   const void* W;        // d_out x d
   const void* V;        // d x k
   const void* M;        // d_out x k
   const float* gram;    // k x k, or null (orthonormal basis)
-  int64_t d, d_out;
-  int k;
-  float eps;
   float* Y;             // 1 x d_out
   uint8_t* flags;       // 1
   float* rho;           // 1, or null
-  // geometry and shared-memory offsets (DecodePlan)
+  int64_t d, d_out;
+  int k;
   int vr, rw, rpc, ks, seg_bytes, sw, red_stride, m_late;
   int off_g, off_y, off_in, off_gram, off_red, off_v, off_m;
-  // grid projection: each cluster's partial g [clusters][k] and ||x||^2
-  // [clusters], published before the grid barrier on the ticket counter
+  // grid projection: each cluster's slice of g is published as epoch-tagged
+  // words in the workspace; 0: the cluster projection
   int grid;
+};
+
+// Single-token decode kernel arguments: one call of the gated map for one
+// token, decide and apply, in one launch.
+struct DecodeArgs {
+  DecodeMap m;
+  float eps;
+  // grid projection: each cluster's partial g [clusters][k] and ||x||^2
+  // [clusters] as epoch-tagged words; the call's epoch comes from a ticket
   float* part_g;
   float* part_x;
   unsigned long long* ticket;
@@ -110,10 +117,33 @@ struct DecodeArgs {
   long long poll_cycles;
 };
 
+// Persistent stack decode: one launch runs up to kStackMaxMaps single-token
+// calls in list order, the calls separated by a grid barrier (map i + 1
+// reads its token only after every CTA has finished map i).  The maps share
+// one element type and row width (one kernel instantiation).
+constexpr int kStackMaxMaps = 112;
+
+struct StackDecodeArgs {
+  DecodeMap maps[kStackMaxMaps];
+  int n_maps;
+  float eps;
+  float* part_g;                // as DecodeArgs
+  float* part_x;
+  unsigned long long* ticket;   // shared with the single-token kernel: numbers the launch
+  unsigned long long* arrive;   // arrivals at the barriers between maps
+  uint32_t* err;
+};
+
 cudaError_t launch_decode(const DecodeArgs& a, const DecodePlan& p, gsi_dtype dt, cudaStream_t s);
+// The persistent stack kernel with `smem` bytes of shared memory (the
+// largest plan of its maps) and `ncta` CTAs (the single-token kernel's grid).
+cudaError_t launch_stack_decode(const StackDecodeArgs& a, size_t smem, int ncta, int nv, gsi_dtype dt,
+                                cudaStream_t s);
 // Co-resident kDecodeCluster-CTA clusters of the single-token decode kernel
 // with `smem` bytes of shared memory per CTA; 0 if none.
 int decode_max_clusters(size_t smem, gsi_dtype dt);
+// The same for the persistent stack kernel (nv vectors of a row per lane).
+int stack_max_clusters(size_t smem, gsi_dtype dt, int nv);
 
 // Tensor-core path (bf16, prefill-sized T).  All pointers are device pointers;
 // Vt, G, Gbf, Gfast, Xslow and idx live in the call's workspace.
@@ -139,6 +169,9 @@ struct TensorArgs {
 };
 
 cudaError_t launch_tensor_path(const TensorArgs& t, cudaStream_t s);
+// M = W V_k (bf16) and the Gram on the tensor cores; Vt: k x d bf16 scratch.
+cudaError_t launch_image_tc(const void* W, const void* V, void* M, float* gram, int64_t d, int64_t d_out, int64_t k,
+                            uint16_t* Vt, uint32_t* err, cudaStream_t s);
 
 // Sets the calling thread's gsi_last_error() message and returns s.
 gsi_status record_error(gsi_status s, const char* msg);

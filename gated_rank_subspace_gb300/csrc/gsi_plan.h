@@ -253,6 +253,9 @@ constexpr int kDecodeCluster = 16;
 constexpr int kDecodeMaxStages = 6;
 constexpr int kDecodeBars = 5;  // Gram, M, partials, shares, gathered g
 constexpr int kDecodeMaxClusters = 16;  // grid projection: clusters whose slices are polled
+constexpr int kDecodeCtaWords = 2;      // 32-bit words after the mbarriers
+// byte offset of those words
+constexpr int kDecodeWordsOff = (kApplyThreads / 32 + kDecodeBars + kApplyThreads / 32 * kDecodeMaxStages) * 8;
 
 struct DecodePlan {
   int vr, rw, rpc, ks, seg_bytes, sw, red_stride, m_late, grid;
@@ -280,7 +283,9 @@ inline DecodePlan plan_decode(int64_t d, int64_t d_out, int64_t k, int es, int n
   p.rpc = int(cdiv(d_out, ncta));
   p.ks = int(cdiv(k, kDecodeCluster));
   p.seg_bytes = int(row_b < kSegBytes ? row_b : kSegBytes);
-  const size_t bars = size_t(nw + kDecodeBars + nw * kDecodeMaxStages) * 8;
+  // mbarriers, then two CTA words (the call's epoch or the launch number, and
+  // the persistent kernel's error flag) at a fixed offset for every map
+  const size_t bars = size_t(nw + kDecodeBars + nw * kDecodeMaxStages) * 8 + kDecodeCtaWords * 4;
   size_t off = (bars + 127) & ~size_t(127);
   auto take = [&](size_t bytes) {
     const size_t at = off;

@@ -162,6 +162,7 @@ struct TcArgs {
   uint32_t* err;
   int ksplit;              // K is cut into ksplit slices (grid z); 0 or 1: none
   int64_t c_split;         // elements between the slices' outputs
+  int c_bf16;              // C is bf16 (rounded to nearest even), not float32
 };
 
 constexpr int kBM = 128, kBK = 64;
@@ -284,8 +285,30 @@ __global__ void __launch_bounds__(128, 1)
     const int64_t my_orow = my_r < rows ? (a.row_map ? int64_t(__ldcg(&a.row_map[my_r])) : int64_t(my_r)) : 0;
     for (int i = 0; i < 32 && r_base + i < rows; ++i) {
       const int64_t orow = __shfl_sync(0xffffffffu, my_orow, i);
-      float* crow = a.C + int64_t(blockIdx.z) * a.c_split + orow * a.ldc + int64_t(n_tile) * BN;
+      const int64_t cofs = int64_t(blockIdx.z) * a.c_split + orow * a.ldc + int64_t(n_tile) * BN;
       const float* srow = st + i * LD;
+      if (a.c_bf16) {
+        // four columns a lane: 8-byte stores of bf16 pairs (ldc and the
+        // column offsets are multiples of 4 elements)
+        __nv_bfloat16* crow = reinterpret_cast<__nv_bfloat16*>(a.C) + cofs;
+        for (int q = lane; q < BN / 4; q += 32) {
+          const int col = n_tile * BN + 4 * q;
+          const float4 v = *reinterpret_cast<const float4*>(srow + 4 * q);
+          if (col + 4 <= a.N) {
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
+            uint2 u;
+            u.x = *reinterpret_cast<const uint32_t*>(&lo);
+            u.y = *reinterpret_cast<const uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(crow + 4 * q) = u;
+          } else {
+            const float f[4] = {v.x, v.y, v.z, v.w};
+            for (int e2 = 0; e2 < 4; ++e2)
+              if (col + e2 < a.N) crow[4 * q + e2] = __float2bfloat16_rn(f[e2]);
+          }
+        }
+        continue;
+      }
+      float* crow = a.C + cofs;
       for (int q = lane; q < BN / 4; q += 32) {
         const int col = n_tile * BN + 4 * q;
         if (vec && col + 4 <= a.N) {
@@ -550,6 +573,39 @@ static cudaError_t launch_pdl(const void* kern, dim3 grid, dim3 block, size_t sm
   cfg.attrs = at;
   cfg.numAttrs = 1;
   return cudaLaunchKernelExC(&cfg, kern, args);
+}
+
+// Image build on the tensor cores (bf16 maps): V_k^T into the scratch, then
+// M = W V_k as the contraction of W (d_out x d) with V_k^T (k x d), stored in
+// bf16 by the epilogue, and Gram = V_k^T V_k (k x k, float32).  Float32
+// accumulation in TMEM; every output is summed in one fixed order.
+cudaError_t launch_image_tc(const void* W, const void* V, void* M, float* gram, int64_t d, int64_t d_out, int64_t k,
+                            uint16_t* Vt, uint32_t* err, cudaStream_t s) {
+  cudaError_t e;
+  {
+    dim3 grid(unsigned(cdiv(k, 32)), unsigned(cdiv(d, 32)));
+    transpose_bf16_kernel<<<grid, dim3(32, 8), 0, s>>>(static_cast<const uint16_t*>(V), Vt, int(d), int(k));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  const int bn = k >= 256 ? 256 : (k >= 128 ? 128 : 64);
+  TcArgs a{};
+  a.rows = int(d_out);
+  a.N = int(k);
+  a.K = int(d);
+  a.C = static_cast<float*>(M);
+  a.ldc = k;
+  a.err = err;
+  a.c_bf16 = 1;
+  if ((e = launch_tc_gemm(W, d_out, Vt, k, int(d), bn, a, s)) != cudaSuccess) return e;
+  if (!gram) return cudaSuccess;
+  TcArgs g{};
+  g.rows = int(k);
+  g.N = int(k);
+  g.K = int(d);
+  g.C = gram;
+  g.ldc = k;
+  g.err = err;
+  return launch_tc_gemm(Vt, k, Vt, k, int(d), bn, g, s);
 }
 
 cudaError_t launch_tensor_path(const TensorArgs& t, cudaStream_t s) {

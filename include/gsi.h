@@ -115,6 +115,19 @@ gsi_status gsi_build_image(const void* W, const void* V, void* M, float* gram,
                            int64_t d, int64_t d_out, int64_t k, gsi_dtype dtype,
                            void* stream);
 
+/* §2.1 image build on the tensor cores.  gsi_build_image_ex computes what
+ * gsi_build_image does; for GSI_BF16 maps with a scratch area it runs on
+ * tcgen05 (V^T formed in the scratch, then M = W V and V^T V as tensor-core
+ * contractions with float32 accumulation in TMEM, M rounded to nearest even
+ * into bf16).  work: device, 256-byte aligned, at least
+ * gsi_build_image_work_bytes(d, k, dtype) bytes (0 for GSI_F32, which keeps
+ * the CUDA-core kernel, as does work == NULL); its first 256 bytes hold an
+ * error word that gsi_workspace_status reads (a bounded wait of the
+ * contraction gave up).  Enqueued on `stream`; allocates nothing. */
+size_t gsi_build_image_work_bytes(int64_t d, int64_t k, gsi_dtype dtype);
+gsi_status gsi_build_image_ex(const void* W, const void* V, void* M, float* gram, int64_t d, int64_t d_out, int64_t k,
+                              gsi_dtype dtype, void* work, size_t work_bytes, void* stream);
+
 /* Bytes of device workspace gsi_linear needs for `map` and T tokens with the
  * given path (host-only arithmetic, no device call).  *bytes is a HOST
  * pointer. */

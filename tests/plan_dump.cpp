@@ -17,11 +17,12 @@ int main() {
         "\"red_stride\": %d, \"m_late\": %d, \"grid\": %d, \"off_g\": %d, \"off_y\": %d, \"off_in\": %d, "
         "\"off_gram\": %d, \"off_red\": %d, \"off_v\": %d, \"off_m\": %d, \"smem\": %zu, "
         "\"nw\": %d, \"cluster\": %d, \"max_stages\": %d, \"bars\": %d, \"max_clusters\": %d, "
-        "\"ws_part_g\": %zu, \"ws_part_x\": %zu, \"ws_total\": %zu}\n",
+        "\"ws_part_g\": %zu, \"ws_part_x\": %zu, \"ws_total\": %zu, \"words_off\": %d, \"words\": %d}\n",
         d, d_out, k, es, ncta, budget, grid, int(p.ok), p.vr, p.rw, p.rpc, p.ks, p.seg_bytes, p.sw, p.red_stride,
         p.m_late, p.grid, p.off_g, p.off_y, p.off_in, p.off_gram, p.off_red, p.off_v, p.off_m, p.smem,
         gsi::kApplyThreads / 32, gsi::kDecodeCluster, gsi::kDecodeMaxStages, gsi::kDecodeBars,
-        gsi::kDecodeMaxClusters, L.part_x - L.part_g, L.total - L.part_x, L.total);
+        gsi::kDecodeMaxClusters, L.part_x - L.part_g, L.total - L.part_x, L.total, gsi::kDecodeWordsOff,
+        gsi::kDecodeCtaWords);
   }
   return 0;
 }

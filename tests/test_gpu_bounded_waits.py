@@ -69,12 +69,12 @@ def test_withheld_slice_times_out_and_recovers(gsi):
     compare(m_in, gm.M, Y2, F2, R2)
 
 
-@pytest.mark.parametrize("shape", [(8200, 520, 64), (32768, 64, 64)])
+@pytest.mark.parametrize("shape", [(8200, 520, 64), (16384, 64, 128)])
 def test_refused_coresident_grid_falls_back(gsi, shape):
     """Launches refused for co-residency: AUTO still runs every call (on a
     kernel that needs no co-resident grid, at the end the two-launch
     streaming kernels) with the same results.  (8200, 520, 64): the
-    single-token kernel's grid projection is refused; (32768, 64, 64): a
+    single-token kernel's grid projection is refused; (16384, 64, 128): a
     sixteenth of V does not fit one CTA, so both single-launch forms need a
     co-resident grid and an explicit fused call reports the refusal."""
     d, d_out, k = shape
@@ -91,7 +91,7 @@ def test_refused_coresident_grid_falls_back(gsi, shape):
             Yc = torch.empty(1, d_out, device="cuda")
             gsi.linear(gm, X[t:t + 1], m_in.eps, Y=Yc, flags=F[t:t + 1], rho=R[t:t + 1], workspace=ws)
             Y[t:t + 1] = Yc
-        if d == 32768:
+        if d == 16384:
             with pytest.raises(gsi.GsiError, match="co-resident"):
                 gsi.linear(gm, X[:1], m_in.eps, workspace=ws, path="fused")
     finally:

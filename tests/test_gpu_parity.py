@@ -55,6 +55,34 @@ def test_image_build(gsi, case):
     assert np.max(np.abs(G - orc.gram(Vn))) <= 1e-5
 
 
+@pytest.mark.parametrize("shape", [(200, 77, 24), (1032, 1000, 136), (5120, 5120, 320), (4096, 16384, 256)])
+def test_image_build_tensor_cores(gsi, shape):
+    """The tcgen05 image build (bf16) against float64 W V_k and V_k^T V_k, and
+    against the CUDA-core build: the same rounding of (differently ordered)
+    float32 sums, so the two M differ by at most one bf16 unit in the last
+    place and their Grams by float32 noise."""
+    d, d_out, k = shape
+    V64 = synth.orthonormal_basis(synth.rng(11, d, k, 2), d, k)
+    m_in = synth.stack_layer(11, d_out, {"qkv": V64}, {"qkv": (d_out, d)}, T=1, f_slow=0.0, roles=("qkv",))[0]
+    W, V = m_in.W.cuda(), m_in.V.cuda()
+    M_tc, G_tc = gsi.build_image(W, V)
+    M_cc, G_cc = gsi.build_image(W, V, tensor_cores=False)
+    torch.cuda.synchronize()
+    Wn, Vn = synth.widen(m_in.W), synth.widen(m_in.V)
+    Mref = orc.image(Wn, Vn)
+    M = synth.widen(M_tc)
+    assert np.linalg.norm(M - Mref) / np.linalg.norm(Mref) <= 4e-3
+    assert np.all(np.abs(M - Mref) <= np.abs(Mref) * 2.0 ** -8 + 1e-5)
+    assert np.max(np.abs(G_tc.cpu().numpy().astype(np.float64) - orc.gram(Vn))) <= 1e-5
+    ulp = np.abs(synth.widen(M_cc)) * 2.0 ** -7 + 1e-30
+    assert np.all(np.abs(M - synth.widen(M_cc)) <= ulp)
+    assert float((G_tc - G_cc).abs().max()) <= 2e-6
+    # the tensor-core build is bitwise reproducible
+    M2, G2 = gsi.build_image(W, V)
+    torch.cuda.synchronize()
+    assert torch.equal(M_tc, M2) and torch.equal(G_tc, G2)
+
+
 # ------------------------------------------------------------------ gate and compaction
 def test_gate_only_config1(gsi):
     m_in = synth.config1()

@@ -101,6 +101,10 @@ def test_plan_invariants(plans):
             assert k % cs == 0 and ncta <= cs * p["max_clusters"], ctx
         # regions in order, 128-byte aligned, no overlap
         bars = (nw + p["bars"] + nw * p["max_stages"]) * 8
+        # the CTA words (call epoch / launch number, error flag) follow the
+        # mbarriers at one offset for every map, before the g area
+        assert p["words_off"] == bars and p["words_off"] % 4 == 0, ctx
+        bars += 4 * p["words"]
         g_bytes = (k + cs + 2 * cs * nw + 4 + nw * 32) * 4
         regions = [("g", p["off_g"], g_bytes), ("y", p["off_y"], p["rpc"] * 4),
                    ("in", p["off_in"], max(cs * p["ks"] * 4, row_b)), ("gram", p["off_gram"], p["ks"] * k * 4)]
@@ -132,8 +136,9 @@ def test_plan_invariants(plans):
         assert p["seg_bytes"] == min(row_b, 4096) and p["seg_bytes"] % 16 == 0, ctx
         assert 2 <= p["sw"] <= p["max_stages"], ctx
         assert p["off_v"] + nw * p["sw"] * p["seg_bytes"] <= p["smem"], ctx
-        # the mbarriers initialised by the kernel (one per thread) fit the bars region
-        assert nw + p["bars"] + nw * p["sw"] <= 256, ctx
+        # the mbarriers initialised by the kernel (one per thread, every ring
+        # slot a map could use) fit the bars region
+        assert nw + p["bars"] + nw * p["max_stages"] <= 256, ctx
         # grid projection: the clusters' epoch-tagged words fit the workspace's
         # partial areas ([clusters][k] and [clusters] 64-bit words)
         if p["grid"]:

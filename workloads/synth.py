@@ -291,3 +291,49 @@ def random_basis_t(config: int, k: int, d: int, salt: int = 0) -> np.ndarray:
     """A seeded random start for basis construction: k x d Gaussian rows
     (orthonormalised by the code under test)."""
     return rng(config, 0, 0, _CAL * 1000 + salt).standard_normal((k, d))
+
+
+def stack_config4(n_layers: int = 40, k: int = 320, pool: int = 64, eps: float = EPS):
+    """40-layer stack of the 13B shapes at k = 320 (bf16), built cheaply.
+
+    Per role: one base weight draw W_base ~ N(0, 1/fan_in) and one basis
+    V_base; layer l's weight is a seeded row permutation with random signs of
+    W_base (still N(0, 1/fan_in), distinct per layer) and its basis a seeded
+    column permutation of V_base (still orthonormal, the same subspace).
+    Tokens come from two pools per role drawn from V_base -- `pool` at the
+    fast noise level s(eps/4) and `pool` at the slow one s(4 eps) -- so any
+    layer's tokens can be picked by per-token slow labels (see pool_tokens).
+
+    Returns (base_W, V64, layer_rows, layer_cols, pools): base_W[role] a bf16
+    tensor, V64[role] float64 d x k, layer_rows[(l, role)] = (perm, signs),
+    layer_cols[(l, role)] a permutation of range(k), pools[role] =
+    (fast, slow) bf16 tensors of pool x d.
+    """
+    c = 4
+    base_W, V64, rows, cols, pools = {}, {}, {}, {}, {}
+    for role in ROLES:
+        d_out, d = SHAPES_13B[role]
+        r = ROLE_ID[role]
+        base_W[role] = storage(gaussian_weight(rng(c, 0, r, _W), d_out, d), torch.bfloat16)
+        V64[role] = orthonormal_basis(rng(c, 0, r, _V), d, k)
+        pools[role] = (map_tokens(c, 0, r, V64[role], pool, 0.0, eps, salt=1),
+                       map_tokens(c, 0, r, V64[role], pool, 1.0, eps, salt=2))
+        for l in range(n_layers):
+            rows[(l, role)] = layer_weight_rows(c, l, r, d_out)
+            cols[(l, role)] = rng(c, l, r, _CHAIN * 1000 + 1).permutation(k)
+    return base_W, V64, rows, cols, pools
+
+
+def pool_tokens(pools, role: str, layer: int, n: int, f_slow: float, salt: int = 0) -> torch.Tensor:
+    """n bf16 tokens for one map of the config-4 stack: per-token Bernoulli(f)
+    slow labels (exact at f = 0 and f = 1), each token a seeded pick from the
+    role's slow or fast pool."""
+    fast, slow = pools[role]
+    g = rng(4, layer, ROLE_ID[role], _LBL * 1000 + 500 + salt)
+    lab = g.random(n) < f_slow
+    pick = torch.from_numpy(g.integers(0, fast.shape[0], n))
+    X = fast[pick].clone()
+    if lab.any():
+        m = torch.from_numpy(lab)
+        X[m] = slow[pick[m]]
+    return X.contiguous()
