@@ -652,6 +652,39 @@ def run_per_call(R=4, n=32, reps_n=10):
         print(json.dumps(out))
 
 
+def probe_stack(n_tokens=16, R=2):
+    """A small case of the bench step for ncu: the four 6B maps over 2 device
+    replicas (about 1 GB of weights), n_tokens decode steps, each one
+    gsi_stack call (one stack_decode_kernel launch), run once.  Prints the
+    algorithmic bytes of every launch (JSON line) so that an ncu capture of a
+    few of them can be compared with what they had to move."""
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import gated_rank_subspace_gb300 as gsi
+
+    dev = torch.device("cuda", 0)
+    maps_in = [synth.map_6b(role, T=n_tokens, n_slow=max(1, n_tokens // 8), k=K_RANK) for role in synth.ROLES]
+    base = [gsi.make_map(m.W.to(dev), m.V.to(dev)) for m in maps_in]
+    reps = [base] + [[gsi.Map(b.W.clone(), b.V.clone(), b.M.clone(), b.gram.clone()) for b in base]
+                     for _ in range(R - 1)]
+    Xs = [m.X.to(dev) for m in maps_in]
+    Ys = [torch.zeros(n_tokens, m.d_out, device=dev) for m in maps_in]
+    Fs = [torch.zeros(n_tokens, dtype=torch.uint8, device=dev) for _ in maps_in]
+    ws = gsi.new_workspace(gsi.stack_workspace_size(base, 1), dev)
+    torch.cuda.synchronize()
+    for t in range(n_tokens):
+        gsi.stack(reps[t % R], [X[t:t + 1] for X in Xs], EPS, Ys=[Y[t:t + 1] for Y in Ys],
+                  flags=[F[t:t + 1] for F in Fs], workspace=ws)
+    torch.cuda.synchronize()
+    assert gsi.workspace_status(ws) == 0
+    flags = [F.cpu().numpy().astype(bool) for F in Fs]
+    per_launch = [sum(call_bytes(m.d, m.d_out, m.k, 1, int(not f[t]), int(f[t])) for m, f in zip(base, flags))
+                  for t in range(n_tokens)]
+    print(json.dumps({"probe_stack": n_tokens, "replicas": R, "algorithmic_bytes_per_launch": per_launch,
+                      "slow_per_launch": [int(sum(f[t] for f in flags)) for t in range(n_tokens)]}))
+
+
 def probe_map(role, eps):
     """Eight one-token gsi_linear calls of one 6B map (default stream)."""
     import __graft_entry__
@@ -686,6 +719,10 @@ def main():
                          "(the command an ncu DRAM-byte capture of the apply launches profiles)")
     ap.add_argument("--probe-map", choices=["qkv", "out", "up", "down"], default=None,
                     help="only run 8 one-token gsi_linear calls of this 6B map (a small case for ncu)")
+    ap.add_argument("--probe-stack", type=int, default=0,
+                    help="only run this many decode steps of the bench's four maps (2 weight replicas, one "
+                         "stack_decode_kernel launch a step) and print each launch's algorithmic bytes "
+                         "(a small case for ncu)")
     ap.add_argument("--probe-eps", type=float, default=0.0,
                     help="threshold of the --probe-map calls (0: every token slow)")
     ap.add_argument("--eps-sweep", action="store_true",
@@ -716,6 +753,9 @@ def main():
         return
     if args.probe_map:
         probe_map(args.probe_map, args.probe_eps)
+        return
+    if args.probe_stack:
+        probe_stack(args.probe_stack)
         return
     if args.impl == "reference":
         run_reference(args)
@@ -886,8 +926,11 @@ def main():
     # is decide_apply_kernel, whose stored-decision launches (gsi_apply) are
     # timed in a graph of their own.
     if sum(per_call) == 4:
-        dom = dict(name="decode_kernel (single-token decode: projection, gate, M g / W x in one launch)",
-                   gbs=step_gbs, bytes_per_launch=ab["total"] / n_launch, ms=ms / n_launch,
+        # the step's only kernel: one persistent launch per decode step runs
+        # the four maps (gsi_stack with one token per map)
+        dom = dict(name="stack_decode_kernel (persistent single-token decode: the four maps of a decode step, "
+                        "projection, gate, M g / W x, in one launch)",
+                   gbs=step_gbs, bytes_per_launch=ab["total"] / T_TOKENS, ms=ms / T_TOKENS,
                    timing="CUDA events over the timed region (graph replays of the step); "
                           "per-launch time = mean launch interval, gaps included")
     else:
@@ -970,7 +1013,7 @@ def main():
             except Exception as e:  # report and go on: the headline line still prints
                 secondary[key] = {"error": f"{type(e).__name__}: {e}"}
 
-    gpu_launches = args.steps * T_TOKENS * sum(per_call)
+    gpu_launches = args.steps * (T_TOKENS if sum(per_call) == 4 else T_TOKENS * sum(per_call))
     line = {
         "metric": "gsi_linear_tokens_per_s_batch1",
         "value": tokens_per_s,
@@ -994,8 +1037,8 @@ def main():
                   "of fast-path weights, 129 MB L2)",
             "parallelism": "replicas only" if world > 1 else "single GPU",
             "graph": "whole step captured in one CUDA graph, programmatic dependent launch between kernels",
-            "path": "single-token decode kernel, one launch per call (cluster projection for qkv, out and "
-                    "up, grid projection for down)"
+            "path": "persistent stack decode kernel, one launch per decode step over the four maps (cluster "
+                    "projection for qkv, out and up, grid projection for down; grid barrier between maps)"
                     if sum(per_call) == 4 else "two-launch streaming kernels",
         },
         "achieved_step_gbs": step_gbs,

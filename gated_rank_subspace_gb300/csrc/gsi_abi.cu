@@ -615,7 +615,9 @@ gsi_status gsi_build_image_ex(const void* W, const void* V, void* M, float* gram
   Ctrl* ctrl = static_cast<Ctrl*>(work);
   if ((s = cuda_check(cudaMemsetAsync(ctrl, 0, sizeof(Ctrl), st), "image scratch clear")) != GSI_OK) return s;
   uint16_t* Vt = reinterpret_cast<uint16_t*>(static_cast<char*>(work) + 256);
-  s = cuda_check(launch_image_tc(W, V, M, gram, d, d_out, k, Vt, &ctrl->err, st), "image kernel launch");
+  if ((s = cuda_check(launch_image_tc(W, V, M, d, d_out, k, Vt, &ctrl->err, st), "image kernel launch")) != GSI_OK)
+    return s;
+  if (gram) s = cuda_check(launch_gram(V, gram, d, k, dtype, st), "Gram kernel launch");
   return s == GSI_OK ? ok() : s;
 }
 

@@ -648,16 +648,19 @@ __global__ void __launch_bounds__(kApplyThreads, 1) stack_decode_kernel(const __
     // memory; its generic writes are ordered before the next map's copies
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     __syncthreads();
+    // map i + 1: barriers; then the last thread arrives for map i (its
+    // returning add is an L2 round trip) while the others issue the weight
+    // copies and the L2 prefetch of map i + 2
+    const DecodeMap& m1 = a.maps[i + 1];
+    decode_init_bars(m1, smem, tid, rank, true);
+    __syncthreads();
+    constexpr int kArrive = kApplyThreads - 1;  // no copy, prefetch or barrier duty
     unsigned long long target = 0;
-    if (tid == 0) {
+    if (tid == kArrive) {
       __threadfence();
       const unsigned long long mine = atomicAdd(a.arrive, 1ull);
       target = (mine / gridDim.x + 1) * gridDim.x;
     }
-    // map i + 1: barriers and weight copies, then the L2 prefetch of map i + 2
-    const DecodeMap& m1 = a.maps[i + 1];
-    decode_init_bars(m1, smem, tid, rank, true);
-    __syncthreads();
     decode_issue_copies<E>(m1, smem, tid, lane, warp, rank);
     if (i + 2 < n) {
       const DecodeMap& nx = a.maps[i + 2];
@@ -666,7 +669,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) stack_decode_kernel(const __
                          reinterpret_cast<const char*>(nx.gram), nx.gram ? uint64_t(nx.k) * nx.k * 4 : 0, tid);
     }
     cluster_arrive_relaxed();
-    if (tid == 0) {
+    if (tid == kArrive) {
       // every CTA has finished map i (bounded); then the grid's error word
       if (ld_acquire_gpu(a.arrive) < target) {
         const long long t0 = clock64();

@@ -112,12 +112,13 @@ cudaError_t launch_image(const void* W, const void* V, void* M, float* gram, int
   else
     e = contract<F32>(W, d, 1, V, k, 1, M, out_bf16, k, d_out, k, d, s);
   if (e != cudaSuccess || !gram) return e;
-  // Gram[a][b] = sum_i V[i][a] V[i][b]
-  if (dt == GSI_BF16)
-    e = contract<BF16>(V, 1, k, V, k, 1, gram, 0, k, k, k, d, s);
-  else
-    e = contract<F32>(V, 1, k, V, k, 1, gram, 0, k, k, k, d, s);
-  return e;
+  return launch_gram(V, gram, d, k, dt, s);
+}
+
+// Gram[a][b] = sum_i V[i][a] V[i][b], float32 FMA chains in one fixed order.
+cudaError_t launch_gram(const void* V, float* gram, int64_t d, int64_t k, gsi_dtype dt, cudaStream_t s) {
+  if (dt == GSI_BF16) return contract<BF16>(V, 1, k, V, k, 1, gram, 0, k, k, k, d, s);
+  return contract<F32>(V, 1, k, V, k, 1, gram, 0, k, k, k, d, s);
 }
 
 }  // namespace gsi

@@ -169,9 +169,11 @@ struct TensorArgs {
 };
 
 cudaError_t launch_tensor_path(const TensorArgs& t, cudaStream_t s);
-// M = W V_k (bf16) and the Gram on the tensor cores; Vt: k x d bf16 scratch.
-cudaError_t launch_image_tc(const void* W, const void* V, void* M, float* gram, int64_t d, int64_t d_out, int64_t k,
+// M = W V_k (bf16) on the tensor cores; Vt: k x d bf16 scratch.
+cudaError_t launch_image_tc(const void* W, const void* V, void* M, int64_t d, int64_t d_out, int64_t k,
                             uint16_t* Vt, uint32_t* err, cudaStream_t s);
+// The Gram matrix V_k^T V_k (k x k float32) on the CUDA cores.
+cudaError_t launch_gram(const void* V, float* gram, int64_t d, int64_t k, gsi_dtype dt, cudaStream_t s);
 
 // Sets the calling thread's gsi_last_error() message and returns s.
 gsi_status record_error(gsi_status s, const char* msg);

@@ -116,10 +116,11 @@ gsi_status gsi_build_image(const void* W, const void* V, void* M, float* gram,
                            void* stream);
 
 /* §2.1 image build on the tensor cores.  gsi_build_image_ex computes what
- * gsi_build_image does; for GSI_BF16 maps with a scratch area it runs on
- * tcgen05 (V^T formed in the scratch, then M = W V and V^T V as tensor-core
- * contractions with float32 accumulation in TMEM, M rounded to nearest even
- * into bf16).  work: device, 256-byte aligned, at least
+ * gsi_build_image does; for GSI_BF16 maps with a scratch area M runs on
+ * tcgen05 (V^T formed in the scratch, then M = W V as a tensor-core
+ * contraction with float32 accumulation in TMEM, rounded to nearest even
+ * into bf16).  The Gram matrix stays on the CUDA cores (float32 FMA chains):
+ * the gate's residual needs it to float32 accuracy.  work: device, 256-byte aligned, at least
  * gsi_build_image_work_bytes(d, k, dtype) bytes (0 for GSI_F32, which keeps
  * the CUDA-core kernel, as does work == NULL); its first 256 bytes hold an
  * error word that gsi_workspace_status reads (a bounded wait of the

@@ -82,3 +82,63 @@ def test_config3_28_layer_stack(gsi):
             rel = np.linalg.norm(Y[fast] - ref) / np.linalg.norm(ref)
             assert rel <= 2e-2, (l, role, rel)
             per_token_rel(Y[fast], ref, 2e-2, f"layer {l} {role}")
+
+
+@pytest.fixture(scope="module")
+def c4(gsi):
+    """The 40-layer 13B stack on the device, built once for the module."""
+    L = 40
+    base_W, V64, rows, cols, pools = synth.stack_config4(L)
+    dev = "cuda"
+    Wb = {r: base_W[r].to(dev) for r in synth.ROLES}
+    Vb = {r: synth.storage(V64[r], torch.bfloat16).to(dev) for r in synth.ROLES}
+    maps, info = [], []
+    for l in range(L):
+        for role in synth.ROLES:
+            perm, signs = rows[(l, role)]
+            W = (Wb[role][torch.from_numpy(perm).to(dev)] *
+                 torch.from_numpy(signs).to(dev, torch.bfloat16)[:, None]).contiguous()
+            V = Vb[role][:, torch.from_numpy(cols[(l, role)]).to(dev)].contiguous()
+            maps.append(gsi.make_map(W, V))
+            info.append((l, role))
+    yield maps, info, pools
+    del maps
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("T,f,steps", [(1, 0.05, 8), (4, 0.05, 4), (16, 0.25, 2)])
+def test_config4_40_layer_stack(gsi, c4, T, f, steps):
+    """13B shapes, k = 320, 40 layers x 4 maps through gsi_stack, T tokens per
+    call with per-token Bernoulli(f) slow labels; every map's gate and the
+    first and last layers' outputs against the oracle."""
+    L = 40
+    maps, info, pools = c4
+    n = T * steps
+    Xs = [synth.pool_tokens(pools, role, l, n, f, salt=T) for (l, role) in info]
+    Xd = [X.cuda() for X in Xs]
+    Ys = [torch.empty(n, m.d_out, device="cuda") for m in maps]
+    Fs = [torch.empty(n, dtype=torch.uint8, device="cuda") for _ in maps]
+    ws = gsi.new_workspace(gsi.stack_workspace_size(maps, T))
+    for s in range(steps):
+        sl = slice(s * T, (s + 1) * T)
+        args = gsi.stack_args(maps, [X[sl] for X in Xd], [Y[sl] for Y in Ys], [F[sl] for F in Fs])
+        gsi.stack_raw(args, len(maps), T, synth.EPS, ws)
+    torch.cuda.synchronize()
+    assert gsi.workspace_status(ws) == 0
+    from oracle import gsi_oracle as orc
+
+    n_slow = 0
+    for i, (l, role) in enumerate(info):
+        F = Fs[i].cpu().numpy().astype(bool)
+        n_slow += int(F.sum())
+        if l in (0, L - 1):
+            m_in = synth.MapInputs(f"c4.l{l}.{role}", maps[i].W.cpu(), maps[i].V.cpu(), Xs[i], synth.EPS)
+            compare(m_in, maps[i].M, Ys[i], Fs[i], None)
+            continue
+        Vn, Xn = synth.widen(maps[i].V), synth.widen(Xs[i])
+        ro = orc.residual_ratio(Xn, orc.residual(Xn, Vn, orc.project(Xn, Vn)))
+        band = np.abs(ro - synth.EPS) <= 1e-3
+        assert np.array_equal(F[~band], orc.gate(ro, synth.EPS)[~band]), (l, role)
+    # the slow fraction follows the labels (sampling noise allowed)
+    frac = n_slow / (n * len(maps))
+    assert abs(frac - f) <= 0.05 + 3 * np.sqrt(f * (1 - f) / (n * len(maps))), frac
