@@ -293,8 +293,8 @@ def graph_time_ms(fn, stream, reps, warm=2):
 def run_config3(gsi, dev, stream, hbm_peak, steps=64, reps=2):
     """The 28-layer linear-only stack of the 6B shapes (depth-coherent bases,
     per-layer slow fraction 5-15%): `steps` single-token decode steps, each one
-    gsi_stack call over the 112 maps (one persistent launch), all steps in one
-    CUDA graph.  Tokens/s counts one token per 28-layer step."""
+    gsi_stack call over the 112 maps (one decode launch per map), all steps in
+    one CUDA graph.  Tokens/s counts one token per 28-layer step."""
     L = 28
     bases, fr, base_W, tokens = synth.stack_config3(L, steps)
     maps, Xs = [], []
@@ -334,7 +334,7 @@ def run_config3(gsi, dev, stream, hbm_peak, steps=64, reps=2):
            "tokens_per_s": steps / (ms * 1e-3), "ms_per_token": ms / steps, "achieved_gbs": gbs,
            "frac_of_hbm_peak": gbs / hbm_peak, "bytes_saved_vs_dense": dense / nbytes,
            "slow_fraction": float(np.mean([f.mean() for f in flags])),
-           "kernel": "stack_decode_kernel (one persistent launch per 112-map step)"}
+           "kernel": "decode_kernel (one launch per gated-map call, 112 per step)"}
     del maps, Xs, Ys, Fs, args, ws
     torch.cuda.empty_cache()
     return out
@@ -406,7 +406,7 @@ def run_config4(gsi, dev, stream, hbm_peak, reps=2):
     out = {"workload": "13B-class linears (qkv 15360x5120, out 5120^2, up 13824x5120, down 5120x13824), "
                        "40 layers, bf16, k=320, eps=0.05; each decode step one gsi_stack call over the 160 maps",
            "points": points,
-           "kernels": "T=1: stack_decode_kernel (persistent); T=4, 16: project_kernel + decide_apply_kernel per map"}
+           "kernels": "T=1: decode_kernel per map; T=4, 16: project_kernel + decide_apply_kernel per map"}
     del maps, ws
     torch.cuda.empty_cache()
     return out
@@ -926,11 +926,10 @@ def main():
     # is decide_apply_kernel, whose stored-decision launches (gsi_apply) are
     # timed in a graph of their own.
     if sum(per_call) == 4:
-        # the step's only kernel: one persistent launch per decode step runs
-        # the four maps (gsi_stack with one token per map)
-        dom = dict(name="stack_decode_kernel (persistent single-token decode: the four maps of a decode step, "
-                        "projection, gate, M g / W x, in one launch)",
-                   gbs=step_gbs, bytes_per_launch=ab["total"] / T_TOKENS, ms=ms / T_TOKENS,
+        # the step's only kernel: one single-token decode launch per
+        # gated-map call (gsi_stack runs the four maps one call each)
+        dom = dict(name="decode_kernel (single-token decode: projection, gate, M g / W x in one launch)",
+                   gbs=step_gbs, bytes_per_launch=ab["total"] / n_launch, ms=ms / n_launch,
                    timing="CUDA events over the timed region (graph replays of the step); "
                           "per-launch time = mean launch interval, gaps included")
     else:
@@ -990,16 +989,31 @@ def main():
 
     # ---- the gate's Gram form checked on the device against the explicit
     # residual x - V g (second pass over V) for the step's 1024 calls
+    torch.cuda.synchronize()
     rho_dev = []
     for i, b in enumerate(base):
         G_i = G_all[i::4].contiguous()
         r_i = rho_all[i::4].contiguous()
-        _, dv = gsi.residual_check(b, Xs[i], G_i, r_i, stream=stream)
+        _, dv = gsi.residual_check(b, Xs[i], G_i, r_i)  # on the stream that made G_i and r_i
         rho_dev.append(dv)
-    stream.synchronize()
+    torch.cuda.synchronize()
     gate_check = {"max_abs_rho2_gram_minus_explicit": max(float(v.item()) for v in rho_dev),
                   "what": "largest |rho^2 (Gram form, gate kernels) - rho^2 (explicit x - V g, second pass)| "
                           "over the 1024 single-token calls of the step (gsi_residual_check)"}
+
+    # the same step with the persistent stack kernel (one launch per decode
+    # step over the four maps, grid barrier between maps), for comparison
+    def step_persistent():
+        for t in range(T_TOKENS):
+            gsi.stack_raw(args_t[t], 4, 1, EPS, ws, stream=stream, mode="persistent")
+
+    ms_pers = graph_time_ms(step_persistent, stream, args.steps)
+    assert gsi.workspace_status(ws, stream=stream) == 0
+    persistent = {"kernel": "stack_decode_kernel (one persistent launch per decode step over the four maps)",
+                  "tokens_per_s": T_TOKENS * world / (ms_pers * 1e-3), "ms_per_step": ms_pers,
+                  "achieved_gbs": ab["total"] / (ms_pers * 1e-3) / 1e9,
+                  "frac_of_hbm_peak": ab["total"] / (ms_pers * 1e-3) / 1e9 / hbm_peak,
+                  "us_per_map_call": ms_pers * 1e3 / n_launch}
 
     secondary = None
     if not args.no_secondary and world == 1:
@@ -1013,7 +1027,7 @@ def main():
             except Exception as e:  # report and go on: the headline line still prints
                 secondary[key] = {"error": f"{type(e).__name__}: {e}"}
 
-    gpu_launches = args.steps * (T_TOKENS if sum(per_call) == 4 else T_TOKENS * sum(per_call))
+    gpu_launches = args.steps * T_TOKENS * sum(per_call)
     line = {
         "metric": "gsi_linear_tokens_per_s_batch1",
         "value": tokens_per_s,
@@ -1037,8 +1051,8 @@ def main():
                   "of fast-path weights, 129 MB L2)",
             "parallelism": "replicas only" if world > 1 else "single GPU",
             "graph": "whole step captured in one CUDA graph, programmatic dependent launch between kernels",
-            "path": "persistent stack decode kernel, one launch per decode step over the four maps (cluster "
-                    "projection for qkv, out and up, grid projection for down; grid barrier between maps)"
+            "path": "single-token decode kernel, one launch per call (cluster projection for qkv, out and "
+                    "up, grid projection for down)"
                     if sum(per_call) == 4 else "two-launch streaming kernels",
         },
         "achieved_step_gbs": step_gbs,
@@ -1068,6 +1082,7 @@ def main():
         "clocks": clocks,
         "cpu_baseline": cpu,
         "gate_check": gate_check,
+        "persistent_stack_same_step": persistent,
         "secondary": secondary,
     }
     if rank == 0:

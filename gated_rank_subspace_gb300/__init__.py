@@ -70,6 +70,7 @@ def lib() -> ctypes.CDLL:
         "gsi_linear_ex": [P(MapDesc), vp, i64, f32, vp, vp, vp, vp, sz, ctypes.c_int, vp],
         "gsi_stack_workspace_size": [P(MapDesc), i64, i64, P(sz)],
         "gsi_stack": [P(MapDesc), i64, P(vp), i64, f32, P(vp), P(vp), vp, sz, vp],
+        "gsi_stack_ex": [P(MapDesc), i64, P(vp), i64, f32, P(vp), P(vp), vp, sz, ctypes.c_int, vp],
         "gsi_path_errors": [P(MapDesc), vp, i64, vp, vp, vp, vp, vp, vp, vp, sz, vp],
         "gsi_eps_sweep": [vp, vp, vp, i64, vp, i64, i64, vp, vp, vp, vp],
         "gsi_basis_orthonormalize": [vp, i64, i64, vp, vp],
@@ -386,7 +387,10 @@ def compact(flags: torch.Tensor, stream=None):
     return idx, counts
 
 
-def stack(maps, Xs, eps: float, Ys=None, flags=None, workspace=None, stream=None):
+STACK_MODES = {"auto": 0, "per_map": 1, "persistent": 2}
+
+
+def stack(maps, Xs, eps: float, Ys=None, flags=None, workspace=None, stream=None, mode: str = "auto"):
     """The gated map over a list of maps, each with its own tokens."""
     n = len(maps)
     T = Xs[0].shape[0]
@@ -398,8 +402,8 @@ def stack(maps, Xs, eps: float, Ys=None, flags=None, workspace=None, stream=None
     if workspace is None:
         workspace = new_workspace(stack_workspace_size(maps, T), dev, stream)
     args = stack_args(maps, Xs, Ys, flags)
-    _check(lib().gsi_stack(args[0], n, args[1], T, float(eps), args[2], args[3],
-                           _ptr(workspace), workspace.numel(), _stream(stream)))
+    _check(lib().gsi_stack_ex(args[0], n, args[1], T, float(eps), args[2], args[3],
+                              _ptr(workspace), workspace.numel(), STACK_MODES[mode], _stream(stream)))
     return Ys, flags
 
 
@@ -413,7 +417,7 @@ def stack_args(maps, Xs, Ys, flags):
             (vp * n)(*[f.data_ptr() for f in flags]))
 
 
-def stack_raw(args, n, T, eps, workspace, stream=None):
-    """gsi_stack on prepared ctypes arrays (no per-call Python allocation)."""
-    _check(lib().gsi_stack(args[0], n, args[1], T, float(eps), args[2], args[3],
-                           _ptr(workspace), workspace.numel(), _stream(stream)))
+def stack_raw(args, n, T, eps, workspace, stream=None, mode: str = "auto"):
+    """gsi_stack_ex on prepared ctypes arrays (no per-call Python allocation)."""
+    _check(lib().gsi_stack_ex(args[0], n, args[1], T, float(eps), args[2], args[3],
+                              _ptr(workspace), workspace.numel(), STACK_MODES[mode], _stream(stream)))

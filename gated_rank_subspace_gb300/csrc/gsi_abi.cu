@@ -886,6 +886,14 @@ gsi_status gsi_stack_workspace_size(const gsi_map_desc* maps, int64_t n_maps, in
 gsi_status gsi_stack(const gsi_map_desc* maps, int64_t n_maps, const void* const* X, int64_t T,
                      float eps, float* const* Y, uint8_t* const* flags, void* workspace,
                      size_t ws_bytes, void* stream) {
+  return gsi_stack_ex(maps, n_maps, X, T, eps, Y, flags, workspace, ws_bytes, GSI_STACK_AUTO, stream);
+}
+
+gsi_status gsi_stack_ex(const gsi_map_desc* maps, int64_t n_maps, const void* const* X, int64_t T,
+                        float eps, float* const* Y, uint8_t* const* flags, void* workspace,
+                        size_t ws_bytes, gsi_stack_mode mode, void* stream) {
+  if (mode != GSI_STACK_AUTO && mode != GSI_STACK_PER_MAP && mode != GSI_STACK_PERSISTENT)
+    return fail(GSI_ERR_INVALID_ARG, "unknown stack mode %d", int(mode));
   if (!maps || n_maps <= 0) return fail(GSI_ERR_INVALID_ARG, "maps is NULL or n_maps <= 0");
   if (!X || !Y || !flags) return fail(GSI_ERR_INVALID_ARG, "X, Y and flags arrays must be non-NULL");
   gsi_status s = check_tokens(T, eps);
@@ -907,12 +915,15 @@ gsi_status gsi_stack(const gsi_map_desc* maps, int64_t n_maps, const void* const
   if (T == 0) return ok();
   if ((s = check_workspace(workspace, ws_bytes, need)) != GSI_OK) return s;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // One token per map: runs of consecutive maps that the single-token kernel
-  // takes (one element type, row width and k) go to the persistent stack
-  // kernel, up to kStackMaxMaps per launch; every other map (and a run the
-  // device refuses) is one call each.
+  // GSI_STACK_PERSISTENT with one token per map: runs of consecutive maps
+  // that the single-token kernel takes (one element type, row width and k)
+  // go to the persistent stack kernel, up to kStackMaxMaps per launch; every
+  // other map (and a run the device refuses) is one call each.  AUTO and
+  // PER_MAP run one call per map: a launch boundary chained by programmatic
+  // dependent launch was measured faster than the persistent kernel's grid
+  // barrier between maps.
   DeviceFacts* f = nullptr;
-  if (T == 1 && (s = device_facts(&f)) != GSI_OK) return s;
+  if (T == 1 && mode == GSI_STACK_PERSISTENT && (s = device_facts(&f)) != GSI_OK) return s;
   auto stackable = [&](int64_t j) {
     gsi_path p;
     return resolve_path(&maps[j], 1, GSI_PATH_AUTO, &p) == GSI_OK && p == GSI_PATH_FUSED &&

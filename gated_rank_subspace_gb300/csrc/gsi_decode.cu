@@ -641,7 +641,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) stack_decode_kernel(const __
   pdl_wait();
   long long lim = kSpinCycles;
   for (int i = 0; i < n; ++i) {
-    const DecodeMap& m = a.maps[i];
+    const DecodeMap m = a.maps[i];  // a register copy: the table is indexed at run time
     decode_run<E, NV>(m, a.eps, a.part_g, a.part_x, (launch << 8) | uint32_t(i + 1), a.err, lim, 0, 0, smem);
     if (i + 1 == n) break;
     // every warp has written its rows of map i and is done with shared

@@ -216,6 +216,30 @@ gsi_status gsi_stack(const gsi_map_desc* maps, int64_t n_maps, const void* const
                      int64_t T, float eps, float* const* Y, uint8_t* const* flags,
                      void* workspace, size_t ws_bytes, void* stream);
 
+/* How gsi_stack_ex runs a list of maps.
+ *   AUTO / PER_MAP -- one gated-map call per map, consecutive calls chained by
+ *             programmatic dependent launch (what gsi_stack does);
+ *   PERSISTENT -- with one token per map, each run of consecutive maps that
+ *             the single-token decode kernel takes (same element type, row
+ *             width and k; at most 112) in ONE persistent launch: the maps'
+ *             calls in list order, a grid barrier on the workspace between
+ *             consecutive maps (map i + 1 still reads its token only after map
+ *             i has finished), the next map's weights staged while the grid
+ *             finishes the current one.  Outputs are bitwise those of one
+ *             call per map.  Other maps, and runs the device refuses to launch
+ *             co-resident, run one call each. */
+typedef enum gsi_stack_mode {
+  GSI_STACK_AUTO = 0,
+  GSI_STACK_PER_MAP = 1,
+  GSI_STACK_PERSISTENT = 2
+} gsi_stack_mode;
+
+/* gsi_stack with an explicit choice of how the list runs (same arguments,
+ * results and workspace). */
+gsi_status gsi_stack_ex(const gsi_map_desc* maps, int64_t n_maps, const void* const* X,
+                        int64_t T, float eps, float* const* Y, uint8_t* const* flags,
+                        void* workspace, size_t ws_bytes, gsi_stack_mode mode, void* stream);
+
 /* §2.2 (Theorem 4) and §4 (static-projection control): both candidate
  * outputs of every token, for error accounting and threshold sweeps.
  * Y_fast (T x d_out float32) receives M g_t for every token (the map at

@@ -1,5 +1,6 @@
-"""The persistent stack kernel: gsi_stack with one token per map runs a list
-of maps in one launch, map after map, with a grid barrier between them
+"""The persistent stack kernel: gsi_stack_ex(GSI_STACK_PERSISTENT) with one
+token per map runs a list of maps in one launch, map after map, with a grid
+barrier between them
 ("Gated Subspace Inference for Transformer Acceleration", §2.2: the gate on
 every linear map of a layer -- QKV, output, MLP up and down -- and on every
 layer).
@@ -40,7 +41,7 @@ def _stack_steps(gsi, maps, Xs, eps, steps):
     ws = gsi.new_workspace(gsi.stack_workspace_size(maps, 1))
     for t in range(steps):
         args = gsi.stack_args(maps, [X[t:t + 1] for X in Xs], [Y[t:t + 1] for Y in Ys], [F[t:t + 1] for F in Fs])
-        gsi.stack_raw(args, len(maps), 1, eps, ws)
+        gsi.stack_raw(args, len(maps), 1, eps, ws, mode="persistent")
     torch.cuda.synchronize()
     assert gsi.workspace_status(ws) == 0
     return Ys, Fs
