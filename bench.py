@@ -655,9 +655,10 @@ def run_per_call(R=4, n=32, reps_n=10):
 def probe_stack(n_tokens=16, R=2):
     """A small case of the bench step for ncu: the four 6B maps over 2 device
     replicas (about 1 GB of weights), n_tokens decode steps, each one
-    gsi_stack call (one stack_decode_kernel launch), run once.  Prints the
-    algorithmic bytes of every launch (JSON line) so that an ncu capture of a
-    few of them can be compared with what they had to move."""
+    gsi_stack call (one decode_kernel launch per map), run once.  Prints the
+    algorithmic bytes of every launch in launch order (JSON line) so that an
+    ncu capture of a few of them can be compared with what they had to
+    move."""
     import __graft_entry__
 
     __graft_entry__.build()
@@ -679,10 +680,10 @@ def probe_stack(n_tokens=16, R=2):
     torch.cuda.synchronize()
     assert gsi.workspace_status(ws) == 0
     flags = [F.cpu().numpy().astype(bool) for F in Fs]
-    per_launch = [sum(call_bytes(m.d, m.d_out, m.k, 1, int(not f[t]), int(f[t])) for m, f in zip(base, flags))
-                  for t in range(n_tokens)]
+    per_launch = [call_bytes(m.d, m.d_out, m.k, 1, int(not f[t]), int(f[t]))
+                  for t in range(n_tokens) for m, f in zip(base, flags)]
     print(json.dumps({"probe_stack": n_tokens, "replicas": R, "algorithmic_bytes_per_launch": per_launch,
-                      "slow_per_launch": [int(sum(f[t] for f in flags)) for t in range(n_tokens)]}))
+                      "slow_per_launch": [int(f[t]) for t in range(n_tokens) for f in flags]}))
 
 
 def probe_map(role, eps):

@@ -151,7 +151,7 @@ static gsi_status resolve_path(const gsi_map_desc* m, int64_t T, gsi_path path, 
     if (fused_fits(m, T))
       *out = GSI_PATH_FUSED;  // falls back to STREAM at run time where the device cannot run it
     else
-      *out = (m->dtype == GSI_BF16 && T >= kTensorMinT) ? GSI_PATH_TENSOR : GSI_PATH_STREAM;
+      *out = (m->dtype == GSI_BF16 && T >= kTensorAutoMinT) ? GSI_PATH_TENSOR : GSI_PATH_STREAM;
     return GSI_OK;
   }
   if (path == GSI_PATH_STREAM) {

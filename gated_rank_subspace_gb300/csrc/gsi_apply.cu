@@ -182,29 +182,46 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
   auto fast_apply = [&](int ntok, auto tok_of, auto emit) {
     const unsigned char* mrows = m_live ? Ms : static_cast<const unsigned char*>(a.M) + r0 * mrow_b;
     const int nvm = mrow_b / 16;
-    auto fast_rows = [&](auto rb_c) {
+    // A block of RB rows at a time: the lane's vectors of those rows are
+    // read once (NL = 1 or 2 vectors a lane) and multiplied with every
+    // token's g, instead of re-reading the rows per token; each product sum
+    // keeps its order (the lane's vectors in order, then the butterfly).
+    auto fast_rows = [&](auto rb_c, auto nl_c) {
       constexpr int RB = decltype(rb_c)::value;
+      constexpr int NL = decltype(nl_c)::value;
       for (int rb = warp * RB; rb < nrows; rb += NCW * RB) {
+        uint4 mv[RB][NL];
+#pragma unroll
+        for (int r = 0; r < RB; ++r)
+#pragma unroll
+          for (int j = 0; j < NL; ++j) {
+            const int vv = lane + 32 * j;
+            mv[r][j] = (rb + r < nrows && vv < nvm)
+                           ? *reinterpret_cast<const uint4*>(mrows + int64_t(rb + r) * mrow_b + vv * 16)
+                           : make_uint4(0u, 0u, 0u, 0u);
+          }
         for (int f = 0; f < ntok; ++f) {
           const int t = tok_of(f);
           float part[RB];
 #pragma unroll
           for (int r = 0; r < RB; ++r) part[r] = 0.f;
-          for (int vv = lane; vv < nvm; vv += 32) {
-            float gv[PV];
 #pragma unroll
-            for (int e4 = 0; e4 < PV / 4; ++e4) {
-              const float4 g4 = *reinterpret_cast<const float4*>(gfull + t * k + vv * PV + 4 * e4);
-              gv[4 * e4] = g4.x;
-              gv[4 * e4 + 1] = g4.y;
-              gv[4 * e4 + 2] = g4.z;
-              gv[4 * e4 + 3] = g4.w;
-            }
+          for (int j = 0; j < NL; ++j) {
+            const int vv = lane + 32 * j;
+            if (vv < nvm) {
+              float gv[PV];
 #pragma unroll
-            for (int r = 0; r < RB; ++r) {
-              if (rb + r < nrows) {
+              for (int e4 = 0; e4 < PV / 4; ++e4) {
+                const float4 g4 = *reinterpret_cast<const float4*>(gfull + t * k + vv * PV + 4 * e4);
+                gv[4 * e4] = g4.x;
+                gv[4 * e4 + 1] = g4.y;
+                gv[4 * e4 + 2] = g4.z;
+                gv[4 * e4 + 3] = g4.w;
+              }
+#pragma unroll
+              for (int r = 0; r < RB; ++r) {
                 float w[PV];
-                E::unpack(*reinterpret_cast<const uint4*>(mrows + int64_t(rb + r) * mrow_b + vv * 16), w);
+                E::unpack(mv[r][j], w);
 #pragma unroll
                 for (int e = 0; e < PV; ++e) part[r] = fmaf(w[e], gv[e], part[r]);
               }
@@ -216,12 +233,17 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
         }
       }
     };
-    if (nrows <= NCW * 4)
-      fast_rows(IntC<4>{});
-    else if (nrows <= NCW * 8)
-      fast_rows(IntC<8>{});
-    else
-      fast_rows(IntC<16>{});
+    // (at most 8 rows a block: the rows' vectors stay in registers)
+    if (nvm > 32) {  // rows over 512 bytes: two vectors a lane
+      if (nrows <= NCW * 4)
+        fast_rows(IntC<4>{}, IntC<2>{});
+      else
+        fast_rows(IntC<8>{}, IntC<2>{});
+    } else if (nrows <= NCW * 4) {
+      fast_rows(IntC<4>{}, IntC<1>{});
+    } else {
+      fast_rows(IntC<8>{}, IntC<1>{});
+    }
   };
   // decide-and-apply calls compute the fast outputs before the decision ends
   const bool yspec = a.mode == 0 && nrows > 0;

@@ -119,8 +119,13 @@ inline TensorLayout layout_tensor(int64_t d, int64_t k, int64_t T) {
   return L;
 }
 
-// Token count from which GSI_PATH_AUTO uses the tensor cores for bf16 maps.
+// Token count of a prefill-sized call: the tensor path's slow-token
+// contraction takes 256 token rows per CTA from here on.
 constexpr int64_t kTensorMinT = 128;
+// Token count from which GSI_PATH_AUTO uses the tensor cores for bf16 maps
+// (measured on the 13B maps: per call at T = 16 the tensor path takes about
+// two thirds of the streaming kernels' time, which grow by ~5 us a token).
+constexpr int64_t kTensorAutoMinT = 16;
 
 // Decide-and-apply kernel geometry (see gsi_apply.cu).  The device part
 // (how many CTAs are co-resident) comes in as ncta; everything else is

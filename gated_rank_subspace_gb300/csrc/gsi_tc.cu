@@ -350,8 +350,9 @@ __global__ void transpose_bf16_kernel(const uint16_t* __restrict__ V, uint16_t* 
 }
 
 // Per token: ||x||^2, g^T Gram g, rho, flag, and g rounded to bf16.
-// One CTA per 8 tokens; thread j owns column j of g.
-constexpr int kFinTok = 8;
+// One CTA per 16 tokens (each CTA reads the whole Gram from L2 once, so
+// fewer, wider CTAs read it fewer times); thread j owns column j of g.
+constexpr int kFinTok = 16;
 
 __global__ void __launch_bounds__(256) tc_finalize_kernel(const uint16_t* __restrict__ X, const float* __restrict__ G,
                                                           const float* __restrict__ gram, int64_t d, int k, int T,
@@ -427,12 +428,12 @@ __global__ void __launch_bounds__(256) tc_finalize_kernel(const uint16_t* __rest
       q[t] = gram ? fmaf(gj, h[t], q[t]) : n[t];
     }
   }
-  // ||x||^2: warp w takes token w, lanes stride over 16-byte vectors
-  if (warp < kFinTok) {
+  // ||x||^2: warp w takes tokens w, w + 8, ..., lanes stride over 16-byte vectors
+  for (int tw = warp; tw < kFinTok; tw += 8) {
     float s = 0.f;
-    if (t0 + warp < T) {
+    if (t0 + tw < T) {
       // eight 16-byte loads in flight per lane, then their squares in order
-      const uint4* xr = reinterpret_cast<const uint4*>(X + int64_t(t0 + warp) * d);
+      const uint4* xr = reinterpret_cast<const uint4*>(X + int64_t(t0 + tw) * d);
       const int64_t nv = d / 8;
       for (int64_t v0 = lane; v0 < nv; v0 += 32 * 8) {
         uint4 xq[8];
@@ -448,7 +449,7 @@ __global__ void __launch_bounds__(256) tc_finalize_kernel(const uint16_t* __rest
       }
     }
     s = warp_sum(s);
-    if (lane == 0) x2s[warp] = s;
+    if (lane == 0) x2s[tw] = s;
   }
 #pragma unroll
   for (int t = 0; t < kFinTok; ++t) {
@@ -691,7 +692,11 @@ cudaError_t launch_tensor_path(const TensorArgs& t, cudaStream_t s) {
   sl.ldc = d_out;
   sl.row_map = t.idx + T;
   sl.err = t.err;
-  // 256 rows per CTA: W is read from L2 once per 256 slow tokens
+  // Prefill-sized T: 256 token rows per CTA (two 128-row tiles), so W is
+  // read from L2 once per 256 slow tokens.  Small T: W dominates the bytes
+  // and one 128-row tile holds every slow token, so 64-row tiles of W spread
+  // it over as many CTAs as possible.
+  if (T < kTensorMinT) return launch_tc_gemm(t.Xslow, T, t.W, d_out, int(d), 64, sl, s, 1);
   return launch_tc_gemm(t.Xslow, T, t.W, d_out, int(d), 256, sl, s, 2);
 }
 

@@ -82,7 +82,7 @@ typedef enum gsi_dtype { GSI_F32 = 0, GSI_BF16 = 1 } gsi_dtype;
  *   TENSOR -- tcgen05 contractions, bf16 only, for prefill-sized T.
  * AUTO picks FUSED for T <= 2 where a slab of V fits shared memory (and
  * STREAM at run time on a device that cannot hold the fused grid), TENSOR
- * for bf16 with T >= 128, STREAM otherwise.  Where the fused kernels' CTAs
+ * for bf16 with T >= 16, STREAM otherwise.  Where the fused kernels' CTAs
  * wait on other clusters, they are launched as a co-resident (cooperative)
  * grid: a grid that cannot be co-resident is refused at launch, and AUTO
  * then runs the call on the STREAM kernels.  Every device wait stays bounded
