@@ -686,6 +686,41 @@ def probe_stack(n_tokens=16, R=2):
                       "slow_per_launch": [int(f[t]) for t in range(n_tokens) for f in flags]}))
 
 
+def probe_batch(spec, L=2, steps=4):
+    """A small case of the 13B small-batch stack for ncu: L layers of the
+    four 13B maps (k=320, about 1 GB of weights per layer), `steps` decode
+    steps of T tokens with slow fraction f (spec "T:f"), each step one
+    gsi_stack call, run once.  Prints the algorithmic bytes of every call in
+    call order (JSON line)."""
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import gated_rank_subspace_gb300 as gsi
+
+    T, f = spec.split(":")
+    T, f = int(T), float(f)
+    dev = torch.device("cuda", 0)
+    maps, pools = config4_maps(gsi, dev, L)
+    n = T * steps
+    Xs = [synth.pool_tokens(pools, role, l, n, f, salt=int(T * 100 + f * 100)).to(dev)
+          for l in range(L) for role in synth.ROLES]
+    Ys = [torch.zeros(n, m.d_out, device=dev) for m in maps]
+    Fs = [torch.zeros(n, dtype=torch.uint8, device=dev) for _ in maps]
+    ws = gsi.new_workspace(gsi.stack_workspace_size(maps, T), dev)
+    torch.cuda.synchronize()
+    for s in range(steps):
+        a = gsi.stack_args(maps, [X[s * T:(s + 1) * T] for X in Xs], [Y[s * T:(s + 1) * T] for Y in Ys],
+                           [F[s * T:(s + 1) * T] for F in Fs])
+        gsi.stack_raw(a, len(maps), T, EPS, ws)
+    torch.cuda.synchronize()
+    assert gsi.workspace_status(ws) == 0
+    fl = [F.cpu().numpy().astype(bool).reshape(steps, T) for F in Fs]
+    per_call = [call_bytes(m.d, m.d_out, m.k, T, T - int(x[s].sum()), int(x[s].sum()))
+                for s in range(steps) for m, x in zip(maps, fl)]
+    print(json.dumps({"probe_batch": spec, "layers": L, "steps": steps, "algorithmic_bytes_per_call": per_call,
+                      "slow_per_call": [int(x[s].sum()) for s in range(steps) for x in fl]}))
+
+
 def probe_map(role, eps):
     """Eight one-token gsi_linear calls of one 6B map (default stream)."""
     import __graft_entry__
@@ -716,14 +751,18 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-traffic", action="store_true",
-                    help="only run the step's 1024 gate launches, then its 1024 apply launches, once "
-                         "(the command an ncu DRAM-byte capture of the apply launches profiles)")
+                    help="only run the step once eagerly (1024 decode_kernel launches), then its 1024 gate and "
+                         "1024 apply launches, and print each decode launch's algorithmic bytes (the command an "
+                         "ncu DRAM-byte capture of a few decode launches profiles)")
     ap.add_argument("--probe-map", choices=["qkv", "out", "up", "down"], default=None,
                     help="only run 8 one-token gsi_linear calls of this 6B map (a small case for ncu)")
     ap.add_argument("--probe-stack", type=int, default=0,
                     help="only run this many decode steps of the bench's four maps (2 weight replicas, one "
-                         "stack_decode_kernel launch a step) and print each launch's algorithmic bytes "
+                         "decode_kernel launch per map) and print each launch's algorithmic bytes "
                          "(a small case for ncu)")
+    ap.add_argument("--probe-batch", default=None, metavar="T:f",
+                    help="only run 4 decode steps of T tokens (slow fraction f) through 2 layers of the 13B "
+                         "maps and print each call's algorithmic bytes (a small case for ncu)")
     ap.add_argument("--probe-eps", type=float, default=0.0,
                     help="threshold of the --probe-map calls (0: every token slow)")
     ap.add_argument("--eps-sweep", action="store_true",
@@ -757,6 +796,9 @@ def main():
         return
     if args.probe_stack:
         probe_stack(args.probe_stack)
+        return
+    if args.probe_batch:
+        probe_batch(args.probe_batch)
         return
     if args.impl == "reference":
         run_reference(args)
@@ -905,6 +947,15 @@ def main():
             run_gates()
             run_applies(None)
         stream.synchronize()
+        # the eager step's decode_kernel launches in launch order (token t,
+        # then the four maps): their algorithmic bytes, to set beside an ncu
+        # capture of a few of them
+        fl = [F.cpu().numpy().astype(bool) for F in Fs]
+        per_launch = [call_bytes(m.d, m.d_out, m.k, 1, int(not f[t]), int(f[t]))
+                      for t in range(T_TOKENS) for m, f in zip(base, fl)]
+        print(json.dumps({"kernel_traffic": "decode_kernel launches of the eager step",
+                          "algorithmic_bytes_per_launch": per_launch,
+                          "mean_algorithmic_bytes_per_launch": sum(per_launch) / len(per_launch)}))
         return
     t_gate = timed_graph(run_gates, args.steps)
     t_fast = timed_graph(lambda: run_applies(False), args.steps)

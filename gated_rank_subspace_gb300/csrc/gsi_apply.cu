@@ -48,6 +48,10 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
   constexpr int PV = E::kPerVec;
   constexpr int NCW = 8;  // consumer warps
   extern __shared__ __align__(128) unsigned char smem[];
+  if (!cluster_shape_ok(CS)) {
+    if (threadIdx.x == 0) atomicOr(a.err, kErrTimeout | kErrLaunchShape);
+    return;  // before any barrier, copy or access to another CTA
+  }
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = int(cluster.block_rank());
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;

@@ -5,6 +5,7 @@
 #include <cuda_bf16.h>
 #include <cooperative_groups.h>
 #include <stdint.h>
+#include <cstdlib>
 
 #include "../../include/gsi.h"
 
@@ -249,10 +250,22 @@ inline cudaError_t set_kernel_smem(K kern, size_t dyn_bytes) {
 // refusal is remembered in *no_coop and the launch is repeated without it
 // (the waits stay bounded).  A refusal for size comes back as
 // cudaErrorCooperativeLaunchTooLarge, for the caller to take another path.
+// GSI_COOPERATIVE=0 in the environment launches these kernels without the
+// attribute, sized as before from the occupancy query (for tools that
+// relaunch kernels themselves and do not keep the cooperative attribute
+// together with the cluster shape; the waits stay bounded).
+inline bool cooperative_launch_enabled() {
+  static const bool on = [] {
+    const char* v = std::getenv("GSI_COOPERATIVE");
+    return !(v && v[0] == '0' && v[1] == '\0');
+  }();
+  return on;
+}
+
 template <class K, class A>
 inline cudaError_t launch_maybe_coop(cudaLaunchConfig_t cfg, cudaLaunchAttribute* attrs, int n_attrs, bool coop,
                                      int* no_coop, K kern, const A& args) {
-  if (coop && !*no_coop) {
+  if (coop && !*no_coop && cooperative_launch_enabled()) {
     attrs[n_attrs].id = cudaLaunchAttributeCooperative;
     attrs[n_attrs].val.cooperative = 1;
     cfg.attrs = attrs;
@@ -292,5 +305,17 @@ constexpr uint32_t kErrTimeout = 1;
 constexpr uint32_t kWaitV = 1u << 4, kWaitGram = 1u << 5, kWaitM = 1u << 6, kWaitPartials = 1u << 7,
                    kWaitGathered = 1u << 8, kWaitShares = 1u << 9, kWaitRing = 1u << 10, kWaitSlices = 1u << 11,
                    kWaitGrid = 1u << 12;
+// The kernel found itself running without the cluster shape it was built
+// for (or with a grid its exchanges cannot address) and returned before its
+// first access to another CTA's shared memory.
+constexpr uint32_t kErrLaunchShape = 1u << 13;
+
+// True when this CTA's cluster has `ctas` CTAs: every rank a kernel maps a
+// shared-memory address to (mapa, st.async) then exists.
+__device__ __forceinline__ bool cluster_shape_ok(unsigned ctas) {
+  unsigned n;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+  return n == ctas;
+}
 
 }  // namespace gsi

@@ -579,6 +579,11 @@ template <class E, int NV>
 __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (!cluster_shape_ok(kDecodeCluster) ||
+      (a.m.grid && (gridDim.x % kDecodeCluster != 0 || gridDim.x / kDecodeCluster > kDecodeMaxClusters))) {
+    if (tid == 0) atomicOr(a.err, kErrTimeout | kErrLaunchShape);
+    return;  // before any barrier, copy or access to another CTA
+  }
   const int rank = int(cg::this_cluster().block_rank());
   const DecodeBars b(smem);
   // ---- prologue: weights only (may overlap the previous kernel's tail)
@@ -619,6 +624,11 @@ template <class E, int NV>
 __global__ void __launch_bounds__(kApplyThreads, 1) stack_decode_kernel(const __grid_constant__ StackDecodeArgs a) {
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (!cluster_shape_ok(kDecodeCluster) || gridDim.x % kDecodeCluster != 0 ||
+      gridDim.x / kDecodeCluster > kDecodeMaxClusters) {
+    if (tid == 0) atomicOr(a.err, kErrTimeout | kErrLaunchShape);
+    return;  // before any barrier, copy or access to another CTA
+  }
   const int rank = int(cg::this_cluster().block_rank());
   const DecodeBars b(smem);
   const int n = a.n_maps;

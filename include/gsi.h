@@ -85,9 +85,13 @@ typedef enum gsi_dtype { GSI_F32 = 0, GSI_BF16 = 1 } gsi_dtype;
  * for bf16 with T >= 16, STREAM otherwise.  Where the fused kernels' CTAs
  * wait on other clusters, they are launched as a co-resident (cooperative)
  * grid: a grid that cannot be co-resident is refused at launch, and AUTO
- * then runs the call on the STREAM kernels.  Every device wait stays bounded
- * (~2 s, then GSI_ERR_TIMEOUT from gsi_workspace_status, after which the
- * workspace must be re-initialised). */
+ * then runs the call on the STREAM kernels.  GSI_COOPERATIVE=0 in the
+ * environment launches them without the co-resident attribute (grid sized
+ * from the occupancy query; for profilers that relaunch kernels without it).
+ * Every device wait stays bounded (~2 s, then GSI_ERR_TIMEOUT from
+ * gsi_workspace_status, after which the workspace must be re-initialised).
+ * A cluster kernel that finds itself running without its cluster shape sets
+ * bit 13 of the error word and returns without touching other CTAs. */
 typedef enum gsi_path {
   GSI_PATH_AUTO = 0,
   GSI_PATH_STREAM = 1,
