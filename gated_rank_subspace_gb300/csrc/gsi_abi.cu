@@ -376,7 +376,9 @@ static gsi_status run_stack_decode(const gsi_map_desc* maps, int n, const void* 
 // Enqueue the decide-and-apply kernel for one map (all arguments validated).
 // mode 0: decide and apply (gsi_linear); 1: decide only (gsi_gate, writes
 // G, rho, flags and the compaction); 2: apply the decision stored by a
-// preceding gsi_gate on the same workspace (gsi_apply).
+// preceding gsi_gate on the same workspace (gsi_apply); 3: decide, apply the
+// fast tokens and write the compaction (the slow rows are left to the
+// tensor-core contraction that follows).
 // fused: the single-launch decode (mode 0 only; the cluster projects x on
 // its own slices of V).  next: the map that follows in a stack, whose
 // weights are staged in L2 while this one runs (nullable).  Returns
@@ -517,7 +519,16 @@ static gsi_status run_stream(const gsi_map_desc* m, const void* X, int64_t T, fl
   }
   gsi_status s = cuda_check(launch_gate(ga, gp, m->dtype, st, true), "projection kernel launch");
   if (s != GSI_OK) return s;
-  return run_decide(m, X, T, eps, apply ? 0 : 1, Y, flags, rho, G_out, nullptr, ws, st, false, next);
+  // bf16 maps: the decide-and-apply kernel writes the fast rows and the
+  // compaction (mode 3), and the slow rows follow on the tensor cores
+  const bool defer = apply && m->dtype == GSI_BF16;
+  s = run_decide(m, X, T, eps, apply ? (defer ? 3 : 0) : 1, Y, flags, rho, G_out, nullptr, ws, st, false, next);
+  if (s != GSI_OK || !defer) return s;
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(base + L.ctrl);
+  s = cuda_check(launch_slow_rows_tc(X, m->W, m->d, m->d_out, T, reinterpret_cast<const int32_t*>(base + L.idx),
+                                     ctrl->counts, reinterpret_cast<uint16_t*>(base + L.xslow), Y, &ctrl->err, st),
+                 "slow-row contraction launch");
+  return s == GSI_OK ? ok() : s;
 }
 
 
@@ -550,6 +561,8 @@ static gsi_status run_tensor(const gsi_map_desc* m, const void* X, int64_t T, fl
   t.flags = flags;
   t.Y = Y;
   t.err = &ctrl->err;
+  t.fpart = reinterpret_cast<float4*>(base + L.fpart);
+  t.fin_arrive = &ctrl->fin_arrive;
   return cuda_check(launch_tensor_path(t, st), "tensor-core path launch");
 }
 

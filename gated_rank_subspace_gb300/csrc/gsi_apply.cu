@@ -29,7 +29,9 @@
 // workspace error word, drains its own copies (bounded) and returns.
 //
 // Modes: decide and apply (gsi_linear), decide only (gsi_gate: writes G,
-// rho, flags and the compaction), apply a stored decision (gsi_apply).
+// rho, flags and the compaction), apply a stored decision (gsi_apply), and
+// decide and apply the fast tokens only, with the compaction (bf16 maps on
+// the two-launch path: the slow rows follow as a tensor-core contraction).
 
 #include "gsi_common.cuh"
 #include "gsi_async.cuh"
@@ -250,7 +252,7 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
     }
   };
   // decide-and-apply calls compute the fast outputs before the decision ends
-  const bool yspec = a.mode == 0 && nrows > 0;
+  const bool yspec = (a.mode == 0 || a.mode == 3) && nrows > 0;
 
   for (int t0 = 0; t0 < T; t0 += TC) {
     const int tc = min(TC, T - t0);
@@ -629,7 +631,8 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
       scount[1] = ok ? ns : 0;
     }
     __syncthreads();
-    const int nf = scount[0], ns = scount[1];
+    // (mode 3 leaves the slow rows to the tensor-core contraction that follows)
+    const int nf = scount[0], ns = a.mode == 3 ? 0 : scount[1];
 
     // -- fast tokens: y = M g.  Decide-and-apply calls computed it for every
     //    token of the chunk while the decision's last exchange was in flight
@@ -815,7 +818,7 @@ __global__ void __maxnreg__(168) decide_apply_kernel(DecideArgs a) {
     if (t0 + TC < T) cluster.sync();
   }
 
-  if (a.mode == 1 && blockIdx.x == 0) {
+  if ((a.mode == 1 || a.mode == 3) && blockIdx.x == 0) {
     __threadfence();
     __syncthreads();
     if (warp == 0) compact_warp(a.flags, T, a.idx, a.counts, lane);

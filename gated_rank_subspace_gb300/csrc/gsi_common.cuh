@@ -295,7 +295,10 @@ struct Ctrl {
   unsigned long long ticket1[2];
   // the persistent stack kernel's arrivals at its barriers between maps
   unsigned long long arrive[2];
-  uint32_t pad[48];
+  // the tensor path's finalize: CTAs of the current launch that have stored
+  // their partial sums (the last one resets it)
+  uint32_t fin_arrive;
+  uint32_t pad[47];
 };
 static_assert(sizeof(Ctrl) == 256, "Ctrl is 256 bytes");
 

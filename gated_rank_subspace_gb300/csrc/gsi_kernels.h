@@ -166,9 +166,18 @@ struct TensorArgs {
   uint8_t* flags;       // T
   float* Y;             // T x d_out
   uint32_t* err;        // device error word
+  float4* fpart;        // finalize partial sums [chunks][blocks][16]
+  uint32_t* fin_arrive; // finalize arrival counter (control words)
 };
 
 cudaError_t launch_tensor_path(const TensorArgs& t, cudaStream_t s);
+// The slow rows of a call whose decision, compaction (idx: fast tokens, then
+// slow tokens from idx + T; counts = {n_fast, n_slow}) and fast rows are done:
+// the slow tokens' x gathered into Xslow (T x d bf16 scratch), then
+// Y[slow] = X_slow W^T as the few-token tensor-core contraction.
+cudaError_t launch_slow_rows_tc(const void* X, const void* W, int64_t d, int64_t d_out, int64_t T,
+                                const int32_t* idx, const int32_t* counts, uint16_t* Xslow, float* Y, uint32_t* err,
+                                cudaStream_t s);
 // M = W V_k (bf16) on the tensor cores; Vt: k x d bf16 scratch.
 cudaError_t launch_image_tc(const void* W, const void* V, void* M, int64_t d, int64_t d_out, int64_t k,
                             uint16_t* Vt, uint32_t* err, cudaStream_t s);

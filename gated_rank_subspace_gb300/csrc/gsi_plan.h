@@ -62,7 +62,7 @@ inline GatePlan plan_gate(int64_t d, int64_t k, int elem_bytes, int64_t T) {
 
 // Workspace layout of one stream-path call (offsets in bytes, 256-aligned).
 struct StreamLayout {
-  size_t ctrl, part_g, part_x, g, idx, flags, total;
+  size_t ctrl, part_g, part_x, g, idx, flags, xslow, total;
 };
 
 inline StreamLayout layout_stream(int64_t d, int64_t k, int elem_bytes, int64_t T) {
@@ -75,6 +75,7 @@ inline StreamLayout layout_stream(int64_t d, int64_t k, int elem_bytes, int64_t 
   L.g = off;       off += align256(size_t(T) * k * 4);
   L.idx = off;     off += align256(size_t(2) * T * 4);
   L.flags = off;   off += align256(size_t(T));
+  L.xslow = off;   off += elem_bytes == 2 ? align256(size_t(T) * d * 2) : 0;  // slow tokens' x (bf16)
   L.total = off;
   return L;
 }
@@ -99,33 +100,52 @@ inline FusedLayout layout_fused(int64_t k, int64_t T) {
 
 // Workspace layout of one tensor-core-path call.
 struct TensorLayout {
-  size_t ctrl, vt, g, gbf, gfast, xslow, idx, total;
+  size_t ctrl, vt, g, gbf, gfast, xslow, idx, fpart, total;
 };
 
-// Split-K slices of the tensor path's projection contraction G = X V_k.
-constexpr int kGSplit = 8;
+// Token count of a prefill-sized call: the tensor path's slow-token
+// contraction takes 256 token rows per CTA from here on.
+constexpr int64_t kTensorMinT = 128;
+
+// Split-K slices of the tensor path's projection contraction G = X V_k: 8 at
+// prefill-sized T, 16 below it (few token rows: more CTAs, shorter chains).
+constexpr int kGSplitMax = 16;
+inline int g_split(int64_t T) { return T < kTensorMinT ? 16 : 8; }
+
+// The tensor path's finalize (rho, flags, bf16 g) takes tokens in chunks of
+// kFinTok and cuts the Gram rows into fin_blocks(T, k) blocks, so that a
+// small T still spreads over the SMs (one block once there are 64 chunks).
+constexpr int kFinTok = 16;
+inline int fin_blocks(int64_t T, int64_t k) {
+  const int64_t chunks = cdiv(T, kFinTok);
+  if (chunks >= 64) return 1;
+  int64_t nb = cdiv(304, chunks);
+  const int64_t cap = k / 8 > 0 ? k / 8 : 1;  // at least 8 Gram rows a block
+  if (nb > cap) nb = cap;
+  if (nb > 64) nb = 64;
+  return int(nb < 1 ? 1 : nb);
+}
 
 inline TensorLayout layout_tensor(int64_t d, int64_t k, int64_t T) {
   TensorLayout L{};
   size_t off = 0;
   L.ctrl = off;   off += 256;
   L.vt = off;     off += align256(size_t(k) * d * 2);
-  L.g = off;      off += align256(size_t(kGSplit) * T * k * 4);  // kGSplit partial projections
+  L.g = off;      off += align256(size_t(g_split(T)) * T * k * 4);  // split-K partial projections
   L.gbf = off;    off += align256(size_t(T) * k * 2);
   L.gfast = off;  off += align256(size_t(T) * k * 2);
   L.xslow = off;  off += align256(size_t(T) * d * 2);
   L.idx = off;    off += align256(size_t(2) * T * 4);
+  L.fpart = off;  off += align256(size_t(cdiv(T, kFinTok)) * fin_blocks(T, k) * kFinTok * 16);
   L.total = off;
   return L;
 }
-
-// Token count of a prefill-sized call: the tensor path's slow-token
-// contraction takes 256 token rows per CTA from here on.
-constexpr int64_t kTensorMinT = 128;
-// Token count from which GSI_PATH_AUTO uses the tensor cores for bf16 maps
-// (measured on the 13B maps: per call at T = 16 the tensor path takes about
-// two thirds of the streaming kernels' time, which grow by ~5 us a token).
-constexpr int64_t kTensorAutoMinT = 16;
+// Token count from which GSI_PATH_AUTO uses the tensor cores for bf16 maps.
+// Measured per call on the 13B maps (d = 5120, k = 320) without slow tokens:
+// 40-46 us on the tensor path from T = 2 to 16; 16-38 us on the streaming
+// kernels up to T = 8 (one chunk of 8 tokens), 67-74 us at T = 12-16 (two
+// chunks).  Slow rows take the tensor cores on both paths (bf16).
+constexpr int64_t kTensorAutoMinT = 9;
 
 // Decide-and-apply kernel geometry (see gsi_apply.cu).  The device part
 // (how many CTAs are co-resident) comes in as ncta; everything else is

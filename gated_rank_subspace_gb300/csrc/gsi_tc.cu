@@ -333,6 +333,184 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 0) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
+// ------------------------------------------------------------------ few-token contraction
+// Y[tok(j)][r] = sum_kk A[r][kk] B[j][kk] for the rows r of a weight matrix A
+// (W or M: n_rows x K, bf16, K-major) and the first n_tok rows of a token
+// matrix B (X_slow or G_fast: K-major), NT token rows per CTA (grid z).  The
+// weight rows are the MMA's M side (128-row tiles) and the tokens its N side
+// (NT columns of TMEM), so a call with few tokens spends no tensor-core work on padding
+// token rows, and the weight stream is spread over the n_rows / 128 tiles
+// times `splits` slices of K.  The slices of one tile are one thread-block
+// cluster (grid x): after its MMAs each CTA stages its partial 128 x NT tile
+// in shared memory, and after a cluster barrier CTA q adds rows
+// [q R, (q + 1) R) over the cluster's CTAs in rank order (distributed shared
+// memory) and writes them, so every output has one fixed summation order.
+// Threads: 0 issues the TMA loads, 32 the MMAs, all four warps the epilogue
+// (warp w reads TMEM lanes 32 w .. 32 w + 31 = weight rows).
+struct SkinnyArgs {
+  int n_rows, K;
+  int n_tok;                 // token rows (used when n_tok_dev is null)
+  const int32_t* n_tok_dev;  // device count of token rows, or null
+  float* Y;
+  int64_t ldy;
+  const int32_t* tok_map;    // output row of token row j is tok_map[j] (null: j)
+  uint32_t* err;
+};
+
+template <int NT>
+struct SkinnyCfg {
+  static constexpr uint32_t A_BYTES = kBM * kBK * 2;
+  static constexpr uint32_t B_BYTES = NT * kBK * 2;
+  static constexpr int STAGES = (100 * 1024) / (A_BYTES + B_BYTES) > 3 ? (100 * 1024) / (A_BYTES + B_BYTES) : 3;
+  static constexpr int TMEM_COLS = NT < 32 ? 32 : NT;
+  static constexpr int LDS = NT + 4;  // staged partial tile row stride (floats)
+  static_assert(size_t(kBM) * LDS * 4 <= size_t(STAGES) * (A_BYTES + B_BYTES), "staging fits");
+  static constexpr size_t SMEM = 1024 + size_t(STAGES) * (A_BYTES + B_BYTES) + 256;
+};
+
+template <int NT>
+__global__ void __launch_bounds__(128, 1)
+    tc_skinny_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb, SkinnyArgs a) {
+  using C = SkinnyCfg<NT>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = base;
+  uint8_t* sB = base + C::STAGES * C::A_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + C::STAGES * C::B_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* done = empty + C::STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+  __shared__ int s_issued;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int splits = int(gridDim.x), sl = int(blockIdx.x);  // K slice = rank in the cluster
+  const int row0 = int(blockIdx.y) * kBM;
+  const int tok0 = int(blockIdx.z) * NT;  // this CTA's token rows [tok0, tok0 + NT)
+  pdl_wait();
+  int n_tok = (a.n_tok_dev ? __ldcg(a.n_tok_dev) : a.n_tok) - tok0;
+  if (n_tok <= 0) return;  // the whole cluster leaves together (same count everywhere)
+  if (n_tok > NT) n_tok = NT;
+  const int32_t* tok_map = a.tok_map ? a.tok_map + tok0 : nullptr;
+  if (splits > 1 && !cluster_shape_ok(unsigned(splits))) {
+    if (threadIdx.x == 0) atomicOr(a.err, kErrTimeout | kErrLaunchShape);
+    return;
+  }
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int nk_all = (a.K + kBK - 1) / kBK;
+  const int kb0 = int(int64_t(nk_all) * sl / splits);
+  const int nk = int(int64_t(nk_all) * (sl + 1) / splits) - kb0;
+
+  if (threadIdx.x == 0) {
+    int kb = 0;
+    for (; kb < nk; ++kb) {
+      const int s = kb % C::STAGES;
+      const uint32_t ph = (kb / C::STAGES) & 1;
+      if (kb >= C::STAGES && !mbar_wait(&empty[s], ph ^ 1, a.err)) break;
+      mbar_expect_tx(&full[s], C::A_BYTES + C::B_BYTES);
+      tma_load_2d(sA + s * C::A_BYTES, &ta, &full[s], (kb0 + kb) * kBK, row0);
+      tma_load_2d(sB + s * C::B_BYTES, &tb, &full[s], (kb0 + kb) * kBK, tok0);
+    }
+    s_issued = kb;
+  } else if (threadIdx.x == 32) {
+    constexpr uint32_t idesc = idesc_bf16_f32(kBM, NT);
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % C::STAGES;
+      const uint32_t ph = (kb / C::STAGES) & 1;
+      if (!mbar_wait(&full[s], ph, a.err)) break;
+      tc_fence_after();
+      const uint64_t ad = smem_desc_sw128(sA + s * C::A_BYTES);
+      const uint64_t bd = smem_desc_sw128(sB + s * C::B_BYTES);
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk)  // advance 16 bf16 = 32 bytes inside the swizzle row
+        umma_bf16(tmem, ad + uint64_t(kk * 2), bd + uint64_t(kk * 2), idesc, (kb | kk) != 0);
+      umma_commit(&empty[s]);
+    }
+    umma_commit(done);  // fires once every MMA issued above has completed
+  }
+  __syncwarp();
+  const bool ok = mbar_wait(done, 0, a.err);
+  tc_fence_after();
+  // tcgen05.ld is warp-collective: decide per warp, never per thread
+  const bool go = __all_sync(0xffffffffu, ok && nk > 0 && *reinterpret_cast<volatile uint32_t*>(a.err) == 0);
+  const int row = warp * 32 + lane;  // this lane's weight row in the tile
+  if (splits == 1) {
+    if (go) {
+#pragma unroll 1
+      for (int c = 0; c < NT; c += 16) {
+        if (c >= n_tok) break;  // warp-uniform
+        float v[16];
+        tmem_ld16(tmem + (uint32_t(warp * 32) << 16) + uint32_t(c), v);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int j = c + i;
+          if (j < n_tok && row0 + row < a.n_rows) {
+            const int64_t orow = tok_map ? int64_t(__ldcg(&tok_map[j])) : int64_t(tok0 + j);
+            a.Y[orow * a.ldy + row0 + row] = v[i];
+          }
+        }
+      }
+    }
+  } else {
+    // stage this slice's partial tile in the (idle) pipeline buffers: every
+    // MMA, and so every operand copy into them, has completed
+    float* st = reinterpret_cast<float*>(base);
+    if (go) {
+#pragma unroll 1
+      for (int c = 0; c < NT; c += 16) {
+        float v[16];
+        tmem_ld16(tmem + (uint32_t(warp * 32) << 16) + uint32_t(c), v);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<float4*>(st + row * C::LDS + c + 4 * q) =
+              make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      }
+    }
+    // every CTA of the cluster passes both barriers, with or without an error
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();  // the partial tiles are staged
+    const bool all_ok = __syncthreads_and(go) != 0;
+    const bool any_err = *reinterpret_cast<volatile uint32_t*>(a.err) != 0;
+    if (all_ok && !any_err) {
+      const int R = (kBM + splits - 1) / splits;
+      const int rb = sl * R, rn = kBM - rb < R ? (kBM - rb > 0 ? kBM - rb : 0) : R;
+      for (int e = threadIdx.x; e < rn * n_tok; e += 128) {
+        const int j = e / rn, r = rb + (e - (e / rn) * rn);
+        float sum = 0.f;
+        for (int q = 0; q < splits; ++q) sum += cluster.map_shared_rank(st, q)[r * C::LDS + j];
+        if (row0 + r < a.n_rows) {
+          const int64_t orow = tok_map ? int64_t(__ldcg(&tok_map[j])) : int64_t(tok0 + j);
+          a.Y[orow * a.ldy + row0 + r] = sum;
+        }
+      }
+    }
+    cluster.sync();  // the peers' reads of this CTA's tile are done
+  }
+  // bounded drain of this CTA's own copies before its shared memory goes away
+  // (only reached with copies in flight after a timeout)
+  if (threadIdx.x == 0 && !ok) {
+    for (int kb = 0; kb < s_issued; ++kb) mbar_wait(&full[kb % C::STAGES], (kb / C::STAGES) & 1, a.err);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
 // ------------------------------------------------------------------ helpers on CUDA cores
 // V_k (d x k) -> V_k^T (k x d), bf16, 32 x 32 tiles through shared memory.
 __global__ void transpose_bf16_kernel(const uint16_t* __restrict__ V, uint16_t* __restrict__ Vt, int d, int k) {
@@ -350,33 +528,51 @@ __global__ void transpose_bf16_kernel(const uint16_t* __restrict__ V, uint16_t* 
 }
 
 // Per token: ||x||^2, g^T Gram g, rho, flag, and g rounded to bf16.
-// One CTA per 16 tokens (each CTA reads the whole Gram from L2 once, so
-// fewer, wider CTAs read it fewer times); thread j owns column j of g.
-constexpr int kFinTok = 16;
+// CTA (c, b) takes tokens [16 c, 16 c + 16), Gram rows [k b / nb, k (b + 1) / nb)
+// and the same share of each token's x for ||x||^2.  Every CTA adds the
+// split-K slices of g for its tokens (all k columns: the Gram form needs
+// them); block 0 also writes the bf16 g and ||g||^2.  With one block (large
+// T) a CTA finishes its tokens itself.  Otherwise each CTA stores its partial
+// sums and the grid's last CTA to arrive (a counter in the control words,
+// reset by that CTA) adds them in block order for every token; every sum has
+// one fixed order.
+__device__ __forceinline__ void fin_token(float qq, float nn, float x2, float eps, float* rho_out, uint8_t* flags,
+                                          int t) {
+  float rr = x2 - 2.f * nn + qq;
+  rr = rr < 0.f ? 0.f : rr;
+  const float rho = x2 == 0.f ? 0.f : sqrtf(rr / x2);
+  if (rho_out) rho_out[t] = rho;
+  flags[t] = (rho < eps) ? uint8_t(0) : uint8_t(1);
+}
 
+template <int GS>
 __global__ void __launch_bounds__(256) tc_finalize_kernel(const uint16_t* __restrict__ X, const float* __restrict__ G,
                                                           const float* __restrict__ gram, int64_t d, int k, int T,
                                                           float eps, float* __restrict__ rho_out,
                                                           uint8_t* __restrict__ flags, uint16_t* __restrict__ Gbf,
-                                                          int gsplit) {
+                                                          int gsplit, int nb, float4* __restrict__ part,
+                                                          uint32_t* arrive) {
   extern __shared__ float fsm[];
   float* gs = fsm;                       // [kFinTok][k]
   float* red = gs + kFinTok * k;         // [8 warps][kFinTok][2]
   float* x2s = red + 8 * kFinTok * 2;    // [kFinTok]
-  const int t0 = blockIdx.x * kFinTok;
+  __shared__ bool s_last;
+  const int cb = blockIdx.x, blk = blockIdx.y;
+  const int t0 = cb * kFinTok;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i0 = int(int64_t(k) * blk / nb), i1 = int(int64_t(k) * (blk + 1) / nb);
   pdl_wait();
   // g = the split-K slices' partial projections, added in slice order; a
-  // thread loads the slices of 4 elements (32 loads in flight) before adding
+  // thread loads the slices of 4 elements (4 GS loads in flight) before adding
   for (int e0 = tid; e0 < kFinTok * k; e0 += 256 * 4) {
-    float v[4][kGSplit];
+    float v[4][GS];
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int e = e0 + q * 256;
       const int t = e / k, j = e - (e / k) * k;
       const bool live = e < kFinTok * k && t0 + t < T;
 #pragma unroll
-      for (int sl = 0; sl < kGSplit; ++sl)
+      for (int sl = 0; sl < GS; ++sl)
         v[q][sl] = (live && sl < gsplit) ? __ldcg(&G[(int64_t(sl) * T + t0 + t) * k + j]) : 0.f;
     }
 #pragma unroll
@@ -386,15 +582,17 @@ __global__ void __launch_bounds__(256) tc_finalize_kernel(const uint16_t* __rest
       const int t = e / k, j = e - (e / k) * k;
       float g = 0.f;
 #pragma unroll
-      for (int sl = 0; sl < kGSplit; ++sl) g += v[q][sl];
+      for (int sl = 0; sl < GS; ++sl) g += v[q][sl];
       gs[e] = g;
-      if (t0 + t < T) {
-        __nv_bfloat16 b = __float2bfloat16_rn(g);
-        Gbf[int64_t(t0 + t) * k + j] = *reinterpret_cast<uint16_t*>(&b);
+      if (blk == 0 && t0 + t < T) {
+        __nv_bfloat16 bv = __float2bfloat16_rn(g);
+        Gbf[int64_t(t0 + t) * k + j] = *reinterpret_cast<uint16_t*>(&bv);
       }
     }
   }
   __syncthreads();
+  // this block's share of g^T Gram g: thread j forms h_j = sum over the
+  // block's rows i of g_i Gram_ij, then adds g_j h_j; block 0: ||g||^2
   float q[kFinTok], n[kFinTok];
 #pragma unroll
   for (int t = 0; t < kFinTok; ++t) q[t] = n[t] = 0.f;
@@ -403,10 +601,9 @@ __global__ void __launch_bounds__(256) tc_finalize_kernel(const uint16_t* __rest
 #pragma unroll
     for (int t = 0; t < kFinTok; ++t) h[t] = 0.f;
     if (gram) {
-      // Gram rows in batches of 32 loads in flight (a row at a time would
-      // wait one L2 round trip per row), added in row order
-      int i = 0;
-      for (; i + 32 <= k; i += 32) {
+      // Gram rows in batches of 32 loads in flight, added in row order
+      int i = i0;
+      for (; i + 32 <= i1; i += 32) {
         float gv[32];
 #pragma unroll
         for (int u = 0; u < 32; ++u) gv[u] = __ldg(&gram[int64_t(i + u) * k + j]);
@@ -415,30 +612,41 @@ __global__ void __launch_bounds__(256) tc_finalize_kernel(const uint16_t* __rest
 #pragma unroll
           for (int t = 0; t < kFinTok; ++t) h[t] = fmaf(gs[t * k + i + u], gv[u], h[t]);
       }
-      for (; i < k; ++i) {
-        const float gij = __ldg(&gram[int64_t(i) * k + j]);
+      if (i < i1) {
+        float gv[32];
 #pragma unroll
-        for (int t = 0; t < kFinTok; ++t) h[t] = fmaf(gs[t * k + i], gij, h[t]);
+        for (int u = 0; u < 32; ++u) gv[u] = i + u < i1 ? __ldg(&gram[int64_t(i + u) * k + j]) : 0.f;
+#pragma unroll
+        for (int u = 0; u < 32; ++u)
+          if (i + u < i1)
+#pragma unroll
+            for (int t = 0; t < kFinTok; ++t) h[t] = fmaf(gs[t * k + i + u], gv[u], h[t]);
       }
     }
 #pragma unroll
     for (int t = 0; t < kFinTok; ++t) {
       const float gj = gs[t * k + j];
-      n[t] = fmaf(gj, gj, n[t]);
-      q[t] = gram ? fmaf(gj, h[t], q[t]) : n[t];
+      if (blk == 0) n[t] = fmaf(gj, gj, n[t]);
+      if (gram) q[t] = fmaf(gj, h[t], q[t]);
     }
   }
-  // ||x||^2: warp w takes tokens w, w + 8, ..., lanes stride over 16-byte vectors
+  // (without a Gram matrix the basis is taken as orthonormal: g^T g)
+  if (!gram) {
+#pragma unroll
+    for (int t = 0; t < kFinTok; ++t) q[t] = n[t];
+  }
+  // ||x||^2 over this block's share of the row's 16-byte vectors: warp w takes
+  // tokens w, w + 8, ..., eight loads in flight per lane, squares in order
+  const int64_t nv = d / 8;
+  const int64_t xv0 = nv * blk / nb, xv1 = nv * (blk + 1) / nb;
   for (int tw = warp; tw < kFinTok; tw += 8) {
     float s = 0.f;
     if (t0 + tw < T) {
-      // eight 16-byte loads in flight per lane, then their squares in order
       const uint4* xr = reinterpret_cast<const uint4*>(X + int64_t(t0 + tw) * d);
-      const int64_t nv = d / 8;
-      for (int64_t v0 = lane; v0 < nv; v0 += 32 * 8) {
+      for (int64_t vb = xv0 + lane; vb < xv1; vb += 32 * 8) {
         uint4 xq[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) xq[u] = v0 + 32 * u < nv ? ld_cg_v4(xr + v0 + 32 * u) : make_uint4(0u, 0u, 0u, 0u);
+        for (int u = 0; u < 8; ++u) xq[u] = vb + 32 * u < xv1 ? ld_cg_v4(xr + vb + 32 * u) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           float f[8];
@@ -466,13 +674,31 @@ __global__ void __launch_bounds__(256) tc_finalize_kernel(const uint16_t* __rest
       qq += red[(w * kFinTok + tid) * 2 + 0];
       nn += red[(w * kFinTok + tid) * 2 + 1];
     }
-    const float x2 = x2s[tid];
-    float rr = x2 - 2.f * nn + qq;
-    rr = rr < 0.f ? 0.f : rr;
-    const float rho = x2 == 0.f ? 0.f : sqrtf(rr / x2);
-    if (rho_out) rho_out[t0 + tid] = rho;
-    flags[t0 + tid] = (rho < eps) ? uint8_t(0) : uint8_t(1);
+    if (nb == 1)
+      fin_token(qq, nn, x2s[tid], eps, rho_out, flags, t0 + tid);
+    else
+      part[(int64_t(cb) * nb + blk) * kFinTok + tid] = make_float4(qq, nn, x2s[tid], 0.f);
   }
+  if (nb == 1) return;
+  // the last CTA of the grid adds every token's block partials in block order
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) s_last = atomicAdd(arrive, 1u) == gridDim.x * gridDim.y - 1u;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int t = tid; t < T; t += 256) {
+    const int c = t / kFinTok, tt = t - c * kFinTok;
+    float qq = 0.f, nn = 0.f, x2 = 0.f;
+    for (int bb = 0; bb < nb; ++bb) {
+      const float4 p = __ldcg(&part[(int64_t(c) * nb + bb) * kFinTok + tt]);
+      qq += p.x;
+      nn += p.y;
+      x2 += p.z;
+    }
+    fin_token(qq, nn, x2, eps, rho_out, flags, t);
+  }
+  if (tid == 0) *arrive = 0u;  // for the next call on this workspace
 }
 
 // Gather rows: dst[j] = src[idx[j]] for j < count (16-byte vectors).
@@ -562,6 +788,55 @@ cudaError_t launch_tc_gemm(const void* A, int64_t a_rows, const void* B, int64_t
   }
 }
 
+// Few-token contraction (see tc_skinny_kernel): A = weights (a_rows x K),
+// B = token rows (b_rows x K) in tiles of NT (grid z), K cut into `splits`
+// slices (one cluster per 128-row tile of A; splits <= 8 and <= the k-blocks).
+template <int NT>
+static cudaError_t launch_skinny_t(const void* A, int64_t a_rows, const void* B, int64_t b_rows, int K, int splits,
+                                   const SkinnyArgs& args, cudaStream_t s) {
+  CUtensorMap ta, tb;
+  cudaError_t e = make_map_2d(&ta, A, a_rows, K, kBM);
+  if (e != cudaSuccess) return e;
+  if ((e = make_map_2d(&tb, B, b_rows, K, NT)) != cudaSuccess) return e;
+  auto kern = tc_skinny_kernel<NT>;
+  static bool attr = false;
+  if (!attr) {
+    if ((e = set_kernel_smem(kern, SkinnyCfg<NT>::SMEM)) != cudaSuccess) return e;
+    attr = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(splits), unsigned(cdiv(a_rows, kBM)), unsigned(cdiv(b_rows, NT)));
+  cfg.blockDim = dim3(128);
+  cfg.dynamicSmemBytes = SkinnyCfg<NT>::SMEM;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  at[1].id = cudaLaunchAttributeClusterDimension;
+  at[1].val.clusterDim.x = unsigned(splits);
+  at[1].val.clusterDim.y = 1;
+  at[1].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kern, ta, tb, args);
+}
+
+static cudaError_t launch_skinny(const void* A, int64_t a_rows, const void* B, int64_t b_rows, int K, int max_tok,
+                                 const SkinnyArgs& args, cudaStream_t s) {
+  // K slices: enough CTAs for two a SM over the 128-row tiles, at most 8 (one
+  // portable cluster) and at least 4 k-blocks a slice
+  const int64_t tiles = cdiv(a_rows, kBM), nk = cdiv(K, kBK);
+  int64_t splits = cdiv(2 * 152, tiles);
+  if (splits > 8) splits = 8;
+  if (splits > nk / 4) splits = nk / 4;
+  if (splits < 1) splits = 1;
+  const int sp = int(splits);
+  if (max_tok <= 16) return launch_skinny_t<16>(A, a_rows, B, b_rows, K, sp, args, s);
+  if (max_tok <= 32) return launch_skinny_t<32>(A, a_rows, B, b_rows, K, sp, args, s);
+  if (max_tok <= 64) return launch_skinny_t<64>(A, a_rows, B, b_rows, K, sp, args, s);
+  return launch_skinny_t<128>(A, a_rows, B, b_rows, K, sp, args, s);
+}
+
 static cudaError_t launch_pdl(const void* kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
@@ -602,6 +877,33 @@ cudaError_t launch_image_tc(const void* W, const void* V, void* M, int64_t d, in
   return launch_tc_gemm(W, d_out, Vt, k, int(d), bn, a, s);
 }
 
+cudaError_t launch_slow_rows_tc(const void* X, const void* W, int64_t d, int64_t d_out, int64_t T,
+                                const int32_t* idx, const int32_t* counts, uint16_t* Xslow, float* Y, uint32_t* err,
+                                cudaStream_t s) {
+  cudaError_t e;
+  {
+    const uint4* src = static_cast<const uint4*>(X);
+    uint4* dst = reinterpret_cast<uint4*>(Xslow);
+    const int32_t* sidx = idx + T;
+    const int32_t* cnt = counts + 1;
+    int64_t rv = d * 2 / 16;
+    int TT = int(T);
+    void* args[] = {&src, &dst, &sidx, &cnt, &rv, &TT};
+    if ((e = launch_pdl(reinterpret_cast<const void*>(gather_rows_kernel), dim3(296), dim3(256), 0, s, args)) !=
+        cudaSuccess)
+      return e;
+  }
+  SkinnyArgs sl{};
+  sl.n_rows = int(d_out);
+  sl.K = int(d);
+  sl.n_tok_dev = counts + 1;
+  sl.Y = Y;
+  sl.ldy = d_out;
+  sl.tok_map = idx + T;
+  sl.err = err;
+  return launch_skinny(W, d_out, Xslow, T, int(d), int(T), sl, s);
+}
+
 cudaError_t launch_tensor_path(const TensorArgs& t, cudaStream_t s) {
   cudaError_t e;
   const int64_t d = t.d, k = t.k, T = t.T, d_out = t.d_out;
@@ -619,12 +921,15 @@ cudaError_t launch_tensor_path(const TensorArgs& t, cudaStream_t s) {
   g.C = t.G;
   g.ldc = k;
   g.err = t.err;
-  // 128 x 256 tiles where k >= 256 (at k = 256, X is read once) and K cut
-  // into kGSplit slices for parallelism; the finalize kernel adds the slices
-  const int gsplit = int(cdiv(d, kBK)) < kGSplit ? int(cdiv(d, kBK)) : kGSplit;  // each slice >= 1 k-block
+  // Prefill-sized T: 128 x 256 tiles where k >= 256 (at k = 256, X is read
+  // once); small T: 128 x 64 tiles (one 128-row tile holds every token, so
+  // narrower tiles give more CTAs).  K is cut into g_split(T) slices for
+  // parallelism; the finalize kernel adds the slices.
+  const int gsplit = int(cdiv(d, kBK)) < g_split(T) ? int(cdiv(d, kBK)) : g_split(T);  // each slice >= 1 k-block
   g.ksplit = gsplit;
   g.c_split = T * k;
-  if ((e = launch_tc_gemm(t.X, T, t.Vt, k, int(d), k >= 256 ? 256 : 64, g, s)) != cudaSuccess) return e;
+  const int g_bn = (T >= kTensorMinT && k >= 256) ? 256 : 64;
+  if ((e = launch_tc_gemm(t.X, T, t.Vt, k, int(d), g_bn, g, s)) != cudaSuccess) return e;
   // 3. rho, flags, bf16 g
   {
     const void* X = t.X;
@@ -637,15 +942,19 @@ cudaError_t launch_tensor_path(const TensorArgs& t, cudaStream_t s) {
     uint8_t* flags = t.flags;
     uint16_t* Gbf = t.Gbf;
     int gs = gsplit;
-    void* args[] = {&X, &G, &gram, &dd, &kk, &TT, &eps, &rho, &flags, &Gbf, &gs};
+    int nb = fin_blocks(T, k);
+    float4* part = t.fpart;
+    uint32_t* arrive = t.fin_arrive;
+    void* args[] = {&X, &G, &gram, &dd, &kk, &TT, &eps, &rho, &flags, &Gbf, &gs, &nb, &part, &arrive};
     const size_t smem = size_t(kFinTok) * k * 4 + 8 * kFinTok * 2 * 4 + kFinTok * 4;
+    const void* kern = gsplit > 8 ? reinterpret_cast<const void*>(tc_finalize_kernel<kGSplitMax>)
+                                  : reinterpret_cast<const void*>(tc_finalize_kernel<8>);
     if (smem > 48 * 1024) {
-      if ((e = cudaFuncSetAttribute(tc_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem))) !=
-          cudaSuccess)
+      if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem))) != cudaSuccess)
         return e;
     }
-    if ((e = launch_pdl(reinterpret_cast<const void*>(tc_finalize_kernel), dim3(unsigned(cdiv(T, kFinTok))),
-                        dim3(256), smem, s, args)) != cudaSuccess)
+    if ((e = launch_pdl(kern, dim3(unsigned(cdiv(T, kFinTok)), unsigned(nb)), dim3(256), smem, s, args)) !=
+        cudaSuccess)
       return e;
   }
   // 4. compaction and gathers
@@ -674,7 +983,29 @@ cudaError_t launch_tensor_path(const TensorArgs& t, cudaStream_t s) {
         cudaSuccess)
       return e;
   }
-  // 5. Y_fast = G_fast M^T, Y_slow = X_slow W^T (rows scattered to token positions)
+  // 5. Y_fast = G_fast M^T, Y_slow = X_slow W^T (rows scattered to token
+  // positions).  Below prefill size the weights are the MMA's 128-row side
+  // and the tokens its narrow side (the few-token contraction).
+  if (T < kTensorMinT) {
+    SkinnyArgs f{};
+    f.n_rows = int(d_out);
+    f.K = int(k);
+    f.n_tok_dev = t.counts;
+    f.Y = t.Y;
+    f.ldy = d_out;
+    f.tok_map = t.idx;
+    f.err = t.err;
+    if ((e = launch_skinny(t.M, d_out, t.Gfast, T, int(k), int(T), f, s)) != cudaSuccess) return e;
+    SkinnyArgs sl{};
+    sl.n_rows = int(d_out);
+    sl.K = int(d);
+    sl.n_tok_dev = t.counts + 1;
+    sl.Y = t.Y;
+    sl.ldy = d_out;
+    sl.tok_map = t.idx + T;
+    sl.err = t.err;
+    return launch_skinny(t.W, d_out, t.Xslow, T, int(d), int(T), sl, s);
+  }
   TcArgs f{};
   f.rows_dev = t.counts;
   f.N = int(d_out);
@@ -692,11 +1023,8 @@ cudaError_t launch_tensor_path(const TensorArgs& t, cudaStream_t s) {
   sl.ldc = d_out;
   sl.row_map = t.idx + T;
   sl.err = t.err;
-  // Prefill-sized T: 256 token rows per CTA (two 128-row tiles), so W is
-  // read from L2 once per 256 slow tokens.  Small T: W dominates the bytes
-  // and one 128-row tile holds every slow token, so 64-row tiles of W spread
-  // it over as many CTAs as possible.
-  if (T < kTensorMinT) return launch_tc_gemm(t.Xslow, T, t.W, d_out, int(d), 64, sl, s, 1);
+  // 256 token rows per CTA (two 128-row tiles), so W is read from L2 once
+  // per 256 slow tokens
   return launch_tc_gemm(t.Xslow, T, t.W, d_out, int(d), 256, sl, s, 2);
 }
 
