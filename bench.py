@@ -740,6 +740,28 @@ def probe_map(role, eps):
     print(json.dumps({"probe_map": role, "eps": eps, "flag": int(F[0])}))
 
 
+def probe_prefill(calls=3):
+    """A small case of the prefill map for ncu: `calls` gsi_linear calls of
+    the T=2048 map (AUTO: the tensor-core path) on the default stream."""
+    import __graft_entry__
+
+    __graft_entry__.build()
+    import gated_rank_subspace_gb300 as gsi
+
+    m_in = synth.config5()
+    m = gsi.make_map(m_in.W.cuda(), m_in.V.cuda())
+    X = m_in.X.cuda()
+    T = X.shape[0]
+    ws = gsi.new_workspace(gsi.workspace_size(m, T, "auto"))
+    Y = torch.empty(T, m.d_out, device="cuda")
+    F = torch.empty(T, dtype=torch.uint8, device="cuda")
+    for _ in range(calls):
+        gsi.linear(m, X, EPS, Y=Y, flags=F, workspace=ws, want_rho=False)
+    torch.cuda.synchronize()
+    assert gsi.workspace_status(ws) == 0
+    print(json.dumps({"probe_prefill": calls, "n_slow": int(F.sum())}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -763,6 +785,8 @@ def main():
     ap.add_argument("--probe-batch", default=None, metavar="T:f",
                     help="only run 4 decode steps of T tokens (slow fraction f) through 2 layers of the 13B "
                          "maps and print each call's algorithmic bytes (a small case for ncu)")
+    ap.add_argument("--probe-prefill", action="store_true",
+                    help="only run 3 calls of the prefill map (T=2048, tensor-core path; a small case for ncu)")
     ap.add_argument("--probe-eps", type=float, default=0.0,
                     help="threshold of the --probe-map calls (0: every token slow)")
     ap.add_argument("--eps-sweep", action="store_true",
@@ -799,6 +823,9 @@ def main():
         return
     if args.probe_batch:
         probe_batch(args.probe_batch)
+        return
+    if args.probe_prefill:
+        probe_prefill()
         return
     if args.impl == "reference":
         run_reference(args)

@@ -25,7 +25,7 @@ LIB_PATH = os.path.join(_PKG, "libgsi.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "gsi.h")
 
 GSI_F32, GSI_BF16 = 0, 1
-PATHS = {"auto": 0, "stream": 1, "tensor": 2, "fused": 3}
+PATHS = {"auto": 0, "stream": 1, "tensor": 2, "fused": 3, "batch": 4}
 STATUS = {0: "GSI_OK", 1: "GSI_ERR_INVALID_ARG", 2: "GSI_ERR_UNSUPPORTED", 3: "GSI_ERR_CUDA",
           4: "GSI_ERR_WORKSPACE", 5: "GSI_ERR_TIMEOUT"}
 

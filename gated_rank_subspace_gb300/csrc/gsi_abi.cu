@@ -143,15 +143,37 @@ static bool fused_fits(const gsi_map_desc* m, int64_t T) {
   return p.ok;
 }
 
-// Resolve the path for a call: the single-launch decode for T <= 2 where it
-// fits, the tensor cores for bf16 maps at prefill-sized T, the two-launch
-// streaming kernels otherwise.
+// The small-batch decode kernel takes bf16 maps (with their Gram) at
+// 2 <= T <= 16 where its plan fits a device of kBatchNominalCtas co-resident
+// CTAs (host-only arithmetic; the run-time plan uses the device's own grid
+// and falls back where it does not fit).
+constexpr int kBatchNominalCtas = 112;
+static bool batch_fits(const gsi_map_desc* m, int64_t T) {
+  if (m->dtype != GSI_BF16 || m->gram == nullptr) return false;
+  return plan_batch(m->d, m->d_out, m->k, T, kBatchNominalCtas, kSmemOptinSm100).ok;
+}
+
+// The path a call takes without the small-batch kernel: the single-launch
+// decode for T <= 2 where it fits, the tensor cores for bf16 maps from
+// kTensorAutoMinT tokens, the two-launch streaming kernels otherwise.
+static gsi_path classic_path(const gsi_map_desc* m, int64_t T) {
+  if (fused_fits(m, T)) return GSI_PATH_FUSED;  // falls back to STREAM at run time where the device cannot run it
+  return (m->dtype == GSI_BF16 && T >= kTensorAutoMinT) ? GSI_PATH_TENSOR : GSI_PATH_STREAM;
+}
+
+// Resolve the path for a call: the single-token decode for T = 1, the
+// small-batch decode for bf16 maps at 2 <= T <= 16, otherwise classic_path.
 static gsi_status resolve_path(const gsi_map_desc* m, int64_t T, gsi_path path, gsi_path* out) {
   if (path == GSI_PATH_AUTO) {
-    if (fused_fits(m, T))
-      *out = GSI_PATH_FUSED;  // falls back to STREAM at run time where the device cannot run it
-    else
-      *out = (m->dtype == GSI_BF16 && T >= kTensorAutoMinT) ? GSI_PATH_TENSOR : GSI_PATH_STREAM;
+    *out = (T >= 2 && batch_fits(m, T)) ? GSI_PATH_BATCH : classic_path(m, T);
+    return GSI_OK;
+  }
+  if (path == GSI_PATH_BATCH) {
+    if (!(T >= kBatchMinT && T <= kBatchMaxT && batch_fits(m, T)))
+      return fail(GSI_ERR_UNSUPPORTED,
+                  "the small-batch decode takes bf16 maps with their Gram, 2 <= T <= 16, k a multiple of 64 "
+                  "(at most 512), d a multiple of 8 and at most 160 output rows a CTA");
+    *out = GSI_PATH_BATCH;
     return GSI_OK;
   }
   if (path == GSI_PATH_STREAM) {
@@ -177,6 +199,11 @@ static gsi_status resolve_path(const gsi_map_desc* m, int64_t T, gsi_path path, 
 // streaming path, so a device that cannot run it can fall back to the
 // two-launch kernels on the same workspace.
 static size_t path_ws(const gsi_map_desc* m, int64_t T, gsi_path p) {
+  if (p == GSI_PATH_BATCH) {
+    // also large enough for the path a device that cannot run it falls back to
+    const size_t b = layout_batch(m->k, T).total, c = path_ws(m, T, classic_path(m, T));
+    return b > c ? b : c;
+  }
   if (p == GSI_PATH_TENSOR) return layout_tensor(m->d, m->k, T).total;
   const size_t st = layout_stream(m->d, m->k, m->dtype == GSI_BF16 ? 2 : 4, T).total;
   if (p != GSI_PATH_FUSED) return st;
@@ -195,6 +222,7 @@ struct DeviceFacts {
   int clusters[2][2][2] = {};  // co-resident clusters per [dtype][fused][cs == 16]; -1: not possible
   int decode_clusters[2] = {};  // co-resident clusters of the single-token decode kernel per dtype
   int stack_clusters[2][2] = {};  // ... of the persistent stack kernel per [dtype][two vectors a lane]
+  int batch_clusters = 0;          // ... of the small-batch decode kernel
 };
 
 // Shared memory of the two-launch decide-and-apply kernel: the device limit
@@ -251,6 +279,20 @@ static int decode_clusters(DeviceFacts* f, gsi_dtype dt) {
   int& c = f->decode_clusters[dt == GSI_BF16];
   if (c == 0) {
     const int n = decode_max_clusters(size_t(f->smem_optin), dt);
+    c = n > 0 ? n : -1;
+  }
+  return c > 0 ? c : 0;
+}
+
+// Co-resident clusters of the small-batch decode kernel (cached); 0 if none.
+// Every launch uses this grid, so the workspace's call numbers (tickets / grid
+// size) stay consistent across calls.
+static int batch_clusters(DeviceFacts* f) {
+  static std::mutex mu;
+  std::lock_guard<std::mutex> lock(mu);
+  int& c = f->batch_clusters;
+  if (c == 0) {
+    const int n = batch_max_clusters(size_t(f->smem_optin));
     c = n > 0 ? n : -1;
   }
   return c > 0 ? c : 0;
@@ -532,6 +574,59 @@ static gsi_status run_stream(const gsi_map_desc* m, const void* X, int64_t T, fl
 }
 
 
+// Enqueue the small-batch decode for one bf16 map (2 <= T <= 16, all
+// arguments validated).  GSI_ERR_UNSUPPORTED, with nothing launched, where
+// this device cannot run it (the caller then takes classic_path).
+static gsi_status run_batch(const gsi_map_desc* m, const void* X, int64_t T, float eps, float* Y, uint8_t* flags,
+                            float* rho, void* ws, cudaStream_t st, const gsi_map_desc* next) {
+  if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
+  DeviceFacts* f = nullptr;
+  gsi_status s = device_facts(&f);
+  if (s != GSI_OK) return s;
+  const int ncl = batch_clusters(f);
+  if (ncl == 0) return fail(GSI_ERR_UNSUPPORTED, "the small-batch decode kernel cannot run on this device");
+  const BatchPlan p = plan_batch(m->d, m->d_out, m->k, T, ncl * kBatchCluster, size_t(f->smem_optin));
+  if (!p.ok || m->dtype != GSI_BF16 || !m->gram)
+    return fail(GSI_ERR_UNSUPPORTED, "the small-batch decode plan does not fit this device");
+  const BatchLayout L = layout_batch(m->k, T);
+  char* base = static_cast<char*>(ws);
+  Ctrl* ctrl = reinterpret_cast<Ctrl*>(base + L.ctrl);
+  BatchCall c{};
+  c.X = X;
+  c.W = m->W;
+  c.V = m->V;
+  c.M = m->M;
+  c.gram = m->gram;
+  c.Y = Y;
+  c.flags = flags;
+  c.rho = rho;
+  c.d = m->d;
+  c.d_out = m->d_out;
+  c.k = int(m->k);
+  c.T = int(T);
+  c.eps = eps;
+  c.part_g = reinterpret_cast<unsigned long long*>(base + L.part_g);
+  c.part_x = reinterpret_cast<unsigned long long*>(base + L.part_x);
+  c.ticket = &ctrl->ticket_b[1];
+  c.err = &ctrl->err;
+  if (next) {
+    const int nes = elem_bytes(next->dtype);
+    c.next_v = static_cast<const char*>(next->V);
+    c.next_v_bytes = uint64_t(next->d) * next->k * nes;
+    c.next_m = static_cast<const char*>(next->M);
+    c.next_m_bytes = uint64_t(next->d_out) * next->k * nes;
+    c.next_gram = reinterpret_cast<const char*>(next->gram);
+    c.next_gram_bytes = next->gram ? uint64_t(next->k) * next->k * 4 : 0;
+  }
+  if (g_withhold.load() > 0 && g_withhold.fetch_sub(1) > 0) {
+    c.dbg_withhold = 1;
+    c.poll_cycles = 20000000;  // ~10 ms
+  }
+  if (refused_coresident())
+    return fail(GSI_ERR_UNSUPPORTED, "small-batch decode kernel launch: co-resident grid refused (test hook)");
+  return coresident_status(launch_batch_decode(c, p, st), "small-batch decode kernel launch");
+}
+
 // Enqueue the tensor-core path for one bf16 map.  All arguments validated.
 static gsi_status run_tensor(const gsi_map_desc* m, const void* X, int64_t T, float eps, float* Y,
                              uint8_t* flags, float* rho, void* ws, cudaStream_t st) {
@@ -571,6 +666,11 @@ static gsi_status run_tensor(const gsi_map_desc* m, const void* X, int64_t T, fl
 static gsi_status run_path(const gsi_map_desc* m, gsi_path p, bool strict, const void* X, int64_t T, float eps,
                            float* Y, uint8_t* flags, float* rho, void* ws, cudaStream_t st,
                            const gsi_map_desc* next = nullptr) {
+  if (p == GSI_PATH_BATCH) {
+    const gsi_status s = run_batch(m, X, T, eps, Y, flags, rho, ws, st, next);
+    if (s != GSI_ERR_UNSUPPORTED || strict) return s;
+    p = classic_path(m, T);
+  }
   if (p == GSI_PATH_TENSOR) return run_tensor(m, X, T, eps, Y, flags, rho, ws, st);
   if (p == GSI_PATH_FUSED) {
     const gsi_status s = run_decide(m, X, T, eps, 0, Y, flags, rho, nullptr, nullptr, ws, st, true, next);
@@ -725,7 +825,7 @@ gsi_status gsi_linear_ex(const gsi_map_desc* map, const void* X, int64_t T, floa
   if (!flags) return fail(GSI_ERR_INVALID_ARG, "flags is NULL");
   if (rho && !aligned(rho, 4)) return fail(GSI_ERR_INVALID_ARG, "rho is misaligned");
   if ((s = check_workspace(workspace, ws_bytes, path_ws(map, T, p))) != GSI_OK) return s;
-  s = run_path(map, p, path == GSI_PATH_FUSED, X, T, eps, Y, flags, rho, workspace,
+  s = run_path(map, p, path == GSI_PATH_FUSED || path == GSI_PATH_BATCH, X, T, eps, Y, flags, rho, workspace,
                static_cast<cudaStream_t>(stream));
   return s == GSI_OK ? ok() : s;
 }

@@ -298,7 +298,10 @@ struct Ctrl {
   // the tensor path's finalize: CTAs of the current launch that have stored
   // their partial sums (the last one resets it)
   uint32_t fin_arrive;
-  uint32_t pad[47];
+  // the small-batch decode's call numbers (its grid projection's epochs), per
+  // element type
+  unsigned long long ticket_b[2];
+  uint32_t pad[42];
 };
 static_assert(sizeof(Ctrl) == 256, "Ctrl is 256 bytes");
 

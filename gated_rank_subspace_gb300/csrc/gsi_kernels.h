@@ -145,6 +145,43 @@ int decode_max_clusters(size_t smem, gsi_dtype dt);
 // The same for the persistent stack kernel (nv vectors of a row per lane).
 int stack_max_clusters(size_t smem, gsi_dtype dt, int nv);
 
+// Small-batch decode (see gsi_batch.cu): one call of a bf16 map for
+// 2 <= T <= 16 tokens in one launch.  Device pointers; part_g / part_x are
+// the workspace's epoch-tagged words (BatchLayout).
+struct BatchCall {
+  const void* X;        // T x d tokens
+  const void* W;        // d_out x d
+  const void* V;        // d x k
+  const void* M;        // d_out x k
+  const float* gram;    // k x k
+  float* Y;             // T x d_out
+  uint8_t* flags;       // T
+  float* rho;           // T, or null
+  int64_t d, d_out;
+  int k, T;
+  float eps;
+  unsigned long long* part_g;  // [clusters][T][k]
+  unsigned long long* part_x;  // [clusters][16]
+  unsigned long long* ticket;  // numbers the calls (the words' epochs)
+  uint32_t* err;               // device error word
+  // weights of the next map of a stack, staged in L2 while this one runs
+  const char* next_v;
+  uint64_t next_v_bytes;
+  const char* next_m;
+  uint64_t next_m_bytes;
+  const char* next_gram;
+  uint64_t next_gram_bytes;
+  // test hook: cluster 0 withholds its words, so the other clusters' polls
+  // give up after poll_cycles (0: the default ~2 s)
+  int dbg_withhold;
+  long long poll_cycles;
+};
+
+cudaError_t launch_batch_decode(const BatchCall& c, const BatchPlan& p, cudaStream_t s);
+// Co-resident kBatchCluster-CTA clusters of the small-batch kernel at the
+// largest shared-memory request; 0 if none.
+int batch_max_clusters(size_t smem);
+
 // Tensor-core path (bf16, prefill-sized T).  All pointers are device pointers;
 // Vt, G, Gbf, Gfast, Xslow and idx live in the call's workspace.
 struct TensorArgs {

@@ -351,4 +351,105 @@ inline DecodePlan plan_decode(int64_t d, int64_t d_out, int64_t k, int es, int n
   return p;
 }
 
+// Small-batch decode kernel geometry (see gsi_batch.cu): 2 <= T <= 16
+// tokens of a bf16 map in one launch, clusters of kBatchCluster CTAs with
+// eight compute warps and one copy warp each.  CTA b projects rows
+// [b * vr, (b + 1) * vr) of V_k and applies output rows [b * rpc, (b + 1) *
+// rpc); both are multiples of 16 (one tensor-core tile).  Shared memory
+// (offsets from a 1024-byte aligned base): mbarriers and words | g in bf16,
+// high and low halves, [2][16][k] | the decision | per-warp shares | then
+// the call's scratch: V slab (128-byte swizzled boxes of 64 columns), the
+// token slab, partial-g inbox, norm inbox, gathered g, share inbox, Gram
+// slice | M rows (swizzled boxes).  Once the flags are known (the fast
+// outputs are then in registers) the W ring -- stages of rpc x 128 columns
+// of W plus T x 128 of X -- takes the space from the scratch on, M rows
+// included; its stages end up holding the warps' partial sums for the final
+// reduction.
+constexpr int kBatchThreads = 288;
+constexpr int kBatchWarps = 8;  // compute warps (the ninth issues copies)
+constexpr int kBatchMaxT = 16;
+constexpr int kBatchMinT = 2;
+constexpr int kBatchCluster = 16;
+constexpr int kBatchMaxClusters = 16;
+constexpr int kBatchMaxMt = 10;   // output rows a CTA: at most 10 tiles of 16
+constexpr int kBatchKC = 128;     // W columns per ring stage (8 steps of 16)
+constexpr int kBatchMaxStages = 6;
+constexpr int kBatchMaxK = 512;
+constexpr int kBatchSmemSlack = 1024;  // the kernel aligns its base to 1024 bytes
+
+struct BatchPlan {
+  int T, ncta, vr, rpc, ks, kb, stages, stage_bytes;
+  int gbf_pitch, xs_pitch;
+  int off_gbf, off_dec, off_wsh, off_scr, off_v, off_xs, off_in, off_nin, off_g32, off_qin, off_gram, off_m;
+  size_t smem;  // dynamic shared memory to request (alignment slack included)
+  bool ok;
+};
+
+inline BatchPlan plan_batch(int64_t d, int64_t d_out, int64_t k, int64_t T, int ncta, size_t smem_budget) {
+  BatchPlan p{};
+  p.ok = false;
+  if (T < kBatchMinT || T > kBatchMaxT || ncta < kBatchCluster || ncta % kBatchCluster) return p;
+  if (k % 64 || k > kBatchMaxK || d % 8 || d < 16 || d_out < 1) return p;
+  if (ncta > kBatchCluster * kBatchMaxClusters) return p;
+  p.T = int(T);
+  p.ncta = ncta;
+  p.vr = int(rup(cdiv(d, ncta), 16));
+  p.rpc = int(rup(cdiv(d_out, ncta), 16));
+  if (p.vr > 256 || p.rpc > 16 * kBatchMaxMt) return p;
+  p.ks = int(k / kBatchCluster);
+  p.kb = int(k / 64);
+  p.gbf_pitch = int(k * 2 + 16);
+  p.xs_pitch = p.vr * 2 + 16;
+  size_t off = 1024;  // mbarriers and CTA words
+  auto take = [&](size_t bytes, size_t align) {
+    off = (off + align - 1) / align * align;
+    const size_t at = off;
+    off += bytes;
+    return int(at);
+  };
+  p.off_gbf = take(size_t(2) * kBatchMaxT * p.gbf_pitch, 128);
+  p.off_dec = take(size_t(2) * kBatchMaxT * 4, 128);
+  p.off_wsh = take(size_t(kBatchWarps) * kBatchMaxT * 2 * 4, 128);
+  p.off_scr = take(0, 1024);
+  p.off_v = take(size_t(p.kb) * p.vr * 128, 1024);
+  p.off_xs = take(size_t(kBatchMaxT) * p.xs_pitch, 128);
+  p.off_in = take(size_t(kBatchCluster) * T * p.ks * 4, 128);
+  p.off_nin = take(size_t(kBatchCluster) * kBatchMaxT * 4, 128);
+  p.off_g32 = take(size_t(T) * k * 4 + kBatchMaxT * 4, 128);  // g, then the 16 norms
+  p.off_qin = take(size_t(kBatchCluster) * kBatchMaxT * 8, 128);
+  p.off_gram = take(size_t(p.ks) * k * 4, 128);
+  p.off_m = take(size_t(p.kb) * p.rpc * 128, 1024);
+  const size_t end_m = off;
+  p.stage_bytes = int(rup(int64_t(p.rpc) * 256 + kBatchMaxT * 256, 1024));
+  const size_t budget = smem_budget > kBatchSmemSlack ? smem_budget - kBatchSmemSlack : 0;
+  if (end_m > budget) return p;
+  int s = int((budget - size_t(p.off_scr)) / size_t(p.stage_bytes));
+  if (s > kBatchMaxStages) s = kBatchMaxStages;
+  if (s < 2) return p;
+  // the warps' partial sums [8][16][rpc] float32 reuse the ring's stages
+  if (size_t(s) * p.stage_bytes < size_t(kBatchWarps) * kBatchMaxT * p.rpc * 4) return p;
+  p.stages = s;
+  const size_t end_ring = size_t(p.off_scr) + size_t(s) * p.stage_bytes;
+  p.smem = (end_ring > end_m ? end_ring : end_m) + kBatchSmemSlack;
+  p.ok = p.smem <= smem_budget;
+  return p;
+}
+
+// Workspace of a small-batch call: the control block, then each cluster's
+// projections [clusters][T][k] and norms [clusters][16] as 64-bit
+// epoch-tagged words.
+struct BatchLayout {
+  size_t ctrl, part_g, part_x, total;
+};
+
+inline BatchLayout layout_batch(int64_t k, int64_t T) {
+  BatchLayout L{};
+  size_t off = 0;
+  L.ctrl = off;    off += 256;
+  L.part_g = off;  off += align256(size_t(kBatchMaxClusters) * T * k * 8);
+  L.part_x = off;  off += align256(size_t(kBatchMaxClusters) * kBatchMaxT * 8);
+  L.total = off;
+  return L;
+}
+
 }  // namespace gsi

@@ -79,10 +79,22 @@ typedef enum gsi_dtype { GSI_F32 = 0, GSI_BF16 = 1 } gsi_dtype;
  *             projects on its share of V, with a grid barrier on the
  *             workspace where V does not fit a cluster;
  *   STREAM -- two launches (projection kernel, then decide-and-apply), any T;
- *   TENSOR -- tcgen05 contractions, bf16 only, for prefill-sized T.
- * AUTO picks FUSED for T <= 2 where a slab of V fits shared memory (and
- * STREAM at run time on a device that cannot hold the fused grid), TENSOR
- * for bf16 with T >= 16, STREAM otherwise.  Where the fused kernels' CTAs
+ *   TENSOR -- tcgen05 contractions, bf16 only, for prefill-sized T;
+ *   BATCH  -- bf16 maps, 2 <= T <= 16: the small-batch decode kernel, one
+ *             launch per call.  Every CTA projects its slab of V on all T
+ *             tokens, the clusters exchange slices of G through epoch-tagged
+ *             words in the workspace, every CTA takes the same flags, and the
+ *             three products (X V, G M^T for the fast tokens, X W^T for the
+ *             slow ones) run as warp-level tensor-core products (bf16
+ *             operands, float32 accumulation; G enters M G as a high and a
+ *             low bf16 part).  Needs k a multiple of 64 (at most 512), d a
+ *             multiple of 8 and d_out / (grid size) at most 160 rows.
+ * AUTO picks FUSED for T = 1, and for T = 2 on float32 maps, where a slab of
+ * V fits shared memory (and STREAM at run time on a device that cannot hold
+ * the fused grid); BATCH for bf16 maps with 2 <= T <= 16 where its plan
+ * fits; TENSOR for bf16 maps with T >= 9 otherwise; STREAM otherwise.  BATCH
+ * and FUSED fall back to those choices at run time where the device cannot
+ * run them.  Where the fused kernels' CTAs
  * wait on other clusters, they are launched as a co-resident (cooperative)
  * grid: a grid that cannot be co-resident is refused at launch, and AUTO
  * then runs the call on the STREAM kernels.  GSI_COOPERATIVE=0 in the
@@ -96,7 +108,8 @@ typedef enum gsi_path {
   GSI_PATH_AUTO = 0,
   GSI_PATH_STREAM = 1,
   GSI_PATH_TENSOR = 2,
-  GSI_PATH_FUSED = 3
+  GSI_PATH_FUSED = 3,
+  GSI_PATH_BATCH = 4
 } gsi_path;
 
 /* One linear map with its cached artefacts (all device pointers). */
