@@ -406,7 +406,7 @@ def run_config4(gsi, dev, stream, hbm_peak, reps=2):
     out = {"workload": "13B-class linears (qkv 15360x5120, out 5120^2, up 13824x5120, down 5120x13824), "
                        "40 layers, bf16, k=320, eps=0.05; each decode step one gsi_stack call over the 160 maps",
            "points": points,
-           "kernels": "T=1: decode_kernel per map; T=4, 16: project_kernel + decide_apply_kernel per map"}
+           "kernels": "T=1: decode_kernel per map; T=4, 16: batch_decode_kernel (small-batch decode) per map"}
     del maps, ws
     torch.cuda.empty_cache()
     return out

@@ -172,7 +172,7 @@ static gsi_status resolve_path(const gsi_map_desc* m, int64_t T, gsi_path path, 
     if (!(T >= kBatchMinT && T <= kBatchMaxT && batch_fits(m, T)))
       return fail(GSI_ERR_UNSUPPORTED,
                   "the small-batch decode takes bf16 maps with their Gram, 2 <= T <= 16, k a multiple of 64 "
-                  "(at most 512), d a multiple of 8 and at most 160 output rows a CTA");
+                  "(at most 384), d a multiple of 8 and at most 160 output rows a CTA");
     *out = GSI_PATH_BATCH;
     return GSI_OK;
   }
@@ -347,7 +347,8 @@ static int decode_nv(const gsi_map_desc* m) { return m->k * elem_bytes(m->dtype)
 // Enqueue the single-token decode kernel (all arguments validated);
 // GSI_ERR_UNSUPPORTED, with nothing launched, when its plan does not fit.
 static gsi_status run_decode(const gsi_map_desc* m, const void* X, float eps, float* Y, uint8_t* flags, float* rho,
-                             void* ws, cudaStream_t st, DeviceFacts* f, const gsi_map_desc* next) {
+                             void* ws, cudaStream_t st, DeviceFacts* f, const gsi_map_desc* next,
+                             const void* next_x) {
   const DecodePlan p = decode_plan(m, f);
   if (!p.ok) return GSI_ERR_UNSUPPORTED;
   Ctrl* ctrl = static_cast<Ctrl*>(ws);
@@ -368,6 +369,10 @@ static gsi_status run_decode(const gsi_map_desc* m, const void* X, float eps, fl
     a.next_m_bytes = uint64_t(next->d_out) * next->k * nes;
     a.next_gram = reinterpret_cast<const char*>(next->gram);
     a.next_gram_bytes = next->gram ? uint64_t(next->k) * next->k * 4 : 0;
+    if (next_x) {
+      a.next_x = static_cast<const char*>(next_x);
+      a.next_x_bytes = uint64_t(next->d) * nes;
+    }
   }
   a.err = &ctrl->err;
   if (p.grid && g_withhold.load() > 0 && g_withhold.fetch_sub(1) > 0) {
@@ -428,7 +433,7 @@ static gsi_status run_stack_decode(const gsi_map_desc* maps, int n, const void* 
 // run on this device, so that callers may fall back to the two launches.
 static gsi_status run_decide(const gsi_map_desc* m, const void* X, int64_t T, float eps, int mode, float* Y,
                              uint8_t* flags, float* rho, float* G, const float* Gin, void* ws, cudaStream_t st,
-                             bool fused = false, const gsi_map_desc* next = nullptr) {
+                             bool fused = false, const gsi_map_desc* next = nullptr, const void* next_x = nullptr) {
   const int es = elem_bytes(m->dtype);
   const GatePlan gp = plan_gate(m->d, m->k, es, T);
   const StreamLayout L = layout_stream(m->d, m->k, es, T);
@@ -441,7 +446,7 @@ static gsi_status run_decide(const gsi_map_desc* m, const void* X, int64_t T, fl
   DecidePlan dp{};
   if (fused && mode == 0 && T == 1) {
     // one token: the single-token decode kernel where the basis fits a cluster
-    s = run_decode(m, X, eps, Y, flags, rho, ws, st, f, next);
+    s = run_decode(m, X, eps, Y, flags, rho, ws, st, f, next, next_x);
     if (s != GSI_ERR_UNSUPPORTED) return s;
   }
   if (fused) {
@@ -578,7 +583,7 @@ static gsi_status run_stream(const gsi_map_desc* m, const void* X, int64_t T, fl
 // arguments validated).  GSI_ERR_UNSUPPORTED, with nothing launched, where
 // this device cannot run it (the caller then takes classic_path).
 static gsi_status run_batch(const gsi_map_desc* m, const void* X, int64_t T, float eps, float* Y, uint8_t* flags,
-                            float* rho, void* ws, cudaStream_t st, const gsi_map_desc* next) {
+                            float* rho, void* ws, cudaStream_t st, const gsi_map_desc* next, const void* next_x) {
   if (injected_failure()) return fail(GSI_ERR_CUDA, "injected failure (gsi_debug_fail_after)");
   DeviceFacts* f = nullptr;
   gsi_status s = device_facts(&f);
@@ -617,6 +622,10 @@ static gsi_status run_batch(const gsi_map_desc* m, const void* X, int64_t T, flo
     c.next_m_bytes = uint64_t(next->d_out) * next->k * nes;
     c.next_gram = reinterpret_cast<const char*>(next->gram);
     c.next_gram_bytes = next->gram ? uint64_t(next->k) * next->k * 4 : 0;
+    if (next_x) {
+      c.next_x = static_cast<const char*>(next_x);
+      c.next_x_bytes = uint64_t(T) * next->d * nes;
+    }
   }
   if (g_withhold.load() > 0 && g_withhold.fetch_sub(1) > 0) {
     c.dbg_withhold = 1;
@@ -665,15 +674,15 @@ static gsi_status run_tensor(const gsi_map_desc* m, const void* X, int64_t T, fl
 // streaming kernels when the device cannot run it and `strict` is false).
 static gsi_status run_path(const gsi_map_desc* m, gsi_path p, bool strict, const void* X, int64_t T, float eps,
                            float* Y, uint8_t* flags, float* rho, void* ws, cudaStream_t st,
-                           const gsi_map_desc* next = nullptr) {
+                           const gsi_map_desc* next = nullptr, const void* next_x = nullptr) {
   if (p == GSI_PATH_BATCH) {
-    const gsi_status s = run_batch(m, X, T, eps, Y, flags, rho, ws, st, next);
+    const gsi_status s = run_batch(m, X, T, eps, Y, flags, rho, ws, st, next, next_x);
     if (s != GSI_ERR_UNSUPPORTED || strict) return s;
     p = classic_path(m, T);
   }
   if (p == GSI_PATH_TENSOR) return run_tensor(m, X, T, eps, Y, flags, rho, ws, st);
   if (p == GSI_PATH_FUSED) {
-    const gsi_status s = run_decide(m, X, T, eps, 0, Y, flags, rho, nullptr, nullptr, ws, st, true, next);
+    const gsi_status s = run_decide(m, X, T, eps, 0, Y, flags, rho, nullptr, nullptr, ws, st, true, next, next_x);
     if (s != GSI_ERR_UNSUPPORTED || strict) return s;
   }
   return run_stream(m, X, T, eps, Y, flags, rho, nullptr, ws, st, true, next);
@@ -1060,7 +1069,7 @@ gsi_status gsi_stack_ex(const gsi_map_desc* maps, int64_t n_maps, const void* co
     gsi_path p;
     resolve_path(&maps[i], T, GSI_PATH_AUTO, &p);
     s = run_path(&maps[i], p, false, X[i], T, eps, Y[i], flags[i], nullptr, workspace, st,
-                 i + 1 < n_maps ? &maps[i + 1] : nullptr);
+                 i + 1 < n_maps ? &maps[i + 1] : nullptr, i + 1 < n_maps ? X[i + 1] : nullptr);
     if (s != GSI_OK) return fail(s, "map %lld: %s", (long long)i, g_err.c_str());
     ++i;
   }

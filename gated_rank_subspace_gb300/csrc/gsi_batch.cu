@@ -115,12 +115,21 @@ __device__ __forceinline__ void st_async_v2(uint32_t raddr, float a, float b, ui
                : "memory");
 }
 
+// Bulk copy of this CTA's shared memory into a peer's (16-byte aligned,
+// multiple of 16 bytes), completing on the peer's mbarrier; the issuing
+// thread tracks it in its bulk async-group.
+__device__ __forceinline__ void bulk_s2c(uint32_t dst_cluster, const void* src, uint32_t bytes, uint32_t bar_cluster) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst_cluster),
+               "r"(sa(src)), "r"(bytes), "r"(bar_cluster)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// The sources of this thread's bulk copies have been read.
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 // The eight compute warps only (named barrier 1).
 __device__ __forceinline__ void compute_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-
-__device__ __forceinline__ void cluster_arrive_release() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
 
 // Byte offset of the 16-byte chunk `ch` (0..7) of row `row` in a box of
 // 128-byte rows written by TMA with 128-byte swizzle (1024-byte aligned).
@@ -142,7 +151,7 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_decode_kernel(const __
   const BatchCall& c = a.c;
   const BatchPlan& p = a.p;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  if (!cluster_shape_ok(CS) || gridDim.x % CS != 0 || gridDim.x / CS > kBatchMaxClusters) {
+  if (gridDim.x % CS != 0 || gridDim.x / CS > kBatchMaxClusters) {
     if (tid == 0) atomicOr(c.err, kErrTimeout | kErrLaunchShape);
     return;  // before any barrier, copy or access to another CTA
   }
@@ -180,8 +189,12 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_decode_kernel(const __
   unsigned char* xs = smem + p.off_xs;                      // [16][xs_pitch] token slab
   float* inbox = reinterpret_cast<float*>(smem + p.off_in);  // [CS][T][ks]
   float* nin = reinterpret_cast<float*>(smem + p.off_nin);   // [CS][16]
-  float* g32 = reinterpret_cast<float*>(smem + p.off_g32);   // [T][k]
+  float* g32 = reinterpret_cast<float*>(smem + p.off_g32);   // [CS][T][ks]: g by column slice
   float* gnx = g32 + T * k;                                  // [16] ||x_t||^2
+  float* gt = inbox;                                         // [T][k]: g by token, once the inboxes are read
+  float* pg = reinterpret_cast<float*>(gbf);                 // [CS][T][ks]: this CTA's partial g
+  float* fs = reinterpret_cast<float*>(smem + p.off_fs);     // [T][ks] this rank's final slice, then 16 norms
+  float* nxs = reinterpret_cast<float*>(smem + p.off_nx);    // [16] the slab's ||x_t||^2
   float2* qin = reinterpret_cast<float2*>(smem + p.off_qin);  // [CS][16]
   const float* gram_s = reinterpret_cast<const float*>(smem + p.off_gram);  // [ks][k]
   unsigned char* ms = smem + p.off_m;                       // kb boxes of [rpc][128 B]
@@ -223,18 +236,17 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_decode_kernel(const __
       bar_expect_tx(vbar, uint32_t(kb * p.vr * 128));
       for (int b = 0; b < kb; ++b) tma2d(vs + b * p.vr * 128, &a.tv, vbar, b * 64, int(v0));
     }
-    if (nrows > 0) {
-      bar_expect_tx(mbar, uint32_t(kb * p.rpc * 128));
-      for (int b = 0; b < kb; ++b) tma2d(ms + b * p.rpc * 128, &a.tm, mbar, b * 64, int(r0));
-    }
     const uint32_t gb = uint32_t(ks) * uint32_t(k) * 4u;
     bar_expect_tx(gbar, gb);
     bulk_g2s(smem + p.off_gram, c.gram + int64_t(c0) * k, gb, gbar);
   }
-  if (tid == 64 || tid == 96 || tid == 128) {
-    // this CTA's share of the next map's weights, into L2
-    const char* base = tid == 64 ? c.next_v : tid == 96 ? c.next_m : c.next_gram;
-    const uint64_t total = tid == 64 ? c.next_v_bytes : tid == 96 ? c.next_m_bytes : c.next_gram_bytes;
+  if (tid == 64 || tid == 96 || tid == 128 || tid == 160) {
+    // this CTA's share of the next map's weights and tokens, into L2
+    const char* base = tid == 64 ? c.next_v : tid == 96 ? c.next_m : tid == 128 ? c.next_gram : c.next_x;
+    const uint64_t total = tid == 64    ? c.next_v_bytes
+                           : tid == 96  ? c.next_m_bytes
+                           : tid == 128 ? c.next_gram_bytes
+                                        : c.next_x_bytes;
     if (base && total) {
       const uint64_t share = ((total + gridDim.x - 1) / gridDim.x + 15) / 16 * 16;
       const uint64_t off = uint64_t(blockIdx.x) * share;
@@ -247,6 +259,7 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_decode_kernel(const __
   // ---- the tokens' elements of this CTA's slab: [16][vr] bf16 (zeros past T and d)
   {
     const int vpt = p.vr / 8;  // 16-byte vectors of a token's slab
+#pragma unroll 1
     for (int e = tid; e < kBatchMaxT * vpt; e += kBatchThreads) {
       const int t = e / vpt, j = e - t * vpt;
       const int64_t col = v0 + 8 * j;
@@ -256,6 +269,13 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_decode_kernel(const __
     }
   }
   __syncthreads();
+  if (warp == NW && lane == 0 && nrows > 0) {
+    // the M rows once the V slab has landed: the projection waits for V, the
+    // fast products only several exchanges later
+    if (has_v) note(bar_wait(vbar, 0, err, lim, kWaitV));
+    bar_expect_tx(mbar, uint32_t(kb * p.rpc * 128));
+    for (int b = 0; b < kb; ++b) tma2d(ms + b * p.rpc * 128, &a.tm, mbar, b * 64, int(r0));
+  }
 
   // ---- projection: this warp's 8-column tiles of g over the slab
   constexpr int kNtW = kBatchMaxK / 8 / NW;  // tiles a warp (k <= kBatchMaxK)
@@ -293,27 +313,47 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_decode_kernel(const __
     }
     nx0 = warp_sum(nx0);
     nx1 = warp_sum(nx1);
-  }
-  cluster_wait();  // every CTA of the cluster runs and has initialised its barriers
-
-  if (warp < NW) {
-    // ---- reduce-scatter: the accumulators go to the ranks owning their columns
+    // the accumulators by column slice (the slice of rank q contiguous), the
+    // norms beside them, for the bulk copies of the reduce-scatter
 #pragma unroll
     for (int j = 0; j < kNtW; ++j) {
       const int nt = warp + j * NW;
       if (nt < n_nt) {
         const int col = nt * 8 + 2 * t4;
         const int q = col / ks, cc = col - q * ks;
-        const uint32_t rb = map_rank(sa(xbar), q);
-        if (g_ < T) st_async_v2(map_rank(sa(inbox + (rank * T + g_) * ks + cc), q), pacc[j][0], pacc[j][1], rb);
+        if (g_ < T) *reinterpret_cast<float2*>(pg + (q * T + g_) * ks + cc) = make_float2(pacc[j][0], pacc[j][1]);
         if (g_ + 8 < T)
-          st_async_v2(map_rank(sa(inbox + (rank * T + g_ + 8) * ks + cc), q), pacc[j][2], pacc[j][3], rb);
+          *reinterpret_cast<float2*>(pg + (q * T + g_ + 8) * ks + cc) = make_float2(pacc[j][2], pacc[j][3]);
       }
     }
     if (lane == 0) {
-      const uint32_t rb = map_rank(sa(xbar), 0);
-      st_async_f32(map_rank(sa(nin + rank * kBatchMaxT + warp), 0), nx0, rb);
-      st_async_f32(map_rank(sa(nin + rank * kBatchMaxT + warp + NW), 0), nx1, rb);
+      nxs[warp] = nx0;
+      nxs[warp + NW] = nx1;
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    compute_sync();
+  }
+  // The cluster shape, checked before the first access to another CTA (read
+  // here, off the path to the token load).  Without it this CTA waits
+  // (bounded) for its own copies and leaves.
+  if (!cluster_shape_ok(CS)) {
+    if (warp == NW && lane == 0) {
+      if (nrows > 0) bar_wait(mbar, 0, err, kSpinCyclesAfterError, kWaitM);
+      bar_wait(gbar, 0, err, kSpinCyclesAfterError, kWaitGram);
+    }
+    if (tid == 0) atomicOr(err, kErrTimeout | kErrLaunchShape);
+    return;
+  }
+  cluster_wait();  // every CTA of the cluster runs and has initialised its barriers
+
+  if (warp < NW) {
+    // ---- reduce-scatter: rank q receives every rank's slice q, and rank 0
+    //      every rank's norms, by one bulk copy each
+    if (tid < CS) {  // lane q of warp 0 sends slice q (lane 0: the norms too)
+      const int q = tid;
+      bulk_s2c(map_rank(sa(inbox + rank * T * ks), q), pg + q * T * ks, uint32_t(T * ks * 4), map_rank(sa(xbar), q));
+      if (q == 0) bulk_s2c(map_rank(sa(nin + rank * kBatchMaxT), 0), nxs, kBatchMaxT * 4, map_rank(sa(xbar), 0));
+      bulk_commit();
     }
     note(bar_wait_cluster(xbar, 0, err, lim, kWaitPartials));
 
@@ -374,54 +414,101 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_decode_kernel(const __
           s0 += v0s[q];
           s1 += v1s[q];
         }
-      const uint32_t dst = sa(gitem ? g32 + t * k + c0 + cc : gnx + tn), rb = sa(gxbar);
-      for (int q = 0; q < CS; ++q) st_async_v2(map_rank(dst, q), s0, s1, map_rank(rb, q));
+      *reinterpret_cast<float2*>(gitem ? fs + t * ks + cc : fs + T * ks + tn) = make_float2(s0, s1);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    compute_sync();
+    // ---- all-gather: this rank's final slice (rank 0: and the norms) to every rank
+    if (tid < CS) {  // lane q of warp 0 sends this rank's slice (rank 0: and the norms) to rank q
+      const int q = tid;
+      bulk_s2c(map_rank(sa(g32 + rank * T * ks), q), fs, uint32_t(T * ks * 4), map_rank(sa(gxbar), q));
+      if (rank == 0) bulk_s2c(map_rank(sa(gnx), q), fs + T * ks, kBatchMaxT * 4, map_rank(sa(gxbar), q));
+      bulk_commit();
     }
     note(bar_wait_cluster(gxbar, 0, err, lim, kWaitGathered));
+    if (tid < CS) bulk_wait_read();  // the partial g's space is about to hold g in bf16
+    // g by token (in the inboxes' space: every item has read them), so that
+    // the products below read consecutive columns of a token
+    {
+      const int f4s = ks / 4, per_q = T * f4s;
+#pragma unroll 1
+      for (int f = tid; f < CS * per_q; f += NC) {
+        const int q = f / per_q, r = f - q * per_q, t = r / f4s, c4 = r - t * f4s;
+        *reinterpret_cast<float4*>(gt + t * k + q * ks + 4 * c4) = reinterpret_cast<const float4*>(g32)[f];
+      }
+    }
+    compute_sync();
 
     // ---- shares of the Gram form: warp w, Gram rows c0 + w, c0 + w + 8, ...
     //      lane l takes the column groups l, l + 32, ... (float4)
     {
       note(__all_sync(FULL, bar_wait(gbar, 0, err, lim, kWaitGram)));
-      constexpr int NG = kBatchMaxK / 4 / 32;
+      constexpr int NG = kBatchMaxK / 4 / 32;                 // float4 groups of a row a lane
+      constexpr int RW = kBatchMaxK / kBatchCluster / NW;     // Gram rows a warp
       const int nf4 = k >> 2;
-      float qacc[kBatchMaxT];
+      // this warp's Gram rows in registers, then every token against them
+      float4 gr[RW][NG];
 #pragma unroll
-      for (int t = 0; t < kBatchMaxT; ++t) qacc[t] = 0.f;
-      float nacc = 0.f;
-      for (int i = c0 + warp; i < c0 + ks; i += NW) {
-        const float4* grow = reinterpret_cast<const float4*>(gram_s + (i - c0) * k);
-        float4 gr[NG];
+      for (int r = 0; r < RW; ++r) {
+        const int i = warp + r * NW;
 #pragma unroll
         for (int u = 0; u < NG; ++u) {
           const int jg = lane + 32 * u;
-          gr[u] = jg < nf4 ? grow[jg] : make_float4(0.f, 0.f, 0.f, 0.f);
+          gr[r][u] = (i < ks && jg < nf4) ? reinterpret_cast<const float4*>(gram_s + i * k)[jg]
+                                          : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+      }
+      // four tokens an iteration (a compact loop: this code runs once a call),
+      // their loads first; per lane the rows in order, then one butterfly
+      // for the four sums (lane l ends with token tb + l / 8)
+#pragma unroll 1
+      for (int tb = 0; tb < T; tb += 4) {
+        float4 gv[4][NG];
+        float gi[4][RW];
 #pragma unroll
-        for (int t = 0; t < kBatchMaxT; ++t) {
-          if (t < T) {
-            const float4* gt = reinterpret_cast<const float4*>(g32 + t * k);
-            float h = 0.f;
+        for (int qq = 0; qq < 4; ++qq) {
+          const int t = tb + qq < T ? tb + qq : T - 1;  // (a repeated token's sum is dropped)
 #pragma unroll
-            for (int u = 0; u < NG; ++u) {
-              const int jg = lane + 32 * u;
-              if (jg < nf4) {
-                const float4 gv = gt[jg];
-                float hu = gr[u].x * gv.x;
-                hu = fmaf(gr[u].y, gv.y, hu);
-                hu = fmaf(gr[u].z, gv.z, hu);
-                hu = fmaf(gr[u].w, gv.w, hu);
+          for (int u = 0; u < NG; ++u) {
+            const int jg = lane + 32 * u;
+            gv[qq][u] = jg < nf4 ? reinterpret_cast<const float4*>(gt + t * k)[jg] : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int r = 0; r < RW; ++r) gi[qq][r] = warp + r * NW < ks ? gt[t * k + c0 + warp + r * NW] : 0.f;
+        }
+        float q[4];
+#pragma unroll
+        for (int qq = 0; qq < 4; ++qq) {
+          q[qq] = 0.f;
+#pragma unroll
+          for (int r = 0; r < RW; ++r) {
+            if (warp + r * NW < ks) {
+              float h = 0.f;
+#pragma unroll
+              for (int u = 0; u < NG; ++u) {
+                float hu = gr[r][u].x * gv[qq][u].x;
+                hu = fmaf(gr[r][u].y, gv[qq][u].y, hu);
+                hu = fmaf(gr[r][u].z, gv[qq][u].z, hu);
+                hu = fmaf(gr[r][u].w, gv[qq][u].w, hu);
                 h += hu;
               }
+              q[qq] = fmaf(gi[qq][r], h, q[qq]);
             }
-            qacc[t] = fmaf(g32[t * k + i], h, qacc[t]);
           }
         }
-        if (lane < T) nacc = fmaf(g32[lane * k + i], g32[lane * k + i], nacc);
+        const float qs = warp_reduce_multi<4>(q, lane);
+        const int t = tb + row_of_lane<4>(lane);
+        if ((lane & 7) == 0 && t < T) wsh[(warp * kBatchMaxT + t) * 2] = qs;
       }
-      const float qs = warp_reduce_multi<kBatchMaxT>(qacc, lane);  // lanes 2t, 2t + 1: token t
-      if ((lane & 1) == 0) wsh[(warp * kBatchMaxT + (lane >> 1)) * 2] = qs;
-      if (lane < kBatchMaxT) wsh[(warp * kBatchMaxT + lane) * 2 + 1] = nacc;
+      if (lane < kBatchMaxT) {
+        float nacc = 0.f;
+        if (lane < T)
+          for (int i = warp; i < ks; i += NW) {
+            const float gi = gt[lane * k + c0 + i];
+            nacc = fmaf(gi, gi, nacc);
+          }
+        wsh[(warp * kBatchMaxT + lane) * 2 + 1] = nacc;
+      }
     }
     compute_sync();
     // thread 16 t + r adds token t's warp shares in warp order and sends the
@@ -437,7 +524,7 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_decode_kernel(const __
       st_async_v2(map_rank(sa(qin + rank * kBatchMaxT + t), r), Q, N, map_rank(sa(qbar), r));
     }
   }
-  cluster_arrive_release();  // this CTA's last push into a peer is issued
+  cluster_arrive_relaxed();  // this CTA's last push into a peer is issued
 
   // ---- fast path for every token: M G = M hi + M lo, 16 x 8 tiles in registers
   constexpr int kUnits = (kBatchMaxMt * NT + NW - 1) / NW;
@@ -446,37 +533,53 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_decode_kernel(const __
   for (int j = 0; j < kUnits; ++j) facc[j][0] = facc[j][1] = facc[j][2] = facc[j][3] = 0.f;
   if (warp < NW) {
     const int gp = p.gbf_pitch;
-    for (int e = tid; e < kBatchMaxT * (k / 2); e += NC) {
-      const int t = e / (k / 2), col = (e - t * (k / 2)) * 2;
-      const float x0 = t < T ? g32[t * k + col] : 0.f, x1 = t < T ? g32[t * k + col + 1] : 0.f;
-      const uint32_t h0 = bf16_bits(x0), h1 = bf16_bits(x1);
-      const uint32_t l0 = bf16_bits(x0 - __uint_as_float(h0 << 16)), l1 = bf16_bits(x1 - __uint_as_float(h1 << 16));
-      *reinterpret_cast<uint32_t*>(gbf + t * gp + col * 2) = h0 | (h1 << 16);
-      *reinterpret_cast<uint32_t*>(gbf + (kBatchMaxT + t) * gp + col * 2) = l0 | (l1 << 16);
+    // warp w: tokens w and w + 8, lanes over column pairs
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int t = warp + h * NW;
+#pragma unroll 1
+      for (int col = 2 * lane; col < k; col += 64) {
+        const float2 x = t < T ? *reinterpret_cast<const float2*>(gt + t * k + col) : make_float2(0.f, 0.f);
+        const uint32_t h0 = bf16_bits(x.x), h1 = bf16_bits(x.y);
+        const uint32_t l0 = bf16_bits(x.x - __uint_as_float(h0 << 16)), l1 = bf16_bits(x.y - __uint_as_float(h1 << 16));
+        *reinterpret_cast<uint32_t*>(gbf + t * gp + col * 2) = h0 | (h1 << 16);
+        *reinterpret_cast<uint32_t*>(gbf + (kBatchMaxT + t) * gp + col * 2) = l0 | (l1 << 16);
+      }
     }
     compute_sync();
     if (nrows > 0) {
       note(__all_sync(FULL, bar_wait(mbar, 0, err, lim, kWaitM)));
       const uint32_t ms_a = sa(ms), gh_a = sa(gbf), gl_a = sa(gbf + kBatchMaxT * gp);
+      // k steps outside, the warp's tiles inside: independent accumulators
+      // (high and low part apart) keep the tensor pipe busy
+      float flo[kUnits][4];
 #pragma unroll
-      for (int j = 0; j < kUnits; ++j) {
-        const int u = warp + j * NW;
-        if (u < n_mt * NT) {
-          const int mt = u / NT, nt = u - mt * NT;
-          const int row = mt * 16 + (lane & 15);
-          const int tok = nt * 8 + (lane & 7);
-          for (int kk = 0; kk < k / 16; ++kk) {
-            const int ch = kk * 2 + (lane >> 4);
+      for (int j = 0; j < kUnits; ++j) flo[j][0] = flo[j][1] = flo[j][2] = flo[j][3] = 0.f;
+      const int nu = n_mt * NT;
+#pragma unroll 2
+      for (int kk = 0; kk < k / 16; ++kk) {
+        const int ch = kk * 2 + (lane >> 4);
+        const uint32_t bch = uint32_t((kk * 2 + ((lane >> 3) & 1)) * 16);
+#pragma unroll
+        for (int j = 0; j < kUnits; ++j) {
+          const int u = warp + j * NW;
+          if (u < nu) {
+            const int mt = u / NT, nt = u - mt * NT;
+            const int row = mt * 16 + (lane & 15);
+            const uint32_t boff = uint32_t((nt * 8 + (lane & 7)) * gp) + bch;
             uint32_t a0, a1, a2, a3, b0, b1, c0r, c1r;
             ldsm_x4(ms_a + (ch >> 3) * p.rpc * 128 + swz(row, ch & 7), a0, a1, a2, a3);
-            const uint32_t boff = uint32_t(tok * gp + (kk * 2 + ((lane >> 3) & 1)) * 16);
             ldsm_x2(gh_a + boff, b0, b1);
             ldsm_x2(gl_a + boff, c0r, c1r);
             mma16816(facc[j], a0, a1, a2, a3, b0, b1);
-            mma16816(facc[j], a0, a1, a2, a3, c0r, c1r);
+            mma16816(flo[j], a0, a1, a2, a3, c0r, c1r);
           }
         }
       }
+#pragma unroll
+      for (int j = 0; j < kUnits; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) facc[j][e] += flo[j][e];
     }
 
     // ---- the decision (warp 0), from the ranks' shares in rank order
@@ -624,6 +727,7 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_decode_kernel(const __
     for (int j = nch - S > 0 ? nch - S : 0; j < nch; ++j)
       bar_wait(&full[j % S], uint32_t(j / S) & 1u, err, ok ? lim : kSpinCyclesAfterError, kWaitRing);
   }
+  if (tid < CS) bulk_wait_read();  // the all-gather's source
   // No CTA leaves while a peer of its cluster may still push into it.
   cluster_wait();
 }

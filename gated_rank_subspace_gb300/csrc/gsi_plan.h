@@ -113,12 +113,13 @@ constexpr int kGSplitMax = 16;
 inline int g_split(int64_t T) { return T < kTensorMinT ? 16 : 8; }
 
 // The tensor path's finalize (rho, flags, bf16 g) takes tokens in chunks of
-// kFinTok and cuts the Gram rows into fin_blocks(T, k) blocks, so that a
-// small T still spreads over the SMs (one block once there are 64 chunks).
+// kFinTok and cuts the Gram rows into fin_blocks(T, k) blocks, so that the
+// grid holds about two CTAs per SM of a GB300 whatever T (one block once
+// there are 304 chunks).
 constexpr int kFinTok = 16;
 inline int fin_blocks(int64_t T, int64_t k) {
   const int64_t chunks = cdiv(T, kFinTok);
-  if (chunks >= 64) return 1;
+  if (chunks >= 304) return 1;
   int64_t nb = cdiv(304, chunks);
   const int64_t cap = k / 8 > 0 ? k / 8 : 1;  // at least 8 Gram rows a block
   if (nb > cap) nb = cap;
@@ -357,8 +358,9 @@ inline DecodePlan plan_decode(int64_t d, int64_t d_out, int64_t k, int es, int n
 // [b * vr, (b + 1) * vr) of V_k and applies output rows [b * rpc, (b + 1) *
 // rpc); both are multiples of 16 (one tensor-core tile).  Shared memory
 // (offsets from a 1024-byte aligned base): mbarriers and words | g in bf16,
-// high and low halves, [2][16][k] | the decision | per-warp shares | then
-// the call's scratch: V slab (128-byte swizzled boxes of 64 columns), the
+// high and low halves, [2][16][k] (before that, the CTA's partial g by
+// column slice) | the decision | per-warp shares | the rank's final slice of
+// g and the norms | the slab norms | then the call's scratch: V slab (128-byte swizzled boxes of 64 columns), the
 // token slab, partial-g inbox, norm inbox, gathered g, share inbox, Gram
 // slice | M rows (swizzled boxes).  Once the flags are known (the fast
 // outputs are then in registers) the W ring -- stages of rpc x 128 columns
@@ -374,13 +376,14 @@ constexpr int kBatchMaxClusters = 16;
 constexpr int kBatchMaxMt = 10;   // output rows a CTA: at most 10 tiles of 16
 constexpr int kBatchKC = 128;     // W columns per ring stage (8 steps of 16)
 constexpr int kBatchMaxStages = 6;
-constexpr int kBatchMaxK = 512;
+constexpr int kBatchMaxK = 384;
 constexpr int kBatchSmemSlack = 1024;  // the kernel aligns its base to 1024 bytes
 
 struct BatchPlan {
   int T, ncta, vr, rpc, ks, kb, stages, stage_bytes;
   int gbf_pitch, xs_pitch;
-  int off_gbf, off_dec, off_wsh, off_scr, off_v, off_xs, off_in, off_nin, off_g32, off_qin, off_gram, off_m;
+  int off_gbf, off_dec, off_wsh, off_fs, off_nx, off_scr, off_v, off_xs, off_in, off_nin, off_g32, off_qin, off_gram,
+      off_m;
   size_t smem;  // dynamic shared memory to request (alignment slack included)
   bool ok;
 };
@@ -410,6 +413,8 @@ inline BatchPlan plan_batch(int64_t d, int64_t d_out, int64_t k, int64_t T, int 
   p.off_gbf = take(size_t(2) * kBatchMaxT * p.gbf_pitch, 128);
   p.off_dec = take(size_t(2) * kBatchMaxT * 4, 128);
   p.off_wsh = take(size_t(kBatchWarps) * kBatchMaxT * 2 * 4, 128);
+  p.off_fs = take(size_t(T) * p.ks * 4 + kBatchMaxT * 4, 128);  // this rank's final slice of G, then the norms
+  p.off_nx = take(kBatchMaxT * 4, 128);                          // the CTA's slab norms
   p.off_scr = take(0, 1024);
   p.off_v = take(size_t(p.kb) * p.vr * 128, 1024);
   p.off_xs = take(size_t(kBatchMaxT) * p.xs_pitch, 128);

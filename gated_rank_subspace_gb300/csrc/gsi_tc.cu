@@ -545,6 +545,10 @@ __device__ __forceinline__ void fin_token(float qq, float nn, float x2, float ep
   flags[t] = (rho < eps) ? uint8_t(0) : uint8_t(1);
 }
 
+// Row stride of the finalize's g-by-column buffer: the chunk's tokens plus
+// four floats (16-byte aligned rows that fall on different banks).
+constexpr int kFinStride = kFinTok + 4;
+
 template <int GS>
 __global__ void __launch_bounds__(256) tc_finalize_kernel(const uint16_t* __restrict__ X, const float* __restrict__ G,
                                                           const float* __restrict__ gram, int64_t d, int k, int T,
@@ -553,8 +557,10 @@ __global__ void __launch_bounds__(256) tc_finalize_kernel(const uint16_t* __rest
                                                           int gsplit, int nb, float4* __restrict__ part,
                                                           uint32_t* arrive) {
   extern __shared__ float fsm[];
-  float* gs = fsm;                       // [kFinTok][k]
-  float* red = gs + kFinTok * k;         // [8 warps][kFinTok][2]
+  // g by column: the chunk's tokens of column j at gs[j * kFinStride ...], so
+  // one 16-byte broadcast load gives four tokens' g_j
+  float* gs = fsm;                       // [k][kFinStride]
+  float* red = gs + kFinStride * k;      // [8 warps][kFinTok][2]
   float* x2s = red + 8 * kFinTok * 2;    // [kFinTok]
   __shared__ bool s_last;
   const int cb = blockIdx.x, blk = blockIdx.y;
@@ -583,7 +589,7 @@ __global__ void __launch_bounds__(256) tc_finalize_kernel(const uint16_t* __rest
       float g = 0.f;
 #pragma unroll
       for (int sl = 0; sl < GS; ++sl) g += v[q][sl];
-      gs[e] = g;
+      gs[j * kFinStride + t] = g;
       if (blk == 0 && t0 + t < T) {
         __nv_bfloat16 bv = __float2bfloat16_rn(g);
         Gbf[int64_t(t0 + t) * k + j] = *reinterpret_cast<uint16_t*>(&bv);
@@ -608,9 +614,17 @@ __global__ void __launch_bounds__(256) tc_finalize_kernel(const uint16_t* __rest
 #pragma unroll
         for (int u = 0; u < 32; ++u) gv[u] = __ldg(&gram[int64_t(i + u) * k + j]);
 #pragma unroll
-        for (int u = 0; u < 32; ++u)
+        for (int u = 0; u < 32; ++u) {
+          const float4* gi = reinterpret_cast<const float4*>(gs + (i + u) * kFinStride);
 #pragma unroll
-          for (int t = 0; t < kFinTok; ++t) h[t] = fmaf(gs[t * k + i + u], gv[u], h[t]);
+          for (int t4 = 0; t4 < kFinTok / 4; ++t4) {
+            const float4 g4 = gi[t4];
+            h[4 * t4] = fmaf(g4.x, gv[u], h[4 * t4]);
+            h[4 * t4 + 1] = fmaf(g4.y, gv[u], h[4 * t4 + 1]);
+            h[4 * t4 + 2] = fmaf(g4.z, gv[u], h[4 * t4 + 2]);
+            h[4 * t4 + 3] = fmaf(g4.w, gv[u], h[4 * t4 + 3]);
+          }
+        }
       }
       if (i < i1) {
         float gv[32];
@@ -620,12 +634,12 @@ __global__ void __launch_bounds__(256) tc_finalize_kernel(const uint16_t* __rest
         for (int u = 0; u < 32; ++u)
           if (i + u < i1)
 #pragma unroll
-            for (int t = 0; t < kFinTok; ++t) h[t] = fmaf(gs[t * k + i + u], gv[u], h[t]);
+            for (int t = 0; t < kFinTok; ++t) h[t] = fmaf(gs[(i + u) * kFinStride + t], gv[u], h[t]);
       }
     }
 #pragma unroll
     for (int t = 0; t < kFinTok; ++t) {
-      const float gj = gs[t * k + j];
+      const float gj = gs[j * kFinStride + t];
       if (blk == 0) n[t] = fmaf(gj, gj, n[t]);
       if (gram) q[t] = fmaf(gj, h[t], q[t]);
     }
@@ -946,7 +960,7 @@ cudaError_t launch_tensor_path(const TensorArgs& t, cudaStream_t s) {
     float4* part = t.fpart;
     uint32_t* arrive = t.fin_arrive;
     void* args[] = {&X, &G, &gram, &dd, &kk, &TT, &eps, &rho, &flags, &Gbf, &gs, &nb, &part, &arrive};
-    const size_t smem = size_t(kFinTok) * k * 4 + 8 * kFinTok * 2 * 4 + kFinTok * 4;
+    const size_t smem = size_t(kFinStride) * k * 4 + 8 * kFinTok * 2 * 4 + kFinTok * 4;
     const void* kern = gsplit > 8 ? reinterpret_cast<const void*>(tc_finalize_kernel<kGSplitMax>)
                                   : reinterpret_cast<const void*>(tc_finalize_kernel<8>);
     if (smem > 48 * 1024) {

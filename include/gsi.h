@@ -87,7 +87,7 @@ typedef enum gsi_dtype { GSI_F32 = 0, GSI_BF16 = 1 } gsi_dtype;
  *             three products (X V, G M^T for the fast tokens, X W^T for the
  *             slow ones) run as warp-level tensor-core products (bf16
  *             operands, float32 accumulation; G enters M G as a high and a
- *             low bf16 part).  Needs k a multiple of 64 (at most 512), d a
+ *             low bf16 part).  Needs k a multiple of 64 (at most 384), d a
  *             multiple of 8 and d_out / (grid size) at most 160 rows.
  * AUTO picks FUSED for T = 1, and for T = 2 on float32 maps, where a slab of
  * V fits shared memory (and STREAM at run time on a device that cannot hold

@@ -16,13 +16,13 @@ int main() {
         "\"vr\": %d, \"rpc\": %d, \"ks\": %d, \"kb\": %d, \"stages\": %d, \"stage_bytes\": %d, \"gbf_pitch\": %d, "
         "\"xs_pitch\": %d, \"off_gbf\": %d, \"off_dec\": %d, \"off_wsh\": %d, \"off_scr\": %d, \"off_v\": %d, "
         "\"off_xs\": %d, \"off_in\": %d, \"off_nin\": %d, \"off_g32\": %d, \"off_qin\": %d, \"off_gram\": %d, "
-        "\"off_m\": %d, \"smem\": %zu, \"threads\": %d, \"warps\": %d, \"maxT\": %d, \"cluster\": %d, "
-        "\"max_clusters\": %d, \"max_mt\": %d, \"kc\": %d, \"max_stages\": %d, \"slack\": %d, "
+        "\"off_m\": %d, \"off_fs\": %d, \"off_nx\": %d, \"smem\": %zu, \"threads\": %d, \"warps\": %d, \"maxT\": %d, \"cluster\": %d, "
+        "\"max_clusters\": %d, \"max_k\": %d, \"max_mt\": %d, \"kc\": %d, \"max_stages\": %d, \"slack\": %d, "
         "\"ws_part_g\": %zu, \"ws_part_x\": %zu, \"ws_total\": %zu}\n",
         d, d_out, k, T, ncta, budget, int(p.ok), p.vr, p.rpc, p.ks, p.kb, p.stages, p.stage_bytes, p.gbf_pitch,
         p.xs_pitch, p.off_gbf, p.off_dec, p.off_wsh, p.off_scr, p.off_v, p.off_xs, p.off_in, p.off_nin, p.off_g32,
-        p.off_qin, p.off_gram, p.off_m, p.smem, gsi::kBatchThreads, gsi::kBatchWarps, gsi::kBatchMaxT,
-        gsi::kBatchCluster, gsi::kBatchMaxClusters, gsi::kBatchMaxMt, gsi::kBatchKC, gsi::kBatchMaxStages,
+        p.off_qin, p.off_gram, p.off_m, p.off_fs, p.off_nx, p.smem, gsi::kBatchThreads, gsi::kBatchWarps, gsi::kBatchMaxT,
+        gsi::kBatchCluster, gsi::kBatchMaxClusters, gsi::kBatchMaxK, gsi::kBatchMaxMt, gsi::kBatchKC, gsi::kBatchMaxStages,
         gsi::kBatchSmemSlack, L.part_g, L.part_x, L.total);
   }
   return 0;

@@ -31,7 +31,8 @@ def cases():
             for d, d_out, k in SHAPES_6B + SHAPES_13B:
                 out.append((d, d_out, k, T, ncta))
             out += [(520, 333, 64, T, ncta), (1032, 2056, 128, T, ncta), (16, 8, 64, T, ncta),
-                    (8200, 520, 64, T, ncta), (4096, 4096, 512, T, ncta), (4104, 12296, 192, T, ncta)]
+                    (8200, 520, 64, T, ncta), (4096, 4096, 384, T, ncta), (4096, 4096, 512, T, ncta),
+                    (4104, 12296, 192, T, ncta)]
     rng = random.Random(11)
     for _ in range(400):
         k = 64 * rng.randint(1, 8)
@@ -63,7 +64,7 @@ def test_benchmark_maps_fit(plans):
 
 def test_rejects_out_of_range(plans):
     for p in plans:
-        if p["T"] < 2 or p["T"] > p["maxT"] or p["k"] % 64 or p["k"] > 512 or p["d"] % 8:
+        if p["T"] < 2 or p["T"] > p["maxT"] or p["k"] % 64 or p["k"] > p["max_k"] or p["d"] % 8:
             assert not p["ok"], p
 
 
@@ -86,6 +87,7 @@ def test_regions_and_indices(plans):
         regions = [
             ("bars", 0, 512 + 8), ("gbf", p["off_gbf"], 2 * maxT * p["gbf_pitch"]),
             ("dec", p["off_dec"], 2 * maxT * 4), ("wsh", p["off_wsh"], NW * maxT * 2 * 4),
+            ("fs", p["off_fs"], T * ks * 4 + maxT * 4), ("nx", p["off_nx"], maxT * 4),
             ("v", p["off_v"], kb * vr * 128), ("xs", p["off_xs"], maxT * p["xs_pitch"]),
             ("in", p["off_in"], CS * T * ks * 4), ("nin", p["off_nin"], CS * maxT * 4),
             ("g32", p["off_g32"], T * k * 4 + maxT * 4), ("qin", p["off_qin"], CS * maxT * 8),
@@ -104,7 +106,13 @@ def test_regions_and_indices(plans):
         assert p["off_gram"] % 16 == 0 and p["gbf_pitch"] % 16 == 0 and p["xs_pitch"] % 16 == 0
         assert p["off_in"] % 8 == 0 and p["off_nin"] % 8 == 0 and p["off_g32"] % 16 == 0 and p["off_qin"] % 8 == 0
         # the scratch starts after the regions that live through the call
-        assert p["off_scr"] >= p["off_wsh"] + NW * maxT * 2 * 4 and p["off_scr"] <= p["off_v"]
+        assert p["off_scr"] >= p["off_nx"] + maxT * 4 and p["off_scr"] <= p["off_v"]
+        # the partial g by column slice [16][T][ks] float32 fits in the bf16 g region it precedes
+        assert T * k * 4 <= 2 * maxT * p["gbf_pitch"]
+        # bulk copies between CTAs: 16-byte aligned sources, destinations and sizes
+        assert (T * ks * 4) % 16 == 0 and p["off_fs"] % 16 == 0 and p["off_nx"] % 16 == 0
+        assert p["off_in"] % 16 == 0 and p["off_nin"] % 16 == 0 and p["off_gbf"] % 16 == 0
+        assert p["off_g32"] % 16 == 0 and (T * k * 4) % 16 == 0
         # ring: S stages of W (2 boxes of rpc rows) + X (2 boxes of up to 16 rows), inside the limit
         assert 2 <= S <= p["max_stages"]
         assert SB >= 2 * rpc * 128 + 2 * maxT * 128
