@@ -347,8 +347,7 @@ static int decode_nv(const gsi_map_desc* m) { return m->k * elem_bytes(m->dtype)
 // Enqueue the single-token decode kernel (all arguments validated);
 // GSI_ERR_UNSUPPORTED, with nothing launched, when its plan does not fit.
 static gsi_status run_decode(const gsi_map_desc* m, const void* X, float eps, float* Y, uint8_t* flags, float* rho,
-                             void* ws, cudaStream_t st, DeviceFacts* f, const gsi_map_desc* next,
-                             const void* next_x) {
+                             void* ws, cudaStream_t st, DeviceFacts* f, const gsi_map_desc* next) {
   const DecodePlan p = decode_plan(m, f);
   if (!p.ok) return GSI_ERR_UNSUPPORTED;
   Ctrl* ctrl = static_cast<Ctrl*>(ws);
@@ -369,10 +368,6 @@ static gsi_status run_decode(const gsi_map_desc* m, const void* X, float eps, fl
     a.next_m_bytes = uint64_t(next->d_out) * next->k * nes;
     a.next_gram = reinterpret_cast<const char*>(next->gram);
     a.next_gram_bytes = next->gram ? uint64_t(next->k) * next->k * 4 : 0;
-    if (next_x) {
-      a.next_x = static_cast<const char*>(next_x);
-      a.next_x_bytes = uint64_t(next->d) * nes;
-    }
   }
   a.err = &ctrl->err;
   if (p.grid && g_withhold.load() > 0 && g_withhold.fetch_sub(1) > 0) {
@@ -433,7 +428,7 @@ static gsi_status run_stack_decode(const gsi_map_desc* maps, int n, const void* 
 // run on this device, so that callers may fall back to the two launches.
 static gsi_status run_decide(const gsi_map_desc* m, const void* X, int64_t T, float eps, int mode, float* Y,
                              uint8_t* flags, float* rho, float* G, const float* Gin, void* ws, cudaStream_t st,
-                             bool fused = false, const gsi_map_desc* next = nullptr, const void* next_x = nullptr) {
+                             bool fused = false, const gsi_map_desc* next = nullptr) {
   const int es = elem_bytes(m->dtype);
   const GatePlan gp = plan_gate(m->d, m->k, es, T);
   const StreamLayout L = layout_stream(m->d, m->k, es, T);
@@ -446,7 +441,7 @@ static gsi_status run_decide(const gsi_map_desc* m, const void* X, int64_t T, fl
   DecidePlan dp{};
   if (fused && mode == 0 && T == 1) {
     // one token: the single-token decode kernel where the basis fits a cluster
-    s = run_decode(m, X, eps, Y, flags, rho, ws, st, f, next, next_x);
+    s = run_decode(m, X, eps, Y, flags, rho, ws, st, f, next);
     if (s != GSI_ERR_UNSUPPORTED) return s;
   }
   if (fused) {
@@ -682,7 +677,7 @@ static gsi_status run_path(const gsi_map_desc* m, gsi_path p, bool strict, const
   }
   if (p == GSI_PATH_TENSOR) return run_tensor(m, X, T, eps, Y, flags, rho, ws, st);
   if (p == GSI_PATH_FUSED) {
-    const gsi_status s = run_decide(m, X, T, eps, 0, Y, flags, rho, nullptr, nullptr, ws, st, true, next, next_x);
+    const gsi_status s = run_decide(m, X, T, eps, 0, Y, flags, rho, nullptr, nullptr, ws, st, true, next);
     if (s != GSI_ERR_UNSUPPORTED || strict) return s;
   }
   return run_stream(m, X, T, eps, Y, flags, rho, nullptr, ws, st, true, next);

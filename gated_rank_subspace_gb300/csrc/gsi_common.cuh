@@ -13,6 +13,25 @@ namespace gsi {
 
 namespace cg = cooperative_groups;
 
+// ---------------------------------------------------------------- packed float pairs
+// Two float32 lanes in one 64-bit register, for the paired FMA of sm_100-class
+// GPUs (fma.rn.f32x2: two independent float32 FMAs, each rounded once).
+__device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(unsigned long long r) {
+  float a, b;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+  return make_float2(a, b);
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b, unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+
 // ---------------------------------------------------------------- element types
 // Both storage types are read as 16-byte vectors: 4 float32 or 8 bf16.
 struct F32 {
@@ -39,6 +58,14 @@ struct F32 {
     acc[1] = fmaf(x, __uint_as_float(w.y), acc[1]);
     acc[2] = fmaf(x, __uint_as_float(w.z), acc[2]);
     acc[3] = fmaf(x, __uint_as_float(w.w), acc[3]);
+  }
+  // sum over the vector of w[e] g[e], in element order
+  __device__ __forceinline__ static float dot_vec(const uint4& w, const float* g) {
+    float p = __uint_as_float(w.x) * g[0];
+    p = fmaf(__uint_as_float(w.y), g[1], p);
+    p = fmaf(__uint_as_float(w.z), g[2], p);
+    p = fmaf(__uint_as_float(w.w), g[3], p);
+    return p;
   }
   // a0 += w.x*x.x + w.z*x.z, a1 += w.y*x.y + w.w*x.w (in that order)
   __device__ __forceinline__ static void dot_acc(const uint4& w, const uint4& x, float& a0, float& a1) {
@@ -96,6 +123,18 @@ struct BF16 {
           "fma.rn.f32.bf16 %0, wl, %3, %0;\n\tfma.rn.f32.bf16 %1, wh, %3, %1;\n\t}"
           : "+f"(acc[2 * c]), "+f"(acc[2 * c + 1])
           : "r"(wv[c]), "h"(xb));
+  }
+  // sum over the vector of w[e] g[e] (g float32): the even elements and the
+  // odd ones in two lanes of paired FMAs (each in element order), then added
+  __device__ __forceinline__ static float dot_vec(const uint4& w, const float* g) {
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+    unsigned long long acc = f2_pack(0.f, 0.f);
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      acc = f2_fma(f2_pack(__uint_as_float(wv[c] << 16), __uint_as_float(wv[c] & 0xffff0000u)),
+                   f2_pack(g[2 * c], g[2 * c + 1]), acc);
+    const float2 r = f2_unpack(acc);
+    return r.x + r.y;
   }
   // a0 += the products of the even elements, a1 of the odd ones, in order
   __device__ __forceinline__ static void dot_acc(const uint4& w, const uint4& x, float& a0, float& a1) {

@@ -449,11 +449,7 @@ __device__ __forceinline__ void decode_run(const DecodeMap& m, const DecodeGeom&
           part[r] = 0.f;
 #pragma unroll
           for (int v = 0; v < NV; ++v) {
-            float w[PV];
-            E::unpack(u[r][v], w);
-            float p = 0.f;
-#pragma unroll
-            for (int e = 0; e < PV; ++e) p = fmaf(w[e], gv[v][e], p);
+            const float p = E::dot_vec(u[r][v], gv[v]);
             part[r] += on[v] ? p : 0.f;
           }
         }
@@ -607,15 +603,9 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
   constexpr unsigned FULL = 0xffffffffu;
   extern __shared__ __align__(128) unsigned char smem[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // The co-resident launches (grid projection) check their launch shape
-  // before any barrier, copy or access to another CTA.  (The launches of the
-  // cluster projection skip it: reading the cluster size on entry measured
-  // ~0.15 us a call.)
-  if (a.m.grid && (!cluster_shape_ok(kDecodeCluster) || gridDim.x % kDecodeCluster != 0 ||
-                   gridDim.x / kDecodeCluster > kDecodeMaxClusters)) {
-    if (tid == 0) atomicOr(a.err, kErrTimeout | kErrLaunchShape);
-    return;
-  }
+  // (No launch-shape check here: reading the cluster size costs ~0.15 us on
+  // a call's path.  Profilers that relaunch kernels must run with
+  // GSI_COOPERATIVE=0, see the header.)
   const int rank = int(cg::this_cluster().block_rank());
   // one instantiation for both projection forms: the four maps of a layer
   // then run the same code, which stays in the instruction cache
@@ -695,13 +685,10 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
       bulk_g2s(Ms, static_cast<const char*>(a.m.M) + r0 * mrow_b, bytes, mbar);
     }
   }
-  // weights and tokens of the next map of a stack, into L2 (this CTA's share)
-  if (tid == 64 || tid == 96 || tid == 128 || tid == 160) {
-    const char* base = tid == 64 ? a.next_v : tid == 96 ? a.next_m : tid == 128 ? a.next_gram : a.next_x;
-    const uint64_t total = tid == 64    ? a.next_v_bytes
-                           : tid == 96  ? a.next_m_bytes
-                           : tid == 128 ? a.next_gram_bytes
-                                        : a.next_x_bytes;
+  // weights of the next map of a stack, into L2 (this CTA's share)
+  if (tid == 64 || tid == 96 || tid == 128) {
+    const char* base = tid == 64 ? a.next_v : tid == 96 ? a.next_m : a.next_gram;
+    const uint64_t total = tid == 64 ? a.next_v_bytes : tid == 96 ? a.next_m_bytes : a.next_gram_bytes;
     if (base && total) {
       const uint64_t share = ((total + gridDim.x - 1) / gridDim.x + 15) / 16 * 16;
       const uint64_t off = uint64_t(blockIdx.x) * share;
@@ -922,11 +909,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) decode_kernel(DecodeArgs a) 
           part[r] = 0.f;
 #pragma unroll
           for (int v = 0; v < NV; ++v) {
-            float w[PV];
-            E::unpack(u[r][v], w);
-            float p = 0.f;
-#pragma unroll
-            for (int e = 0; e < PV; ++e) p = fmaf(w[e], gv[v][e], p);
+            const float p = E::dot_vec(u[r][v], gv[v]);
             part[r] += on[v] ? p : 0.f;
           }
         }

@@ -110,9 +110,6 @@ struct DecodeArgs {
   uint64_t next_m_bytes;
   const char* next_gram;
   uint64_t next_gram_bytes;
-  // the next map's tokens, into L2 as well
-  const char* next_x;
-  uint64_t next_x_bytes;
   uint32_t* err;        // device error word (bounded waits)
   // test hook (grid projection): cluster 0 withholds its slice words, so the
   // other ranks' polls give up after poll_cycles (0: the default ~2 s)

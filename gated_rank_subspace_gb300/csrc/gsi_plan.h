@@ -115,8 +115,9 @@ inline int g_split(int64_t T) { return T < kTensorMinT ? 16 : 8; }
 // The tensor path's finalize (rho, flags, bf16 g) takes tokens in chunks of
 // kFinTok and cuts the Gram rows into fin_blocks(T, k) blocks, so that the
 // grid holds about two CTAs per SM of a GB300 whatever T (one block once
-// there are 304 chunks).
-constexpr int kFinTok = 16;
+// there are 304 chunks).  (16 tokens a CTA read the Gram half as often but
+// measured ~20 us slower at T = 2048: fewer CTAs, twice the accumulators.)
+constexpr int kFinTok = 8;
 inline int fin_blocks(int64_t T, int64_t k) {
   const int64_t chunks = cdiv(T, kFinTok);
   if (chunks >= 304) return 1;
