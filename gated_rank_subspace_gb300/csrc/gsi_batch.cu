@@ -28,11 +28,10 @@
 //             order and pushes the slice of the final g to every rank of its
 //             cluster (rank 0 does the same for the norms).  Every CTA ends
 //             with the same bits of G [T][k] and of ||x_t||^2.
-//   decide    warp w takes the rows c0 + w, c0 + w + 8, ... of the rank's
-//             Gram slice: per token its share of g^T (V_k^T V_k) g and of
-//             ||g||^2.  The CTA adds its warps' shares in warp order and
-//             sends them to every rank; every CTA adds the ranks' shares in
-//             rank order, so every CTA takes the same flags.
+//   decide    warp w takes tokens w and w + 8 over all of the rank's Gram
+//             slice: their shares of g^T (V_k^T V_k) g and of ||g||^2 go to
+//             every rank; every CTA adds the ranks' shares in rank order, so
+//             every CTA takes the same flags.
 //   fast      while the shares are in flight, G is rounded to bf16 as a high
 //             and a low part (their sum is g to about 2^-16 relative) and
 //             M G = M hi + M lo is formed for the CTA's rows and every token
@@ -184,7 +183,7 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_decode_kernel(const __
   unsigned char* gbf = smem + p.off_gbf;  // [2][16][gbf_pitch]: g in bf16, high then low part
   uint32_t* dflag = reinterpret_cast<uint32_t*>(smem + p.off_dec);  // [16]
   float* drho = reinterpret_cast<float*>(smem + p.off_dec) + kBatchMaxT;  // [16]
-  float* wsh = reinterpret_cast<float*>(smem + p.off_wsh);  // [NW][16][2] warp shares
+  float* wsh = reinterpret_cast<float*>(smem + p.off_wsh);  // [16][2] the rank's shares of each token
   unsigned char* vs = smem + p.off_v;                       // kb boxes of [vr][128 B]
   unsigned char* xs = smem + p.off_xs;                      // [16][xs_pitch] token slab
   float* inbox = reinterpret_cast<float*>(smem + p.off_in);  // [CS][T][ks]
@@ -439,89 +438,86 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_decode_kernel(const __
     }
     compute_sync();
 
-    // ---- shares of the Gram form: warp w, Gram rows c0 + w, c0 + w + 8, ...
-    //      lane l takes the column groups l, l + 32, ... (float4)
+    // ---- shares of the Gram form: warp w takes tokens w and w + 8 over all of
+    //      the rank's Gram rows i (columns c0 + i of g); lane l owns the column
+    //      groups l, l + 32, ... (float4): u_j = sum_i g_i Gram[i][j] over the
+    //      rows in order, then the token's share sum_j g_j u_j (a butterfly
+    //      over the lanes) and its share of ||g||^2 over the rank's columns
     {
       note(__all_sync(FULL, bar_wait(gbar, 0, err, lim, kWaitGram)));
-      constexpr int NG = kBatchMaxK / 4 / 32;                 // float4 groups of a row a lane
-      constexpr int RW = kBatchMaxK / kBatchCluster / NW;     // Gram rows a warp
+      constexpr int NG = kBatchMaxK / 4 / 32;  // float4 groups of a row a lane
       const int nf4 = k >> 2;
-      // this warp's Gram rows in registers, then every token against them
-      float4 gr[RW][NG];
+      const int t_a = warp, t_b = warp + NW;
+      const float* ga_row = gt + (t_a < T ? t_a : 0) * k;
+      const float* gb_row = gt + (t_b < T ? t_b : 0) * k;
+      float4 ua[NG], ub[NG];
 #pragma unroll
-      for (int r = 0; r < RW; ++r) {
-        const int i = warp + r * NW;
-#pragma unroll
-        for (int u = 0; u < NG; ++u) {
-          const int jg = lane + 32 * u;
-          gr[r][u] = (i < ks && jg < nf4) ? reinterpret_cast<const float4*>(gram_s + i * k)[jg]
-                                          : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      }
-      // four tokens an iteration (a compact loop: this code runs once a call),
-      // their loads first; per lane the rows in order, then one butterfly
-      // for the four sums (lane l ends with token tb + l / 8)
+      for (int u = 0; u < NG; ++u) ua[u] = ub[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      // the rows four at a time (ks is a multiple of 4), their loads first
 #pragma unroll 1
-      for (int tb = 0; tb < T; tb += 4) {
-        float4 gv[4][NG];
-        float gi[4][RW];
+      for (int i0 = 0; i0 < ks; i0 += 4) {
+        float4 gr[4][NG];
+        float ca[4], cb[4];
 #pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          const int t = tb + qq < T ? tb + qq : T - 1;  // (a repeated token's sum is dropped)
+        for (int r = 0; r < 4; ++r) {
 #pragma unroll
           for (int u = 0; u < NG; ++u) {
             const int jg = lane + 32 * u;
-            gv[qq][u] = jg < nf4 ? reinterpret_cast<const float4*>(gt + t * k)[jg] : make_float4(0.f, 0.f, 0.f, 0.f);
+            gr[r][u] = jg < nf4 ? reinterpret_cast<const float4*>(gram_s + (i0 + r) * k)[jg]
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
           }
-#pragma unroll
-          for (int r = 0; r < RW; ++r) gi[qq][r] = warp + r * NW < ks ? gt[t * k + c0 + warp + r * NW] : 0.f;
+          ca[r] = ga_row[c0 + i0 + r];
+          cb[r] = gb_row[c0 + i0 + r];
         }
-        float q[4];
 #pragma unroll
-        for (int qq = 0; qq < 4; ++qq) {
-          q[qq] = 0.f;
+        for (int r = 0; r < 4; ++r)
 #pragma unroll
-          for (int r = 0; r < RW; ++r) {
-            if (warp + r * NW < ks) {
-              float h = 0.f;
-#pragma unroll
-              for (int u = 0; u < NG; ++u) {
-                float hu = gr[r][u].x * gv[qq][u].x;
-                hu = fmaf(gr[r][u].y, gv[qq][u].y, hu);
-                hu = fmaf(gr[r][u].z, gv[qq][u].z, hu);
-                hu = fmaf(gr[r][u].w, gv[qq][u].w, hu);
-                h += hu;
-              }
-              q[qq] = fmaf(gi[qq][r], h, q[qq]);
-            }
+          for (int u = 0; u < NG; ++u) {
+            ua[u].x = fmaf(ca[r], gr[r][u].x, ua[u].x);
+            ua[u].y = fmaf(ca[r], gr[r][u].y, ua[u].y);
+            ua[u].z = fmaf(ca[r], gr[r][u].z, ua[u].z);
+            ua[u].w = fmaf(ca[r], gr[r][u].w, ua[u].w);
+            ub[u].x = fmaf(cb[r], gr[r][u].x, ub[u].x);
+            ub[u].y = fmaf(cb[r], gr[r][u].y, ub[u].y);
+            ub[u].z = fmaf(cb[r], gr[r][u].z, ub[u].z);
+            ub[u].w = fmaf(cb[r], gr[r][u].w, ub[u].w);
           }
-        }
-        const float qs = warp_reduce_multi<4>(q, lane);
-        const int t = tb + row_of_lane<4>(lane);
-        if ((lane & 7) == 0 && t < T) wsh[(warp * kBatchMaxT + t) * 2] = qs;
       }
-      if (lane < kBatchMaxT) {
-        float nacc = 0.f;
-        if (lane < T)
-          for (int i = warp; i < ks; i += NW) {
-            const float gi = gt[lane * k + c0 + i];
-            nacc = fmaf(gi, gi, nacc);
-          }
-        wsh[(warp * kBatchMaxT + lane) * 2 + 1] = nacc;
+      float qa = 0.f, qb = 0.f;
+#pragma unroll
+      for (int u = 0; u < NG; ++u) {
+        const int jg = lane + 32 * u;
+        if (jg < nf4) {
+          const float4 a = reinterpret_cast<const float4*>(ga_row)[jg], b = reinterpret_cast<const float4*>(gb_row)[jg];
+          qa = fmaf(a.x, ua[u].x, qa);
+          qa = fmaf(a.y, ua[u].y, qa);
+          qa = fmaf(a.z, ua[u].z, qa);
+          qa = fmaf(a.w, ua[u].w, qa);
+          qb = fmaf(b.x, ub[u].x, qb);
+          qb = fmaf(b.y, ub[u].y, qb);
+          qb = fmaf(b.z, ub[u].z, qb);
+          qb = fmaf(b.w, ub[u].w, qb);
+        }
+      }
+      // ||g||^2 over the rank's columns: lane l takes column c0 + l (ks <= 32)
+      const float ea = lane < ks ? ga_row[c0 + lane] : 0.f, eb = lane < ks ? gb_row[c0 + lane] : 0.f;
+      float na = ea * ea, nb = eb * eb;
+      qa = warp_sum(qa);
+      qb = warp_sum(qb);
+      na = warp_sum(na);
+      nb = warp_sum(nb);
+      if (lane == 0) {
+        wsh[t_a * 2] = qa;
+        wsh[t_a * 2 + 1] = na;
+        wsh[t_b * 2] = qb;
+        wsh[t_b * 2 + 1] = nb;
       }
     }
     compute_sync();
-    // thread 16 t + r adds token t's warp shares in warp order and sends the
-    // rank's pair to rank r
+    // thread 16 t + r sends the rank's pair of token t to rank r
     if (tid < T * CS) {
       const int t = tid >> 4, r = tid & (CS - 1);
-      float Q = 0.f, N = 0.f;
-#pragma unroll
-      for (int w = 0; w < NW; ++w) {
-        Q += wsh[(w * kBatchMaxT + t) * 2];
-        N += wsh[(w * kBatchMaxT + t) * 2 + 1];
-      }
-      st_async_v2(map_rank(sa(qin + rank * kBatchMaxT + t), r), Q, N, map_rank(sa(qbar), r));
+      st_async_v2(map_rank(sa(qin + rank * kBatchMaxT + t), r), wsh[t * 2], wsh[t * 2 + 1], map_rank(sa(qbar), r));
     }
   }
   cluster_arrive_relaxed();  // this CTA's last push into a peer is issued

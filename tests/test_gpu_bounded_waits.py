@@ -101,3 +101,48 @@ def test_refused_coresident_grid_falls_back(gsi, shape):
     torch.cuda.synchronize()
     assert gsi.workspace_status(ws) == 0
     compare(m_in, gm.M, Y, F, R)
+
+
+def test_small_batch_withheld_slice_times_out_and_recovers(gsi):
+    """The small-batch kernel (2 <= T <= 16, bf16) exchanges slices of G
+    across clusters through the same kind of epoch-tagged words: with cluster
+    0 withholding its words the polls give up (~10 ms), the call finishes,
+    the workspace reports the timeout and the wait that gave up, and after
+    re-initialisation the call is correct.  A refused co-resident launch
+    falls back to the earlier kernels with the same results."""
+    d, d_out, k = 1032, 1000, 128
+    V64 = synth.orthonormal_basis(synth.rng(9, d, k, 3), d, k)
+    m_in = synth.stack_layer(9, 1, {"qkv": V64}, {"qkv": (d_out, d)}, T=6, f_slow=0.5, roles=("qkv",))[0]
+    gm, X = upload(m_in)
+    ws = gsi.new_workspace(gsi.workspace_size(gm, 6, "batch"))
+    Y, F, R = gsi.linear(gm, X, m_in.eps, workspace=ws, path="batch")
+    torch.cuda.synchronize()
+    assert gsi.workspace_status(ws) == 0
+
+    gsi.lib().gsi_debug_withhold_slice(1)
+    t0 = time.perf_counter()
+    try:
+        gsi.linear(gm, X, m_in.eps, Y=Y, flags=F, rho=R, workspace=ws, path="batch")
+        torch.cuda.synchronize()
+    finally:
+        gsi.lib().gsi_debug_withhold_slice(0)
+    assert time.perf_counter() - t0 < 1.5, "the poll should give up after ~10 ms"
+    assert gsi.workspace_status(ws) == 1 | (1 << 11)
+
+    gsi.lib().gsi_workspace_init(ws.data_ptr(), ws.numel(), torch.cuda.current_stream().cuda_stream)
+    Y, F, R = gsi.linear(gm, X, m_in.eps, workspace=ws, path="batch")
+    torch.cuda.synchronize()
+    assert gsi.workspace_status(ws) == 0
+    compare(m_in, gm.M, Y, F, R)
+
+    # a refused co-resident launch: AUTO runs the call on the earlier kernels
+    gsi.lib().gsi_debug_refuse_coresident(1 << 20)
+    try:
+        Y2, F2, R2 = gsi.linear(gm, X, m_in.eps, workspace=ws)
+        with pytest.raises(gsi.GsiError, match="co-resident"):
+            gsi.linear(gm, X, m_in.eps, workspace=ws, path="batch")
+    finally:
+        gsi.lib().gsi_debug_refuse_coresident(0)
+    torch.cuda.synchronize()
+    assert gsi.workspace_status(ws) == 0
+    compare(m_in, gm.M, Y2, F2, R2)
