@@ -188,9 +188,9 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_decode_kernel(const __
   unsigned char* xs = smem + p.off_xs;                      // [16][xs_pitch] token slab
   float* inbox = reinterpret_cast<float*>(smem + p.off_in);  // [CS][T][ks]
   float* nin = reinterpret_cast<float*>(smem + p.off_nin);   // [CS][16]
-  float* g32 = reinterpret_cast<float*>(smem + p.off_g32);   // [CS][T][ks]: g by column slice
+  float* g32 = reinterpret_cast<float*>(smem + p.off_g32);   // [T][k]: g by token
   float* gnx = g32 + T * k;                                  // [16] ||x_t||^2
-  float* gt = inbox;                                         // [T][k]: g by token, once the inboxes are read
+  float* gt = g32;
   float* pg = reinterpret_cast<float*>(gbf);                 // [CS][T][ks]: this CTA's partial g
   float* fs = reinterpret_cast<float*>(smem + p.off_fs);     // [T][ks] this rank's final slice, then 16 norms
   float* nxs = reinterpret_cast<float*>(smem + p.off_nx);    // [16] the slab's ||x_t||^2
@@ -417,26 +417,17 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_decode_kernel(const __
     }
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     compute_sync();
-    // ---- all-gather: this rank's final slice (rank 0: and the norms) to every rank
-    if (tid < CS) {  // lane q of warp 0 sends this rank's slice (rank 0: and the norms) to rank q
-      const int q = tid;
-      bulk_s2c(map_rank(sa(g32 + rank * T * ks), q), fs, uint32_t(T * ks * 4), map_rank(sa(gxbar), q));
-      if (rank == 0) bulk_s2c(map_rank(sa(gnx), q), fs + T * ks, kBatchMaxT * 4, map_rank(sa(gxbar), q));
+    // ---- all-gather: thread 16 t + q sends token t of this rank's final
+    //      slice to rank q, where it lands in token order (rank 0: the norms
+    //      too), so the products below read consecutive columns of a token
+    if (tid < T * CS) {
+      const int t = tid >> 4, q = tid & (CS - 1);
+      bulk_s2c(map_rank(sa(g32 + t * k + rank * ks), q), fs + t * ks, uint32_t(ks * 4), map_rank(sa(gxbar), q));
+      if (rank == 0 && t == 0) bulk_s2c(map_rank(sa(gnx), q), fs + T * ks, kBatchMaxT * 4, map_rank(sa(gxbar), q));
       bulk_commit();
     }
     note(bar_wait_cluster(gxbar, 0, err, lim, kWaitGathered));
     if (tid < CS) bulk_wait_read();  // the partial g's space is about to hold g in bf16
-    // g by token (in the inboxes' space: every item has read them), so that
-    // the products below read consecutive columns of a token
-    {
-      const int f4s = ks / 4, per_q = T * f4s;
-#pragma unroll 1
-      for (int f = tid; f < CS * per_q; f += NC) {
-        const int q = f / per_q, r = f - q * per_q, t = r / f4s, c4 = r - t * f4s;
-        *reinterpret_cast<float4*>(gt + t * k + q * ks + 4 * c4) = reinterpret_cast<const float4*>(g32)[f];
-      }
-    }
-    compute_sync();
 
     // ---- shares of the Gram form: warp w takes tokens w and w + 8 over all of
     //      the rank's Gram rows i (columns c0 + i of g); lane l owns the column
@@ -522,13 +513,16 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_decode_kernel(const __
   }
   cluster_arrive_relaxed();  // this CTA's last push into a peer is issued
 
-  // ---- fast path for every token: M G = M hi + M lo, 16 x 8 tiles in registers
+  // ---- fast path for every token: M G = M hi + M lo, 16 x 8 tiles in
+  //      registers.  (Spreading the tiles over the copy warp too measured
+  //      slower: the tensor pipes are per SM sub-partition, and a ninth warp
+  //      puts three warps' tiles on one of them.)
   constexpr int kUnits = (kBatchMaxMt * NT + NW - 1) / NW;
   float facc[kUnits][4];
 #pragma unroll
   for (int j = 0; j < kUnits; ++j) facc[j][0] = facc[j][1] = facc[j][2] = facc[j][3] = 0.f;
+  const int gp = p.gbf_pitch;
   if (warp < NW) {
-    const int gp = p.gbf_pitch;
     // warp w: tokens w and w + 8, lanes over column pairs
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -542,7 +536,7 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_decode_kernel(const __
         *reinterpret_cast<uint32_t*>(gbf + (kBatchMaxT + t) * gp + col * 2) = l0 | (l1 << 16);
       }
     }
-    compute_sync();
+    compute_sync();  // g in bf16 is in place
     if (nrows > 0) {
       note(__all_sync(FULL, bar_wait(mbar, 0, err, lim, kWaitM)));
       const uint32_t ms_a = sa(ms), gh_a = sa(gbf), gl_a = sa(gbf + kBatchMaxT * gp);
@@ -723,7 +717,7 @@ __global__ void __launch_bounds__(kBatchThreads, 1) batch_decode_kernel(const __
     for (int j = nch - S > 0 ? nch - S : 0; j < nch; ++j)
       bar_wait(&full[j % S], uint32_t(j / S) & 1u, err, ok ? lim : kSpinCyclesAfterError, kWaitRing);
   }
-  if (tid < CS) bulk_wait_read();  // the all-gather's source
+  if (tid < T * CS) bulk_wait_read();  // the all-gather's source
   // No CTA leaves while a peer of its cluster may still push into it.
   cluster_wait();
 }
