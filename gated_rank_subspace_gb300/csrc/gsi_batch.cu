@@ -13,21 +13,23 @@
 // fp32 on the CUDA cores.
 //
 //   prologue  the copy warp (the ninth) issues the TMA copies of the CTA's
-//             V_k slab and M rows and the bulk copy of its rank's Gram slice
-//             (weight traffic, before the dependency wait on the previous
-//             kernel of the stream).
+//             V_k slab and the bulk copy of its rank's Gram slice (weight
+//             traffic, before the dependency wait on the previous kernel of
+//             the stream), and the M rows once the V_k slab has landed;
+//             three threads stage the next map's weights and tokens in L2.
 //   project   CTA b multiplies its token slab [16 x vr] by its V_k slab
 //             [vr x k] (grid projection); warp w takes the 8-column tiles
-//             w, w + 8, ... of g.  The fp32 partials go from the
-//             accumulators to the rank owning their columns (st.async into
-//             its shared memory, completion on its mbarrier), the slab's
-//             ||x_t||^2 to rank 0.
-//   reduce    rank q adds its inboxes in rank order and publishes its slice
-//             of the cluster's sum as epoch-tagged 64-bit words; it polls
-//             every cluster's words of that slice, adds them in cluster
-//             order and pushes the slice of the final g to every rank of its
-//             cluster (rank 0 does the same for the norms).  Every CTA ends
-//             with the same bits of G [T][k] and of ||x_t||^2.
+//             w, w + 8, ... of g.  The fp32 accumulators go to shared memory
+//             by column slice; lane q of warp 0 sends slice q to rank q with
+//             one bulk copy into its shared memory (completion on its
+//             mbarrier), and the slab's ||x_t||^2 to rank 0.
+//   reduce    rank q adds its 16 inboxes in rank order and publishes its
+//             slice of the cluster's sum as epoch-tagged 64-bit words; it
+//             polls every cluster's words of that slice, adds them in
+//             cluster order and sends the final slice to every rank of its
+//             cluster, one bulk copy per token, landing in token order (rank
+//             0 does the same for the norms).  Every CTA ends with the same
+//             bits of G [T][k] and of ||x_t||^2.
 //   decide    warp w takes tokens w and w + 8 over all of the rank's Gram
 //             slice: their shares of g^T (V_k^T V_k) g and of ||g||^2 go to
 //             every rank; every CTA adds the ranks' shares in rank order, so
