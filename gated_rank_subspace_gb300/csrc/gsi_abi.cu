@@ -660,8 +660,8 @@ static gsi_status run_tensor(const gsi_map_desc* m, const void* X, int64_t T, fl
   t.flags = flags;
   t.Y = Y;
   t.err = &ctrl->err;
-  t.fpart = reinterpret_cast<float4*>(base + L.fpart);
-  t.fin_arrive = &ctrl->fin_arrive;
+  t.gT = reinterpret_cast<float*>(base + L.gt);
+  t.norms = reinterpret_cast<float2*>(base + L.norms);
   return cuda_check(launch_tensor_path(t, st), "tensor-core path launch");
 }
 

@@ -334,9 +334,7 @@ struct Ctrl {
   unsigned long long ticket1[2];
   // the persistent stack kernel's arrivals at its barriers between maps
   unsigned long long arrive[2];
-  // the tensor path's finalize: CTAs of the current launch that have stored
-  // their partial sums (the last one resets it)
-  uint32_t fin_arrive;
+  uint32_t unused0;
   // the small-batch decode's call numbers (its grid projection's epochs), per
   // element type
   unsigned long long ticket_b[2];

@@ -205,8 +205,8 @@ struct TensorArgs {
   uint8_t* flags;       // T
   float* Y;             // T x d_out
   uint32_t* err;        // device error word
-  float4* fpart;        // finalize partial sums [chunks][blocks][16]
-  uint32_t* fin_arrive; // finalize arrival counter (control words)
+  float* gT;            // float32 g by chunks of 8 tokens: [chunk][k][8]
+  float2* norms;        // per token (||g||^2, ||x||^2)
 };
 
 cudaError_t launch_tensor_path(const TensorArgs& t, cudaStream_t s);

@@ -100,7 +100,7 @@ inline FusedLayout layout_fused(int64_t k, int64_t T) {
 
 // Workspace layout of one tensor-core-path call.
 struct TensorLayout {
-  size_t ctrl, vt, g, gbf, gfast, xslow, idx, fpart, total;
+  size_t ctrl, vt, g, gbf, gfast, xslow, idx, gt, norms, total;
 };
 
 // Token count of a prefill-sized call: the tensor path's slow-token
@@ -112,20 +112,32 @@ constexpr int64_t kTensorMinT = 128;
 constexpr int kGSplitMax = 16;
 inline int g_split(int64_t T) { return T < kTensorMinT ? 16 : 8; }
 
-// The tensor path's finalize (rho, flags, bf16 g) takes tokens in chunks of
-// kFinTok and cuts the Gram rows into fin_blocks(T, k) blocks, so that the
-// grid holds about two CTAs per SM of a GB300 whatever T (one block once
-// there are 304 chunks).  (16 tokens a CTA read the Gram half as often but
-// measured ~20 us slower at T = 2048: fewer CTAs, twice the accumulators.)
+// The tensor path's finalize (rho, flags, bf16 g) runs as two kernels: a
+// per-token pass (kNormThreads threads a token: split-K sum of g, ||g||^2,
+// ||x||^2) and the Gram form, which takes tokens in chunks of kFinTok and
+// cuts the Gram rows into fin_blocks(T, k) blocks, one thread-block cluster
+// a chunk, so that every T gives about three CTAs an SM of a GB300 (456) or
+// more: at most kFinMaxBlocks blocks (a portable cluster) and at least 32
+// Gram rows a block.  A CTA of the Gram form has kFinThreads threads (two
+// token quads x 64 column quads of a kFinCols-column pass) and streams its
+// Gram rows through kFinStages shared-memory stages of kFinStageBytes.
 constexpr int kFinTok = 8;
+constexpr int kNormThreads = 64;
+constexpr int kFinThreads = 128;
+constexpr int kFinCols = 256;
+constexpr int kFinStages = 3;
+constexpr int64_t kFinStageBytes = 12288;
+constexpr int kFinMaxBlocks = 8;
 inline int fin_blocks(int64_t T, int64_t k) {
   const int64_t chunks = cdiv(T, kFinTok);
-  if (chunks >= 304) return 1;
-  int64_t nb = cdiv(304, chunks);
-  const int64_t cap = k / 8 > 0 ? k / 8 : 1;  // at least 8 Gram rows a block
+  int64_t nb = cdiv(456, chunks);
+  int64_t cap = k / 32 < kFinMaxBlocks ? k / 32 : kFinMaxBlocks;
+  if (cap < 1) cap = 1;
   if (nb > cap) nb = cap;
-  if (nb > 64) nb = 64;
   return int(nb < 1 ? 1 : nb);
+}
+inline size_t fin_smem(int64_t k) {
+  return size_t(kFinStages) * kFinStageBytes + size_t(kFinTok) * k * 4 + 4 * kFinTok * 4;
 }
 
 inline TensorLayout layout_tensor(int64_t d, int64_t k, int64_t T) {
@@ -138,7 +150,8 @@ inline TensorLayout layout_tensor(int64_t d, int64_t k, int64_t T) {
   L.gfast = off;  off += align256(size_t(T) * k * 2);
   L.xslow = off;  off += align256(size_t(T) * d * 2);
   L.idx = off;    off += align256(size_t(2) * T * 4);
-  L.fpart = off;  off += align256(size_t(cdiv(T, kFinTok)) * fin_blocks(T, k) * kFinTok * 16);
+  L.gt = off;     off += align256(size_t(cdiv(T, kFinTok)) * kFinTok * k * 4);  // g by chunk, column, token slot
+  L.norms = off;  off += align256(size_t(T) * 8);                                  // (||g||^2, ||x||^2)
   L.total = off;
   return L;
 }

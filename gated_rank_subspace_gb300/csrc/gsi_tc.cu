@@ -47,6 +47,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
                : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -75,6 +79,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
 
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// 1-D bulk copy global -> shared completing on an mbarrier (both addresses
+// 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y) {
@@ -527,15 +540,25 @@ __global__ void transpose_bf16_kernel(const uint16_t* __restrict__ V, uint16_t* 
   }
 }
 
-// Per token: ||x||^2, g^T Gram g, rho, flag, and g rounded to bf16.
-// CTA (c, b) takes tokens [16 c, 16 c + 16), Gram rows [k b / nb, k (b + 1) / nb)
-// and the same share of each token's x for ||x||^2.  Every CTA adds the
-// split-K slices of g for its tokens (all k columns: the Gram form needs
-// them); block 0 also writes the bf16 g and ||g||^2.  With one block (large
-// T) a CTA finishes its tokens itself.  Otherwise each CTA stores its partial
-// sums and the grid's last CTA to arrive (a counter in the control words,
-// reset by that CTA) adds them in block order for every token; every sum has
-// one fixed order.
+// The finalize: per token ||x||^2, ||g||^2, g^T Gram g, rho, flag and g
+// rounded to bf16, in two kernels.
+//
+// tc_norms_kernel, one CTA of 64 threads a token: adds the split-K slices of
+// g in slice order (four columns a thread, every slice's 16-byte load in
+// flight together with the first batch of x's vectors), writes the bf16 g and
+// the float32 g into gT, laid out by chunks of kFinTok tokens as
+// [chunk][column j][token slot] so that a chunk is one contiguous block with
+// the chunk's g_j side by side, and stores (||g||^2, ||x||^2).
+//
+// tc_gramq_kernel, CTA (c, b) of a (1, nb, 1) cluster: the chunk's g lands by
+// one bulk copy; Gram rows [k b / nb, k (b + 1) / nb) stream through a ring
+// of kFinStages shared-memory stages, one bulk copy a row into a fixed row
+// stride.  Register-tiled Gram form: thread (tq, cq) keeps h[t][v] = sum over
+// the block's rows i of g_t[i] Gram[i][c + v] for the four tokens t of quad
+// tq and the four columns c + v of quad cq in each 256-column pass (two
+// 16-byte shared loads per sixteen FMAs), then adds g_t[c + v] h[t][v].  The
+// blocks' partial sums meet in the cluster's rank 0, which adds them in block
+// order and takes rho and the flag.  Every sum has one fixed order.
 __device__ __forceinline__ void fin_token(float qq, float nn, float x2, float eps, float* rho_out, uint8_t* flags,
                                           int t) {
   float rr = x2 - 2.f * nn + qq;
@@ -545,174 +568,258 @@ __device__ __forceinline__ void fin_token(float qq, float nn, float x2, float ep
   flags[t] = (rho < eps) ? uint8_t(0) : uint8_t(1);
 }
 
-// Row stride of the finalize's g-by-column buffer: the chunk's tokens plus
-// four floats (16-byte aligned rows that fall on different banks).
-constexpr int kFinStride = kFinTok + 4;
-
 template <int GS>
-__global__ void __launch_bounds__(256) tc_finalize_kernel(const uint16_t* __restrict__ X, const float* __restrict__ G,
-                                                          const float* __restrict__ gram, int64_t d, int k, int T,
-                                                          float eps, float* __restrict__ rho_out,
-                                                          uint8_t* __restrict__ flags, uint16_t* __restrict__ Gbf,
-                                                          int gsplit, int nb, float4* __restrict__ part,
-                                                          uint32_t* arrive) {
-  extern __shared__ float fsm[];
-  // g by column: the chunk's tokens of column j at gs[j * kFinStride ...], so
-  // one 16-byte broadcast load gives four tokens' g_j
-  float* gs = fsm;                       // [k][kFinStride]
-  float* red = gs + kFinStride * k;      // [8 warps][kFinTok][2]
-  float* x2s = red + 8 * kFinTok * 2;    // [kFinTok]
-  __shared__ bool s_last;
-  const int cb = blockIdx.x, blk = blockIdx.y;
+__global__ void __launch_bounds__(kNormThreads) tc_norms_kernel(const uint16_t* __restrict__ X,
+                                                                const float* __restrict__ G, int64_t d, int k,
+                                                                int T, int gsplit, float* __restrict__ gT,
+                                                                uint16_t* __restrict__ Gbf,
+                                                                float2* __restrict__ norms) {
+  __shared__ float red[2][2];
+  const int t = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();
+  const uint4* xr = reinterpret_cast<const uint4*>(X + int64_t(t) * d);
+  const int64_t nv = d / 8;
+  // the first batch of x's 16-byte vectors, in flight while g is summed
+  uint4 xq[8];
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    xq[u] = tid + kNormThreads * u < nv ? ld_cg_v4(xr + tid + kNormThreads * u) : make_uint4(0u, 0u, 0u, 0u);
+  const int kq = k / 4;
+  const int64_t ss4 = int64_t(T) * kq;  // slice stride in 16-byte units
+  const float4* g0 = reinterpret_cast<const float4*>(G) + int64_t(t) * kq;
+  float* gc = gT + int64_t(t / kFinTok) * k * kFinTok + (t % kFinTok);
+  float nn = 0.f;
+  for (int j4 = tid; j4 < kq; j4 += kNormThreads) {
+    float4 v[GS];
+#pragma unroll
+    for (int sl = 0; sl < GS; ++sl) v[sl] = sl < gsplit ? __ldcg(g0 + sl * ss4 + j4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 g = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int sl = 0; sl < GS; ++sl) {
+      g.x += v[sl].x;
+      g.y += v[sl].y;
+      g.z += v[sl].z;
+      g.w += v[sl].w;
+    }
+    const int j = 4 * j4;
+    gc[(j + 0) * kFinTok] = g.x;
+    gc[(j + 1) * kFinTok] = g.y;
+    gc[(j + 2) * kFinTok] = g.z;
+    gc[(j + 3) * kFinTok] = g.w;
+    __nv_bfloat162 lo = __floats2bfloat162_rn(g.x, g.y), hi = __floats2bfloat162_rn(g.z, g.w);
+    uint2 pk;
+    pk.x = *reinterpret_cast<uint32_t*>(&lo);
+    pk.y = *reinterpret_cast<uint32_t*>(&hi);
+    *reinterpret_cast<uint2*>(Gbf + int64_t(t) * k + j) = pk;
+    nn = fmaf(g.x, g.x, nn);
+    nn = fmaf(g.y, g.y, nn);
+    nn = fmaf(g.z, g.z, nn);
+    nn = fmaf(g.w, g.w, nn);
+  }
+  // ||x||^2: squares in vector order a thread
+  float xx = 0.f;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    float f[8];
+    BF16::unpack(xq[u], f);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) xx = fmaf(f[e], f[e], xx);
+  }
+  for (int64_t vb = tid + kNormThreads * 8; vb < nv; vb += kNormThreads * 8) {
+#pragma unroll
+    for (int u = 0; u < 8; ++u)
+      xq[u] = vb + kNormThreads * u < nv ? ld_cg_v4(xr + vb + kNormThreads * u) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      float f[8];
+      BF16::unpack(xq[u], f);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) xx = fmaf(f[e], f[e], xx);
+    }
+  }
+  nn = warp_sum(nn);
+  xx = warp_sum(xx);
+  if (lane == 0) {
+    red[warp][0] = nn;
+    red[warp][1] = xx;
+  }
+  __syncthreads();
+  if (tid == 0) norms[t] = make_float2(red[0][0] + red[1][0], red[0][1] + red[1][1]);
+}
+
+__device__ __forceinline__ void quad_fma(float (&h)[4][4], const float4 g, const float4 m) {
+  const float gt[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+  for (int t = 0; t < 4; ++t) {
+    h[t][0] = fmaf(gt[t], m.x, h[t][0]);
+    h[t][1] = fmaf(gt[t], m.y, h[t][1]);
+    h[t][2] = fmaf(gt[t], m.z, h[t][2]);
+    h[t][3] = fmaf(gt[t], m.w, h[t][3]);
+  }
+}
+
+// nr Gram rows of one ring stage (row stride KS) into the first NL passes'
+// accumulators, in row order.
+template <int NP, int NL, int R, int KS>
+__device__ __forceinline__ void gram_rows(float (&h)[NP][4][4], const float* sg, const float* gr, int nr) {
+  if (nr == R) {
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      const float4 g4 = *reinterpret_cast<const float4*>(gr + r * kFinTok);
+#pragma unroll
+      for (int p = 0; p < NL; ++p)
+        quad_fma(h[p], g4, *reinterpret_cast<const float4*>(sg + r * KS + p * kFinCols));
+    }
+  } else {
+    for (int r = 0; r < nr; ++r) {
+      const float4 g4 = *reinterpret_cast<const float4*>(gr + r * kFinTok);
+#pragma unroll
+      for (int p = 0; p < NL; ++p)
+        quad_fma(h[p], g4, *reinterpret_cast<const float4*>(sg + r * KS + p * kFinCols));
+    }
+  }
+}
+
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void st_cluster_f32(const float* local, uint32_t rank, float v) {
+  uint32_t raddr;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(smem_u32(local)), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(raddr), "f"(v) : "memory");
+}
+
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// NP: 256-column passes over the Gram (k <= 256 NP).  Warps 0-3 compute;
+// warp 4 fills the ring: a stage is refilled once the four compute warps
+// have arrived on its "empty" barrier.
+template <int NP>
+__global__ void __launch_bounds__(kFinThreads + 32) tc_gramq_kernel(const float* __restrict__ gT,
+                                                                    const float* __restrict__ gram,
+                                                                    const float2* __restrict__ norms, int k, int T,
+                                                                    float eps, float* __restrict__ rho_out,
+                                                                    uint8_t* __restrict__ flags, int nb,
+                                                                    uint32_t* err) {
+  constexpr int KS = NP * kFinCols;                    // ring row stride (floats)
+  constexpr int R = int(kFinStageBytes / (KS * 4));    // Gram rows a stage
+  extern __shared__ float4 fsm4[];
+  __shared__ uint64_t full[kFinStages], empty[kFinStages], gbar;
+  __shared__ float qred[kFinMaxBlocks][kFinTok];       // rank 0: the blocks' q partials
+  float* ring = reinterpret_cast<float*>(fsm4);        // [kFinStages][R][KS]
+  float* gs = ring + kFinStages * R * KS;              // [k][kFinTok]
+  float* red = gs + kFinTok * k;                       // [4 warps][kFinTok]
+  const int cb = blockIdx.x, blk = blockIdx.y;         // blk: rank in the (1, nb, 1) cluster
   const int t0 = cb * kFinTok;
+  const int tn = T - t0 < kFinTok ? T - t0 : kFinTok;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int i0 = int(int64_t(k) * blk / nb), i1 = int(int64_t(k) * (blk + 1) / nb);
+  const int nchunk = gram ? (i1 - i0 + R - 1) / R : 0;
+  if (nb > 1) cluster_arrive_relaxed();
+  if (tid == kFinThreads) {
+    for (int s = 0; s < kFinStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 4);
+    }
+    mbar_init(&gbar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
   pdl_wait();
-  // g = the split-K slices' partial projections, added in slice order; a
-  // thread loads the slices of 4 elements (4 GS loads in flight) before adding
-  for (int e0 = tid; e0 < kFinTok * k; e0 += 256 * 4) {
-    float v[4][GS];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int e = e0 + q * 256;
-      const int t = e / k, j = e - (e / k) * k;
-      const bool live = e < kFinTok * k && t0 + t < T;
-#pragma unroll
-      for (int sl = 0; sl < GS; ++sl)
-        v[q][sl] = (live && sl < gsplit) ? __ldcg(&G[(int64_t(sl) * T + t0 + t) * k + j]) : 0.f;
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int e = e0 + q * 256;
-      if (e >= kFinTok * k) break;
-      const int t = e / k, j = e - (e / k) * k;
-      float g = 0.f;
-#pragma unroll
-      for (int sl = 0; sl < GS; ++sl) g += v[q][sl];
-      gs[j * kFinStride + t] = g;
-      if (blk == 0 && t0 + t < T) {
-        __nv_bfloat16 bv = __float2bfloat16_rn(g);
-        Gbf[int64_t(t0 + t) * k + j] = *reinterpret_cast<uint16_t*>(&bv);
-      }
-    }
-  }
-  __syncthreads();
-  // this block's share of g^T Gram g: thread j forms h_j = sum over the
-  // block's rows i of g_i Gram_ij, then adds g_j h_j; block 0: ||g||^2
-  float q[kFinTok], n[kFinTok];
-#pragma unroll
-  for (int t = 0; t < kFinTok; ++t) q[t] = n[t] = 0.f;
-  for (int j = tid; j < k; j += 256) {
-    float h[kFinTok];
-#pragma unroll
-    for (int t = 0; t < kFinTok; ++t) h[t] = 0.f;
-    if (gram) {
-      // Gram rows in batches of 32 loads in flight, added in row order
-      int i = i0;
-      for (; i + 32 <= i1; i += 32) {
-        float gv[32];
-#pragma unroll
-        for (int u = 0; u < 32; ++u) gv[u] = __ldg(&gram[int64_t(i + u) * k + j]);
-#pragma unroll
-        for (int u = 0; u < 32; ++u) {
-          const float4* gi = reinterpret_cast<const float4*>(gs + (i + u) * kFinStride);
-#pragma unroll
-          for (int t4 = 0; t4 < kFinTok / 4; ++t4) {
-            const float4 g4 = gi[t4];
-            h[4 * t4] = fmaf(g4.x, gv[u], h[4 * t4]);
-            h[4 * t4 + 1] = fmaf(g4.y, gv[u], h[4 * t4 + 1]);
-            h[4 * t4 + 2] = fmaf(g4.z, gv[u], h[4 * t4 + 2]);
-            h[4 * t4 + 3] = fmaf(g4.w, gv[u], h[4 * t4 + 3]);
-          }
-        }
-      }
-      if (i < i1) {
-        float gv[32];
-#pragma unroll
-        for (int u = 0; u < 32; ++u) gv[u] = i + u < i1 ? __ldg(&gram[int64_t(i + u) * k + j]) : 0.f;
-#pragma unroll
-        for (int u = 0; u < 32; ++u)
-          if (i + u < i1)
-#pragma unroll
-            for (int t = 0; t < kFinTok; ++t) h[t] = fmaf(gs[(i + u) * kFinStride + t], gv[u], h[t]);
-      }
-    }
-#pragma unroll
-    for (int t = 0; t < kFinTok; ++t) {
-      const float gj = gs[j * kFinStride + t];
-      if (blk == 0) n[t] = fmaf(gj, gj, n[t]);
-      if (gram) q[t] = fmaf(gj, h[t], q[t]);
-    }
-  }
-  // (without a Gram matrix the basis is taken as orthonormal: g^T g)
-  if (!gram) {
-#pragma unroll
-    for (int t = 0; t < kFinTok; ++t) q[t] = n[t];
-  }
-  // ||x||^2 over this block's share of the row's 16-byte vectors: warp w takes
-  // tokens w, w + 8, ..., eight loads in flight per lane, squares in order
-  const int64_t nv = d / 8;
-  const int64_t xv0 = nv * blk / nb, xv1 = nv * (blk + 1) / nb;
-  for (int tw = warp; tw < kFinTok; tw += 8) {
-    float s = 0.f;
-    if (t0 + tw < T) {
-      const uint4* xr = reinterpret_cast<const uint4*>(X + int64_t(t0 + tw) * d);
-      for (int64_t vb = xv0 + lane; vb < xv1; vb += 32 * 8) {
-        uint4 xq[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) xq[u] = vb + 32 * u < xv1 ? ld_cg_v4(xr + vb + 32 * u) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          float f[8];
-          BF16::unpack(xq[u], f);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) s = fmaf(f[e], f[e], s);
-        }
-      }
-    }
-    s = warp_sum(s);
-    if (lane == 0) x2s[tw] = s;
-  }
-#pragma unroll
-  for (int t = 0; t < kFinTok; ++t) {
-    const float a = warp_sum(q[t]), b = warp_sum(n[t]);
+  float qq = 0.f;
+  if (warp == 4) {
+    // ---- producer: the chunk's g, then the block's Gram rows, lane r a row
     if (lane == 0) {
-      red[(warp * kFinTok + t) * 2 + 0] = a;
-      red[(warp * kFinTok + t) * 2 + 1] = b;
+      mbar_expect_tx(&gbar, uint32_t(kFinTok) * k * 4);
+      bulk_load_1d(gs, gT + int64_t(cb) * kFinTok * k, uint32_t(kFinTok) * k * 4, &gbar);
+    }
+    for (int ch = 0; ch < nchunk; ++ch) {
+      const int st = ch % kFinStages;
+      const int r0 = i0 + ch * R, nr = i1 - r0 < R ? i1 - r0 : R;
+      if (ch >= kFinStages &&
+          !__all_sync(0xffffffffu, mbar_wait(&empty[st], uint32_t(ch / kFinStages - 1) & 1u, err)))
+        break;  // a compute warp never released the stage (error word set)
+      if (lane == 0) mbar_expect_tx(&full[st], uint32_t(nr) * k * 4);
+      __syncwarp();
+      if (lane < nr)
+        bulk_load_1d(ring + (size_t(st) * R + lane) * KS, gram + int64_t(r0 + lane) * k, uint32_t(k) * 4,
+                     &full[st]);
+    }
+  } else {
+    // ---- compute warps
+    bool failed = !mbar_wait(&gbar, 0, err);
+    // token slots past T hold whatever the workspace held: zero them
+    if (tn < kFinTok) {
+      for (int e = tid; e < kFinTok * k; e += kFinThreads)
+        if (e % kFinTok >= tn) gs[e] = 0.f;
+      consumer_sync();
+    }
+    // this block's share of g^T Gram g, the Gram rows in row order
+    const int tq = tid >> 6, cq = tid & 63;
+    const bool live0 = 4 * cq < k;                       // k % 8 == 0: a quad is whole or absent
+    const bool live1 = NP == 2 && kFinCols + 4 * cq < k;
+    float h[NP][4][4];
+#pragma unroll
+    for (int p = 0; p < NP; ++p)
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) h[p][t][v] = 0.f;
+    for (int ch = 0; ch < nchunk; ++ch) {
+      const int st = ch % kFinStages;
+      const int r0 = i0 + ch * R, nr = i1 - r0 < R ? i1 - r0 : R;
+      if (!failed && !mbar_wait(&full[st], uint32_t(ch / kFinStages) & 1u, err)) failed = true;
+      const float* sg = ring + size_t(st) * R * KS + 4 * cq;
+      const float* gr = gs + r0 * kFinTok + 4 * tq;
+      if (live1)
+        gram_rows<NP, (NP > 1 ? 2 : 1), R, KS>(h, sg, gr, nr);
+      else if (live0)
+        gram_rows<NP, 1, R, KS>(h, sg, gr, nr);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with the stage
+    }
+    // q_t over the thread's columns: sum of g_t[c + v] h[t][v]
+    float q[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int p = 0; p < NP; ++p) {
+      if (!(p == 0 ? live0 : live1)) continue;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const float4 gc = *reinterpret_cast<const float4*>(gs + (p * kFinCols + 4 * cq + v) * kFinTok + 4 * tq);
+        q[0] = fmaf(gc.x, h[p][0][v], q[0]);
+        q[1] = fmaf(gc.y, h[p][1][v], q[1]);
+        q[2] = fmaf(gc.z, h[p][2][v], q[2]);
+        q[3] = fmaf(gc.w, h[p][3][v], q[3]);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float a = warp_sum(q[t]);
+      if (lane == 0) red[warp * kFinTok + 4 * tq + t] = a;
+    }
+    consumer_sync();
+    if (tid < kFinTok) {
+      const int w0 = (tid >> 2) * 2;  // the two warps of this token's quad
+      qq = red[w0 * kFinTok + tid] + red[(w0 + 1) * kFinTok + tid];
     }
   }
-  __syncthreads();
-  if (tid < kFinTok && t0 + tid < T) {
-    float qq = 0.f, nn = 0.f;
-    for (int w = 0; w < 8; ++w) {
-      qq += red[(w * kFinTok + tid) * 2 + 0];
-      nn += red[(w * kFinTok + tid) * 2 + 1];
+  if (nb > 1) {
+    cluster_wait();  // every CTA of the cluster runs: rank 0's shared memory is live
+    if (tid < kFinTok) st_cluster_f32(&qred[blk][tid], 0u, qq);
+    cluster_arrive_release();
+    cluster_wait();
+    if (blk != 0) return;
+    if (tid < kFinTok) {
+      qq = 0.f;
+      for (int b = 0; b < nb; ++b) qq += qred[b][tid];
     }
-    if (nb == 1)
-      fin_token(qq, nn, x2s[tid], eps, rho_out, flags, t0 + tid);
-    else
-      part[(int64_t(cb) * nb + blk) * kFinTok + tid] = make_float4(qq, nn, x2s[tid], 0.f);
   }
-  if (nb == 1) return;
-  // the last CTA of the grid adds every token's block partials in block order
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) s_last = atomicAdd(arrive, 1u) == gridDim.x * gridDim.y - 1u;
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int t = tid; t < T; t += 256) {
-    const int c = t / kFinTok, tt = t - c * kFinTok;
-    float qq = 0.f, nn = 0.f, x2 = 0.f;
-    for (int bb = 0; bb < nb; ++bb) {
-      const float4 p = __ldcg(&part[(int64_t(c) * nb + bb) * kFinTok + tt]);
-      qq += p.x;
-      nn += p.y;
-      x2 += p.z;
-    }
-    fin_token(qq, nn, x2, eps, rho_out, flags, t);
+  if (tid < tn) {
+    const float2 nx = __ldcg(&norms[t0 + tid]);
+    // (without a Gram matrix the basis is taken as orthonormal: g^T g)
+    fin_token(gram ? qq : nx.x, nx.x, nx.y, eps, rho_out, flags, t0 + tid);
   }
-  if (tid == 0) *arrive = 0u;  // for the next call on this workspace
 }
 
 // Gather rows: dst[j] = src[idx[j]] for j < count (16-byte vectors).
@@ -851,17 +958,26 @@ static cudaError_t launch_skinny(const void* A, int64_t a_rows, const void* B, i
   return launch_skinny_t<128>(A, a_rows, B, b_rows, K, sp, args, s);
 }
 
-static cudaError_t launch_pdl(const void* kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args) {
+// cluster_y > 1: thread-block clusters of (1, cluster_y, 1).
+static cudaError_t launch_pdl(const void* kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s, void** args,
+                              unsigned cluster_y = 1) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   at[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
+  if (cluster_y > 1) {
+    at[1].id = cudaLaunchAttributeClusterDimension;
+    at[1].val.clusterDim.x = 1;
+    at[1].val.clusterDim.y = cluster_y;
+    at[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   return cudaLaunchKernelExC(&cfg, kern, args);
 }
 
@@ -944,31 +1060,40 @@ cudaError_t launch_tensor_path(const TensorArgs& t, cudaStream_t s) {
   g.c_split = T * k;
   const int g_bn = (T >= kTensorMinT && k >= 256) ? 256 : 64;
   if ((e = launch_tc_gemm(t.X, T, t.Vt, k, int(d), g_bn, g, s)) != cudaSuccess) return e;
-  // 3. rho, flags, bf16 g
+  // 3. rho, flags, bf16 g: the per-token pass, then the Gram form
   {
-    const void* X = t.X;
+    const uint16_t* X = static_cast<const uint16_t*>(t.X);
     const float* G = t.G;
-    const float* gram = t.gram;
     int64_t dd = d;
+    int kk = int(k), TT = int(T), gs = gsplit;
+    float* gT = t.gT;
+    uint16_t* Gbf = t.Gbf;
+    float2* norms = t.norms;
+    void* args[] = {&X, &G, &dd, &kk, &TT, &gs, &gT, &Gbf, &norms};
+    const void* kern = gsplit > 8 ? reinterpret_cast<const void*>(tc_norms_kernel<kGSplitMax>)
+                                  : reinterpret_cast<const void*>(tc_norms_kernel<8>);
+    if ((e = launch_pdl(kern, dim3(unsigned(T)), dim3(kNormThreads), 0, s, args)) != cudaSuccess) return e;
+  }
+  {
+    const float* gT = t.gT;
+    const float* gram = t.gram;
+    const float2* norms = t.norms;
     int kk = int(k), TT = int(T);
     float eps = t.eps;
     float* rho = t.rho;
     uint8_t* flags = t.flags;
-    uint16_t* Gbf = t.Gbf;
-    int gs = gsplit;
     int nb = fin_blocks(T, k);
-    float4* part = t.fpart;
-    uint32_t* arrive = t.fin_arrive;
-    void* args[] = {&X, &G, &gram, &dd, &kk, &TT, &eps, &rho, &flags, &Gbf, &gs, &nb, &part, &arrive};
-    const size_t smem = size_t(kFinStride) * k * 4 + 8 * kFinTok * 2 * 4 + kFinTok * 4;
-    const void* kern = gsplit > 8 ? reinterpret_cast<const void*>(tc_finalize_kernel<kGSplitMax>)
-                                  : reinterpret_cast<const void*>(tc_finalize_kernel<8>);
+    uint32_t* err = t.err;
+    void* args[] = {&gT, &gram, &norms, &kk, &TT, &eps, &rho, &flags, &nb, &err};
+    const size_t smem = fin_smem(k);
+    const void* kern = k > kFinCols ? reinterpret_cast<const void*>(tc_gramq_kernel<2>)
+                                    : reinterpret_cast<const void*>(tc_gramq_kernel<1>);
     if (smem > 48 * 1024) {
       if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem))) != cudaSuccess)
         return e;
     }
-    if ((e = launch_pdl(kern, dim3(unsigned(cdiv(T, kFinTok)), unsigned(nb)), dim3(256), smem, s, args)) !=
-        cudaSuccess)
+    if ((e = launch_pdl(kern, dim3(unsigned(cdiv(T, kFinTok)), unsigned(nb)), dim3(kFinThreads + 32), smem, s,
+                        args, unsigned(nb))) != cudaSuccess)
       return e;
   }
   // 4. compaction and gathers
