@@ -77,8 +77,46 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32
   return true;
 }
 
+// The same wait with a suspend-time hint: a waiting thread sleeps until the
+// phase completes (or ~0.1 ms pass) instead of spinning on the barrier, so it
+// takes no issue slots from the warps that compute.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(100000u)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t* err) {
+  if (mbar_try_wait_sleep(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait_sleep(bar, parity)) {
+    if (clock64() - t0 > kWaitCycles) {
+      atomicOr(err, kErrTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
 __device__ __forceinline__ void fence_barrier_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// 1-D bulk copy shared -> global in the thread's bulk group (both addresses
+// 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_store_1d(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_store_commit_wait_read() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
 // 1-D bulk copy global -> shared completing on an mbarrier (both addresses
@@ -282,6 +320,11 @@ __global__ void __launch_bounds__(128, 1)
     static_assert(size_t(kBM) * LD * 4 <= size_t(C::STAGES) * (C::A_BYTES + C::B_BYTES), "staging fits");
     float* st = reinterpret_cast<float*>(sA) + size_t(warp) * 32 * LD;
     const bool vec = (a.ldc % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.C) & 15) == 0);
+    // float32 rows with 16-byte aligned starts and lengths leave by bulk
+    // copies: lane i sends the staged row i, and the warp waits only until
+    // the copies have read the staging buffer, so the writes drain to memory
+    // while the CTA finishes and the next CTA of the SM loads its operands
+    const bool bulk = !a.c_bf16 && vec && (a.N % 4 == 0) && (a.c_split % 4 == 0);
 #pragma unroll 1
     for (int u = 0; u < MT; ++u) {
 #pragma unroll 1
@@ -296,6 +339,17 @@ __global__ void __launch_bounds__(128, 1)
     const int r_base = (m_tile * MT + u) * kBM + warp * 32;
     const int my_r = r_base + lane;
     const int64_t my_orow = my_r < rows ? (a.row_map ? int64_t(__ldcg(&a.row_map[my_r])) : int64_t(my_r)) : 0;
+    if (bulk) {
+      const int ncols = a.N - n_tile * BN < BN ? a.N - n_tile * BN : BN;
+      if (my_r < rows && ncols > 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // this lane's staged row -> async proxy
+        bulk_store_1d(a.C + int64_t(blockIdx.z) * a.c_split + my_orow * a.ldc + int64_t(n_tile) * BN, st + lane * LD,
+                      uint32_t(ncols) * 4);
+      }
+      bulk_store_commit_wait_read();
+      __syncwarp();
+      continue;
+    }
     for (int i = 0; i < 32 && r_base + i < rows; ++i) {
       const int64_t orow = __shfl_sync(0xffffffffu, my_orow, i);
       const int64_t cofs = int64_t(blockIdx.z) * a.c_split + orow * a.ldc + int64_t(n_tile) * BN;
@@ -553,10 +607,10 @@ __global__ void transpose_bf16_kernel(const uint16_t* __restrict__ V, uint16_t* 
 // tc_gramq_kernel, CTA (c, b) of a (1, nb, 1) cluster: the chunk's g lands by
 // one bulk copy; Gram rows [k b / nb, k (b + 1) / nb) stream through a ring
 // of kFinStages shared-memory stages, one bulk copy a row into a fixed row
-// stride.  Register-tiled Gram form: thread (tq, cq) keeps h[t][v] = sum over
-// the block's rows i of g_t[i] Gram[i][c + v] for the four tokens t of quad
-// tq and the four columns c + v of quad cq in each 256-column pass (two
-// 16-byte shared loads per sixteen FMAs), then adds g_t[c + v] h[t][v].  The
+// stride.  Register-tiled Gram form: thread (to, cq) keeps h[t][v] = sum over
+// the block's rows i of g_t[i] Gram[i][c + v] for the eight tokens t of octet
+// to and the four columns c + v of quad cq in each 256-column pass (three
+// 16-byte shared loads per 32 FMAs), then adds g_t[c + v] h[t][v].  The
 // blocks' partial sums meet in the cluster's rank 0, which adds them in block
 // order and takes rho and the flag.  Every sum has one fixed order.
 __device__ __forceinline__ void fin_token(float qq, float nn, float x2, float eps, float* rho_out, uint8_t* flags,
@@ -648,10 +702,11 @@ __global__ void __launch_bounds__(kNormThreads) tc_norms_kernel(const uint16_t* 
   if (tid == 0) norms[t] = make_float2(red[0][0] + red[1][0], red[0][1] + red[1][1]);
 }
 
-__device__ __forceinline__ void quad_fma(float (&h)[4][4], const float4 g, const float4 m) {
-  const float gt[4] = {g.x, g.y, g.z, g.w};
+// h[t][v] += g_t m_v for the eight tokens of an octet (ga: tokens 0-3, gb: 4-7).
+__device__ __forceinline__ void octet_fma(float (&h)[8][4], const float4 ga, const float4 gb, const float4 m) {
+  const float gt[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
 #pragma unroll
-  for (int t = 0; t < 4; ++t) {
+  for (int t = 0; t < 8; ++t) {
     h[t][0] = fmaf(gt[t], m.x, h[t][0]);
     h[t][1] = fmaf(gt[t], m.y, h[t][1]);
     h[t][2] = fmaf(gt[t], m.z, h[t][2]);
@@ -662,21 +717,23 @@ __device__ __forceinline__ void quad_fma(float (&h)[4][4], const float4 g, const
 // nr Gram rows of one ring stage (row stride KS) into the first NL passes'
 // accumulators, in row order.
 template <int NP, int NL, int R, int KS>
-__device__ __forceinline__ void gram_rows(float (&h)[NP][4][4], const float* sg, const float* gr, int nr) {
+__device__ __forceinline__ void gram_rows(float (&h)[NP][8][4], const float* sg, const float* gr, int nr) {
   if (nr == R) {
 #pragma unroll
     for (int r = 0; r < R; ++r) {
-      const float4 g4 = *reinterpret_cast<const float4*>(gr + r * kFinTok);
+      const float4 ga = *reinterpret_cast<const float4*>(gr + r * kFinTok);
+      const float4 gb = *reinterpret_cast<const float4*>(gr + r * kFinTok + 4);
 #pragma unroll
       for (int p = 0; p < NL; ++p)
-        quad_fma(h[p], g4, *reinterpret_cast<const float4*>(sg + r * KS + p * kFinCols));
+        octet_fma(h[p], ga, gb, *reinterpret_cast<const float4*>(sg + r * KS + p * kFinCols));
     }
   } else {
     for (int r = 0; r < nr; ++r) {
-      const float4 g4 = *reinterpret_cast<const float4*>(gr + r * kFinTok);
+      const float4 ga = *reinterpret_cast<const float4*>(gr + r * kFinTok);
+      const float4 gb = *reinterpret_cast<const float4*>(gr + r * kFinTok + 4);
 #pragma unroll
       for (int p = 0; p < NL; ++p)
-        quad_fma(h[p], g4, *reinterpret_cast<const float4*>(sg + r * KS + p * kFinCols));
+        octet_fma(h[p], ga, gb, *reinterpret_cast<const float4*>(sg + r * KS + p * kFinCols));
     }
   }
 }
@@ -709,7 +766,7 @@ __global__ void __launch_bounds__(kFinThreads + 32) tc_gramq_kernel(const float*
   __shared__ float qred[kFinMaxBlocks][kFinTok];       // rank 0: the blocks' q partials
   float* ring = reinterpret_cast<float*>(fsm4);        // [kFinStages][R][KS]
   float* gs = ring + kFinStages * R * KS;              // [k][kFinTok]
-  float* red = gs + kFinTok * k;                       // [4 warps][kFinTok]
+  float* red = gs + kFinTok * k;                       // [4 warps][kFinTok]: q partials
   const int cb = blockIdx.x, blk = blockIdx.y;         // blk: rank in the (1, nb, 1) cluster
   const int t0 = cb * kFinTok;
   const int tn = T - t0 < kFinTok ? T - t0 : kFinTok;
@@ -738,7 +795,7 @@ __global__ void __launch_bounds__(kFinThreads + 32) tc_gramq_kernel(const float*
       const int st = ch % kFinStages;
       const int r0 = i0 + ch * R, nr = i1 - r0 < R ? i1 - r0 : R;
       if (ch >= kFinStages &&
-          !__all_sync(0xffffffffu, mbar_wait(&empty[st], uint32_t(ch / kFinStages - 1) & 1u, err)))
+          !__all_sync(0xffffffffu, mbar_wait_sleep(&empty[st], uint32_t(ch / kFinStages - 1) & 1u, err)))
         break;  // a compute warp never released the stage (error word set)
       if (lane == 0) mbar_expect_tx(&full[st], uint32_t(nr) * k * 4);
       __syncwarp();
@@ -748,7 +805,7 @@ __global__ void __launch_bounds__(kFinThreads + 32) tc_gramq_kernel(const float*
     }
   } else {
     // ---- compute warps
-    bool failed = !mbar_wait(&gbar, 0, err);
+    bool failed = !mbar_wait_sleep(&gbar, 0, err);
     // token slots past T hold whatever the workspace held: zero them
     if (tn < kFinTok) {
       for (int e = tid; e < kFinTok * k; e += kFinThreads)
@@ -756,22 +813,22 @@ __global__ void __launch_bounds__(kFinThreads + 32) tc_gramq_kernel(const float*
       consumer_sync();
     }
     // this block's share of g^T Gram g, the Gram rows in row order
-    const int tq = tid >> 6, cq = tid & 63;
+    const int to = tid >> 6, cq = tid & 63;
     const bool live0 = 4 * cq < k;                       // k % 8 == 0: a quad is whole or absent
     const bool live1 = NP == 2 && kFinCols + 4 * cq < k;
-    float h[NP][4][4];
+    float h[NP][8][4];
 #pragma unroll
     for (int p = 0; p < NP; ++p)
 #pragma unroll
-      for (int t = 0; t < 4; ++t)
+      for (int t = 0; t < 8; ++t)
 #pragma unroll
         for (int v = 0; v < 4; ++v) h[p][t][v] = 0.f;
     for (int ch = 0; ch < nchunk; ++ch) {
       const int st = ch % kFinStages;
       const int r0 = i0 + ch * R, nr = i1 - r0 < R ? i1 - r0 : R;
-      if (!failed && !mbar_wait(&full[st], uint32_t(ch / kFinStages) & 1u, err)) failed = true;
+      if (!failed && !mbar_wait_sleep(&full[st], uint32_t(ch / kFinStages) & 1u, err)) failed = true;
       const float* sg = ring + size_t(st) * R * KS + 4 * cq;
-      const float* gr = gs + r0 * kFinTok + 4 * tq;
+      const float* gr = gs + r0 * kFinTok + 8 * to;
       if (live1)
         gram_rows<NP, (NP > 1 ? 2 : 1), R, KS>(h, sg, gr, nr);
       else if (live0)
@@ -780,27 +837,29 @@ __global__ void __launch_bounds__(kFinThreads + 32) tc_gramq_kernel(const float*
       if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with the stage
     }
     // q_t over the thread's columns: sum of g_t[c + v] h[t][v]
-    float q[4] = {0.f, 0.f, 0.f, 0.f};
+    float q[8];
+#pragma unroll
+    for (int t = 0; t < 8; ++t) q[t] = 0.f;
 #pragma unroll
     for (int p = 0; p < NP; ++p) {
       if (!(p == 0 ? live0 : live1)) continue;
 #pragma unroll
       for (int v = 0; v < 4; ++v) {
-        const float4 gc = *reinterpret_cast<const float4*>(gs + (p * kFinCols + 4 * cq + v) * kFinTok + 4 * tq);
-        q[0] = fmaf(gc.x, h[p][0][v], q[0]);
-        q[1] = fmaf(gc.y, h[p][1][v], q[1]);
-        q[2] = fmaf(gc.z, h[p][2][v], q[2]);
-        q[3] = fmaf(gc.w, h[p][3][v], q[3]);
+        const float* gc = gs + (p * kFinCols + 4 * cq + v) * kFinTok + 8 * to;
+        const float4 ga = *reinterpret_cast<const float4*>(gc), gb = *reinterpret_cast<const float4*>(gc + 4);
+        const float gt[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+#pragma unroll
+        for (int t = 0; t < 8; ++t) q[t] = fmaf(gt[t], h[p][t][v], q[t]);
       }
     }
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
+    for (int t = 0; t < 8; ++t) {
       const float a = warp_sum(q[t]);
-      if (lane == 0) red[warp * kFinTok + 4 * tq + t] = a;
+      if (lane == 0) red[warp * kFinTok + 8 * to + t] = a;
     }
     consumer_sync();
     if (tid < kFinTok) {
-      const int w0 = (tid >> 2) * 2;  // the two warps of this token's quad
+      const int w0 = (tid >> 3) * 2;  // the two warps of this token's octet
       qq = red[w0 * kFinTok + tid] + red[(w0 + 1) * kFinTok + tid];
     }
   }
