@@ -185,6 +185,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// tcgen05.ld of 16 columns without the wait: several loads in flight, then
+// one tmem_ld_wait() before any of their registers is read.
+__device__ __forceinline__ void tmem_ld16_nowait(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
 // Shared-memory matrix descriptor: K-major operand tile written by TMA with
 // 128-byte swizzle (rows of 64 bf16, 8-row / 1024-byte swizzle atoms).
 __device__ __forceinline__ uint64_t smem_desc_sw128(const void* tile) {
@@ -328,12 +341,19 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll 1
     for (int u = 0; u < MT; ++u) {
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 16) {
-      float v[16];
-      tmem_ld16(tmem + (uint32_t(warp * 32) << 16) + uint32_t(u * BN + c), v);
+    for (int c = 0; c < BN; c += 64) {  // four 16-column loads in flight, one wait
+      uint32_t r[4][16];
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        *reinterpret_cast<float4*>(st + lane * LD + c + 4 * q) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+      for (int h = 0; h < 4; ++h)
+        tmem_ld16_nowait(tmem + (uint32_t(warp * 32) << 16) + uint32_t(u * BN + c + 16 * h), r[h]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int h = 0; h < 4; ++h)
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          *reinterpret_cast<float4*>(st + lane * LD + c + 16 * h + 4 * q) =
+              make_float4(__uint_as_float(r[h][4 * q]), __uint_as_float(r[h][4 * q + 1]),
+                          __uint_as_float(r[h][4 * q + 2]), __uint_as_float(r[h][4 * q + 3]));
     }
     __syncwarp();
     const int r_base = (m_tile * MT + u) * kBM + warp * 32;
@@ -881,6 +901,34 @@ __global__ void __launch_bounds__(kFinThreads + 32) tc_gramq_kernel(const float*
   }
 }
 
+// Two row gathers in one launch (the prefill path's X_slow and G_fast): CTAs
+// [0, nb0) copy dst0[j] = src0[idx0[j]] for j < count0, the others
+// dst1[j] = src1[idx1[j]] for j < count1 (16-byte vectors).
+struct GatherJob {
+  const uint4* src;
+  uint4* dst;
+  const int32_t* idx;
+  const int32_t* count;
+  int64_t row_vecs;
+};
+__global__ void gather_rows2_kernel(GatherJob j0, GatherJob j1, int nb0) {
+  pdl_wait();
+  const bool second = int(blockIdx.x) >= nb0;
+  const uint4* src = second ? j1.src : j0.src;
+  uint4* dst = second ? j1.dst : j0.dst;
+  const int32_t* idx = second ? j1.idx : j0.idx;
+  const int64_t rv = second ? j1.row_vecs : j0.row_vecs;
+  const int b = second ? int(blockIdx.x) - nb0 : int(blockIdx.x);
+  const int nbk = second ? int(gridDim.x) - nb0 : nb0;
+  const int n = __ldcg(second ? j1.count : j0.count);
+  const int64_t total = int64_t(n) * rv;
+  for (int64_t e = int64_t(b) * blockDim.x + threadIdx.x; e < total; e += int64_t(nbk) * blockDim.x) {
+    const int64_t j = e / rv, v = e - j * rv;
+    const int32_t t = __ldcg(&idx[j]);
+    dst[e] = ld_cg_v4(src + int64_t(t) * rv + v);
+  }
+}
+
 // Gather rows: dst[j] = src[idx[j]] for j < count (16-byte vectors).
 __global__ void gather_rows_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, const int32_t* idx,
                                    const int32_t* count, int64_t row_vecs, int T) {
@@ -1158,27 +1206,14 @@ cudaError_t launch_tensor_path(const TensorArgs& t, cudaStream_t s) {
   // 4. compaction and gathers
   if ((e = launch_compact(t.flags, int(T), t.idx, t.counts, s)) != cudaSuccess) return e;
   {
-    const uint4* src = static_cast<const uint4*>(t.X);
-    uint4* dst = reinterpret_cast<uint4*>(t.Xslow);
-    const int32_t* idx = t.idx + T;
-    const int32_t* cnt = t.counts + 1;
-    int64_t rv = d * 2 / 16;
-    int TT = int(T);
-    void* args[] = {&src, &dst, &idx, &cnt, &rv, &TT};
-    if ((e = launch_pdl(reinterpret_cast<const void*>(gather_rows_kernel), dim3(296), dim3(256), 0, s, args)) !=
-        cudaSuccess)
-      return e;
-  }
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(t.Gbf);
-    uint4* dst = reinterpret_cast<uint4*>(t.Gfast);
-    const int32_t* idx = t.idx;
-    const int32_t* cnt = t.counts;
-    int64_t rv = k * 2 / 16;
-    int TT = int(T);
-    void* args[] = {&src, &dst, &idx, &cnt, &rv, &TT};
-    if ((e = launch_pdl(reinterpret_cast<const void*>(gather_rows_kernel), dim3(148), dim3(256), 0, s, args)) !=
-        cudaSuccess)
+    GatherJob xs{static_cast<const uint4*>(t.X), reinterpret_cast<uint4*>(t.Xslow), t.idx + T, t.counts + 1,
+                 d * 2 / 16};
+    GatherJob gf{reinterpret_cast<const uint4*>(t.Gbf), reinterpret_cast<uint4*>(t.Gfast), t.idx, t.counts,
+                 k * 2 / 16};
+    int nb0 = 296;
+    void* args[] = {&xs, &gf, &nb0};
+    if ((e = launch_pdl(reinterpret_cast<const void*>(gather_rows2_kernel), dim3(296 + 148), dim3(256), 0, s,
+                        args)) != cudaSuccess)
       return e;
   }
   // 5. Y_fast = G_fast M^T, Y_slow = X_slow W^T (rows scattered to token
