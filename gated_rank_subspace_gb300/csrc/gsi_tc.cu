@@ -232,8 +232,9 @@ struct TcArgs {
 constexpr int kBM = 128, kBK = 64;
 
 // SG: pipeline stages (0: the default -- 4 for BN = 256, else 6; 3 when the
-// CTA takes two row tiles).  Short contractions (K = 256) take 3 stages, so
-// two CTAs share an SM and one's epilogue overlaps the other's loads and MMAs.
+// CTA takes two row tiles).  Short contractions (K <= 256, BN = 128) take 2
+// stages, so three CTAs share an SM and their epilogues (staged 64 columns at
+// a time) overlap the others' loads and MMAs.
 // MT: 128-row tiles of A per CTA; with MT = 2 every B tile feeds two MMAs
 // into two TMEM accumulators (B is read from L2 half as often).
 template <int BN, int SG = 0, int MT = 1>
@@ -245,6 +246,11 @@ struct TcCfg {
   static_assert(TMEM_COLS <= 512, "TMEM holds 512 columns");
   static constexpr uint32_t B_BYTES = BN * kBK * 2;
   static constexpr size_t SMEM = 1024 + size_t(STAGES) * (A_BYTES + B_BYTES) + 256;
+  // epilogue column chunk: all BN columns where 128 staged rows of them fit
+  // the idle ring, else the widest multiple of 64 that does
+  static constexpr int CW = size_t(kBM) * (BN + 4) * 4 <= size_t(STAGES) * (A_BYTES + B_BYTES) ? BN
+                          : size_t(kBM) * (BN / 2 + 4) * 4 <= size_t(STAGES) * (A_BYTES + B_BYTES) ? BN / 2
+                                                                                                    : 64;
 };
 
 template <int BN, int SG, int MT>
@@ -326,11 +332,14 @@ __global__ void __launch_bounds__(128, 1)
   const bool go = __all_sync(0xffffffffu, ok && *reinterpret_cast<volatile uint32_t*>(a.err) == 0);
   if (go) {
     // The pipeline buffers are idle (every MMA, and so every operand load,
-    // has completed): each warp stages its 32 rows x BN columns there, then
-    // writes whole row segments -- consecutive lanes on consecutive columns,
-    // 16-byte stores -- instead of one 16-byte piece of 32 rows per store.
-    constexpr int LD = BN + 4;  // staged row stride in floats (conflict-free 16-byte accesses)
+    // has completed): each warp stages its 32 rows x CW columns there at a
+    // time (CW = BN where the buffers hold all of it), then writes whole row
+    // segments -- consecutive lanes on consecutive columns, 16-byte stores --
+    // instead of one 16-byte piece of 32 rows per store.
+    constexpr int CW = C::CW;
+    constexpr int LD = CW + 4;  // staged row stride in floats (conflict-free 16-byte accesses)
     static_assert(size_t(kBM) * LD * 4 <= size_t(C::STAGES) * (C::A_BYTES + C::B_BYTES), "staging fits");
+    static_assert(BN % CW == 0 && CW % 64 == 0, "column chunks");
     float* st = reinterpret_cast<float*>(sA) + size_t(warp) * 32 * LD;
     const bool vec = (a.ldc % 4 == 0) && ((reinterpret_cast<uintptr_t>(a.C) & 15) == 0);
     // float32 rows with 16-byte aligned starts and lengths leave by bulk
@@ -340,12 +349,17 @@ __global__ void __launch_bounds__(128, 1)
     const bool bulk = !a.c_bf16 && vec && (a.N % 4 == 0) && (a.c_split % 4 == 0);
 #pragma unroll 1
     for (int u = 0; u < MT; ++u) {
+    const int r_base = (m_tile * MT + u) * kBM + warp * 32;
+    const int my_r = r_base + lane;
+    const int64_t my_orow = my_r < rows ? (a.row_map ? int64_t(__ldcg(&a.row_map[my_r])) : int64_t(my_r)) : 0;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 64) {  // four 16-column loads in flight, one wait
+    for (int c0 = 0; c0 < BN; c0 += CW) {
+#pragma unroll 1
+    for (int c = 0; c < CW; c += 64) {  // four 16-column loads in flight, one wait
       uint32_t r[4][16];
 #pragma unroll
       for (int h = 0; h < 4; ++h)
-        tmem_ld16_nowait(tmem + (uint32_t(warp * 32) << 16) + uint32_t(u * BN + c + 16 * h), r[h]);
+        tmem_ld16_nowait(tmem + (uint32_t(warp * 32) << 16) + uint32_t(u * BN + c0 + c + 16 * h), r[h]);
       tmem_ld_wait();
 #pragma unroll
       for (int h = 0; h < 4; ++h)
@@ -356,14 +370,12 @@ __global__ void __launch_bounds__(128, 1)
                           __uint_as_float(r[h][4 * q + 2]), __uint_as_float(r[h][4 * q + 3]));
     }
     __syncwarp();
-    const int r_base = (m_tile * MT + u) * kBM + warp * 32;
-    const int my_r = r_base + lane;
-    const int64_t my_orow = my_r < rows ? (a.row_map ? int64_t(__ldcg(&a.row_map[my_r])) : int64_t(my_r)) : 0;
+    const int col0 = n_tile * BN + c0;  // first output column of this chunk
     if (bulk) {
-      const int ncols = a.N - n_tile * BN < BN ? a.N - n_tile * BN : BN;
+      const int ncols = a.N - col0 < CW ? a.N - col0 : CW;
       if (my_r < rows && ncols > 0) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // this lane's staged row -> async proxy
-        bulk_store_1d(a.C + int64_t(blockIdx.z) * a.c_split + my_orow * a.ldc + int64_t(n_tile) * BN, st + lane * LD,
+        bulk_store_1d(a.C + int64_t(blockIdx.z) * a.c_split + my_orow * a.ldc + int64_t(col0), st + lane * LD,
                       uint32_t(ncols) * 4);
       }
       bulk_store_commit_wait_read();
@@ -372,14 +384,14 @@ __global__ void __launch_bounds__(128, 1)
     }
     for (int i = 0; i < 32 && r_base + i < rows; ++i) {
       const int64_t orow = __shfl_sync(0xffffffffu, my_orow, i);
-      const int64_t cofs = int64_t(blockIdx.z) * a.c_split + orow * a.ldc + int64_t(n_tile) * BN;
+      const int64_t cofs = int64_t(blockIdx.z) * a.c_split + orow * a.ldc + int64_t(col0);
       const float* srow = st + i * LD;
       if (a.c_bf16) {
         // four columns a lane: 8-byte stores of bf16 pairs (ldc and the
         // column offsets are multiples of 4 elements)
         __nv_bfloat16* crow = reinterpret_cast<__nv_bfloat16*>(a.C) + cofs;
-        for (int q = lane; q < BN / 4; q += 32) {
-          const int col = n_tile * BN + 4 * q;
+        for (int q = lane; q < CW / 4; q += 32) {
+          const int col = col0 + 4 * q;
           const float4 v = *reinterpret_cast<const float4*>(srow + 4 * q);
           if (col + 4 <= a.N) {
             const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y), hi = __floats2bfloat162_rn(v.z, v.w);
@@ -396,8 +408,8 @@ __global__ void __launch_bounds__(128, 1)
         continue;
       }
       float* crow = a.C + cofs;
-      for (int q = lane; q < BN / 4; q += 32) {
-        const int col = n_tile * BN + 4 * q;
+      for (int q = lane; q < CW / 4; q += 32) {
+        const int col = col0 + 4 * q;
         if (vec && col + 4 <= a.N) {
           *reinterpret_cast<float4*>(crow + 4 * q) = *reinterpret_cast<const float4*>(srow + 4 * q);
         } else {
@@ -406,7 +418,8 @@ __global__ void __launch_bounds__(128, 1)
         }
       }
     }
-    __syncwarp();  // the staging rows are read before the next row tile overwrites them
+    __syncwarp();  // the staging rows are read before the next chunk overwrites them
+    }
     }
   }
   // Bounded drain of this CTA's own copies before its shared memory goes away
@@ -1010,7 +1023,7 @@ cudaError_t launch_tc_gemm(const void* A, int64_t a_rows, const void* B, int64_t
   switch (bn) {
     case 64: return launch_tc_gemm_t<64>(A, a_rows, B, b_rows, K, args, s);
     case 128:
-      return K <= 256 ? launch_tc_gemm_t<128, 3>(A, a_rows, B, b_rows, K, args, s)
+      return K <= 256 ? launch_tc_gemm_t<128, 2>(A, a_rows, B, b_rows, K, args, s)
                       : launch_tc_gemm_t<128>(A, a_rows, B, b_rows, K, args, s);
     default: return launch_tc_gemm_t<256>(A, a_rows, B, b_rows, K, args, s);
   }
