@@ -1024,7 +1024,7 @@ cudaError_t launch_tc_gemm(const void* A, int64_t a_rows, const void* B, int64_t
     case 64: return launch_tc_gemm_t<64>(A, a_rows, B, b_rows, K, args, s);
     case 128:
       return K <= 256 ? launch_tc_gemm_t<128, 2>(A, a_rows, B, b_rows, K, args, s)
-                      : launch_tc_gemm_t<128>(A, a_rows, B, b_rows, K, args, s);
+                      : launch_tc_gemm_t<128, 3>(A, a_rows, B, b_rows, K, args, s);
     default: return launch_tc_gemm_t<256>(A, a_rows, B, b_rows, K, args, s);
   }
 }
@@ -1171,14 +1171,15 @@ cudaError_t launch_tensor_path(const TensorArgs& t, cudaStream_t s) {
   g.C = t.G;
   g.ldc = k;
   g.err = t.err;
-  // Prefill-sized T: 128 x 256 tiles where k >= 256 (at k = 256, X is read
-  // once); small T: 128 x 64 tiles (one 128-row tile holds every token, so
-  // narrower tiles give more CTAs).  K is cut into g_split(T) slices for
-  // parallelism; the finalize kernel adds the slices.
+  // Prefill-sized T: 128 x 128 tiles where k >= 256 (X read from L2 once
+  // per 128 columns of G; 3 stages, two CTAs an SM, so the grid of 16 x 2 x 8
+  // CTAs at T = 2048, k = 256 is one wave); small T: 128 x 64 tiles (one
+  // 128-row tile holds every token, so narrower tiles give more CTAs).  K is
+  // cut into g_split(T) slices for parallelism; the finalize adds the slices.
   const int gsplit = int(cdiv(d, kBK)) < g_split(T) ? int(cdiv(d, kBK)) : g_split(T);  // each slice >= 1 k-block
   g.ksplit = gsplit;
   g.c_split = T * k;
-  const int g_bn = (T >= kTensorMinT && k >= 256) ? 256 : 64;
+  const int g_bn = (T >= kTensorMinT && k >= 256) ? 128 : 64;
   if ((e = launch_tc_gemm(t.X, T, t.Vt, k, int(d), g_bn, g, s)) != cudaSuccess) return e;
   // 3. rho, flags, bf16 g: the per-token pass, then the Gram form
   {
