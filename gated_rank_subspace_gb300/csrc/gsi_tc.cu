@@ -433,6 +433,160 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 0) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
+// ------------------------------------------------------------------ persistent contraction (Y_fast)
+// C[row_map(m)][n] = sum_k A[m][k] B[n][k] over 128 x 128 tiles, float32 C,
+// one CTA an SM looping over the tiles t = blockIdx.x, + gridDim.x, ...
+// (tile t: row tile t % n_m, column tile t / n_m).  Warp 0 (one thread)
+// streams the operand k-blocks of its tiles through a kPS-stage ring, running
+// ahead across tile boundaries; warp 1 allocates two TMEM accumulators and
+// one thread of it issues the MMAs of tile j into accumulator j % 2; warps
+// 2-5 drain accumulator j % 2 (warp w reads TMEM lanes 32 (w % 4) ..) into
+// staging rows, hand it back, and send each row by one bulk copy while the
+// MMAs of tile j + 1 run.  Each output is summed in the same k-block and MMA
+// order as in tc_gemm_kernel<128>.
+constexpr int kPS = 4;
+constexpr int kPBN = 128;
+constexpr uint32_t kPTile = uint32_t(kBM) * kBK * 2;  // one 128-row tile of a stage (A or B)
+constexpr int kPLD = kPBN + 4;                          // staged row stride (floats)
+constexpr size_t kPSmem = 1024 + size_t(kPS) * 2 * kPTile + size_t(kBM) * kPLD * 4 + 256;
+constexpr int kPThreads = 192;
+
+__global__ void __launch_bounds__(kPThreads, 1)
+    tc_gemm_persist_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb, TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* staging = reinterpret_cast<float*>(base + size_t(kPS) * 2 * kPTile);
+  uint64_t* full = reinterpret_cast<uint64_t*>(staging + size_t(kBM) * kPLD);
+  uint64_t* empty = full + kPS;
+  uint64_t* tfull = empty + kPS;  // accumulator j % 2 holds tile j (tcgen05.commit)
+  uint64_t* tempty = tfull + 2;   // accumulator drained (the four epilogue warps)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  pdl_wait();
+  const int rows = a.rows_dev ? __ldcg(a.rows_dev) : a.rows;
+  const int n_m = (rows + kBM - 1) / kBM, n_n = (a.N + kPBN - 1) / kPBN;
+  const int n_tiles = n_m * n_n;
+  if (int(blockIdx.x) >= n_tiles) return;  // whole CTA, before any barrier or TMEM
+  const int nk = (a.K + kBK - 1) / kBK;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int u = 0; u < 2; ++u) {
+      mbar_init(&tfull[u], 1);
+      mbar_init(&tempty[u], 4);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 2 * kPBN);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---- operand loads
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+        const int m_tile = t % n_m, n_tile = t / n_m;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = int(it % kPS);
+          if (it >= uint32_t(kPS) && !mbar_wait(&empty[s], ((it / kPS) & 1u) ^ 1u, a.err)) {
+            ok = false;
+            break;
+          }
+          mbar_expect_tx(&full[s], 2 * kPTile);
+          tma_load_2d(base + size_t(s) * 2 * kPTile, &ta, &full[s], kb * kBK, m_tile * kBM);
+          tma_load_2d(base + size_t(s) * 2 * kPTile + kPTile, &tb, &full[s], kb * kBK, n_tile * kPBN);
+        }
+      }
+      // bounded drain: the last issue of every stage has landed before the
+      // CTA's shared memory can go away (already so on the normal path)
+      for (uint32_t i = it > uint32_t(kPS) ? it - kPS : 0u; i < it; ++i)
+        mbar_wait(&full[i % kPS], (i / kPS) & 1u, a.err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---- MMAs
+      constexpr uint32_t idesc = idesc_bf16_f32(kBM, kPBN);
+      uint32_t it = 0;
+      int j = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++j) {
+        const int acc = j & 1;
+        if (j >= 2 && !mbar_wait(&tempty[acc], uint32_t((j >> 1) - 1) & 1u, a.err)) break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + uint32_t(acc * kPBN);
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = int(it % kPS);
+          if (!mbar_wait(&full[s], (it / kPS) & 1u, a.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint64_t ad = smem_desc_sw128(base + size_t(s) * 2 * kPTile);
+          const uint64_t bd = smem_desc_sw128(base + size_t(s) * 2 * kPTile + kPTile);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            umma_bf16(d_tmem, ad + uint64_t(kk * 2), bd + uint64_t(kk * 2), idesc, (kb | kk) != 0);
+          umma_commit(&empty[s]);
+        }
+        if (ok) umma_commit(&tfull[acc]);
+      }
+    }
+  } else {
+    // ---- epilogue: TMEM lane quarter q, staged rows, one bulk copy a row
+    const int q = warp & 3;
+    float* st = staging + size_t(q) * 32 * kPLD;
+    int j = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++j) {
+      const int acc = j & 1;
+      const int m_tile = t % n_m, n_tile = t / n_m;
+      if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], uint32_t(j >> 1) & 1u, a.err))) break;
+      tc_fence_after();
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");  // the previous tile's rows have left
+      __syncwarp();
+#pragma unroll 1
+      for (int c = 0; c < kPBN; c += 64) {  // four 16-column loads in flight, one wait
+        uint32_t r[4][16];
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+          tmem_ld16_nowait(tmem + (uint32_t(q * 32) << 16) + uint32_t(acc * kPBN + c + 16 * h), r[h]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int h = 0; h < 4; ++h)
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            *reinterpret_cast<float4*>(st + lane * kPLD + c + 16 * h + 4 * v) =
+                make_float4(__uint_as_float(r[h][4 * v]), __uint_as_float(r[h][4 * v + 1]),
+                            __uint_as_float(r[h][4 * v + 2]), __uint_as_float(r[h][4 * v + 3]));
+      }
+      // the accumulator is read: the MMAs of tile j + 2 may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      const int my_r = m_tile * kBM + q * 32 + lane;
+      const int col0 = n_tile * kPBN;
+      const int ncols = a.N - col0 < kPBN ? a.N - col0 : kPBN;
+      if (my_r < rows) {
+        const int64_t orow = a.row_map ? int64_t(__ldcg(&a.row_map[my_r])) : int64_t(my_r);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // this lane's staged row -> async proxy
+        bulk_store_1d(a.C + orow * a.ldc + int64_t(col0), st + lane * kPLD, uint32_t(ncols) * 4);
+      }
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, 2 * kPBN);
+}
+
 // ------------------------------------------------------------------ few-token contraction
 // Y[tok(j)][r] = sum_kk A[r][kk] B[j][kk] for the rows r of a weight matrix A
 // (W or M: n_rows x K, bf16, K-major) and the first n_tok rows of a token
@@ -1029,6 +1183,36 @@ cudaError_t launch_tc_gemm(const void* A, int64_t a_rows, const void* B, int64_t
   }
 }
 
+// The persistent 128 x 128 contraction (float32 C with 16-byte aligned rows):
+// one CTA an SM, at most as many as the tiles of a_rows rows.
+static cudaError_t launch_tc_gemm_persist(const void* A, int64_t a_rows, const void* B, int64_t b_rows, int K,
+                                          const TcArgs& args, cudaStream_t s) {
+  CUtensorMap ta, tb;
+  cudaError_t e = make_map_2d(&ta, A, a_rows, K, kBM);
+  if (e != cudaSuccess) return e;
+  if ((e = make_map_2d(&tb, B, b_rows, K, kPBN)) != cudaSuccess) return e;
+  static bool attr = false;
+  if (!attr) {
+    if ((e = set_kernel_smem(tc_gemm_persist_kernel, kPSmem)) != cudaSuccess) return e;
+    attr = true;
+  }
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  const int64_t tiles = cdiv(a_rows, kBM) * cdiv(b_rows, kPBN);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(tiles < sms ? tiles : sms));
+  cfg.blockDim = dim3(kPThreads);
+  cfg.dynamicSmemBytes = kPSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, tc_gemm_persist_kernel, ta, tb, args);
+}
+
 // Few-token contraction (see tc_skinny_kernel): A = weights (a_rows x K),
 // B = token rows (b_rows x K) in tiles of NT (grid z), K cut into `splits`
 // slices (one cluster per 128-row tile of A; splits <= 8 and <= the k-blocks).
@@ -1261,7 +1445,11 @@ cudaError_t launch_tensor_path(const TensorArgs& t, cudaStream_t s) {
   f.ldc = d_out;
   f.row_map = t.idx;
   f.err = t.err;
-  if ((e = launch_tc_gemm(t.Gfast, T, t.M, d_out, int(k), 128, f, s)) != cudaSuccess) return e;
+  // float32 rows that bulk copies can send: the persistent contraction
+  const bool persist = d_out % 4 == 0 && (reinterpret_cast<uintptr_t>(t.Y) & 15) == 0;
+  if ((e = persist ? launch_tc_gemm_persist(t.Gfast, T, t.M, d_out, int(k), f, s)
+                   : launch_tc_gemm(t.Gfast, T, t.M, d_out, int(k), 128, f, s)) != cudaSuccess)
+    return e;
   TcArgs sl{};
   sl.rows_dev = t.counts + 1;
   sl.N = int(d_out);
