@@ -118,10 +118,11 @@ inline int g_split(int64_t T) { return T < kTensorMinT ? 16 : 8; }
 // cuts the Gram rows into fin_blocks(T, k) blocks, one thread-block cluster
 // a chunk, so that every T gives about three CTAs an SM of a GB300 (456) or
 // more: at most kFinMaxBlocks blocks (a portable cluster) and at least 32
-// Gram rows a block.  A CTA of the Gram form has kFinThreads threads (two
-// token quads x 64 column quads of a kFinCols-column pass) and streams its
-// Gram rows through kFinStages shared-memory stages of kFinStageBytes.
-constexpr int kFinTok = 8;
+// Gram rows a block.  A CTA of the Gram form has kFinThreads compute threads
+// (two token octets x 64 column quads of a kFinCols-column pass) and one
+// copy warp, and streams its Gram rows through kFinStages shared-memory
+// stages of kFinStageBytes.
+constexpr int kFinTok = 16;
 constexpr int kNormThreads = 64;
 constexpr int kFinThreads = 128;
 constexpr int kFinCols = 256;
