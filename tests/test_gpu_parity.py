@@ -266,10 +266,12 @@ def test_stack_matches_single_calls(gsi):
 
 # ------------------------------------------------------------------ tensor-core path (prefill T)
 @pytest.mark.parametrize("shape", [(512, 384, 64, 160, 0.3), (1032, 1000, 136, 300, 0.2), (4096, 4096, 256, 129, 0.1),
-                                   (2048, 1000, 320, 160, 0.25), (1024, 512, 512, 136, 0.3)])
+                                   (2048, 1000, 320, 160, 0.25), (1024, 512, 512, 136, 0.3),
+                                   (1024, 333, 128, 200, 0.3)])
 def test_tensor_path_against_oracle_and_stream(gsi, shape):
     """tcgen05 contractions (G = X V, M G_fast, W X_slow) vs the oracle, ragged tiles; k = 320 and
-    k = 512 take the finalize's two 256-column passes over the Gram."""
+    k = 512 take the finalize's two 256-column passes over the Gram; d_out = 333 (rows that bulk
+    copies cannot send) takes the per-tile contraction's store loop for Y_fast, 64 columns at a time."""
     d, d_out, k, T, f = shape
     V64 = synth.orthonormal_basis(synth.rng(10, d, k, 2), d, k)
     m_in = synth.stack_layer(10, T, {"up": V64}, {"up": (d_out, d)}, T=T, f_slow=f, roles=("up",))[0]
